@@ -1,0 +1,386 @@
+#!/usr/bin/env python
+"""Throughput of the latent MoE layer on B300: one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the whole layer (router, top-k, permutation, W_in,
+expert SwiGLU, weighted group reduce, W_out, combine) over one batch of
+synthetic seeded tokens of the named workload (default: the Edge0-shaped
+layer at a decode / speculative-verify batch of 8 tokens). Weights are
+rotated over several device copies so that no step finds its weights in L2.
+value = tokens/s over the device-timed region (CUDA events, max over ranks);
+e2e = the same through lmoe_layer_forward_host (pinned host buffers, copies
+in the timed region). --impl reference times the CPU oracle instead.
+Multi-GPU: independent replicas (no collective), one process per GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s at decode batch 8 and 16K prefill; % HBM / tensor roofline"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="decode_t8")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--copies", type=int, default=8, help="device weight copies rotated across steps")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------- distributed
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def dist_init(world, use_cuda):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    dist.init_process_group(backend="nccl" if use_cuda else "gloo")
+    return dist
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, v: float, device=None) -> float:
+    if dist is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.th.join(timeout=2)
+        sm = [float(r[0]) for r in self.rows if len(r) >= 8 and r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if len(r) >= 8 and r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in self.rows:
+            if len(r) >= 8:
+                for n, v in zip(names, r[4:8]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------- roofline bits
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("hbm_gbs", 6400.0), d.get("bf16_tflops", 1800.0), d.get("bf16_tflops_sustained", 1400.0), "measured"
+    return 6400.0, 1800.0, 1400.0, "fallback"
+
+
+def stage_bytes(sh, T, idx):
+    """Algorithmic HBM bytes of each decode-path kernel for one pass: every
+    weight byte the routing needs, read once (int4 + bf16 scales = 9/16 byte
+    per weight), plus activations in and out."""
+    import numpy as np
+    epg = sh.E // sh.G
+    experts = np.unique(idx.reshape(-1))
+    groups = np.unique(experts // epg)
+    wq = 0.5 + 2.0 / 32  # bytes per int4 weight including its scale
+    b = {}
+    b["route"] = 4 * sh.d * sh.E + 2 * T * sh.d + (4 * sh.E if sh.has_bias else 0)
+    b["win"] = len(groups) * sh.L * sh.d * wq + 2 * T * sh.d
+    b["gateup"] = len(experts) * 2 * sh.f * sh.L * wq
+    b["down"] = len(experts) * sh.L * sh.f * wq
+    b["wout"] = len(groups) * sh.d * sh.L * wq + 2 * T * sh.d
+    if sh.lora_rank:
+        r = sh.lora_rank
+        b["lora_p"] = len(groups) * sh.d * r * 2
+        b["win"] += len(groups) * r * sh.L * 2
+        b["lora_q"] = len(groups) * sh.L * r * 2
+        b["wout"] += len(groups) * r * sh.d * 2
+    return b
+
+
+def read_traffic(kernel: str):
+    """dram bytes per launch of a kernel from a committed ncu summary, if the
+    summary matches the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        ent = d.get(kernel)
+        if not ent:
+            return None
+        import hashlib
+        src = open(os.path.join(ROOT, ent["source"]), "rb").read()
+        if hashlib.sha256(src).hexdigest()[:16] != ent["source_sha"]:
+            return None
+        return ent["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ oracle
+
+def oracle_tokens_per_s(name: str, budget_s: float = 12.0, tokens=None):
+    import lmoe_synth as S
+    import oracle as O
+    sh, T, W, x = S.make_workload(name)
+    Ly = O.Layer(sh, W)
+    sel = x if tokens is None else x[tokens]
+    n = 0
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        O.layer_forward(Ly, sel)
+        n += sel.shape[0]
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return n / dt, reps, sel.shape[0]
+
+
+def run_reference(args):
+    rank, local, world = dist_env()
+    if rank != 0:
+        return
+    import lmoe_synth as S
+    import oracle as O
+    sh, T, W, x = S.make_workload(args.workload)
+    Ly = O.Layer(sh, W)
+    for i in range(max(args.warmup, 0)):
+        O.layer_forward(Ly, x[i % T:i % T + 1])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        O.layer_forward(Ly, x[i % T:i % T + 1])
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.workload, "tokens_per_step": 1, "T": T},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"one token of {args.workload} per step (full layer, literal per-assignment form)"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------- ours
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import lmoe_synth as S
+    from sparse_latent_moe_lmoe_b300 import LatentMoE, capi
+    from sparse_latent_moe_lmoe_b300.layer import to_device
+
+    rank, local, world = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = dist_init(world, True)
+    sh, T, W, x = S.make_workload(args.workload)
+    base = {n: to_device(W.get(n), dev) for n in capi.WEIGHT_FIELDS}
+    copies = [base] + [{n: (None if t is None else t.clone()) for n, t in base.items()} for _ in range(args.copies - 1)]
+    layers = [LatentMoE(sh, c, device=local) for c in copies]
+    xt = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+    y = torch.empty_like(xt)
+    stream = torch.cuda.current_stream()
+    for m in layers:
+        m.workspace(T, host_staging=True)
+    idx, _, _ = layers[0].route(xt)
+    idx_np = idx.cpu().numpy()
+    sb = stage_bytes(sh, T, idx_np)
+    n_kernels = capi.lmoe_stage_name(layers[0].h, T, 0)[1]
+
+    # one CUDA graph per weight copy: a replay launches the whole layer
+    for i, m in enumerate(layers):
+        m.forward(xt, out=y)
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream()
+    graphs = []
+    for m in layers:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            m.forward(xt, out=y)
+        graphs.append(g)
+    torch.cuda.synchronize()
+
+    def step(i):
+        graphs[i % len(graphs)].replay()
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, device time
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(dist)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    ms = e0.elapsed_time(e1)
+    ck = clocks.stop()
+    ms = max_over_ranks(dist, ms, dev)
+    value = world * T * args.steps / (ms / 1000.0)
+
+    # ---- per-kernel durations: the same graphs with an event pair captured
+    # around every kernel launch (on the launching stream), replayed K times
+    import ctypes
+    names = [capi.lmoe_stage_name(layers[0].h, T, i)[0] for i in range(n_kernels)]
+    per = {n: 0.0 for n in names}
+    pgraphs = []
+    for m in layers:
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_kernels)]
+        for e in ev:  # torch creates the CUDA event on first record
+            e.record(stream)
+        torch.cuda.synchronize()
+        arr = (ctypes.c_void_p * (2 * n_kernels))(*[e.cuda_event for e in ev])
+        capi.lmoe_set_stage_events(m.h, arr, n_kernels)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            m.forward(xt, out=y)
+        capi.lmoe_set_stage_events(m.h, None, 0)
+        pgraphs.append((g, ev))
+    torch.cuda.synchronize()
+    try:
+        for i in range(args.steps):
+            g, ev = pgraphs[i % len(pgraphs)]
+            g.replay()
+            torch.cuda.synchronize()
+            for j, n in enumerate(names):
+                per[n] += ev[2 * j].elapsed_time(ev[2 * j + 1]) / args.steps
+        stage_timing = "graph replay, event pair around each kernel"
+    except Exception:  # event nodes not timeable here: time stream launches instead
+        per = {n: 0.0 for n in names}
+        for i in range(args.steps):
+            m = layers[i % len(layers)]
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_kernels)]
+            for e in ev:
+                e.record(stream)
+            arr = (ctypes.c_void_p * (2 * n_kernels))(*[e.cuda_event for e in ev])
+            capi.lmoe_set_stage_events(m.h, arr, n_kernels)
+            m.forward(xt, out=y)
+            capi.lmoe_set_stage_events(m.h, None, 0)
+            torch.cuda.synchronize()
+            for j, n in enumerate(names):
+                per[n] += ev[2 * j].elapsed_time(ev[2 * j + 1]) / args.steps
+        stage_timing = "stream launches, event pair around each kernel"
+    dom = max(per, key=per.get)
+    hbm, bf16, bf16s, peak_src = measured_peaks()
+    achieved = sb.get(dom, 0.0) / (per[dom] * 1e-3) / 1e9
+    total_bytes = sum(sb.values())
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": read_traffic(dom), "peak_source": peak_src,
+                "bytes_per_launch": sb.get(dom, 0.0), "timing": stage_timing,
+                "step": {"bytes": total_bytes, "achieved": total_bytes / (ms / args.steps * 1e-3) / 1e9,
+                         "frac": total_bytes / (ms / args.steps * 1e-3) / 1e9 / hbm}}
+
+    # ---- e2e through the host-buffer entry point
+    xh = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    for i in range(3):
+        layers[i % len(layers)].forward_host(xh, yh)
+    barrier(dist)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        layers[i % len(layers)].forward_host(xh, yh)
+    t1 = time.perf_counter()
+    e2e_s = max_over_ranks(dist, t1 - t0, dev)
+    e2e = {"value": world * T * args.steps / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": T * sh.d * 2,
+           "d2h_bytes_per_step": T * sh.d * 2}
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int4 weights, fp16 tensor-core operands, fp32 accumulate",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "T": T, "d": sh.d, "E": sh.E, "G": sh.G, "k": sh.k, "L": sh.L,
+                       "f": sh.f, "lora_rank": sh.lora_rank, "parallelism": f"replicas x{world}",
+                       "l2": f"{args.copies} rotating device weight copies (> L2)",
+                       "distinct_experts": int(len(np.unique(idx_np))),
+                       "active_groups": int(len(np.unique(idx_np // (sh.E // sh.G))))},
+            "roofline": roofline, "stages_us": {n: 1000 * v for n, v in per.items()},
+            "e2e": e2e, "gpu_launches": n_kernels * args.steps, "clocks": ck}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, reps, n = oracle_tokens_per_s(args.workload)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": f"all {n} tokens of {args.workload}, full layer, repeated {reps}x"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

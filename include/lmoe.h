@@ -1,0 +1,217 @@
+/*
+ * lmoe -- the latent mixture-of-experts layer of Edge0-145B on NVIDIA B300
+ * (sm_103a), behind a plain C ABI.
+ *
+ * The layer (sources, by page title and section):
+ *  - "Edge0-145B: Frontier AI Capabilities on Your Own Computer", "Under the
+ *    Hood of Edge0", paragraph "Architecture: share large matrices across
+ *    sparse experts": groups of 64 experts share two large matrices, each
+ *    expert keeps a small set of its own parameters.
+ *  - "Edge0-145B: Run a 145B Open-Source Model on Your Laptop", "Not
+ *    Compression -- Architecture": 512 experts, 10 active per token, 48
+ *    layers; "The Three Pillars That Make It Fast": int4 expert tensors and a
+ *    Recover-LoRA branch in parallel with the frozen 4-bit base.
+ *
+ * Concrete form (this library's stated assumption; the pages sketch it only):
+ *   logits  l = x W_r^T (+ b)                               fp32 router
+ *   top-k   the k largest l, descending, ties -> lower index; w = softmax over them
+ *   group   g(e) = e / (E/G)
+ *   h       = Win[g] x  (+ B_in[g]^T A_in[g]^T x)            Win: int4 [L][d]
+ *   u_e     = Down_e( silu(Gate_e h) * Up_e h )               int4 [f][L], [f][L], [L][f]
+ *   y       = sum_g Wout[g] sum_{j: g(e_j)=g} w_j u_{e_j}   (+ LoRA)  Wout: int4 [d][L]
+ * int4: symmetric groups of 32 consecutive elements along the reduction
+ * dimension, one bf16 scale per group; byte j of a row holds element 2j in
+ * its low nibble and 2j+1 in its high nibble (two's complement, -7..7).
+ *
+ * Conventions for every entry point:
+ *  - Pointers named x, y, idx, w, logits, Y, ws, residual and the weight
+ *    pointers are DEVICE pointers on the handle's device, except in
+ *    lmoe_layer_forward_host. bf16 tensors are passed as uint16_t bit
+ *    patterns. All buffers are owned by the caller; the handle borrows the
+ *    weight pointers for its lifetime (they must stay valid and unchanged).
+ *  - Arrays read with 128-bit loads must be 16-byte aligned: x, y, residual,
+ *    every weight pointer, Y and ws. Misalignment -> LMOE_ERR_ALIGNMENT.
+ *  - Arguments are validated on the host before anything is launched; on an
+ *    error nothing is enqueued. Work is enqueued on the given stream
+ *    (NULL = legacy default stream) and the call returns without waiting.
+ *    Errors raised by kernels are reported by the next call or by
+ *    lmoe_check. No function throws across the ABI.
+ *  - A handle is thread-compatible, not thread-safe: do not use one handle
+ *    from two host threads at once. Calls enqueued on different streams with
+ *    the same workspace race.
+ */
+#ifndef LMOE_H
+#define LMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* lmoe_stream; /* == cudaStream_t */
+
+typedef enum {
+  LMOE_OK = 0,
+  LMOE_ERR_INVALID_ARG = 1,   /* null pointer, bad size, bad handle */
+  LMOE_ERR_UNSUPPORTED = 2,   /* a shape outside what the kernels support */
+  LMOE_ERR_ALIGNMENT = 3,     /* a pointer not 16-byte aligned */
+  LMOE_ERR_CUDA = 4,          /* a CUDA runtime error (launch or earlier async failure) */
+  LMOE_ERR_TIMEOUT = 5,       /* a bounded device-side wait ran out */
+  LMOE_ERR_DEVICE_CHECK = 6,  /* a kernel found invalid data (e.g. expert index out of range) */
+  LMOE_ERR_NO_MEMORY = 7      /* lmoe_create could not allocate its private copies */
+} lmoe_status;
+
+/* Execution path for lmoe_layer_forward / lmoe_expert_forward. */
+enum { LMOE_PATH_AUTO = 0, LMOE_PATH_DECODE = 1, LMOE_PATH_PREFILL = 2 };
+
+typedef struct {
+  int d;            /* model width; multiple of 128 */
+  int E;            /* experts; multiple of G, <= 1024 */
+  int G;            /* expert groups (shared-matrix groups); <= 64 */
+  int k;            /* experts per token; 1 <= k <= min(16, E) */
+  int L;            /* latent width; multiple of 32 (prefill path: of 64) */
+  int f;            /* per-expert SwiGLU width; multiple of 32 (prefill path: of 64) */
+  int qgroup;       /* int4 group size along the reduction dimension; must be 32 */
+  int lora_rank;    /* 0 = no LoRA branch; else a multiple of 16, <= 128 */
+  int has_bias;     /* nonzero: router bias b_r is used */
+  unsigned flags;   /* reserved, must be 0 */
+  long long timeout_cycles; /* bound on any device-side wait (clock64 cycles); 0 = 2^31 */
+  int decode_max_T; /* token count up to which AUTO takes the decode path; 0 = 16; <= 16 */
+  int force_path;   /* LMOE_PATH_* */
+} lmoe_config;
+
+/* Device pointers to the layer's weights (borrowed for the handle's life).
+ * Shapes as in the layer description; packed int4 rows are [rows][K/2] bytes
+ * and their scales [rows][K/32] bf16. */
+typedef struct {
+  const float* W_r;           /* [E][d] fp32 */
+  const float* b_r;           /* [E] fp32, or NULL when has_bias == 0 */
+  const uint8_t* W_in_q;      /* [G][L][d/2] */
+  const uint16_t* W_in_s;     /* [G][L][d/32] */
+  const uint8_t* W_out_q;     /* [G][d][L/2] */
+  const uint16_t* W_out_s;    /* [G][d][L/32] */
+  const uint8_t* gate_q;      /* [E][f][L/2] */
+  const uint16_t* gate_s;     /* [E][f][L/32] */
+  const uint8_t* up_q;        /* [E][f][L/2] */
+  const uint16_t* up_s;       /* [E][f][L/32] */
+  const uint8_t* down_q;      /* [E][L][f/2] */
+  const uint16_t* down_s;     /* [E][L][f/32] */
+  const uint16_t* A_in;       /* [G][d][r] bf16, NULL when lora_rank == 0 */
+  const uint16_t* B_in;       /* [G][r][L] */
+  const uint16_t* A_out;      /* [G][L][r] */
+  const uint16_t* B_out;      /* [G][r][d] */
+} lmoe_weights;
+
+/* The token permutation (device arrays, caller-allocated, capacities in
+ * brackets). Assignment a = t*k + j is token t's j-th expert.
+ *   expert_offsets [E+1]  exclusive prefix sum of tokens per expert
+ *   sorted_assign  [T*k]  assignments sorted by (expert, a), stable
+ *   inv            [T*k]  inv[sorted_assign[p]] = p
+ *   group_offsets  [G+1]  = expert_offsets[g*E/G] (assignment level)
+ *   group_tok_offsets [G+1], group_tokens [T*min(G,k)]: per group the
+ *                         distinct tokens routed into it, ascending
+ *   assign_row     [T*k]  row of (t, group of a) in group_tokens
+ * Rows of Y in lmoe_expert_forward / lmoe_combine follow group_tokens. */
+typedef struct {
+  int32_t* expert_offsets;
+  int32_t* sorted_assign;
+  int32_t* inv;
+  int32_t* group_offsets;
+  int32_t* group_tok_offsets;
+  int32_t* group_tokens;
+  int32_t* assign_row;
+} lmoe_perm;
+
+typedef struct lmoe_handle lmoe_handle;
+
+/* Human-readable name of a status (static string). */
+const char* lmoe_status_string(lmoe_status s);
+
+/* ABI version of this header (major*100 + minor). */
+int lmoe_version(void);
+
+/* Create a handle on `device` for the given shapes and weights. Validates the
+ * config, checks the device is sm_103 with enough shared memory, and makes
+ * the small private derived copies the kernels use (a 3-way bf16 split of
+ * W_r for the tensor-core router; freed by lmoe_destroy). Does not read the
+ * int4 weights. Synchronous. *out is NULL on error. */
+lmoe_status lmoe_create(lmoe_handle** out, const lmoe_config* cfg, const lmoe_weights* w, int device);
+
+/* Free the handle and its private copies (waits for the device first). NULL is a no-op. */
+lmoe_status lmoe_destroy(lmoe_handle* h);
+
+/* Bytes of workspace (device memory, 256-byte aligned) that a call with T
+ * tokens needs; the same bound serves every entry point. 0 on a bad handle or T < 0. */
+size_t lmoe_workspace_size(const lmoe_handle* h, int T);
+
+/* Router and top-k ("512 experts, 10 activated per token").
+ *  x [T][d] bf16 -> idx [T][k] int32 (descending logit, ties to the lower
+ *  expert index), w [T][k] fp32 (softmax over the selected logits), and, if
+ *  logits != NULL, the fp32 router logits [T][E] the selection was made on.
+ *  T == 0 is a no-op. */
+lmoe_status lmoe_route(lmoe_handle* h, const uint16_t* x, int T, int32_t* idx, float* w, float* logits, void* ws,
+                       lmoe_stream stream);
+
+/* Token permutation by group, then expert (groups of 64 experts share the
+ * two large matrices, so tokens are gathered per group first). idx [T][k] ->
+ * every array of *out (see lmoe_perm). Deterministic: bit-identical for
+ * identical idx. Indices outside [0, E) set LMOE_ERR_DEVICE_CHECK. */
+lmoe_status lmoe_permute(lmoe_handle* h, const int32_t* idx, int T, const lmoe_perm* out, void* ws,
+                         lmoe_stream stream);
+
+/* The latent expert FFN for routed tokens: for every (group g, token t) row
+ * r of the permutation,
+ *   Y[r] = Wout[g] ( sum_{j: g(idx[t][j]) = g} w[t][j] * u_{idx[t][j]}( Win[g] x_t ) )  (+ LoRA)
+ * x [T][d] bf16, idx/w [T][k], perm from lmoe_permute on the same idx,
+ * Y [rows][d] fp32 with rows = group_tok_offsets[G] (capacity T*min(G,k)). */
+lmoe_status lmoe_expert_forward(lmoe_handle* h, const uint16_t* x, int T, const int32_t* idx, const float* w,
+                                const lmoe_perm* perm, float* Y, void* ws, lmoe_stream stream);
+
+/* Weighted un-permute and combine: y_t = sum over the groups of t, in
+ * ascending group order, of Y[row(g, t)] (+ residual_t), rounded once to
+ * bf16. Y as produced by lmoe_expert_forward; residual [T][d] bf16 or NULL. */
+lmoe_status lmoe_combine(lmoe_handle* h, const float* Y, const int32_t* idx, const lmoe_perm* perm, int T,
+                         const uint16_t* residual, uint16_t* y, lmoe_stream stream);
+
+/* The whole layer: y = bf16(layer(x) (+ residual)). x, residual (nullable)
+ * and y are [T][d] bf16; y may alias residual but not x. */
+lmoe_status lmoe_layer_forward(lmoe_handle* h, const uint16_t* x, int T, const uint16_t* residual, uint16_t* y,
+                               void* ws, lmoe_stream stream);
+
+/* The whole layer from and to HOST memory: copies x (and residual) from
+ * host to the workspace, runs lmoe_layer_forward, copies y back and waits
+ * for the stream. x_host, residual_host (nullable) and y_host are host
+ * pointers ([T][d] bf16; page-locked memory gives asynchronous copies). The
+ * workspace must hold lmoe_workspace_size(h, T) + lmoe_host_staging_size(h, T) bytes. */
+lmoe_status lmoe_layer_forward_host(lmoe_handle* h, const uint16_t* x_host, int T, const uint16_t* residual_host,
+                                    uint16_t* y_host, void* ws, lmoe_stream stream);
+
+/* Extra workspace bytes lmoe_layer_forward_host needs for its staging copies. */
+size_t lmoe_host_staging_size(const lmoe_handle* h, int T);
+
+/* Wait for `stream`, then read and clear the handle's device error word.
+ * Returns LMOE_OK, LMOE_ERR_TIMEOUT, LMOE_ERR_DEVICE_CHECK or LMOE_ERR_CUDA. */
+lmoe_status lmoe_check(lmoe_handle* h, lmoe_stream stream);
+
+/* Test hook for the bounded-wait path: sets the handle's wait budget (clock64
+ * cycles; 0 restores the default). A budget of 1 makes the layer's ticketed
+ * combine report LMOE_ERR_TIMEOUT through lmoe_check instead of waiting. */
+lmoe_status lmoe_set_timeout(lmoe_handle* h, long long cycles);
+
+/* Profiling hook: when events != NULL, lmoe_layer_forward records
+ * events[2*i] / events[2*i+1] (cudaEvent_t) on its stream around launch i of
+ * its kernel sequence, for i < n. The stage names are given by
+ * lmoe_stage_name. Pass NULL to turn it off. */
+lmoe_status lmoe_set_stage_events(lmoe_handle* h, void* const* events, int n);
+
+/* Name of kernel i of lmoe_layer_forward's sequence for T tokens ("" if none),
+ * and the count of kernels launched per call through *count. */
+const char* lmoe_stage_name(const lmoe_handle* h, int T, int i, int* count);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LMOE_H */

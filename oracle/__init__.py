@@ -66,6 +66,7 @@ def _lib_():
         lib.oracle_layer_forward.argtypes = [P, I, P, P, P, P, P]
         lib.oracle_group_row.argtypes = [P, I, P, P, P, P]
         lib.oracle_residual.argtypes = [I64, P, P, P]
+        lib.oracle_combine.argtypes = [I, I, I, I, I, P, P, P, P, P]
         _lib = lib
     return _lib
 
@@ -225,3 +226,17 @@ def residual(x: np.ndarray, y: np.ndarray) -> np.ndarray:
     out = np.empty(x.shape, np.uint16)
     _lib_().oracle_residual(x.size, _p(x), _p(y), _p(out))
     return out
+
+
+def combine(Y: np.ndarray, idx: np.ndarray, assign_row: np.ndarray, E: int, G: int, residual=None) -> np.ndarray:
+    """fp64 combine of per-(group, token) rows Y [rows][d] (fp32)."""
+    Y = np.ascontiguousarray(Y, np.float32)
+    idx = np.ascontiguousarray(idx, np.int32)
+    assign_row = np.ascontiguousarray(assign_row, np.int32)
+    T, k = idx.shape
+    d = Y.shape[1]
+    if residual is not None:
+        residual = np.ascontiguousarray(residual, np.uint16)
+    y = np.empty((T, d), np.float64)
+    _lib_().oracle_combine(T, d, k, G, E // G, _p(Y), _p(idx), _p(assign_row), _p(residual), _p(y))
+    return y

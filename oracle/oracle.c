@@ -426,3 +426,22 @@ void oracle_residual(int64_t n, const uint16_t* x, const double* y, uint16_t* x_
     x_next[i] = oracle_bf16_round(oracle_bf16_value(x[i]) + yb);
   }
 }
+
+/* The weighted un-permute and combine on its own: y_t = sum over the
+ * distinct groups g of token t's experts, in ascending g, of Y[row(g, t)]
+ * (+ residual_t), where row(g, t) = assign_row[t*k + j] for any j with
+ * g(idx[t][j]) = g. Y holds one fp32 row of width d per (group, token). */
+void oracle_combine(int T, int d, int k, int G, int epg, const float* Y, const int32_t* idx,
+                    const int32_t* assign_row, const uint16_t* residual, double* y) {
+  for (int t = 0; t < T; t++) {
+    double* yt = y + (int64_t)t * d;
+    for (int i = 0; i < d; i++) yt[i] = residual ? oracle_bf16_value(residual[(int64_t)t * d + i]) : 0.0;
+    for (int g = 0; g < G; g++) {
+      int row = -1;
+      for (int j = 0; j < k; j++)
+        if (idx[t * k + j] / epg == g) row = assign_row[t * k + j];
+      if (row < 0) continue;
+      for (int i = 0; i < d; i++) yt[i] += (double)Y[(int64_t)row * d + i];
+    }
+  }
+}

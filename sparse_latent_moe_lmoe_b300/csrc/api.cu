@@ -1,0 +1,533 @@
+// The C ABI of the latent MoE layer (declared in include/lmoe.h): host-side
+// validation, the handle, the workspace layout and the dispatch to the
+// decode-path and prefill-path kernels.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <new>
+#include <vector>
+
+#include "../../include/lmoe.h"
+#include "decode.cuh"
+#include "prefill.cuh"
+
+using namespace lmoe;
+
+struct lmoe_handle {
+  lmoe_config cfg;
+  lmoe_weights w;
+  int device;
+  int num_sms;
+  unsigned* d_err;       // device error word
+  unsigned* d_tickets;   // ticket counters, zero between calls
+  uint16_t* d_wr_split;  // [3][E][d] bf16 split of W_r (hi, mid, lo) for the tensor-core router
+  long long timeout;
+  std::vector<cudaEvent_t> events;
+};
+
+namespace {
+
+constexpr int kMaxDecodeT = 16;
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+lmoe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA; }
+
+lmoe_status validate_config(const lmoe_config* c) {
+  if (!c) return LMOE_ERR_INVALID_ARG;
+  if (c->d <= 0 || c->E <= 0 || c->G <= 0 || c->k <= 0 || c->L <= 0 || c->f <= 0) return LMOE_ERR_INVALID_ARG;
+  if (c->qgroup != 32) return LMOE_ERR_UNSUPPORTED;
+  if (c->E % c->G != 0) return LMOE_ERR_INVALID_ARG;
+  if (c->k > c->E) return LMOE_ERR_INVALID_ARG;
+  if (c->k > 16 || c->E > 1024 || c->G > 64) return LMOE_ERR_UNSUPPORTED;
+  if (c->d % 128 != 0 || c->L % 32 != 0 || c->f % 32 != 0) return LMOE_ERR_UNSUPPORTED;
+  if (c->L % 16 != 0 || c->f % 16 != 0) return LMOE_ERR_UNSUPPORTED;
+  if (c->lora_rank < 0 || c->lora_rank > 128 || c->lora_rank % 16 != 0) return LMOE_ERR_UNSUPPORTED;
+  if (c->flags != 0) return LMOE_ERR_UNSUPPORTED;
+  if (c->decode_max_T < 0 || c->decode_max_T > kMaxDecodeT) return LMOE_ERR_UNSUPPORTED;
+  if (c->force_path < LMOE_PATH_AUTO || c->force_path > LMOE_PATH_PREFILL) return LMOE_ERR_INVALID_ARG;
+  if (c->timeout_cycles < 0) return LMOE_ERR_INVALID_ARG;
+  return LMOE_OK;
+}
+
+lmoe_status validate_weights(const lmoe_config* c, const lmoe_weights* w) {
+  if (!w) return LMOE_ERR_INVALID_ARG;
+  const void* req[] = {w->W_r, w->W_in_q, w->W_in_s, w->W_out_q, w->W_out_s, w->gate_q,
+                       w->gate_s, w->up_q, w->up_s, w->down_q, w->down_s};
+  for (const void* p : req) {
+    if (!p) return LMOE_ERR_INVALID_ARG;
+    if (!aligned16(p)) return LMOE_ERR_ALIGNMENT;
+  }
+  if (c->has_bias && !w->b_r) return LMOE_ERR_INVALID_ARG;
+  if (c->lora_rank > 0) {
+    const void* lr[] = {w->A_in, w->B_in, w->A_out, w->B_out};
+    for (const void* p : lr) {
+      if (!p) return LMOE_ERR_INVALID_ARG;
+      if (!aligned16(p)) return LMOE_ERR_ALIGNMENT;
+    }
+  }
+  return LMOE_OK;
+}
+
+lmoe_status check_handle(const lmoe_handle* h) { return h ? LMOE_OK : LMOE_ERR_INVALID_ARG; }
+
+int ks_in_for(const lmoe_config& c) {
+  const int nch = (c.d + 127) / 128;
+  return nch < 4 ? nch : 4;
+}
+
+// ----------------------------------------------------------- workspace map
+struct DecodeWs {
+  size_t logits, idx, w, eo, sa, inv, go, gto, gt, ar, Hp, V, Z, Yp, Pin, Qout, perm_scratch, end;
+};
+
+DecodeWs decode_ws(const lmoe_config& c, int T) {
+  DecodeWs m;
+  const int n = kMaxDecodeT;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align_up(o + bytes);
+    return at;
+  };
+  const int gk = c.G < c.k ? c.G : c.k;
+  m.logits = take((size_t)n * c.E * 4);
+  m.idx = take((size_t)n * c.k * 4);
+  m.w = take((size_t)n * c.k * 4);
+  m.eo = take((size_t)(c.E + 1) * 4);
+  m.sa = take((size_t)n * c.k * 4);
+  m.inv = take((size_t)n * c.k * 4);
+  m.go = take((size_t)(c.G + 1) * 4);
+  m.gto = take((size_t)(c.G + 1) * 4);
+  m.gt = take((size_t)n * gk * 4);
+  m.ar = take((size_t)n * c.k * 4);
+  m.Hp = take((size_t)ks_in_for(c) * c.G * n * c.L * 4);
+  m.V = take((size_t)n * c.k * c.f * 4);
+  m.Z = take((size_t)c.G * n * c.L * 4);
+  m.Yp = take((size_t)c.G * n * c.d * 4);
+  m.Pin = take((size_t)c.G * n * (c.lora_rank > 0 ? c.lora_rank : 1) * 4);
+  m.Qout = take((size_t)c.G * n * (c.lora_rank > 0 ? c.lora_rank : 1) * 4);
+  m.perm_scratch = take(permute_scratch_bytes(T > n ? T : n, c.E, c.G));
+  m.end = o;
+  return m;
+}
+
+bool use_prefill(const lmoe_handle* h, int T) {
+  const lmoe_config& c = h->cfg;
+  if (!prefill_available()) return false;
+  if (c.force_path == LMOE_PATH_DECODE) return false;
+  if (c.force_path == LMOE_PATH_PREFILL) return T > 0;
+  const int mt = c.decode_max_T ? c.decode_max_T : kMaxDecodeT;
+  return T > mt;
+}
+
+DecodeArgs base_args(const lmoe_handle* h, void* ws) {
+  const lmoe_config& c = h->cfg;
+  DecodeArgs A;
+  memset(&A, 0, sizeof(A));
+  A.d = c.d; A.E = c.E; A.G = c.G; A.k = c.k; A.L = c.L; A.f = c.f; A.r = c.lora_rank;
+  A.epg = c.E / c.G;
+  A.ks_in = ks_in_for(c);
+  A.W_r = h->w.W_r; A.b_r = c.has_bias ? h->w.b_r : nullptr;
+  A.W_in_q = h->w.W_in_q; A.W_in_s = h->w.W_in_s; A.W_out_q = h->w.W_out_q; A.W_out_s = h->w.W_out_s;
+  A.gate_q = h->w.gate_q; A.gate_s = h->w.gate_s; A.up_q = h->w.up_q; A.up_s = h->w.up_s;
+  A.down_q = h->w.down_q; A.down_s = h->w.down_s;
+  A.A_in = h->w.A_in; A.B_in = h->w.B_in; A.A_out = h->w.A_out; A.B_out = h->w.B_out;
+  const DecodeWs m = decode_ws(c, 0);
+  char* b = reinterpret_cast<char*>(ws);
+  A.idx = reinterpret_cast<int32_t*>(b + m.idx);
+  A.w = reinterpret_cast<float*>(b + m.w);
+  A.pm.expert_offsets = reinterpret_cast<int32_t*>(b + m.eo);
+  A.pm.sorted_assign = reinterpret_cast<int32_t*>(b + m.sa);
+  A.pm.inv = reinterpret_cast<int32_t*>(b + m.inv);
+  A.pm.group_offsets = reinterpret_cast<int32_t*>(b + m.go);
+  A.pm.group_tok_offsets = reinterpret_cast<int32_t*>(b + m.gto);
+  A.pm.group_tokens = reinterpret_cast<int32_t*>(b + m.gt);
+  A.pm.assign_row = reinterpret_cast<int32_t*>(b + m.ar);
+  A.Hp = reinterpret_cast<float*>(b + m.Hp);
+  A.V = reinterpret_cast<float*>(b + m.V);
+  A.Z = reinterpret_cast<float*>(b + m.Z);
+  A.Yp = reinterpret_cast<float*>(b + m.Yp);
+  A.Pin = reinterpret_cast<float*>(b + m.Pin);
+  A.Qout = reinterpret_cast<float*>(b + m.Qout);
+  A.tickets = h->d_tickets;
+  A.err = h->d_err;
+  return A;
+}
+
+float* ws_logits(const lmoe_handle* h, void* ws) {
+  return reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + decode_ws(h->cfg, 0).logits);
+}
+
+// Records an event; inside a stream capture the record becomes an external
+// event node, which stays usable for timing after each graph launch.
+void record_event(cudaEvent_t e, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, s);
+}
+
+struct EventHook : StageHook {
+  const std::vector<cudaEvent_t>* ev;
+  int i = 0;
+  void before(cudaStream_t s) override {
+    if (ev && 2 * i < (int)ev->size()) record_event((*ev)[2 * i], s);
+  }
+  void after(cudaStream_t s) override {
+    if (ev && 2 * i + 1 < (int)ev->size()) record_event((*ev)[2 * i + 1], s);
+    ++i;
+  }
+};
+
+lmoe_status pending_error() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int cur;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+// decode path for any T, in passes of <= 16 tokens
+lmoe_status decode_layer(lmoe_handle* h, const uint16_t* x, int T, const uint16_t* residual, uint16_t* y, void* ws,
+                         cudaStream_t st) {
+  const lmoe_config& c = h->cfg;
+  EventHook hook;
+  hook.ev = h->events.empty() ? nullptr : &h->events;
+  for (int t0 = 0; t0 < T; t0 += kMaxDecodeT) {
+    DecodeArgs A = base_args(h, ws);
+    A.T = T - t0 < kMaxDecodeT ? T - t0 : kMaxDecodeT;
+    A.x = x + (size_t)t0 * c.d;
+    A.residual = residual ? residual + (size_t)t0 * c.d : nullptr;
+    A.y = y + (size_t)t0 * c.d;
+    hook.before(st);
+    cudaError_t e = launch_route(A, 1, ws_logits(h, ws), st);
+    hook.after(st);
+    if (e != cudaSuccess) return LMOE_ERR_CUDA;
+    if (A.r > 0) {
+      hook.before(st);
+      e = launch_lora_proj(A, 0, st);
+      hook.after(st);
+      if (e != cudaSuccess) return LMOE_ERR_CUDA;
+    }
+    e = launch_experts(A, 0, st, &hook);
+    if (e != cudaSuccess) return LMOE_ERR_CUDA;
+  }
+  return LMOE_OK;
+}
+
+PrefillArgs prefill_args(const lmoe_handle* h) {
+  PrefillArgs P;
+  memset(&P, 0, sizeof(P));
+  const lmoe_config& c = h->cfg;
+  P.d = c.d; P.E = c.E; P.G = c.G; P.k = c.k; P.L = c.L; P.f = c.f; P.r = c.lora_rank;
+  P.epg = c.E / c.G;
+  P.W_r = h->w.W_r; P.b_r = c.has_bias ? h->w.b_r : nullptr;
+  P.W_r_split = h->d_wr_split;
+  P.W_in_q = h->w.W_in_q; P.W_in_s = h->w.W_in_s; P.W_out_q = h->w.W_out_q; P.W_out_s = h->w.W_out_s;
+  P.gate_q = h->w.gate_q; P.gate_s = h->w.gate_s; P.up_q = h->w.up_q; P.up_s = h->w.up_s;
+  P.down_q = h->w.down_q; P.down_s = h->w.down_s;
+  P.A_in = h->w.A_in; P.B_in = h->w.B_in; P.A_out = h->w.A_out; P.B_out = h->w.B_out;
+  P.err = h->d_err;
+  P.num_sms = h->num_sms;
+  P.timeout = h->timeout;
+  return P;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* lmoe_status_string(lmoe_status s) {
+  switch (s) {
+    case LMOE_OK: return "ok";
+    case LMOE_ERR_INVALID_ARG: return "invalid argument";
+    case LMOE_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case LMOE_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case LMOE_ERR_CUDA: return "CUDA error";
+    case LMOE_ERR_TIMEOUT: return "device wait timed out";
+    case LMOE_ERR_DEVICE_CHECK: return "device-side check failed (invalid data)";
+    case LMOE_ERR_NO_MEMORY: return "out of device memory";
+  }
+  return "unknown status";
+}
+
+int lmoe_version(void) { return 100; }
+
+lmoe_status lmoe_create(lmoe_handle** out, const lmoe_config* cfg, const lmoe_weights* w, int device) {
+  if (!out) return LMOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  lmoe_status s = validate_config(cfg);
+  if (s != LMOE_OK) return s;
+  s = validate_weights(cfg, w);
+  if (s != LMOE_OK) return s;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
+    cudaGetLastError();
+    return device < 0 ? LMOE_ERR_INVALID_ARG : LMOE_ERR_CUDA;
+  }
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return LMOE_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return LMOE_ERR_UNSUPPORTED;  // built for sm_103a only
+  DeviceGuard guard(device);
+  lmoe_handle* h = new (std::nothrow) lmoe_handle();
+  if (!h) return LMOE_ERR_NO_MEMORY;
+  h->cfg = *cfg;
+  h->w = *w;
+  h->device = device;
+  h->num_sms = prop.multiProcessorCount;
+  h->timeout = cfg->timeout_cycles ? cfg->timeout_cycles : (1ll << 31);
+  const size_t nt = 1 + (size_t)(cfg->d + 63) / 64 + 64;
+  if (cudaMalloc(&h->d_err, sizeof(unsigned)) != cudaSuccess ||
+      cudaMalloc(&h->d_tickets, nt * sizeof(unsigned)) != cudaSuccess) {
+    cudaGetLastError();
+    lmoe_destroy(h);
+    return LMOE_ERR_NO_MEMORY;
+  }
+  cudaMemset(h->d_err, 0, sizeof(unsigned));
+  cudaMemset(h->d_tickets, 0, nt * sizeof(unsigned));
+  if (cudaMalloc(&h->d_wr_split, (size_t)3 * cfg->E * cfg->d * 2) != cudaSuccess) {
+    cudaGetLastError();
+    lmoe_destroy(h);
+    return LMOE_ERR_NO_MEMORY;
+  }
+  if (decode_set_attributes() != cudaSuccess || permute_set_attributes() != cudaSuccess) {
+    lmoe_destroy(h);
+    return LMOE_ERR_CUDA;
+  }
+  if (launch_split_router(h->w.W_r, cfg->E, cfg->d, h->d_wr_split, 0) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    lmoe_destroy(h);
+    return LMOE_ERR_CUDA;
+  }
+  *out = h;
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_destroy(lmoe_handle* h) {
+  if (!h) return LMOE_OK;
+  DeviceGuard guard(h->device);
+  cudaDeviceSynchronize();
+  if (h->d_err) cudaFree(h->d_err);
+  if (h->d_tickets) cudaFree(h->d_tickets);
+  if (h->d_wr_split) cudaFree(h->d_wr_split);
+  delete h;
+  return pending_error();
+}
+
+size_t lmoe_workspace_size(const lmoe_handle* h, int T) {
+  if (!h || T < 0) return 0;
+  size_t a = decode_ws(h->cfg, T).end;
+  size_t b = prefill_workspace_bytes(prefill_args(h), T);
+  return a > b ? a : b;
+}
+
+size_t lmoe_host_staging_size(const lmoe_handle* h, int T) {
+  if (!h || T < 0) return 0;
+  return 3 * align_up((size_t)T * h->cfg.d * 2);
+}
+
+lmoe_status lmoe_route(lmoe_handle* h, const uint16_t* x, int T, int32_t* idx, float* w, float* logits, void* ws,
+                       lmoe_stream stream) {
+  if (check_handle(h) != LMOE_OK || T < 0) return LMOE_ERR_INVALID_ARG;
+  if (T == 0) return LMOE_OK;
+  if (!x || !idx || !w || !ws) return LMOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(ws)) return LMOE_ERR_ALIGNMENT;
+  lmoe_status s = pending_error();
+  if (s != LMOE_OK) return s;
+  DeviceGuard guard(h->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  const lmoe_config& c = h->cfg;
+  if (use_prefill(h, T)) {
+    PrefillArgs P = prefill_args(h);
+    return cuda_status(launch_prefill_route(P, x, T, idx, w, logits, ws, st));
+  }
+  for (int t0 = 0; t0 < T; t0 += kMaxDecodeT) {
+    DecodeArgs A = base_args(h, ws);
+    A.T = T - t0 < kMaxDecodeT ? T - t0 : kMaxDecodeT;
+    A.x = x + (size_t)t0 * c.d;
+    A.idx = idx + (size_t)t0 * c.k;
+    A.w = w + (size_t)t0 * c.k;
+    float* lg = logits ? logits + (size_t)t0 * c.E : ws_logits(h, ws);
+    if (launch_route(A, 0, lg, st) != cudaSuccess) return LMOE_ERR_CUDA;
+  }
+  return LMOE_OK;
+}
+
+static lmoe_status check_perm(const lmoe_perm* p) {
+  if (!p || !p->expert_offsets || !p->sorted_assign || !p->inv || !p->group_offsets || !p->group_tok_offsets ||
+      !p->group_tokens || !p->assign_row)
+    return LMOE_ERR_INVALID_ARG;
+  return LMOE_OK;
+}
+
+static PermPtrs to_ptrs(const lmoe_perm* p) {
+  PermPtrs q;
+  q.expert_offsets = p->expert_offsets; q.sorted_assign = p->sorted_assign; q.inv = p->inv;
+  q.group_offsets = p->group_offsets; q.group_tok_offsets = p->group_tok_offsets;
+  q.group_tokens = p->group_tokens; q.assign_row = p->assign_row;
+  return q;
+}
+
+lmoe_status lmoe_permute(lmoe_handle* h, const int32_t* idx, int T, const lmoe_perm* out, void* ws,
+                         lmoe_stream stream) {
+  if (check_handle(h) != LMOE_OK || T < 0) return LMOE_ERR_INVALID_ARG;
+  if (check_perm(out) != LMOE_OK || !ws || (T > 0 && !idx)) return LMOE_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return LMOE_ERR_ALIGNMENT;
+  lmoe_status s = pending_error();
+  if (s != LMOE_OK) return s;
+  DeviceGuard guard(h->device);
+  const DecodeWs m = decode_ws(h->cfg, T);
+  void* scratch = reinterpret_cast<char*>(ws) + m.perm_scratch;
+  return cuda_status(launch_permute(idx, T, h->cfg.E, h->cfg.G, h->cfg.k, to_ptrs(out), scratch, h->d_err,
+                                    (cudaStream_t)stream));
+}
+
+lmoe_status lmoe_expert_forward(lmoe_handle* h, const uint16_t* x, int T, const int32_t* idx, const float* w,
+                                const lmoe_perm* perm, float* Y, void* ws, lmoe_stream stream) {
+  if (check_handle(h) != LMOE_OK || T < 0) return LMOE_ERR_INVALID_ARG;
+  if (T == 0) return LMOE_OK;
+  if (!x || !idx || !w || !Y || !ws || check_perm(perm) != LMOE_OK) return LMOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(Y) || !aligned16(ws)) return LMOE_ERR_ALIGNMENT;
+  lmoe_status s = pending_error();
+  if (s != LMOE_OK) return s;
+  DeviceGuard guard(h->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  const lmoe_config& c = h->cfg;
+  if (use_prefill(h, T)) {
+    PrefillArgs P = prefill_args(h);
+    return cuda_status(launch_prefill_experts(P, x, T, idx, w, to_ptrs(perm), Y, nullptr, nullptr, ws, st));
+  }
+  const DecodeWs m = decode_ws(c, T);
+  for (int t0 = 0; t0 < T; t0 += kMaxDecodeT) {
+    DecodeArgs A = base_args(h, ws);
+    A.T = T - t0 < kMaxDecodeT ? T - t0 : kMaxDecodeT;
+    A.x = x + (size_t)t0 * c.d;
+    // this pass's routing (caller's) and its own local permutation
+    A.idx = const_cast<int32_t*>(idx) + (size_t)t0 * c.k;
+    A.w = const_cast<float*>(w) + (size_t)t0 * c.k;
+    void* scratch = reinterpret_cast<char*>(ws) + m.perm_scratch;
+    if (launch_permute(A.idx, A.T, c.E, c.G, c.k, A.pm, scratch, h->d_err, st) != cudaSuccess) return LMOE_ERR_CUDA;
+    if (A.r > 0 && launch_lora_proj(A, 0, st) != cudaSuccess) return LMOE_ERR_CUDA;
+    A.tok0 = t0;
+    A.idx_all = idx;
+    A.assign_row_all = perm->assign_row;
+    A.Yrows = Y;
+    if (launch_experts(A, 1, st, nullptr) != cudaSuccess) return LMOE_ERR_CUDA;
+  }
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_combine(lmoe_handle* h, const float* Y, const int32_t* idx, const lmoe_perm* perm, int T,
+                         const uint16_t* residual, uint16_t* y, lmoe_stream stream) {
+  if (check_handle(h) != LMOE_OK || T < 0) return LMOE_ERR_INVALID_ARG;
+  if (T == 0) return LMOE_OK;
+  if (!Y || !idx || !y || check_perm(perm) != LMOE_OK) return LMOE_ERR_INVALID_ARG;
+  if (!aligned16(Y) || !aligned16(y) || (residual && !aligned16(residual))) return LMOE_ERR_ALIGNMENT;
+  lmoe_status s = pending_error();
+  if (s != LMOE_OK) return s;
+  DeviceGuard guard(h->device);
+  const lmoe_config& c = h->cfg;
+  return cuda_status(launch_combine(Y, idx, perm->assign_row, T, c.d, c.k, c.E / c.G, residual, y,
+                                    (cudaStream_t)stream));
+}
+
+lmoe_status lmoe_layer_forward(lmoe_handle* h, const uint16_t* x, int T, const uint16_t* residual, uint16_t* y,
+                               void* ws, lmoe_stream stream) {
+  if (check_handle(h) != LMOE_OK || T < 0) return LMOE_ERR_INVALID_ARG;
+  if (T == 0) return LMOE_OK;
+  if (!x || !y || !ws) return LMOE_ERR_INVALID_ARG;
+  if (x == y) return LMOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(ws) || (residual && !aligned16(residual)))
+    return LMOE_ERR_ALIGNMENT;
+  lmoe_status s = pending_error();
+  if (s != LMOE_OK) return s;
+  DeviceGuard guard(h->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (use_prefill(h, T)) {
+    PrefillArgs P = prefill_args(h);
+    return cuda_status(launch_prefill_layer(P, x, T, residual, y, ws, st, h->events.empty() ? nullptr : &h->events));
+  }
+  return decode_layer(h, x, T, residual, y, ws, st);
+}
+
+lmoe_status lmoe_layer_forward_host(lmoe_handle* h, const uint16_t* x_host, int T, const uint16_t* residual_host,
+                                    uint16_t* y_host, void* ws, lmoe_stream stream) {
+  if (check_handle(h) != LMOE_OK || T < 0) return LMOE_ERR_INVALID_ARG;
+  if (T == 0) return LMOE_OK;
+  if (!x_host || !y_host || !ws) return LMOE_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return LMOE_ERR_ALIGNMENT;
+  lmoe_status s = pending_error();
+  if (s != LMOE_OK) return s;
+  DeviceGuard guard(h->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t bytes = (size_t)T * h->cfg.d * 2;
+  char* stage = reinterpret_cast<char*>(ws) + align_up(lmoe_workspace_size(h, T));
+  uint16_t* dx = reinterpret_cast<uint16_t*>(stage);
+  uint16_t* dr = reinterpret_cast<uint16_t*>(stage + align_up(bytes));
+  uint16_t* dy = reinterpret_cast<uint16_t*>(stage + 2 * align_up(bytes));
+  if (cudaMemcpyAsync(dx, x_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return LMOE_ERR_CUDA;
+  if (residual_host && cudaMemcpyAsync(dr, residual_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  s = lmoe_layer_forward(h, dx, T, residual_host ? dr : nullptr, dy, ws, stream);
+  if (s != LMOE_OK) return s;
+  if (cudaMemcpyAsync(y_host, dy, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return LMOE_ERR_CUDA;
+  return cuda_status(cudaStreamSynchronize(st));
+}
+
+lmoe_status lmoe_check(lmoe_handle* h, lmoe_stream stream) {
+  if (check_handle(h) != LMOE_OK) return LMOE_ERR_INVALID_ARG;
+  DeviceGuard guard(h->device);
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return LMOE_ERR_CUDA;
+  unsigned e = 0;
+  if (cudaMemcpy(&e, h->d_err, sizeof(e), cudaMemcpyDeviceToHost) != cudaSuccess) return LMOE_ERR_CUDA;
+  if (e && cudaMemset(h->d_err, 0, sizeof(unsigned)) != cudaSuccess) return LMOE_ERR_CUDA;
+  if (e & ERRBIT_TIMEOUT) return LMOE_ERR_TIMEOUT;
+  if (e) return LMOE_ERR_DEVICE_CHECK;
+  return pending_error();
+}
+
+lmoe_status lmoe_set_timeout(lmoe_handle* h, long long cycles) {
+  if (check_handle(h) != LMOE_OK || cycles < 0) return LMOE_ERR_INVALID_ARG;
+  h->timeout = cycles ? cycles : (h->cfg.timeout_cycles ? h->cfg.timeout_cycles : (1ll << 31));
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_set_stage_events(lmoe_handle* h, void* const* events, int n) {
+  if (check_handle(h) != LMOE_OK || n < 0 || (n > 0 && !events)) return LMOE_ERR_INVALID_ARG;
+  h->events.clear();
+  if (events)
+    for (int i = 0; i < 2 * n; ++i) h->events.push_back((cudaEvent_t)events[i]);
+  return LMOE_OK;
+}
+
+const char* lmoe_stage_name(const lmoe_handle* h, int T, int i, int* count) {
+  static const char* dec[] = {"route", "win", "gateup", "down", "wout"};
+  static const char* dec_lora[] = {"route", "lora_p", "win", "gateup", "down", "lora_q", "wout"};
+  if (!h) {
+    if (count) *count = 0;
+    return "";
+  }
+  if (use_prefill(h, T)) return prefill_stage_name(prefill_args(h), T, i, count);
+  const bool lora = h->cfg.lora_rank > 0;
+  const int per = lora ? 7 : 5;
+  const int passes = (T + kMaxDecodeT - 1) / kMaxDecodeT;
+  if (count) *count = per * passes;
+  if (i < 0 || i >= per * passes) return "";
+  return lora ? dec_lora[i % per] : dec[i % per];
+}
+
+}  // extern "C"

@@ -1,0 +1,83 @@
+// Argument block and launchers of the decode-path kernels (<= 16 tokens).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace lmoe {
+
+// device error word bits
+enum : unsigned { ERRBIT_TIMEOUT = 1u, ERRBIT_BAD_INDEX = 2u, ERRBIT_BAD_DATA = 4u };
+
+struct PermPtrs {
+  int32_t* expert_offsets;
+  int32_t* sorted_assign;
+  int32_t* inv;
+  int32_t* group_offsets;
+  int32_t* group_tok_offsets;
+  int32_t* group_tokens;
+  int32_t* assign_row;
+};
+
+// Everything one decode pass reads or writes (device pointers).
+struct DecodeArgs {
+  int T, d, E, G, k, L, f, r, epg, ks_in;
+  // weights
+  const float* W_r;
+  const float* b_r;
+  const uint8_t* W_in_q;
+  const uint16_t* W_in_s;
+  const uint8_t* W_out_q;
+  const uint16_t* W_out_s;
+  const uint8_t* gate_q;
+  const uint16_t* gate_s;
+  const uint8_t* up_q;
+  const uint16_t* up_s;
+  const uint8_t* down_q;
+  const uint16_t* down_s;
+  const uint16_t* A_in;
+  const uint16_t* B_in;
+  const uint16_t* A_out;
+  const uint16_t* B_out;
+  // this pass's tokens
+  const uint16_t* x;         // [T][d]
+  const uint16_t* residual;  // [T][d] or null
+  uint16_t* y;               // [T][d]
+  int32_t* idx;              // [T][k]
+  float* w;                  // [T][k]
+  PermPtrs pm;               // permutation of this pass's tokens
+  float* Hp;                 // [ks_in][G][16][L]
+  float* V;                  // [16*k][f]
+  float* Z;                  // [G][16][L]
+  float* Yp;                 // [G][16][d]
+  float* Pin;                // [G][16][r]
+  float* Qout;               // [G][16][r]
+  unsigned* tickets;         // [1 + d/64], zero between calls
+  unsigned* err;             // device error word
+  // expert_forward (rows mode): the caller's full routing and permutation
+  int tok0;                  // index of this pass's first token
+  const int32_t* idx_all;
+  const int32_t* assign_row_all;
+  float* Yrows;
+};
+
+// Records timing events around each launch when attached.
+struct StageHook {
+  virtual void before(cudaStream_t) {}
+  virtual void after(cudaStream_t) {}
+  virtual ~StageHook() {}
+};
+
+cudaError_t decode_set_attributes();
+cudaError_t permute_set_attributes();
+cudaError_t launch_route(const DecodeArgs& A, int do_perm, float* logits_out, cudaStream_t st);
+cudaError_t launch_lora_proj(const DecodeArgs& A, int which, cudaStream_t st);
+cudaError_t launch_experts(const DecodeArgs& A, int mode, cudaStream_t st, StageHook* hook);
+cudaError_t launch_combine(const float* Y, const int32_t* idx, const int32_t* assign_row, int T, int d, int k,
+                           int epg, const uint16_t* residual, uint16_t* y, cudaStream_t st);
+
+// General permutation for any T (multi-CTA, deterministic).
+size_t permute_scratch_bytes(int T, int E, int G);
+cudaError_t launch_permute(const int32_t* idx, int T, int E, int G, int k, const PermPtrs& pm, void* scratch,
+                           unsigned* err, cudaStream_t st);
+
+}  // namespace lmoe

@@ -1,0 +1,50 @@
+// Argument block and launchers of the prefill-path kernels (many tokens).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "decode.cuh"
+
+namespace lmoe {
+
+struct PrefillArgs {
+  int d, E, G, k, L, f, r, epg;
+  const float* W_r;
+  const float* b_r;
+  const uint16_t* W_r_split;  // [3][E][d] bf16: W_r = hi + mid + lo
+  const uint8_t* W_in_q;
+  const uint16_t* W_in_s;
+  const uint8_t* W_out_q;
+  const uint16_t* W_out_s;
+  const uint8_t* gate_q;
+  const uint16_t* gate_s;
+  const uint8_t* up_q;
+  const uint16_t* up_s;
+  const uint8_t* down_q;
+  const uint16_t* down_s;
+  const uint16_t* A_in;
+  const uint16_t* B_in;
+  const uint16_t* A_out;
+  const uint16_t* B_out;
+  unsigned* err;
+  int num_sms;
+  long long timeout;
+};
+
+// W_r fp32 [E][d] -> three bf16 matrices whose sum is W_r (to fp32 rounding).
+cudaError_t launch_split_router(const float* W_r, int E, int d, uint16_t* out, cudaStream_t st);
+
+bool prefill_available();
+size_t prefill_workspace_bytes(const PrefillArgs& P, int T);
+cudaError_t launch_prefill_route(const PrefillArgs& P, const uint16_t* x, int T, int32_t* idx, float* w,
+                                 float* logits, void* ws, cudaStream_t st);
+cudaError_t launch_prefill_experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_t* idx, const float* w,
+                                   const PermPtrs& perm, float* Yrows, const uint16_t* residual, uint16_t* y,
+                                   void* ws, cudaStream_t st);
+cudaError_t launch_prefill_layer(const PrefillArgs& P, const uint16_t* x, int T, const uint16_t* residual,
+                                 uint16_t* y, void* ws, cudaStream_t st, const std::vector<cudaEvent_t>* events);
+const char* prefill_stage_name(const PrefillArgs& P, int T, int i, int* count);
+
+}  // namespace lmoe

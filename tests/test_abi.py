@@ -1,0 +1,60 @@
+"""The C ABI library without a GPU: it loads, exports every entry point the
+header declares, and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "lmoe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(lmoe_[a-z_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_function():
+    from sparse_latent_moe_lmoe_b300 import capi
+    lib = ctypes.CDLL(capi.LIB_PATH)
+    names = header_functions()
+    assert len(names) >= 16
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(capi.EXPORTS)
+
+
+def test_host_side_validation_without_gpu():
+    from sparse_latent_moe_lmoe_b300 import capi
+    lib = capi.library()
+    assert capi.lmoe_version() == 100
+    assert lib.lmoe_workspace_size(None, 8) == 0
+    assert lib.lmoe_route(None, None, 8, None, None, None, None, None) == 1
+    assert lib.lmoe_layer_forward(None, None, 8, None, None, None, None) == 1
+    assert lib.lmoe_set_timeout(None, 5) == 1
+    assert lib.lmoe_check(None, None) == 1
+    assert lib.lmoe_destroy(None) == 0
+    h = ctypes.c_void_p()
+    cfg = capi.LmoeConfig(256, 16, 2, 2, 64, 32, 16, 0, 0, 0, 0, 0, 0)  # qgroup 16: unsupported
+    w = capi.LmoeWeights()
+    assert lib.lmoe_create(ctypes.byref(h), ctypes.byref(cfg), ctypes.byref(w), 0) == 2
+    cfg.qgroup = 32
+    cfg.G = 3  # E % G != 0
+    assert lib.lmoe_create(ctypes.byref(h), ctypes.byref(cfg), ctypes.byref(w), 0) == 1
+    cfg.G = 2
+    assert lib.lmoe_create(ctypes.byref(h), ctypes.byref(cfg), ctypes.byref(w), 0) == 1  # null weights
+    assert h.value is None
+    for s in range(8):
+        assert capi.lmoe_status_string(s)
+    name, count = capi.lmoe_stage_name(None, 8, 0)
+    assert name == "" and count == 0
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    """The package has no fallback: a missing library is an ImportError."""
+    import importlib
+    import sparse_latent_moe_lmoe_b300.capi as capi
+    monkeypatch.setattr(capi, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        capi._load()

@@ -451,3 +451,15 @@ def test_full_layer_against_numpy_chain_tiny():
             Dn = dense(W["down_q"][e], W["down_s"][e])
             ref += wj * (Wout[g] @ (Dn @ (silu(Gt @ h) * (Up @ h))))
         assert np.allclose(y[t], ref, rtol=1e-10, atol=1e-16)
+
+
+def test_combine_closed_form():
+    """Rows summed per token over its distinct groups (a group hit twice is
+    counted once), plus the residual."""
+    Y = np.arange(12, dtype=np.float32).reshape(3, 4)
+    idx = np.array([[0, 3], [2, 1], [3, 2]], np.int32)        # E=4, G=2: groups 0,1 | 1,0 | 1,1
+    ar = np.array([0, 1, 2, 0, 2, 2], np.int32)
+    y = O.combine(Y, idx, ar, 4, 2)
+    assert np.array_equal(y, np.stack([Y[0] + Y[1], Y[0] + Y[2], Y[2]]))
+    res = np.full((3, 4), ONE, np.uint16)
+    assert np.array_equal(O.combine(Y, idx, ar, 4, 2, residual=res), y + 1.0)
