@@ -64,6 +64,10 @@ typedef enum {
   LMOE_ERR_NO_MEMORY = 7      /* lmoe_create could not allocate its private copies */
 } lmoe_status;
 
+/* config.flags: LMOE_FLAG_MULTI_KERNEL_DECODE runs the decode path as its
+ * sequence of per-step kernels instead of the single persistent kernel. */
+enum { LMOE_FLAG_MULTI_KERNEL_DECODE = 1u };
+
 /* Execution path for lmoe_layer_forward / lmoe_expert_forward. */
 enum { LMOE_PATH_AUTO = 0, LMOE_PATH_DECODE = 1, LMOE_PATH_PREFILL = 2 };
 
@@ -77,7 +81,7 @@ typedef struct {
   int qgroup;       /* int4 group size along the reduction dimension; must be 32 */
   int lora_rank;    /* 0 = no LoRA branch; else a multiple of 16, <= 128 */
   int has_bias;     /* nonzero: router bias b_r is used */
-  unsigned flags;   /* reserved, must be 0 */
+  unsigned flags;   /* LMOE_FLAG_* bits */
   long long timeout_cycles; /* bound on any device-side wait (clock64 cycles); 0 = 2^31 */
   int decode_max_T; /* token count up to which AUTO takes the decode path; 0 = 16; <= 16 */
   int force_path;   /* LMOE_PATH_* */
@@ -196,9 +200,12 @@ size_t lmoe_host_staging_size(const lmoe_handle* h, int T);
  * Returns LMOE_OK, LMOE_ERR_TIMEOUT, LMOE_ERR_DEVICE_CHECK or LMOE_ERR_CUDA. */
 lmoe_status lmoe_check(lmoe_handle* h, lmoe_stream stream);
 
-/* Test hook for the bounded-wait path: sets the handle's wait budget (clock64
- * cycles; 0 restores the default). A budget of 1 makes the layer's ticketed
- * combine report LMOE_ERR_TIMEOUT through lmoe_check instead of waiting. */
+/* Sets the handle's budget for bounded device-side waits (clock64 cycles;
+ * 0 restores the config's value, or 2^31). The single-kernel decode pass
+ * waits at grid barriers; when a wait runs out the kernel sets the device
+ * error word and finishes without waiting further, so lmoe_check reports
+ * LMOE_ERR_TIMEOUT and that call's output is invalid. A budget of 1 makes
+ * every such wait run out at once (a test hook for the error path). */
 lmoe_status lmoe_set_timeout(lmoe_handle* h, long long cycles);
 
 /* Profiling hook: when events != NULL, lmoe_layer_forward records

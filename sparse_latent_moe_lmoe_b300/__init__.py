@@ -4,12 +4,22 @@ The layer -- router, top-k with softmax renormalisation, the token
 permutation by group then expert, shared int4 projections around a
 per-expert latent SwiGLU, the optional Recover-LoRA branch and the weighted
 combine -- runs in hand-written CUDA kernels for sm_103a behind the C ABI of
-include/lmoe.h (liblmoe.so, built in-tree). This package is the thin Python
-binding: `capi` has the C functions by name, `LatentMoE` wraps a handle with
-torch-allocated device memory.
+include/lmoe.h (liblmoe.so, built in-tree by `python -m
+sparse_latent_moe_lmoe_b300.build`). This package is the thin Python binding:
+`capi` has the C functions by name, `LatentMoE` wraps a handle with
+torch-allocated device memory. Touching either loads the library and raises
+ImportError if it has not been built -- there is no fallback.
 """
-from . import capi  # noqa: F401  (loads liblmoe.so; raises ImportError if it is not built)
-from .capi import LmoeError, PATH_AUTO, PATH_DECODE, PATH_PREFILL  # noqa: F401
-from .layer import LatentMoE  # noqa: F401
+import importlib
 
 __all__ = ["capi", "LatentMoE", "LmoeError", "PATH_AUTO", "PATH_DECODE", "PATH_PREFILL"]
+
+
+def __getattr__(name):
+    if name == "capi":
+        return importlib.import_module(".capi", __name__)
+    if name == "LatentMoE":
+        return importlib.import_module(".layer", __name__).LatentMoE
+    if name in ("LmoeError", "PATH_AUTO", "PATH_DECODE", "PATH_PREFILL"):
+        return getattr(importlib.import_module(".capi", __name__), name)
+    raise AttributeError(name)

@@ -16,6 +16,7 @@ LMOE_OK = 0
 STATUS = {0: "LMOE_OK", 1: "LMOE_ERR_INVALID_ARG", 2: "LMOE_ERR_UNSUPPORTED", 3: "LMOE_ERR_ALIGNMENT",
           4: "LMOE_ERR_CUDA", 5: "LMOE_ERR_TIMEOUT", 6: "LMOE_ERR_DEVICE_CHECK", 7: "LMOE_ERR_NO_MEMORY"}
 PATH_AUTO, PATH_DECODE, PATH_PREFILL = 0, 1, 2
+FLAG_MULTI_KERNEL_DECODE = 1
 
 EXPORTS = ("lmoe_status_string", "lmoe_version", "lmoe_create", "lmoe_destroy", "lmoe_workspace_size", "lmoe_route",
            "lmoe_permute", "lmoe_expert_forward", "lmoe_combine", "lmoe_layer_forward", "lmoe_layer_forward_host",

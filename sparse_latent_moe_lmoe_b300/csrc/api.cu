@@ -23,6 +23,7 @@ struct lmoe_handle {
   unsigned* d_tickets;   // ticket counters, zero between calls
   uint16_t* d_wr_split;  // [3][E][d] bf16 split of W_r (hi, mid, lo) for the tensor-core router
   long long timeout;
+  int fused_grid;  // CTAs of the single-kernel decode pass (0: unavailable)
   std::vector<cudaEvent_t> events;
 };
 
@@ -46,7 +47,7 @@ lmoe_status validate_config(const lmoe_config* c) {
   if (c->d % 128 != 0 || c->L % 32 != 0 || c->f % 32 != 0) return LMOE_ERR_UNSUPPORTED;
   if (c->L % 16 != 0 || c->f % 16 != 0) return LMOE_ERR_UNSUPPORTED;
   if (c->lora_rank < 0 || c->lora_rank > 128 || c->lora_rank % 16 != 0) return LMOE_ERR_UNSUPPORTED;
-  if (c->flags != 0) return LMOE_ERR_UNSUPPORTED;
+  if (c->flags & ~(unsigned)LMOE_FLAG_MULTI_KERNEL_DECODE) return LMOE_ERR_UNSUPPORTED;
   if (c->decode_max_T < 0 || c->decode_max_T > kMaxDecodeT) return LMOE_ERR_UNSUPPORTED;
   if (c->force_path < LMOE_PATH_AUTO || c->force_path > LMOE_PATH_PREFILL) return LMOE_ERR_INVALID_ARG;
   if (c->timeout_cycles < 0) return LMOE_ERR_INVALID_ARG;
@@ -74,14 +75,34 @@ lmoe_status validate_weights(const lmoe_config* c, const lmoe_weights* w) {
 
 lmoe_status check_handle(const lmoe_handle* h) { return h ? LMOE_OK : LMOE_ERR_INVALID_ARG; }
 
+// K splits of the shared down-projection on the decode path: at most 8
+// chunks of 128 per split (one activation slot), at least min(4, chunks).
 int ks_in_for(const lmoe_config& c) {
   const int nch = (c.d + 127) / 128;
-  return nch < 4 ? nch : 4;
+  const int a = nch < 4 ? nch : 4, b = (nch + 7) / 8;
+  return a > b ? a : b;
+}
+
+// ticket layout in the handle: [0] route, [1 .. 1+d/64) multi-kernel wout,
+// then the fused kernel's barrier and tickets
+struct TicketMap {
+  size_t bar, tk_router, tk_win, tk_wout, total;
+};
+TicketMap ticket_map(const lmoe_config& c) {
+  TicketMap t;
+  size_t o = 1 + (size_t)(c.d + 63) / 64 + 64;
+  o = (o + 1) & ~(size_t)1;  // 8-byte aligned 64-bit counter
+  t.bar = o; o += 2;
+  t.tk_router = o; o += (size_t)(c.E + 1) / 2;
+  t.tk_win = o; o += (size_t)c.G * (c.L / 16);
+  t.tk_wout = o; o += (size_t)c.d / 16;
+  t.total = o + 64;
+  return t;
 }
 
 // ----------------------------------------------------------- workspace map
 struct DecodeWs {
-  size_t logits, idx, w, eo, sa, inv, go, gto, gt, ar, Hp, V, Z, Yp, Pin, Qout, perm_scratch, end;
+  size_t logits, idx, w, eo, sa, inv, go, gto, gt, ar, Hp, V, Z, Yp, Pin, Qout, Lp, H, perm_scratch, end;
 };
 
 DecodeWs decode_ws(const lmoe_config& c, int T) {
@@ -105,11 +126,13 @@ DecodeWs decode_ws(const lmoe_config& c, int T) {
   m.gt = take((size_t)n * gk * 4);
   m.ar = take((size_t)n * c.k * 4);
   m.Hp = take((size_t)ks_in_for(c) * c.G * n * c.L * 4);
-  m.V = take((size_t)n * c.k * c.f * 4);
+  m.V = take((size_t)256 * n * c.f * 4);  // [routed-expert slot <= 256][16][f]
   m.Z = take((size_t)c.G * n * c.L * 4);
   m.Yp = take((size_t)c.G * n * c.d * 4);
   m.Pin = take((size_t)c.G * n * (c.lora_rank > 0 ? c.lora_rank : 1) * 4);
   m.Qout = take((size_t)c.G * n * (c.lora_rank > 0 ? c.lora_rank : 1) * 4);
+  m.Lp = take((size_t)(c.d / 128 + 1) * n * c.E * 4);
+  m.H = take((size_t)c.G * n * c.L * 4);
   m.perm_scratch = take(permute_scratch_bytes(T > n ? T : n, c.E, c.G));
   m.end = o;
   return m;
@@ -201,6 +224,28 @@ struct DeviceGuard {
   }
 };
 
+bool use_fused(const lmoe_handle* h, const DecodeArgs& A) {
+  return !(h->cfg.flags & LMOE_FLAG_MULTI_KERNEL_DECODE) && h->fused_grid > 0 && fused_decode_supported(A);
+}
+
+FusedArgs fused_args(const lmoe_handle* h, const DecodeArgs& A, void* ws) {
+  FusedArgs F;
+  memset(&F, 0, sizeof(F));
+  F.A = A;
+  const DecodeWs m = decode_ws(h->cfg, 0);
+  char* b = reinterpret_cast<char*>(ws);
+  F.Lp = reinterpret_cast<float*>(b + m.Lp);
+  F.logits = reinterpret_cast<float*>(b + m.logits);
+  F.H = reinterpret_cast<float*>(b + m.H);
+  const TicketMap tm = ticket_map(h->cfg);
+  F.bar = reinterpret_cast<unsigned long long*>(h->d_tickets + tm.bar);
+  F.tk_router = h->d_tickets + tm.tk_router;
+  F.tk_win = h->d_tickets + tm.tk_win;
+  F.tk_wout = h->d_tickets + tm.tk_wout;
+  F.timeout = h->timeout;
+  return F;
+}
+
 // decode path for any T, in passes of <= 16 tokens
 lmoe_status decode_layer(lmoe_handle* h, const uint16_t* x, int T, const uint16_t* residual, uint16_t* y, void* ws,
                          cudaStream_t st) {
@@ -213,6 +258,14 @@ lmoe_status decode_layer(lmoe_handle* h, const uint16_t* x, int T, const uint16_
     A.x = x + (size_t)t0 * c.d;
     A.residual = residual ? residual + (size_t)t0 * c.d : nullptr;
     A.y = y + (size_t)t0 * c.d;
+    if (use_fused(h, A)) {
+      FusedArgs F = fused_args(h, A, ws);
+      hook.before(st);
+      cudaError_t e = launch_decode_fused(F, h->fused_grid, st);
+      hook.after(st);
+      if (e != cudaSuccess) return LMOE_ERR_CUDA;
+      continue;
+    }
     hook.before(st);
     cudaError_t e = launch_route(A, 1, ws_logits(h, ws), st);
     hook.after(st);
@@ -290,7 +343,7 @@ lmoe_status lmoe_create(lmoe_handle** out, const lmoe_config* cfg, const lmoe_we
   h->device = device;
   h->num_sms = prop.multiProcessorCount;
   h->timeout = cfg->timeout_cycles ? cfg->timeout_cycles : (1ll << 31);
-  const size_t nt = 1 + (size_t)(cfg->d + 63) / 64 + 64;
+  const size_t nt = ticket_map(*cfg).total;
   if (cudaMalloc(&h->d_err, sizeof(unsigned)) != cudaSuccess ||
       cudaMalloc(&h->d_tickets, nt * sizeof(unsigned)) != cudaSuccess) {
     cudaGetLastError();
@@ -304,10 +357,12 @@ lmoe_status lmoe_create(lmoe_handle** out, const lmoe_config* cfg, const lmoe_we
     lmoe_destroy(h);
     return LMOE_ERR_NO_MEMORY;
   }
-  if (decode_set_attributes() != cudaSuccess || permute_set_attributes() != cudaSuccess) {
+  if (decode_set_attributes() != cudaSuccess || permute_set_attributes() != cudaSuccess ||
+      fused_set_attributes() != cudaSuccess) {
     lmoe_destroy(h);
     return LMOE_ERR_CUDA;
   }
+  h->fused_grid = fused_grid(h->num_sms);
   if (launch_split_router(h->w.W_r, cfg->E, cfg->d, h->d_wr_split, 0) != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess) {
     lmoe_destroy(h);
@@ -523,6 +578,13 @@ const char* lmoe_stage_name(const lmoe_handle* h, int T, int i, int* count) {
   }
   if (use_prefill(h, T)) return prefill_stage_name(prefill_args(h), T, i, count);
   const bool lora = h->cfg.lora_rank > 0;
+  DecodeArgs probe = base_args(h, nullptr);
+  probe.T = T < kMaxDecodeT ? T : kMaxDecodeT;
+  if (T >= 1 && use_fused(h, probe)) {
+    const int passes = (T + kMaxDecodeT - 1) / kMaxDecodeT;
+    if (count) *count = passes;
+    return (i >= 0 && i < passes) ? "decode_fused" : "";
+  }
   const int per = lora ? 7 : 5;
   const int passes = (T + kMaxDecodeT - 1) / kMaxDecodeT;
   if (count) *count = per * passes;

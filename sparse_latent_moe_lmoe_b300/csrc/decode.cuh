@@ -60,6 +60,24 @@ struct DecodeArgs {
   float* Yrows;
 };
 
+// The single-kernel decode pass (decode_fused.cu).
+struct FusedArgs {
+  DecodeArgs A;
+  float* Lp;            // [d / router_slice][16][E] router partial sums
+  float* logits;        // [16][E]
+  float* H;             // [G][16][L] shared down-projection outputs
+  unsigned long long* bar;  // grid barrier arrival counter (monotonic)
+  unsigned* tk_router;  // [E/2]
+  unsigned* tk_win;     // [G * L/16]
+  unsigned* tk_wout;    // [d/16]
+  long long timeout;    // spin budget (clock64 cycles)
+  int router_slice;
+};
+bool fused_decode_supported(const DecodeArgs& A);
+cudaError_t fused_set_attributes();
+int fused_grid(int num_sms);
+cudaError_t launch_decode_fused(FusedArgs F, int grid, cudaStream_t st);
+
 // Records timing events around each launch when attached.
 struct StageHook {
   virtual void before(cudaStream_t) {}

@@ -45,12 +45,12 @@ class LatentMoE:
     """
 
     def __init__(self, shape, weights: dict, device: int = 0, force_path: int = capi.PATH_AUTO,
-                 decode_max_T: int = 0, timeout_cycles: int = 0):
+                 decode_max_T: int = 0, timeout_cycles: int = 0, flags: int = 0):
         self.shape = shape
         self.device = torch.device("cuda", device)
         self.dev_weights = {n: to_device(weights.get(n), self.device) for n in capi.WEIGHT_FIELDS}
         self.cfg = LmoeConfig(shape.d, shape.E, shape.G, shape.k, shape.L, shape.f, 32, shape.lora_rank,
-                              1 if shape.has_bias else 0, 0, timeout_cycles, decode_max_T, force_path)
+                              1 if shape.has_bias else 0, flags, timeout_cycles, decode_max_T, force_path)
         self.wts = LmoeWeights(*[None if t is None else t.data_ptr() for t in
                                  (self.dev_weights[n] for n in capi.WEIGHT_FIELDS)])
         self.h = capi.lmoe_create(self.cfg, self.wts, device)
