@@ -138,9 +138,11 @@ DecodeWs decode_ws(const lmoe_config& c, int T) {
   return m;
 }
 
+PrefillArgs prefill_args(const lmoe_handle* h);
+
 bool use_prefill(const lmoe_handle* h, int T) {
   const lmoe_config& c = h->cfg;
-  if (!prefill_available()) return false;
+  if (!prefill_supported(prefill_args(h))) return false;
   if (c.force_path == LMOE_PATH_DECODE) return false;
   if (c.force_path == LMOE_PATH_PREFILL) return T > 0;
   const int mt = c.decode_max_T ? c.decode_max_T : kMaxDecodeT;
@@ -358,7 +360,7 @@ lmoe_status lmoe_create(lmoe_handle** out, const lmoe_config* cfg, const lmoe_we
     return LMOE_ERR_NO_MEMORY;
   }
   if (decode_set_attributes() != cudaSuccess || permute_set_attributes() != cudaSuccess ||
-      fused_set_attributes() != cudaSuccess) {
+      fused_set_attributes() != cudaSuccess || prefill_set_attributes() != cudaSuccess) {
     lmoe_destroy(h);
     return LMOE_ERR_CUDA;
   }

@@ -1,9 +1,474 @@
-// Prefill path of the latent MoE layer (many tokens): grouped int4-dequant
-// GEMMs on the tcgen05 tensor cores.
+// Prefill path of the latent MoE layer (many tokens): the router and every
+// projection are GEMMs on the tcgen05 tensor cores (tc_gemm.cuh), with the
+// int4 weights dequantised to fp16 by the GEMM's own producer warps.
+//
+//   route    logits = x . (W_hi + W_mid + W_lo)^T  (W_r split into three
+//            bf16 terms at create time; x is exact in bf16; fp32 accumulate)
+//            with the top-k and softmax renormalisation in the epilogue
+//            (one thread per token, all E logits of its row from TMEM)
+//   permute  the deterministic multi-CTA permutation (permute.cu)
+//   win      H[(g,t)] = Win[g] x_t        grouped by group, rows gathered
+//   gateup   V[a] = silu(Gate_e h) * Up_e h   grouped by expert (128 gate
+//            rows + the matching 128 up rows per tile, SwiGLU in the epilogue)
+//   down     U[a] = w_a * Down_e V[a]     grouped by expert
+//   zreduce  Z[(g,t)] = sum_{j: g(e_j) = g} U[(t,j)]  in ascending j
+//   wout     y_t = sum_g Wout[g] Z[(g,t)] (+ residual): one GEMM over K =
+//            G*L per token tile (absent (g,t) rows read as zero), so the
+//            weighted combine happens in the accumulator
+// Intermediates H, V, Z are fp16 tensor-core operands, U is fp32.
+#include <cuda.h>
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "prefill.cuh"
+#include "tc_gemm.cuh"
 
 namespace lmoe {
+
+using tc::Tile;
+
+// ------------------------------------------------------------- tile tables
+
+// scratch[0..n] = exclusive prefix of per-problem tile counts (computed by
+// the whole CTA); returns through scratch[n] the total.
+template <class CountF>
+LMOE_DEV void tile_prefix(int* scratch, int n, CountF count) {
+  __shared__ int warp_tot[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x;
+  int carry = 0;
+  for (int b0 = 0; b0 < n; b0 += nt) {
+    const int i = b0 + tid;
+    const int v = i < n ? count(i) : 0;
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
+    }
+    if (lane == 31) warp_tot[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+      const int nw = nt >> 5;
+      int wv = lane < nw ? warp_tot[lane] : 0, wi = wv;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += t;
+      }
+      if (lane < nw) warp_tot[lane] = wi - wv;
+    }
+    __syncthreads();
+    if (i < n) scratch[i] = carry + warp_tot[warp] + inc - v;
+    if (tid == nt - 1) scratch[n] = carry + warp_tot[warp] + inc;  // running total
+    __syncthreads();
+    carry = scratch[n];
+    __syncthreads();
+  }
+  if (n == 0 && tid == 0) scratch[0] = 0;
+  __syncthreads();
+}
+
+// largest p with scratch[p] <= t (problems with zero tiles are skipped)
+LMOE_DEV int find_prob(const int* scratch, int n, int t) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (scratch[mid] <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+struct ProbBase {
+  long long budget;
+  unsigned* err;
+};
+
+LMOE_DEV void mma_k4(uint32_t d_tmem, uint64_t da, uint64_t db, uint32_t id, int kb) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) tc::mma_f16(d_tmem, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), id, (kb > 0 || k > 0) ? 1u : 0u);
+}
+
+LMOE_DEV void store_half16(__half* dst, const float v[16]) {
+  uint32_t h[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) h[i] = pack_half2(v[2 * i], v[2 * i + 1]);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  d4[0] = make_uint4(h[0], h[1], h[2], h[3]);
+  d4[1] = make_uint4(h[4], h[5], h[6], h[7]);
+}
+
+// ------------------------------------------------------------------ router
+struct ProbRoute : ProbBase {
+  static constexpr int BN = 512, ACC_COLS = 512, A_MODE = 2, B_MODE = 1, STAGES = 2;
+  const uint16_t* x;      // [T][d] bf16
+  const uint16_t* wsplit; // [3][E][d] bf16
+  const float* bias;      // [E] or null
+  int T, d, E, k;
+  int32_t* idx;
+  float* w;
+  float* logits;          // [T][E] or null
+  LMOE_DEV void init(int*) {}
+  LMOE_DEV int num_tiles(const int*) const { return (T + 127) / 128; }
+  LMOE_DEV Tile tile(const int*, int t) const {
+    Tile tl;
+    tl.prob = 0;
+    tl.m0 = t * 128;
+    tl.n0 = 0;
+    tl.rows = min(128, T - tl.m0);
+    tl.nkb = 3 * (d / 64);
+    return tl;
+  }
+  LMOE_DEV const void* a_row(const int*, const Tile& tl, int r, int kb) const {
+    return x + (size_t)(tl.m0 + r) * d + (kb / 3) * 64;
+  }
+  LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int n, int kb) const {
+    if (n >= E) return nullptr;
+    return wsplit + ((size_t)(kb % 3) * E + n) * d + (kb / 3) * 64;
+  }
+  LMOE_DEV bool b_row(const int*, const Tile&, int, int, const uint8_t*&, const uint16_t*&) const { return false; }
+  LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
+    const uint32_t id = tc::idesc(128, 256, 1);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
+      tc::mma_f16(d_tmem, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), id, acc);
+      tc::mma_f16(d_tmem + 256, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k) + (uint64_t)((256 * 128) >> 4), id, acc);
+    }
+  }
+  // one thread per token: top-k (descending logit, ties to the lower index)
+  // over the row's E logits, softmax over the selected ones
+  LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase) const {
+    float tv[16];
+    int te[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      tv[j] = -INFINITY;
+      te[j] = 0x7fffffff;
+    }
+    const bool valid = row < tl.rows;
+    const int t = tl.m0 + row;
+    for (int c0 = 0; c0 < 512; c0 += 16) {
+      float v[16];
+      tc::tmem_ld16(tbase + (uint32_t)c0, v);  // warp-collective: every lane loads
+      if (!valid || c0 >= E) continue;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int e = c0 + i;
+        if (e >= E) continue;
+        float l = v[i];
+        if (bias) l += bias[e];
+        if (logits) logits[(size_t)t * E + e] = l;
+        // insert if strictly better than the current k-th (an equal later index loses)
+        float kth = tv[15];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (j == k - 1) kth = tv[j];
+        if (l > kth) {
+          float cv = l;
+          int ce = e;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (j < k && cv > tv[j]) {
+              const float sv = tv[j];
+              const int se = te[j];
+              tv[j] = cv;
+              te[j] = ce;
+              cv = sv;
+              ce = se;
+            }
+          }
+        }
+      }
+    }
+    if (!valid) return;
+    float z = 0.f, ex[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      ex[j] = j < k ? __expf(tv[j] - tv[0]) : 0.f;
+      z += ex[j];
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (j < k) {
+        idx[(size_t)t * k + j] = te[j];
+        w[(size_t)t * k + j] = ex[j] / z;
+      }
+  }
+};
+
+// -------------------------------------------------------------------- W_in
+struct ProbWin : ProbBase {
+  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 1, B_MODE = 0, STAGES = 4;
+  const uint16_t* x;  // [T][d] bf16
+  int d, L, G;
+  const int32_t* gto;
+  const int32_t* gtok;
+  const uint8_t* Wq;
+  const uint16_t* Ws;
+  __half* H;  // [rows][L]
+  LMOE_DEV int ntn() const { return L / 256; }
+  LMOE_DEV void init(int* sc) {
+    tile_prefix(sc, G, [&](int g) { return ((gto[g + 1] - gto[g] + 127) / 128) * ntn(); });
+  }
+  LMOE_DEV int num_tiles(const int* sc) const { return sc[G]; }
+  LMOE_DEV Tile tile(const int* sc, int t) const {
+    Tile tl;
+    const int g = find_prob(sc, G, t), loc = t - sc[g];
+    tl.prob = g;
+    tl.m0 = (loc / ntn()) * 128;
+    tl.n0 = (loc % ntn()) * 256;
+    tl.rows = min(128, gto[g + 1] - gto[g] - tl.m0);
+    tl.nkb = d / 64;
+    return tl;
+  }
+  LMOE_DEV const void* a_row(const int*, const Tile& tl, int r, int kb) const {
+    const int tok = gtok[gto[tl.prob] + tl.m0 + r];
+    return x + (size_t)tok * d + kb * 64;
+  }
+  LMOE_DEV bool b_row(const int*, const Tile& tl, int n, int kb, const uint8_t*& q, const uint16_t*& s) const {
+    const size_t row = (size_t)tl.prob * L + tl.n0 + n;
+    q = Wq + row * (d / 2) + kb * 32;
+    s = Ws + row * (d / 32) + kb * 2;
+    return true;
+  }
+  LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int, int) const { return nullptr; }
+  LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
+    mma_k4(d_tmem, da, db, tc::idesc(128, 256, 0), kb);
+  }
+  LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase) const {
+    for (int c0 = 0; c0 < 256; c0 += 16) {
+      float v[16];
+      tc::tmem_ld16(tbase + (uint32_t)c0, v);
+      if (row < tl.rows) store_half16(H + (size_t)(gto[tl.prob] + tl.m0 + row) * L + tl.n0 + c0, v);
+    }
+  }
+};
+
+// ---------------------------------------------------------------- gate/up
+struct ProbGateUp : ProbBase {
+  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 0, B_MODE = 0, STAGES = 4;
+  const __half* H;
+  int L, f, E;
+  const int32_t* eo;
+  const int32_t* sa;
+  const int32_t* arow;
+  const uint8_t *gq, *uq;
+  const uint16_t *gs, *us;
+  __half* V;  // [T*k][f]
+  LMOE_DEV int ntn() const { return f / 128; }
+  LMOE_DEV void init(int* sc) {
+    tile_prefix(sc, E, [&](int e) { return ((eo[e + 1] - eo[e] + 127) / 128) * ntn(); });
+  }
+  LMOE_DEV int num_tiles(const int* sc) const { return sc[E]; }
+  LMOE_DEV Tile tile(const int* sc, int t) const {
+    Tile tl;
+    const int e = find_prob(sc, E, t), loc = t - sc[e];
+    tl.prob = e;
+    tl.m0 = (loc / ntn()) * 128;
+    tl.n0 = (loc % ntn()) * 128;
+    tl.rows = min(128, eo[e + 1] - eo[e] - tl.m0);
+    tl.nkb = L / 64;
+    return tl;
+  }
+  LMOE_DEV const void* a_row(const int*, const Tile& tl, int r, int kb) const {
+    const int p = eo[tl.prob] + tl.m0 + r;
+    return H + (size_t)arow[sa[p]] * L + kb * 64;
+  }
+  LMOE_DEV bool b_row(const int*, const Tile& tl, int n, int kb, const uint8_t*& q, const uint16_t*& s) const {
+    const bool up = n >= 128;
+    const size_t row = (size_t)tl.prob * f + tl.n0 + (n & 127);
+    q = (up ? uq : gq) + row * (L / 2) + kb * 32;
+    s = (up ? us : gs) + row * (L / 32) + kb * 2;
+    return true;
+  }
+  LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int, int) const { return nullptr; }
+  LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
+    mma_k4(d_tmem, da, db, tc::idesc(128, 256, 0), kb);
+  }
+  LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase) const {
+    for (int c0 = 0; c0 < 128; c0 += 16) {
+      float g[16], u[16];
+      tc::tmem_ld16(tbase + (uint32_t)c0, g);
+      tc::tmem_ld16(tbase + (uint32_t)(128 + c0), u);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) g[i] = silu(g[i]) * u[i];
+      if (row < tl.rows) store_half16(V + (size_t)(eo[tl.prob] + tl.m0 + row) * f + tl.n0 + c0, g);
+    }
+  }
+};
+
+// ------------------------------------------------------------------- down
+struct ProbDown : ProbBase {
+  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 0, B_MODE = 0, STAGES = 4;
+  const __half* V;
+  int L, f, E;
+  const int32_t* eo;
+  const int32_t* sa;
+  const float* wts;  // [T*k]
+  const uint8_t* dq;
+  const uint16_t* ds;
+  float* U;  // [T*k][L]
+  LMOE_DEV int ntn() const { return L / 256; }
+  LMOE_DEV void init(int* sc) {
+    tile_prefix(sc, E, [&](int e) { return ((eo[e + 1] - eo[e] + 127) / 128) * ntn(); });
+  }
+  LMOE_DEV int num_tiles(const int* sc) const { return sc[E]; }
+  LMOE_DEV Tile tile(const int* sc, int t) const {
+    Tile tl;
+    const int e = find_prob(sc, E, t), loc = t - sc[e];
+    tl.prob = e;
+    tl.m0 = (loc / ntn()) * 128;
+    tl.n0 = (loc % ntn()) * 256;
+    tl.rows = min(128, eo[e + 1] - eo[e] - tl.m0);
+    tl.nkb = f / 64;
+    return tl;
+  }
+  LMOE_DEV const void* a_row(const int*, const Tile& tl, int r, int kb) const {
+    return V + (size_t)(eo[tl.prob] + tl.m0 + r) * f + kb * 64;
+  }
+  LMOE_DEV bool b_row(const int*, const Tile& tl, int n, int kb, const uint8_t*& q, const uint16_t*& s) const {
+    const size_t row = (size_t)tl.prob * L + tl.n0 + n;
+    q = dq + row * (f / 2) + kb * 32;
+    s = ds + row * (f / 32) + kb * 2;
+    return true;
+  }
+  LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int, int) const { return nullptr; }
+  LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
+    mma_k4(d_tmem, da, db, tc::idesc(128, 256, 0), kb);
+  }
+  LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase) const {
+    const bool valid = row < tl.rows;
+    const int p = eo[tl.prob] + tl.m0 + row;
+    const float wt = valid ? wts[sa[p]] : 0.f;
+    for (int c0 = 0; c0 < 256; c0 += 16) {
+      float v[16];
+      tc::tmem_ld16(tbase + (uint32_t)c0, v);
+      if (!valid) continue;
+      float4* dst = reinterpret_cast<float4*>(U + (size_t)p * L + tl.n0 + c0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) dst[i] = make_float4(wt * v[4 * i], wt * v[4 * i + 1], wt * v[4 * i + 2], wt * v[4 * i + 3]);
+    }
+  }
+};
+
+// ------------------------------------------------------------------- W_out
+// mode 0: y_t = sum_g Wout[g] Z[(g,t)] (+ residual), tiles over tokens, K = G*L
+// mode 1: Y[(g,t)] = Wout[g] Z[(g,t)] (fp32 rows), tiles over group rows
+struct ProbWout : ProbBase {
+  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 0, B_MODE = 0, STAGES = 4;
+  const __half* Z;        // [rows][L]
+  const int32_t* tokrow;  // [T][G]: row of (g, t) in Z or -1
+  const int32_t* gto;
+  int T, d, L, G, mode;
+  const uint8_t* Wq;
+  const uint16_t* Ws;
+  const uint16_t* residual;
+  uint16_t* y;  // [T][d] bf16 (mode 0)
+  float* Y;     // [rows][d] (mode 1)
+  LMOE_DEV int ntn() const { return d / 256; }
+  LMOE_DEV int kpg() const { return L / 64; }
+  LMOE_DEV void init(int* sc) {
+    if (mode == 1) tile_prefix(sc, G, [&](int g) { return ((gto[g + 1] - gto[g] + 127) / 128) * ntn(); });
+  }
+  LMOE_DEV int num_tiles(const int* sc) const { return mode == 0 ? ((T + 127) / 128) * ntn() : sc[G]; }
+  LMOE_DEV Tile tile(const int* sc, int t) const {
+    Tile tl;
+    if (mode == 0) {
+      tl.prob = 0;
+      tl.m0 = (t / ntn()) * 128;
+      tl.n0 = (t % ntn()) * 256;
+      tl.rows = min(128, T - tl.m0);
+      tl.nkb = G * kpg();
+    } else {
+      const int g = find_prob(sc, G, t), loc = t - sc[g];
+      tl.prob = g;
+      tl.m0 = (loc / ntn()) * 128;
+      tl.n0 = (loc % ntn()) * 256;
+      tl.rows = min(128, gto[g + 1] - gto[g] - tl.m0);
+      tl.nkb = kpg();
+    }
+    return tl;
+  }
+  LMOE_DEV const void* a_row(const int*, const Tile& tl, int r, int kb) const {
+    if (mode == 0) {
+      const int g = kb / kpg(), kk = kb % kpg();
+      const int zr = tokrow[(size_t)(tl.m0 + r) * G + g];
+      return zr < 0 ? nullptr : Z + (size_t)zr * L + kk * 64;
+    }
+    return Z + (size_t)(gto[tl.prob] + tl.m0 + r) * L + kb * 64;
+  }
+  LMOE_DEV bool b_row(const int*, const Tile& tl, int n, int kb, const uint8_t*& q, const uint16_t*& s) const {
+    const int g = mode == 0 ? kb / kpg() : tl.prob, kk = mode == 0 ? kb % kpg() : kb;
+    const size_t row = (size_t)g * d + tl.n0 + n;
+    q = Wq + row * (L / 2) + kk * 32;
+    s = Ws + row * (L / 32) + kk * 2;
+    return true;
+  }
+  LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int, int) const { return nullptr; }
+  LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
+    mma_k4(d_tmem, da, db, tc::idesc(128, 256, 0), kb);
+  }
+  LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase) const {
+    const bool valid = row < tl.rows;
+    for (int c0 = 0; c0 < 256; c0 += 16) {
+      float v[16];
+      tc::tmem_ld16(tbase + (uint32_t)c0, v);
+      if (!valid) continue;
+      if (mode == 0) {
+        const size_t o = (size_t)(tl.m0 + row) * d + tl.n0 + c0;
+        uint32_t h[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float a = v[2 * i], b = v[2 * i + 1];
+          if (residual) {
+            a += bf16_to_f32(residual[o + 2 * i]);
+            b += bf16_to_f32(residual[o + 2 * i + 1]);
+          }
+          h[i] = (uint32_t)f32_to_bf16_rne(a) | ((uint32_t)f32_to_bf16_rne(b) << 16);
+        }
+        uint4* d4 = reinterpret_cast<uint4*>(y + o);
+        d4[0] = make_uint4(h[0], h[1], h[2], h[3]);
+        d4[1] = make_uint4(h[4], h[5], h[6], h[7]);
+      } else {
+        float4* dst = reinterpret_cast<float4*>(Y + (size_t)(gto[tl.prob] + tl.m0 + row) * d + tl.n0 + c0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      }
+    }
+  }
+};
+
+// ----------------------------------------------------------------- zreduce
+// One warp per (group, token) row: Z[row] = sum over the token's experts in
+// that group, in ascending j, of U[inv[t*k + j]]; tokrow[t][g] = row.
+__global__ void zreduce_kernel(const float* __restrict__ U, const int32_t* __restrict__ idx,
+                               const int32_t* __restrict__ inv, const int32_t* __restrict__ gto,
+                               const int32_t* __restrict__ gtok, int G, int k, int epg, int L, __half* __restrict__ Z,
+                               int32_t* __restrict__ tokrow) {
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= gto[G]) return;
+  int g = 0;
+  while (g + 1 < G && gto[g + 1] <= row) ++g;
+  const int t = gtok[row];
+  if (lane == 0) tokrow[(size_t)t * G + g] = row;
+  for (int c = lane * 8; c < L; c += 256) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < k; ++j) {
+      if (idx[(size_t)t * k + j] / epg != g) continue;
+      const float4* u = reinterpret_cast<const float4*>(U + (size_t)inv[(size_t)t * k + j] * L + c);
+      const float4 a = u[0], b = u[1];
+      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    }
+    uint4 o;
+    o.x = pack_half2(acc[0], acc[1]);
+    o.y = pack_half2(acc[2], acc[3]);
+    o.z = pack_half2(acc[4], acc[5]);
+    o.w = pack_half2(acc[6], acc[7]);
+    *reinterpret_cast<uint4*>(Z + (size_t)row * L + c) = o;
+  }
+}
 
 // W = hi + mid + lo with each term the bf16 rounding of what remains; the
 // three terms carry 24 significant bits, so the split is exact for every
@@ -27,28 +492,224 @@ cudaError_t launch_split_router(const float* W_r, int E, int d, uint16_t* out, c
   return cudaGetLastError();
 }
 
-bool prefill_available() { return false; }
+// ------------------------------------------------------------------ host side
 
-size_t prefill_workspace_bytes(const PrefillArgs&, int) { return 0; }
+namespace {
 
-cudaError_t launch_prefill_route(const PrefillArgs&, const uint16_t*, int, int32_t*, float*, float*, void*,
-                                 cudaStream_t) {
-  return cudaErrorNotSupported;
+constexpr size_t kAl = 256;
+size_t al(size_t v) { return (v + kAl - 1) & ~(kAl - 1); }
+
+struct PWs {
+  size_t idx, w, eo, sa, inv, go, gto, gt, ar, perm_scratch, H, V, U, Z, tokrow, end;
+};
+
+PWs pws(const PrefillArgs& P, int T) {
+  PWs m;
+  size_t o = 0;
+  auto take = [&](size_t b) {
+    size_t at = o;
+    o = al(o + b);
+    return at;
+  };
+  const size_t n = (size_t)T * P.k, gk = (size_t)T * (P.G < P.k ? P.G : P.k);
+  m.idx = take(n * 4);
+  m.w = take(n * 4);
+  m.eo = take((size_t)(P.E + 1) * 4);
+  m.sa = take(n * 4);
+  m.inv = take(n * 4);
+  m.go = take((size_t)(P.G + 1) * 4);
+  m.gto = take((size_t)(P.G + 1) * 4);
+  m.gt = take(gk * 4);
+  m.ar = take(n * 4);
+  m.perm_scratch = take(permute_scratch_bytes(T, P.E, P.G));
+  m.H = take(gk * P.L * 2);
+  m.V = take(n * P.f * 2);
+  m.U = take(n * P.L * 4);
+  m.Z = take(gk * P.L * 2);
+  m.tokrow = take((size_t)T * P.G * 4);
+  m.end = o;
+  return m;
 }
 
-cudaError_t launch_prefill_experts(const PrefillArgs&, const uint16_t*, int, const int32_t*, const float*,
-                                   const PermPtrs&, float*, const uint16_t*, uint16_t*, void*, cudaStream_t) {
-  return cudaErrorNotSupported;
+template <class Prob>
+cudaError_t set_attr() {
+  return cudaFuncSetAttribute(tc::gemm_kernel<Prob>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              tc::smem_bytes<Prob>());
 }
 
-cudaError_t launch_prefill_layer(const PrefillArgs&, const uint16_t*, int, const uint16_t*, uint16_t*, void*,
-                                 cudaStream_t, const std::vector<cudaEvent_t>*) {
-  return cudaErrorNotSupported;
+template <class Prob>
+cudaError_t run_gemm(const Prob& p, int grid, cudaStream_t st) {
+  tc::gemm_kernel<Prob><<<grid, tc::THREADS, tc::smem_bytes<Prob>(), st>>>(p);
+  return cudaGetLastError();
 }
 
-const char* prefill_stage_name(const PrefillArgs&, int, int, int* count) {
-  if (count) *count = 0;
-  return "";
+struct EvHook {
+  const std::vector<cudaEvent_t>* ev;
+  int i = 0;
+  void rec(cudaEvent_t e, cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+      cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+    else
+      cudaEventRecord(e, s);
+  }
+  void before(cudaStream_t s) {
+    if (ev && 2 * i < (int)ev->size()) rec((*ev)[2 * i], s);
+  }
+  void after(cudaStream_t s) {
+    if (ev && 2 * i + 1 < (int)ev->size()) rec((*ev)[2 * i + 1], s);
+    ++i;
+  }
+};
+
+PermPtrs perm_ptrs(char* b, const PWs& m) {
+  PermPtrs pm;
+  pm.expert_offsets = reinterpret_cast<int32_t*>(b + m.eo);
+  pm.sorted_assign = reinterpret_cast<int32_t*>(b + m.sa);
+  pm.inv = reinterpret_cast<int32_t*>(b + m.inv);
+  pm.group_offsets = reinterpret_cast<int32_t*>(b + m.go);
+  pm.group_tok_offsets = reinterpret_cast<int32_t*>(b + m.gto);
+  pm.group_tokens = reinterpret_cast<int32_t*>(b + m.gt);
+  pm.assign_row = reinterpret_cast<int32_t*>(b + m.ar);
+  return pm;
+}
+
+ProbBase base(const PrefillArgs& P) {
+  ProbBase b;
+  b.budget = P.timeout;
+  b.err = P.err;
+  return b;
+}
+
+// expert part of the layer after routing and permutation: win, gateup, down,
+// zreduce, then wout (mode 0 -> y, mode 1 -> Yrows)
+cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_t* idx, const float* w,
+                    const PermPtrs& pm, char* b, const PWs& m, int mode, float* Yrows, const uint16_t* residual,
+                    uint16_t* y, cudaStream_t st, EvHook* hook) {
+  const int grid = P.num_sms;
+  __half* H = reinterpret_cast<__half*>(b + m.H);
+  __half* V = reinterpret_cast<__half*>(b + m.V);
+  float* U = reinterpret_cast<float*>(b + m.U);
+  __half* Z = reinterpret_cast<__half*>(b + m.Z);
+  int32_t* tokrow = reinterpret_cast<int32_t*>(b + m.tokrow);
+  cudaError_t e;
+  {
+    ProbWin p;
+    static_cast<ProbBase&>(p) = base(P);
+    p.x = x; p.d = P.d; p.L = P.L; p.G = P.G; p.gto = pm.group_tok_offsets; p.gtok = pm.group_tokens;
+    p.Wq = P.W_in_q; p.Ws = P.W_in_s; p.H = H;
+    if (hook) hook->before(st);
+    if ((e = run_gemm(p, grid, st)) != cudaSuccess) return e;
+    if (hook) hook->after(st);
+  }
+  {
+    ProbGateUp p;
+    static_cast<ProbBase&>(p) = base(P);
+    p.H = H; p.L = P.L; p.f = P.f; p.E = P.E; p.eo = pm.expert_offsets; p.sa = pm.sorted_assign; p.arow = pm.assign_row;
+    p.gq = P.gate_q; p.gs = P.gate_s; p.uq = P.up_q; p.us = P.up_s; p.V = V;
+    if (hook) hook->before(st);
+    if ((e = run_gemm(p, grid, st)) != cudaSuccess) return e;
+    if (hook) hook->after(st);
+  }
+  {
+    ProbDown p;
+    static_cast<ProbBase&>(p) = base(P);
+    p.V = V; p.L = P.L; p.f = P.f; p.E = P.E; p.eo = pm.expert_offsets; p.sa = pm.sorted_assign; p.wts = w;
+    p.dq = P.down_q; p.ds = P.down_s; p.U = U;
+    if (hook) hook->before(st);
+    if ((e = run_gemm(p, grid, st)) != cudaSuccess) return e;
+    if (hook) hook->after(st);
+  }
+  {
+    if (hook) hook->before(st);
+    cudaMemsetAsync(tokrow, 0xff, (size_t)T * P.G * 4, st);
+    const int rows_cap = T * (P.G < P.k ? P.G : P.k);
+    zreduce_kernel<<<(rows_cap + 7) / 8, 256, 0, st>>>(U, idx, pm.inv, pm.group_tok_offsets, pm.group_tokens, P.G,
+                                                      P.k, P.epg, P.L, Z, tokrow);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (hook) hook->after(st);
+  }
+  {
+    ProbWout p;
+    static_cast<ProbBase&>(p) = base(P);
+    p.Z = Z; p.tokrow = tokrow; p.gto = pm.group_tok_offsets; p.T = T; p.d = P.d; p.L = P.L; p.G = P.G; p.mode = mode;
+    p.Wq = P.W_out_q; p.Ws = P.W_out_s; p.residual = residual; p.y = y; p.Y = Yrows;
+    if (hook) hook->before(st);
+    if ((e = run_gemm(p, grid, st)) != cudaSuccess) return e;
+    if (hook) hook->after(st);
+  }
+  return cudaSuccess;
+}
+
+cudaError_t route(const PrefillArgs& P, const uint16_t* x, int T, int32_t* idx, float* w, float* logits,
+                  cudaStream_t st) {
+  ProbRoute p;
+  static_cast<ProbBase&>(p) = base(P);
+  p.x = x; p.wsplit = P.W_r_split; p.bias = P.b_r; p.T = T; p.d = P.d; p.E = P.E; p.k = P.k;
+  p.idx = idx; p.w = w; p.logits = logits;
+  return run_gemm(p, P.num_sms, st);
+}
+
+}  // namespace
+
+cudaError_t prefill_set_attributes() {
+  cudaError_t e;
+  if ((e = set_attr<ProbRoute>()) != cudaSuccess) return e;
+  if ((e = set_attr<ProbWin>()) != cudaSuccess) return e;
+  if ((e = set_attr<ProbGateUp>()) != cudaSuccess) return e;
+  if ((e = set_attr<ProbDown>()) != cudaSuccess) return e;
+  return set_attr<ProbWout>();
+}
+
+bool prefill_supported(const PrefillArgs& P) {
+  if (P.r != 0) return false;  // the LoRA branch runs on the decode path
+  if (P.d % 256 != 0 || P.L % 256 != 0 || P.f % 128 != 0) return false;
+  if (P.E > 512 || P.k > 16 || P.G > 64) return false;  // router tile: all experts in one accumulator
+  return P.num_sms > 0;
+}
+
+size_t prefill_workspace_bytes(const PrefillArgs& P, int T) {
+  if (!prefill_supported(P) || T <= 0) return 0;
+  return pws(P, T).end;
+}
+
+cudaError_t launch_prefill_route(const PrefillArgs& P, const uint16_t* x, int T, int32_t* idx, float* w,
+                                 float* logits, void*, cudaStream_t st) {
+  return route(P, x, T, idx, w, logits, st);
+}
+
+cudaError_t launch_prefill_experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_t* idx, const float* w,
+                                   const PermPtrs& perm, float* Yrows, const uint16_t*, uint16_t*, void* ws,
+                                   cudaStream_t st) {
+  char* b = reinterpret_cast<char*>(ws);
+  const PWs m = pws(P, T);
+  return experts(P, x, T, idx, w, perm, b, m, 1, Yrows, nullptr, nullptr, st, nullptr);
+}
+
+cudaError_t launch_prefill_layer(const PrefillArgs& P, const uint16_t* x, int T, const uint16_t* residual,
+                                 uint16_t* y, void* ws, cudaStream_t st, const std::vector<cudaEvent_t>* events) {
+  char* b = reinterpret_cast<char*>(ws);
+  const PWs m = pws(P, T);
+  int32_t* idx = reinterpret_cast<int32_t*>(b + m.idx);
+  float* w = reinterpret_cast<float*>(b + m.w);
+  const PermPtrs pm = perm_ptrs(b, m);
+  EvHook hook;
+  hook.ev = events;
+  EvHook* hk = events ? &hook : nullptr;
+  cudaError_t e;
+  if (hk) hk->before(st);
+  if ((e = route(P, x, T, idx, w, nullptr, st)) != cudaSuccess) return e;
+  if (hk) hk->after(st);
+  if (hk) hk->before(st);
+  if ((e = launch_permute(idx, T, P.E, P.G, P.k, pm, b + m.perm_scratch, P.err, st)) != cudaSuccess) return e;
+  if (hk) hk->after(st);
+  return experts(P, x, T, idx, w, pm, b, m, 0, nullptr, residual, y, st, hk);
+}
+
+const char* prefill_stage_name(const PrefillArgs&, int, int i, int* count) {
+  static const char* names[] = {"route", "permute", "win", "gateup", "down", "zreduce", "wout"};
+  if (count) *count = 7;
+  return (i >= 0 && i < 7) ? names[i] : "";
 }
 
 }  // namespace lmoe

@@ -36,7 +36,8 @@ struct PrefillArgs {
 // W_r fp32 [E][d] -> three bf16 matrices whose sum is W_r (to fp32 rounding).
 cudaError_t launch_split_router(const float* W_r, int E, int d, uint16_t* out, cudaStream_t st);
 
-bool prefill_available();
+bool prefill_supported(const PrefillArgs& P);
+cudaError_t prefill_set_attributes();
 size_t prefill_workspace_bytes(const PrefillArgs& P, int T);
 cudaError_t launch_prefill_route(const PrefillArgs& P, const uint16_t* x, int T, int32_t* idx, float* w,
                                  float* logits, void* ws, cudaStream_t st);

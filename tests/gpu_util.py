@@ -6,8 +6,9 @@ Bars (derivations in DESIGN.md, "Parity bars"):
     unique at the logit tolerance (a near-tie between the k-th and (k+1)-th
     oracle logits) may differ and are counted, and their outputs excluded;
   - router logits: |l_gpu - l_ref| <= 1e-5 * max_e |l_ref| per token;
-  - renormalised weights: relative 2e-5 (fp32 exp and sum of logits that
-    agree to the logit bar);
+  - renormalised weights: relative 2 * (logit bar of the row) + 2e-6 (the
+    weights depend on logit differences, each known to the logit bar, plus
+    fp32 exp and sum);
   - layer outputs (bf16): compared with bf16(oracle): mean relative error
     sum|y - bf16(y_ref)| / sum|y_ref| <= 1e-3 and max-abs <= 2e-2.
 """
@@ -18,7 +19,7 @@ import lmoe_synth as S
 import oracle as O
 
 LOGIT_RTOL = 1e-5
-W_RTOL = 2e-5
+W_RTOL = 2e-6
 MEAN_REL = 1e-3
 MAX_ABS = 2e-2
 
@@ -60,7 +61,8 @@ def check_routing(lg_gpu, idx_gpu, w_gpu, lg_ref, idx_ref, w_ref, k):
             sel = np.sort(lg_ref[t, idx_ref[t]])
             assert np.min(np.diff(sel)) <= 2 * tol[t], f"order differs on token {t}"
         else:
-            assert np.allclose(w_gpu[t], w_ref[t], rtol=W_RTOL, atol=1e-7), (t, w_gpu[t], w_ref[t])
+            rt = 2 * tol[t] + W_RTOL
+            assert np.allclose(w_gpu[t], w_ref[t], rtol=rt, atol=1e-7), (t, w_gpu[t], w_ref[t], rt)
     return ~amb
 
 
