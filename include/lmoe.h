@@ -185,6 +185,41 @@ lmoe_status lmoe_combine(lmoe_handle* h, const float* Y, const int32_t* idx, con
 lmoe_status lmoe_layer_forward(lmoe_handle* h, const uint16_t* x, int T, const uint16_t* residual, uint16_t* y,
                                void* ws, lmoe_stream stream);
 
+/* Largest batch and scratch size of lmoe_layer_forward_noalloc. */
+#define LMOE_NOALLOC_MAX_T 16
+#define LMOE_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* The layer at decode batch sizes without a workspace argument, for callers
+ * that cannot allocate device memory at call time: serving runtimes that
+ * reserve nearly all of the device's memory for their own pools and caches
+ * up front, and code that must not trigger the device-wide synchronisation
+ * that cudaMalloc / cudaFree can cause. This entry point is an addition of
+ * this library; the layer's description has no counterpart.
+ *
+ * It computes exactly what lmoe_layer_forward computes on the decode path
+ * (one pass of at most LMOE_NOALLOC_MAX_T tokens), with its scratch in one
+ * fixed LMOE_NOALLOC_SCRATCH_BYTES array per device that is part of the
+ * library's device image. Nothing is allocated by the call, by CUDA or by
+ * anything else. x, residual (nullable) and y are [T][d] bf16 device
+ * pointers as for lmoe_layer_forward, 16-byte aligned; y may alias residual
+ * but not x.
+ *
+ * The first call on a device looks up that array's address (once per device,
+ * with the handle's device current); make that first call outside any stream
+ * capture. All calls on a device share the one array and it keeps the last
+ * call's contents; no word of it needs to start at zero, because every word a
+ * call reads it has first written. Calls whose work overlaps on the GPU (two
+ * streams, two handles on one device) race on the array and give undefined
+ * results: order them on one stream, or use lmoe_layer_forward with separate
+ * workspaces.
+ *
+ * Returns LMOE_ERR_INVALID_ARG for T < 0 or T > LMOE_NOALLOC_MAX_T (and for
+ * the argument errors of lmoe_layer_forward), LMOE_ERR_UNSUPPORTED when the
+ * layer's shape needs more than LMOE_NOALLOC_SCRATCH_BYTES of scratch at that
+ * T, LMOE_ERR_ALIGNMENT and LMOE_ERR_CUDA as lmoe_layer_forward does. */
+lmoe_status lmoe_layer_forward_noalloc(lmoe_handle* h, const uint16_t* x, int T, const uint16_t* residual,
+                                       uint16_t* y, lmoe_stream stream);
+
 /* The whole layer from and to HOST memory: copies x (and residual) from
  * host to the workspace, runs lmoe_layer_forward, copies y back and waits
  * for the stream. x_host, residual_host (nullable) and y_host are host

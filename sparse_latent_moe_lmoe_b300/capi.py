@@ -19,7 +19,8 @@ PATH_AUTO, PATH_DECODE, PATH_PREFILL = 0, 1, 2
 FLAG_MULTI_KERNEL_DECODE = 1
 
 EXPORTS = ("lmoe_status_string", "lmoe_version", "lmoe_create", "lmoe_destroy", "lmoe_workspace_size", "lmoe_route",
-           "lmoe_permute", "lmoe_expert_forward", "lmoe_combine", "lmoe_layer_forward", "lmoe_layer_forward_host",
+           "lmoe_permute", "lmoe_expert_forward", "lmoe_combine", "lmoe_layer_forward", "lmoe_layer_forward_noalloc",
+           "lmoe_layer_forward_host",
            "lmoe_host_staging_size", "lmoe_check", "lmoe_set_timeout", "lmoe_set_stage_events", "lmoe_stage_name")
 
 
@@ -71,6 +72,7 @@ def _load():
         "lmoe_expert_forward": ([P, P, I, P, P, ctypes.POINTER(LmoePerm), P, P, P], S),
         "lmoe_combine": ([P, P, P, ctypes.POINTER(LmoePerm), I, P, P, P], S),
         "lmoe_layer_forward": ([P, P, I, P, P, P, P], S),
+        "lmoe_layer_forward_noalloc": ([P, P, I, P, P, P], S),
         "lmoe_layer_forward_host": ([P, P, I, P, P, P, P], S),
         "lmoe_check": ([P, P], S),
         "lmoe_set_timeout": ([P, ctypes.c_longlong], S),
@@ -146,6 +148,14 @@ def lmoe_combine(h, Y, idx, perm: LmoePerm, T, residual, y, stream) -> None:
 
 def lmoe_layer_forward(h, x, T, residual, y, ws, stream) -> None:
     _ok(_lib.lmoe_layer_forward(h, x, int(T), residual, y, ws, stream), "lmoe_layer_forward")
+
+
+def lmoe_layer_forward_noalloc(h, x, T, residual, y, stream) -> None:
+    _ok(_lib.lmoe_layer_forward_noalloc(h, x, int(T), residual, y, stream), "lmoe_layer_forward_noalloc")
+
+
+NOALLOC_MAX_T = 16
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 def lmoe_layer_forward_host(h, x_host, T, residual_host, y_host, ws, stream) -> None:

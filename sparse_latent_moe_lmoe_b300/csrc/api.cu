@@ -5,6 +5,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -302,6 +303,32 @@ PrefillArgs prefill_args(const lmoe_handle* h) {
   return P;
 }
 
+// Scratch of lmoe_layer_forward_noalloc, looked up once per device.
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+}  // namespace
+
+// One fixed scratch array per device, in this library's device image: the
+// workspace of lmoe_layer_forward_noalloc, which therefore allocates nothing.
+static __device__ __align__(256) unsigned char lmoe_noalloc_scratch[LMOE_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+// Device address of the scratch array on `device`, which must be current.
+lmoe_status noalloc_scratch(int device, void** out) {
+  if (device < 0 || device >= kNoAllocMaxDevices) return LMOE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[device]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, lmoe_noalloc_scratch) != cudaSuccess || !p) return LMOE_ERR_CUDA;
+    g_noalloc_ptr[device] = p;
+  }
+  *out = g_noalloc_ptr[device];
+  return LMOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -519,6 +546,22 @@ lmoe_status lmoe_layer_forward(lmoe_handle* h, const uint16_t* x, int T, const u
     return cuda_status(launch_prefill_layer(P, x, T, residual, y, ws, st, h->events.empty() ? nullptr : &h->events));
   }
   return decode_layer(h, x, T, residual, y, ws, st);
+}
+
+lmoe_status lmoe_layer_forward_noalloc(lmoe_handle* h, const uint16_t* x, int T, const uint16_t* residual,
+                                       uint16_t* y, lmoe_stream stream) {
+  if (check_handle(h) != LMOE_OK || T < 0 || T > LMOE_NOALLOC_MAX_T) return LMOE_ERR_INVALID_ARG;
+  if (T == 0) return LMOE_OK;
+  if (!x || !y || x == y) return LMOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || (residual && !aligned16(residual))) return LMOE_ERR_ALIGNMENT;
+  if (decode_ws(h->cfg, T).end > (size_t)LMOE_NOALLOC_SCRATCH_BYTES) return LMOE_ERR_UNSUPPORTED;
+  lmoe_status s = pending_error();
+  if (s != LMOE_OK) return s;
+  DeviceGuard guard(h->device);
+  void* ws = nullptr;
+  s = noalloc_scratch(h->device, &ws);
+  if (s != LMOE_OK) return s;
+  return decode_layer(h, x, T, residual, y, ws, (cudaStream_t)stream);
 }
 
 lmoe_status lmoe_layer_forward_host(lmoe_handle* h, const uint16_t* x_host, int T, const uint16_t* residual_host,

@@ -128,6 +128,15 @@ class LatentMoE:
                                 _stream(stream))
         return y
 
+    def forward_noalloc(self, x: torch.Tensor, residual=None, out=None, stream=None) -> torch.Tensor:
+        """The layer for T <= 16 tokens with the library's fixed per-device
+        scratch instead of a workspace (lmoe_layer_forward_noalloc): the C call
+        allocates nothing. `out` must be given by a caller that cannot allocate."""
+        T = x.shape[0]
+        y = out if out is not None else torch.empty((T, self.shape.d), dtype=torch.bfloat16, device=self.device)
+        capi.lmoe_layer_forward_noalloc(self.h, _ptr(x), T, _ptr(residual), _ptr(y), _stream(stream))
+        return y
+
     def forward_host(self, x_host: torch.Tensor, y_host: torch.Tensor, residual_host=None, stream=None):
         """Host (ideally pinned) bf16 tensors in and out; waits for the result."""
         T = x_host.shape[0]

@@ -32,6 +32,7 @@ def test_host_side_validation_without_gpu():
     assert lib.lmoe_workspace_size(None, 8) == 0
     assert lib.lmoe_route(None, None, 8, None, None, None, None, None) == 1
     assert lib.lmoe_layer_forward(None, None, 8, None, None, None, None) == 1
+    assert lib.lmoe_layer_forward_noalloc(None, None, 8, None, None, None) == 1
     assert lib.lmoe_set_timeout(None, 5) == 1
     assert lib.lmoe_check(None, None) == 1
     assert lib.lmoe_destroy(None) == 0
