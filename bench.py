@@ -174,24 +174,33 @@ def stage_flops(sh, T, idx):
     return f, rows
 
 
-def read_traffic(kernel: str):
-    """dram bytes per launch of a kernel from a committed ncu summary, if the
-    summary matches the current kernel source; else None."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+def source_sha(files) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of a kernel on a workload, from the committed ncu
+    summary table profiles/traffic.txt, if the sources the counters were taken
+    on are unchanged; else None. Table rows: kernel, workload, bytes per
+    launch, comma-separated source files, sha256 prefix of those sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
         return None
-    try:
-        d = json.load(open(p))
-        ent = d.get(kernel)
-        if not ent:
+    for line in open(p):
+        f = line.split("#", 1)[0].split()
+        if len(f) != 5 or f[0] != kernel or f[1] != workload:
+            continue
+        try:
+            if source_sha(f[3].split(",")) != f[4]:
+                return None
+            return float(f[2])
+        except OSError:
             return None
-        import hashlib
-        src = open(os.path.join(ROOT, ent["source"]), "rb").read()
-        if hashlib.sha256(src).hexdigest()[:16] != ent["source_sha"]:
-            return None
-        return ent["dram_bytes_per_launch"]
-    except Exception:
-        return None
+    return None
 
 
 # ------------------------------------------------------------------ oracle
@@ -358,7 +367,7 @@ def run_ours(args):
         achieved = sf.get(dom, 0.0) / (per[dom] * 1e-3) / 1e12
         total = sum(sf.values())
         roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": bf16s, "unit": "TFLOP/s",
-                    "frac": achieved / bf16s, "traffic": read_traffic(dom), "peak_source": peak_src + " sustained",
+                    "frac": achieved / bf16s, "traffic": read_traffic(dom, args.workload), "peak_source": peak_src + " sustained",
                     "flops_per_launch": sf.get(dom, 0.0), "timing": stage_timing,
                     "step": {"flops": total, "achieved": total / (ms / args.steps * 1e-3) / 1e12,
                              "frac": total / (ms / args.steps * 1e-3) / 1e12 / bf16s,
@@ -368,7 +377,7 @@ def run_ours(args):
         achieved = sb.get(dom, 0.0) / (per[dom] * 1e-3) / 1e9
         total_bytes = sum(v for n, v in sb.items() if n != "decode_fused")
         roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                    "frac": achieved / hbm, "traffic": read_traffic(dom), "peak_source": peak_src,
+                    "frac": achieved / hbm, "traffic": read_traffic(dom, args.workload), "peak_source": peak_src,
                     "bytes_per_launch": sb.get(dom, 0.0), "timing": stage_timing,
                     "step": {"bytes": total_bytes, "achieved": total_bytes / (ms / args.steps * 1e-3) / 1e9,
                              "frac": total_bytes / (ms / args.steps * 1e-3) / 1e9 / hbm}}
