@@ -187,7 +187,7 @@ lmoe_status lmoe_layer_forward(lmoe_handle* h, const uint16_t* x, int T, const u
 
 /* Largest batch and scratch size of lmoe_layer_forward_noalloc. */
 #define LMOE_NOALLOC_MAX_T 16
-#define LMOE_NOALLOC_SCRATCH_BYTES (16u << 20)
+#define LMOE_NOALLOC_SCRATCH_BYTES (32u << 20)
 
 /* The layer at decode batch sizes without a workspace argument, for callers
  * that cannot allocate device memory at call time: serving runtimes that

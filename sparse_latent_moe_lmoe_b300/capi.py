@@ -155,7 +155,7 @@ def lmoe_layer_forward_noalloc(h, x, T, residual, y, stream) -> None:
 
 
 NOALLOC_MAX_T = 16
-NOALLOC_SCRATCH_BYTES = 16 << 20
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 def lmoe_layer_forward_host(h, x_host, T, residual_host, y_host, ws, stream) -> None:

@@ -25,6 +25,10 @@ struct lmoe_handle {
   uint16_t* d_wr_split;  // [3][E][d] bf16 split of W_r (hi, mid, lo) for the tensor-core router
   long long timeout;
   int fused_grid;  // CTAs of the single-kernel decode pass (0: unavailable)
+  DecodeMaps maps;                   // TMA descriptors of the weights (single-kernel decode)
+  bool maps_ok;
+  unsigned* d_ctr;                   // its arrival counters (two copies)
+  unsigned long long* d_launches;    // its launch counter
   std::vector<cudaEvent_t> events;
 };
 
@@ -84,26 +88,19 @@ int ks_in_for(const lmoe_config& c) {
   return a > b ? a : b;
 }
 
-// ticket layout in the handle: [0] route, [1 .. 1+d/64) multi-kernel wout,
-// then the fused kernel's barrier and tickets
+// ticket layout in the handle: [0] route, [1 .. 1+d/64) multi-kernel wout
 struct TicketMap {
-  size_t bar, tk_router, tk_win, tk_wout, total;
+  size_t total;
 };
 TicketMap ticket_map(const lmoe_config& c) {
   TicketMap t;
-  size_t o = 1 + (size_t)(c.d + 63) / 64 + 64;
-  o = (o + 1) & ~(size_t)1;  // 8-byte aligned 64-bit counter
-  t.bar = o; o += 2;
-  t.tk_router = o; o += (size_t)(c.E + 1) / 2;
-  t.tk_win = o; o += (size_t)c.G * (c.L / 16);
-  t.tk_wout = o; o += (size_t)c.d / 16;
-  t.total = o + 64;
+  t.total = 1 + (size_t)(c.d + 63) / 64 + 64;
   return t;
 }
 
 // ----------------------------------------------------------- workspace map
 struct DecodeWs {
-  size_t logits, idx, w, eo, sa, inv, go, gto, gt, ar, Hp, V, Z, Yp, Pin, Qout, Lp, H, perm_scratch, end;
+  size_t logits, idx, w, eo, sa, inv, go, gto, gt, ar, Hp, V, Z, Yp, Pin, Qout, Lp, H, Zp, Hf, Vf, Zf, perm_scratch, end;
 };
 
 DecodeWs decode_ws(const lmoe_config& c, int T) {
@@ -126,7 +123,8 @@ DecodeWs decode_ws(const lmoe_config& c, int T) {
   m.gto = take((size_t)(c.G + 1) * 4);
   m.gt = take((size_t)n * gk * 4);
   m.ar = take((size_t)n * c.k * 4);
-  m.Hp = take((size_t)ks_in_for(c) * c.G * n * c.L * 4);
+  const int ks = ks_in_for(c) > c.d / 1024 ? ks_in_for(c) : c.d / 1024;
+  m.Hp = take((size_t)ks * c.G * n * c.L * 4);
   m.V = take((size_t)256 * n * c.f * 4);  // [routed-expert slot <= 256][16][f]
   m.Z = take((size_t)c.G * n * c.L * 4);
   m.Yp = take((size_t)c.G * n * c.d * 4);
@@ -134,6 +132,10 @@ DecodeWs decode_ws(const lmoe_config& c, int T) {
   m.Qout = take((size_t)c.G * n * (c.lora_rank > 0 ? c.lora_rank : 1) * 4);
   m.Lp = take((size_t)(c.d / 128 + 1) * n * c.E * 4);
   m.H = take((size_t)c.G * n * c.L * 4);
+  m.Zp = take((size_t)256 * n * c.L * 4);  // [routed-expert slot <= 256][16][L]
+  m.Hf = take((size_t)c.G * c.L * 32);     // fp16 fragments, two token tiles: L/128 x 256 x 16 B
+  m.Vf = take((size_t)256 * c.f * 32);
+  m.Zf = take((size_t)c.G * c.L * 32);
   m.perm_scratch = take(permute_scratch_bytes(T > n ? T : n, c.E, c.G));
   m.end = o;
   return m;
@@ -228,23 +230,28 @@ struct DeviceGuard {
 };
 
 bool use_fused(const lmoe_handle* h, const DecodeArgs& A) {
-  return !(h->cfg.flags & LMOE_FLAG_MULTI_KERNEL_DECODE) && h->fused_grid > 0 && fused_decode_supported(A);
+  return !(h->cfg.flags & LMOE_FLAG_MULTI_KERNEL_DECODE) && h->fused_grid > 0 && h->maps_ok &&
+         fused_decode_supported(A);
 }
+
+bool use_fused(const lmoe_handle* h, const DecodeArgs& A);
 
 FusedArgs fused_args(const lmoe_handle* h, const DecodeArgs& A, void* ws) {
   FusedArgs F;
   memset(&F, 0, sizeof(F));
   F.A = A;
+  F.maps = h->maps;
   const DecodeWs m = decode_ws(h->cfg, 0);
   char* b = reinterpret_cast<char*>(ws);
   F.Lp = reinterpret_cast<float*>(b + m.Lp);
   F.logits = reinterpret_cast<float*>(b + m.logits);
   F.H = reinterpret_cast<float*>(b + m.H);
-  const TicketMap tm = ticket_map(h->cfg);
-  F.bar = reinterpret_cast<unsigned long long*>(h->d_tickets + tm.bar);
-  F.tk_router = h->d_tickets + tm.tk_router;
-  F.tk_win = h->d_tickets + tm.tk_win;
-  F.tk_wout = h->d_tickets + tm.tk_wout;
+  F.Zp = reinterpret_cast<float*>(b + m.Zp);
+  F.Hf = reinterpret_cast<uint4*>(b + m.Hf);
+  F.Vf = reinterpret_cast<uint4*>(b + m.Vf);
+  F.Zf = reinterpret_cast<uint4*>(b + m.Zf);
+  F.ctr = h->d_ctr;
+  F.launches = h->d_launches;
   F.timeout = h->timeout;
   return F;
 }
@@ -392,6 +399,20 @@ lmoe_status lmoe_create(lmoe_handle** out, const lmoe_config* cfg, const lmoe_we
     return LMOE_ERR_CUDA;
   }
   h->fused_grid = fused_grid(h->num_sms);
+  {
+    const size_t nc = fused_counter_words(cfg->d, cfg->E, cfg->G, cfg->L);
+    if (cudaMalloc(&h->d_ctr, nc * sizeof(unsigned)) != cudaSuccess ||
+        cudaMalloc(&h->d_launches, sizeof(unsigned long long)) != cudaSuccess) {
+      cudaGetLastError();
+      lmoe_destroy(h);
+      return LMOE_ERR_NO_MEMORY;
+    }
+    cudaMemset(h->d_ctr, 0, nc * sizeof(unsigned));
+    cudaMemset(h->d_launches, 0, sizeof(unsigned long long));
+    DecodeArgs probe = base_args(h, nullptr);
+    probe.T = 1;
+    h->maps_ok = fused_decode_supported(probe) && fused_make_maps(probe, &h->maps);
+  }
   if (launch_split_router(h->w.W_r, cfg->E, cfg->d, h->d_wr_split, 0) != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess) {
     lmoe_destroy(h);
@@ -408,6 +429,8 @@ lmoe_status lmoe_destroy(lmoe_handle* h) {
   if (h->d_err) cudaFree(h->d_err);
   if (h->d_tickets) cudaFree(h->d_tickets);
   if (h->d_wr_split) cudaFree(h->d_wr_split);
+  if (h->d_ctr) cudaFree(h->d_ctr);
+  if (h->d_launches) cudaFree(h->d_launches);
   delete h;
   return pending_error();
 }

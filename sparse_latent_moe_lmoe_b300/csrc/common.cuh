@@ -193,4 +193,31 @@ LMOE_DEV void set_error(unsigned* err, unsigned bits) {
   if (err) atomicOr(err, bits);
 }
 
+// ------------------------------------------------------------- mbarriers
+LMOE_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+LMOE_DEV void mbar_init(uint64_t* m, uint32_t cnt) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(m)), "r"(cnt));
+}
+LMOE_DEV void mbar_arrive(uint64_t* m) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(smem_u32(m)) : "memory");
+}
+// bounded wait for the phase with the given parity to complete
+LMOE_DEV void mbar_wait(uint64_t* m, uint32_t parity, long long budget, unsigned* err) {
+  const long long t0 = clock64();
+  while (true) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_u32(m)), "r"(parity)
+        : "memory");
+    if (ok) return;
+    if (clock64() - t0 > budget) {
+      set_error(err, ERRBIT_TIMEOUT);
+      return;
+    }
+  }
+}
+
 }  // namespace lmoe

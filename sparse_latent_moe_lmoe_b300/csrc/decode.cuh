@@ -1,5 +1,6 @@
 // Argument block and launchers of the decode-path kernels (<= 16 tokens).
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -60,23 +61,40 @@ struct DecodeArgs {
   float* Yrows;
 };
 
+// TMA descriptors of the weights for the single-kernel decode pass (made
+// once per handle). Packed int4 matrices are viewed as [rows][K/256][128 B]
+// (128-byte swizzle), their scales as [rows][K/32] bf16, W_r as
+// [E][d/256][256] fp32.
+struct DecodeMaps {
+  CUtensorMap wr;
+  CUtensorMap win_q, win_s;
+  CUtensorMap gate_q, gate_s, up_q, up_s;
+  CUtensorMap down_q, down_s;
+  CUtensorMap wout_q, wout_s;
+};
+
 // The single-kernel decode pass (decode_fused.cu).
 struct FusedArgs {
   DecodeArgs A;
-  float* Lp;            // [d / router_slice][16][E] router partial sums
-  float* logits;        // [16][E]
-  float* H;             // [G][16][L] shared down-projection outputs
-  unsigned long long* bar;  // grid barrier arrival counter (monotonic)
-  unsigned* tk_router;  // [E/2]
-  unsigned* tk_win;     // [G * L/16]
-  unsigned* tk_wout;    // [d/16]
-  long long timeout;    // spin budget (clock64 cycles)
-  int router_slice;
+  DecodeMaps maps;
+  float* Lp;                     // [d/1024][16][E] router partial sums
+  float* logits;                 // [16][E]
+  float* H;                      // [G][16][L] shared down-projection outputs
+  float* Zp;                     // [256][16][L] per-expert down-projection partials
+  uint4* Hf;                     // [G][L/128][128 NT] H as fp16 fragments (NT = token tiles of the launch)
+  uint4* Vf;                     // [256][f/128][128 NT] weighted SwiGLU outputs as fragments
+  uint4* Zf;                     // [G][L/128][128 NT] Z as fragments
+  unsigned* ctr;                 // arrival counters, two copies (fused_counter_words)
+  unsigned long long* launches;  // launch counter (selects the counter copy)
+  long long timeout;             // spin budget (clock64 cycles)
 };
+size_t fused_counter_words(int d, int E, int G, int L);
+// Encodes the tensor maps; false if the driver refuses one of them.
+bool fused_make_maps(const DecodeArgs& A, DecodeMaps* maps);
 bool fused_decode_supported(const DecodeArgs& A);
 cudaError_t fused_set_attributes();
 int fused_grid(int num_sms);
-cudaError_t launch_decode_fused(FusedArgs F, int grid, cudaStream_t st);
+cudaError_t launch_decode_fused(const FusedArgs& F, int grid, cudaStream_t st);
 
 // Records timing events around each launch when attached.
 struct StageHook {

@@ -1,108 +1,164 @@
-// The decode-path layer as one persistent cooperative kernel (<= 16 tokens,
-// no LoRA branch): one CTA per SM, phases separated by grid barriers.
+// The decode-path layer (<= 16 tokens, no LoRA branch) as one persistent
+// cooperative kernel built around a shared-memory weight ring.
 //
-//   P0  router logits, split along d; a ticket per expert pair sums the
-//       partial sums in fixed order (deterministic)
-//   P1  every CTA: top-k with softmax renormalisation for all tokens and the
-//       routed-expert / routed-group tables (no serial single-CTA tail)
-//   P2  H[g][t] = Win[g] x_t, split along d, reduced by a ticket per tile
-//   P3  V[e][t] = silu(Gate_e h) * Up_e h for each routed (expert, token)
-//   P4  Z[g][t] = sum_{e in g} w Down_e V: one CTA per (group, 64 rows),
-//       all of the group's experts accumulated in registers
-//   P5  Y[g][t] = Wout[g] Z[g][t]; the last group to finish a 16-row tile
-//       sums the routed groups in ascending order (+ residual) into y
+// Per CTA (one per SM, 16 warps): warp 15 is the producer. Its lane 0 walks
+// the CTA's list of weight chunks for the whole layer and loads each into the
+// next ring slot with TMA tensor copies (one box of up to 8 KB of packed int4
+// in 128-byte swizzle plus one box of bf16 scales, or 8 KB of fp32 router
+// rows), as far ahead as the ring allows. Warps 0..14 consume the chunks with
+// tensor-core MMAs (int4 dequantised in registers, fp16 operands, fp32
+// accumulation) against activation fragments staged in shared memory.
 //
-// Weights stream through a register prefetch ring (PFD chunks of 16 rows x
-// 128 reduction elements in flight per warp).
+// Work, in ring order (KS = d/1024 reduction segments):
+//   A1  router logits: (segment, expert pair) items, partial sums reduced in
+//       segment order by the last arriver of each pair
+//   --  every CTA computes the routing itself (top-k, softmax, tables)
+//   A2  H[g] = W_in[g] x for every group: (segment, group, 16-row tile)
+//       items, reduced in segment order by the last arriver of each tile
+//   B   V[e] = silu(Gate_e h) * Up_e h for each routed expert: (expert,
+//       16-row tile) items, gate and up chunks back to back
+//   C   Z[g] = sum_{e in g} Down_e (w V_e): (expert, 32-row block) items with
+//       per-expert partials, summed in ascending expert order by the last
+//       arriver of each (group, block)
+//   D   Y[g] = W_out[g] Z[g]: (group, 16-row tile) items; the last group to
+//       finish a tile sums the groups in ascending order (+ residual) into y
+// Dependencies between CTAs are arrival counters (per group for H and Z, per
+// expert for V, one for the logits) instead of grid barriers: a CTA waits
+// only for the data it stages next, and the producer keeps streaming the next
+// phase's weights meanwhile. The counters come in two copies used by
+// alternate launches; each launch clears the copy the next one uses, so a
+// launch that ran out of its wait budget leaves the next one correct.
 //
-// Every spin is bounded by the handle's cycle budget; running out sets the
-// timeout bit of the device error word and the kernel carries on (the output
-// is then invalid and lmoe_check reports LMOE_ERR_TIMEOUT).
+// Every wait is bounded by the handle's cycle budget; running out sets the
+// timeout bit of the device error word and the kernel carries on to the end
+// (the output is then invalid and lmoe_check reports LMOE_ERR_TIMEOUT).
 #include "common.cuh"
 #include "decode.cuh"
+#include "ring.cuh"
 
 namespace lmoe {
 
-constexpr int FW = 16;             // warps per CTA
-constexpr int FT = FW * 32;        // threads per CTA
-constexpr int SLOT_BYTES = 32768;  // one staged activation set
-constexpr int NSLOT = 3;           // activation sets staged at once
-constexpr int RED_BYTES = 3 * 4 * 16 * 16 * 4;
-constexpr int DYN_SMEM = NSLOT * SLOT_BYTES;
-constexpr int MAX_ACT = 256;       // routed experts per pass: <= 16 tokens * 16
-constexpr int PFD = 6;             // register prefetch depth (chunks)
+// cold, once-per-phase code is kept out of line: the kernel's instruction
+// footprint, not its arithmetic, bounds how fast every SM gets through it
+#define LMOE_COLD __device__ __noinline__
 
-// Grid barrier on a monotonically increasing 64-bit arrival counter: the
-// k-th barrier of a launch completes when the counter reaches the next
-// multiple of the grid size. Nothing is ever reset, so a launch leaves the
-// counter at a multiple of the grid size even when a wait ran out of budget
-// (every CTA still arrives exactly once per barrier).
-LMOE_DEV void grid_sync(unsigned long long* bar, long long budget, unsigned* err) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned long long n = gridDim.x;
-    const unsigned long long arrived = atomicAdd(bar, 1ull);
-    const unsigned long long target = (arrived / n + 1) * n;
-    volatile unsigned long long* vb = bar;
-    const long long t0 = clock64();
-    while (*vb < target) {
-      if (clock64() - t0 > budget) {
-        set_error(err, ERRBIT_TIMEOUT);
-        break;
-      }
-      __nanosleep(32);
-    }
-    __threadfence();
-  }
-  __syncthreads();
+namespace {
+
+constexpr int NWARP = 16, NTHR = NWARP * 32, NCW = NWARP - 1, PROD = NWARP - 1, NCT = NCW * 32;
+constexpr int SLOT_BYTES = 10240;  // 8 KB of weights + 1 KB of scales, 1024-byte aligned
+constexpr int KEYS = 3;            // activation sets staged at once
+constexpr int KSEG = 1024;         // reduction segment of the router and W_in
+constexpr int DR = 32;             // rows of a down chunk
+constexpr int MAX_ACT = 256;       // routed experts per pass (16 tokens x k <= 16)
+
+template <int NT>
+__host__ __device__ constexpr int nslot() {
+  return NT == 1 ? 16 : 12;
 }
-
-// The last of `n` arrivals on a ticket returns true (and resets it). Called
-// by one lane after its writes; the caller fences before.
-LMOE_DEV bool ticket_last(unsigned* t, unsigned n) {
-  const unsigned old = atomicAdd(t, 1u);
-  if (old == n - 1) {
-    *t = 0;
-    __threadfence();
-    return true;
-  }
-  return false;
+template <int NT>
+__host__ __device__ constexpr int key_bytes() {
+  return 16384 * NT;
+}
+template <int NT>
+__host__ __device__ constexpr int dyn_smem() {
+  return 1024 + nslot<NT>() * SLOT_BYTES + KEYS * key_bytes<NT>();
 }
 
 struct Tables {
   int32_t idx[16 * 16];
   float w[16 * 16];
-  unsigned emask[1024];   // routed tokens per expert
-  int16_t elist[MAX_ACT]; // routed experts, ascending
-  int16_t glist[64];      // routed groups, ascending
-  int16_t gslot0[65];     // first expert slot of each routed group
-  int n_act, n_actg;
-  // per-phase item ranges of this CTA
-  int nq, per_q, lo2, hi2, lo3, hi3, N4, nblk, lo5, hi5;
-  int slot_key[NSLOT];
+  uint16_t emask[512];       // routed tokens per expert
+  int16_t elist[MAX_ACT];    // routed experts, ascending
+  int16_t glist[64];         // routed groups, ascending
+  int16_t gslot0[65];        // first expert slot of each routed group
+  int n_act, n_actg, par;
+  volatile int tables_ready;
+  int key[KEYS];
+  uint64_t full[16], empty[16];
+  volatile int seq[16];
 };
 
+LMOE_DEV unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+LMOE_COLD void wait_count(const unsigned* p, unsigned target, long long budget, unsigned* err) {
+  const long long t0 = clock64();
+  #pragma unroll 1
+  while (ld_acquire(p) < target) {
+    if (clock64() - t0 > budget) {
+      set_error(err, ERRBIT_TIMEOUT);
+      return;
+    }
+    __nanosleep(32);
+  }
+}
+
+// consumer warps only (the producer never joins)
+LMOE_DEV void cons_sync() { asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory"); }
+
+// The last of n arrivals on a ticket returns true; called by one lane after a
+// __threadfence that publishes the caller's partial results.
+LMOE_DEV bool ticket_last(unsigned* t, unsigned n) { return atomicAdd(t, 1u) == n - 1; }
+
 LMOE_DEV float route_weight(const Tables& tb, int t, int e, int k) {
+  #pragma unroll 1
   for (int j = 0; j < k; ++j)
     if (tb.idx[t * 16 + j] == e) return tb.w[t * 16 + j];
   return 0.f;
 }
 
-// fp32 activations [T][K] (row stride K) -> frags for all chunks of K
+// Counter layout (one copy; two copies alternate between launches).
+struct CtrMap {
+  int tk_router, done_router, done_topk, tk_win, done_in, done_gu, tk_down, done_down, tk_wout, n;
+};
+__host__ __device__ inline CtrMap ctr_map(int d, int E, int G, int L) {
+  CtrMap m;
+  int o = 0;
+  m.tk_router = o; o += E / 2;
+  m.done_router = o; o += 1;
+  m.done_topk = o; o += 1;
+  m.tk_win = o; o += G * (L / 16);
+  m.done_in = o; o += G;
+  m.done_gu = o; o += MAX_ACT;
+  m.tk_down = o; o += G * (L / DR);
+  m.done_down = o; o += G;
+  m.tk_wout = o; o += d / 16;
+  m.n = (o + 31) & ~31;
+  return m;
+}
+
+// index range of CTA c of nC over n items
+LMOE_DEV void split(int n, int c, int nC, int& lo, int& hi) {
+  lo = (int)((long long)c * n / nC);
+  hi = (int)((long long)(c + 1) * n / nC);
+}
+
+// ------------------------------------------------------------ staging
+// Fragment layout of an activation set over K elements: frag_index(chunk c of
+// 128, token tile nt, m pair mp, lane) -> 8 consecutive elements of token
+// 8*nt + lane/4 starting at 128 c + 32 (lane % 4) + 8 mp, as fp16 pairs
+// (e0,e4) (e1,e5) (e2,e6) (e3,e7).
 template <int NT>
-LMOE_DEV void stage_f32(uint4* fr, const float* src, int T, int K) {
-  const int nslots = (K / 128) * NT * 128;
-  for (int si = threadIdx.x; si < nslots; si += FT) {
+LMOE_COLD void stage_x(uint4* fr, const uint16_t* x, int T, int d, int ks, int ctid) {
+  const int n = (KSEG / 128) * NT * 128;
+  #pragma unroll 1
+  for (int si = ctid; si < n; si += NCT) {
     const int ln = si & 31, mp = (si >> 5) & 3, rest = si >> 7;
     const int nt = rest % NT, cc = rest / NT;
-    const int n = nt * 8 + (ln >> 2), tg = ln & 3;
-    const int k0 = cc * 128 + tg * 32 + mp * 8;
+    const int tok = nt * 8 + (ln >> 2), tg = ln & 3;
+    const int k0 = ks * KSEG + cc * 128 + tg * 32 + mp * 8;
     float e[8];
-    if (n < T) {
-      const float4 a = __ldcg(reinterpret_cast<const float4*>(src + (size_t)n * K + k0));
-      const float4 b = __ldcg(reinterpret_cast<const float4*>(src + (size_t)n * K + k0 + 4));
-      e[0] = a.x; e[1] = a.y; e[2] = a.z; e[3] = a.w; e[4] = b.x; e[5] = b.y; e[6] = b.z; e[7] = b.w;
+    if (tok < T) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * d + k0));
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        e[2 * h] = __uint_as_float(u[h] << 16);
+        e[2 * h + 1] = __uint_as_float(u[h] & 0xffff0000u);
+      }
     } else {
 #pragma unroll
       for (int h = 0; h < 8; ++h) e[h] = 0.f;
@@ -111,232 +167,196 @@ LMOE_DEV void stage_f32(uint4* fr, const float* src, int T, int K) {
   }
 }
 
-// Stage the distinct keys (nondecreasing over items [lo, hi)) into the
-// activation slots, at most NSLOT of them; tb.slot_key[s] = key or -1.
-template <class KeyF, class StageF>
-LMOE_DEV void stage_keys(Tables& tb, int lo, int hi, KeyF key, StageF stage, unsigned* err) {
+// Index of the fragment entry holding elements k0 .. k0+7 (k0 a multiple of
+// 8) of token n, in the layout above.
+template <int NT>
+LMOE_DEV int entry_index(int k0, int n) {
+  return frag_index(k0 >> 7, n >> 3, (k0 & 31) >> 3, (n & 7) * 4 + ((k0 & 127) >> 5), NT);
+}
+
+// n fragment entries from global memory into shared memory (consumer threads)
+LMOE_COLD void copy_frags(uint4* dst, const uint4* src, int n, int ctid) {
+  #pragma unroll 1
+  for (int i = ctid; i < n; i += 4 * NCT) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = (i + u * NCT < n) ? __ldcg(src + i + u * NCT) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i + u * NCT < n) dst[i + u * NCT] = v[u];
+  }
+}
+
+// Distinct keys of items [lo, hi) (nondecreasing) into the key table; returns
+// false (and flags bad data) if more than KEYS are needed. Consumer thread 0.
+template <class KeyF>
+LMOE_COLD void collect_keys(Tables& tb, int lo, int hi, KeyF key, unsigned* err) {
   int n = 0, last = -1;
+  #pragma unroll 1
   for (int i = lo; i < hi; ++i) {
     const int kk = key(i);
     if (kk != last) {
-      if (n == NSLOT) {
-        if (threadIdx.x == 0) set_error(err, ERRBIT_BAD_DATA);
+      if (n == KEYS) {
+        set_error(err, ERRBIT_BAD_DATA);
         break;
       }
-      stage(n, kk);
-      if (threadIdx.x == 0) tb.slot_key[n] = kk;
-      ++n;
+      tb.key[n++] = kk;
       last = kk;
     }
   }
-  if (threadIdx.x == 0)
-    for (int s = n; s < NSLOT; ++s) tb.slot_key[s] = -1;
-  __syncthreads();
+  #pragma unroll 1
+  for (int s = n; s < KEYS; ++s) tb.key[s] = -1;
 }
 
-LMOE_DEV int slot_of(const Tables& tb, int kk) {
-  for (int s = 0; s < NSLOT; ++s)
-    if (tb.slot_key[s] == kk) return s;
+LMOE_DEV int key_slot(const Tables& tb, int kk) {
+  #pragma unroll 1
+  for (int s = 0; s < KEYS; ++s)
+    if (tb.key[s] == kk) return s;
   return 0;
 }
 
-template <int NT>
-__global__ void __launch_bounds__(FT, 1) decode_fused_kernel(FusedArgs F) {
-  extern __shared__ __align__(128) unsigned char dsm[];
-  __shared__ Tables tb;
-  const DecodeArgs& A = F.A;
-  const int T = A.T, d = A.d, E = A.E, G = A.G, k = A.k, L = A.L, f = A.f, epg = A.epg;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
-  const int nC = gridDim.x, c = blockIdx.x;
-  uint4* slot_base = reinterpret_cast<uint4*>(dsm);
-  auto slot = [&](int s) { return slot_base + s * (SLOT_BYTES / 16); };
+// ------------------------------------------------------------ ring access
+template <int NS>
+LMOE_DEV const unsigned char* cons_wait(Tables& tb, unsigned char* ring, int j, long long budget, unsigned* err) {
+  const int s = j % NS, u = j / NS;
+  const long long t0 = clock64();
+  #pragma unroll 1
+  while (tb.seq[s] != j) {
+    if (clock64() - t0 > budget) {
+      set_error(err, ERRBIT_TIMEOUT);
+      break;
+    }
+    __nanosleep(20);
+  }
+  mbar_wait(&tb.full[s], u & 1, budget, err);
+  return ring + s * SLOT_BYTES;
+}
 
-  // item -> weights of each phase
-  auto win_item = [&](int i, const uint8_t*& q, const uint16_t*& sc, int& r0, int& c0, int& c1, int& g, int& q_) {
-    const int ntile = L / 16, nch = d / 128;
-    q_ = i / tb.per_q;
-    const int rem = i % tb.per_q, gi = rem / ntile, rt = rem % ntile;
-    g = tb.glist[gi];
-    q = A.W_in_q + (size_t)g * L * (d / 2);
-    sc = A.W_in_s + (size_t)g * L * (d / 32);
-    r0 = rt * 16;
-    c0 = q_ * nch / tb.nq;
-    c1 = (q_ + 1) * nch / tb.nq;
-  };
-  // ---------------------------------------------------------------- P0 router
-  {
-    // The W_in and W_out tickets count arrivals that depend on the routing;
-    // clearing them here (they are first used after the next barrier) keeps a
-    // launch correct even after one whose waits ran out of budget. The
-    // router's tickets always see exactly d/RS arrivals and reset themselves.
-    for (int i = c * FT + threadIdx.x; i < G * (L / 16); i += nC * FT) F.tk_win[i] = 0u;
-    for (int i = c * FT + threadIdx.x; i < d / 16; i += nC * FT) F.tk_wout[i] = 0u;
-    const int RS = F.router_slice, nslice = d / RS, nrp = E / 2;
-    const int N0 = nslice * nrp;
-    const int lo = (int)((long long)c * N0 / nC), hi = (int)((long long)(c + 1) * N0 / nC);
-    stage_keys(
-        tb, lo, hi, [&](int i) { return i / nrp; },
-        [&](int s, int sl) {  // x[:, sl*RS .. +RS] as bf16 [T][RS]
-          uint4* dst = slot(s);
-          const int per = RS / 8;
-          for (int i = threadIdx.x; i < T * per; i += FT) {
-            const int t = i / per, p = i % per;
-            dst[i] = *reinterpret_cast<const uint4*>(A.x + (size_t)t * d + (size_t)sl * RS + p * 8);
-          }
-        },
-        A.err);
-    for (int i = lo + warp; i < hi; i += FW) {
-      const int sl = i / nrp, rp = i % nrp, e0 = 2 * rp;
-      const uint16_t* xs = reinterpret_cast<const uint16_t*>(slot(slot_of(tb, sl)));
-      const float* w0 = A.W_r + (size_t)e0 * d + (size_t)sl * RS;
-      const float* w1 = w0 + d;
-      float4 wa[4], wb[4];  // RS <= 512: all of this lane's weights in flight at once
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int pos = lane * 4 + u * 128;
-        wa[u] = pos < RS ? __ldg(reinterpret_cast<const float4*>(w0 + pos)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        wb[u] = pos < RS ? __ldg(reinterpret_cast<const float4*>(w1 + pos)) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      float acc[2][16];
-#pragma unroll
-      for (int r = 0; r < 2; ++r)
-#pragma unroll
-        for (int t = 0; t < 16; ++t) acc[r][t] = 0.f;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int pos = lane * 4 + u * 128;
-        if (pos >= RS) continue;
-        const float4 a = wa[u], b = wb[u];
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          if (t < T) {
-            const uint2 xb = *reinterpret_cast<const uint2*>(xs + t * RS + pos);
-            const float x0 = __uint_as_float(xb.x << 16), x1 = __uint_as_float(xb.x & 0xffff0000u);
-            const float x2 = __uint_as_float(xb.y << 16), x3 = __uint_as_float(xb.y & 0xffff0000u);
-            acc[0][t] = fmaf(a.w, x3, fmaf(a.z, x2, fmaf(a.y, x1, fmaf(a.x, x0, acc[0][t]))));
-            acc[1][t] = fmaf(b.w, x3, fmaf(b.z, x2, fmaf(b.y, x1, fmaf(b.x, x0, acc[1][t]))));
-          }
-        }
-      }
-#pragma unroll
-      for (int r = 0; r < 2; ++r)
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          float v = acc[r][t];
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-          acc[r][t] = v;
-        }
-      {  // lane (t, r) writes its partial, the last of the slices sums them
-        const int t = lane >> 1, r = lane & 1;
-        float mine = 0.f;
-#pragma unroll
-        for (int tt = 0; tt < 16; ++tt)
-          if (tt == t) mine = acc[r][tt];
-        if (t < T) F.Lp[((size_t)sl * 16 + t) * E + e0 + r] = mine;
-        __threadfence();
-        __syncwarp();
-        bool last = false;
-        if (lane == 0) last = ticket_last(F.tk_router + rp, (unsigned)nslice);
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last && t < T) {
-          float part[16];
-#pragma unroll
-          for (int s2 = 0; s2 < 16; ++s2)
-            part[s2] = s2 < nslice ? __ldcg(F.Lp + ((size_t)s2 * 16 + t) * E + e0 + r) : 0.f;
-          float v = 0.f;
-#pragma unroll
-          for (int s2 = 0; s2 < 16; ++s2) v += part[s2];
-          if (A.b_r) v += A.b_r[e0 + r];
-          F.logits[(size_t)t * E + e0 + r] = v;
-        }
+template <int NS>
+LMOE_DEV void cons_release(Tables& tb, int j) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&tb.empty[j % NS]);
+}
+
+// producer lane 0: claim the slot of chunk j and announce its bytes. The slot
+// is re-armed only once its previous copies have landed and its consumer has
+// released it; if either wait runs out of budget the producer stops (returns
+// null) rather than arm a barrier phase that is still in flight.
+template <int NS>
+LMOE_COLD unsigned char* prod_begin(Tables& tb, unsigned char* ring, int j, uint32_t bytes, long long budget,
+                                   unsigned* err) {
+  const int s = j % NS, u = j / NS;
+  if (u > 0) {
+    const long long t0 = clock64();
+    #pragma unroll 1
+    while (!mbar_test(&tb.full[s], (u - 1) & 1) || !mbar_test(&tb.empty[s], (u - 1) & 1)) {
+      if (clock64() - t0 > budget) {
+        set_error(err, ERRBIT_TIMEOUT);
+        return nullptr;
       }
     }
   }
-  grid_sync(F.bar, F.timeout, A.err);
+  tb.seq[s] = j;
+  mbar_expect_tx(&tb.full[s], bytes);
+  return ring + s * SLOT_BYTES;
+}
 
-  // --------------------------------------------------------------- P1 routing
-  {
-    float* lg = reinterpret_cast<float*>(slot(0));  // [T][E] logits in shared memory
-    for (int i = threadIdx.x; i < T * E / 4; i += FT)
-      reinterpret_cast<float4*>(lg)[i] = __ldcg(reinterpret_cast<const float4*>(F.logits) + i);
-    for (int e = threadIdx.x; e < E; e += FT) tb.emask[e] = 0u;
-    __syncthreads();
-    if (warp < T) {
-      // top-k of token `warp`: lane holds logits lane, lane+32, ... (E <= 512)
-      // in registers and its own best remaining one; each round the warp picks
-      // the best lane head (ties -> lower index) and only the winner rescans
-      const float* row = lg + (size_t)warp * E;
-      float v[16];
+}  // namespace
+
+// ==================================================================== kernel
+// Top-k with softmax renormalisation of one token's logits by one warp: each
+// lane holds logits lane, lane+32, ... (E <= 512) and its best remaining one;
+// every round the warp picks the best lane head (ties -> lower index) and only
+// the winner rescans. Lane j < k returns the j-th expert and its weight.
+LMOE_COLD float2 topk_warp(const float* row, int E, int k) {
+  int sel_e;
+  float sel_w;
+  const int lane = threadIdx.x & 31;
+  float v[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = (lane + 32 * i < E) ? row[lane + 32 * i] : -INFINITY;
-      auto lane_best = [&](float& bv, int& be) {
-        bv = -INFINITY;
-        be = 0x7fffffff;
+  for (int i = 0; i < 16; ++i) v[i] = (lane + 32 * i < E) ? __ldcg(row + lane + 32 * i) : -INFINITY;
+  auto lane_best = [&](float& bv, int& be) {
+    bv = -INFINITY;
+    be = 0x7fffffff;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int e = lane + 32 * i;
-          if (e < E && (v[i] > bv || (v[i] == bv && e < be))) {
-            bv = v[i];
-            be = e;
-          }
-        }
-      };
-      float mv;
-      int me;
+    for (int i = 0; i < 16; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && (v[i] > bv || (v[i] == bv && e < be))) {
+        bv = v[i];
+        be = e;
+      }
+    }
+  };
+  float mv;
+  int me;
+  lane_best(mv, me);
+  float sel = 0.f, l0 = 0.f;
+  sel_e = 0;
+  #pragma unroll 1
+  for (int j = 0; j < k; ++j) {
+    float bv = mv;
+    int be = me;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (ov > bv || (ov == bv && oe < be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if (be >= E) be = 0;
+    if (be == me) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (lane + 32 * i == be) v[i] = -INFINITY;
       lane_best(mv, me);
-      float sel = 0.f, l0 = 0.f;
-      int sel_e = 0;
-      for (int j = 0; j < k; ++j) {
-        float bv = mv;
-        int be = me;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-          if (ov > bv || (ov == bv && oe < be)) {
-            bv = ov;
-            be = oe;
-          }
-        }
-        if (be >= E) be = 0;
-        if (be == me) {  // the winning lane drops that logit and finds its next best
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (lane + 32 * i == be) v[i] = -INFINITY;
-          lane_best(mv, me);
-          if (mv == -INFINITY) me = 0x7fffffff;
-        }
-        if (j == 0) l0 = bv;
-        if (lane == j) {
-          sel = bv;
-          sel_e = be;
-        }
-      }
-      const float ex = (lane < k) ? __expf(sel - l0) : 0.f;
-      float z = ex;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-      if (lane < k) {
-        tb.idx[warp * 16 + lane] = sel_e;
-        tb.w[warp * 16 + lane] = ex / z;
-        if (c == 0) {
-          A.idx[warp * k + lane] = sel_e;
-          A.w[warp * k + lane] = ex / z;
-        }
-      }
+      if (mv == -INFINITY) me = 0x7fffffff;
     }
-    __syncthreads();
-    if (threadIdx.x < T * k) {
-      const int t = threadIdx.x / k, j = threadIdx.x % k;
-      atomicOr(&tb.emask[tb.idx[t * 16 + j]], 1u << t);
+    if (j == 0) l0 = bv;
+    if (lane == j) {
+      sel = bv;
+      sel_e = be;
     }
-    __syncthreads();
-    if (warp == 0) {  // ascending compaction of routed experts
+  }
+  const float ex = (lane < k) ? __expf(sel - l0) : 0.f;
+  float z = ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  sel_w = ex / z;
+  return make_float2(__int_as_float(sel_e), sel_w);
+}
+
+// Routing tables of the pass from the published top-k (one warp).
+LMOE_COLD void build_tables(Tables& tb, const int32_t* gidx, const float* gw, int T, int k, int E, int G, int epg,
+                            unsigned* err) {
+  const int lane = threadIdx.x & 31;
+    #pragma unroll 1
+    for (int i = lane; i < T * k; i += 32) {
+      const int t = i / k, jj = i % k;
+      int e = __ldcg(gidx + i);
+      if (e < 0 || e >= E) {
+        set_error(err, ERRBIT_BAD_INDEX);
+        e = 0;
+      }
+      tb.idx[t * 16 + jj] = e;
+      tb.w[t * 16 + jj] = __ldcg(gw + i);
+    }
+    #pragma unroll 1
+    for (int e = lane; e < E; e += 32) tb.emask[e] = 0;
+    __syncwarp();
+    #pragma unroll 1
+    for (int i = lane; i < T * k; i += 32) {
+      const int t = i / k, e = tb.idx[t * 16 + i % k];
+      atomicOr(reinterpret_cast<unsigned*>(&tb.emask[0]) + (e >> 1), (1u << t) << ((e & 1) * 16));
+    }
+    __syncwarp();
+    {  // ascending compaction of routed experts
       int base = 0;
+      #pragma unroll 1
       for (int e0 = 0; e0 < E; e0 += 32) {
         const int e = e0 + lane;
-        const bool on = e < E && tb.emask[e] != 0u;
+        const bool on = e < E && tb.emask[e] != 0;
         const unsigned bal = __ballot_sync(0xffffffffu, on);
         const int pos = base + __popc(bal & ((1u << lane) - 1u));
         if (on) tb.elist[pos] = (int16_t)e;
@@ -344,13 +364,15 @@ __global__ void __launch_bounds__(FT, 1) decode_fused_kernel(FusedArgs F) {
       }
       if (lane == 0) tb.n_act = base;
     }
-    __syncthreads();
-    if (warp == 1) {  // routed groups: per-group expert counts scanned by one warp
+    __syncwarp();
+    {  // routed groups and their first expert slots
       int cnt0 = 0, cnt1 = 0;  // groups lane and lane + 32
       if (lane < G)
-        for (int e = lane * epg; e < (lane + 1) * epg; ++e) cnt0 += tb.emask[e] != 0u;
+        #pragma unroll 1
+        for (int e = lane * epg; e < (lane + 1) * epg; ++e) cnt0 += tb.emask[e] != 0;
       if (lane + 32 < G)
-        for (int e = (lane + 32) * epg; e < (lane + 33) * epg; ++e) cnt1 += tb.emask[e] != 0u;
+        #pragma unroll 1
+        for (int e = (lane + 32) * epg; e < (lane + 33) * epg; ++e) cnt1 += tb.emask[e] != 0;
       int inc0 = cnt0, inc1 = cnt1;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -374,200 +396,457 @@ __global__ void __launch_bounds__(FT, 1) decode_fused_kernel(FusedArgs F) {
         tb.gslot0[gi] = (int16_t)(tot0 + inc1 - cnt1);
       }
       const int ng = n0 + __popc(b1);
+      __syncwarp();
       if (lane == 0) {
         tb.gslot0[ng] = (int16_t)tb.n_act;
         tb.n_actg = ng;
-        tb.nq = A.ks_in;
-        tb.per_q = ng * (L / 16);
-        const int N2 = tb.nq * tb.per_q, N3 = tb.n_act * (f / 16), N5 = ng * (d / 16);
-        tb.lo2 = (int)((long long)c * N2 / nC); tb.hi2 = (int)((long long)(c + 1) * N2 / nC);
-        tb.lo3 = (int)((long long)c * N3 / nC); tb.hi3 = (int)((long long)(c + 1) * N3 / nC);
-        tb.nblk = L / 64; tb.N4 = ng * tb.nblk;
-        tb.lo5 = (int)((long long)c * N5 / nC); tb.hi5 = (int)((long long)(c + 1) * N5 / nC);
       }
     }
-    __syncthreads();
-  }
+}
 
-  // ------------------------------------------------------------------ P2 W_in
-  {
-    const int nch = d / 128, ntile = L / 16;
-    stage_keys(
-        tb, tb.lo2, tb.hi2, [&](int i) { return i / tb.per_q; },
-        [&](int s, int q) {
-          const int c0 = q * nch / tb.nq, c1 = (q + 1) * nch / tb.nq;
-          const int nslots = (c1 - c0) * NT * 128;
-          uint4* fr = slot(s);
-          for (int si = threadIdx.x; si < nslots; si += FT) {
-            const int ln = si & 31, mp = (si >> 5) & 3, rest = si >> 7;
-            const int nt = rest % NT, cc = rest / NT;
-            const int n = nt * 8 + (ln >> 2), tg = ln & 3;
-            const int k0 = (c0 + cc) * 128 + tg * 32 + mp * 8;
-            float e[8];
-            if (n < T) {
-              const uint4 v = *reinterpret_cast<const uint4*>(A.x + (size_t)n * d + k0);
-              const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-              for (int h = 0; h < 4; ++h) {
-                e[2 * h] = __uint_as_float(u[h] << 16);
-                e[2 * h + 1] = __uint_as_float(u[h] & 0xffff0000u);
-              }
-            } else {
-#pragma unroll
-              for (int h = 0; h < 8; ++h) e[h] = 0.f;
-            }
-            fr[si] = pack_frag8(e);
-          }
-        },
-        A.err);
-    for (int i = tb.lo2 + warp; i < tb.hi2; i += FW) {
-      const uint8_t* q; const uint16_t* sc; int r0, c0, c1, g, qq;
-      win_item(i, q, sc, r0, c0, c1, g, qq);
-      const int rt = r0 / 16, nq = tb.nq;
-      float acc[NT][4] = {};
-      mma_rows<NT, PFD>(q, sc, d, r0, c0, c1, c0, slot(slot_of(tb, qq)), acc);
-      float* Hp = A.Hp + ((size_t)qq * G + g) * 16 * L;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const int row = r0 + gid + ((h & 2) ? 8 : 0), t = nt * 8 + 2 * tig + (h & 1);
-          if (t < T) Hp[(size_t)t * L + row] = acc[nt][h];
-        }
+template <int NT>
+__global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_constant__ FusedArgs F) {
+  constexpr int NS = nslot<NT>();
+  constexpr int FR = 128 * NT;  // fragment entries per 128 elements of an activation set
+  extern __shared__ unsigned char dsm_raw[];
+  __shared__ Tables tb;
+  unsigned char* dsm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~(uintptr_t)1023);
+  unsigned char* ring = dsm;
+  uint4* keyset = reinterpret_cast<uint4*>(dsm + NS * SLOT_BYTES);
+  auto kfr = [&](int s) { return keyset + s * (key_bytes<NT>() / 16); };
+
+  const DecodeArgs& A = F.A;
+  const int T = A.T, d = A.d, E = A.E, G = A.G, k = A.k, L = A.L, f = A.f, epg = A.epg;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+  const int nC = gridDim.x, c = blockIdx.x;
+  const int KS = d / KSEG, NPAIR = E / 2, NRT_IN = L / 16, NRB = L / DR, NRT_OUT = d / 16;
+  const long long budget = F.timeout;
+  unsigned* err = A.err;
+  const CtrMap cm = ctr_map(d, E, G, L);
+
+  // ---------------------------------------------------------------- set-up
+  if (threadIdx.x == 0) {
+    const unsigned long long old = atomicAdd(F.launches, 1ull);
+    tb.par = (int)((old / (unsigned long long)nC) & 1ull);
+    tb.tables_ready = 0;
+    #pragma unroll 1
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&tb.full[s], 1);
+      mbar_init(&tb.empty[s], 1);
+      tb.seq[s] = -1;
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  unsigned* ctr = F.ctr + (size_t)tb.par * cm.n;
+  {  // clear the copy of the counters the next launch uses
+    unsigned* nxt = F.ctr + (size_t)(tb.par ^ 1) * cm.n;
+    #pragma unroll 1
+    for (int i = c * NTHR + threadIdx.x; i < cm.n; i += nC * NTHR) nxt[i] = 0u;
+  }
+  int a1lo, a1hi, a2lo, a2hi;
+  split(KS * NPAIR, c, nC, a1lo, a1hi);
+  split(KS * G * NRT_IN, c, nC, a2lo, a2hi);
+  const int nA1 = a1hi - a1lo, nA2 = a2hi - a2lo;
+
+  if (warp == PROD) {
+    // ================================================== producer + routing
+    int j = 0;
+    bool ok = true;
+    if (lane == 0) {
+      #pragma unroll 1
+      for (int i = a1lo; ok && i < a1hi; ++i, ++j) {
+        const int ks = i / NPAIR, pr = i % NPAIR;
+        unsigned char* dst = prod_begin<NS>(tb, ring, j, 2 * KSEG * 4, budget, err);
+        if (!(ok = dst != nullptr)) break;
+        tma_load_3d(dst, &F.maps.wr, 0, ks * (KSEG / 256), 2 * pr, &tb.full[j % NS]);
+      }
+      #pragma unroll 1
+      for (int i = a2lo; ok && i < a2hi; ++i, ++j) {
+        const int ks = i / (G * NRT_IN), rem = i % (G * NRT_IN), g = rem / NRT_IN, rt = rem % NRT_IN;
+        unsigned char* dst = prod_begin<NS>(tb, ring, j, 16 * KSEG / 2 + 16 * KSEG / 16, budget, err);
+        if (!(ok = dst != nullptr)) break;
+        tma_load_3d(dst, &F.maps.win_q, 0, ks * (KSEG / 256), g * L + rt * 16, &tb.full[j % NS]);
+        tma_load_2d(dst + 16 * KSEG / 2, &F.maps.win_s, ks * (KSEG / 32), g * L + rt * 16, &tb.full[j % NS]);
+      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    j = __shfl_sync(0xffffffffu, j, 0);
+    // the top-k of token c, published for every CTA
+    if (c < T) {
+      if (lane == 0) wait_count(ctr + cm.done_router, (unsigned)NPAIR, budget, err);
+      __syncwarp();
+      const float2 sw = topk_warp(F.logits + (size_t)c * E, E, k);
+      const int sel_e = __float_as_int(sw.x);
+      const float sel_w = sw.y;
+      if (lane < k) {
+        A.idx[c * k + lane] = sel_e;
+        A.w[c * k + lane] = sel_w;
+      }
       __threadfence();
       __syncwarp();
-      bool last = false;
-      if (lane == 0) last = ticket_last(F.tk_win + g * ntile + rt, (unsigned)nq);
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {  // sum the K-split partials: each lane 8 outputs, loads issued together
-        float part[8][8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int o = lane + 32 * u, row = r0 + (o & 15), t = o >> 4;
-#pragma unroll
-          for (int q2 = 0; q2 < 8; ++q2)
-            part[u][q2] = (t < T && q2 < nq) ? __ldcg(A.Hp + (((size_t)q2 * G + g) * 16 + t) * L + row) : 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int o = lane + 32 * u, row = r0 + (o & 15), t = o >> 4;
-          float v = 0.f;
-#pragma unroll
-          for (int q2 = 0; q2 < 8; ++q2) v += part[u][q2];
-          if (t < T) F.H[((size_t)g * 16 + t) * L + row] = v;
+      if (lane == 0) atomicAdd(ctr + cm.done_topk, 1u);
+    }
+    // routing tables, built by this warp
+    if (lane == 0) wait_count(ctr + cm.done_topk, (unsigned)T, budget, err);
+    __syncwarp();
+    build_tables(tb, A.idx, A.w, T, k, E, G, epg, err);
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      tb.tables_ready = 1;
+      const int n_act = tb.n_act, n_actg = tb.n_actg;
+      int lo = 0, hi = 0;
+      if (ok) split(n_act * (f / 16), c, nC, lo, hi);
+      #pragma unroll 1
+      for (int i = lo; ok && i < hi; ++i) {
+        const int es = i / (f / 16), rt = i % (f / 16), e = tb.elist[es];
+        #pragma unroll 1
+        for (int gu = 0; gu < 2; ++gu, ++j) {
+          unsigned char* dst = prod_begin<NS>(tb, ring, j, 16 * L / 2 + 16 * L / 16, budget, err);
+          if (!(ok = dst != nullptr)) break;
+          tma_load_3d(dst, gu ? &F.maps.up_q : &F.maps.gate_q, 0, 0, e * f + rt * 16, &tb.full[j % NS]);
+          tma_load_2d(dst + 16 * L / 2, gu ? &F.maps.up_s : &F.maps.gate_s, 0, e * f + rt * 16, &tb.full[j % NS]);
         }
       }
+      if (ok) split(n_act * NRB, c, nC, lo, hi);
+      #pragma unroll 1
+      for (int i = lo; ok && i < hi; ++i, ++j) {
+        const int es = i / NRB, rb = i % NRB, e = tb.elist[es];
+        unsigned char* dst = prod_begin<NS>(tb, ring, j, DR * f / 2 + DR * f / 16, budget, err);
+        if (!(ok = dst != nullptr)) break;
+        tma_load_3d(dst, &F.maps.down_q, 0, 0, e * L + rb * DR, &tb.full[j % NS]);
+        tma_load_2d(dst + DR * f / 2, &F.maps.down_s, 0, e * L + rb * DR, &tb.full[j % NS]);
+      }
+      if (ok) split(n_actg * NRT_OUT, c, nC, lo, hi);
+      #pragma unroll 1
+      for (int i = lo; ok && i < hi; ++i, ++j) {
+        const int gi = i / NRT_OUT, rt = i % NRT_OUT, g = tb.glist[gi];
+        unsigned char* dst = prod_begin<NS>(tb, ring, j, 16 * L / 2 + 16 * L / 16, budget, err);
+        if (!(ok = dst != nullptr)) break;
+        tma_load_3d(dst, &F.maps.wout_q, 0, 0, g * d + rt * 16, &tb.full[j % NS]);
+        tma_load_2d(dst + 16 * L / 2, &F.maps.wout_s, 0, g * d + rt * 16, &tb.full[j % NS]);
+      }
+      // Wait for the copies still in flight before the CTA may exit. They do
+      // not depend on other CTAs, so this drain gets a budget of its own.
+      const long long drain = budget > (1ll << 28) ? budget : (1ll << 28);
+      #pragma unroll 1
+      for (int jj = (j > NS ? j - NS : 0); jj < j; ++jj) mbar_wait(&tb.full[jj % NS], (jj / NS) & 1, drain, err);
+    }
+    return;
+  }
+
+  // ================================================================ consumers
+  const int ctid = threadIdx.x;  // 0 .. NCT-1
+  int jbase = 0;
+
+  // ------------------------------------------------- segments of x (A1, A2)
+  if (ctid == 0) {
+    const int k1lo = a1lo / NPAIR, k1hi = (a1hi - 1) / NPAIR, k2lo = a2lo / (G * NRT_IN),
+              k2hi = (a2hi - 1) / (G * NRT_IN);
+    int n = 0;
+    #pragma unroll 1
+    for (int ks = 0; ks < KS; ++ks) {
+      const bool need = (nA1 > 0 && ks >= k1lo && ks <= k1hi) || (nA2 > 0 && ks >= k2lo && ks <= k2hi);
+      if (!need) continue;
+      if (n == KEYS) {
+        set_error(err, ERRBIT_BAD_DATA);
+        break;
+      }
+      tb.key[n++] = ks;
+    }
+    #pragma unroll 1
+    for (int s = n; s < KEYS; ++s) tb.key[s] = -1;
+  }
+  cons_sync();
+  #pragma unroll 1
+  for (int s = 0; s < KEYS; ++s)
+    if (tb.key[s] >= 0) stage_x<NT>(kfr(s), A.x, T, d, tb.key[s], ctid);
+  cons_sync();
+
+  // ------------------------------------------------------------ A1 router
+  #pragma unroll 1
+  for (int li = warp; li < nA1; li += NCW) {
+    const int i = a1lo + li, ks = i / NPAIR, pr = i % NPAIR, e0 = 2 * pr;
+    const float* wr = reinterpret_cast<const float*>(cons_wait<NS>(tb, ring, jbase + li, budget, err));
+    const uint4* fr = kfr(key_slot(tb, ks));
+    // token by token (compact code): lane covers elements u*256 + 8*lane .. +7
+    float mine = 0.f;  // lane 2t + r ends with the partial logit of (token t, expert e0 + r)
+#pragma unroll 1
+    for (int t = 0; t < T; ++t) {
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll 1
+      for (int u = 0; u < 4; ++u) {
+        const int kk = u * 256 + lane * 8;
+        const int cc = kk >> 7, tg = (kk & 127) >> 5, mp = (kk & 31) >> 3;
+        const float4 a0 = *reinterpret_cast<const float4*>(wr + kk);
+        const float4 a1 = *reinterpret_cast<const float4*>(wr + kk + 4);
+        const float4 b0 = *reinterpret_cast<const float4*>(wr + KSEG + kk);
+        const float4 b1 = *reinterpret_cast<const float4*>(wr + KSEG + kk + 4);
+        const uint4 xv = fr[((cc * NT + (t >> 3)) * 4 + mp) * 32 + (t & 7) * 4 + tg];
+        const float2 p0 = __half22float2(*reinterpret_cast<const __half2*>(&xv.x));  // e0, e4
+        const float2 p1 = __half22float2(*reinterpret_cast<const __half2*>(&xv.y));  // e1, e5
+        const float2 p2 = __half22float2(*reinterpret_cast<const __half2*>(&xv.z));  // e2, e6
+        const float2 p3 = __half22float2(*reinterpret_cast<const __half2*>(&xv.w));  // e3, e7
+        s0 = fmaf(a0.x, p0.x, s0); s0 = fmaf(a0.y, p1.x, s0); s0 = fmaf(a0.z, p2.x, s0); s0 = fmaf(a0.w, p3.x, s0);
+        s0 = fmaf(a1.x, p0.y, s0); s0 = fmaf(a1.y, p1.y, s0); s0 = fmaf(a1.z, p2.y, s0); s0 = fmaf(a1.w, p3.y, s0);
+        s1 = fmaf(b0.x, p0.x, s1); s1 = fmaf(b0.y, p1.x, s1); s1 = fmaf(b0.z, p2.x, s1); s1 = fmaf(b0.w, p3.x, s1);
+        s1 = fmaf(b1.x, p0.y, s1); s1 = fmaf(b1.y, p1.y, s1); s1 = fmaf(b1.z, p2.y, s1); s1 = fmaf(b1.w, p3.y, s1);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+      }
+      if (lane == 2 * t) mine = s0;
+      if (lane == 2 * t + 1) mine = s1;
+    }
+    cons_release<NS>(tb, jbase + li);
+    const int t = lane >> 1, r = lane & 1;
+    if (t < T) F.Lp[((size_t)ks * 16 + t) * E + e0 + r] = mine;
+    __threadfence();
+    __syncwarp();
+    bool last = false;
+    if (lane == 0) last = ticket_last(ctr + cm.tk_router + pr, (unsigned)KS);
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+      __threadfence();
+      if (t < T) {
+        float part[8];
+#pragma unroll
+        for (int s2 = 0; s2 < 8; ++s2) part[s2] = s2 < KS ? __ldcg(F.Lp + ((size_t)s2 * 16 + t) * E + e0 + r) : 0.f;
+        float v = 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < 8; ++s2) v += part[s2];
+        if (A.b_r) v += A.b_r[e0 + r];
+        F.logits[(size_t)t * E + e0 + r] = v;
+      }
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) atomicAdd(ctr + cm.done_router, 1u);
     }
   }
-  grid_sync(F.bar, F.timeout, A.err);
+  jbase += nA1;
 
-  // --------------------------------------------------------------- P3 gate/up
+  // ------------------------------------------------------------ A2 W_in
+  #pragma unroll 1
+  for (int li = warp; li < nA2; li += NCW) {
+    const int i = a2lo + li, ks = i / (G * NRT_IN), rem = i % (G * NRT_IN), g = rem / NRT_IN, rt = rem % NRT_IN;
+    const unsigned char* sl = cons_wait<NS>(tb, ring, jbase + li, budget, err);
+    float acc[NT][4] = {};
+    mma_ring_rows_swz<NT>(sl, KSEG / 256, 0, reinterpret_cast<const uint16_t*>(sl + 16 * KSEG / 2), KSEG / 32,
+                          KSEG / 128, kfr(key_slot(tb, ks)), acc);
+    cons_release<NS>(tb, jbase + li);
+    float* Hp = A.Hp + ((size_t)ks * G + g) * 16 * L;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const int row = rt * 16 + gid + ((h & 2) ? 8 : 0), t = nt * 8 + 2 * tig + (h & 1);
+        if (t < T) Hp[(size_t)t * L + row] = acc[nt][h];
+      }
+    __threadfence();
+    __syncwarp();
+    bool last = false;
+    if (lane == 0) last = ticket_last(ctr + cm.tk_win + g * NRT_IN + rt, (unsigned)KS);
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {  // sum the segment partials in order, straight into fp16 fragments
+      __threadfence();
+      const int run = lane & 1, n = lane >> 1, k0 = rt * 16 + run * 8;
+      float e[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (n < T) {
+        float4 p[8][2];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float* src = A.Hp + (((size_t)q * G + g) * 16 + n) * L + k0;
+          p[q][0] = q < KS ? __ldcg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+          p[q][1] = q < KS ? __ldcg(reinterpret_cast<const float4*>(src + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          e[0] += p[q][0].x; e[1] += p[q][0].y; e[2] += p[q][0].z; e[3] += p[q][0].w;
+          e[4] += p[q][1].x; e[5] += p[q][1].y; e[6] += p[q][1].z; e[7] += p[q][1].w;
+        }
+      }
+      if (n < 8 * NT) F.Hf[(size_t)g * (L / 128) * FR + entry_index<NT>(k0, n)] = pack_frag8(e);
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) atomicAdd(ctr + cm.done_in + g, 1u);
+    }
+  }
+  jbase += nA2;
+
+  // ---------------------------------------------------- routing tables ready
+  if (ctid == 0) {
+    const long long t0 = clock64();
+    #pragma unroll 1
+    while (tb.tables_ready == 0) {
+      if (clock64() - t0 > budget) {
+        set_error(err, ERRBIT_TIMEOUT);
+        break;
+      }
+      __nanosleep(64);
+    }
+    __threadfence_block();
+  }
+  cons_sync();
+  const int n_act = tb.n_act, n_actg = tb.n_actg;
+
+  // ------------------------------------------------------------ B gate/up
   {
-    const int nch = L / 128, ntile = f / 16;
-    stage_keys(
-        tb, tb.lo3, tb.hi3, [&](int i) { return tb.elist[i / ntile] / epg; },
-        [&](int s, int g) { stage_f32<NT>(slot(s), F.H + (size_t)g * 16 * L, T, L); }, A.err);
-    for (int i = tb.lo3 + warp; i < tb.hi3; i += FW) {
-      const int es = i / ntile, rt = i % ntile, e = tb.elist[es];
-      const uint4* fr = slot(slot_of(tb, e / epg));
+    int lo, hi;
+    split(n_act * (f / 16), c, nC, lo, hi);
+    if (ctid == 0) collect_keys(tb, lo, hi, [&](int i) { return tb.elist[i / (f / 16)] / epg; }, err);
+    cons_sync();
+    if (ctid < KEYS && tb.key[ctid] >= 0) wait_count(ctr + cm.done_in + tb.key[ctid], (unsigned)NRT_IN, budget, err);
+    cons_sync();
+    #pragma unroll 1
+    for (int s = 0; s < KEYS; ++s)
+      if (tb.key[s] >= 0) copy_frags(kfr(s), F.Hf + (size_t)tb.key[s] * (L / 128) * FR, (L / 128) * FR, ctid);
+    cons_sync();
+    #pragma unroll 1
+    for (int li = warp; li < hi - lo; li += NCW) {
+      const int i = lo + li, es = i / (f / 16), rt = i % (f / 16), e = tb.elist[es];
+      const uint4* fr = kfr(key_slot(tb, e / epg));
       float ag[NT][4] = {}, au[NT][4] = {};
-      mma_rows<NT, PFD>(A.gate_q + (size_t)e * f * (L / 2), A.gate_s + (size_t)e * f * (L / 32), L, rt * 16, 0, nch, 0,
-                        fr, ag);
-      mma_rows<NT, PFD>(A.up_q + (size_t)e * f * (L / 2), A.up_s + (size_t)e * f * (L / 32), L, rt * 16, 0, nch, 0,
-                        fr, au);
-      const unsigned m = tb.emask[e];
+      const unsigned char* sg = cons_wait<NS>(tb, ring, jbase + 2 * li, budget, err);
+      const unsigned char* su = cons_wait<NS>(tb, ring, jbase + 2 * li + 1, budget, err);
+      mma_ring_rows_swz2<NT>(sg, reinterpret_cast<const uint16_t*>(sg + 16 * L / 2), su,
+                             reinterpret_cast<const uint16_t*>(su + 16 * L / 2), L / 256, L / 32, L / 128, fr, ag, au);
+      cons_release<NS>(tb, jbase + 2 * li);
+      cons_release<NS>(tb, jbase + 2 * li + 1);
+      // v = w(t, e) * silu(gate) * up, as the down projection's fragments
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const int row = rt * 16 + gid + ((h & 2) ? 8 : 0), t = nt * 8 + 2 * tig + (h & 1);
-          if (t < T && ((m >> t) & 1u)) A.V[((size_t)es * 16 + t) * f + row] = silu(ag[nt][h]) * au[nt][h];
-        }
-    }
-  }
-  grid_sync(F.bar, F.timeout, A.err);
-
-  // ------------------------------------------------------------------ P4 down
-  {
-    const int nch = f / 128;
-    const int per_e = nch * NT * 128;  // uint4 per expert
-    const int nb_max = (NSLOT * SLOT_BYTES - RED_BYTES) / (per_e * 16);
-    float* red = reinterpret_cast<float*>(dsm + NSLOT * SLOT_BYTES - RED_BYTES);  // [3][4][16][16]
-    const int rt = warp & 3, es = warp >> 2;
-    for (int it = c; it < tb.N4; it += nC) {
-      const int gi = it / tb.nblk, blk = it % tb.nblk, g = tb.glist[gi];
-      const int s0 = tb.gslot0[gi], s1 = tb.gslot0[gi + 1];
-      const int row0 = blk * 64 + rt * 16;
-      float acc[NT][4] = {};
-      for (int b0 = s0; b0 < s1; b0 += nb_max) {
-        const int nb = min(nb_max, s1 - b0);
-        __syncthreads();
-        uint4* fr = slot_base;
-        for (int si = threadIdx.x; si < nb * per_e; si += FT) {
-          const int bi = si / per_e, sj = si % per_e;
-          const int ln = sj & 31, mp = (sj >> 5) & 3, rest = sj >> 7;
-          const int nt = rest % NT, cc = rest / NT;
-          const int n = nt * 8 + (ln >> 2), tg = ln & 3;
-          const int k0 = cc * 128 + tg * 32 + mp * 8;
-          const int sl = b0 + bi, e = tb.elist[sl];
-          float ev[8];
-          if (n < T && ((tb.emask[e] >> n) & 1u)) {
-            const float wt = route_weight(tb, n, e, k);
-            const float* vp = A.V + ((size_t)sl * 16 + n) * f + k0;
-            const float4 a = __ldcg(reinterpret_cast<const float4*>(vp));
-            const float4 b = __ldcg(reinterpret_cast<const float4*>(vp + 4));
-            ev[0] = wt * a.x; ev[1] = wt * a.y; ev[2] = wt * a.z; ev[3] = wt * a.w;
-            ev[4] = wt * b.x; ev[5] = wt * b.y; ev[6] = wt * b.z; ev[7] = wt * b.w;
-          } else {
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int t = nt * 8 + 2 * tig + h2;
+          const float wt = t < T ? route_weight(tb, t, e, k) : 0.f;
 #pragma unroll
-            for (int h = 0; h < 8; ++h) ev[h] = 0.f;
+          for (int hh = 0; hh < 2; ++hh) {
+            const float a = ag[nt][hh * 2 + h2];
+            ag[nt][hh * 2 + h2] = wt != 0.f ? wt * a * __frcp_rn(1.f + __expf(-a)) * au[nt][hh * 2 + h2] : 0.f;
           }
-          fr[si] = pack_frag8(ev);
         }
-        __syncthreads();
-        for (int sl = s0 + es; sl < b0 + nb; sl += 4) {
-          if (sl < b0) continue;
-          const int e = tb.elist[sl];
-          mma_rows<NT, PFD>(A.down_q + (size_t)e * L * (f / 2), A.down_s + (size_t)e * L * (f / 32), f, row0, 0, nch, 0,
-                            fr + (sl - b0) * per_e, acc);
-        }
-      }
-      if (es > 0) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int h = 0; h < 4; ++h)
-            red[(((es - 1) * 4 + rt) * 16 + gid + ((h & 2) ? 8 : 0)) * 16 + nt * 8 + 2 * tig + (h & 1)] = acc[nt][h];
-      }
-      __syncthreads();
-      if (es == 0) {
-        float* Z = A.Z + (size_t)g * 16 * L;
+      float ev[8];
+      acc_to_entry<NT>(ag, ev);
+      const int run = lane & 1, n = lane >> 1;
+      if (n < 8 * NT) F.Vf[(size_t)es * (f / 128) * FR + entry_index<NT>(rt * 16 + run * 8, n)] = pack_frag8(ev);
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) atomicAdd(ctr + cm.done_gu + es, 1u);
+    }
+    jbase += 2 * (hi - lo);
+  }
+
+  // ------------------------------------------------------------ C down
+  {
+    int lo, hi;
+    split(n_act * NRB, c, nC, lo, hi);
+    cons_sync();
+    if (ctid == 0) collect_keys(tb, lo, hi, [&](int i) { return i / NRB; }, err);
+    cons_sync();
+    if (ctid < KEYS && tb.key[ctid] >= 0) wait_count(ctr + cm.done_gu + tb.key[ctid], (unsigned)(f / 16), budget, err);
+    cons_sync();
+    #pragma unroll 1
+    for (int s = 0; s < KEYS; ++s)
+      if (tb.key[s] >= 0) copy_frags(kfr(s), F.Vf + (size_t)tb.key[s] * (f / 128) * FR, (f / 128) * FR, ctid);
+    cons_sync();
+    #pragma unroll 1
+    for (int li = warp; li < hi - lo; li += NCW) {
+      const int i = lo + li, es = i / NRB, rb = i % NRB, e = tb.elist[es], g = e / epg;
+      const uint4* fr = kfr(key_slot(tb, es));
+      const unsigned char* sl = cons_wait<NS>(tb, ring, jbase + li, budget, err);
+      float* Zp = F.Zp + (size_t)es * 16 * L;
+#pragma unroll 1
+      for (int mt = 0; mt < DR / 16; ++mt) {
+        float acc[NT][4] = {};
+        mma_ring_rows_swz<NT>(sl, f / 256, mt * 16, reinterpret_cast<const uint16_t*>(sl + DR * f / 2), f / 32, f / 128,
+                              fr, acc);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
-            const int rr = gid + ((h & 2) ? 8 : 0), t = nt * 8 + 2 * tig + (h & 1);
-            float v = acc[nt][h];
-            for (int s2 = 0; s2 < 3; ++s2) v += red[((s2 * 4 + rt) * 16 + rr) * 16 + t];
-            if (t < T) Z[(size_t)t * L + row0 + rr] = v;
+            const int row = rb * DR + mt * 16 + gid + ((h & 2) ? 8 : 0), t = nt * 8 + 2 * tig + (h & 1);
+            if (t < T) Zp[(size_t)t * L + row] = acc[nt][h];
           }
       }
-      __syncthreads();
+      cons_release<NS>(tb, jbase + li);
+      int gi = 0;
+      #pragma unroll 1
+      while (gi < n_actg && tb.glist[gi] != g) ++gi;
+      const int s0 = tb.gslot0[gi], s1 = tb.gslot0[gi + 1];
+      __threadfence();
+      __syncwarp();
+      bool last = false;
+      if (lane == 0) last = ticket_last(ctr + cm.tk_down + g * NRB + rb, (unsigned)(s1 - s0));
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {  // Z rows of this block: the group's experts in ascending order, into fragments
+        __threadfence();
+        constexpr int PE = DR / 8 * 16 / 32;  // fragment entries per lane (DR/8 runs x 16 tokens)
+        float ev[PE][8];
+#pragma unroll
+        for (int u = 0; u < PE; ++u)
+#pragma unroll
+          for (int h = 0; h < 8; ++h) ev[u][h] = 0.f;
+#pragma unroll 1
+        for (int sl2 = s0; sl2 < s1; sl2 += 4) {
+          float4 p[4][PE][2];
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int u = 0; u < PE; ++u) {
+              const int en = lane + 32 * u, run = en % (DR / 8), n = en / (DR / 8);
+              const float* src = F.Zp + ((size_t)(sl2 + q) * 16 + n) * L + rb * DR + run * 8;
+              const bool v = n < T && sl2 + q < s1;
+              p[q][u][0] = v ? __ldcg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+              p[q][u][1] = v ? __ldcg(reinterpret_cast<const float4*>(src + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int u = 0; u < PE; ++u) {
+              ev[u][0] += p[q][u][0].x; ev[u][1] += p[q][u][0].y; ev[u][2] += p[q][u][0].z; ev[u][3] += p[q][u][0].w;
+              ev[u][4] += p[q][u][1].x; ev[u][5] += p[q][u][1].y; ev[u][6] += p[q][u][1].z; ev[u][7] += p[q][u][1].w;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < PE; ++u) {
+          const int en = lane + 32 * u, run = en % (DR / 8), n = en / (DR / 8);
+          if (n < 8 * NT)
+            F.Zf[(size_t)g * (L / 128) * FR + entry_index<NT>(rb * DR + run * 8, n)] = pack_frag8(ev[u]);
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(ctr + cm.done_down + g, 1u);
+      }
     }
+    jbase += hi - lo;
   }
-  grid_sync(F.bar, F.timeout, A.err);
 
-  // ------------------------------------------------------------------ P5 W_out
+  // ------------------------------------------------------------ D W_out
   {
-    const int nch = L / 128, ntile = d / 16;
-    stage_keys(
-        tb, tb.lo5, tb.hi5, [&](int i) { return i / ntile; },
-        [&](int s, int gi) { stage_f32<NT>(slot(s), A.Z + (size_t)tb.glist[gi] * 16 * L, T, L); }, A.err);
-    for (int i = tb.lo5 + warp; i < tb.hi5; i += FW) {
-      const int gi = i / ntile, rt = i % ntile, g = tb.glist[gi];
+    int lo, hi;
+    split(n_actg * NRT_OUT, c, nC, lo, hi);
+    cons_sync();
+    if (ctid == 0) collect_keys(tb, lo, hi, [&](int i) { return i / NRT_OUT; }, err);
+    cons_sync();
+    if (ctid < KEYS && tb.key[ctid] >= 0)
+      wait_count(ctr + cm.done_down + tb.glist[tb.key[ctid]], (unsigned)NRB, budget, err);
+    cons_sync();
+    #pragma unroll 1
+    for (int s = 0; s < KEYS; ++s)
+      if (tb.key[s] >= 0)
+        copy_frags(kfr(s), F.Zf + (size_t)tb.glist[tb.key[s]] * (L / 128) * FR, (L / 128) * FR, ctid);
+    cons_sync();
+    #pragma unroll 1
+    for (int li = warp; li < hi - lo; li += NCW) {
+      const int i = lo + li, gi = i / NRT_OUT, rt = i % NRT_OUT, g = tb.glist[gi];
+      const unsigned char* sl = cons_wait<NS>(tb, ring, jbase + li, budget, err);
       float acc[NT][4] = {};
-      mma_rows<NT, PFD>(A.W_out_q + (size_t)g * d * (L / 2), A.W_out_s + (size_t)g * d * (L / 32), L, rt * 16, 0, nch,
-                        0, slot(slot_of(tb, gi)), acc);
+      mma_ring_rows_swz<NT>(sl, L / 256, 0, reinterpret_cast<const uint16_t*>(sl + 16 * L / 2), L / 32, L / 128,
+                            kfr(key_slot(tb, gi)), acc);
+      cons_release<NS>(tb, jbase + li);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -578,85 +857,157 @@ __global__ void __launch_bounds__(FT, 1) decode_fused_kernel(FusedArgs F) {
       __threadfence();
       __syncwarp();
       bool last = false;
-      if (lane == 0) last = ticket_last(F.tk_wout + rt, (unsigned)tb.n_actg);
+      if (lane == 0) last = ticket_last(ctr + cm.tk_wout + rt, (unsigned)n_actg);
       last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {  // weighted combine in ascending group order, 8 groups' loads at a time
-        float v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = 0.f;
-        for (int g0 = 0; g0 < tb.n_actg; g0 += 8) {
-          float part[8][8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int o = lane + 32 * u, row = rt * 16 + (o & 15), t = o >> 4;
+      if (last) {  // combine in ascending group order: lane -> 4 rows x 1 token, one float4 per group
+        __threadfence();
+#pragma unroll 1
+        for (int q = lane; q < 4 * T; q += 32) {
+          const int rq = q & 3, t = q >> 2, row = rt * 16 + rq * 4;
+          float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+          for (int g0 = 0; g0 < n_actg; g0 += 8) {
+            float4 p4[8];
 #pragma unroll
             for (int gg = 0; gg < 8; ++gg)
-              part[u][gg] = (t < T && g0 + gg < tb.n_actg)
-                                ? __ldcg(A.Yp + ((size_t)tb.glist[g0 + gg] * 16 + t) * d + row)
-                                : 0.f;
+              p4[gg] = g0 + gg < n_actg
+                           ? __ldcg(reinterpret_cast<const float4*>(A.Yp + ((size_t)tb.glist[g0 + gg] * 16 + t) * d + row))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int gg = 0; gg < 8; ++gg) {
+              acc4.x += p4[gg].x; acc4.y += p4[gg].y; acc4.z += p4[gg].z; acc4.w += p4[gg].w;
+            }
           }
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-#pragma unroll
-            for (int gg = 0; gg < 8; ++gg) v[u] += part[u][gg];
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int o = lane + 32 * u, row = rt * 16 + (o & 15), t = o >> 4;
-          if (t >= T) continue;
-          float r = v[u];
-          if (A.residual) r += bf16_to_f32(A.residual[(size_t)t * d + row]);
-          A.y[(size_t)t * d + row] = f32_to_bf16_rne(r);
+          if (A.residual) {
+            const uint2 rb = *reinterpret_cast<const uint2*>(A.residual + (size_t)t * d + row);
+            acc4.x += __uint_as_float(rb.x << 16);
+            acc4.y += __uint_as_float(rb.x & 0xffff0000u);
+            acc4.z += __uint_as_float(rb.y << 16);
+            acc4.w += __uint_as_float(rb.y & 0xffff0000u);
+          }
+          uint2 o;
+          o.x = (uint32_t)f32_to_bf16_rne(acc4.x) | ((uint32_t)f32_to_bf16_rne(acc4.y) << 16);
+          o.y = (uint32_t)f32_to_bf16_rne(acc4.z) | ((uint32_t)f32_to_bf16_rne(acc4.w) << 16);
+          *reinterpret_cast<uint2*>(A.y + (size_t)t * d + row) = o;
         }
       }
     }
   }
 }
 
+// ===================================================================== host
+size_t fused_counter_words(int d, int E, int G, int L) { return 2 * (size_t)ctr_map(d, E, G, L).n; }
+
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    cudaGetLastError();
+  }
+  return fn;
+}
+
+// packed int4 [rows][K/2] as [rows][K/256][128 B], box {128, lines, box_rows}
+bool map_q(CUtensorMap* m, const uint8_t* q, long long rows, int K, int lines, int box_rows) {
+  const cuuint64_t dims[3] = {128, (cuuint64_t)(K / 256), (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {128, (cuuint64_t)(K / 2)};
+  const cuuint32_t box[3] = {128, (cuuint32_t)lines, (cuuint32_t)box_rows}, es[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(q), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// bf16 scales [rows][K/32], box {box_cols, box_rows}
+bool map_s(CUtensorMap* m, const uint16_t* s, long long rows, int K, int box_cols, int box_rows) {
+  const cuuint64_t dims[2] = {(cuuint64_t)(K / 32), (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)(K / 32 * 2)};
+  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows}, es[2] = {1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(s), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
+bool fused_make_maps(const DecodeArgs& A, DecodeMaps* mp) {
+  if (!encode_fn() || !A.W_r) return false;
+  const int d = A.d, E = A.E, G = A.G, L = A.L, f = A.f;
+  if (d % KSEG != 0 || L % 256 != 0 || f % 256 != 0) return false;
+  bool ok = true;
+  {
+    const cuuint64_t dims[3] = {256, (cuuint64_t)(d / 256), (cuuint64_t)E};
+    const cuuint64_t strides[2] = {1024, (cuuint64_t)d * 4};
+    const cuuint32_t box[3] = {256, KSEG / 256, 2}, es[3] = {1, 1, 1};
+    ok = ok && encode_fn()(&mp->wr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(A.W_r), dims, strides, box,
+                           es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
+  ok = ok && map_q(&mp->win_q, A.W_in_q, (long long)G * L, d, KSEG / 256, 16);
+  ok = ok && map_s(&mp->win_s, A.W_in_s, (long long)G * L, d, KSEG / 32, 16);
+  ok = ok && map_q(&mp->gate_q, A.gate_q, (long long)E * f, L, L / 256, 16);
+  ok = ok && map_s(&mp->gate_s, A.gate_s, (long long)E * f, L, L / 32, 16);
+  ok = ok && map_q(&mp->up_q, A.up_q, (long long)E * f, L, L / 256, 16);
+  ok = ok && map_s(&mp->up_s, A.up_s, (long long)E * f, L, L / 32, 16);
+  ok = ok && map_q(&mp->down_q, A.down_q, (long long)E * L, f, f / 256, DR);
+  ok = ok && map_s(&mp->down_s, A.down_s, (long long)E * L, f, f / 32, DR);
+  ok = ok && map_q(&mp->wout_q, A.W_out_q, (long long)G * d, L, L / 256, 16);
+  ok = ok && map_s(&mp->wout_s, A.W_out_s, (long long)G * d, L, L / 32, 16);
+  return ok;
+}
+
 bool fused_decode_supported(const DecodeArgs& A) {
   if (A.r != 0 || A.T < 1 || A.T > 16) return false;
-  if (A.E > 1024 || A.E % 2 != 0 || A.G > 64) return false;
-  // every streamed matrix walks whole chunks of 128 (scale rows 8-byte aligned);
-  // these bounds keep each CTA's activation sets within NSLOT slots
-  if (A.d % 128 != 0 || A.L % 128 != 0 || A.f % 128 != 0) return false;
-  if (A.L < 256 || A.L > 1024 || A.f < 128 || A.d < 128) return false;
-  if ((A.d / 128 + A.ks_in - 1) / A.ks_in > 8 || A.ks_in > 8) return false;
-  const int RS = A.d % 512 == 0 ? 512 : 128;
-  if (A.d / RS > 16) return false;  // router partial sums reduced 16 at a time
-  if ((long long)A.T * RS * 2 > SLOT_BYTES) return false;
-  const int nchf = A.f / 128;
-  if (nchf * 2 * 128 * 16 > NSLOT * SLOT_BYTES - RED_BYTES) return false;
-  if ((long long)A.T * A.E * 4 > SLOT_BYTES || A.E > 512) return false;  // logits: one slot, 16 per lane
+  if (A.E > 512 || A.E % 2 != 0 || A.G > 64 || A.k > 16) return false;
+  if (A.d % KSEG != 0 || A.d / KSEG > 8) return false;
+  if (A.L != 256 && A.L != 512 && A.L != 1024) return false;  // gate/up/W_out chunks: 16 rows x L in one slot
+  if (A.f != 256 && A.f != 512) return false;                  // down chunks: 32 rows x f in one slot
+  if (A.f % 16 != 0 || (long long)A.T * A.k > MAX_ACT) return false;
   return true;
 }
 
 cudaError_t fused_set_attributes() {
-  cudaFuncSetAttribute(decode_fused_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, DYN_SMEM);
-  cudaFuncSetAttribute(decode_fused_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, DYN_SMEM);
+  cudaFuncSetAttribute(decode_fused_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<1>());
+  cudaFuncSetAttribute(decode_fused_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<2>());
   return cudaGetLastError();
 }
 
 int fused_grid(int num_sms) {
-  int per = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, decode_fused_kernel<2>, FT, DYN_SMEM) != cudaSuccess ||
-      per < 1)
+  int per1 = 0, per2 = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per1, decode_fused_kernel<1>, NTHR, dyn_smem<1>()) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per2, decode_fused_kernel<2>, NTHR, dyn_smem<2>()) !=
+          cudaSuccess ||
+      per1 < 1 || per2 < 1) {
+    cudaGetLastError();
     return 0;
+  }
   return num_sms;  // one CTA per SM
 }
 
-cudaError_t launch_decode_fused(FusedArgs F, int grid, cudaStream_t st) {
-  F.router_slice = F.A.d % 512 == 0 ? 512 : 128;
+cudaError_t launch_decode_fused(const FusedArgs& F, int grid, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(FT);
-  cfg.dynamicSmemBytes = DYN_SMEM;
+  cfg.blockDim = dim3(NTHR);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (F.A.T <= 8) return cudaLaunchKernelEx(&cfg, decode_fused_kernel<1>, F);
+  if (F.A.T <= 8) {
+    cfg.dynamicSmemBytes = dyn_smem<1>();
+    return cudaLaunchKernelEx(&cfg, decode_fused_kernel<1>, F);
+  }
+  cfg.dynamicSmemBytes = dyn_smem<2>();
   return cudaLaunchKernelEx(&cfg, decode_fused_kernel<2>, F);
 }
 

@@ -1,0 +1,213 @@
+// A shared-memory weight ring for the decode path: one producer warp streams
+// the CTA's weight chunks (row segments of packed int4 plus their bf16
+// scales, or fp32 rows) into fixed slots with 16-byte asynchronous copies,
+// far ahead of the warps that consume them; each slot is handed over with an
+// mbarrier pair (full: one arrival per producer lane once its copies have
+// landed; empty: one arrival by the consuming warp).
+//
+// Slot layout for an int4 chunk of R rows x Kseg elements: weight rows at a
+// padded stride RS = Kseg/2 + 64 bytes (a stride of 64 mod 128 bytes makes the
+// 16-byte fragment loads of rows gid and gid+1 fall in different banks), then
+// the scales, [R][Kseg/32] bf16.
+#pragma once
+#include "common.cuh"
+
+namespace lmoe {
+
+LMOE_DEV void mbar_expect_tx(uint64_t* m, uint32_t bytes) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }" ::"r"(smem_u32(m)),
+               "r"(bytes)
+               : "memory");
+}
+
+// global -> shared bulk copy (16-byte aligned addresses, size a multiple of
+// 16) completing on mbarrier m
+LMOE_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* m) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(m))
+      : "memory");
+}
+
+// TMA tensor loads (tile mode) completing on mbarrier m; coordinates
+// innermost first. The tensor map lives in kernel parameter space.
+LMOE_DEV void tma_load_2d(void* dst, const void* tmap, int c0, int c1, uint64_t* m) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(smem_u32(dst)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(smem_u32(m))
+      : "memory");
+}
+LMOE_DEV void tma_load_3d(void* dst, const void* tmap, int c0, int c1, int c2, uint64_t* m) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(m))
+      : "memory");
+}
+
+// 16-byte global -> shared copy (cp.async, bypassing L1)
+LMOE_DEV void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+// One arrival on m once every cp.async this thread issued before has landed
+// (the barrier's expected count includes these arrivals).
+LMOE_DEV void cp_async_arrive(uint64_t* m) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(m)) : "memory");
+}
+
+LMOE_DEV bool mbar_test(uint64_t* m, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+               : "=r"(ok)
+               : "r"(smem_u32(m)), "r"(parity)
+               : "memory");
+  return ok != 0;
+}
+
+// acc[nt] += W[16 rows][128*nc elements] * frags, with W in a ring slot:
+// rows at byte stride RS from `w` (already offset to the first row and the
+// first 128-element chunk), scales at element stride SS from `s` (offset
+// likewise). frag points at the fragments of the first chunk (see
+// frag_index; chunk c of the slot uses fragment chunk c).
+template <int NT>
+LMOE_DEV void mma_ring_rows(const unsigned char* w, int RS, const uint16_t* s, int SS, int nc, const uint4* frag,
+                            float acc[NT][4]) {
+  const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+  const unsigned char* p0 = w + gid * RS + tig * 16;
+  const unsigned char* p8 = p0 + 8 * RS;
+  const uint16_t* s0 = s + gid * SS + tig;
+  const uint16_t* s8 = s0 + 8 * SS;
+#pragma unroll 2
+  for (int c = 0; c < nc; ++c) {
+    const uint4 a = *reinterpret_cast<const uint4*>(p0 + c * 64);
+    const uint4 b = *reinterpret_cast<const uint4*>(p8 + c * 64);
+    const __half2 h0 = scale_h2(s0[c * 4]), h8 = scale_h2(s8[c * 4]);
+    const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
+    const uint32_t wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int mp = 0; mp < 4; ++mp) {
+      uint32_t A[4], B8[4];
+      dequant_word(wa[mp], h0, A);
+      dequant_word(wb[mp], h8, B8);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint4 f = frag[frag_index(c, nt, mp, lane, NT)];
+        mma16816(acc[nt], A[0], B8[0], A[1], B8[1], f.x, f.y);
+        mma16816(acc[nt], A[2], B8[2], A[3], B8[3], f.z, f.w);
+      }
+    }
+  }
+}
+
+// The same contraction with W stored densely by a TMA box with 128-byte
+// swizzle: row r of the chunk is LPR 128-byte lines (line i = r*LPR + k/256
+// for element k), and 16-byte unit j of line i sits at unit j ^ (i & 7).
+// `w` is the (1024-byte aligned) slot base, row0 the first row of the tile,
+// `s` the chunk's scales [rows][SS].
+template <int NT>
+LMOE_DEV void mma_ring_rows_swz(const unsigned char* w, int LPR, int row0, const uint16_t* s, int SS, int nc,
+                                const uint4* frag, float acc[NT][4]) {
+  const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+  const int r0 = row0 + gid, r8 = r0 + 8;
+  const uint16_t* s0 = s + r0 * SS + tig;
+  const uint16_t* s8 = s + r8 * SS + tig;
+  float acc2[NT][4];  // a second accumulator chain (odd m) halves the MMA dependency chain
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int h = 0; h < 4; ++h) acc2[nt][h] = 0.f;
+#pragma unroll 1
+  for (int c = 0; c < nc; ++c) {
+    const int i0 = r0 * LPR + (c >> 1), i8 = r8 * LPR + (c >> 1), j = ((c & 1) << 2) | tig;
+    const uint4 a = *reinterpret_cast<const uint4*>(w + i0 * 128 + ((j ^ (i0 & 7)) << 4));
+    const uint4 b = *reinterpret_cast<const uint4*>(w + i8 * 128 + ((j ^ (i8 & 7)) << 4));
+    const __half2 h0 = scale_h2(s0[c * 4]), h8 = scale_h2(s8[c * 4]);
+    const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
+    const uint32_t wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int mp = 0; mp < 4; ++mp) {
+      uint32_t A[4], B8[4];
+      dequant_word(wa[mp], h0, A);
+      dequant_word(wb[mp], h8, B8);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint4 f = frag[frag_index(c, nt, mp, lane, NT)];
+        mma16816(acc[nt], A[0], B8[0], A[1], B8[1], f.x, f.y);
+        mma16816(acc2[nt], A[2], B8[2], A[3], B8[3], f.z, f.w);
+      }
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int h = 0; h < 4; ++h) acc[nt][h] += acc2[nt][h];
+}
+
+// Two matrices (same shape, same activations) in one pass: the fragment
+// loads are shared and the two accumulator chains interleave.
+template <int NT>
+LMOE_DEV void mma_ring_rows_swz2(const unsigned char* w1, const uint16_t* s1, const unsigned char* w2,
+                                 const uint16_t* s2, int LPR, int SS, int nc, const uint4* frag, float acc1[NT][4],
+                                 float acc2[NT][4]) {
+  const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+  const int r0 = gid, r8 = gid + 8;
+  const uint16_t* s10 = s1 + r0 * SS + tig;
+  const uint16_t* s18 = s1 + r8 * SS + tig;
+  const uint16_t* s20 = s2 + r0 * SS + tig;
+  const uint16_t* s28 = s2 + r8 * SS + tig;
+#pragma unroll 1
+  for (int c = 0; c < nc; ++c) {
+    const int i0 = r0 * LPR + (c >> 1), i8 = r8 * LPR + (c >> 1), j = ((c & 1) << 2) | tig;
+    const int o0 = i0 * 128 + ((j ^ (i0 & 7)) << 4), o8 = i8 * 128 + ((j ^ (i8 & 7)) << 4);
+    const uint4 a = *reinterpret_cast<const uint4*>(w1 + o0);
+    const uint4 b = *reinterpret_cast<const uint4*>(w1 + o8);
+    const uint4 a2 = *reinterpret_cast<const uint4*>(w2 + o0);
+    const uint4 b2 = *reinterpret_cast<const uint4*>(w2 + o8);
+    const __half2 h0 = scale_h2(s10[c * 4]), h8 = scale_h2(s18[c * 4]);
+    const __half2 g0 = scale_h2(s20[c * 4]), g8 = scale_h2(s28[c * 4]);
+    const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+    const uint32_t va[4] = {a2.x, a2.y, a2.z, a2.w}, vb[4] = {b2.x, b2.y, b2.z, b2.w};
+#pragma unroll
+    for (int mp = 0; mp < 4; ++mp) {
+      uint32_t A[4], B8[4], C[4], D8[4];
+      dequant_word(wa[mp], h0, A);
+      dequant_word(wb[mp], h8, B8);
+      dequant_word(va[mp], g0, C);
+      dequant_word(vb[mp], g8, D8);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint4 f = frag[frag_index(c, nt, mp, lane, NT)];
+        mma16816(acc1[nt], A[0], B8[0], A[1], B8[1], f.x, f.y);
+        mma16816(acc2[nt], C[0], D8[0], C[1], D8[1], f.x, f.y);
+        mma16816(acc1[nt], A[2], B8[2], A[3], B8[3], f.z, f.w);
+        mma16816(acc2[nt], C[2], D8[2], C[3], D8[3], f.z, f.w);
+      }
+    }
+  }
+}
+
+// Transpose a warp's m16n8 accumulators (rows r0..r0+15 of an activation
+// that is the reduction dimension of the next contraction, tokens 8*nt + ..)
+// into this lane's fragment entry: lane = 2*n + run holds rows r0 + 8*run ..
+// + 7 of token n (n < 8*NT). Returns the 8 values in e[].
+template <int NT>
+LMOE_DEV void acc_to_entry(const float acc[NT][4], float e[8]) {
+  const int lane = threadIdx.x & 31, run = lane & 1, n = lane >> 1;
+  const int want = run * 2 + (n & 1), src_t = (n & 7) >> 1, want_nt = n >> 3;
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    float v = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const float x = __shfl_sync(0xffffffffu, acc[nt][h], g * 4 + src_t);
+        if (nt == want_nt && h == want) v = x;
+      }
+    e[g] = v;
+  }
+}
+
+}  // namespace lmoe

@@ -211,3 +211,23 @@ def test_fused_timeout_path_reports_and_recovers(cuda_device):
     y = bf16_bits(m.forward(xt))
     m.check()
     check_outputs(y, y_ref, "after timeout")
+
+
+@pytest.mark.parametrize("T", [1, 3, 9, 16])
+def test_fused_decode_ragged_T(T, cuda_device):
+    """The single persistent kernel at token counts that leave ragged token
+    tiles (one and two 8-token tiles), against the oracle."""
+    from sparse_latent_moe_lmoe_b300 import LatentMoE, capi
+    sh, _, W, _x, Ly, _y, _i, _w, _l = workload("decode_t8")
+    x = S.make_x(T, sh.d, 40 + T)
+    y_ref, idx_ref, w_ref, lg_ref = O.layer_forward(Ly, x)
+    m = LatentMoE(sh, W, device=0)
+    assert capi.lmoe_stage_name(m.h, T, 0)[0] == "decode_fused"
+    xt = bf16_tensor(x, cuda_device)
+    idx, w, lg = m.route(xt, want_logits=True)
+    got = bf16_bits(m.forward(xt))
+    m.check()
+    from gpu_util import ambiguous_rows
+    keep = ~ambiguous_rows(lg_ref, sh.k, 1e-5 * np.abs(lg_ref).max(axis=1))
+    mr, ma, _ = check_outputs(got[keep], y_ref[keep], f"fused T={T}")
+    print(f"fused T={T}: mean rel {mr:.2e} max abs {ma:.2e}")
