@@ -112,14 +112,13 @@ LMOE_DEV float route_weight(const Tables& tb, int t, int e, int k) {
 
 // Counter layout (one copy; two copies alternate between launches).
 struct CtrMap {
-  int tk_router, done_router, done_topk, tk_win, done_in, done_gu, tk_down, done_down, tk_wout, n;
+  int tk_router, done_router, tk_win, done_in, done_gu, tk_down, done_down, tk_wout, n;
 };
 __host__ __device__ inline CtrMap ctr_map(int d, int E, int G, int L) {
   CtrMap m;
   int o = 0;
   m.tk_router = o; o += E / 2;
   m.done_router = o; o += 1;
-  m.done_topk = o; o += 1;
   m.tk_win = o; o += G * (L / 16);
   m.done_in = o; o += G;
   m.done_gu = o; o += MAX_ACT;
@@ -327,81 +326,43 @@ LMOE_COLD float2 topk_warp(const float* row, int E, int k) {
   return make_float2(__int_as_float(sel_e), sel_w);
 }
 
-// Routing tables of the pass from the published top-k (one warp).
-LMOE_COLD void build_tables(Tables& tb, const int32_t* gidx, const float* gw, int T, int k, int E, int G, int epg,
-                            unsigned* err) {
+// Routed-expert and routed-group tables from the token masks (one warp):
+// elist = routed experts ascending, glist = their groups, gslot0[gi] = first
+// slot of group gi in elist (gslot0[n_actg] = n_act).
+LMOE_COLD void build_tables(Tables& tb, int E, int epg) {
   const int lane = threadIdx.x & 31;
-    #pragma unroll 1
-    for (int i = lane; i < T * k; i += 32) {
-      const int t = i / k, jj = i % k;
-      int e = __ldcg(gidx + i);
-      if (e < 0 || e >= E) {
-        set_error(err, ERRBIT_BAD_INDEX);
-        e = 0;
-      }
-      tb.idx[t * 16 + jj] = e;
-      tb.w[t * 16 + jj] = __ldcg(gw + i);
+  int base = 0;
+#pragma unroll 1
+  for (int e0 = 0; e0 < E; e0 += 32) {
+    const int e = e0 + lane;
+    const bool on = e < E && tb.emask[e] != 0;
+    const unsigned bal = __ballot_sync(0xffffffffu, on);
+    if (on) tb.elist[base + __popc(bal & ((1u << lane) - 1u))] = (int16_t)e;
+    base += __popc(bal);
+  }
+  __syncwarp();
+  const int n_act = base;
+  int ng = 0;
+#pragma unroll 1
+  for (int i0 = 0; i0 < n_act; i0 += 32) {
+    const int i = i0 + lane;
+    const int g = i < n_act ? tb.elist[i] / epg : -1;
+    const int gp = (i > 0 && i < n_act) ? tb.elist[i - 1] / epg : -1;
+    const bool first = i < n_act && g != gp;
+    const unsigned bal = __ballot_sync(0xffffffffu, first);
+    if (first) {
+      const int gi = ng + __popc(bal & ((1u << lane) - 1u));
+      tb.glist[gi] = (int16_t)g;
+      tb.gslot0[gi] = (int16_t)i;
     }
-    #pragma unroll 1
-    for (int e = lane; e < E; e += 32) tb.emask[e] = 0;
-    __syncwarp();
-    #pragma unroll 1
-    for (int i = lane; i < T * k; i += 32) {
-      const int t = i / k, e = tb.idx[t * 16 + i % k];
-      atomicOr(reinterpret_cast<unsigned*>(&tb.emask[0]) + (e >> 1), (1u << t) << ((e & 1) * 16));
-    }
-    __syncwarp();
-    {  // ascending compaction of routed experts
-      int base = 0;
-      #pragma unroll 1
-      for (int e0 = 0; e0 < E; e0 += 32) {
-        const int e = e0 + lane;
-        const bool on = e < E && tb.emask[e] != 0;
-        const unsigned bal = __ballot_sync(0xffffffffu, on);
-        const int pos = base + __popc(bal & ((1u << lane) - 1u));
-        if (on) tb.elist[pos] = (int16_t)e;
-        base += __popc(bal);
-      }
-      if (lane == 0) tb.n_act = base;
-    }
-    __syncwarp();
-    {  // routed groups and their first expert slots
-      int cnt0 = 0, cnt1 = 0;  // groups lane and lane + 32
-      if (lane < G)
-        #pragma unroll 1
-        for (int e = lane * epg; e < (lane + 1) * epg; ++e) cnt0 += tb.emask[e] != 0;
-      if (lane + 32 < G)
-        #pragma unroll 1
-        for (int e = (lane + 32) * epg; e < (lane + 33) * epg; ++e) cnt1 += tb.emask[e] != 0;
-      int inc0 = cnt0, inc1 = cnt1;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int a0 = __shfl_up_sync(0xffffffffu, inc0, o), a1 = __shfl_up_sync(0xffffffffu, inc1, o);
-        if (lane >= o) {
-          inc0 += a0;
-          inc1 += a1;
-        }
-      }
-      const int tot0 = __shfl_sync(0xffffffffu, inc0, 31);
-      const unsigned b0 = __ballot_sync(0xffffffffu, cnt0 > 0), b1 = __ballot_sync(0xffffffffu, cnt1 > 0);
-      const int n0 = __popc(b0);
-      if (cnt0 > 0) {
-        const int gi = __popc(b0 & ((1u << lane) - 1u));
-        tb.glist[gi] = (int16_t)lane;
-        tb.gslot0[gi] = (int16_t)(inc0 - cnt0);
-      }
-      if (cnt1 > 0) {
-        const int gi = n0 + __popc(b1 & ((1u << lane) - 1u));
-        tb.glist[gi] = (int16_t)(lane + 32);
-        tb.gslot0[gi] = (int16_t)(tot0 + inc1 - cnt1);
-      }
-      const int ng = n0 + __popc(b1);
-      __syncwarp();
-      if (lane == 0) {
-        tb.gslot0[ng] = (int16_t)tb.n_act;
-        tb.n_actg = ng;
-      }
-    }
+    ng += __popc(bal);
+  }
+  if (lane == 0) {
+    tb.n_act = n_act;
+    tb.n_actg = ng;
+    tb.gslot0[ng] = (int16_t)n_act;
+  }
+  __syncwarp();
 }
 
 template <int NT>
@@ -472,29 +433,21 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
     }
     ok = __shfl_sync(0xffffffffu, ok, 0);
     j = __shfl_sync(0xffffffffu, j, 0);
-    // the top-k of token c, published for every CTA
-    if (c < T) {
-      if (lane == 0) wait_count(ctr + cm.done_router, (unsigned)NPAIR, budget, err);
-      __syncwarp();
-      const float2 sw = topk_warp(F.logits + (size_t)c * E, E, k);
-      const int sel_e = __float_as_int(sw.x);
-      const float sel_w = sw.y;
-      if (lane < k) {
-        A.idx[c * k + lane] = sel_e;
-        A.w[c * k + lane] = sel_w;
+    // routing tables (built by the consumers)
+    if (lane == 0 && ok) {
+      const long long t0 = clock64();
+#pragma unroll 1
+      while (tb.tables_ready == 0) {
+        if (clock64() - t0 > budget) {
+          set_error(err, ERRBIT_TIMEOUT);
+          ok = false;
+          break;
+        }
+        __nanosleep(64);
       }
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) atomicAdd(ctr + cm.done_topk, 1u);
-    }
-    // routing tables, built by this warp
-    if (lane == 0) wait_count(ctr + cm.done_topk, (unsigned)T, budget, err);
-    __syncwarp();
-    build_tables(tb, A.idx, A.w, T, k, E, G, epg, err);
-    __syncwarp();
-    if (lane == 0) {
       __threadfence_block();
-      tb.tables_ready = 1;
+    }
+    if (lane == 0) {
       const int n_act = tb.n_act, n_actg = tb.n_actg;
       int lo = 0, hi = 0;
       if (ok) split(n_act * (f / 16), c, nC, lo, hi);
@@ -676,20 +629,37 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
   }
   jbase += nA2;
 
-  // ---------------------------------------------------- routing tables ready
-  if (ctid == 0) {
-    const long long t0 = clock64();
-    #pragma unroll 1
-    while (tb.tables_ready == 0) {
-      if (clock64() - t0 > budget) {
-        set_error(err, ERRBIT_TIMEOUT);
-        break;
+  // ------------------------------------------------------------ routing
+  // every CTA: top-k of each token (one warp per token), then the tables
+  cons_sync();
+  if (ctid == 0) wait_count(ctr + cm.done_router, (unsigned)NPAIR, budget, err);
+  cons_sync();
+#pragma unroll 1
+  for (int tw = warp; tw < T; tw += NCW) {
+    const float2 sw = topk_warp(F.logits + (size_t)tw * E, E, k);
+    if (lane < k) {
+      tb.idx[tw * 16 + lane] = __float_as_int(sw.x);
+      tb.w[tw * 16 + lane] = sw.y;
+      if (c == 0) {
+        A.idx[tw * k + lane] = __float_as_int(sw.x);
+        A.w[tw * k + lane] = sw.y;
       }
-      __nanosleep(64);
     }
-    __threadfence_block();
+  }
+#pragma unroll 1
+  for (int e = ctid; e < E; e += NCT) tb.emask[e] = 0;
+  cons_sync();
+  if (ctid < T * k) {
+    const int t = ctid / k, e = tb.idx[t * 16 + ctid % k];
+    atomicOr(reinterpret_cast<unsigned*>(&tb.emask[0]) + (e >> 1), (1u << t) << ((e & 1) * 16));
   }
   cons_sync();
+  if (warp == 0) build_tables(tb, E, epg);
+  cons_sync();
+  if (ctid == 0) {
+    __threadfence_block();
+    tb.tables_ready = 1;
+  }
   const int n_act = tb.n_act, n_actg = tb.n_actg;
 
   // ------------------------------------------------------------ B gate/up
