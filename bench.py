@@ -171,6 +171,7 @@ def stage_flops(sh, T, idx):
     f["wout"] = 2.0 * sh.L * sh.d * rows
     f["permute"] = 0.0
     f["zreduce"] = 0.0
+    f["dequant"] = 0.0
     return f, rows
 
 
@@ -278,7 +279,7 @@ def run_ours(args):
     idx_np = idx.cpu().numpy()
     sb = stage_bytes(sh, T, idx_np)
     n_kernels = capi.lmoe_stage_name(layers[0].h, T, 0)[1]
-    prefill = capi.lmoe_stage_name(layers[0].h, T, 2)[0] == "win"
+    prefill = capi.lmoe_stage_name(layers[0].h, T, 1)[0] == "permute"
 
     # one CUDA graph per weight copy: a replay launches the whole layer
     for i, m in enumerate(layers):

@@ -35,6 +35,7 @@
 #include "common.cuh"
 #include "decode.cuh"
 #include "ring.cuh"
+#include "tmap.cuh"
 
 namespace lmoe {
 
@@ -869,57 +870,34 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
 size_t fused_counter_words(int d, int E, int G, int L) { return 2 * (size_t)ctr_map(d, E, G, L).n; }
 
 namespace {
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-    cudaGetLastError();
-  }
-  return fn;
-}
-
 // packed int4 [rows][K/2] as [rows][K/256][128 B], box {128, lines, box_rows}
 bool map_q(CUtensorMap* m, const uint8_t* q, long long rows, int K, int lines, int box_rows) {
   const cuuint64_t dims[3] = {128, (cuuint64_t)(K / 256), (cuuint64_t)rows};
   const cuuint64_t strides[2] = {128, (cuuint64_t)(K / 2)};
-  const cuuint32_t box[3] = {128, (cuuint32_t)lines, (cuuint32_t)box_rows}, es[3] = {1, 1, 1};
-  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(q), dims, strides, box, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const cuuint32_t box[3] = {128, (cuuint32_t)lines, (cuuint32_t)box_rows};
+  return tmap_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, q, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // bf16 scales [rows][K/32], box {box_cols, box_rows}
 bool map_s(CUtensorMap* m, const uint16_t* s, long long rows, int K, int box_cols, int box_rows) {
   const cuuint64_t dims[2] = {(cuuint64_t)(K / 32), (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)(K / 32 * 2)};
-  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows}, es[2] = {1, 1};
-  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(s), dims, strides, box, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  return tmap_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, s, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 }  // namespace
 
 bool fused_make_maps(const DecodeArgs& A, DecodeMaps* mp) {
-  if (!encode_fn() || !A.W_r) return false;
+  if (!tmap_encode_fn() || !A.W_r) return false;
   const int d = A.d, E = A.E, G = A.G, L = A.L, f = A.f;
   if (d % KSEG != 0 || L % 256 != 0 || f % 256 != 0) return false;
   bool ok = true;
   {
     const cuuint64_t dims[3] = {256, (cuuint64_t)(d / 256), (cuuint64_t)E};
     const cuuint64_t strides[2] = {1024, (cuuint64_t)d * 4};
-    const cuuint32_t box[3] = {256, KSEG / 256, 2}, es[3] = {1, 1, 1};
-    ok = ok && encode_fn()(&mp->wr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(A.W_r), dims, strides, box,
-                           es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const cuuint32_t box[3] = {256, KSEG / 256, 2};
+    ok = ok && tmap_encode(&mp->wr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, A.W_r, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_NONE);
   }
   ok = ok && map_q(&mp->win_q, A.W_in_q, (long long)G * L, d, KSEG / 256, 16);
   ok = ok && map_s(&mp->win_s, A.W_in_s, (long long)G * L, d, KSEG / 32, 16);

@@ -1,6 +1,10 @@
 // Prefill path of the latent MoE layer (many tokens): the router and every
-// projection are GEMMs on the tcgen05 tensor cores (tc_gemm.cuh), with the
-// int4 weights dequantised to fp16 by the GEMM's own producer warps.
+// projection are GEMMs on the tcgen05 tensor cores (tc_gemm.cuh). The two
+// shared matrices, which every token tile of a group multiplies, are
+// dequantised to fp16 once per call and fed to the tensor cores by TMA; the
+// per-expert int4 weights are dequantised by the GEMM's own producer warps.
+//
+//   dequant  Win, Wout -> fp16 (q*s is exact in fp16), x -> fp16
 //
 //   route    logits = x . (W_hi + W_mid + W_lo)^T  (W_r split into three
 //            bf16 terms at create time; x is exact in bf16; fp32 accumulate)
@@ -22,6 +26,7 @@
 #include "common.cuh"
 #include "prefill.cuh"
 #include "tc_gemm.cuh"
+#include "tmap.cuh"
 
 namespace lmoe {
 
@@ -108,7 +113,7 @@ struct ProbRoute : ProbBase {
   int32_t* idx;
   float* w;
   float* logits;          // [T][E] or null
-  LMOE_DEV void init(int*) {}
+  LMOE_DEV void init(int*) const {}
   LMOE_DEV int num_tiles(const int*) const { return (T + 127) / 128; }
   LMOE_DEV Tile tile(const int*, int t) const {
     Tile tl;
@@ -199,16 +204,15 @@ struct ProbRoute : ProbBase {
 
 // -------------------------------------------------------------------- W_in
 struct ProbWin : ProbBase {
-  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 1, B_MODE = 0, STAGES = 4;
-  const uint16_t* x;  // [T][d] bf16
+  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 0, B_MODE = 2, STAGES = 3;
+  CUtensorMap bm;      // Win in fp16 as [G][L][d], box {64, 256, 1}
+  const __half* x16;   // [T][d] fp16
   int d, L, G;
   const int32_t* gto;
   const int32_t* gtok;
-  const uint8_t* Wq;
-  const uint16_t* Ws;
   __half* H;  // [rows][L]
   LMOE_DEV int ntn() const { return L / 256; }
-  LMOE_DEV void init(int* sc) {
+  LMOE_DEV void init(int* sc) const {
     tile_prefix(sc, G, [&](int g) { return ((gto[g + 1] - gto[g] + 127) / 128) * ntn(); });
   }
   LMOE_DEV int num_tiles(const int* sc) const { return sc[G]; }
@@ -224,14 +228,15 @@ struct ProbWin : ProbBase {
   }
   LMOE_DEV const void* a_row(const int*, const Tile& tl, int r, int kb) const {
     const int tok = gtok[gto[tl.prob] + tl.m0 + r];
-    return x + (size_t)tok * d + kb * 64;
+    return x16 + (size_t)tok * d + kb * 64;
   }
-  LMOE_DEV bool b_row(const int*, const Tile& tl, int n, int kb, const uint8_t*& q, const uint16_t*& s) const {
-    const size_t row = (size_t)tl.prob * L + tl.n0 + n;
-    q = Wq + row * (d / 2) + kb * 32;
-    s = Ws + row * (d / 32) + kb * 2;
-    return true;
+  LMOE_DEV const CUtensorMap* bmap() const { return &bm; }
+  LMOE_DEV void b_coords(const Tile& tl, int kb, int& c0, int& c1, int& c2) const {
+    c0 = kb * 64;
+    c1 = tl.n0;
+    c2 = tl.prob;
   }
+  LMOE_DEV bool b_row(const int*, const Tile&, int, int, const uint8_t*&, const uint16_t*&) const { return false; }
   LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int, int) const { return nullptr; }
   LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
     mma_k4(d_tmem, da, db, tc::idesc(128, 256, 0), kb);
@@ -257,7 +262,7 @@ struct ProbGateUp : ProbBase {
   const uint16_t *gs, *us;
   __half* V;  // [T*k][f]
   LMOE_DEV int ntn() const { return f / 128; }
-  LMOE_DEV void init(int* sc) {
+  LMOE_DEV void init(int* sc) const {
     tile_prefix(sc, E, [&](int e) { return ((eo[e + 1] - eo[e] + 127) / 128) * ntn(); });
   }
   LMOE_DEV int num_tiles(const int* sc) const { return sc[E]; }
@@ -310,7 +315,7 @@ struct ProbDown : ProbBase {
   const uint16_t* ds;
   float* U;  // [T*k][L]
   LMOE_DEV int ntn() const { return L / 256; }
-  LMOE_DEV void init(int* sc) {
+  LMOE_DEV void init(int* sc) const {
     tile_prefix(sc, E, [&](int e) { return ((eo[e + 1] - eo[e] + 127) / 128) * ntn(); });
   }
   LMOE_DEV int num_tiles(const int* sc) const { return sc[E]; }
@@ -356,19 +361,18 @@ struct ProbDown : ProbBase {
 // mode 0: y_t = sum_g Wout[g] Z[(g,t)] (+ residual), tiles over tokens, K = G*L
 // mode 1: Y[(g,t)] = Wout[g] Z[(g,t)] (fp32 rows), tiles over group rows
 struct ProbWout : ProbBase {
-  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 0, B_MODE = 0, STAGES = 4;
+  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 0, B_MODE = 2, STAGES = 3;
+  CUtensorMap bm;         // Wout in fp16 as [G][d][L], box {64, 256, 1}
   const __half* Z;        // [rows][L]
   const int32_t* tokrow;  // [T][G]: row of (g, t) in Z or -1
   const int32_t* gto;
   int T, d, L, G, mode;
-  const uint8_t* Wq;
-  const uint16_t* Ws;
   const uint16_t* residual;
   uint16_t* y;  // [T][d] bf16 (mode 0)
   float* Y;     // [rows][d] (mode 1)
   LMOE_DEV int ntn() const { return d / 256; }
   LMOE_DEV int kpg() const { return L / 64; }
-  LMOE_DEV void init(int* sc) {
+  LMOE_DEV void init(int* sc) const {
     if (mode == 1) tile_prefix(sc, G, [&](int g) { return ((gto[g + 1] - gto[g] + 127) / 128) * ntn(); });
   }
   LMOE_DEV int num_tiles(const int* sc) const { return mode == 0 ? ((T + 127) / 128) * ntn() : sc[G]; }
@@ -398,13 +402,13 @@ struct ProbWout : ProbBase {
     }
     return Z + (size_t)(gto[tl.prob] + tl.m0 + r) * L + kb * 64;
   }
-  LMOE_DEV bool b_row(const int*, const Tile& tl, int n, int kb, const uint8_t*& q, const uint16_t*& s) const {
-    const int g = mode == 0 ? kb / kpg() : tl.prob, kk = mode == 0 ? kb % kpg() : kb;
-    const size_t row = (size_t)g * d + tl.n0 + n;
-    q = Wq + row * (L / 2) + kk * 32;
-    s = Ws + row * (L / 32) + kk * 2;
-    return true;
+  LMOE_DEV const CUtensorMap* bmap() const { return &bm; }
+  LMOE_DEV void b_coords(const Tile& tl, int kb, int& c0, int& c1, int& c2) const {
+    c2 = mode == 0 ? kb / kpg() : tl.prob;
+    c0 = (mode == 0 ? kb % kpg() : kb) * 64;
+    c1 = tl.n0;
   }
+  LMOE_DEV bool b_row(const int*, const Tile&, int, int, const uint8_t*&, const uint16_t*&) const { return false; }
   LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int, int) const { return nullptr; }
   LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
     mma_k4(d_tmem, da, db, tc::idesc(128, 256, 0), kb);
@@ -492,6 +496,34 @@ cudaError_t launch_split_router(const float* W_r, int E, int d, uint16_t* out, c
   return cudaGetLastError();
 }
 
+// int4 rows [rows][K/2] + bf16 scales [rows][K/32] -> fp16 [rows][K]; one
+// 32-bit word (8 elements, natural order) per thread and step
+__global__ void dequant_f16_kernel(const uint8_t* __restrict__ q, const uint16_t* __restrict__ s, size_t words, int K,
+                                   __half* __restrict__ out) {
+  const int wpr = K / 8;  // words per row
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < words; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t row = i / wpr;
+    const int wi = (int)(i % wpr);
+    const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(q) + i);
+    const __half2 s2 = scale_h2(__ldg(s + row * (K / 32) + wi / 4));
+    uint32_t o[4];
+    tc::dequant_word_natural(v, s2, o);
+    reinterpret_cast<uint4*>(out)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// bf16 -> fp16, 8 elements per thread and step
+__global__ void bf16_to_f16_kernel(const uint16_t* __restrict__ x, size_t n8, __half* __restrict__ out) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(x) + i);
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    uint32_t h[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) h[j] = pack_half2(__uint_as_float(u[j] << 16), __uint_as_float(u[j] & 0xffff0000u));
+    reinterpret_cast<uint4*>(out)[i] = make_uint4(h[0], h[1], h[2], h[3]);
+  }
+}
+
 // ------------------------------------------------------------------ host side
 
 namespace {
@@ -500,7 +532,7 @@ constexpr size_t kAl = 256;
 size_t al(size_t v) { return (v + kAl - 1) & ~(kAl - 1); }
 
 struct PWs {
-  size_t idx, w, eo, sa, inv, go, gto, gt, ar, perm_scratch, H, V, U, Z, tokrow, end;
+  size_t idx, w, eo, sa, inv, go, gto, gt, ar, perm_scratch, H, V, U, Z, tokrow, x16, win16, wout16, end;
 };
 
 PWs pws(const PrefillArgs& P, int T) {
@@ -527,6 +559,9 @@ PWs pws(const PrefillArgs& P, int T) {
   m.U = take(n * P.L * 4);
   m.Z = take(gk * P.L * 2);
   m.tokrow = take((size_t)T * P.G * 4);
+  m.x16 = take((size_t)T * P.d * 2);
+  m.win16 = take((size_t)P.G * P.L * P.d * 2);
+  m.wout16 = take((size_t)P.G * P.d * P.L * 2);
   m.end = o;
   return m;
 }
@@ -592,12 +627,31 @@ cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_
   float* U = reinterpret_cast<float*>(b + m.U);
   __half* Z = reinterpret_cast<__half*>(b + m.Z);
   int32_t* tokrow = reinterpret_cast<int32_t*>(b + m.tokrow);
+  __half* x16 = reinterpret_cast<__half*>(b + m.x16);
+  __half* win16 = reinterpret_cast<__half*>(b + m.win16);
+  __half* wout16 = reinterpret_cast<__half*>(b + m.wout16);
   cudaError_t e;
+  {  // the shared matrices and x in fp16, once per call
+    if (hook) hook->before(st);
+    const size_t wwords = (size_t)P.G * P.L * P.d / 8;
+    dequant_f16_kernel<<<4 * grid, 256, 0, st>>>(P.W_in_q, P.W_in_s, wwords, P.d, win16);
+    dequant_f16_kernel<<<4 * grid, 256, 0, st>>>(P.W_out_q, P.W_out_s, wwords, P.L, wout16);
+    bf16_to_f16_kernel<<<4 * grid, 256, 0, st>>>(x, (size_t)T * P.d / 8, x16);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (hook) hook->after(st);
+  }
   {
     ProbWin p;
     static_cast<ProbBase&>(p) = base(P);
-    p.x = x; p.d = P.d; p.L = P.L; p.G = P.G; p.gto = pm.group_tok_offsets; p.gtok = pm.group_tokens;
-    p.Wq = P.W_in_q; p.Ws = P.W_in_s; p.H = H;
+    {
+      const cuuint64_t dims[3] = {(cuuint64_t)P.d, (cuuint64_t)P.L, (cuuint64_t)P.G};
+      const cuuint64_t strides[2] = {(cuuint64_t)P.d * 2, (cuuint64_t)P.L * P.d * 2};
+      const cuuint32_t box[3] = {64, 256, 1};
+      if (!tmap_encode(&p.bm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, win16, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    }
+    p.x16 = x16; p.d = P.d; p.L = P.L; p.G = P.G; p.gto = pm.group_tok_offsets; p.gtok = pm.group_tokens;
+    p.H = H;
     if (hook) hook->before(st);
     if ((e = run_gemm(p, grid, st)) != cudaSuccess) return e;
     if (hook) hook->after(st);
@@ -632,8 +686,16 @@ cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_
   {
     ProbWout p;
     static_cast<ProbBase&>(p) = base(P);
+    {
+      const cuuint64_t dims[3] = {(cuuint64_t)P.L, (cuuint64_t)P.d, (cuuint64_t)P.G};
+      const cuuint64_t strides[2] = {(cuuint64_t)P.L * 2, (cuuint64_t)P.d * P.L * 2};
+      const cuuint32_t box[3] = {64, 256, 1};
+      if (!tmap_encode(&p.bm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, wout16, dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    }
     p.Z = Z; p.tokrow = tokrow; p.gto = pm.group_tok_offsets; p.T = T; p.d = P.d; p.L = P.L; p.G = P.G; p.mode = mode;
-    p.Wq = P.W_out_q; p.Ws = P.W_out_s; p.residual = residual; p.y = y; p.Y = Yrows;
+    p.residual = residual; p.y = y; p.Y = Yrows;
     if (hook) hook->before(st);
     if ((e = run_gemm(p, grid, st)) != cudaSuccess) return e;
     if (hook) hook->after(st);
@@ -707,9 +769,9 @@ cudaError_t launch_prefill_layer(const PrefillArgs& P, const uint16_t* x, int T,
 }
 
 const char* prefill_stage_name(const PrefillArgs&, int, int i, int* count) {
-  static const char* names[] = {"route", "permute", "win", "gateup", "down", "zreduce", "wout"};
-  if (count) *count = 7;
-  return (i >= 0 && i < 7) ? names[i] : "";
+  static const char* names[] = {"route", "permute", "dequant", "win", "gateup", "down", "zreduce", "wout"};
+  if (count) *count = 8;
+  return (i >= 0 && i < 8) ? names[i] : "";
 }
 
 }  // namespace lmoe

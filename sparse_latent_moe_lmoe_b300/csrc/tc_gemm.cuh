@@ -16,6 +16,7 @@
 // word and the wait gives up (the output is then invalid).
 #pragma once
 #include "common.cuh"
+#include "ring.cuh"
 
 namespace lmoe {
 namespace tc {
@@ -104,10 +105,11 @@ struct Shared {
   int scratch[1024 + 64];  // problem-specific (tile prefix sums)
 };
 
-// B_MODE 0: int4 + bf16 scales dequantised by the producers; 1: bf16 rows copied
+// B_MODE 0: int4 + bf16 scales dequantised by the producers; 1: bf16 rows copied;
+//         2: fp16 rows by one TMA box {64, BN} per stage (128-byte swizzle)
 // A_MODE 0: fp16 rows by cp.async; 1: bf16 rows converted to fp16; 2: bf16 rows by cp.async
 template <class P>
-__global__ void __launch_bounds__(THREADS, 1) gemm_kernel(P prob) {
+__global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant__ P prob) {
   extern __shared__ __align__(1024) unsigned char dyn[];
   __shared__ Shared sh;
   constexpr int BN = P::BN;                      // B rows per stage (<= 256)
@@ -125,7 +127,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(P prob) {
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&sh.full[s], NPROD_WARPS * 32);
+      mbar_init(&sh.full[s], NPROD_WARPS * 32 + (P::B_MODE == 2 ? 1 : 0));
       mbar_init(&sh.empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -146,7 +148,72 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(P prob) {
   const uint32_t tmem = sh.tmem_base;
   const int ntiles = prob.num_tiles(sh.scratch);
 
+  constexpr bool ASYNC = P::A_MODE != 1 && P::B_MODE != 0;
   if (warp < NPROD_WARPS) {
+   if constexpr (ASYNC) {
+    // ------------------------------------------------ producers, all copies asynchronous
+    // A rows by cp.async (gathered through the problem's row map), B by TMA
+    // (B_MODE 2, thread 0) or cp.async (B_MODE 1); STAGES-1 K blocks ahead.
+    const int pt = tid;  // 0..255
+    const int ar = pt >> 1, ac0 = (pt & 1) * 4;
+    constexpr int LA = STAGES - 1;
+    int t_i = blockIdx.x, kb_i = 0;
+    Tile tl_i = t_i < ntiles ? prob.tile(sh.scratch, t_i) : Tile{};
+    int issued = 0, done = 0;
+    auto issue_next = [&]() {
+      const int kiter = issued, s = kiter % STAGES, use = kiter / STAGES;
+      if (use > 0) mbar_wait(&sh.empty[s], (use - 1) & 1, budget, err);
+      unsigned char* sa = base + s * STAGE_BYTES;
+      unsigned char* sb = sa + A_BYTES;
+      const void* src = ar < tl_i.rows ? prob.a_row(sh.scratch, tl_i, ar, kb_i) : nullptr;
+      if (src) {
+        const char* s1 = reinterpret_cast<const char*>(src);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) cp16(sa + swz(ar, ac0 + c), s1 + (ac0 + c) * 16, true);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(sa + swz(ar, ac0 + c)) = make_uint4(0, 0, 0, 0);
+      }
+      if constexpr (P::B_MODE == 2) {
+        if (pt == 0) {
+          int c0, c1, c2;
+          prob.b_coords(tl_i, kb_i, c0, c1, c2);
+          mbar_expect_tx(&sh.full[s], (uint32_t)B_BYTES);
+          tma_load_3d(sb, prob.bmap(), c0, c1, c2, &sh.full[s]);
+        }
+      } else {
+        for (int n = pt; n < BN; n += NPROD_WARPS * 32) {
+          const uint16_t* bsrc = prob.b_row_bf16(sh.scratch, tl_i, n, kb_i);
+          if (bsrc) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) cp16(sb + swz(n, c), bsrc + c * 8, true);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(sb + swz(n, c)) = make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      ++issued;
+      if (++kb_i == tl_i.nkb) {
+        kb_i = 0;
+        t_i += gridDim.x;
+        if (t_i < ntiles) tl_i = prob.tile(sh.scratch, t_i);
+      }
+    };
+    while (issued < LA && t_i < ntiles) issue_next();
+    while (done < issued) {
+      if (t_i < ntiles) {
+        issue_next();
+        asm volatile("cp.async.wait_group %0;" ::"n"(LA) : "memory");
+      } else {
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+      }
+      fence_async_smem();
+      mbar_arrive(&sh.full[done % STAGES]);
+      ++done;
+    }
+   } else {
     // ---------------------------------------------------------------- producers
     // One K block ahead: while K block i is converted into its stage, the
     // global loads (cp.async for fp16 A rows, registers for int4 / bf16 data)
@@ -267,6 +334,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(P prob) {
       kb_cur = kb_n;
       tl_cur = tl_n;
     }
+   }
   } else if (warp == MMA_WARP) {
     // -------------------------------------------------------------- MMA issue
     if (lane == 0) {

@@ -30,7 +30,7 @@ def test_small_layer_prefill_full_oracle(cuda_device):
     x = S.make_x(T, sh.d, 12)
     y_ref, idx_ref, w_ref, lg_ref = O.layer_forward(O.Layer(sh, W), x)
     m = make(sh, W, capi.PATH_PREFILL)
-    assert capi.lmoe_stage_name(m.h, T, 2)[0] == "win"
+    assert capi.lmoe_stage_name(m.h, T, 1)[0] == "permute"
     xt = bf16_tensor(x, cuda_device)
     idx, w, lg = m.route(xt, want_logits=True)
     torch.cuda.synchronize()
