@@ -105,9 +105,9 @@ LMOE_DEV void store_half16(__half* dst, const float v[16]) {
 
 // ------------------------------------------------------------------ router
 struct ProbRoute : ProbBase {
-  static constexpr int BN = 512, ACC_COLS = 512, A_MODE = 2, B_MODE = 1, STAGES = 2;
-  const uint16_t* x;      // [T][d] bf16
-  const uint16_t* wsplit; // [3][E][d] bf16
+  static constexpr int BN = 512, ACC_COLS = 512, A_MODE = 3, B_MODE = 2, STAGES = 2;
+  CUtensorMap am;         // x as [T][d] bf16, box {64, 128}
+  CUtensorMap bm;         // the split W_r as [3][E][d] bf16, box {64, 256, 1}
   const float* bias;      // [E] or null
   int T, d, E, k;
   int32_t* idx;
@@ -124,13 +124,17 @@ struct ProbRoute : ProbBase {
     tl.nkb = 3 * (d / 64);
     return tl;
   }
-  LMOE_DEV const void* a_row(const int*, const Tile& tl, int r, int kb) const {
-    return x + (size_t)(tl.m0 + r) * d + (kb / 3) * 64;
+  // K block kb: bf16 term kb % 3 of W_r against x's K block kb / 3 (rows
+  // beyond T or E read as zero)
+  LMOE_DEV void load_a(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
+    tma_load_2d(dst, &am, (kb / 3) * 64, tl.m0, bar);
   }
-  LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int n, int kb) const {
-    if (n >= E) return nullptr;
-    return wsplit + ((size_t)(kb % 3) * E + n) * d + (kb / 3) * 64;
+  LMOE_DEV void load_b(const Tile&, int kb, void* dst, uint64_t* bar) const {
+    tma_load_3d(dst, &bm, (kb / 3) * 64, 0, kb % 3, bar);
+    tma_load_3d(static_cast<char*>(dst) + 256 * 128, &bm, (kb / 3) * 64, 256, kb % 3, bar);
   }
+  LMOE_DEV const void* a_row(const int*, const Tile&, int, int) const { return nullptr; }
+  LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int, int) const { return nullptr; }
   LMOE_DEV bool b_row(const int*, const Tile&, int, int, const uint8_t*&, const uint16_t*&) const { return false; }
   LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
     const uint32_t id = tc::idesc(128, 256, 1);
@@ -230,11 +234,8 @@ struct ProbWin : ProbBase {
     const int tok = gtok[gto[tl.prob] + tl.m0 + r];
     return x16 + (size_t)tok * d + kb * 64;
   }
-  LMOE_DEV const CUtensorMap* bmap() const { return &bm; }
-  LMOE_DEV void b_coords(const Tile& tl, int kb, int& c0, int& c1, int& c2) const {
-    c0 = kb * 64;
-    c1 = tl.n0;
-    c2 = tl.prob;
+  LMOE_DEV void load_b(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
+    tma_load_3d(dst, &bm, kb * 64, tl.n0, tl.prob, bar);
   }
   LMOE_DEV bool b_row(const int*, const Tile&, int, int, const uint8_t*&, const uint16_t*&) const { return false; }
   LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int, int) const { return nullptr; }
@@ -252,14 +253,13 @@ struct ProbWin : ProbBase {
 
 // ---------------------------------------------------------------- gate/up
 struct ProbGateUp : ProbBase {
-  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 0, B_MODE = 0, STAGES = 4;
+  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 0, B_MODE = 2, STAGES = 3;
+  CUtensorMap gm, um;  // gate / up in fp16 as [E*f][L], box {64, 128}
   const __half* H;
   int L, f, E;
   const int32_t* eo;
   const int32_t* sa;
   const int32_t* arow;
-  const uint8_t *gq, *uq;
-  const uint16_t *gs, *us;
   __half* V;  // [T*k][f]
   LMOE_DEV int ntn() const { return f / 128; }
   LMOE_DEV void init(int* sc) const {
@@ -280,13 +280,12 @@ struct ProbGateUp : ProbBase {
     const int p = eo[tl.prob] + tl.m0 + r;
     return H + (size_t)arow[sa[p]] * L + kb * 64;
   }
-  LMOE_DEV bool b_row(const int*, const Tile& tl, int n, int kb, const uint8_t*& q, const uint16_t*& s) const {
-    const bool up = n >= 128;
-    const size_t row = (size_t)tl.prob * f + tl.n0 + (n & 127);
-    q = (up ? uq : gq) + row * (L / 2) + kb * 32;
-    s = (up ? us : gs) + row * (L / 32) + kb * 2;
-    return true;
+  // B rows 0..127: gate rows n0.. of expert e; 128..255: the matching up rows
+  LMOE_DEV void load_b(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
+    tma_load_2d(dst, &gm, kb * 64, tl.prob * f + tl.n0, bar);
+    tma_load_2d(static_cast<char*>(dst) + 128 * 128, &um, kb * 64, tl.prob * f + tl.n0, bar);
   }
+  LMOE_DEV bool b_row(const int*, const Tile&, int, int, const uint8_t*&, const uint16_t*&) const { return false; }
   LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int, int) const { return nullptr; }
   LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
     mma_k4(d_tmem, da, db, tc::idesc(128, 256, 0), kb);
@@ -305,14 +304,13 @@ struct ProbGateUp : ProbBase {
 
 // ------------------------------------------------------------------- down
 struct ProbDown : ProbBase {
-  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 0, B_MODE = 0, STAGES = 4;
-  const __half* V;
+  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 3, B_MODE = 2, STAGES = 4;
+  CUtensorMap am;  // V as [T*k][f] fp16, box {64, 128}
+  CUtensorMap bm;  // down in fp16 as [E*L][f], box {64, 256}
   int L, f, E;
   const int32_t* eo;
   const int32_t* sa;
   const float* wts;  // [T*k]
-  const uint8_t* dq;
-  const uint16_t* ds;
   float* U;  // [T*k][L]
   LMOE_DEV int ntn() const { return L / 256; }
   LMOE_DEV void init(int* sc) const {
@@ -329,15 +327,16 @@ struct ProbDown : ProbBase {
     tl.nkb = f / 64;
     return tl;
   }
-  LMOE_DEV const void* a_row(const int*, const Tile& tl, int r, int kb) const {
-    return V + (size_t)(eo[tl.prob] + tl.m0 + r) * f + kb * 64;
+  // A: the expert's rows of V (rows past its range belong to the next expert
+  // or read as zero; their outputs are not stored)
+  LMOE_DEV void load_a(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
+    tma_load_2d(dst, &am, kb * 64, eo[tl.prob] + tl.m0, bar);
   }
-  LMOE_DEV bool b_row(const int*, const Tile& tl, int n, int kb, const uint8_t*& q, const uint16_t*& s) const {
-    const size_t row = (size_t)tl.prob * L + tl.n0 + n;
-    q = dq + row * (f / 2) + kb * 32;
-    s = ds + row * (f / 32) + kb * 2;
-    return true;
+  LMOE_DEV void load_b(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
+    tma_load_2d(dst, &bm, kb * 64, tl.prob * L + tl.n0, bar);
   }
+  LMOE_DEV const void* a_row(const int*, const Tile&, int, int) const { return nullptr; }
+  LMOE_DEV bool b_row(const int*, const Tile&, int, int, const uint8_t*&, const uint16_t*&) const { return false; }
   LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int, int) const { return nullptr; }
   LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
     mma_k4(d_tmem, da, db, tc::idesc(128, 256, 0), kb);
@@ -402,11 +401,9 @@ struct ProbWout : ProbBase {
     }
     return Z + (size_t)(gto[tl.prob] + tl.m0 + r) * L + kb * 64;
   }
-  LMOE_DEV const CUtensorMap* bmap() const { return &bm; }
-  LMOE_DEV void b_coords(const Tile& tl, int kb, int& c0, int& c1, int& c2) const {
-    c2 = mode == 0 ? kb / kpg() : tl.prob;
-    c0 = (mode == 0 ? kb % kpg() : kb) * 64;
-    c1 = tl.n0;
+  LMOE_DEV void load_b(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
+    const int g = mode == 0 ? kb / kpg() : tl.prob;
+    tma_load_3d(dst, &bm, (mode == 0 ? kb % kpg() : kb) * 64, tl.n0, g, bar);
   }
   LMOE_DEV bool b_row(const int*, const Tile&, int, int, const uint8_t*&, const uint16_t*&) const { return false; }
   LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int, int) const { return nullptr; }
@@ -532,7 +529,8 @@ constexpr size_t kAl = 256;
 size_t al(size_t v) { return (v + kAl - 1) & ~(kAl - 1); }
 
 struct PWs {
-  size_t idx, w, eo, sa, inv, go, gto, gt, ar, perm_scratch, H, V, U, Z, tokrow, x16, win16, wout16, end;
+  size_t idx, w, eo, sa, inv, go, gto, gt, ar, perm_scratch, H, V, U, Z, tokrow, x16, win16, wout16, gate16, up16,
+      down16, end;
 };
 
 PWs pws(const PrefillArgs& P, int T) {
@@ -562,6 +560,9 @@ PWs pws(const PrefillArgs& P, int T) {
   m.x16 = take((size_t)T * P.d * 2);
   m.win16 = take((size_t)P.G * P.L * P.d * 2);
   m.wout16 = take((size_t)P.G * P.d * P.L * 2);
+  m.gate16 = take((size_t)P.E * P.f * P.L * 2);
+  m.up16 = take((size_t)P.E * P.f * P.L * 2);
+  m.down16 = take((size_t)P.E * P.L * P.f * 2);
   m.end = o;
   return m;
 }
@@ -630,6 +631,9 @@ cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_
   __half* x16 = reinterpret_cast<__half*>(b + m.x16);
   __half* win16 = reinterpret_cast<__half*>(b + m.win16);
   __half* wout16 = reinterpret_cast<__half*>(b + m.wout16);
+  __half* gate16 = reinterpret_cast<__half*>(b + m.gate16);
+  __half* up16 = reinterpret_cast<__half*>(b + m.up16);
+  __half* down16 = reinterpret_cast<__half*>(b + m.down16);
   cudaError_t e;
   {  // the shared matrices and x in fp16, once per call
     if (hook) hook->before(st);
@@ -637,6 +641,10 @@ cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_
     dequant_f16_kernel<<<4 * grid, 256, 0, st>>>(P.W_in_q, P.W_in_s, wwords, P.d, win16);
     dequant_f16_kernel<<<4 * grid, 256, 0, st>>>(P.W_out_q, P.W_out_s, wwords, P.L, wout16);
     bf16_to_f16_kernel<<<4 * grid, 256, 0, st>>>(x, (size_t)T * P.d / 8, x16);
+    const size_t ewords = (size_t)P.E * P.f * P.L / 8;
+    dequant_f16_kernel<<<4 * grid, 256, 0, st>>>(P.gate_q, P.gate_s, ewords, P.L, gate16);
+    dequant_f16_kernel<<<4 * grid, 256, 0, st>>>(P.up_q, P.up_s, ewords, P.L, up16);
+    dequant_f16_kernel<<<4 * grid, 256, 0, st>>>(P.down_q, P.down_s, ewords, P.f, down16);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (hook) hook->after(st);
   }
@@ -660,7 +668,15 @@ cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_
     ProbGateUp p;
     static_cast<ProbBase&>(p) = base(P);
     p.H = H; p.L = P.L; p.f = P.f; p.E = P.E; p.eo = pm.expert_offsets; p.sa = pm.sorted_assign; p.arow = pm.assign_row;
-    p.gq = P.gate_q; p.gs = P.gate_s; p.uq = P.up_q; p.us = P.up_s; p.V = V;
+    {
+      const cuuint64_t dims[2] = {(cuuint64_t)P.L, (cuuint64_t)P.E * P.f}, strides[1] = {(cuuint64_t)P.L * 2};
+      const cuuint32_t box[2] = {64, 128};
+      if (!tmap_encode(&p.gm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, gate16, dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !tmap_encode(&p.um, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, up16, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    }
+    p.V = V;
     if (hook) hook->before(st);
     if ((e = run_gemm(p, grid, st)) != cudaSuccess) return e;
     if (hook) hook->after(st);
@@ -668,8 +684,17 @@ cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_
   {
     ProbDown p;
     static_cast<ProbBase&>(p) = base(P);
-    p.V = V; p.L = P.L; p.f = P.f; p.E = P.E; p.eo = pm.expert_offsets; p.sa = pm.sorted_assign; p.wts = w;
-    p.dq = P.down_q; p.ds = P.down_s; p.U = U;
+    p.L = P.L; p.f = P.f; p.E = P.E; p.eo = pm.expert_offsets; p.sa = pm.sorted_assign; p.wts = w;
+    {
+      const cuuint64_t ad[2] = {(cuuint64_t)P.f, (cuuint64_t)T * P.k}, as[1] = {(cuuint64_t)P.f * 2};
+      const cuuint32_t ab[2] = {64, 128};
+      const cuuint64_t bd[2] = {(cuuint64_t)P.f, (cuuint64_t)P.E * P.L}, bs[1] = {(cuuint64_t)P.f * 2};
+      const cuuint32_t bb[2] = {64, 256};
+      if (!tmap_encode(&p.am, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, V, ad, as, ab, CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !tmap_encode(&p.bm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, down16, bd, bs, bb, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    }
+    p.U = U;
     if (hook) hook->before(st);
     if ((e = run_gemm(p, grid, st)) != cudaSuccess) return e;
     if (hook) hook->after(st);
@@ -707,7 +732,17 @@ cudaError_t route(const PrefillArgs& P, const uint16_t* x, int T, int32_t* idx, 
                   cudaStream_t st) {
   ProbRoute p;
   static_cast<ProbBase&>(p) = base(P);
-  p.x = x; p.wsplit = P.W_r_split; p.bias = P.b_r; p.T = T; p.d = P.d; p.E = P.E; p.k = P.k;
+  {
+    const cuuint64_t ad[2] = {(cuuint64_t)P.d, (cuuint64_t)T}, as[1] = {(cuuint64_t)P.d * 2};
+    const cuuint32_t ab[2] = {64, 128};
+    const cuuint64_t bd[3] = {(cuuint64_t)P.d, (cuuint64_t)P.E, 3},
+                     bs[2] = {(cuuint64_t)P.d * 2, (cuuint64_t)P.E * P.d * 2};
+    const cuuint32_t bb[3] = {64, 256, 1};
+    if (!tmap_encode(&p.am, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, ad, as, ab, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !tmap_encode(&p.bm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, P.W_r_split, bd, bs, bb, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  p.bias = P.b_r; p.T = T; p.d = P.d; p.E = P.E; p.k = P.k;
   p.idx = idx; p.w = w; p.logits = logits;
   return run_gemm(p, P.num_sms, st);
 }

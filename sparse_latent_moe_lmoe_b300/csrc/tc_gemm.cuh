@@ -106,8 +106,10 @@ struct Shared {
 };
 
 // B_MODE 0: int4 + bf16 scales dequantised by the producers; 1: bf16 rows copied;
-//         2: fp16 rows by one TMA box {64, BN} per stage (128-byte swizzle)
-// A_MODE 0: fp16 rows by cp.async; 1: bf16 rows converted to fp16; 2: bf16 rows by cp.async
+//         2: 16-bit rows loaded by the problem's own TMA boxes (prob.load_b,
+//            128-byte swizzle, BN rows x 64 elements per stage)
+// A_MODE 0: fp16 rows by cp.async; 1: bf16 rows converted to fp16; 2: bf16 rows by cp.async;
+//        3: 16-bit rows by the problem's TMA boxes (prob.load_a; needs B_MODE 2)
 template <class P>
 __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant__ P prob) {
   extern __shared__ __align__(1024) unsigned char dyn[];
@@ -127,7 +129,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&sh.full[s], NPROD_WARPS * 32 + (P::B_MODE == 2 ? 1 : 0));
+      mbar_init(&sh.full[s], P::A_MODE == 3 ? 1 : NPROD_WARPS * 32 + (P::B_MODE == 2 ? 1 : 0));
       mbar_init(&sh.empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -149,8 +151,25 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
   const int ntiles = prob.num_tiles(sh.scratch);
 
   constexpr bool ASYNC = P::A_MODE != 1 && P::B_MODE != 0;
+  static_assert(P::A_MODE != 3 || P::B_MODE == 2, "A by TMA needs B by TMA");
   if (warp < NPROD_WARPS) {
-   if constexpr (ASYNC) {
+   if constexpr (P::A_MODE == 3) {
+    // ------------------------------------------------ producer: TMA only (one thread)
+    if (tid == 0) {
+      int kiter = 0;
+      for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+        const Tile tl = prob.tile(sh.scratch, t);
+        for (int kb = 0; kb < tl.nkb; ++kb, ++kiter) {
+          const int s = kiter % STAGES, use = kiter / STAGES;
+          if (use > 0) mbar_wait(&sh.empty[s], (use - 1) & 1, budget, err);
+          unsigned char* sa = base + s * STAGE_BYTES;
+          mbar_expect_tx(&sh.full[s], (uint32_t)(A_BYTES + B_BYTES));
+          prob.load_a(tl, kb, sa, &sh.full[s]);
+          prob.load_b(tl, kb, sa + A_BYTES, &sh.full[s]);
+        }
+      }
+    }
+   } else if constexpr (ASYNC) {
     // ------------------------------------------------ producers, all copies asynchronous
     // A rows by cp.async (gathered through the problem's row map), B by TMA
     // (B_MODE 2, thread 0) or cp.async (B_MODE 1); STAGES-1 K blocks ahead.
@@ -176,10 +195,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
       }
       if constexpr (P::B_MODE == 2) {
         if (pt == 0) {
-          int c0, c1, c2;
-          prob.b_coords(tl_i, kb_i, c0, c1, c2);
           mbar_expect_tx(&sh.full[s], (uint32_t)B_BYTES);
-          tma_load_3d(sb, prob.bmap(), c0, c1, c2, &sh.full[s]);
+          prob.load_b(tl_i, kb_i, sb, &sh.full[s]);
         }
       } else {
         for (int n = pt; n < BN; n += NPROD_WARPS * 32) {
