@@ -231,6 +231,26 @@ def run_reference(args):
         return
     import lmoe_synth as S
     import oracle as O
+    if args.workload in S.STACK_WORKLOADS:  # one token through one layer per step; value over the whole stack
+        sh, nl, T, xseed = S.STACK_WORKLOADS[args.workload]
+        Ly = O.Layer(sh, S.make_stack_layer(sh, 0))
+        x = S.make_x(1, sh.d, xseed)
+        for _ in range(max(args.warmup, 0)):
+            O.layer_forward(Ly, x)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            O.layer_forward(Ly, x)
+        dt = time.perf_counter() - t0
+        value = args.steps / dt / nl
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": args.workload, "layers": nl, "T": T},
+                "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                 "sample": f"one token through one of the {nl} layers per step"},
+                "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
     sh, T, W, x = S.make_workload(args.workload)
     Ly = O.Layer(sh, W)
     for i in range(max(args.warmup, 0)):
@@ -418,10 +438,144 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------------- stack
+
+def run_stack(args):
+    """A stack of layers (x_{l+1} = bf16(x_l + bf16(layer_l(x_l)))), each
+    layer with its own weights (13 GB for 48 Edge0 layers, far beyond L2, so
+    no rotation is needed). A step is one pass of T tokens through all
+    layers; value = T / step time."""
+    import numpy as np
+    import torch
+
+    import lmoe_synth as S
+    from sparse_latent_moe_lmoe_b300 import LatentMoE, LatentMoEStack, capi
+
+    rank, local, world = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = dist_init(world, True)
+    sh, nl, T, xseed = S.STACK_WORKLOADS[args.workload]
+    t0 = time.perf_counter()
+    layers = []
+    for l in range(nl):
+        W = S.make_stack_layer(sh, l)
+        layers.append(LatentMoE(sh, W, device=local))
+        del W
+    gen_s = time.perf_counter() - t0
+    stack = LatentMoEStack(layers)
+    x = S.make_x(T, sh.d, xseed)
+    xt = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+    y = torch.empty_like(xt)
+    stack.workspace(T)
+    # the algorithmic work of this input, layer by layer on the stack's own chain
+    decode = T <= 16
+    total_bytes = total_flops = 0.0
+    int4_bytes = 0.0
+    cur = xt
+    for m in layers:
+        idx, _, _ = m.route(cur)
+        idx_np = idx.cpu().numpy()
+        sb = stage_bytes(sh, T, idx_np)
+        total_bytes += sum(v for n, v in sb.items() if n != "decode_fused")
+        int4_bytes += sum(v for n, v in sb.items() if n in ("win", "gateup", "down", "wout")) - 4 * T * sh.d
+        sf, _ = stage_flops(sh, T, idx_np)
+        total_flops += sum(sf.values())
+        yl = m.forward(cur)
+        cur = (cur.float() + yl.float()).to(torch.bfloat16)
+    per_layer = capi.lmoe_stage_name(layers[0].h, T, 0)[1]
+    stack.forward(xt, out=y)
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        stack.forward(xt, out=y)
+    torch.cuda.synchronize()
+    for _ in range(max(args.warmup, 3)):
+        g.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(dist)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    ms = max_over_ranks(dist, e0.elapsed_time(e1), dev)
+    ck = clocks.stop()
+    step_s = ms / args.steps / 1000.0
+    value = world * T / step_s
+    hbm, bf16, bf16s, peak_src = measured_peaks()
+    if decode:
+        achieved = total_bytes / step_s / 1e9
+        roofline = {"bound": "hbm", "kernel": "stack", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                    "frac": achieved / hbm, "traffic": None, "peak_source": peak_src,
+                    "bytes_per_launch": total_bytes, "timing": "graph replay of the whole stack"}
+    else:
+        achieved = total_flops / step_s / 1e12
+        roofline = {"bound": "tensor", "kernel": "stack", "achieved": achieved, "peak": bf16s, "unit": "TFLOP/s",
+                    "frac": achieved / bf16s, "traffic": None, "peak_source": peak_src + " sustained",
+                    "flops_per_launch": total_flops, "timing": "graph replay of the whole stack"}
+    # end to end: pinned host x in, y out, every step
+    xh = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    xd = torch.empty_like(xt)
+    for _ in range(2):
+        xd.copy_(xh, non_blocking=True)
+        stack.forward(xd, out=y)
+        yh.copy_(y, non_blocking=True)
+    torch.cuda.synchronize()
+    n_e2e = max(1, min(args.steps, 20))
+    ta = time.perf_counter()
+    for _ in range(n_e2e):
+        xd.copy_(xh, non_blocking=True)
+        stack.forward(xd, out=y)
+        yh.copy_(y, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_s = max_over_ranks(dist, time.perf_counter() - ta, dev) / n_e2e
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int4 weights, fp16 tensor-core operands, fp32 accumulate",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "layers": nl, "T": T, "d": sh.d, "E": sh.E, "G": sh.G, "k": sh.k,
+                       "L": sh.L, "f": sh.f, "parallelism": f"replicas x{world}",
+                       "l2": f"{nl} layers of distinct weights ({nl * 272.6 / 1000:.1f} GB > L2)",
+                       "weight_generation_s": round(gen_s, 1)},
+            "int4_bytes_per_token": int4_bytes / T, "weight_bytes_per_token": total_bytes / T,
+            "roofline": roofline,
+            "e2e": {"value": world * T / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": T * sh.d * 2,
+                    "d2h_bytes_per_step": T * sh.d * 2},
+            "gpu_launches": nl * (per_layer + 1) * args.steps, "clocks": ck}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle as O
+        Ly = O.Layer(sh, S.make_stack_layer(sh, 0))
+        xt1 = x[:1]
+        tb = time.perf_counter()
+        cur1 = xt1
+        for _ in range(nl):  # the oracle's cost does not depend on the weights: layer 0's reused
+            y1, _, _, _ = O.layer_forward(Ly, cur1)
+            cur1 = O.residual(cur1, y1)
+        cs = time.perf_counter() - tb
+        line["cpu_baseline"] = {"value": 1.0 / cs, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": f"one token through {nl} oracle layer evaluations (layer-0 weights reused)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
+    import lmoe_synth as S
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload in S.STACK_WORKLOADS:
+        run_stack(args)
     else:
         run_ours(args)
 

@@ -231,6 +231,23 @@ lmoe_status lmoe_layer_forward_host(lmoe_handle* h, const uint16_t* x_host, int 
 /* Extra workspace bytes lmoe_layer_forward_host needs for its staging copies. */
 size_t lmoe_host_staging_size(const lmoe_handle* h, int T);
 
+/* A stack of layers without attention ("512 expert networks across 48
+ * layers"): x_0 = x, x_{l+1} = bf16(x_l + bf16(layer_l(x_l))) for
+ * l = 0 .. n_layers-1, y = x_{n_layers}. layers[l] are handles of the same
+ * shape (d, E, G, k, L, f, lora_rank) on the same device, each with its own
+ * weights; x and y are [T][d] bf16 device pointers (y may alias x). Each
+ * layer runs exactly as lmoe_layer_forward without a residual; the residual
+ * step is a separate kernel that rounds the sum once. ws must hold
+ * lmoe_stack_workspace_size(layers[0], T) bytes. Returns LMOE_ERR_INVALID_ARG
+ * for n_layers < 1, a null handle or mismatched shapes or devices, and the
+ * errors of lmoe_layer_forward. */
+lmoe_status lmoe_stack_forward(lmoe_handle* const* layers, int n_layers, const uint16_t* x, int T, uint16_t* y,
+                               void* ws, lmoe_stream stream);
+
+/* Workspace bytes of lmoe_stack_forward: one layer's workspace plus two
+ * [T][d] bf16 activation buffers. 0 on a bad handle or T < 0. */
+size_t lmoe_stack_workspace_size(const lmoe_handle* h, int T);
+
 /* Wait for `stream`, then read and clear the handle's device error word.
  * Returns LMOE_OK, LMOE_ERR_TIMEOUT, LMOE_ERR_DEVICE_CHECK or LMOE_ERR_CUDA. */
 lmoe_status lmoe_check(lmoe_handle* h, lmoe_stream stream);

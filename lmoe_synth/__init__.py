@@ -199,5 +199,18 @@ def stack_layer_seed(layer: int) -> int:
     return 1000 + layer
 
 
+def make_stack_layer(shape: LayerShape, layer: int) -> dict:
+    """Weights of layer `layer` of a stack of `shape` layers."""
+    return make_layer(shape, stack_layer_seed(layer))
+
+
+STACK_WORKLOADS = {
+    # name: (layer shape, layers, tokens per step, x seed)
+    "stack48_t1": (EDGE0, 48, 1, 1),
+    "stack48_t8": (EDGE0, 48, 8, 1),
+    "stack48_prefill_t4096": (EDGE0, 48, 4096, 1),
+}
+
+
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (b.astype(np.uint32) << 16).view(np.float32)

@@ -20,7 +20,7 @@ FLAG_MULTI_KERNEL_DECODE = 1
 
 EXPORTS = ("lmoe_status_string", "lmoe_version", "lmoe_create", "lmoe_destroy", "lmoe_workspace_size", "lmoe_route",
            "lmoe_permute", "lmoe_expert_forward", "lmoe_combine", "lmoe_layer_forward", "lmoe_layer_forward_noalloc",
-           "lmoe_layer_forward_host",
+           "lmoe_layer_forward_host", "lmoe_stack_forward", "lmoe_stack_workspace_size",
            "lmoe_host_staging_size", "lmoe_check", "lmoe_set_timeout", "lmoe_set_stage_events", "lmoe_stage_name")
 
 
@@ -74,6 +74,8 @@ def _load():
         "lmoe_layer_forward": ([P, P, I, P, P, P, P], S),
         "lmoe_layer_forward_noalloc": ([P, P, I, P, P, P], S),
         "lmoe_layer_forward_host": ([P, P, I, P, P, P, P], S),
+        "lmoe_stack_forward": ([P, I, P, I, P, P, P], S),
+        "lmoe_stack_workspace_size": ([P, I], sz),
         "lmoe_check": ([P, P], S),
         "lmoe_set_timeout": ([P, ctypes.c_longlong], S),
         "lmoe_set_stage_events": ([P, P, I], S),
@@ -156,6 +158,15 @@ def lmoe_layer_forward_noalloc(h, x, T, residual, y, stream) -> None:
 
 NOALLOC_MAX_T = 16
 NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def lmoe_stack_forward(handles, x, T, y, ws, stream) -> None:
+    arr = (ctypes.c_void_p * len(handles))(*handles)
+    _ok(_lib.lmoe_stack_forward(arr, len(handles), x, int(T), y, ws, stream), "lmoe_stack_forward")
+
+
+def lmoe_stack_workspace_size(h, T: int) -> int:
+    return _lib.lmoe_stack_workspace_size(h, int(T))
 
 
 def lmoe_layer_forward_host(h, x_host, T, residual_host, y_host, ws, stream) -> None:

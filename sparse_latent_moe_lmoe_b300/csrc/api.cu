@@ -587,6 +587,51 @@ lmoe_status lmoe_layer_forward_noalloc(lmoe_handle* h, const uint16_t* x, int T,
   return decode_layer(h, x, T, residual, y, ws, (cudaStream_t)stream);
 }
 
+size_t lmoe_stack_workspace_size(const lmoe_handle* h, int T) {
+  if (!h || T < 0) return 0;
+  return align_up(lmoe_workspace_size(h, T)) + 2 * align_up((size_t)T * h->cfg.d * 2);
+}
+
+lmoe_status lmoe_stack_forward(lmoe_handle* const* layers, int n_layers, const uint16_t* x, int T, uint16_t* y,
+                               void* ws, lmoe_stream stream) {
+  if (!layers || n_layers < 1 || T < 0 || !x || !y || !ws) return LMOE_ERR_INVALID_ARG;
+  const lmoe_handle* h0 = layers[0];
+  if (!h0) return LMOE_ERR_INVALID_ARG;
+  const lmoe_config& c0 = h0->cfg;
+  for (int l = 1; l < n_layers; ++l) {
+    const lmoe_handle* h = layers[l];
+    if (!h || h->device != h0->device) return LMOE_ERR_INVALID_ARG;
+    const lmoe_config& c = h->cfg;
+    if (c.d != c0.d || c.E != c0.E || c.G != c0.G || c.k != c0.k || c.L != c0.L || c.f != c0.f ||
+        c.lora_rank != c0.lora_rank)
+      return LMOE_ERR_INVALID_ARG;
+  }
+  if (T == 0) return LMOE_OK;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(ws)) return LMOE_ERR_ALIGNMENT;
+  if (c0.d % 8 != 0) return LMOE_ERR_UNSUPPORTED;
+  size_t need = 0;
+  for (int l = 0; l < n_layers; ++l) {
+    const size_t n = lmoe_workspace_size(layers[l], T);
+    need = n > need ? n : need;
+  }
+  const size_t act = align_up((size_t)T * c0.d * 2);
+  char* b = reinterpret_cast<char*>(ws) + align_up(need);
+  uint16_t* ybuf = reinterpret_cast<uint16_t*>(b);
+  uint16_t* xbuf = reinterpret_cast<uint16_t*>(b + act);
+  DeviceGuard guard(h0->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t n = (size_t)T * c0.d;
+  const uint16_t* xin = x;
+  for (int l = 0; l < n_layers; ++l) {
+    lmoe_status s = lmoe_layer_forward(layers[l], xin, T, nullptr, ybuf, ws, stream);
+    if (s != LMOE_OK) return s;
+    uint16_t* xout = l == n_layers - 1 ? y : xbuf;
+    if (launch_residual_add(xin, ybuf, n, xout, st) != cudaSuccess) return LMOE_ERR_CUDA;
+    xin = xout;
+  }
+  return LMOE_OK;
+}
+
 lmoe_status lmoe_layer_forward_host(lmoe_handle* h, const uint16_t* x_host, int T, const uint16_t* residual_host,
                                     uint16_t* y_host, void* ws, lmoe_stream stream) {
   if (check_handle(h) != LMOE_OK || T < 0) return LMOE_ERR_INVALID_ARG;

@@ -689,6 +689,31 @@ cudaError_t launch_experts(const DecodeArgs& A, int mode, cudaStream_t st, Stage
   return launch_experts_nt<2>(A, mode, st, hook);
 }
 
+// x_next = bf16(x + y) for bf16 x, y (the sum of two bf16 values is exact in
+// fp32, so this is the single rounding of the residual step)
+__global__ void residual_add_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ y, size_t n8,
+                                    uint16_t* __restrict__ out) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+    const uint4 a = reinterpret_cast<const uint4*>(x)[i], b = reinterpret_cast<const uint4*>(y)[i];
+    const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float lo = __uint_as_float(av[j] << 16) + __uint_as_float(bv[j] << 16);
+      const float hi = __uint_as_float(av[j] & 0xffff0000u) + __uint_as_float(bv[j] & 0xffff0000u);
+      o[j] = (uint32_t)f32_to_bf16_rne(lo) | ((uint32_t)f32_to_bf16_rne(hi) << 16);
+    }
+    reinterpret_cast<uint4*>(out)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+cudaError_t launch_residual_add(const uint16_t* x, const uint16_t* y, size_t n, uint16_t* out, cudaStream_t st) {
+  const size_t n8 = n / 8;
+  const int blocks = (int)((n8 + 255) / 256 < 1184 ? (n8 + 255) / 256 : 1184);
+  residual_add_kernel<<<blocks > 0 ? blocks : 1, 256, 0, st>>>(x, y, n8, out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_combine(const float* Y, const int32_t* idx, const int32_t* assign_row, int T, int d, int k,
                            int epg, const uint16_t* residual, uint16_t* y, cudaStream_t st) {
   if (T == 0) return cudaSuccess;

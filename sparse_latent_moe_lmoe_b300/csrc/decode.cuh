@@ -108,6 +108,8 @@ cudaError_t permute_set_attributes();
 cudaError_t launch_route(const DecodeArgs& A, int do_perm, float* logits_out, cudaStream_t st);
 cudaError_t launch_lora_proj(const DecodeArgs& A, int which, cudaStream_t st);
 cudaError_t launch_experts(const DecodeArgs& A, int mode, cudaStream_t st, StageHook* hook);
+// out = bf16(x + y), n a multiple of 8 (the residual step of a layer stack)
+cudaError_t launch_residual_add(const uint16_t* x, const uint16_t* y, size_t n, uint16_t* out, cudaStream_t st);
 cudaError_t launch_combine(const float* Y, const int32_t* idx, const int32_t* assign_row, int T, int d, int k,
                            int epg, const uint16_t* residual, uint16_t* y, cudaStream_t st);
 

@@ -144,3 +144,28 @@ class LatentMoE:
         capi.lmoe_layer_forward_host(self.h, _ptr(x_host), T, _ptr(residual_host), _ptr(y_host), _ptr(ws),
                                      _stream(stream))
         return y_host
+
+
+class LatentMoEStack:
+    """A stack of LatentMoE layers of one shape (lmoe_stack_forward):
+    x_{l+1} = bf16(x_l + bf16(layer_l(x_l)))."""
+
+    def __init__(self, layers):
+        self.layers = list(layers)
+        if not self.layers:
+            raise ValueError("empty stack")
+        self.device = self.layers[0].device
+        self._ws = None
+
+    def workspace(self, T: int) -> torch.Tensor:
+        n = capi.lmoe_stack_workspace_size(self.layers[0].h, T)
+        if self._ws is None or self._ws.numel() < n:
+            self._ws = torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
+        return self._ws
+
+    def forward(self, x: torch.Tensor, out=None, stream=None) -> torch.Tensor:
+        T = x.shape[0]
+        y = out if out is not None else torch.empty_like(x)
+        capi.lmoe_stack_forward([m.h for m in self.layers], _ptr(x), T, _ptr(y), _ptr(self.workspace(T)),
+                                _stream(stream))
+        return y

@@ -1,0 +1,94 @@
+"""GPU parity of the layer stack (lmoe_stack_forward) against the oracle:
+x_{l+1} = bf16(x_l + bf16(layer_l(x_l))). The stack must equal the chain of
+single-layer calls bit for bit; each layer is checked teacher-forced (the
+oracle runs layer l on the GPU's own x_l, so a near-tie routing difference
+in one layer cannot spread); the end-to-end output is compared with the
+oracle's own chain."""
+import numpy as np
+import pytest
+import torch
+
+import lmoe_synth as S
+import oracle as O
+from gpu_util import ambiguous_rows, bf16_bits, bf16_tensor, check_outputs
+
+pytestmark = pytest.mark.gpu
+
+
+def build(shape, n, dev):
+    from sparse_latent_moe_lmoe_b300 import LatentMoE, LatentMoEStack
+    Ws = [S.make_stack_layer(shape, l) for l in range(n)]
+    layers = [LatentMoE(shape, W, device=dev.index or 0) for W in Ws]
+    return Ws, layers, LatentMoEStack(layers)
+
+
+def gpu_chain(layers, xt):
+    """x_l (l = 0..n) and y_l (l < n) as bf16 bits, from single-layer calls"""
+    xs, ys = [bf16_bits(xt)], []
+    cur = xt
+    for m in layers:
+        y = m.forward(cur)
+        ys.append(bf16_bits(y))
+        nxt = (cur.float() + y.float()).to(torch.bfloat16)
+        xs.append(bf16_bits(nxt))
+        cur = nxt
+    return xs, ys
+
+
+def check_stack(shape, n, T, dev, xseed, sample=None):
+    Ws, layers, stack = build(shape, n, dev)
+    x = S.make_x(T, shape.d, xseed)
+    xt = bf16_tensor(x, dev)
+    y = bf16_bits(stack.forward(xt))
+    for m in layers:
+        m.check()
+    xs, ys = gpu_chain(layers, xt)
+    assert np.array_equal(y, xs[-1]), "stack differs from the chain of layer calls"
+    rows = np.arange(T) if sample is None else sample
+    for l in range(n):
+        # the residual rule, bit-exact on the GPU's own values
+        assert np.array_equal(O.residual(xs[l], O.bf16_value(ys[l])), xs[l + 1])
+        # the layer, teacher-forced: the oracle runs layer l on the GPU's x_l
+        y_ref, idx_ref, w_ref, lg_ref = O.layer_forward(O.Layer(shape, Ws[l]), xs[l][rows])
+        keep = ~ambiguous_rows(lg_ref, shape.k, 1e-5 * np.abs(lg_ref).max(axis=1))
+        mr, ma, _ = check_outputs(ys[l][rows][keep], y_ref[keep], f"stack layer {l}")
+        print(f"layer {l}: mean rel {mr:.2e} max abs {ma:.2e}")
+    return y, x, Ws, rows
+
+
+def test_stack_tiny_three_layers(cuda_device):
+    y, x, Ws, rows = check_stack(S.TINY, 3, 64, cuda_device, 5)
+    # end to end against the oracle's own chain: differences are whole bf16
+    # ulps of x where a rounding of x + bf16(y) fell the other way
+    cur = x
+    for W in Ws:
+        yl, _, _, _ = O.layer_forward(O.Layer(S.TINY, W), cur)
+        cur = O.residual(cur, yl)
+    d = np.abs(O.bf16_value(y) - O.bf16_value(cur))
+    rel = d.mean() / np.abs(O.bf16_value(cur)).mean()
+    print(f"tiny 3-layer stack end to end: {np.count_nonzero(d)} of {d.size} elements differ, mean rel {rel:.2e}")
+    assert rel < 1e-3
+
+
+def test_stack_edge0_decode_two_layers(cuda_device):
+    check_stack(S.EDGE0, 2, 8, cuda_device, 6)
+
+
+def test_stack_edge0_prefill_two_layers_sampled(cuda_device):
+    rows = np.array([0, 1, 100, 511, 700, 1023])
+    check_stack(S.EDGE0, 2, 1024, cuda_device, 7, sample=rows)
+
+
+def test_stack_rejects_mismatched_shapes(cuda_device):
+    from sparse_latent_moe_lmoe_b300 import LatentMoE, capi
+    a = LatentMoE(S.TINY, S.make_layer(S.TINY, 1), device=0)
+    other = S.LayerShape(d=256, E=16, G=2, k=2, L=64, f=64)
+    b = LatentMoE(other, S.make_layer(other, 2), device=0)
+    x = torch.zeros((4, 256), dtype=torch.bfloat16, device=cuda_device)
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=cuda_device)
+    arr = [a.h, b.h]
+    import ctypes
+    carr = (ctypes.c_void_p * 2)(*arr)
+    st = capi.library().lmoe_stack_forward(carr, 2, ctypes.c_void_p(x.data_ptr()), 4, ctypes.c_void_p(x.data_ptr()),
+                                           ctypes.c_void_p(ws.data_ptr()), None)
+    assert st == 1
