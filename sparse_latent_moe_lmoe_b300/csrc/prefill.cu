@@ -11,7 +11,8 @@
 //            with the top-k and softmax renormalisation in the epilogue
 //            (one thread per token, all E logits of its row from TMEM)
 //   permute  the deterministic multi-CTA permutation (permute.cu)
-//   win      H[(g,t)] = Win[g] x_t        grouped by group, rows gathered
+//   win      H[g][t] = Win[g] x_t for every (g, t) (dense; rows of tokens
+//            with no expert in g are never read)
 //   gateup   V[a] = silu(Gate_e h) * Up_e h   grouped by expert (128 gate
 //            rows + the matching 128 up rows per tile, SwiGLU in the epilogue)
 //   down     U[a] = w_a * Down_e V[a]     grouped by expert
@@ -208,35 +209,35 @@ struct ProbRoute : ProbBase {
 
 // -------------------------------------------------------------------- W_in
 struct ProbWin : ProbBase {
-  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 0, B_MODE = 2, STAGES = 3;
-  CUtensorMap bm;      // Win in fp16 as [G][L][d], box {64, 256, 1}
-  const __half* x16;   // [T][d] fp16
-  int d, L, G;
-  const int32_t* gto;
-  const int32_t* gtok;
-  __half* H;  // [rows][L]
+  // H for every (group, token): one dense GEMM per group, A = x by TMA. The
+  // rows of tokens with no expert in a group are computed and never read --
+  // cheaper than gathering each group's tokens.
+  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 3, B_MODE = 2, STAGES = 4;
+  CUtensorMap am;   // x in fp16 as [T][d], box {64, 128}
+  CUtensorMap bm;   // Win in fp16 as [G][L][d], box {64, 256, 1}
+  int T, d, L, G;
+  __half* H;        // [G][T][L]
   LMOE_DEV int ntn() const { return L / 256; }
-  LMOE_DEV void init(int* sc) const {
-    tile_prefix(sc, G, [&](int g) { return ((gto[g + 1] - gto[g] + 127) / 128) * ntn(); });
-  }
-  LMOE_DEV int num_tiles(const int* sc) const { return sc[G]; }
-  LMOE_DEV Tile tile(const int* sc, int t) const {
+  LMOE_DEV int ntm() const { return (T + 127) / 128; }
+  LMOE_DEV void init(int*) const {}
+  LMOE_DEV int num_tiles(const int*) const { return G * ntm() * ntn(); }
+  LMOE_DEV Tile tile(const int*, int t) const {
     Tile tl;
-    const int g = find_prob(sc, G, t), loc = t - sc[g];
-    tl.prob = g;
+    tl.prob = t / (ntm() * ntn());
+    const int loc = t % (ntm() * ntn());
     tl.m0 = (loc / ntn()) * 128;
     tl.n0 = (loc % ntn()) * 256;
-    tl.rows = min(128, gto[g + 1] - gto[g] - tl.m0);
+    tl.rows = min(128, T - tl.m0);
     tl.nkb = d / 64;
     return tl;
   }
-  LMOE_DEV const void* a_row(const int*, const Tile& tl, int r, int kb) const {
-    const int tok = gtok[gto[tl.prob] + tl.m0 + r];
-    return x16 + (size_t)tok * d + kb * 64;
+  LMOE_DEV void load_a(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
+    tma_load_2d(dst, &am, kb * 64, tl.m0, bar);
   }
   LMOE_DEV void load_b(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
     tma_load_3d(dst, &bm, kb * 64, tl.n0, tl.prob, bar);
   }
+  LMOE_DEV const void* a_row(const int*, const Tile&, int, int) const { return nullptr; }
   LMOE_DEV bool b_row(const int*, const Tile&, int, int, const uint8_t*&, const uint16_t*&) const { return false; }
   LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int, int) const { return nullptr; }
   LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
@@ -246,16 +247,17 @@ struct ProbWin : ProbBase {
     for (int c0 = 0; c0 < 256; c0 += 16) {
       float v[16];
       tc::tmem_ld16(tbase + (uint32_t)c0, v);
-      if (row < tl.rows) store_half16(H + (size_t)(gto[tl.prob] + tl.m0 + row) * L + tl.n0 + c0, v);
+      if (row < tl.rows) store_half16(H + ((size_t)tl.prob * T + tl.m0 + row) * L + tl.n0 + c0, v);
     }
   }
 };
 
 // ---------------------------------------------------------------- gate/up
 struct ProbGateUp : ProbBase {
-  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 0, B_MODE = 2, STAGES = 3;
+  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 0, B_MODE = 2, STAGES = 4;
   CUtensorMap gm, um;  // gate / up in fp16 as [E*f][L], box {64, 128}
-  const __half* H;
+  const __half* H;     // [G][T][L]
+  int T, k, epg;
   int L, f, E;
   const int32_t* eo;
   const int32_t* sa;
@@ -278,7 +280,8 @@ struct ProbGateUp : ProbBase {
   }
   LMOE_DEV const void* a_row(const int*, const Tile& tl, int r, int kb) const {
     const int p = eo[tl.prob] + tl.m0 + r;
-    return H + (size_t)arow[sa[p]] * L + kb * 64;
+    const int t = sa[p] / k;  // assignment -> token
+    return H + ((size_t)(tl.prob / epg) * T + t) * L + kb * 64;
   }
   // B rows 0..127: gate rows n0.. of expert e; 128..255: the matching up rows
   LMOE_DEV void load_b(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
@@ -360,10 +363,10 @@ struct ProbDown : ProbBase {
 // mode 0: y_t = sum_g Wout[g] Z[(g,t)] (+ residual), tiles over tokens, K = G*L
 // mode 1: Y[(g,t)] = Wout[g] Z[(g,t)] (fp32 rows), tiles over group rows
 struct ProbWout : ProbBase {
-  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 0, B_MODE = 2, STAGES = 3;
+  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 3, B_MODE = 2, STAGES = 4;
   CUtensorMap bm;         // Wout in fp16 as [G][d][L], box {64, 256, 1}
-  const __half* Z;        // [rows][L]
-  const int32_t* tokrow;  // [T][G]: row of (g, t) in Z or -1
+  CUtensorMap am;         // mode 0: Z by token as [T][G*L] (zero rows for absent (t, g));
+                          // mode 1: Z by group rows as [rows][L]; box {64, 128}
   const int32_t* gto;
   int T, d, L, G, mode;
   const uint16_t* residual;
@@ -393,14 +396,13 @@ struct ProbWout : ProbBase {
     }
     return tl;
   }
-  LMOE_DEV const void* a_row(const int*, const Tile& tl, int r, int kb) const {
-    if (mode == 0) {
-      const int g = kb / kpg(), kk = kb % kpg();
-      const int zr = tokrow[(size_t)(tl.m0 + r) * G + g];
-      return zr < 0 ? nullptr : Z + (size_t)zr * L + kk * 64;
-    }
-    return Z + (size_t)(gto[tl.prob] + tl.m0 + r) * L + kb * 64;
+  LMOE_DEV void load_a(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
+    if (mode == 0)
+      tma_load_2d(dst, &am, kb * 64, tl.m0, bar);
+    else  // rows past the group's range belong to the next group or read as zero; not stored
+      tma_load_2d(dst, &am, kb * 64, gto[tl.prob] + tl.m0, bar);
   }
+  LMOE_DEV const void* a_row(const int*, const Tile&, int, int) const { return nullptr; }
   LMOE_DEV void load_b(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
     const int g = mode == 0 ? kb / kpg() : tl.prob;
     tma_load_3d(dst, &bm, (mode == 0 ? kb % kpg() : kb) * 64, tl.n0, g, bar);
@@ -471,6 +473,34 @@ __global__ void zreduce_kernel(const float* __restrict__ U, const int32_t* __res
   }
 }
 
+// Mode-0 operand of W_out: Ztok[t][g][:] = sum over the token's experts in
+// group g, in ascending j, of U[inv[t*k + j]], or zero when the token has no
+// expert in g. One warp per (t, g).
+__global__ void zreduce_tok_kernel(const float* __restrict__ U, const int32_t* __restrict__ idx,
+                                   const int32_t* __restrict__ inv, int T, int G, int k, int epg, int L,
+                                   __half* __restrict__ Ztok) {
+  const int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (item >= T * G) return;
+  const int t = item / G, g = item % G;
+  __half* dst = Ztok + ((size_t)t * G + g) * L;
+  for (int c = lane * 8; c < L; c += 256) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < k; ++j) {
+      if (idx[(size_t)t * k + j] / epg != g) continue;
+      const float4* u = reinterpret_cast<const float4*>(U + (size_t)inv[(size_t)t * k + j] * L + c);
+      const float4 a = u[0], b = u[1];
+      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    }
+    uint4 o;
+    o.x = pack_half2(acc[0], acc[1]);
+    o.y = pack_half2(acc[2], acc[3]);
+    o.z = pack_half2(acc[4], acc[5]);
+    o.w = pack_half2(acc[6], acc[7]);
+    *reinterpret_cast<uint4*>(dst + c) = o;
+  }
+}
+
 // W = hi + mid + lo with each term the bf16 rounding of what remains; the
 // three terms carry 24 significant bits, so the split is exact for every
 // fp32 value in bf16's normal range.
@@ -494,18 +524,20 @@ cudaError_t launch_split_router(const float* W_r, int E, int d, uint16_t* out, c
 }
 
 // int4 rows [rows][K/2] + bf16 scales [rows][K/32] -> fp16 [rows][K]; one
-// 32-bit word (8 elements, natural order) per thread and step
-__global__ void dequant_f16_kernel(const uint8_t* __restrict__ q, const uint16_t* __restrict__ s, size_t words, int K,
+// scale group (16 bytes of int4, 32 elements, natural order) per thread and step
+__global__ void dequant_f16_kernel(const uint8_t* __restrict__ q, const uint16_t* __restrict__ s, size_t groups,
                                    __half* __restrict__ out) {
-  const int wpr = K / 8;  // words per row
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < words; i += (size_t)gridDim.x * blockDim.x) {
-    const size_t row = i / wpr;
-    const int wi = (int)(i % wpr);
-    const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(q) + i);
-    const __half2 s2 = scale_h2(__ldg(s + row * (K / 32) + wi / 4));
-    uint32_t o[4];
-    tc::dequant_word_natural(v, s2, o);
-    reinterpret_cast<uint4*>(out)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < groups; i += (size_t)gridDim.x * blockDim.x) {
+    const uint4 v = ldg_stream(q + i * 16);
+    const __half2 s2 = scale_h2(__ldg(s + i));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint4* o4 = reinterpret_cast<uint4*>(out) + i * 4;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t o[4];
+      tc::dequant_word_natural(w[j], s2, o);
+      o4[j] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
   }
 }
 
@@ -530,7 +562,7 @@ size_t al(size_t v) { return (v + kAl - 1) & ~(kAl - 1); }
 
 struct PWs {
   size_t idx, w, eo, sa, inv, go, gto, gt, ar, perm_scratch, H, V, U, Z, tokrow, x16, win16, wout16, gate16, up16,
-      down16, end;
+      down16, ztok, end;
 };
 
 PWs pws(const PrefillArgs& P, int T) {
@@ -552,7 +584,7 @@ PWs pws(const PrefillArgs& P, int T) {
   m.gt = take(gk * 4);
   m.ar = take(n * 4);
   m.perm_scratch = take(permute_scratch_bytes(T, P.E, P.G));
-  m.H = take(gk * P.L * 2);
+  m.H = take((size_t)T * P.G * P.L * 2);
   m.V = take(n * P.f * 2);
   m.U = take(n * P.L * 4);
   m.Z = take(gk * P.L * 2);
@@ -563,6 +595,7 @@ PWs pws(const PrefillArgs& P, int T) {
   m.gate16 = take((size_t)P.E * P.f * P.L * 2);
   m.up16 = take((size_t)P.E * P.f * P.L * 2);
   m.down16 = take((size_t)P.E * P.L * P.f * 2);
+  m.ztok = take((size_t)T * P.G * P.L * 2);
   m.end = o;
   return m;
 }
@@ -634,17 +667,19 @@ cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_
   __half* gate16 = reinterpret_cast<__half*>(b + m.gate16);
   __half* up16 = reinterpret_cast<__half*>(b + m.up16);
   __half* down16 = reinterpret_cast<__half*>(b + m.down16);
+  __half* ztok = reinterpret_cast<__half*>(b + m.ztok);
   cudaError_t e;
   {  // the shared matrices and x in fp16, once per call
     if (hook) hook->before(st);
-    const size_t wwords = (size_t)P.G * P.L * P.d / 8;
-    dequant_f16_kernel<<<4 * grid, 256, 0, st>>>(P.W_in_q, P.W_in_s, wwords, P.d, win16);
-    dequant_f16_kernel<<<4 * grid, 256, 0, st>>>(P.W_out_q, P.W_out_s, wwords, P.L, wout16);
-    bf16_to_f16_kernel<<<4 * grid, 256, 0, st>>>(x, (size_t)T * P.d / 8, x16);
-    const size_t ewords = (size_t)P.E * P.f * P.L / 8;
-    dequant_f16_kernel<<<4 * grid, 256, 0, st>>>(P.gate_q, P.gate_s, ewords, P.L, gate16);
-    dequant_f16_kernel<<<4 * grid, 256, 0, st>>>(P.up_q, P.up_s, ewords, P.L, up16);
-    dequant_f16_kernel<<<4 * grid, 256, 0, st>>>(P.down_q, P.down_s, ewords, P.f, down16);
+    // a row of K elements is K/32 consecutive scale groups in both arrays
+    const size_t wgroups = (size_t)P.G * P.L * P.d / 32;
+    dequant_f16_kernel<<<8 * grid, 256, 0, st>>>(P.W_in_q, P.W_in_s, wgroups, win16);
+    dequant_f16_kernel<<<8 * grid, 256, 0, st>>>(P.W_out_q, P.W_out_s, wgroups, wout16);
+    bf16_to_f16_kernel<<<8 * grid, 256, 0, st>>>(x, (size_t)T * P.d / 8, x16);
+    const size_t egroups = (size_t)P.E * P.f * P.L / 32;
+    dequant_f16_kernel<<<8 * grid, 256, 0, st>>>(P.gate_q, P.gate_s, egroups, gate16);
+    dequant_f16_kernel<<<8 * grid, 256, 0, st>>>(P.up_q, P.up_s, egroups, up16);
+    dequant_f16_kernel<<<8 * grid, 256, 0, st>>>(P.down_q, P.down_s, egroups, down16);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (hook) hook->after(st);
   }
@@ -652,14 +687,16 @@ cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_
     ProbWin p;
     static_cast<ProbBase&>(p) = base(P);
     {
-      const cuuint64_t dims[3] = {(cuuint64_t)P.d, (cuuint64_t)P.L, (cuuint64_t)P.G};
-      const cuuint64_t strides[2] = {(cuuint64_t)P.d * 2, (cuuint64_t)P.L * P.d * 2};
-      const cuuint32_t box[3] = {64, 256, 1};
-      if (!tmap_encode(&p.bm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, win16, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      const cuuint64_t ad[2] = {(cuuint64_t)P.d, (cuuint64_t)T}, as[1] = {(cuuint64_t)P.d * 2};
+      const cuuint32_t ab[2] = {64, 128};
+      const cuuint64_t bd[3] = {(cuuint64_t)P.d, (cuuint64_t)P.L, (cuuint64_t)P.G};
+      const cuuint64_t bs[2] = {(cuuint64_t)P.d * 2, (cuuint64_t)P.L * P.d * 2};
+      const cuuint32_t bb[3] = {64, 256, 1};
+      if (!tmap_encode(&p.am, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x16, ad, as, ab, CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !tmap_encode(&p.bm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, win16, bd, bs, bb, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     }
-    p.x16 = x16; p.d = P.d; p.L = P.L; p.G = P.G; p.gto = pm.group_tok_offsets; p.gtok = pm.group_tokens;
-    p.H = H;
+    p.T = T; p.d = P.d; p.L = P.L; p.G = P.G; p.H = H;
     if (hook) hook->before(st);
     if ((e = run_gemm(p, grid, st)) != cudaSuccess) return e;
     if (hook) hook->after(st);
@@ -667,7 +704,8 @@ cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_
   {
     ProbGateUp p;
     static_cast<ProbBase&>(p) = base(P);
-    p.H = H; p.L = P.L; p.f = P.f; p.E = P.E; p.eo = pm.expert_offsets; p.sa = pm.sorted_assign; p.arow = pm.assign_row;
+    p.H = H; p.T = T; p.k = P.k; p.epg = P.epg;
+    p.L = P.L; p.f = P.f; p.E = P.E; p.eo = pm.expert_offsets; p.sa = pm.sorted_assign; p.arow = pm.assign_row;
     {
       const cuuint64_t dims[2] = {(cuuint64_t)P.L, (cuuint64_t)P.E * P.f}, strides[1] = {(cuuint64_t)P.L * 2};
       const cuuint32_t box[2] = {64, 128};
@@ -701,10 +739,14 @@ cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_
   }
   {
     if (hook) hook->before(st);
-    cudaMemsetAsync(tokrow, 0xff, (size_t)T * P.G * 4, st);
-    const int rows_cap = T * (P.G < P.k ? P.G : P.k);
-    zreduce_kernel<<<(rows_cap + 7) / 8, 256, 0, st>>>(U, idx, pm.inv, pm.group_tok_offsets, pm.group_tokens, P.G,
-                                                      P.k, P.epg, P.L, Z, tokrow);
+    if (mode == 0) {
+      zreduce_tok_kernel<<<(T * P.G + 7) / 8, 256, 0, st>>>(U, idx, pm.inv, T, P.G, P.k, P.epg, P.L, ztok);
+    } else {
+      cudaMemsetAsync(tokrow, 0xff, (size_t)T * P.G * 4, st);
+      const int rows_cap = T * (P.G < P.k ? P.G : P.k);
+      zreduce_kernel<<<(rows_cap + 7) / 8, 256, 0, st>>>(U, idx, pm.inv, pm.group_tok_offsets, pm.group_tokens, P.G,
+                                                        P.k, P.epg, P.L, Z, tokrow);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (hook) hook->after(st);
   }
@@ -719,7 +761,16 @@ cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_
                        CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     }
-    p.Z = Z; p.tokrow = tokrow; p.gto = pm.group_tok_offsets; p.T = T; p.d = P.d; p.L = P.L; p.G = P.G; p.mode = mode;
+    {
+      const int rows_cap = T * (P.G < P.k ? P.G : P.k);
+      const cuuint64_t ad0[2] = {(cuuint64_t)P.G * P.L, (cuuint64_t)T}, as0[1] = {(cuuint64_t)P.G * P.L * 2};
+      const cuuint64_t ad1[2] = {(cuuint64_t)P.L, (cuuint64_t)rows_cap}, as1[1] = {(cuuint64_t)P.L * 2};
+      const cuuint32_t ab[2] = {64, 128};
+      if (!tmap_encode(&p.am, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, mode == 0 ? (const void*)ztok : (const void*)Z,
+                       mode == 0 ? ad0 : ad1, mode == 0 ? as0 : as1, ab, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    }
+    p.gto = pm.group_tok_offsets; p.T = T; p.d = P.d; p.L = P.L; p.G = P.G; p.mode = mode;
     p.residual = residual; p.y = y; p.Y = Yrows;
     if (hook) hook->before(st);
     if ((e = run_gemm(p, grid, st)) != cudaSuccess) return e;
