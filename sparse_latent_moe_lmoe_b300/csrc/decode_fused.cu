@@ -238,28 +238,6 @@ LMOE_DEV void cons_release(Tables& tb, int j) {
   if ((threadIdx.x & 31) == 0) mbar_arrive(&tb.empty[j % NS]);
 }
 
-// producer lane 0: claim the slot of chunk j and announce its bytes. The slot
-// is re-armed only once its previous copies have landed and its consumer has
-// released it; if either wait runs out of budget the producer stops (returns
-// null) rather than arm a barrier phase that is still in flight.
-template <int NS>
-LMOE_COLD unsigned char* prod_begin(Tables& tb, unsigned char* ring, int j, uint32_t bytes, long long budget,
-                                   unsigned* err) {
-  const int s = j % NS, u = j / NS;
-  if (u > 0) {
-    const long long t0 = clock64();
-    #pragma unroll 1
-    while (!mbar_test(&tb.full[s], (u - 1) & 1) || !mbar_test(&tb.empty[s], (u - 1) & 1)) {
-      if (clock64() - t0 > budget) {
-        set_error(err, ERRBIT_TIMEOUT);
-        return nullptr;
-      }
-    }
-  }
-  tb.seq[s] = j;
-  mbar_expect_tx(&tb.full[s], bytes);
-  return ring + s * SLOT_BYTES;
-}
 
 }  // namespace
 
@@ -275,17 +253,29 @@ LMOE_COLD float2 topk_warp(const float* row, int E, int k) {
   float v[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = (lane + 32 * i < E) ? __ldcg(row + lane + 32 * i) : -INFINITY;
+  // best remaining logit of this lane (ties -> lower index): a depth-4
+  // tournament; element i has index lane + 32 i, so a later element wins
+  // only when strictly larger
   auto lane_best = [&](float& bv, int& be) {
-    bv = -INFINITY;
-    be = 0x7fffffff;
+    float tv[8];
+    int ti[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && (v[i] > bv || (v[i] == bv && e < be))) {
-        bv = v[i];
-        be = e;
-      }
+    for (int i = 0; i < 8; ++i) {
+      const bool hi = v[2 * i + 1] > v[2 * i];
+      tv[i] = hi ? v[2 * i + 1] : v[2 * i];
+      ti[i] = hi ? 2 * i + 1 : 2 * i;
     }
+#pragma unroll
+    for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+      for (int i = 0; i < w; ++i) {
+        const bool hi = tv[2 * i + 1] > tv[2 * i];
+        tv[i] = hi ? tv[2 * i + 1] : tv[2 * i];
+        ti[i] = hi ? ti[2 * i + 1] : ti[2 * i];
+      }
+    bv = tv[0];
+    be = lane + 32 * ti[0];
+    if (be >= E || bv == -INFINITY) be = 0x7fffffff;
   };
   float mv;
   int me;
@@ -412,79 +402,137 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
   const int nA1 = a1hi - a1lo, nA2 = a2hi - a2lo;
 
   if (warp == PROD) {
-    // ================================================== producer + routing
-    int j = 0;
+    // ================================================== producer
+    // Lane 0 issues every chunk. Its loop is kept short (no divisions, no
+    // calls): it shares an SM sub-partition with three consumer warps, and
+    // its issue rate bounds how fast weights reach the ring.
+    int j = 0, slot = 0, use = 0;
     bool ok = true;
-    if (lane == 0) {
-      #pragma unroll 1
-      for (int i = a1lo; ok && i < a1hi; ++i, ++j) {
-        const int ks = i / NPAIR, pr = i % NPAIR;
-        unsigned char* dst = prod_begin<NS>(tb, ring, j, 2 * KSEG * 4, budget, err);
-        if (!(ok = dst != nullptr)) break;
-        tma_load_3d(dst, &F.maps.wr, 0, ks * (KSEG / 256), 2 * pr, &tb.full[j % NS]);
-      }
-      #pragma unroll 1
-      for (int i = a2lo; ok && i < a2hi; ++i, ++j) {
-        const int ks = i / (G * NRT_IN), rem = i % (G * NRT_IN), g = rem / NRT_IN, rt = rem % NRT_IN;
-        unsigned char* dst = prod_begin<NS>(tb, ring, j, 16 * KSEG / 2 + 16 * KSEG / 16, budget, err);
-        if (!(ok = dst != nullptr)) break;
-        tma_load_3d(dst, &F.maps.win_q, 0, ks * (KSEG / 256), g * L + rt * 16, &tb.full[j % NS]);
-        tma_load_2d(dst + 16 * KSEG / 2, &F.maps.win_s, ks * (KSEG / 32), g * L + rt * 16, &tb.full[j % NS]);
-      }
-    }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    j = __shfl_sync(0xffffffffu, j, 0);
-    // routing tables (built by the consumers)
-    if (lane == 0 && ok) {
-      const long long t0 = clock64();
-#pragma unroll 1
-      while (tb.tables_ready == 0) {
-        if (clock64() - t0 > budget) {
-          set_error(err, ERRBIT_TIMEOUT);
-          ok = false;
-          break;
+    auto claim = [&](uint32_t bytes) -> unsigned char* {  // next chunk's slot, armed for `bytes`
+      if (use > 0) {
+        const long long t0 = clock64();
+        while (!mbar_test(&tb.full[slot], (use - 1) & 1) || !mbar_test(&tb.empty[slot], (use - 1) & 1)) {
+          if (clock64() - t0 > budget) {
+            set_error(err, ERRBIT_TIMEOUT);
+            ok = false;
+            return nullptr;
+          }
         }
-        __nanosleep(64);
       }
-      __threadfence_block();
-    }
+      tb.seq[slot] = j;
+      mbar_expect_tx(&tb.full[slot], bytes);
+      return ring + slot * SLOT_BYTES;
+    };
+    auto advance = [&]() {
+      ++j;
+      if (++slot == NS) {
+        slot = 0;
+        ++use;
+      }
+    };
     if (lane == 0) {
-      const int n_act = tb.n_act, n_actg = tb.n_actg;
+      {  // router: (segment, expert pair)
+        int ks = a1lo / NPAIR, pr = a1lo % NPAIR;
+#pragma unroll 1
+        for (int i = a1lo; ok && i < a1hi; ++i) {
+          unsigned char* dst = claim(2 * KSEG * 4);
+          if (!dst) break;
+          tma_load_3d(dst, &F.maps.wr, 0, ks * (KSEG / 256), 2 * pr, &tb.full[slot]);
+          advance();
+          if (++pr == NPAIR) { pr = 0; ++ks; }
+        }
+      }
+      {  // W_in: (segment, group, 16-row tile)
+        const int per_ks = G * NRT_IN;
+        int ks = a2lo / per_ks, row = a2lo % per_ks;  // row tile index g * NRT_IN + rt
+#pragma unroll 1
+        for (int i = a2lo; ok && i < a2hi; ++i) {
+          unsigned char* dst = claim(16 * KSEG / 2 + 16 * KSEG / 16);
+          if (!dst) break;
+          tma_load_3d(dst, &F.maps.win_q, 0, ks * (KSEG / 256), row * 16, &tb.full[slot]);
+          tma_load_2d(dst + 16 * KSEG / 2, &F.maps.win_s, ks * (KSEG / 32), row * 16, &tb.full[slot]);
+          advance();
+          if (++row == per_ks) { row = 0; ++ks; }
+        }
+      }
+      if (ok) {  // the routing tables (built by the consumers)
+        const long long t0 = clock64();
+#pragma unroll 1
+        while (tb.tables_ready == 0) {
+          if (clock64() - t0 > budget) {
+            set_error(err, ERRBIT_TIMEOUT);
+            ok = false;
+            break;
+          }
+          __nanosleep(64);
+        }
+        __threadfence_block();
+      }
+      const int n_act = tb.n_act, n_actg = tb.n_actg, FT = f / 16;
       int lo = 0, hi = 0;
-      if (ok) split(n_act * (f / 16), c, nC, lo, hi);
-      #pragma unroll 1
-      for (int i = lo; ok && i < hi; ++i) {
-        const int es = i / (f / 16), rt = i % (f / 16), e = tb.elist[es];
-        #pragma unroll 1
-        for (int gu = 0; gu < 2; ++gu, ++j) {
-          unsigned char* dst = prod_begin<NS>(tb, ring, j, 16 * L / 2 + 16 * L / 16, budget, err);
-          if (!(ok = dst != nullptr)) break;
-          tma_load_3d(dst, gu ? &F.maps.up_q : &F.maps.gate_q, 0, 0, e * f + rt * 16, &tb.full[j % NS]);
-          tma_load_2d(dst + 16 * L / 2, gu ? &F.maps.up_s : &F.maps.gate_s, 0, e * f + rt * 16, &tb.full[j % NS]);
+      if (ok) split(n_act * FT, c, nC, lo, hi);
+      {  // gate/up: (expert slot, 16-row tile), gate then up
+        int es = lo / FT, rt = lo % FT;
+        int e = es < n_act ? tb.elist[es] : 0;
+#pragma unroll 1
+        for (int i = lo; ok && i < hi; ++i) {
+          const int row = e * f + rt * 16;
+          unsigned char* dst = claim(16 * L / 2 + 16 * L / 16);
+          if (!dst) break;
+          tma_load_3d(dst, &F.maps.gate_q, 0, 0, row, &tb.full[slot]);
+          tma_load_2d(dst + 16 * L / 2, &F.maps.gate_s, 0, row, &tb.full[slot]);
+          advance();
+          dst = claim(16 * L / 2 + 16 * L / 16);
+          if (!dst) break;
+          tma_load_3d(dst, &F.maps.up_q, 0, 0, row, &tb.full[slot]);
+          tma_load_2d(dst + 16 * L / 2, &F.maps.up_s, 0, row, &tb.full[slot]);
+          advance();
+          if (++rt == FT) {
+            rt = 0;
+            if (++es < n_act) e = tb.elist[es];
+          }
         }
       }
       if (ok) split(n_act * NRB, c, nC, lo, hi);
-      #pragma unroll 1
-      for (int i = lo; ok && i < hi; ++i, ++j) {
-        const int es = i / NRB, rb = i % NRB, e = tb.elist[es];
-        unsigned char* dst = prod_begin<NS>(tb, ring, j, DR * f / 2 + DR * f / 16, budget, err);
-        if (!(ok = dst != nullptr)) break;
-        tma_load_3d(dst, &F.maps.down_q, 0, 0, e * L + rb * DR, &tb.full[j % NS]);
-        tma_load_2d(dst + DR * f / 2, &F.maps.down_s, 0, e * L + rb * DR, &tb.full[j % NS]);
+      {  // down: (expert slot, 32-row block)
+        int es = lo / NRB, rb = lo % NRB;
+        int e = es < n_act ? tb.elist[es] : 0;
+#pragma unroll 1
+        for (int i = lo; ok && i < hi; ++i) {
+          const int row = e * L + rb * DR;
+          unsigned char* dst = claim(DR * f / 2 + DR * f / 16);
+          if (!dst) break;
+          tma_load_3d(dst, &F.maps.down_q, 0, 0, row, &tb.full[slot]);
+          tma_load_2d(dst + DR * f / 2, &F.maps.down_s, 0, row, &tb.full[slot]);
+          advance();
+          if (++rb == NRB) {
+            rb = 0;
+            if (++es < n_act) e = tb.elist[es];
+          }
+        }
       }
       if (ok) split(n_actg * NRT_OUT, c, nC, lo, hi);
-      #pragma unroll 1
-      for (int i = lo; ok && i < hi; ++i, ++j) {
-        const int gi = i / NRT_OUT, rt = i % NRT_OUT, g = tb.glist[gi];
-        unsigned char* dst = prod_begin<NS>(tb, ring, j, 16 * L / 2 + 16 * L / 16, budget, err);
-        if (!(ok = dst != nullptr)) break;
-        tma_load_3d(dst, &F.maps.wout_q, 0, 0, g * d + rt * 16, &tb.full[j % NS]);
-        tma_load_2d(dst + 16 * L / 2, &F.maps.wout_s, 0, g * d + rt * 16, &tb.full[j % NS]);
+      {  // W_out: (group slot, 16-row tile)
+        int gi = lo / NRT_OUT, rt = lo % NRT_OUT;
+        int g = gi < n_actg ? tb.glist[gi] : 0;
+#pragma unroll 1
+        for (int i = lo; ok && i < hi; ++i) {
+          const int row = g * d + rt * 16;
+          unsigned char* dst = claim(16 * L / 2 + 16 * L / 16);
+          if (!dst) break;
+          tma_load_3d(dst, &F.maps.wout_q, 0, 0, row, &tb.full[slot]);
+          tma_load_2d(dst + 16 * L / 2, &F.maps.wout_s, 0, row, &tb.full[slot]);
+          advance();
+          if (++rt == NRT_OUT) {
+            rt = 0;
+            if (++gi < n_actg) g = tb.glist[gi];
+          }
+        }
       }
       // Wait for the copies still in flight before the CTA may exit. They do
       // not depend on other CTAs, so this drain gets a budget of its own.
       const long long drain = budget > (1ll << 28) ? budget : (1ll << 28);
-      #pragma unroll 1
+#pragma unroll 1
       for (int jj = (j > NS ? j - NS : 0); jj < j; ++jj) mbar_wait(&tb.full[jj % NS], (jj / NS) & 1, drain, err);
     }
     return;

@@ -118,14 +118,28 @@ LMOE_DEV void mma_ring_rows_swz(const unsigned char* w, int LPR, int row0, const
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int h = 0; h < 4; ++h) acc2[nt][h] = 0.f;
+  // the next chunk's weights and scales are loaded while this one is contracted
+  auto ld = [&](int c, uint4& a, uint4& b, uint16_t& sa, uint16_t& sb) {
+    const int i0 = r0 * LPR + (c >> 1), i8 = r8 * LPR + (c >> 1), j = ((c & 1) << 2) | tig;
+    a = *reinterpret_cast<const uint4*>(w + i0 * 128 + ((j ^ (i0 & 7)) << 4));
+    b = *reinterpret_cast<const uint4*>(w + i8 * 128 + ((j ^ (i8 & 7)) << 4));
+    sa = s0[c * 4];
+    sb = s8[c * 4];
+  };
+  uint4 a, b;
+  uint16_t sa, sb;
+  ld(0, a, b, sa, sb);
 #pragma unroll 1
   for (int c = 0; c < nc; ++c) {
-    const int i0 = r0 * LPR + (c >> 1), i8 = r8 * LPR + (c >> 1), j = ((c & 1) << 2) | tig;
-    const uint4 a = *reinterpret_cast<const uint4*>(w + i0 * 128 + ((j ^ (i0 & 7)) << 4));
-    const uint4 b = *reinterpret_cast<const uint4*>(w + i8 * 128 + ((j ^ (i8 & 7)) << 4));
-    const __half2 h0 = scale_h2(s0[c * 4]), h8 = scale_h2(s8[c * 4]);
     const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
     const uint32_t wb[4] = {b.x, b.y, b.z, b.w};
+    const __half2 h0 = scale_h2(sa), h8 = scale_h2(sb);
+    if (c + 1 < nc) ld(c + 1, a, b, sa, sb);
+    uint4 fv[4][NT];
+#pragma unroll
+    for (int mp = 0; mp < 4; ++mp)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) fv[mp][nt] = frag[frag_index(c, nt, mp, lane, NT)];
 #pragma unroll
     for (int mp = 0; mp < 4; ++mp) {
       uint32_t A[4], B8[4];
@@ -133,7 +147,7 @@ LMOE_DEV void mma_ring_rows_swz(const unsigned char* w, int LPR, int row0, const
       dequant_word(wb[mp], h8, B8);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const uint4 f = frag[frag_index(c, nt, mp, lane, NT)];
+        const uint4 f = fv[mp][nt];
         mma16816(acc[nt], A[0], B8[0], A[1], B8[1], f.x, f.y);
         mma16816(acc2[nt], A[2], B8[2], A[3], B8[3], f.z, f.w);
       }
@@ -157,18 +171,32 @@ LMOE_DEV void mma_ring_rows_swz2(const unsigned char* w1, const uint16_t* s1, co
   const uint16_t* s18 = s1 + r8 * SS + tig;
   const uint16_t* s20 = s2 + r0 * SS + tig;
   const uint16_t* s28 = s2 + r8 * SS + tig;
-#pragma unroll 1
-  for (int c = 0; c < nc; ++c) {
+  auto ld = [&](int c, uint4& a, uint4& b, uint4& a2, uint4& b2, uint16_t (&sc)[4]) {
     const int i0 = r0 * LPR + (c >> 1), i8 = r8 * LPR + (c >> 1), j = ((c & 1) << 2) | tig;
     const int o0 = i0 * 128 + ((j ^ (i0 & 7)) << 4), o8 = i8 * 128 + ((j ^ (i8 & 7)) << 4);
-    const uint4 a = *reinterpret_cast<const uint4*>(w1 + o0);
-    const uint4 b = *reinterpret_cast<const uint4*>(w1 + o8);
-    const uint4 a2 = *reinterpret_cast<const uint4*>(w2 + o0);
-    const uint4 b2 = *reinterpret_cast<const uint4*>(w2 + o8);
-    const __half2 h0 = scale_h2(s10[c * 4]), h8 = scale_h2(s18[c * 4]);
-    const __half2 g0 = scale_h2(s20[c * 4]), g8 = scale_h2(s28[c * 4]);
+    a = *reinterpret_cast<const uint4*>(w1 + o0);
+    b = *reinterpret_cast<const uint4*>(w1 + o8);
+    a2 = *reinterpret_cast<const uint4*>(w2 + o0);
+    b2 = *reinterpret_cast<const uint4*>(w2 + o8);
+    sc[0] = s10[c * 4];
+    sc[1] = s18[c * 4];
+    sc[2] = s20[c * 4];
+    sc[3] = s28[c * 4];
+  };
+  uint4 a, b, a2, b2;
+  uint16_t sc[4];
+  ld(0, a, b, a2, b2, sc);
+#pragma unroll 1
+  for (int c = 0; c < nc; ++c) {
     const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
     const uint32_t va[4] = {a2.x, a2.y, a2.z, a2.w}, vb[4] = {b2.x, b2.y, b2.z, b2.w};
+    const __half2 h0 = scale_h2(sc[0]), h8 = scale_h2(sc[1]), g0 = scale_h2(sc[2]), g8 = scale_h2(sc[3]);
+    if (c + 1 < nc) ld(c + 1, a, b, a2, b2, sc);
+    uint4 fv[4][NT];
+#pragma unroll
+    for (int mp = 0; mp < 4; ++mp)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) fv[mp][nt] = frag[frag_index(c, nt, mp, lane, NT)];
 #pragma unroll
     for (int mp = 0; mp < 4; ++mp) {
       uint32_t A[4], B8[4], C[4], D8[4];
@@ -178,7 +206,7 @@ LMOE_DEV void mma_ring_rows_swz2(const unsigned char* w1, const uint16_t* s1, co
       dequant_word(vb[mp], g8, D8);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const uint4 f = frag[frag_index(c, nt, mp, lane, NT)];
+        const uint4 f = fv[mp][nt];
         mma16816(acc1[nt], A[0], B8[0], A[1], B8[1], f.x, f.y);
         mma16816(acc2[nt], C[0], D8[0], C[1], D8[1], f.x, f.y);
         mma16816(acc1[nt], A[2], B8[2], A[3], B8[3], f.z, f.w);
