@@ -246,75 +246,67 @@ LMOE_DEV void cons_release(Tables& tb, int j) {
 // lane holds logits lane, lane+32, ... (E <= 512) and its best remaining one;
 // every round the warp picks the best lane head (ties -> lower index) and only
 // the winner rescans. Lane j < k returns the j-th expert and its weight.
+// order-preserving key of a float (larger float <-> larger key)
+LMOE_DEV unsigned float_key(float x) {
+  const unsigned b = __float_as_uint(x);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+LMOE_DEV float key_float(unsigned k) { return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k); }
+
 LMOE_COLD float2 topk_warp(const float* row, int E, int k) {
-  int sel_e;
-  float sel_w;
   const int lane = threadIdx.x & 31;
-  float v[16];
+  unsigned key[16];  // element i is expert lane + 32 i; 0 = none (below every finite key)
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = (lane + 32 * i < E) ? __ldcg(row + lane + 32 * i) : -INFINITY;
-  // best remaining logit of this lane (ties -> lower index): a depth-4
-  // tournament; element i has index lane + 32 i, so a later element wins
-  // only when strictly larger
-  auto lane_best = [&](float& bv, int& be) {
-    float tv[8];
+  for (int i = 0; i < 16; ++i) key[i] = lane + 32 * i < E ? float_key(__ldcg(row + lane + 32 * i)) : 0u;
+  // this lane's best remaining element, ties to the lower i: a depth-4 tournament
+  auto best = [&](unsigned& bk, int& bi) {
+    unsigned tk[8];
     int ti[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const bool hi = v[2 * i + 1] > v[2 * i];
-      tv[i] = hi ? v[2 * i + 1] : v[2 * i];
+      const bool hi = key[2 * i + 1] > key[2 * i];
+      tk[i] = hi ? key[2 * i + 1] : key[2 * i];
       ti[i] = hi ? 2 * i + 1 : 2 * i;
     }
 #pragma unroll
     for (int w = 4; w >= 1; w >>= 1)
 #pragma unroll
       for (int i = 0; i < w; ++i) {
-        const bool hi = tv[2 * i + 1] > tv[2 * i];
-        tv[i] = hi ? tv[2 * i + 1] : tv[2 * i];
+        const bool hi = tk[2 * i + 1] > tk[2 * i];
+        tk[i] = hi ? tk[2 * i + 1] : tk[2 * i];
         ti[i] = hi ? ti[2 * i + 1] : ti[2 * i];
       }
-    bv = tv[0];
-    be = lane + 32 * ti[0];
-    if (be >= E || bv == -INFINITY) be = 0x7fffffff;
+    bk = tk[0];
+    bi = ti[0];
   };
-  float mv;
-  int me;
-  lane_best(mv, me);
-  float sel = 0.f, l0 = 0.f;
-  sel_e = 0;
-  #pragma unroll 1
+  unsigned bk;
+  int bi;
+  best(bk, bi);
+  unsigned sel = 0, k0 = 0;
+  int sel_e = 0;
+  // each round: the warp's largest key, then the lowest expert index holding it
+#pragma unroll 1
   for (int j = 0; j < k; ++j) {
-    float bv = mv;
-    int be = me;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (ov > bv || (ov == bv && oe < be)) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    if (be >= E) be = 0;
-    if (be == me) {
+    const unsigned m = __reduce_max_sync(0xffffffffu, bk);
+    const int mine = lane + 32 * bi;
+    const unsigned wi = __reduce_min_sync(0xffffffffu, bk == m ? (unsigned)mine : 0xffffffffu);
+    if ((unsigned)mine == wi) {
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        if (lane + 32 * i == be) v[i] = -INFINITY;
-      lane_best(mv, me);
-      if (mv == -INFINITY) me = 0x7fffffff;
+        if (i == bi) key[i] = 0u;
+      best(bk, bi);
     }
-    if (j == 0) l0 = bv;
+    if (j == 0) k0 = m;
     if (lane == j) {
-      sel = bv;
-      sel_e = be;
+      sel = m;
+      sel_e = wi < (unsigned)E ? (int)wi : 0;
     }
   }
-  const float ex = (lane < k) ? __expf(sel - l0) : 0.f;
+  const float ex = (lane < k) ? __expf(key_float(sel) - key_float(k0)) : 0.f;
   float z = ex;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-  sel_w = ex / z;
-  return make_float2(__int_as_float(sel_e), sel_w);
+  return make_float2(__int_as_float(sel_e), ex / z);
 }
 
 // Routed-expert and routed-group tables from the token masks (one warp):
