@@ -427,7 +427,7 @@ def run_ours(args):
                        "distinct_experts": int(len(np.unique(idx_np))),
                        "active_groups": int(len(np.unique(idx_np // (sh.E // sh.G))))},
             "roofline": roofline, "stages_us": {n: 1000 * v for n, v in per.items()},
-            "e2e": e2e, "gpu_launches": n_kernels * args.steps, "clocks": ck}
+            "e2e": e2e, "gpu_launches": capi.lmoe_launch_count(layers[0].h, T) * args.steps, "clocks": ck}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, reps, n = oracle_tokens_per_s(args.workload)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
@@ -483,7 +483,7 @@ def run_stack(args):
         total_flops += sum(sf.values())
         yl = m.forward(cur)
         cur = (cur.float() + yl.float()).to(torch.bfloat16)
-    per_layer = capi.lmoe_stage_name(layers[0].h, T, 0)[1]
+    per_layer = capi.lmoe_launch_count(layers[0].h, T)
     stack.forward(xt, out=y)
     torch.cuda.synchronize()
     cap = torch.cuda.Stream()

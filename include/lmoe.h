@@ -263,12 +263,19 @@ lmoe_status lmoe_set_timeout(lmoe_handle* h, long long cycles);
 /* Profiling hook: when events != NULL, lmoe_layer_forward records
  * events[2*i] / events[2*i+1] (cudaEvent_t) on its stream around launch i of
  * its kernel sequence, for i < n. The stage names are given by
- * lmoe_stage_name. Pass NULL to turn it off. */
+ * lmoe_stage_name; in the prefill path, a stage (for instance "route": the
+ * router GEMM and the top-k kernel) may span several kernels. Pass NULL to
+ * turn it off. */
 lmoe_status lmoe_set_stage_events(lmoe_handle* h, void* const* events, int n);
 
 /* Name of kernel i of lmoe_layer_forward's sequence for T tokens ("" if none),
  * and the count of kernels launched per call through *count. */
 const char* lmoe_stage_name(const lmoe_handle* h, int T, int i, int* count);
+
+/* Number of kernels one lmoe_layer_forward call launches for T tokens (a
+ * stage of the prefill path may launch several); 0 for a null handle or
+ * T < 1. Host only; launches nothing. */
+int lmoe_launch_count(const lmoe_handle* h, int T);
 
 #ifdef __cplusplus
 }

@@ -21,7 +21,8 @@ FLAG_MULTI_KERNEL_DECODE = 1
 EXPORTS = ("lmoe_status_string", "lmoe_version", "lmoe_create", "lmoe_destroy", "lmoe_workspace_size", "lmoe_route",
            "lmoe_permute", "lmoe_expert_forward", "lmoe_combine", "lmoe_layer_forward", "lmoe_layer_forward_noalloc",
            "lmoe_layer_forward_host", "lmoe_stack_forward", "lmoe_stack_workspace_size",
-           "lmoe_host_staging_size", "lmoe_check", "lmoe_set_timeout", "lmoe_set_stage_events", "lmoe_stage_name")
+           "lmoe_host_staging_size", "lmoe_check", "lmoe_set_timeout", "lmoe_set_stage_events", "lmoe_stage_name",
+           "lmoe_launch_count")
 
 
 class LmoeError(RuntimeError):
@@ -80,6 +81,7 @@ def _load():
         "lmoe_set_timeout": ([P, ctypes.c_longlong], S),
         "lmoe_set_stage_events": ([P, P, I], S),
         "lmoe_stage_name": ([P, I, I, ctypes.POINTER(I)], ctypes.c_char_p),
+        "lmoe_launch_count": ([P, I], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -188,6 +190,10 @@ def lmoe_set_timeout(h, cycles: int) -> None:
 
 def lmoe_set_stage_events(h, events_ptr, n: int) -> None:
     _ok(_lib.lmoe_set_stage_events(h, events_ptr, int(n)), "lmoe_set_stage_events")
+
+
+def lmoe_launch_count(h, T: int) -> int:
+    return int(_lib.lmoe_launch_count(h, int(T)))
 
 
 def lmoe_stage_name(h, T: int, i: int):

@@ -705,4 +705,12 @@ const char* lmoe_stage_name(const lmoe_handle* h, int T, int i, int* count) {
   return lora ? dec_lora[i % per] : dec[i % per];
 }
 
+int lmoe_launch_count(const lmoe_handle* h, int T) {
+  if (!h || T < 1) return 0;
+  if (use_prefill(h, T)) return prefill_launch_count(prefill_args(h), T);
+  int n = 0;
+  lmoe_stage_name(h, T, 0, &n);  // decode: one kernel per stage
+  return n;
+}
+
 }  // extern "C"

@@ -36,6 +36,7 @@
 #include "decode.cuh"
 #include "ring.cuh"
 #include "tmap.cuh"
+#include "topk.cuh"
 
 namespace lmoe {
 
@@ -242,73 +243,6 @@ LMOE_DEV void cons_release(Tables& tb, int j) {
 }  // namespace
 
 // ==================================================================== kernel
-// Top-k with softmax renormalisation of one token's logits by one warp: each
-// lane holds logits lane, lane+32, ... (E <= 512) and its best remaining one;
-// every round the warp picks the best lane head (ties -> lower index) and only
-// the winner rescans. Lane j < k returns the j-th expert and its weight.
-// order-preserving key of a float (larger float <-> larger key)
-LMOE_DEV unsigned float_key(float x) {
-  const unsigned b = __float_as_uint(x);
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-LMOE_DEV float key_float(unsigned k) { return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k); }
-
-LMOE_COLD float2 topk_warp(const float* row, int E, int k) {
-  const int lane = threadIdx.x & 31;
-  unsigned key[16];  // element i is expert lane + 32 i; 0 = none (below every finite key)
-#pragma unroll
-  for (int i = 0; i < 16; ++i) key[i] = lane + 32 * i < E ? float_key(__ldcg(row + lane + 32 * i)) : 0u;
-  // this lane's best remaining element, ties to the lower i: a depth-4 tournament
-  auto best = [&](unsigned& bk, int& bi) {
-    unsigned tk[8];
-    int ti[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const bool hi = key[2 * i + 1] > key[2 * i];
-      tk[i] = hi ? key[2 * i + 1] : key[2 * i];
-      ti[i] = hi ? 2 * i + 1 : 2 * i;
-    }
-#pragma unroll
-    for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-      for (int i = 0; i < w; ++i) {
-        const bool hi = tk[2 * i + 1] > tk[2 * i];
-        tk[i] = hi ? tk[2 * i + 1] : tk[2 * i];
-        ti[i] = hi ? ti[2 * i + 1] : ti[2 * i];
-      }
-    bk = tk[0];
-    bi = ti[0];
-  };
-  unsigned bk;
-  int bi;
-  best(bk, bi);
-  unsigned sel = 0, k0 = 0;
-  int sel_e = 0;
-  // each round: the warp's largest key, then the lowest expert index holding it
-#pragma unroll 1
-  for (int j = 0; j < k; ++j) {
-    const unsigned m = __reduce_max_sync(0xffffffffu, bk);
-    const int mine = lane + 32 * bi;
-    const unsigned wi = __reduce_min_sync(0xffffffffu, bk == m ? (unsigned)mine : 0xffffffffu);
-    if ((unsigned)mine == wi) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        if (i == bi) key[i] = 0u;
-      best(bk, bi);
-    }
-    if (j == 0) k0 = m;
-    if (lane == j) {
-      sel = m;
-      sel_e = wi < (unsigned)E ? (int)wi : 0;
-    }
-  }
-  const float ex = (lane < k) ? __expf(key_float(sel) - key_float(k0)) : 0.f;
-  float z = ex;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-  return make_float2(__int_as_float(sel_e), ex / z);
-}
-
 // Routed-expert and routed-group tables from the token masks (one warp):
 // elist = routed experts ascending, glist = their groups, gslot0[gi] = first
 // slot of group gi in elist (gslot0[n_actg] = n_act).

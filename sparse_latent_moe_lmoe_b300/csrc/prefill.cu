@@ -1,15 +1,14 @@
 // Prefill path of the latent MoE layer (many tokens): the router and every
-// projection are GEMMs on the tcgen05 tensor cores (tc_gemm.cuh). The two
-// shared matrices, which every token tile of a group multiplies, are
-// dequantised to fp16 once per call and fed to the tensor cores by TMA; the
-// per-expert int4 weights are dequantised by the GEMM's own producer warps.
+// projection are GEMMs on the tcgen05 tensor cores (tc_gemm.cuh), both
+// operands fed by TMA wherever their rows are contiguous. The int4 matrices
+// are dequantised to fp16 once per call (q*s is exact in fp16).
 //
-//   dequant  Win, Wout -> fp16 (q*s is exact in fp16), x -> fp16
+//   dequant  Win, Wout, Gate, Up, Down -> fp16, x -> fp16
 //
 //   route    logits = x . (W_hi + W_mid + W_lo)^T  (W_r split into three
 //            bf16 terms at create time; x is exact in bf16; fp32 accumulate)
-//            with the top-k and softmax renormalisation in the epilogue
-//            (one thread per token, all E logits of its row from TMEM)
+//            in 128-token x 256-expert tiles, then the top-k and softmax
+//            renormalisation by one warp per token over its E logits
 //   permute  the deterministic multi-CTA permutation (permute.cu)
 //   win      H[g][t] = Win[g] x_t for every (g, t) (dense; rows of tokens
 //            with no expert in g are never read)
@@ -20,7 +19,7 @@
 //   wout     y_t = sum_g Wout[g] Z[(g,t)] (+ residual): one GEMM over K =
 //            G*L per token tile (absent (g,t) rows read as zero), so the
 //            weighted combine happens in the accumulator
-// Intermediates H, V, Z are fp16 tensor-core operands, U is fp32.
+// Intermediates H, V, U, Z are fp16 (fp32 accumulation everywhere).
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -28,6 +27,7 @@
 #include "prefill.cuh"
 #include "tc_gemm.cuh"
 #include "tmap.cuh"
+#include "topk.cuh"
 
 namespace lmoe {
 
@@ -106,21 +106,22 @@ LMOE_DEV void store_half16(__half* dst, const float v[16]) {
 
 // ------------------------------------------------------------------ router
 struct ProbRoute : ProbBase {
-  static constexpr int BN = 512, ACC_COLS = 512, A_MODE = 3, B_MODE = 2, STAGES = 2;
+  // logits[t][e] (+ bias) for 128 tokens x 256 experts per tile; the top-k
+  // runs afterwards (route_topk_kernel), one warp per token.
+  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 3, B_MODE = 2, STAGES = 4;
   CUtensorMap am;         // x as [T][d] bf16, box {64, 128}
   CUtensorMap bm;         // the split W_r as [3][E][d] bf16, box {64, 256, 1}
   const float* bias;      // [E] or null
-  int T, d, E, k;
-  int32_t* idx;
-  float* w;
-  float* logits;          // [T][E] or null
+  int T, d, E;
+  float* logits;          // [T][E]
+  LMOE_DEV int ntn() const { return (E + 255) / 256; }
   LMOE_DEV void init(int*) const {}
-  LMOE_DEV int num_tiles(const int*) const { return (T + 127) / 128; }
+  LMOE_DEV int num_tiles(const int*) const { return ((T + 127) / 128) * ntn(); }
   LMOE_DEV Tile tile(const int*, int t) const {
     Tile tl;
     tl.prob = 0;
-    tl.m0 = t * 128;
-    tl.n0 = 0;
+    tl.m0 = (t / ntn()) * 128;  // both expert halves of a token tile run side by side (x shared in L2)
+    tl.n0 = (t % ntn()) * 256;
     tl.rows = min(128, T - tl.m0);
     tl.nkb = 3 * (d / 64);
     return tl;
@@ -130,9 +131,8 @@ struct ProbRoute : ProbBase {
   LMOE_DEV void load_a(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
     tma_load_2d(dst, &am, (kb / 3) * 64, tl.m0, bar);
   }
-  LMOE_DEV void load_b(const Tile&, int kb, void* dst, uint64_t* bar) const {
-    tma_load_3d(dst, &bm, (kb / 3) * 64, 0, kb % 3, bar);
-    tma_load_3d(static_cast<char*>(dst) + 256 * 128, &bm, (kb / 3) * 64, 256, kb % 3, bar);
+  LMOE_DEV void load_b(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
+    tma_load_3d(dst, &bm, (kb / 3) * 64, tl.n0, kb % 3, bar);
   }
   LMOE_DEV const void* a_row(const int*, const Tile&, int, int) const { return nullptr; }
   LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int, int) const { return nullptr; }
@@ -140,72 +140,45 @@ struct ProbRoute : ProbBase {
   LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
     const uint32_t id = tc::idesc(128, 256, 1);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
-      tc::mma_f16(d_tmem, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), id, acc);
-      tc::mma_f16(d_tmem + 256, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k) + (uint64_t)((256 * 128) >> 4), id, acc);
-    }
+    for (int k = 0; k < 4; ++k)
+      tc::mma_f16(d_tmem, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), id, (kb > 0 || k > 0) ? 1u : 0u);
   }
-  // one thread per token: top-k (descending logit, ties to the lower index)
-  // over the row's E logits, softmax over the selected ones
+  // one thread per token row: 256 logits (+ bias) to global memory
   LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase) const {
-    float tv[16];
-    int te[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      tv[j] = -INFINITY;
-      te[j] = 0x7fffffff;
-    }
     const bool valid = row < tl.rows;
-    const int t = tl.m0 + row;
-    for (int c0 = 0; c0 < 512; c0 += 16) {
+    float* out = logits + (size_t)(tl.m0 + row) * E + tl.n0;
+    const int ne = min(256, E - tl.n0);
+    for (int c0 = 0; c0 < 256; c0 += 16) {
       float v[16];
       tc::tmem_ld16(tbase + (uint32_t)c0, v);  // warp-collective: every lane loads
-      if (!valid || c0 >= E) continue;
+      if (!valid || c0 >= ne) continue;
+      if (bias) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int e = c0 + i;
-        if (e >= E) continue;
-        float l = v[i];
-        if (bias) l += bias[e];
-        if (logits) logits[(size_t)t * E + e] = l;
-        // insert if strictly better than the current k-th (an equal later index loses)
-        float kth = tv[15];
+        for (int i = 0; i < 16; ++i) v[i] += c0 + i < ne ? bias[tl.n0 + c0 + i] : 0.f;
+      }
+      if (c0 + 16 <= ne) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (j == k - 1) kth = tv[j];
-        if (l > kth) {
-          float cv = l;
-          int ce = e;
+        for (int i = 0; i < 16; i += 4) *reinterpret_cast<float4*>(out + c0 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+      } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            if (j < k && cv > tv[j]) {
-              const float sv = tv[j];
-              const int se = te[j];
-              tv[j] = cv;
-              te[j] = ce;
-              cv = sv;
-              ce = se;
-            }
-          }
-        }
+        for (int i = 0; i < 16; ++i)
+          if (c0 + i < ne) out[c0 + i] = v[i];
       }
     }
-    if (!valid) return;
-    float z = 0.f, ex[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      ex[j] = j < k ? __expf(tv[j] - tv[0]) : 0.f;
-      z += ex[j];
-    }
-#pragma unroll
-    for (int j = 0; j < 16; ++j)
-      if (j < k) {
-        idx[(size_t)t * k + j] = te[j];
-        w[(size_t)t * k + j] = ex[j] / z;
-      }
   }
 };
+
+// top-k with softmax renormalisation, one warp per token
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                         int32_t* __restrict__ idx, float* __restrict__ w) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const float2 sw = topk_warp(logits + (size_t)t * E, E, k);
+  if (lane < k) {
+    idx[(size_t)t * k + lane] = __float_as_int(sw.x);
+    w[(size_t)t * k + lane] = sw.y;
+  }
+}
 
 // -------------------------------------------------------------------- W_in
 struct ProbWin : ProbBase {
@@ -314,7 +287,7 @@ struct ProbDown : ProbBase {
   const int32_t* eo;
   const int32_t* sa;
   const float* wts;  // [T*k]
-  float* U;  // [T*k][L]
+  __half* U;  // [T*k][L]
   LMOE_DEV int ntn() const { return L / 256; }
   LMOE_DEV void init(int* sc) const {
     tile_prefix(sc, E, [&](int e) { return ((eo[e + 1] - eo[e] + 127) / 128) * ntn(); });
@@ -352,9 +325,11 @@ struct ProbDown : ProbBase {
       float v[16];
       tc::tmem_ld16(tbase + (uint32_t)c0, v);
       if (!valid) continue;
-      float4* dst = reinterpret_cast<float4*>(U + (size_t)p * L + tl.n0 + c0);
+      uint4* dst = reinterpret_cast<uint4*>(U + (size_t)p * L + tl.n0 + c0);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) dst[i] = make_float4(wt * v[4 * i], wt * v[4 * i + 1], wt * v[4 * i + 2], wt * v[4 * i + 3]);
+      for (int i = 0; i < 2; ++i)
+        dst[i] = make_uint4(pack_half2(wt * v[8 * i], wt * v[8 * i + 1]), pack_half2(wt * v[8 * i + 2], wt * v[8 * i + 3]),
+                            pack_half2(wt * v[8 * i + 4], wt * v[8 * i + 5]), pack_half2(wt * v[8 * i + 6], wt * v[8 * i + 7]));
     }
   }
 };
@@ -445,7 +420,7 @@ struct ProbWout : ProbBase {
 // ----------------------------------------------------------------- zreduce
 // One warp per (group, token) row: Z[row] = sum over the token's experts in
 // that group, in ascending j, of U[inv[t*k + j]]; tokrow[t][g] = row.
-__global__ void zreduce_kernel(const float* __restrict__ U, const int32_t* __restrict__ idx,
+__global__ void zreduce_kernel(const __half* __restrict__ U, const int32_t* __restrict__ idx,
                                const int32_t* __restrict__ inv, const int32_t* __restrict__ gto,
                                const int32_t* __restrict__ gtok, int G, int k, int epg, int L, __half* __restrict__ Z,
                                int32_t* __restrict__ tokrow) {
@@ -459,10 +434,11 @@ __global__ void zreduce_kernel(const float* __restrict__ U, const int32_t* __res
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < k; ++j) {
       if (idx[(size_t)t * k + j] / epg != g) continue;
-      const float4* u = reinterpret_cast<const float4*>(U + (size_t)inv[(size_t)t * k + j] * L + c);
-      const float4 a = u[0], b = u[1];
-      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+      const uint4 u = __ldcs(reinterpret_cast<const uint4*>(U + (size_t)inv[(size_t)t * k + j] * L + c));
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x)), b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+      const float2 c2 = __half22float2(*reinterpret_cast<const __half2*>(&u.z)), d2 = __half22float2(*reinterpret_cast<const __half2*>(&u.w));
+      acc[0] += a.x; acc[1] += a.y; acc[2] += b.x; acc[3] += b.y;
+      acc[4] += c2.x; acc[5] += c2.y; acc[6] += d2.x; acc[7] += d2.y;
     }
     uint4 o;
     o.x = pack_half2(acc[0], acc[1]);
@@ -476,7 +452,7 @@ __global__ void zreduce_kernel(const float* __restrict__ U, const int32_t* __res
 // Mode-0 operand of W_out: Ztok[t][g][:] = sum over the token's experts in
 // group g, in ascending j, of U[inv[t*k + j]], or zero when the token has no
 // expert in g. One warp per (t, g).
-__global__ void zreduce_tok_kernel(const float* __restrict__ U, const int32_t* __restrict__ idx,
+__global__ void zreduce_tok_kernel(const __half* __restrict__ U, const int32_t* __restrict__ idx,
                                    const int32_t* __restrict__ inv, int T, int G, int k, int epg, int L,
                                    __half* __restrict__ Ztok) {
   const int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
@@ -487,10 +463,11 @@ __global__ void zreduce_tok_kernel(const float* __restrict__ U, const int32_t* _
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < k; ++j) {
       if (idx[(size_t)t * k + j] / epg != g) continue;
-      const float4* u = reinterpret_cast<const float4*>(U + (size_t)inv[(size_t)t * k + j] * L + c);
-      const float4 a = u[0], b = u[1];
-      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+      const uint4 u = __ldcs(reinterpret_cast<const uint4*>(U + (size_t)inv[(size_t)t * k + j] * L + c));
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x)), b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+      const float2 c2 = __half22float2(*reinterpret_cast<const __half2*>(&u.z)), d2 = __half22float2(*reinterpret_cast<const __half2*>(&u.w));
+      acc[0] += a.x; acc[1] += a.y; acc[2] += b.x; acc[3] += b.y;
+      acc[4] += c2.x; acc[5] += c2.y; acc[6] += d2.x; acc[7] += d2.y;
     }
     uint4 o;
     o.x = pack_half2(acc[0], acc[1]);
@@ -523,33 +500,48 @@ cudaError_t launch_split_router(const float* W_r, int E, int d, uint16_t* out, c
   return cudaGetLastError();
 }
 
-// int4 rows [rows][K/2] + bf16 scales [rows][K/32] -> fp16 [rows][K]; one
-// scale group (16 bytes of int4, 32 elements, natural order) per thread and step
-__global__ void dequant_f16_kernel(const uint8_t* __restrict__ q, const uint16_t* __restrict__ s, size_t groups,
-                                   __half* __restrict__ out) {
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < groups; i += (size_t)gridDim.x * blockDim.x) {
-    const uint4 v = ldg_stream(q + i * 16);
-    const __half2 s2 = scale_h2(__ldg(s + i));
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint4* o4 = reinterpret_cast<uint4*>(out) + i * 4;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      uint32_t o[4];
-      tc::dequant_word_natural(w[j], s2, o);
-      o4[j] = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-  }
-}
+// Every int4 matrix to fp16 and x to fp16, in one launch. An int4 matrix of
+// rows [rows][K/2] with bf16 scales [rows][K/32] is a run of 32-bit words of
+// 8 elements each, 4 words per scale group, and its fp16 copy the matching
+// run of 16-byte words: a warp takes 32 consecutive words, so both its loads
+// and its stores are contiguous.
+struct DqSeg {
+  const uint32_t* q;
+  const uint16_t* s;
+  uint4* out;
+  size_t n;  // 32-bit words
+};
+struct DqJob {
+  DqSeg seg[5];
+  int nseg;
+  const uint4* x;  // bf16, 8 per 16-byte word
+  uint4* x16;
+  size_t nx;
+};
 
-// bf16 -> fp16, 8 elements per thread and step
-__global__ void bf16_to_f16_kernel(const uint16_t* __restrict__ x, size_t n8, __half* __restrict__ out) {
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(x) + i);
+__global__ void __launch_bounds__(256) dequant_all_kernel(const __grid_constant__ DqJob J) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x, base = 0;
+#pragma unroll 1
+  for (int g = 0; g < J.nseg; ++g) {
+    const DqSeg S = J.seg[g];
+#pragma unroll 4
+    for (; i < base + S.n; i += stride) {
+      const size_t w = i - base;
+      uint32_t o[4];
+      tc::dequant_word_natural(__ldcs(S.q + w), scale_h2(__ldg(S.s + (w >> 2))), o);
+      __stcs(S.out + w, make_uint4(o[0], o[1], o[2], o[3]));
+    }
+    base += S.n;
+  }
+#pragma unroll 4
+  for (; i < base + J.nx; i += stride) {
+    const uint4 v = __ldcs(J.x + (i - base));
     const uint32_t u[4] = {v.x, v.y, v.z, v.w};
     uint32_t h[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) h[j] = pack_half2(__uint_as_float(u[j] << 16), __uint_as_float(u[j] & 0xffff0000u));
-    reinterpret_cast<uint4*>(out)[i] = make_uint4(h[0], h[1], h[2], h[3]);
+    J.x16[i - base] = make_uint4(h[0], h[1], h[2], h[3]);
   }
 }
 
@@ -561,7 +553,7 @@ constexpr size_t kAl = 256;
 size_t al(size_t v) { return (v + kAl - 1) & ~(kAl - 1); }
 
 struct PWs {
-  size_t idx, w, eo, sa, inv, go, gto, gt, ar, perm_scratch, H, V, U, Z, tokrow, x16, win16, wout16, gate16, up16,
+  size_t logits, idx, w, eo, sa, inv, go, gto, gt, ar, perm_scratch, H, V, U, Z, tokrow, x16, win16, wout16, gate16, up16,
       down16, ztok, end;
 };
 
@@ -574,6 +566,7 @@ PWs pws(const PrefillArgs& P, int T) {
     return at;
   };
   const size_t n = (size_t)T * P.k, gk = (size_t)T * (P.G < P.k ? P.G : P.k);
+  m.logits = take((size_t)T * P.E * 4);
   m.idx = take(n * 4);
   m.w = take(n * 4);
   m.eo = take((size_t)(P.E + 1) * 4);
@@ -586,7 +579,7 @@ PWs pws(const PrefillArgs& P, int T) {
   m.perm_scratch = take(permute_scratch_bytes(T, P.E, P.G));
   m.H = take((size_t)T * P.G * P.L * 2);
   m.V = take(n * P.f * 2);
-  m.U = take(n * P.L * 4);
+  m.U = take(n * P.L * 2);
   m.Z = take(gk * P.L * 2);
   m.tokrow = take((size_t)T * P.G * 4);
   m.x16 = take((size_t)T * P.d * 2);
@@ -658,7 +651,7 @@ cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_
   const int grid = P.num_sms;
   __half* H = reinterpret_cast<__half*>(b + m.H);
   __half* V = reinterpret_cast<__half*>(b + m.V);
-  float* U = reinterpret_cast<float*>(b + m.U);
+  __half* U = reinterpret_cast<__half*>(b + m.U);
   __half* Z = reinterpret_cast<__half*>(b + m.Z);
   int32_t* tokrow = reinterpret_cast<int32_t*>(b + m.tokrow);
   __half* x16 = reinterpret_cast<__half*>(b + m.x16);
@@ -671,15 +664,22 @@ cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_
   cudaError_t e;
   {  // the shared matrices and x in fp16, once per call
     if (hook) hook->before(st);
-    // a row of K elements is K/32 consecutive scale groups in both arrays
-    const size_t wgroups = (size_t)P.G * P.L * P.d / 32;
-    dequant_f16_kernel<<<8 * grid, 256, 0, st>>>(P.W_in_q, P.W_in_s, wgroups, win16);
-    dequant_f16_kernel<<<8 * grid, 256, 0, st>>>(P.W_out_q, P.W_out_s, wgroups, wout16);
-    bf16_to_f16_kernel<<<8 * grid, 256, 0, st>>>(x, (size_t)T * P.d / 8, x16);
-    const size_t egroups = (size_t)P.E * P.f * P.L / 32;
-    dequant_f16_kernel<<<8 * grid, 256, 0, st>>>(P.gate_q, P.gate_s, egroups, gate16);
-    dequant_f16_kernel<<<8 * grid, 256, 0, st>>>(P.up_q, P.up_s, egroups, up16);
-    dequant_f16_kernel<<<8 * grid, 256, 0, st>>>(P.down_q, P.down_s, egroups, down16);
+    DqJob J;
+    const size_t wwords = (size_t)P.G * P.L * P.d / 8, ewords = (size_t)P.E * P.f * P.L / 8;
+    const void* q[5] = {P.W_in_q, P.W_out_q, P.gate_q, P.up_q, P.down_q};
+    const uint16_t* sc[5] = {P.W_in_s, P.W_out_s, P.gate_s, P.up_s, P.down_s};
+    __half* out[5] = {win16, wout16, gate16, up16, down16};
+    for (int i = 0; i < 5; ++i) {
+      J.seg[i].q = static_cast<const uint32_t*>(q[i]);
+      J.seg[i].s = sc[i];
+      J.seg[i].out = reinterpret_cast<uint4*>(out[i]);
+      J.seg[i].n = i < 2 ? wwords : ewords;
+    }
+    J.nseg = 5;
+    J.x = reinterpret_cast<const uint4*>(x);
+    J.x16 = reinterpret_cast<uint4*>(x16);
+    J.nx = (size_t)T * P.d / 8;
+    dequant_all_kernel<<<8 * grid, 256, 0, st>>>(J);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (hook) hook->after(st);
   }
@@ -793,9 +793,12 @@ cudaError_t route(const PrefillArgs& P, const uint16_t* x, int T, int32_t* idx, 
         !tmap_encode(&p.bm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, P.W_r_split, bd, bs, bb, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
-  p.bias = P.b_r; p.T = T; p.d = P.d; p.E = P.E; p.k = P.k;
-  p.idx = idx; p.w = w; p.logits = logits;
-  return run_gemm(p, P.num_sms, st);
+  p.bias = P.b_r; p.T = T; p.d = P.d; p.E = P.E;
+  p.logits = logits;
+  cudaError_t e = run_gemm(p, P.num_sms, st);
+  if (e != cudaSuccess) return e;
+  route_topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits, T, P.E, P.k, idx, w);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -812,7 +815,7 @@ cudaError_t prefill_set_attributes() {
 bool prefill_supported(const PrefillArgs& P) {
   if (P.r != 0) return false;  // the LoRA branch runs on the decode path
   if (P.d % 256 != 0 || P.L % 256 != 0 || P.f % 128 != 0) return false;
-  if (P.E > 512 || P.k > 16 || P.G > 64) return false;  // router tile: all experts in one accumulator
+  if (P.E > 512 || P.k > 16 || P.G > 64) return false;  // top-k: E <= 512 logits per warp
   return P.num_sms > 0;
 }
 
@@ -822,7 +825,8 @@ size_t prefill_workspace_bytes(const PrefillArgs& P, int T) {
 }
 
 cudaError_t launch_prefill_route(const PrefillArgs& P, const uint16_t* x, int T, int32_t* idx, float* w,
-                                 float* logits, void*, cudaStream_t st) {
+                                 float* logits, void* ws, cudaStream_t st) {
+  if (!logits) logits = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + pws(P, T).logits);
   return route(P, x, T, idx, w, logits, st);
 }
 
@@ -846,12 +850,18 @@ cudaError_t launch_prefill_layer(const PrefillArgs& P, const uint16_t* x, int T,
   EvHook* hk = events ? &hook : nullptr;
   cudaError_t e;
   if (hk) hk->before(st);
-  if ((e = route(P, x, T, idx, w, nullptr, st)) != cudaSuccess) return e;
+  if ((e = route(P, x, T, idx, w, reinterpret_cast<float*>(b + m.logits), st)) != cudaSuccess) return e;
   if (hk) hk->after(st);
   if (hk) hk->before(st);
   if ((e = launch_permute(idx, T, P.E, P.G, P.k, pm, b + m.perm_scratch, P.err, st)) != cudaSuccess) return e;
   if (hk) hk->after(st);
   return experts(P, x, T, idx, w, pm, b, m, 0, nullptr, residual, y, st, hk);
+}
+
+int prefill_launch_count(const PrefillArgs&, int T) {
+  // route: GEMM + top-k; permute: count, scan, scatter; dequant; win; gateup;
+  // down; zreduce; wout
+  return T > 0 ? 11 : 0;
 }
 
 const char* prefill_stage_name(const PrefillArgs&, int, int i, int* count) {

@@ -47,5 +47,7 @@ cudaError_t launch_prefill_experts(const PrefillArgs& P, const uint16_t* x, int 
 cudaError_t launch_prefill_layer(const PrefillArgs& P, const uint16_t* x, int T, const uint16_t* residual,
                                  uint16_t* y, void* ws, cudaStream_t st, const std::vector<cudaEvent_t>* events);
 const char* prefill_stage_name(const PrefillArgs& P, int T, int i, int* count);
+// kernels launched by launch_prefill_layer
+int prefill_launch_count(const PrefillArgs& P, int T);
 
 }  // namespace lmoe

@@ -1,0 +1,80 @@
+// Top-k with softmax renormalisation of one token's router logits by one warp
+// (E <= 512, k <= 16): the k largest logits in descending order, ties going to
+// the lower expert index, and w_j = exp(l_j - l_max) / sum of those over the
+// selected j.
+//
+// Each lane holds experts lane, lane + 32, ... as order-preserving integer
+// keys and its best remaining one (a depth-4 tournament); every round the
+// warp takes the largest head key (a warp max reduction), then the lowest
+// expert index holding it (a warp min reduction), and only the winning lane
+// rescans.
+#pragma once
+#include "common.cuh"
+
+namespace lmoe {
+
+// order-preserving key of a float (larger float <-> larger unsigned key)
+static LMOE_DEV unsigned float_key(float x) {
+  const unsigned b = __float_as_uint(x);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+static LMOE_DEV float key_float(unsigned k) { return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k); }
+
+// Lane j < k returns (expert of the j-th pick as int bits, its weight); other
+// lanes return (0, 0). `row` holds the token's E logits (read through L2).
+static __device__ __noinline__ float2 topk_warp(const float* row, int E, int k) {
+  const int lane = threadIdx.x & 31;
+  unsigned key[16];  // element i is expert lane + 32 i; 0 = none (below every finite key)
+#pragma unroll
+  for (int i = 0; i < 16; ++i) key[i] = lane + 32 * i < E ? float_key(__ldcg(row + lane + 32 * i)) : 0u;
+  // this lane's best remaining element, ties to the lower i: a depth-4 tournament
+  auto best = [&](unsigned& bk, int& bi) {
+    unsigned tk[8];
+    int ti[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const bool hi = key[2 * i + 1] > key[2 * i];
+      tk[i] = hi ? key[2 * i + 1] : key[2 * i];
+      ti[i] = hi ? 2 * i + 1 : 2 * i;
+    }
+#pragma unroll
+    for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+      for (int i = 0; i < w; ++i) {
+        const bool hi = tk[2 * i + 1] > tk[2 * i];
+        tk[i] = hi ? tk[2 * i + 1] : tk[2 * i];
+        ti[i] = hi ? ti[2 * i + 1] : ti[2 * i];
+      }
+    bk = tk[0];
+    bi = ti[0];
+  };
+  unsigned bk;
+  int bi;
+  best(bk, bi);
+  unsigned sel = 0, k0 = 0;
+  int sel_e = 0;
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) {
+    const unsigned m = __reduce_max_sync(0xffffffffu, bk);
+    const int mine = lane + 32 * bi;
+    const unsigned wi = __reduce_min_sync(0xffffffffu, bk == m ? (unsigned)mine : 0xffffffffu);
+    if ((unsigned)mine == wi) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (i == bi) key[i] = 0u;
+      best(bk, bi);
+    }
+    if (j == 0) k0 = m;
+    if (lane == j) {
+      sel = m;
+      sel_e = wi < (unsigned)E ? (int)wi : 0;
+    }
+  }
+  const float ex = (lane < k) ? __expf(key_float(sel) - key_float(k0)) : 0.f;
+  float z = ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  return make_float2(__int_as_float(sel_e), lane < k ? ex / z : 0.f);
+}
+
+}  // namespace lmoe

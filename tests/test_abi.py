@@ -50,6 +50,7 @@ def test_host_side_validation_without_gpu():
         assert capi.lmoe_status_string(s)
     name, count = capi.lmoe_stage_name(None, 8, 0)
     assert name == "" and count == 0
+    assert capi.lmoe_launch_count(None, 8) == 0
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
