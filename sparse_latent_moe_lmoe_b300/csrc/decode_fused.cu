@@ -69,12 +69,13 @@ __host__ __device__ constexpr int dyn_smem() {
 struct Tables {
   int32_t idx[16 * 16];
   float w[16 * 16];
-  uint16_t emask[512];       // routed tokens per expert
+  unsigned emask[16];        // bit e: expert e is routed by some token (E <= 512)
   int16_t elist[MAX_ACT];    // routed experts, ascending
   int16_t glist[64];         // routed groups, ascending
   int16_t gslot0[65];        // first expert slot of each routed group
   int n_act, n_actg, par;
   volatile int tables_ready;
+  volatile int x_issued;     // the consumers' loads of x are in flight: weight copies may start
   int key[KEYS];
   uint64_t full[16], empty[16];
   volatile int seq[16];
@@ -86,20 +87,30 @@ LMOE_DEV unsigned ld_acquire(const unsigned* p) {
   return v;
 }
 
-LMOE_COLD void wait_count(const unsigned* p, unsigned target, long long budget, unsigned* err) {
+// Whole warp, no divergence: lane i waits until *p_i >= target (p_i null:
+// nothing to wait for), polling with acquire loads.
+LMOE_COLD void wait_counts(const unsigned* p, unsigned target, long long budget, unsigned* err) {
   const long long t0 = clock64();
   #pragma unroll 1
-  while (ld_acquire(p) < target) {
-    if (clock64() - t0 > budget) {
-      set_error(err, ERRBIT_TIMEOUT);
+  while (!__all_sync(0xffffffffu, p == nullptr || ld_acquire(p) >= target)) {
+    if (__any_sync(0xffffffffu, clock64() - t0 > budget)) {
+      if ((threadIdx.x & 31) == 0) set_error(err, ERRBIT_TIMEOUT);
       return;
     }
     __nanosleep(32);
   }
 }
 
-// consumer warps only (the producer never joins)
-LMOE_DEV void cons_sync() { asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory"); }
+// Every warp, once, at the end of the kernel.
+LMOE_DEV void end_sync() { asm volatile("barrier.sync 2, %0;" ::"n"(NTHR) : "memory"); }
+
+// Consumer warps only (the producer never joins). Callers often reach it from
+// divergent code (a few lanes waiting on a counter), so the warp reconverges
+// first and the barrier is the non-aligned form, which counts every thread.
+LMOE_DEV void cons_sync() {
+  __syncwarp();
+  asm volatile("barrier.sync 1, %0;" ::"n"(NCT) : "memory");
+}
 
 // The last of n arrivals on a ticket returns true; called by one lane after a
 // __threadfence that publishes the caller's partial results.
@@ -112,7 +123,10 @@ LMOE_DEV float route_weight(const Tables& tb, int t, int e, int k) {
   return 0.f;
 }
 
-// Counter layout (one copy; two copies alternate between launches).
+// Counter layout (one copy; two copies alternate between launches). The
+// completion counters that whole CTAs poll sit one per 128-byte line (CSTR
+// words apart); the tickets, which only see atomics, are packed.
+constexpr int CSTR = 32;
 struct CtrMap {
   int tk_router, done_router, tk_win, done_in, done_gu, tk_down, done_down, tk_wout, n;
 };
@@ -120,12 +134,12 @@ __host__ __device__ inline CtrMap ctr_map(int d, int E, int G, int L) {
   CtrMap m;
   int o = 0;
   m.tk_router = o; o += E / 2;
-  m.done_router = o; o += 1;
+  m.done_router = o; o += CSTR;
   m.tk_win = o; o += G * (L / 16);
-  m.done_in = o; o += G;
-  m.done_gu = o; o += MAX_ACT;
+  m.done_in = o; o += G * CSTR;
+  m.done_gu = o; o += MAX_ACT * CSTR;
   m.tk_down = o; o += G * (L / DR);
-  m.done_down = o; o += G;
+  m.done_down = o; o += G * CSTR;
   m.tk_wout = o; o += d / 16;
   m.n = (o + 31) & ~31;
   return m;
@@ -143,28 +157,43 @@ LMOE_DEV void split(int n, int c, int nC, int& lo, int& hi) {
 // 8*nt + lane/4 starting at 128 c + 32 (lane % 4) + 8 mp, as fp16 pairs
 // (e0,e4) (e1,e5) (e2,e6) (e3,e7).
 template <int NT>
-LMOE_COLD void stage_x(uint4* fr, const uint16_t* x, int T, int d, int ks, int ctid) {
-  const int n = (KSEG / 128) * NT * 128;
-  #pragma unroll 1
-  for (int si = ctid; si < n; si += NCT) {
-    const int ln = si & 31, mp = (si >> 5) & 3, rest = si >> 7;
-    const int nt = rest % NT, cc = rest / NT;
-    const int tok = nt * 8 + (ln >> 2), tg = ln & 3;
-    const int k0 = ks * KSEG + cc * 128 + tg * 32 + mp * 8;
-    float e[8];
-    if (tok < T) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * d + k0));
-      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+LMOE_COLD void stage_x(Tables& tb, uint4* keyset, const uint16_t* x, int T, int d, int ctid) {
+  constexpr int N = (KSEG / 128) * NT * 128, PER = (N + NCT - 1) / NCT;
+  // every load first, then let the producer start the weight copies: x's
+  // loads must not queue behind them
+  uint4 v[KEYS][PER];
+#pragma unroll
+  for (int s = 0; s < KEYS; ++s) {
+    const int ks = tb.key[s];
+#pragma unroll
+    for (int r = 0; r < PER; ++r) {
+      const int si = ctid + r * NCT;
+      const int ln = si & 31, mp = (si >> 5) & 3, rest = si >> 7;
+      const int nt = rest % NT, cc = rest / NT;
+      const int tok = nt * 8 + (ln >> 2), tg = ln & 3;
+      const int k0 = ks * KSEG + cc * 128 + tg * 32 + mp * 8;
+      v[s][r] = (ks >= 0 && si < N && tok < T) ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * d + k0))
+                                               : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  cons_sync();
+  if (ctid == 0) tb.x_issued = 1;
+#pragma unroll
+  for (int s = 0; s < KEYS; ++s) {
+    uint4* fr = keyset + s * (key_bytes<NT>() / 16);
+#pragma unroll
+    for (int r = 0; r < PER; ++r) {
+      const int si = ctid + r * NCT;
+      if (tb.key[s] < 0 || si >= N) continue;
+      const uint32_t u[4] = {v[s][r].x, v[s][r].y, v[s][r].z, v[s][r].w};
+      float e[8];
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         e[2 * h] = __uint_as_float(u[h] << 16);
         e[2 * h + 1] = __uint_as_float(u[h] & 0xffff0000u);
       }
-    } else {
-#pragma unroll
-      for (int h = 0; h < 8; ++h) e[h] = 0.f;
+      fr[si] = pack_frag8(e);
     }
-    fr[si] = pack_frag8(e);
   }
 }
 
@@ -243,22 +272,28 @@ LMOE_DEV void cons_release(Tables& tb, int j) {
 }  // namespace
 
 // ==================================================================== kernel
-// Routed-expert and routed-group tables from the token masks (one warp):
-// elist = routed experts ascending, glist = their groups, gslot0[gi] = first
-// slot of group gi in elist (gslot0[n_actg] = n_act).
-LMOE_COLD void build_tables(Tables& tb, int E, int epg) {
+// Routed-expert and routed-group tables from the routed-expert bit mask (one
+// warp): elist = routed experts ascending, glist = their groups, gslot0[gi] =
+// first slot of group gi in elist (gslot0[n_actg] = n_act).
+LMOE_COLD void build_tables(Tables& tb, int epg) {
   const int lane = threadIdx.x & 31;
-  int base = 0;
+  const unsigned m = lane < 16 ? tb.emask[lane] : 0u;  // experts 32 lane .. 32 lane + 31
+  const int cnt = __popc(m);
+  int pre = cnt;  // inclusive prefix over lanes
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, pre, o);
+    if (lane >= o) pre += y;
+  }
+  const int n_act = __shfl_sync(0xffffffffu, pre, 31);
+  int pos = pre - cnt;
+  unsigned mm = m;
 #pragma unroll 1
-  for (int e0 = 0; e0 < E; e0 += 32) {
-    const int e = e0 + lane;
-    const bool on = e < E && tb.emask[e] != 0;
-    const unsigned bal = __ballot_sync(0xffffffffu, on);
-    if (on) tb.elist[base + __popc(bal & ((1u << lane) - 1u))] = (int16_t)e;
-    base += __popc(bal);
+  while (mm) {
+    tb.elist[pos++] = (int16_t)(32 * lane + __ffs(mm) - 1);
+    mm &= mm - 1u;
   }
   __syncwarp();
-  const int n_act = base;
   int ng = 0;
 #pragma unroll 1
   for (int i0 = 0; i0 < n_act; i0 += 32) {
@@ -307,6 +342,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
     const unsigned long long old = atomicAdd(F.launches, 1ull);
     tb.par = (int)((old / (unsigned long long)nC) & 1ull);
     tb.tables_ready = 0;
+    tb.x_issued = 0;
     #pragma unroll 1
     for (int s = 0; s < NS; ++s) {
       mbar_init(&tb.full[s], 1);
@@ -357,13 +393,26 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
       }
     };
     if (lane == 0) {
+      const uint64_t pol = l2_evict_first();  // weights are read once per pass
+      {  // x first: its loads are small and every CTA waits on them
+        const long long t0 = clock64();
+#pragma unroll 1
+        while (tb.x_issued == 0) {
+          if (clock64() - t0 > budget) {
+            set_error(err, ERRBIT_TIMEOUT);
+            ok = false;
+            break;
+          }
+          __nanosleep(32);
+        }
+      }
       {  // router: (segment, expert pair)
         int ks = a1lo / NPAIR, pr = a1lo % NPAIR;
 #pragma unroll 1
         for (int i = a1lo; ok && i < a1hi; ++i) {
           unsigned char* dst = claim(2 * KSEG * 4);
           if (!dst) break;
-          tma_load_3d(dst, &F.maps.wr, 0, ks * (KSEG / 256), 2 * pr, &tb.full[slot]);
+          tma_load_3d_hint(dst, &F.maps.wr, 0, ks * (KSEG / 256), 2 * pr, &tb.full[slot], pol);
           advance();
           if (++pr == NPAIR) { pr = 0; ++ks; }
         }
@@ -375,8 +424,8 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
         for (int i = a2lo; ok && i < a2hi; ++i) {
           unsigned char* dst = claim(16 * KSEG / 2 + 16 * KSEG / 16);
           if (!dst) break;
-          tma_load_3d(dst, &F.maps.win_q, 0, ks * (KSEG / 256), row * 16, &tb.full[slot]);
-          tma_load_2d(dst + 16 * KSEG / 2, &F.maps.win_s, ks * (KSEG / 32), row * 16, &tb.full[slot]);
+          tma_load_3d_hint(dst, &F.maps.win_q, 0, ks * (KSEG / 256), row * 16, &tb.full[slot], pol);
+          tma_load_2d_hint(dst + 16 * KSEG / 2, &F.maps.win_s, ks * (KSEG / 32), row * 16, &tb.full[slot], pol);
           advance();
           if (++row == per_ks) { row = 0; ++ks; }
         }
@@ -405,13 +454,13 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
           const int row = e * f + rt * 16;
           unsigned char* dst = claim(16 * L / 2 + 16 * L / 16);
           if (!dst) break;
-          tma_load_3d(dst, &F.maps.gate_q, 0, 0, row, &tb.full[slot]);
-          tma_load_2d(dst + 16 * L / 2, &F.maps.gate_s, 0, row, &tb.full[slot]);
+          tma_load_3d_hint(dst, &F.maps.gate_q, 0, 0, row, &tb.full[slot], pol);
+          tma_load_2d_hint(dst + 16 * L / 2, &F.maps.gate_s, 0, row, &tb.full[slot], pol);
           advance();
           dst = claim(16 * L / 2 + 16 * L / 16);
           if (!dst) break;
-          tma_load_3d(dst, &F.maps.up_q, 0, 0, row, &tb.full[slot]);
-          tma_load_2d(dst + 16 * L / 2, &F.maps.up_s, 0, row, &tb.full[slot]);
+          tma_load_3d_hint(dst, &F.maps.up_q, 0, 0, row, &tb.full[slot], pol);
+          tma_load_2d_hint(dst + 16 * L / 2, &F.maps.up_s, 0, row, &tb.full[slot], pol);
           advance();
           if (++rt == FT) {
             rt = 0;
@@ -428,8 +477,8 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
           const int row = e * L + rb * DR;
           unsigned char* dst = claim(DR * f / 2 + DR * f / 16);
           if (!dst) break;
-          tma_load_3d(dst, &F.maps.down_q, 0, 0, row, &tb.full[slot]);
-          tma_load_2d(dst + DR * f / 2, &F.maps.down_s, 0, row, &tb.full[slot]);
+          tma_load_3d_hint(dst, &F.maps.down_q, 0, 0, row, &tb.full[slot], pol);
+          tma_load_2d_hint(dst + DR * f / 2, &F.maps.down_s, 0, row, &tb.full[slot], pol);
           advance();
           if (++rb == NRB) {
             rb = 0;
@@ -446,8 +495,8 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
           const int row = g * d + rt * 16;
           unsigned char* dst = claim(16 * L / 2 + 16 * L / 16);
           if (!dst) break;
-          tma_load_3d(dst, &F.maps.wout_q, 0, 0, row, &tb.full[slot]);
-          tma_load_2d(dst + 16 * L / 2, &F.maps.wout_s, 0, row, &tb.full[slot]);
+          tma_load_3d_hint(dst, &F.maps.wout_q, 0, 0, row, &tb.full[slot], pol);
+          tma_load_2d_hint(dst + 16 * L / 2, &F.maps.wout_s, 0, row, &tb.full[slot], pol);
           advance();
           if (++rt == NRT_OUT) {
             rt = 0;
@@ -461,6 +510,10 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
 #pragma unroll 1
       for (int jj = (j > NS ? j - NS : 0); jj < j; ++jj) mbar_wait(&tb.full[jj % NS], (jj / NS) & 1, drain, err);
     }
+    // The whole producer warp stays resident until every consumer is done: a
+    // warp that exits changes what the consumers' named barrier counts.
+    __syncwarp();
+    end_sync();
     return;
   }
 
@@ -487,9 +540,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
     for (int s = n; s < KEYS; ++s) tb.key[s] = -1;
   }
   cons_sync();
-  #pragma unroll 1
-  for (int s = 0; s < KEYS; ++s)
-    if (tb.key[s] >= 0) stage_x<NT>(kfr(s), A.x, T, d, tb.key[s], ctid);
+  stage_x<NT>(tb, keyset, A.x, T, d, ctid);
   cons_sync();
 
   // ------------------------------------------------------------ A1 router
@@ -498,40 +549,63 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
     const int i = a1lo + li, ks = i / NPAIR, pr = i % NPAIR, e0 = 2 * pr;
     const float* wr = reinterpret_cast<const float*>(cons_wait<NS>(tb, ring, jbase + li, budget, err));
     const uint4* fr = kfr(key_slot(tb, ks));
-    // token by token (compact code): lane covers elements u*256 + 8*lane .. +7
-    float mine = 0.f;  // lane 2t + r ends with the partial logit of (token t, expert e0 + r)
+    // lane covers elements u*256 + 8*lane .. +7 (u < 4) of both experts; for
+    // each half of u the 32 weights stay in registers while the tokens stream
+    // past, 16 independent sums per lane
 #pragma unroll 1
-    for (int t = 0; t < T; ++t) {
-      float s0 = 0.f, s1 = 0.f;
-#pragma unroll 1
-      for (int u = 0; u < 4; ++u) {
-        const int kk = u * 256 + lane * 8;
-        const int cc = kk >> 7, tg = (kk & 127) >> 5, mp = (kk & 31) >> 3;
-        const float4 a0 = *reinterpret_cast<const float4*>(wr + kk);
-        const float4 a1 = *reinterpret_cast<const float4*>(wr + kk + 4);
-        const float4 b0 = *reinterpret_cast<const float4*>(wr + KSEG + kk);
-        const float4 b1 = *reinterpret_cast<const float4*>(wr + KSEG + kk + 4);
-        const uint4 xv = fr[((cc * NT + (t >> 3)) * 4 + mp) * 32 + (t & 7) * 4 + tg];
-        const float2 p0 = __half22float2(*reinterpret_cast<const __half2*>(&xv.x));  // e0, e4
-        const float2 p1 = __half22float2(*reinterpret_cast<const __half2*>(&xv.y));  // e1, e5
-        const float2 p2 = __half22float2(*reinterpret_cast<const __half2*>(&xv.z));  // e2, e6
-        const float2 p3 = __half22float2(*reinterpret_cast<const __half2*>(&xv.w));  // e3, e7
-        s0 = fmaf(a0.x, p0.x, s0); s0 = fmaf(a0.y, p1.x, s0); s0 = fmaf(a0.z, p2.x, s0); s0 = fmaf(a0.w, p3.x, s0);
-        s0 = fmaf(a1.x, p0.y, s0); s0 = fmaf(a1.y, p1.y, s0); s0 = fmaf(a1.z, p2.y, s0); s0 = fmaf(a1.w, p3.y, s0);
-        s1 = fmaf(b0.x, p0.x, s1); s1 = fmaf(b0.y, p1.x, s1); s1 = fmaf(b0.z, p2.x, s1); s1 = fmaf(b0.w, p3.x, s1);
-        s1 = fmaf(b1.x, p0.y, s1); s1 = fmaf(b1.y, p1.y, s1); s1 = fmaf(b1.z, p2.y, s1); s1 = fmaf(b1.w, p3.y, s1);
-      }
+    for (int nt = 0; nt < NT; ++nt) {
+      float v[16];  // v[2 t + r]: token 8 nt + t, expert e0 + r
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        s0 += __shfl_xor_sync(0xffffffffu, s0, o);
-        s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+      for (int q = 0; q < 16; ++q) v[q] = 0.f;
+#pragma unroll
+      for (int uh = 0; uh < 2; ++uh) {
+        float4 w0[2][2], w1[2][2];
+#pragma unroll
+        for (int u2 = 0; u2 < 2; ++u2) {
+          const int kk = (2 * uh + u2) * 256 + lane * 8;
+          w0[u2][0] = *reinterpret_cast<const float4*>(wr + kk);
+          w0[u2][1] = *reinterpret_cast<const float4*>(wr + kk + 4);
+          w1[u2][0] = *reinterpret_cast<const float4*>(wr + KSEG + kk);
+          w1[u2][1] = *reinterpret_cast<const float4*>(wr + KSEG + kk + 4);
+        }
+        if (uh == 1 && nt == NT - 1) cons_release<NS>(tb, jbase + li);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          float s0 = v[2 * t], s1 = v[2 * t + 1];
+#pragma unroll
+          for (int u2 = 0; u2 < 2; ++u2) {
+            const int kk = (2 * uh + u2) * 256 + lane * 8;
+            const int cc = kk >> 7, tg = (kk & 127) >> 5, mp = (kk & 31) >> 3;
+            const uint4 xv = fr[((cc * NT + nt) * 4 + mp) * 32 + t * 4 + tg];
+            const float2 p0 = __half22float2(*reinterpret_cast<const __half2*>(&xv.x));  // e0, e4
+            const float2 p1 = __half22float2(*reinterpret_cast<const __half2*>(&xv.y));  // e1, e5
+            const float2 p2 = __half22float2(*reinterpret_cast<const __half2*>(&xv.z));  // e2, e6
+            const float2 p3 = __half22float2(*reinterpret_cast<const __half2*>(&xv.w));  // e3, e7
+            const float4 a0 = w0[u2][0], a1 = w0[u2][1], b0 = w1[u2][0], b1 = w1[u2][1];
+            s0 = fmaf(a0.x, p0.x, s0); s0 = fmaf(a0.y, p1.x, s0); s0 = fmaf(a0.z, p2.x, s0); s0 = fmaf(a0.w, p3.x, s0);
+            s0 = fmaf(a1.x, p0.y, s0); s0 = fmaf(a1.y, p1.y, s0); s0 = fmaf(a1.z, p2.y, s0); s0 = fmaf(a1.w, p3.y, s0);
+            s1 = fmaf(b0.x, p0.x, s1); s1 = fmaf(b0.y, p1.x, s1); s1 = fmaf(b0.z, p2.x, s1); s1 = fmaf(b0.w, p3.x, s1);
+            s1 = fmaf(b1.x, p0.y, s1); s1 = fmaf(b1.y, p1.y, s1); s1 = fmaf(b1.z, p2.y, s1); s1 = fmaf(b1.w, p3.y, s1);
+          }
+          v[2 * t] = s0;
+          v[2 * t + 1] = s1;
+        }
       }
-      if (lane == 2 * t) mine = s0;
-      if (lane == 2 * t + 1) mine = s1;
+      // butterfly reduce-scatter over the warp: lanes 2q, 2q + 1 end with the
+      // sum of v[q] over all lanes
+#pragma unroll
+      for (int h = 8; h >= 1; h >>= 1) {
+        const bool hi = lane & (2 * h);
+#pragma unroll
+        for (int j = 0; j < h; ++j) {
+          const float keep = hi ? v[j + h] : v[j], send = hi ? v[j] : v[j + h];
+          v[j] = keep + __shfl_xor_sync(0xffffffffu, send, 2 * h);
+        }
+      }
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+      const int t = nt * 8 + (lane >> 2), r = (lane >> 1) & 1;
+      if ((lane & 1) == 0 && t < T) F.Lp[((size_t)ks * 16 + t) * E + e0 + r] = v[0];
     }
-    cons_release<NS>(tb, jbase + li);
-    const int t = lane >> 1, r = lane & 1;
-    if (t < T) F.Lp[((size_t)ks * 16 + t) * E + e0 + r] = mine;
     __threadfence();
     __syncwarp();
     bool last = false;
@@ -539,6 +613,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
     last = __shfl_sync(0xffffffffu, last, 0);
     if (last) {
       __threadfence();
+      const int t = lane >> 1, r = lane & 1;
       if (t < T) {
         float part[8];
 #pragma unroll
@@ -599,37 +674,33 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
       if (n < 8 * NT) F.Hf[(size_t)g * (L / 128) * FR + entry_index<NT>(k0, n)] = pack_frag8(e);
       __threadfence();
       __syncwarp();
-      if (lane == 0) atomicAdd(ctr + cm.done_in + g, 1u);
+      if (lane == 0) atomicAdd(ctr + cm.done_in + g * CSTR, 1u);
     }
   }
   jbase += nA2;
 
   // ------------------------------------------------------------ routing
   // every CTA: top-k of each token (one warp per token), then the tables
+  if (ctid < 16) tb.emask[ctid] = 0u;
   cons_sync();
-  if (ctid == 0) wait_count(ctr + cm.done_router, (unsigned)NPAIR, budget, err);
+  if (warp == 0) wait_counts(lane == 0 ? ctr + cm.done_router : nullptr, (unsigned)NPAIR, budget, err);
   cons_sync();
 #pragma unroll 1
   for (int tw = warp; tw < T; tw += NCW) {
     const float2 sw = topk_warp(F.logits + (size_t)tw * E, E, k);
     if (lane < k) {
-      tb.idx[tw * 16 + lane] = __float_as_int(sw.x);
+      const int e = __float_as_int(sw.x);
+      tb.idx[tw * 16 + lane] = e;
       tb.w[tw * 16 + lane] = sw.y;
+      atomicOr(&tb.emask[e >> 5], 1u << (e & 31));
       if (c == 0) {
-        A.idx[tw * k + lane] = __float_as_int(sw.x);
+        A.idx[tw * k + lane] = e;
         A.w[tw * k + lane] = sw.y;
       }
     }
   }
-#pragma unroll 1
-  for (int e = ctid; e < E; e += NCT) tb.emask[e] = 0;
   cons_sync();
-  if (ctid < T * k) {
-    const int t = ctid / k, e = tb.idx[t * 16 + ctid % k];
-    atomicOr(reinterpret_cast<unsigned*>(&tb.emask[0]) + (e >> 1), (1u << t) << ((e & 1) * 16));
-  }
-  cons_sync();
-  if (warp == 0) build_tables(tb, E, epg);
+  if (warp == 0) build_tables(tb, epg);
   cons_sync();
   if (ctid == 0) {
     __threadfence_block();
@@ -643,7 +714,8 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
     split(n_act * (f / 16), c, nC, lo, hi);
     if (ctid == 0) collect_keys(tb, lo, hi, [&](int i) { return tb.elist[i / (f / 16)] / epg; }, err);
     cons_sync();
-    if (ctid < KEYS && tb.key[ctid] >= 0) wait_count(ctr + cm.done_in + tb.key[ctid], (unsigned)NRT_IN, budget, err);
+    if (warp == 0)
+      wait_counts(lane < KEYS && tb.key[lane] >= 0 ? ctr + cm.done_in + tb.key[lane] * CSTR : nullptr, (unsigned)NRT_IN, budget, err);
     cons_sync();
     #pragma unroll 1
     for (int s = 0; s < KEYS; ++s)
@@ -679,7 +751,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
       if (n < 8 * NT) F.Vf[(size_t)es * (f / 128) * FR + entry_index<NT>(rt * 16 + run * 8, n)] = pack_frag8(ev);
       __threadfence();
       __syncwarp();
-      if (lane == 0) atomicAdd(ctr + cm.done_gu + es, 1u);
+      if (lane == 0) atomicAdd(ctr + cm.done_gu + es * CSTR, 1u);
     }
     jbase += 2 * (hi - lo);
   }
@@ -691,7 +763,9 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
     cons_sync();
     if (ctid == 0) collect_keys(tb, lo, hi, [&](int i) { return i / NRB; }, err);
     cons_sync();
-    if (ctid < KEYS && tb.key[ctid] >= 0) wait_count(ctr + cm.done_gu + tb.key[ctid], (unsigned)(f / 16), budget, err);
+    if (warp == 0)
+      wait_counts(lane < KEYS && tb.key[lane] >= 0 ? ctr + cm.done_gu + tb.key[lane] * CSTR : nullptr, (unsigned)(f / 16), budget,
+                  err);
     cons_sync();
     #pragma unroll 1
     for (int s = 0; s < KEYS; ++s)
@@ -763,7 +837,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
         }
         __threadfence();
         __syncwarp();
-        if (lane == 0) atomicAdd(ctr + cm.done_down + g, 1u);
+        if (lane == 0) atomicAdd(ctr + cm.done_down + g * CSTR, 1u);
       }
     }
     jbase += hi - lo;
@@ -776,8 +850,9 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
     cons_sync();
     if (ctid == 0) collect_keys(tb, lo, hi, [&](int i) { return i / NRT_OUT; }, err);
     cons_sync();
-    if (ctid < KEYS && tb.key[ctid] >= 0)
-      wait_count(ctr + cm.done_down + tb.glist[tb.key[ctid]], (unsigned)NRB, budget, err);
+    if (warp == 0)
+      wait_counts(lane < KEYS && tb.key[lane] >= 0 ? ctr + cm.done_down + tb.glist[tb.key[lane]] * CSTR : nullptr, (unsigned)NRB,
+                  budget, err);
     cons_sync();
     #pragma unroll 1
     for (int s = 0; s < KEYS; ++s)
@@ -838,6 +913,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
       }
     }
   }
+  end_sync();
 }
 
 // ===================================================================== host

@@ -46,6 +46,28 @@ LMOE_DEV void tma_load_3d(void* dst, const void* tmap, int c0, int c1, int c2, u
       : "memory");
 }
 
+// An L2 policy under which the lines a copy brings in are evicted first
+// (data read once per pass, such as weights streamed through a ring).
+LMOE_DEV uint64_t l2_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+LMOE_DEV void tma_load_2d_hint(void* dst, const void* tmap, int c0, int c1, uint64_t* m, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(smem_u32(m)), "l"(pol)
+      : "memory");
+}
+LMOE_DEV void tma_load_3d_hint(void* dst, const void* tmap, int c0, int c1, int c2, uint64_t* m, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(m)), "l"(pol)
+      : "memory");
+}
+
 // 16-byte global -> shared copy (cp.async, bypassing L1)
 LMOE_DEV void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
