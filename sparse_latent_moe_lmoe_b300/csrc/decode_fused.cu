@@ -732,13 +732,15 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
                              reinterpret_cast<const uint16_t*>(su + 16 * L / 2), L / 256, L / 32, L / 128, fr, ag, au);
       cons_release<NS>(tb, jbase + 2 * li);
       cons_release<NS>(tb, jbase + 2 * li + 1);
-      // v = w(t, e) * silu(gate) * up, as the down projection's fragments
+      // v = w(t, e) * silu(gate) * up, as the down projection's fragments;
+      // lane t < T looks up w(t, e), the other lanes take it by shuffle
+      const float wl = lane < T ? route_weight(tb, lane, e, k) : 0.f;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           const int t = nt * 8 + 2 * tig + h2;
-          const float wt = t < T ? route_weight(tb, t, e, k) : 0.f;
+          const float wt = __shfl_sync(0xffffffffu, wl, t);
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             const float a = ag[nt][hh * 2 + h2];
@@ -802,17 +804,19 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
       last = __shfl_sync(0xffffffffu, last, 0);
       if (last) {  // Z rows of this block: the group's experts in ascending order, into fragments
         __threadfence();
-        constexpr int PE = DR / 8 * 16 / 32;  // fragment entries per lane (DR/8 runs x 16 tokens)
+        // fragment entries per lane: DR/8 runs x 8 NT tokens over 32 lanes;
+        // the experts' partials are loaded QB at a time, all loads first
+        constexpr int PE = DR / 8 * 8 * NT / 32, QB = NT == 1 ? 12 : 4;
         float ev[PE][8];
 #pragma unroll
         for (int u = 0; u < PE; ++u)
 #pragma unroll
           for (int h = 0; h < 8; ++h) ev[u][h] = 0.f;
 #pragma unroll 1
-        for (int sl2 = s0; sl2 < s1; sl2 += 4) {
-          float4 p[4][PE][2];
+        for (int sl2 = s0; sl2 < s1; sl2 += QB) {
+          float4 p[QB][PE][2];
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
+          for (int q = 0; q < QB; ++q)
 #pragma unroll
             for (int u = 0; u < PE; ++u) {
               const int en = lane + 32 * u, run = en % (DR / 8), n = en / (DR / 8);
@@ -822,7 +826,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
               p[q][u][1] = v ? __ldcg(reinterpret_cast<const float4*>(src + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
+          for (int q = 0; q < QB; ++q)
 #pragma unroll
             for (int u = 0; u < PE; ++u) {
               ev[u][0] += p[q][u][0].x; ev[u][1] += p[q][u][0].y; ev[u][2] += p[q][u][0].z; ev[u][3] += p[q][u][0].w;

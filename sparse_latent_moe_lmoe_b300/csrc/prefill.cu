@@ -11,7 +11,8 @@
 //            renormalisation by one warp per token over its E logits
 //   permute  the deterministic multi-CTA permutation (permute.cu)
 //   win      H[g][t] = Win[g] x_t for every (g, t) (dense; rows of tokens
-//            with no expert in g are never read)
+//            with no expert in g are dropped), stored once per assignment
+//            in the expert-sorted order
 //   gateup   V[a] = silu(Gate_e h) * Up_e h   grouped by expert (128 gate
 //            rows + the matching 128 up rows per tile, SwiGLU in the epilogue)
 //   down     U[a] = w_a * Down_e V[a]     grouped by expert
@@ -183,13 +184,18 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
 // -------------------------------------------------------------------- W_in
 struct ProbWin : ProbBase {
   // H for every (group, token): one dense GEMM per group, A = x by TMA. The
-  // rows of tokens with no expert in a group are computed and never read --
-  // cheaper than gathering each group's tokens.
+  // rows of tokens with no expert in a group are computed and dropped --
+  // cheaper than gathering each group's tokens. The epilogue writes row
+  // (g, t) once for each of the token's assignments in group g, at that
+  // assignment's position in the expert-sorted order, so the expert GEMM
+  // reads its A operand by plain TMA boxes.
   static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 3, B_MODE = 2, STAGES = 4;
   CUtensorMap am;   // x in fp16 as [T][d], box {64, 128}
   CUtensorMap bm;   // Win in fp16 as [G][L][d], box {64, 256, 1}
-  int T, d, L, G;
-  __half* H;        // [G][T][L]
+  int T, d, L, G, k, epg;
+  const int32_t* idx;  // [T*k] routed experts
+  const int32_t* inv;  // [T*k] assignment -> position in the expert-sorted order
+  __half* H;           // [T*k][L] by sorted position
   LMOE_DEV int ntn() const { return L / 256; }
   LMOE_DEV int ntm() const { return (T + 127) / 128; }
   LMOE_DEV void init(int*) const {}
@@ -217,24 +223,27 @@ struct ProbWin : ProbBase {
     mma_k4(d_tmem, da, db, tc::idesc(128, 256, 0), kb);
   }
   LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase) const {
+    const int t = tl.m0 + row;
+    unsigned dest = 0;  // bit j: assignment j of token t is an expert of group tl.prob
+    if (row < tl.rows)
+      for (int j = 0; j < k; ++j)
+        if (idx[(size_t)t * k + j] / epg == tl.prob) dest |= 1u << j;
     for (int c0 = 0; c0 < 256; c0 += 16) {
       float v[16];
-      tc::tmem_ld16(tbase + (uint32_t)c0, v);
-      if (row < tl.rows) store_half16(H + ((size_t)tl.prob * T + tl.m0 + row) * L + tl.n0 + c0, v);
+      tc::tmem_ld16(tbase + (uint32_t)c0, v);  // warp-collective: every lane loads
+      for (unsigned m = dest; m; m &= m - 1u)
+        store_half16(H + (size_t)inv[(size_t)t * k + __ffs(m) - 1] * L + tl.n0 + c0, v);
     }
   }
 };
 
 // ---------------------------------------------------------------- gate/up
 struct ProbGateUp : ProbBase {
-  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 0, B_MODE = 2, STAGES = 4;
+  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 3, B_MODE = 2, STAGES = 4;
   CUtensorMap gm, um;  // gate / up in fp16 as [E*f][L], box {64, 128}
-  const __half* H;     // [G][T][L]
-  int T, k, epg;
+  CUtensorMap am;      // H by sorted position as [T*k][L] fp16, box {64, 128}
   int L, f, E;
   const int32_t* eo;
-  const int32_t* sa;
-  const int32_t* arow;
   __half* V;  // [T*k][f]
   LMOE_DEV int ntn() const { return f / 128; }
   LMOE_DEV void init(int* sc) const {
@@ -251,11 +260,12 @@ struct ProbGateUp : ProbBase {
     tl.nkb = L / 64;
     return tl;
   }
-  LMOE_DEV const void* a_row(const int*, const Tile& tl, int r, int kb) const {
-    const int p = eo[tl.prob] + tl.m0 + r;
-    const int t = sa[p] / k;  // assignment -> token
-    return H + ((size_t)(tl.prob / epg) * T + t) * L + kb * 64;
+  // A rows: the expert's assignments (rows past the expert's end belong to
+  // the next expert or lie beyond T*k and read as zero; the epilogue drops them)
+  LMOE_DEV void load_a(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
+    tma_load_2d(dst, &am, kb * 64, eo[tl.prob] + tl.m0, bar);
   }
+  LMOE_DEV const void* a_row(const int*, const Tile&, int, int) const { return nullptr; }
   // B rows 0..127: gate rows n0.. of expert e; 128..255: the matching up rows
   LMOE_DEV void load_b(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
     tma_load_2d(dst, &gm, kb * 64, tl.prob * f + tl.n0, bar);
@@ -287,7 +297,7 @@ struct ProbDown : ProbBase {
   const int32_t* eo;
   const int32_t* sa;
   const float* wts;  // [T*k]
-  __half* U;  // [T*k][L]
+  __half* U;  // [T*k][L] by sorted position
   LMOE_DEV int ntn() const { return L / 256; }
   LMOE_DEV void init(int* sc) const {
     tile_prefix(sc, E, [&](int e) { return ((eo[e + 1] - eo[e] + 127) / 128) * ntn(); });
@@ -420,62 +430,75 @@ struct ProbWout : ProbBase {
 // ----------------------------------------------------------------- zreduce
 // One warp per (group, token) row: Z[row] = sum over the token's experts in
 // that group, in ascending j, of U[inv[t*k + j]]; tokrow[t][g] = row.
+// One warp: out[0 .. L) = sum over the set bits j of `mask`, ascending, of
+// the fp16 rows U + row[j] * L, in fp32, rounded to fp16. Each pass over j
+// loads four 256-element runs of the row at once.
+LMOE_DEV void sum_rows_f16(const __half* __restrict__ U, const int32_t* __restrict__ row, unsigned mask, int L,
+                           __half* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  for (int c0 = 0; c0 < L; c0 += 1024) {
+    float acc[4][8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int h = 0; h < 8; ++h) acc[q][h] = 0.f;
+    unsigned m = mask;
+    while (m) {
+      const int rj = row[__ffs(m) - 1];
+      m &= m - 1u;
+      uint4 u[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int c = c0 + q * 256 + lane * 8;
+        u[q] = c < L ? __ldcs(reinterpret_cast<const uint4*>(U + (size_t)rj * L + c)) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t w[4] = {u[q].x, u[q].y, u[q].z, u[q].w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[h]));
+          acc[q][2 * h] += f.x;
+          acc[q][2 * h + 1] += f.y;
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int c = c0 + q * 256 + lane * 8;
+      if (c < L)
+        *reinterpret_cast<uint4*>(out + c) = make_uint4(pack_half2(acc[q][0], acc[q][1]), pack_half2(acc[q][2], acc[q][3]),
+                                                        pack_half2(acc[q][4], acc[q][5]), pack_half2(acc[q][6], acc[q][7]));
+    }
+  }
+}
+
+// Mode-1 Z rows: Z[row] for row = (g, t) of the group-token lists, one warp
+// per row (k <= 32).
 __global__ void zreduce_kernel(const __half* __restrict__ U, const int32_t* __restrict__ idx,
-                               const int32_t* __restrict__ inv, const int32_t* __restrict__ gto,
-                               const int32_t* __restrict__ gtok, int G, int k, int epg, int L, __half* __restrict__ Z,
-                               int32_t* __restrict__ tokrow) {
+                               const int32_t* __restrict__ inv, const int32_t* __restrict__ gto, const int32_t* __restrict__ gtok, int G, int k, int epg,
+                               int L, __half* __restrict__ Z, int32_t* __restrict__ tokrow) {
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (row >= gto[G]) return;
   int g = 0;
   while (g + 1 < G && gto[g + 1] <= row) ++g;
   const int t = gtok[row];
   if (lane == 0) tokrow[(size_t)t * G + g] = row;
-  for (int c = lane * 8; c < L; c += 256) {
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-      if (idx[(size_t)t * k + j] / epg != g) continue;
-      const uint4 u = __ldcs(reinterpret_cast<const uint4*>(U + (size_t)inv[(size_t)t * k + j] * L + c));
-      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x)), b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-      const float2 c2 = __half22float2(*reinterpret_cast<const __half2*>(&u.z)), d2 = __half22float2(*reinterpret_cast<const __half2*>(&u.w));
-      acc[0] += a.x; acc[1] += a.y; acc[2] += b.x; acc[3] += b.y;
-      acc[4] += c2.x; acc[5] += c2.y; acc[6] += d2.x; acc[7] += d2.y;
-    }
-    uint4 o;
-    o.x = pack_half2(acc[0], acc[1]);
-    o.y = pack_half2(acc[2], acc[3]);
-    o.z = pack_half2(acc[4], acc[5]);
-    o.w = pack_half2(acc[6], acc[7]);
-    *reinterpret_cast<uint4*>(Z + (size_t)row * L + c) = o;
-  }
+  const unsigned mask = __ballot_sync(0xffffffffu, lane < k && idx[(size_t)t * k + lane] / epg == g);
+  sum_rows_f16(U, inv + (size_t)t * k, mask, L, Z + (size_t)row * L);
 }
 
 // Mode-0 operand of W_out: Ztok[t][g][:] = sum over the token's experts in
 // group g, in ascending j, of U[inv[t*k + j]], or zero when the token has no
-// expert in g. One warp per (t, g).
+// expert in g. One warp per (t, g) (k <= 32).
 __global__ void zreduce_tok_kernel(const __half* __restrict__ U, const int32_t* __restrict__ idx,
                                    const int32_t* __restrict__ inv, int T, int G, int k, int epg, int L,
                                    __half* __restrict__ Ztok) {
   const int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (item >= T * G) return;
   const int t = item / G, g = item % G;
-  __half* dst = Ztok + ((size_t)t * G + g) * L;
-  for (int c = lane * 8; c < L; c += 256) {
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-      if (idx[(size_t)t * k + j] / epg != g) continue;
-      const uint4 u = __ldcs(reinterpret_cast<const uint4*>(U + (size_t)inv[(size_t)t * k + j] * L + c));
-      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x)), b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-      const float2 c2 = __half22float2(*reinterpret_cast<const __half2*>(&u.z)), d2 = __half22float2(*reinterpret_cast<const __half2*>(&u.w));
-      acc[0] += a.x; acc[1] += a.y; acc[2] += b.x; acc[3] += b.y;
-      acc[4] += c2.x; acc[5] += c2.y; acc[6] += d2.x; acc[7] += d2.y;
-    }
-    uint4 o;
-    o.x = pack_half2(acc[0], acc[1]);
-    o.y = pack_half2(acc[2], acc[3]);
-    o.z = pack_half2(acc[4], acc[5]);
-    o.w = pack_half2(acc[6], acc[7]);
-    *reinterpret_cast<uint4*>(dst + c) = o;
-  }
+  const unsigned mask = __ballot_sync(0xffffffffu, lane < k && idx[(size_t)t * k + lane] / epg == g);
+  sum_rows_f16(U, inv + (size_t)t * k, mask, L, Ztok + ((size_t)t * G + g) * L);
 }
 
 // W = hi + mid + lo with each term the bf16 rounding of what remains; the
@@ -577,7 +600,7 @@ PWs pws(const PrefillArgs& P, int T) {
   m.gt = take(gk * 4);
   m.ar = take(n * 4);
   m.perm_scratch = take(permute_scratch_bytes(T, P.E, P.G));
-  m.H = take((size_t)T * P.G * P.L * 2);
+  m.H = take(n * P.L * 2);
   m.V = take(n * P.f * 2);
   m.U = take(n * P.L * 2);
   m.Z = take(gk * P.L * 2);
@@ -696,7 +719,7 @@ cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_
           !tmap_encode(&p.bm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, win16, bd, bs, bb, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     }
-    p.T = T; p.d = P.d; p.L = P.L; p.G = P.G; p.H = H;
+    p.T = T; p.d = P.d; p.L = P.L; p.G = P.G; p.k = P.k; p.epg = P.epg; p.idx = idx; p.inv = pm.inv; p.H = H;
     if (hook) hook->before(st);
     if ((e = run_gemm(p, grid, st)) != cudaSuccess) return e;
     if (hook) hook->after(st);
@@ -704,14 +727,15 @@ cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_
   {
     ProbGateUp p;
     static_cast<ProbBase&>(p) = base(P);
-    p.H = H; p.T = T; p.k = P.k; p.epg = P.epg;
-    p.L = P.L; p.f = P.f; p.E = P.E; p.eo = pm.expert_offsets; p.sa = pm.sorted_assign; p.arow = pm.assign_row;
+    p.L = P.L; p.f = P.f; p.E = P.E; p.eo = pm.expert_offsets;
     {
       const cuuint64_t dims[2] = {(cuuint64_t)P.L, (cuuint64_t)P.E * P.f}, strides[1] = {(cuuint64_t)P.L * 2};
       const cuuint32_t box[2] = {64, 128};
+      const cuuint64_t ad[2] = {(cuuint64_t)P.L, (cuuint64_t)T * P.k}, as[1] = {(cuuint64_t)P.L * 2};
       if (!tmap_encode(&p.gm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, gate16, dims, strides, box,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-          !tmap_encode(&p.um, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, up16, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+          !tmap_encode(&p.um, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, up16, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !tmap_encode(&p.am, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, H, ad, as, box, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     }
     p.V = V;
