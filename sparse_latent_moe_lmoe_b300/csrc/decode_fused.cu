@@ -101,6 +101,12 @@ LMOE_COLD void wait_counts(const unsigned* p, unsigned target, long long budget,
   }
 }
 
+// The routing warps (the last n consumer warps).
+LMOE_DEV void route_sync(int n) {
+  __syncwarp();
+  asm volatile("barrier.sync 3, %0;" ::"r"(n * 32) : "memory");
+}
+
 // Every warp, once, at the end of the kernel.
 LMOE_DEV void end_sync() { asm volatile("barrier.sync 2, %0;" ::"n"(NTHR) : "memory"); }
 
@@ -680,32 +686,39 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
   jbase += nA2;
 
   // ------------------------------------------------------------ routing
-  // every CTA: top-k of each token (one warp per token), then the tables
-  if (ctid < 16) tb.emask[ctid] = 0u;
-  cons_sync();
-  if (warp == 0) wait_counts(lane == 0 ? ctr + cm.done_router : nullptr, (unsigned)NPAIR, budget, err);
-  cons_sync();
+  // Every CTA routes all tokens itself: top-k of each token (a warp per
+  // token), then the tables. The warps without a router item finish the A
+  // phase first; they route while the others finish their W_in items.
+  const int rw0 = nA1 < NCW - 1 ? nA1 : NCW - 1, nrw = NCW - rw0;
+  if (warp >= rw0) {
+    const int rt = (warp - rw0) * 32 + lane;
+    if (rt < 16) tb.emask[rt] = 0u;
+    if (warp == rw0) wait_counts(lane == 0 ? ctr + cm.done_router : nullptr, (unsigned)NPAIR, budget, err);
+    route_sync(nrw);
 #pragma unroll 1
-  for (int tw = warp; tw < T; tw += NCW) {
-    const float2 sw = topk_warp(F.logits + (size_t)tw * E, E, k);
-    if (lane < k) {
-      const int e = __float_as_int(sw.x);
-      tb.idx[tw * 16 + lane] = e;
-      tb.w[tw * 16 + lane] = sw.y;
-      atomicOr(&tb.emask[e >> 5], 1u << (e & 31));
-      if (c == 0) {
-        A.idx[tw * k + lane] = e;
-        A.w[tw * k + lane] = sw.y;
+    for (int tw = warp - rw0; tw < T; tw += nrw) {
+      const float2 sw = topk_warp(F.logits + (size_t)tw * E, E, k);
+      if (lane < k) {
+        const int e = __float_as_int(sw.x);
+        tb.idx[tw * 16 + lane] = e;
+        tb.w[tw * 16 + lane] = sw.y;
+        atomicOr(&tb.emask[e >> 5], 1u << (e & 31));
+        if (c == 0) {
+          A.idx[tw * k + lane] = e;
+          A.w[tw * k + lane] = sw.y;
+        }
+      }
+    }
+    route_sync(nrw);
+    if (warp == rw0) {
+      build_tables(tb, epg);
+      if (lane == 0) {
+        __threadfence_block();
+        tb.tables_ready = 1;  // the producer may issue the expert weights
       }
     }
   }
   cons_sync();
-  if (warp == 0) build_tables(tb, epg);
-  cons_sync();
-  if (ctid == 0) {
-    __threadfence_block();
-    tb.tables_ready = 1;
-  }
   const int n_act = tb.n_act, n_actg = tb.n_actg;
 
   // ------------------------------------------------------------ B gate/up
@@ -773,9 +786,11 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
     for (int s = 0; s < KEYS; ++s)
       if (tb.key[s] >= 0) copy_frags(kfr(s), F.Vf + (size_t)tb.key[s] * (f / 128) * FR, (f / 128) * FR, ctid);
     cons_sync();
-    #pragma unroll 1
-    for (int li = warp; li < hi - lo; li += NCW) {
-      const int i = lo + li, es = i / NRB, rb = i % NRB, e = tb.elist[es], g = e / epg;
+    // A warp's items are contracted back to back, then their partials are
+    // published with one fence: the second item does not wait on the first
+    // one's ticket and reduction
+    auto c_compute = [&](int li) {
+      const int i = lo + li, es = i / NRB, rb = i % NRB;
       const uint4* fr = kfr(key_slot(tb, es));
       const unsigned char* sl = cons_wait<NS>(tb, ring, jbase + li, budget, err);
       float* Zp = F.Zp + (size_t)es * 16 * L;
@@ -793,12 +808,13 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
           }
       }
       cons_release<NS>(tb, jbase + li);
+    };
+    auto c_chain = [&](int li) {
+      const int i = lo + li, es = i / NRB, rb = i % NRB, g = tb.elist[es] / epg;
       int gi = 0;
       #pragma unroll 1
       while (gi < n_actg && tb.glist[gi] != g) ++gi;
       const int s0 = tb.gslot0[gi], s1 = tb.gslot0[gi + 1];
-      __threadfence();
-      __syncwarp();
       bool last = false;
       if (lane == 0) last = ticket_last(ctr + cm.tk_down + g * NRB + rb, (unsigned)(s1 - s0));
       last = __shfl_sync(0xffffffffu, last, 0);
@@ -843,6 +859,16 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
         __syncwarp();
         if (lane == 0) atomicAdd(ctr + cm.done_down + g * CSTR, 1u);
       }
+    };
+    #pragma unroll 1
+    for (int li = warp; li < hi - lo; li += 2 * NCW) {
+      const bool two = li + NCW < hi - lo;
+      c_compute(li);
+      if (two) c_compute(li + NCW);
+      __threadfence();
+      __syncwarp();
+      c_chain(li);
+      if (two) c_chain(li + NCW);
     }
     jbase += hi - lo;
   }
