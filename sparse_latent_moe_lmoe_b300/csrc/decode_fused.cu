@@ -81,6 +81,14 @@ struct Tables {
   volatile int seq[16];
 };
 
+// Orders this thread's earlier memory accesses before its later ones at GPU
+// scope. Every hand-off between CTAs here is a release/acquire pair (data,
+// fence, counter atomic; counter seen, fence or acquire load, data), for
+// which an acquire-release fence suffices: the sequentially consistent
+// fence (__threadfence) also joins one total order of all such fences on
+// the GPU, which thousands of hand-offs a pass would wait on.
+LMOE_DEV void fence_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 LMOE_DEV unsigned ld_acquire(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -119,7 +127,7 @@ LMOE_DEV void cons_sync() {
 }
 
 // The last of n arrivals on a ticket returns true; called by one lane after a
-// __threadfence that publishes the caller's partial results.
+// fence_gpu that publishes the caller's partial results.
 LMOE_DEV bool ticket_last(unsigned* t, unsigned n) { return atomicAdd(t, 1u) == n - 1; }
 
 LMOE_DEV float route_weight(const Tables& tb, int t, int e, int k) {
@@ -129,9 +137,11 @@ LMOE_DEV float route_weight(const Tables& tb, int t, int e, int k) {
   return 0.f;
 }
 
-// Counter layout (one copy; two copies alternate between launches). The
-// completion counters that whole CTAs poll sit one per 128-byte line (CSTR
-// words apart); the tickets, which only see atomics, are packed.
+// Counter layout (one copy; two copies alternate between launches). Every
+// counter sits on a 128-byte line of its own (CSTR words apart): the
+// completion counters are polled by whole CTAs, and the tickets take up to
+// a few hundred atomics each within microseconds, which one L2 line would
+// serialise.
 constexpr int CSTR = 32;
 struct CtrMap {
   int tk_router, done_router, tk_win, done_in, done_gu, tk_down, done_down, tk_wout, n;
@@ -139,14 +149,14 @@ struct CtrMap {
 __host__ __device__ inline CtrMap ctr_map(int d, int E, int G, int L) {
   CtrMap m;
   int o = 0;
-  m.tk_router = o; o += E / 2;
+  m.tk_router = o; o += E / 2 * CSTR;
   m.done_router = o; o += CSTR;
-  m.tk_win = o; o += G * (L / 16);
+  m.tk_win = o; o += G * (L / 16) * CSTR;
   m.done_in = o; o += G * CSTR;
   m.done_gu = o; o += MAX_ACT * CSTR;
-  m.tk_down = o; o += G * (L / DR);
+  m.tk_down = o; o += G * (L / DR) * CSTR;
   m.done_down = o; o += G * CSTR;
-  m.tk_wout = o; o += d / 16;
+  m.tk_wout = o; o += d / 16 * CSTR;
   m.n = (o + 31) & ~31;
   return m;
 }
@@ -474,6 +484,19 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
           }
         }
       }
+      if (ok) {  // this CTA's W_out chunks into L2 now, while the experts are computed:
+                 // fetched in a burst at the end they would slow the Z reductions
+        int plo, phi;
+        split(n_actg * NRT_OUT, c, nC, plo, phi);
+        int gi = plo / NRT_OUT, rt = plo % NRT_OUT;
+#pragma unroll 1
+        for (int i = plo; i < phi; ++i) {
+          const int row = tb.glist[gi] * d + rt * 16;
+          tma_prefetch_3d(&F.maps.wout_q, 0, 0, row);
+          tma_prefetch_2d(&F.maps.wout_s, 0, row);
+          if (++rt == NRT_OUT) { rt = 0; ++gi; }
+        }
+      }
       if (ok) split(n_act * NRB, c, nC, lo, hi);
       {  // down: (expert slot, 32-row block)
         int es = lo / NRB, rb = lo % NRB;
@@ -612,13 +635,13 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
       const int t = nt * 8 + (lane >> 2), r = (lane >> 1) & 1;
       if ((lane & 1) == 0 && t < T) F.Lp[((size_t)ks * 16 + t) * E + e0 + r] = v[0];
     }
-    __threadfence();
+    fence_gpu();
     __syncwarp();
     bool last = false;
-    if (lane == 0) last = ticket_last(ctr + cm.tk_router + pr, (unsigned)KS);
+    if (lane == 0) last = ticket_last(ctr + cm.tk_router + pr * CSTR, (unsigned)KS);
     last = __shfl_sync(0xffffffffu, last, 0);
     if (last) {
-      __threadfence();
+      fence_gpu();
       const int t = lane >> 1, r = lane & 1;
       if (t < T) {
         float part[8];
@@ -630,7 +653,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
         if (A.b_r) v += A.b_r[e0 + r];
         F.logits[(size_t)t * E + e0 + r] = v;
       }
-      __threadfence();
+      fence_gpu();
       __syncwarp();
       if (lane == 0) atomicAdd(ctr + cm.done_router, 1u);
     }
@@ -654,13 +677,13 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
         const int row = rt * 16 + gid + ((h & 2) ? 8 : 0), t = nt * 8 + 2 * tig + (h & 1);
         if (t < T) Hp[(size_t)t * L + row] = acc[nt][h];
       }
-    __threadfence();
+    fence_gpu();
     __syncwarp();
     bool last = false;
-    if (lane == 0) last = ticket_last(ctr + cm.tk_win + g * NRT_IN + rt, (unsigned)KS);
+    if (lane == 0) last = ticket_last(ctr + cm.tk_win + (g * NRT_IN + rt) * CSTR, (unsigned)KS);
     last = __shfl_sync(0xffffffffu, last, 0);
     if (last) {  // sum the segment partials in order, straight into fp16 fragments
-      __threadfence();
+      fence_gpu();
       const int run = lane & 1, n = lane >> 1, k0 = rt * 16 + run * 8;
       float e[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       if (n < T) {
@@ -678,7 +701,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
         }
       }
       if (n < 8 * NT) F.Hf[(size_t)g * (L / 128) * FR + entry_index<NT>(k0, n)] = pack_frag8(e);
-      __threadfence();
+      fence_gpu();
       __syncwarp();
       if (lane == 0) atomicAdd(ctr + cm.done_in + g * CSTR, 1u);
     }
@@ -764,7 +787,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
       acc_to_entry<NT>(ag, ev);
       const int run = lane & 1, n = lane >> 1;
       if (n < 8 * NT) F.Vf[(size_t)es * (f / 128) * FR + entry_index<NT>(rt * 16 + run * 8, n)] = pack_frag8(ev);
-      __threadfence();
+      fence_gpu();
       __syncwarp();
       if (lane == 0) atomicAdd(ctr + cm.done_gu + es * CSTR, 1u);
     }
@@ -809,17 +832,19 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
       }
       cons_release<NS>(tb, jbase + li);
     };
-    auto c_chain = [&](int li) {
-      const int i = lo + li, es = i / NRB, rb = i % NRB, g = tb.elist[es] / epg;
+    // block (group, row block) of item li: its ticket and its group's expert slots
+    auto c_block = [&](int li, int& g, int& rb, int& s0, int& s1) {
+      const int i = lo + li, es = i / NRB;
+      rb = i % NRB;
+      g = tb.elist[es] / epg;
       int gi = 0;
       #pragma unroll 1
       while (gi < n_actg && tb.glist[gi] != g) ++gi;
-      const int s0 = tb.gslot0[gi], s1 = tb.gslot0[gi + 1];
-      bool last = false;
-      if (lane == 0) last = ticket_last(ctr + cm.tk_down + g * NRB + rb, (unsigned)(s1 - s0));
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {  // Z rows of this block: the group's experts in ascending order, into fragments
-        __threadfence();
+      s0 = tb.gslot0[gi];
+      s1 = tb.gslot0[gi + 1];
+    };
+    // Z rows of a block: the group's experts in ascending order, into fragments
+    auto c_reduce = [&](int g, int rb, int s0, int s1) {
         // fragment entries per lane: DR/8 runs x 8 NT tokens over 32 lanes;
         // the experts' partials are loaded QB at a time, all loads first
         constexpr int PE = DR / 8 * 8 * NT / 32, QB = NT == 1 ? 12 : 4;
@@ -855,20 +880,38 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
           if (n < 8 * NT)
             F.Zf[(size_t)g * (L / 128) * FR + entry_index<NT>(rb * DR + run * 8, n)] = pack_frag8(ev[u]);
         }
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) atomicAdd(ctr + cm.done_down + g * CSTR, 1u);
-      }
     };
     #pragma unroll 1
     for (int li = warp; li < hi - lo; li += 2 * NCW) {
       const bool two = li + NCW < hi - lo;
       c_compute(li);
       if (two) c_compute(li + NCW);
-      __threadfence();
+      fence_gpu();
       __syncwarp();
-      c_chain(li);
-      if (two) c_chain(li + NCW);
+      // both tickets in flight at once; a block's last arriver reduces it
+      int g0, rb0, a0, b0, g1 = 0, rb1 = 0, a1 = 0, b1 = 0;
+      c_block(li, g0, rb0, a0, b0);
+      if (two) c_block(li + NCW, g1, rb1, a1, b1);
+      bool l0 = false, l1 = false;
+      if (lane == 0) {
+        const unsigned o0 = atomicAdd(ctr + cm.tk_down + (g0 * NRB + rb0) * CSTR, 1u);
+        const unsigned o1 = two ? atomicAdd(ctr + cm.tk_down + (g1 * NRB + rb1) * CSTR, 1u) : 0u;
+        l0 = o0 == (unsigned)(b0 - a0 - 1);
+        l1 = two && o1 == (unsigned)(b1 - a1 - 1);
+      }
+      l0 = __shfl_sync(0xffffffffu, l0, 0);
+      l1 = __shfl_sync(0xffffffffu, l1, 0);
+      if (l0 || l1) {
+        fence_gpu();
+        if (l0) c_reduce(g0, rb0, a0, b0);
+        if (l1) c_reduce(g1, rb1, a1, b1);
+        fence_gpu();
+        __syncwarp();
+        if (lane == 0) {
+          if (l0) atomicAdd(ctr + cm.done_down + g0 * CSTR, 1u);
+          if (l1) atomicAdd(ctr + cm.done_down + g1 * CSTR, 1u);
+        }
+      }
     }
     jbase += hi - lo;
   }
@@ -904,13 +947,13 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
           const int row = rt * 16 + gid + ((h & 2) ? 8 : 0), t = nt * 8 + 2 * tig + (h & 1);
           if (t < T) A.Yp[((size_t)g * 16 + t) * d + row] = acc[nt][h];
         }
-      __threadfence();
+      fence_gpu();
       __syncwarp();
       bool last = false;
-      if (lane == 0) last = ticket_last(ctr + cm.tk_wout + rt, (unsigned)n_actg);
+      if (lane == 0) last = ticket_last(ctr + cm.tk_wout + rt * CSTR, (unsigned)n_actg);
       last = __shfl_sync(0xffffffffu, last, 0);
       if (last) {  // combine in ascending group order: lane -> 4 rows x 1 token, one float4 per group
-        __threadfence();
+        fence_gpu();
 #pragma unroll 1
         for (int q = lane; q < 4 * T; q += 32) {
           const int rq = q & 3, t = q >> 2, row = rt * 16 + rq * 4;

@@ -68,6 +68,17 @@ LMOE_DEV void tma_load_3d_hint(void* dst, const void* tmap, int c0, int c1, int 
       : "memory");
 }
 
+// Prefetch of one tensor-map box into L2 (no shared-memory destination).
+LMOE_DEV void tma_prefetch_2d(const void* tmap, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap), "r"(c0), "r"(c1)
+               : "memory");
+}
+LMOE_DEV void tma_prefetch_3d(const void* tmap, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap), "r"(c0), "r"(c1),
+               "r"(c2)
+               : "memory");
+}
+
 // 16-byte global -> shared copy (cp.async, bypassing L1)
 LMOE_DEV void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
