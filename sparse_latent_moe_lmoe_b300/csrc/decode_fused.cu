@@ -76,7 +76,8 @@ struct Tables {
   int n_act, n_actg, par;
   volatile int tables_ready;
   volatile int x_issued;     // the consumers' loads of x are in flight: weight copies may start
-  int key[KEYS];
+  int key[KEYS];              // activation sets of the B, C and D phases
+  int keyA[KEYS];             // segments of x staged for the A phase
   uint64_t full[16], empty[16];
   volatile int seq[16];
 };
@@ -180,7 +181,7 @@ LMOE_COLD void stage_x(Tables& tb, uint4* keyset, const uint16_t* x, int T, int 
   uint4 v[KEYS][PER];
 #pragma unroll
   for (int s = 0; s < KEYS; ++s) {
-    const int ks = tb.key[s];
+    const int ks = tb.keyA[s];
 #pragma unroll
     for (int r = 0; r < PER; ++r) {
       const int si = ctid + r * NCT;
@@ -200,7 +201,7 @@ LMOE_COLD void stage_x(Tables& tb, uint4* keyset, const uint16_t* x, int T, int 
 #pragma unroll
     for (int r = 0; r < PER; ++r) {
       const int si = ctid + r * NCT;
-      if (tb.key[s] < 0 || si >= N) continue;
+      if (tb.keyA[s] < 0 || si >= N) continue;
       const uint32_t u[4] = {v[s][r].x, v[s][r].y, v[s][r].z, v[s][r].w};
       float e[8];
 #pragma unroll
@@ -236,7 +237,7 @@ LMOE_COLD void copy_frags(uint4* dst, const uint4* src, int n, int ctid) {
 // Distinct keys of items [lo, hi) (nondecreasing) into the key table; returns
 // false (and flags bad data) if more than KEYS are needed. Consumer thread 0.
 template <class KeyF>
-LMOE_COLD void collect_keys(Tables& tb, int lo, int hi, KeyF key, unsigned* err) {
+LMOE_COLD void collect_keys(int* keys, int lo, int hi, KeyF key, unsigned* err) {
   int n = 0, last = -1;
   #pragma unroll 1
   for (int i = lo; i < hi; ++i) {
@@ -246,18 +247,18 @@ LMOE_COLD void collect_keys(Tables& tb, int lo, int hi, KeyF key, unsigned* err)
         set_error(err, ERRBIT_BAD_DATA);
         break;
       }
-      tb.key[n++] = kk;
+      keys[n++] = kk;
       last = kk;
     }
   }
   #pragma unroll 1
-  for (int s = n; s < KEYS; ++s) tb.key[s] = -1;
+  for (int s = n; s < KEYS; ++s) keys[s] = -1;
 }
 
-LMOE_DEV int key_slot(const Tables& tb, int kk) {
+LMOE_DEV int key_slot(const int* keys, int kk) {
   #pragma unroll 1
   for (int s = 0; s < KEYS; ++s)
-    if (tb.key[s] == kk) return s;
+    if (keys[s] == kk) return s;
   return 0;
 }
 
@@ -563,10 +564,10 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
         set_error(err, ERRBIT_BAD_DATA);
         break;
       }
-      tb.key[n++] = ks;
+      tb.keyA[n++] = ks;
     }
     #pragma unroll 1
-    for (int s = n; s < KEYS; ++s) tb.key[s] = -1;
+    for (int s = n; s < KEYS; ++s) tb.keyA[s] = -1;
   }
   cons_sync();
   stage_x<NT>(tb, keyset, A.x, T, d, ctid);
@@ -577,7 +578,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
   for (int li = warp; li < nA1; li += NCW) {
     const int i = a1lo + li, ks = i / NPAIR, pr = i % NPAIR, e0 = 2 * pr;
     const float* wr = reinterpret_cast<const float*>(cons_wait<NS>(tb, ring, jbase + li, budget, err));
-    const uint4* fr = kfr(key_slot(tb, ks));
+    const uint4* fr = kfr(key_slot(tb.keyA, ks));
     // lane covers elements u*256 + 8*lane .. +7 (u < 4) of both experts; for
     // each half of u the 32 weights stay in registers while the tokens stream
     // past, 16 independent sums per lane
@@ -667,7 +668,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
     const unsigned char* sl = cons_wait<NS>(tb, ring, jbase + li, budget, err);
     float acc[NT][4] = {};
     mma_ring_rows_swz<NT>(sl, KSEG / 256, 0, reinterpret_cast<const uint16_t*>(sl + 16 * KSEG / 2), KSEG / 32,
-                          KSEG / 128, kfr(key_slot(tb, ks)), acc);
+                          KSEG / 128, kfr(key_slot(tb.keyA, ks)), acc);
     cons_release<NS>(tb, jbase + li);
     float* Hp = A.Hp + ((size_t)ks * G + g) * 16 * L;
 #pragma unroll
@@ -739,6 +740,14 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
         __threadfence_block();
         tb.tables_ready = 1;  // the producer may issue the expert weights
       }
+      // the B phase's groups and the completion of their H, while the other
+      // warps finish the A phase
+      int lo, hi;
+      split(tb.n_act * (f / 16), c, nC, lo, hi);
+      if (lane == 0) collect_keys(tb.key, lo, hi, [&](int i) { return tb.elist[i / (f / 16)] / epg; }, err);
+      __syncwarp();
+      wait_counts(lane < KEYS && tb.key[lane] >= 0 ? ctr + cm.done_in + tb.key[lane] * CSTR : nullptr, (unsigned)NRT_IN,
+                  budget, err);
     }
   }
   cons_sync();
@@ -747,12 +756,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
   // ------------------------------------------------------------ B gate/up
   {
     int lo, hi;
-    split(n_act * (f / 16), c, nC, lo, hi);
-    if (ctid == 0) collect_keys(tb, lo, hi, [&](int i) { return tb.elist[i / (f / 16)] / epg; }, err);
-    cons_sync();
-    if (warp == 0)
-      wait_counts(lane < KEYS && tb.key[lane] >= 0 ? ctr + cm.done_in + tb.key[lane] * CSTR : nullptr, (unsigned)NRT_IN, budget, err);
-    cons_sync();
+    split(n_act * (f / 16), c, nC, lo, hi);  // keys collected, H completion awaited by the routing
     #pragma unroll 1
     for (int s = 0; s < KEYS; ++s)
       if (tb.key[s] >= 0) copy_frags(kfr(s), F.Hf + (size_t)tb.key[s] * (L / 128) * FR, (L / 128) * FR, ctid);
@@ -760,7 +764,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
     #pragma unroll 1
     for (int li = warp; li < hi - lo; li += NCW) {
       const int i = lo + li, es = i / (f / 16), rt = i % (f / 16), e = tb.elist[es];
-      const uint4* fr = kfr(key_slot(tb, e / epg));
+      const uint4* fr = kfr(key_slot(tb.key, e / epg));
       float ag[NT][4] = {}, au[NT][4] = {};
       const unsigned char* sg = cons_wait<NS>(tb, ring, jbase + 2 * li, budget, err);
       const unsigned char* su = cons_wait<NS>(tb, ring, jbase + 2 * li + 1, budget, err);
@@ -799,7 +803,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
     int lo, hi;
     split(n_act * NRB, c, nC, lo, hi);
     cons_sync();
-    if (ctid == 0) collect_keys(tb, lo, hi, [&](int i) { return i / NRB; }, err);
+    if (ctid == 0) collect_keys(tb.key, lo, hi, [&](int i) { return i / NRB; }, err);
     cons_sync();
     if (warp == 0)
       wait_counts(lane < KEYS && tb.key[lane] >= 0 ? ctr + cm.done_gu + tb.key[lane] * CSTR : nullptr, (unsigned)(f / 16), budget,
@@ -814,7 +818,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
     // one's ticket and reduction
     auto c_compute = [&](int li) {
       const int i = lo + li, es = i / NRB, rb = i % NRB;
-      const uint4* fr = kfr(key_slot(tb, es));
+      const uint4* fr = kfr(key_slot(tb.key, es));
       const unsigned char* sl = cons_wait<NS>(tb, ring, jbase + li, budget, err);
       float* Zp = F.Zp + (size_t)es * 16 * L;
 #pragma unroll 1
@@ -921,7 +925,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
     int lo, hi;
     split(n_actg * NRT_OUT, c, nC, lo, hi);
     cons_sync();
-    if (ctid == 0) collect_keys(tb, lo, hi, [&](int i) { return i / NRT_OUT; }, err);
+    if (ctid == 0) collect_keys(tb.key, lo, hi, [&](int i) { return i / NRT_OUT; }, err);
     cons_sync();
     if (warp == 0)
       wait_counts(lane < KEYS && tb.key[lane] >= 0 ? ctr + cm.done_down + tb.glist[tb.key[lane]] * CSTR : nullptr, (unsigned)NRB,
@@ -938,7 +942,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
       const unsigned char* sl = cons_wait<NS>(tb, ring, jbase + li, budget, err);
       float acc[NT][4] = {};
       mma_ring_rows_swz<NT>(sl, L / 256, 0, reinterpret_cast<const uint16_t*>(sl + 16 * L / 2), L / 32, L / 128,
-                            kfr(key_slot(tb, gi)), acc);
+                            kfr(key_slot(tb.key, gi)), acc);
       cons_release<NS>(tb, jbase + li);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
