@@ -78,6 +78,7 @@ struct Tables {
   volatile int x_issued;     // the consumers' loads of x are in flight: weight copies may start
   int key[KEYS];              // activation sets of the B, C and D phases
   int keyA[KEYS];             // segments of x staged for the A phase
+  uint2 tkscr[NCW][32];       // top-k candidates, per routing warp
   uint64_t full[16], empty[16];
   volatile int seq[16];
 };
@@ -721,7 +722,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
     route_sync(nrw);
 #pragma unroll 1
     for (int tw = warp - rw0; tw < T; tw += nrw) {
-      const float2 sw = topk_warp(F.logits + (size_t)tw * E, E, k);
+      const float2 sw = topk_warp_thr(F.logits + (size_t)tw * E, E, k, tb.tkscr[warp]);
       if (lane < k) {
         const int e = __float_as_int(sw.x);
         tb.idx[tw * 16 + lane] = e;

@@ -172,9 +172,10 @@ struct ProbRoute : ProbBase {
 // top-k with softmax renormalisation, one warp per token
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                                                          int32_t* __restrict__ idx, float* __restrict__ w) {
+  __shared__ uint2 scratch[8][32];
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (t >= T) return;
-  const float2 sw = topk_warp(logits + (size_t)t * E, E, k);
+  const float2 sw = topk_warp_thr(logits + (size_t)t * E, E, k, scratch[threadIdx.x >> 5]);
   if (lane < k) {
     idx[(size_t)t * k + lane] = __float_as_int(sw.x);
     w[(size_t)t * k + lane] = sw.y;

@@ -77,4 +77,64 @@ static __device__ __noinline__ float2 topk_warp(const float* row, int E, int k) 
   return make_float2(__int_as_float(sel_e), lane < k ? ex / z : 0.f);
 }
 
+// The same selection by a threshold: the k-th largest of the 32 lane maxima
+// bounds the k-th largest logit from below, so the logits at or above it
+// (usually a few more than k) hold the whole answer; they are gathered in
+// shared memory and sorted across the warp by (logit desc, expert asc).
+// Falls back to topk_warp when more than 32 logits reach the threshold.
+// `scratch` is 32 entries of shared memory owned by the calling warp.
+static __device__ __noinline__ float2 topk_warp_thr(const float* row, int E, int k, uint2* scratch) {
+  const int lane = threadIdx.x & 31;
+  unsigned key[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) key[i] = lane + 32 * i < E ? float_key(__ldcg(row + lane + 32 * i)) : 0u;
+  unsigned v = key[0];
+#pragma unroll
+  for (int i = 1; i < 16; ++i) v = max(v, key[i]);
+  // bitonic sort of the lane maxima, descending
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const unsigned o = __shfl_xor_sync(0xffffffffu, v, stride);
+      const bool desc = (lane & size) == 0, lower = (lane & stride) == 0;
+      v = (lower == desc) ? max(v, o) : min(v, o);
+    }
+  const unsigned tau = __shfl_sync(0xffffffffu, v, k - 1);
+  int cnt = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) cnt += key[i] >= tau;
+  int pre = cnt;  // inclusive prefix over lanes
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, pre, o);
+    if (lane >= o) pre += y;
+  }
+  if (__shfl_sync(0xffffffffu, pre, 31) > 32) return topk_warp(row, E, k);
+  int pos = pre - cnt;
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    if (key[i] >= tau) scratch[pos++] = make_uint2(key[i], (unsigned)(lane + 32 * i));
+  __syncwarp();
+  const int C = __shfl_sync(0xffffffffu, pre, 31);
+  uint2 cd = lane < C ? scratch[lane] : make_uint2(0u, 0xffffffffu);
+  __syncwarp();
+  // bitonic sort of the candidates: larger logit first, then lower expert
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const unsigned ox = __shfl_xor_sync(0xffffffffu, cd.x, stride), oy = __shfl_xor_sync(0xffffffffu, cd.y, stride);
+      const bool desc = (lane & size) == 0, lower = (lane & stride) == 0;
+      const bool mine_first = cd.x > ox || (cd.x == ox && cd.y < oy);
+      if ((lower == desc) != mine_first) cd = make_uint2(ox, oy);
+    }
+  const unsigned k0 = __shfl_sync(0xffffffffu, cd.x, 0);
+  const float ex = (lane < k) ? __expf(key_float(cd.x) - key_float(k0)) : 0.f;
+  float z = ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  return make_float2(__int_as_float(lane < k && cd.y < (unsigned)E ? (int)cd.y : 0), lane < k ? ex / z : 0.f);
+}
+
 }  // namespace lmoe
