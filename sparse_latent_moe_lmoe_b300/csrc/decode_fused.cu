@@ -588,7 +588,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
       float v[16];  // v[2 t + r]: token 8 nt + t, expert e0 + r
 #pragma unroll
       for (int q = 0; q < 16; ++q) v[q] = 0.f;
-#pragma unroll
+#pragma unroll 1
       for (int uh = 0; uh < 2; ++uh) {
         float4 w0[2][2], w1[2][2];
 #pragma unroll
@@ -889,8 +889,8 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
     #pragma unroll 1
     for (int li = warp; li < hi - lo; li += 2 * NCW) {
       const bool two = li + NCW < hi - lo;
-      c_compute(li);
-      if (two) c_compute(li + NCW);
+      #pragma unroll 1
+      for (int q = 0; q < (two ? 2 : 1); ++q) c_compute(li + q * NCW);  // one copy of the code
       fence_gpu();
       __syncwarp();
       // both tickets in flight at once; a block's last arriver reduces it
@@ -908,8 +908,9 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
       l1 = __shfl_sync(0xffffffffu, l1, 0);
       if (l0 || l1) {
         fence_gpu();
-        if (l0) c_reduce(g0, rb0, a0, b0);
-        if (l1) c_reduce(g1, rb1, a1, b1);
+        #pragma unroll 1
+        for (int q = 0; q < 2; ++q)
+          if (q ? l1 : l0) c_reduce(q ? g1 : g0, q ? rb1 : rb0, q ? a1 : a0, q ? b1 : b0);
         fence_gpu();
         __syncwarp();
         if (lane == 0) {
