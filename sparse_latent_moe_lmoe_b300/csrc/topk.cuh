@@ -4,10 +4,11 @@
 // selected j.
 //
 // Each lane holds experts lane, lane + 32, ... as order-preserving integer
-// keys and its best remaining one (a depth-4 tournament); every round the
-// warp takes the largest head key (a warp max reduction), then the lowest
-// expert index holding it (a warp min reduction), and only the winning lane
-// rescans.
+// keys. topk_warp_thr gathers the logits at or above a threshold and sorts
+// them across the warp; topk_warp, its fallback, runs k rounds in which the
+// warp takes the largest remaining key (a warp max reduction), then the
+// lowest expert index holding it (a warp min reduction), and only the
+// winning lane rescans its keys.
 #pragma once
 #include "common.cuh"
 
@@ -22,39 +23,33 @@ static LMOE_DEV float key_float(unsigned k) { return __uint_as_float((k & 0x8000
 
 // Lane j < k returns (expert of the j-th pick as int bits, its weight); other
 // lanes return (0, 0). `row` holds the token's E logits (read through L2).
+// Used where more than 32 logits tie at the k-th place (see topk_warp_thr).
 static __device__ __noinline__ float2 topk_warp(const float* row, int E, int k) {
   const int lane = threadIdx.x & 31;
   unsigned key[16];  // element i is expert lane + 32 i; 0 = none (below every finite key)
 #pragma unroll
   for (int i = 0; i < 16; ++i) key[i] = lane + 32 * i < E ? float_key(__ldcg(row + lane + 32 * i)) : 0u;
-  // this lane's best remaining element, ties to the lower i: a depth-4 tournament
-  auto best = [&](unsigned& bk, int& bi) {
-    unsigned tk[8];
-    int ti[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const bool hi = key[2 * i + 1] > key[2 * i];
-      tk[i] = hi ? key[2 * i + 1] : key[2 * i];
-      ti[i] = hi ? 2 * i + 1 : 2 * i;
-    }
-#pragma unroll
-    for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-      for (int i = 0; i < w; ++i) {
-        const bool hi = tk[2 * i + 1] > tk[2 * i];
-        tk[i] = hi ? tk[2 * i + 1] : tk[2 * i];
-        ti[i] = hi ? ti[2 * i + 1] : ti[2 * i];
-      }
-    bk = tk[0];
-    bi = ti[0];
-  };
-  unsigned bk;
-  int bi;
-  best(bk, bi);
+  // this lane's best remaining element (ties to the lower i), recomputed by a
+  // linear scan when the lane's head was taken: one copy of the scan keeps
+  // the code small
+  unsigned bk = 0;
+  int bi = 0;
+  bool stale = true;
   unsigned sel = 0, k0 = 0;
   int sel_e = 0;
 #pragma unroll 1
   for (int j = 0; j < k; ++j) {
+    if (stale) {
+      bk = key[0];
+      bi = 0;
+#pragma unroll
+      for (int i = 1; i < 16; ++i)
+        if (key[i] > bk) {
+          bk = key[i];
+          bi = i;
+        }
+      stale = false;
+    }
     const unsigned m = __reduce_max_sync(0xffffffffu, bk);
     const int mine = lane + 32 * bi;
     const unsigned wi = __reduce_min_sync(0xffffffffu, bk == m ? (unsigned)mine : 0xffffffffu);
@@ -62,7 +57,7 @@ static __device__ __noinline__ float2 topk_warp(const float* row, int E, int k) 
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         if (i == bi) key[i] = 0u;
-      best(bk, bi);
+      stale = true;
     }
     if (j == 0) k0 = m;
     if (lane == j) {
@@ -91,10 +86,11 @@ static __device__ __noinline__ float2 topk_warp_thr(const float* row, int E, int
   unsigned v = key[0];
 #pragma unroll
   for (int i = 1; i < 16; ++i) v = max(v, key[i]);
-  // bitonic sort of the lane maxima, descending
-#pragma unroll
+  // bitonic sort of the lane maxima, descending (loops kept rolled: this code
+  // runs once per token and its size, not its issue count, is what costs)
+#pragma unroll 1
   for (int size = 2; size <= 32; size <<= 1)
-#pragma unroll
+#pragma unroll 1
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       const unsigned o = __shfl_xor_sync(0xffffffffu, v, stride);
       const bool desc = (lane & size) == 0, lower = (lane & stride) == 0;
@@ -120,9 +116,9 @@ static __device__ __noinline__ float2 topk_warp_thr(const float* row, int E, int
   uint2 cd = lane < C ? scratch[lane] : make_uint2(0u, 0xffffffffu);
   __syncwarp();
   // bitonic sort of the candidates: larger logit first, then lower expert
-#pragma unroll
+#pragma unroll 1
   for (int size = 2; size <= 32; size <<= 1)
-#pragma unroll
+#pragma unroll 1
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       const unsigned ox = __shfl_xor_sync(0xffffffffu, cd.x, stride), oy = __shfl_xor_sync(0xffffffffu, cd.y, stride);
       const bool desc = (lane & size) == 0, lower = (lane & stride) == 0;
