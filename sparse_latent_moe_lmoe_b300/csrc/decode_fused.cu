@@ -5,16 +5,19 @@
 // the CTA's list of weight chunks for the whole layer and loads each into the
 // next ring slot with TMA tensor copies (one box of up to 8 KB of packed int4
 // in 128-byte swizzle plus one box of bf16 scales, or 8 KB of fp32 router
-// rows), as far ahead as the ring allows. Warps 0..14 consume the chunks with
-// tensor-core MMAs (int4 dequantised in registers, fp16 operands, fp32
-// accumulation) against activation fragments staged in shared memory.
+// rows), as far ahead as the ring allows (weights with an evict-first L2
+// policy; W_out also prefetched into L2 during the expert phases). Warps
+// 0..14 consume the chunks with tensor-core MMAs (int4 dequantised in
+// registers, fp16 operands, fp32 accumulation) against activation fragments
+// staged in shared memory.
 //
 // Work, in ring order (KS = d/1024 reduction segments):
 //   A1  router logits: (segment, expert pair) items, partial sums reduced in
 //       segment order by the last arriver of each pair
-//   --  every CTA computes the routing itself (top-k, softmax, tables)
 //   A2  H[g] = W_in[g] x for every group: (segment, group, 16-row tile)
 //       items, reduced in segment order by the last arriver of each tile
+//   --  every CTA computes the routing itself (top-k, softmax, tables) on
+//       the warps without a router item, while the others finish A2
 //   B   V[e] = silu(Gate_e h) * Up_e h for each routed expert: (expert,
 //       16-row tile) items, gate and up chunks back to back
 //   C   Z[g] = sum_{e in g} Down_e (w V_e): (expert, 32-row block) items with
