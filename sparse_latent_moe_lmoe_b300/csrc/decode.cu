@@ -274,21 +274,55 @@ __global__ void __launch_bounds__(ROUTE_WARPS * 32) route_kernel(DecodeArgs A, i
 }
 
 // ------------------------------------------------------------------- LoRA
-// P[g][t][c] = sum_i act(t, i) * A[g][i][c]: one CTA per (g, t), one thread per c.
-__global__ void lora_proj_kernel(DecodeArgs A, int which) {
-  const int g = blockIdx.x, t = blockIdx.y, c = threadIdx.x, r = A.r;
-  if (c >= r) return;
-  if (which == 0) {
-    const uint16_t* Am = A.A_in + (size_t)g * A.d * r;
-    float acc = 0.f;
-    for (int i = 0; i < A.d; ++i) acc = fmaf(bf16_to_f32(A.x[(size_t)t * A.d + i]), bf16_to_f32(Am[(size_t)i * r + c]), acc);
-    A.Pin[((size_t)g * 16 + t) * r + c] = acc;
-  } else {
-    const uint16_t* Am = A.A_out + (size_t)g * A.L * r;
-    const float* z = A.Z + ((size_t)g * 16 + t) * A.L;
-    float acc = 0.f;
-    for (int l = 0; l < A.L; ++l) acc = fmaf(z[l], bf16_to_f32(Am[(size_t)l * r + c]), acc);
-    A.Qout[((size_t)g * 16 + t) * r + c] = acc;
+// P[g][t][c] = sum_i act(t, i) * M[g][i][c] (M = A_in over i < d with act = x,
+// or A_out over i < L with act = Z): one CTA of 8 warps per (g, t). Warp w
+// takes rows w, w + 8, ... (four rows in flight), lane l the column pairs
+// 2 (l + 32 q), so a warp reads whole 128-byte rows of M; the warps' sums are
+// added in warp order.
+__global__ void __launch_bounds__(256) lora_proj_kernel(DecodeArgs A, int which) {
+  constexpr int QP = 2;  // column pairs per lane: r <= 128
+  __shared__ float red[8][128];
+  const int g = blockIdx.x, t = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31, r = A.r;
+  const int K = which == 0 ? A.d : A.L;
+  const uint16_t* M = which == 0 ? A.A_in + (size_t)g * A.d * r : A.A_out + (size_t)g * A.L * r;
+  const uint16_t* xr = A.x + (size_t)t * A.d;
+  const float* zr = A.Z + ((size_t)g * 16 + t) * A.L;
+  float s[QP][2][4];
+#pragma unroll
+  for (int q = 0; q < QP; ++q)
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) s[q][h][u] = 0.f;
+  for (int i0 = warp; i0 < K; i0 += 32) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + 8 * u;
+      if (i >= K) continue;
+      const float act = which == 0 ? bf16_to_f32(xr[i]) : zr[i];
+#pragma unroll
+      for (int q = 0; q < QP; ++q) {
+        const int c = 2 * (lane + 32 * q);
+        if (c >= r) continue;
+        const uint32_t m2 = *reinterpret_cast<const uint32_t*>(M + (size_t)i * r + c);
+        s[q][0][u] = fmaf(act, __uint_as_float(m2 << 16), s[q][0][u]);
+        s[q][1][u] = fmaf(act, __uint_as_float(m2 & 0xffff0000u), s[q][1][u]);
+      }
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < QP; ++q) {
+    const int c = 2 * (lane + 32 * q);
+    if (c >= r) continue;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) red[warp][c + h] = (s[q][h][0] + s[q][h][1]) + (s[q][h][2] + s[q][h][3]);
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < r; c += blockDim.x) {
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) v += red[w][c];
+    (which == 0 ? A.Pin : A.Qout)[((size_t)g * 16 + t) * r + c] = v;
   }
 }
 
@@ -644,7 +678,7 @@ cudaError_t launch_route(const DecodeArgs& A, int do_perm, float* logits_out, cu
 }
 
 cudaError_t launch_lora_proj(const DecodeArgs& A, int which, cudaStream_t st) {
-  lora_proj_kernel<<<dim3(A.G, A.T), 128, 0, st>>>(A, which);
+  lora_proj_kernel<<<dim3(A.G, A.T), 256, 0, st>>>(A, which);
   return cudaGetLastError();
 }
 
@@ -672,7 +706,7 @@ static cudaError_t launch_experts_nt(const DecodeArgs& A, int mode, cudaStream_t
   }
   if (A.r > 0) {
     if (hook) hook->before(st);
-    lora_proj_kernel<<<dim3(A.G, A.T), 128, 0, st>>>(A, 1);
+    lora_proj_kernel<<<dim3(A.G, A.T), 256, 0, st>>>(A, 1);
     if (hook) hook->after(st);
   }
   {
