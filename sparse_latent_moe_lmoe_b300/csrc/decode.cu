@@ -275,53 +275,50 @@ __global__ void __launch_bounds__(ROUTE_WARPS * 32) route_kernel(DecodeArgs A, i
 
 // ------------------------------------------------------------------- LoRA
 // P[g][t][c] = sum_i act(t, i) * M[g][i][c] (M = A_in over i < d with act = x,
-// or A_out over i < L with act = Z): one CTA of 8 warps per (g, t). Warp w
-// takes rows w, w + 8, ... (four rows in flight), lane l the column pairs
-// 2 (l + 32 q), so a warp reads whole 128-byte rows of M; the warps' sums are
-// added in warp order.
+// or A_out over i < L with act = Z): one CTA of 8 warps per (g, t). A row of M
+// is r/8 16-byte chunks; lane l of a warp takes chunk l % (r/8) of row
+// l / (r/8) of the warp's rows, and eight row passes are loaded before any is
+// used, so a CTA keeps 32 KB of M in flight. Partial sums are added in a
+// fixed order (warp, then row within the warp).
 __global__ void __launch_bounds__(256) lora_proj_kernel(DecodeArgs A, int which) {
-  constexpr int QP = 2;  // column pairs per lane: r <= 128
-  __shared__ float red[8][128];
-  const int g = blockIdx.x, t = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31, r = A.r;
+  __shared__ float red[256][8];
+  const int g = blockIdx.x, t = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, r = A.r;
+  const int cpr = r / 8, rpw = 32 / cpr;  // chunks per row (2..16), rows per warp pass
+  const int rl = lane / cpr, cc = lane % cpr, step = 8 * rpw;
   const int K = which == 0 ? A.d : A.L;
   const uint16_t* M = which == 0 ? A.A_in + (size_t)g * A.d * r : A.A_out + (size_t)g * A.L * r;
   const uint16_t* xr = A.x + (size_t)t * A.d;
   const float* zr = A.Z + ((size_t)g * 16 + t) * A.L;
-  float s[QP][2][4];
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (rl < rpw) {
+    for (int i0 = warp * rpw + rl; i0 < K; i0 += 8 * step) {
+      uint4 m[8];
+      float act[8];
 #pragma unroll
-  for (int q = 0; q < QP; ++q)
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * step;
+        m[u] = i < K ? __ldg(reinterpret_cast<const uint4*>(M + (size_t)i * r + cc * 8)) : make_uint4(0u, 0u, 0u, 0u);
+        act[u] = i < K ? (which == 0 ? bf16_to_f32(xr[i]) : zr[i]) : 0.f;
+      }
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t w[4] = {m[u].x, m[u].y, m[u].z, m[u].w};
 #pragma unroll
-      for (int u = 0; u < 4; ++u) s[q][h][u] = 0.f;
-  for (int i0 = warp; i0 < K; i0 += 32) {
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + 8 * u;
-      if (i >= K) continue;
-      const float act = which == 0 ? bf16_to_f32(xr[i]) : zr[i];
-#pragma unroll
-      for (int q = 0; q < QP; ++q) {
-        const int c = 2 * (lane + 32 * q);
-        if (c >= r) continue;
-        const uint32_t m2 = *reinterpret_cast<const uint32_t*>(M + (size_t)i * r + c);
-        s[q][0][u] = fmaf(act, __uint_as_float(m2 << 16), s[q][0][u]);
-        s[q][1][u] = fmaf(act, __uint_as_float(m2 & 0xffff0000u), s[q][1][u]);
+        for (int h = 0; h < 4; ++h) {
+          acc[2 * h] = fmaf(act[u], __uint_as_float(w[h] << 16), acc[2 * h]);
+          acc[2 * h + 1] = fmaf(act[u], __uint_as_float(w[h] & 0xffff0000u), acc[2 * h + 1]);
+        }
       }
     }
   }
 #pragma unroll
-  for (int q = 0; q < QP; ++q) {
-    const int c = 2 * (lane + 32 * q);
-    if (c >= r) continue;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) red[warp][c + h] = (s[q][h][0] + s[q][h][1]) + (s[q][h][2] + s[q][h][3]);
-  }
+  for (int j = 0; j < 8; ++j) red[tid][j] = acc[j];
   __syncthreads();
-  for (int c = threadIdx.x; c < r; c += blockDim.x) {
+  for (int c = tid; c < r; c += blockDim.x) {
+    const int chunk = c / 8, j = c % 8;
     float v = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) v += red[w][c];
+    for (int w = 0; w < 8; ++w)
+      for (int q = 0; q < rpw; ++q) v += red[w * 32 + q * cpr + chunk][j];
     (which == 0 ? A.Pin : A.Qout)[((size_t)g * 16 + t) * r + c] = v;
   }
 }
