@@ -176,19 +176,6 @@ LMOE_DEV void mma_rows(const uint8_t* __restrict__ q, const uint16_t* __restrict
   }
 }
 
-// Write a warp's accumulator tile to smem as [16 rows][8*NT tokens] floats.
-template <int NT>
-LMOE_DEV void acc_to_smem(const float acc[NT][4], float* tile /* [16][8*NT] */) {
-  const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    tile[gid * (8 * NT) + nt * 8 + 2 * tig] = acc[nt][0];
-    tile[gid * (8 * NT) + nt * 8 + 2 * tig + 1] = acc[nt][1];
-    tile[(gid + 8) * (8 * NT) + nt * 8 + 2 * tig] = acc[nt][2];
-    tile[(gid + 8) * (8 * NT) + nt * 8 + 2 * tig + 1] = acc[nt][3];
-  }
-}
-
 LMOE_DEV void set_error(unsigned* err, unsigned bits) {
   if (err) atomicOr(err, bits);
 }

@@ -20,15 +20,6 @@ LMOE_DEV void mbar_expect_tx(uint64_t* m, uint32_t bytes) {
                : "memory");
 }
 
-// global -> shared bulk copy (16-byte aligned addresses, size a multiple of
-// 16) completing on mbarrier m
-LMOE_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* m) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(m))
-      : "memory");
-}
-
 // TMA tensor loads (tile mode) completing on mbarrier m; coordinates
 // innermost first. The tensor map lives in kernel parameter space.
 LMOE_DEV void tma_load_2d(void* dst, const void* tmap, int c0, int c1, uint64_t* m) {
@@ -79,17 +70,6 @@ LMOE_DEV void tma_prefetch_3d(const void* tmap, int c0, int c1, int c2) {
                : "memory");
 }
 
-// 16-byte global -> shared copy (cp.async, bypassing L1)
-LMOE_DEV void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-
-// One arrival on m once every cp.async this thread issued before has landed
-// (the barrier's expected count includes these arrivals).
-LMOE_DEV void cp_async_arrive(uint64_t* m) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(m)) : "memory");
-}
-
 LMOE_DEV bool mbar_test(uint64_t* m, uint32_t parity) {
   uint32_t ok;
   asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
@@ -99,46 +79,12 @@ LMOE_DEV bool mbar_test(uint64_t* m, uint32_t parity) {
   return ok != 0;
 }
 
-// acc[nt] += W[16 rows][128*nc elements] * frags, with W in a ring slot:
-// rows at byte stride RS from `w` (already offset to the first row and the
-// first 128-element chunk), scales at element stride SS from `s` (offset
-// likewise). frag points at the fragments of the first chunk (see
-// frag_index; chunk c of the slot uses fragment chunk c).
-template <int NT>
-LMOE_DEV void mma_ring_rows(const unsigned char* w, int RS, const uint16_t* s, int SS, int nc, const uint4* frag,
-                            float acc[NT][4]) {
-  const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
-  const unsigned char* p0 = w + gid * RS + tig * 16;
-  const unsigned char* p8 = p0 + 8 * RS;
-  const uint16_t* s0 = s + gid * SS + tig;
-  const uint16_t* s8 = s0 + 8 * SS;
-#pragma unroll 2
-  for (int c = 0; c < nc; ++c) {
-    const uint4 a = *reinterpret_cast<const uint4*>(p0 + c * 64);
-    const uint4 b = *reinterpret_cast<const uint4*>(p8 + c * 64);
-    const __half2 h0 = scale_h2(s0[c * 4]), h8 = scale_h2(s8[c * 4]);
-    const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
-    const uint32_t wb[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-    for (int mp = 0; mp < 4; ++mp) {
-      uint32_t A[4], B8[4];
-      dequant_word(wa[mp], h0, A);
-      dequant_word(wb[mp], h8, B8);
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const uint4 f = frag[frag_index(c, nt, mp, lane, NT)];
-        mma16816(acc[nt], A[0], B8[0], A[1], B8[1], f.x, f.y);
-        mma16816(acc[nt], A[2], B8[2], A[3], B8[3], f.z, f.w);
-      }
-    }
-  }
-}
-
-// The same contraction with W stored densely by a TMA box with 128-byte
-// swizzle: row r of the chunk is LPR 128-byte lines (line i = r*LPR + k/256
-// for element k), and 16-byte unit j of line i sits at unit j ^ (i & 7).
-// `w` is the (1024-byte aligned) slot base, row0 the first row of the tile,
-// `s` the chunk's scales [rows][SS].
+// acc[nt] += W[16 rows][128*nc elements] * fragments (see frag_index; chunk c
+// of the slot uses fragment chunk c), with W in a ring slot as a TMA box with
+// 128-byte swizzle: row r of the chunk is LPR 128-byte lines (line i = r*LPR
+// + k/256 for element k), and 16-byte unit j of line i sits at unit
+// j ^ (i & 7). `w` is the (1024-byte aligned) slot base, row0 the first row
+// of the tile, `s` the chunk's scales [rows][SS].
 template <int NT>
 LMOE_DEV void mma_ring_rows_swz(const unsigned char* w, int LPR, int row0, const uint16_t* s, int SS, int nc,
                                 const uint4* frag, float acc[NT][4]) {
