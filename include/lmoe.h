@@ -151,7 +151,10 @@ lmoe_status lmoe_destroy(lmoe_handle* h);
  * tokens needs; the same bound serves every entry point. 0 on a bad handle or T < 0. */
 size_t lmoe_workspace_size(const lmoe_handle* h, int T);
 
-/* Router and top-k ("512 experts, 10 activated per token").
+/* Router and top-k. Source: "Edge0-145B: Run a 145B Open-Source Model on
+ * Your Laptop", section "Not Compression -- Architecture" (512 experts, 10
+ * active per token); the selection rule (descending logit, ties to the lower
+ * index, softmax over the selected logits) is this library's reading.
  *  x [T][d] bf16 -> idx [T][k] int32 (descending logit, ties to the lower
  *  expert index), w [T][k] fp32 (softmax over the selected logits), and, if
  *  logits != NULL, the fp32 router logits [T][E] the selection was made on.
@@ -159,29 +162,48 @@ size_t lmoe_workspace_size(const lmoe_handle* h, int T);
 lmoe_status lmoe_route(lmoe_handle* h, const uint16_t* x, int T, int32_t* idx, float* w, float* logits, void* ws,
                        lmoe_stream stream);
 
-/* Token permutation by group, then expert (groups of 64 experts share the
- * two large matrices, so tokens are gathered per group first). idx [T][k] ->
+/* Token permutation by group, then expert. Source: "Edge0-145B: Frontier AI
+ * Capabilities on Your Own Computer", section "Under the Hood of Edge0",
+ * paragraph "Architecture: share large matrices across sparse experts"
+ * (groups of 64 experts share two large matrices, so tokens are gathered per
+ * group first, then by expert). idx [T][k] ->
  * every array of *out (see lmoe_perm). Deterministic: bit-identical for
  * identical idx. Indices outside [0, E) set LMOE_ERR_DEVICE_CHECK. */
 lmoe_status lmoe_permute(lmoe_handle* h, const int32_t* idx, int T, const lmoe_perm* out, void* ws,
                          lmoe_stream stream);
 
-/* The latent expert FFN for routed tokens: for every (group g, token t) row
- * r of the permutation,
+/* The latent expert FFN for routed tokens. Source: "Edge0-145B: Frontier AI
+ * Capabilities on Your Own Computer", section "Under the Hood of Edge0",
+ * paragraph "Architecture: share large matrices across sparse experts" (two
+ * large matrices shared by a group of 64 experts, a small set of parameters
+ * per expert), and "Edge0-145B: Run a 145B Open-Source Model on Your Laptop",
+ * section "The Three Pillars That Make It Fast" (int4 expert tensors; the
+ * Recover-LoRA branch beside the frozen 4-bit base). For every (group g,
+ * token t) row r of the permutation,
  *   Y[r] = Wout[g] ( sum_{j: g(idx[t][j]) = g} w[t][j] * u_{idx[t][j]}( Win[g] x_t ) )  (+ LoRA)
  * x [T][d] bf16, idx/w [T][k], perm from lmoe_permute on the same idx,
  * Y [rows][d] fp32 with rows = group_tok_offsets[G] (capacity T*min(G,k)). */
 lmoe_status lmoe_expert_forward(lmoe_handle* h, const uint16_t* x, int T, const int32_t* idx, const float* w,
                                 const lmoe_perm* perm, float* Y, void* ws, lmoe_stream stream);
 
-/* Weighted un-permute and combine: y_t = sum over the groups of t, in
+/* Weighted un-permute and combine. Source: the same "Architecture: share
+ * large matrices across sparse experts" paragraph (the experts of a token
+ * contribute through their groups' shared output matrices, so the weighted
+ * expert outputs are summed per group before the shared up-projection and
+ * the group results are summed per token). y_t = sum over the groups of t, in
  * ascending group order, of Y[row(g, t)] (+ residual_t), rounded once to
  * bf16. Y as produced by lmoe_expert_forward; residual [T][d] bf16 or NULL. */
 lmoe_status lmoe_combine(lmoe_handle* h, const float* Y, const int32_t* idx, const lmoe_perm* perm, int T,
                          const uint16_t* residual, uint16_t* y, lmoe_stream stream);
 
-/* The whole layer: y = bf16(layer(x) (+ residual)). x, residual (nullable)
- * and y are [T][d] bf16; y may alias residual but not x. */
+/* The whole layer: y = bf16(layer(x) (+ residual)). Sources: every passage
+ * cited above -- router and top-k ("Not Compression -- Architecture"), the
+ * group-shared latent FFN and its combine ("Architecture: share large
+ * matrices across sparse experts"), int4 tensors and Recover-LoRA ("The
+ * Three Pillars That Make It Fast"). x, residual (nullable) and y are [T][d]
+ * bf16; y may alias residual but not x. T <= decode_max_T (default 16) runs
+ * the decode path in passes of at most 16 tokens, larger T the prefill path
+ * (unless force_path says otherwise). */
 lmoe_status lmoe_layer_forward(lmoe_handle* h, const uint16_t* x, int T, const uint16_t* residual, uint16_t* y,
                                void* ws, lmoe_stream stream);
 
@@ -197,16 +219,19 @@ lmoe_status lmoe_layer_forward(lmoe_handle* h, const uint16_t* x, int T, const u
  * this library; the layer's description has no counterpart.
  *
  * It computes exactly what lmoe_layer_forward computes on the decode path
- * (one pass of at most LMOE_NOALLOC_MAX_T tokens), with its scratch in one
+ * (one pass of at most LMOE_NOALLOC_MAX_T tokens, bit for bit the same
+ * result), and it always takes the decode path: the handle's force_path and
+ * decode_max_T are ignored here. Its scratch lives in one
  * fixed LMOE_NOALLOC_SCRATCH_BYTES array per device that is part of the
  * library's device image. Nothing is allocated by the call, by CUDA or by
  * anything else. x, residual (nullable) and y are [T][d] bf16 device
  * pointers as for lmoe_layer_forward, 16-byte aligned; y may alias residual
  * but not x.
  *
- * The first call on a device looks up that array's address (once per device,
- * with the handle's device current); make that first call outside any stream
- * capture. All calls on a device share the one array and it keeps the last
+ * The first call on a device (and the first call after that device's
+ * primary context was destroyed and made again, e.g. by cudaDeviceReset)
+ * looks up that array's address, with the handle's device current; make that
+ * first call outside any stream capture. All calls on a device share the one array and it keeps the last
  * call's contents; no word of it needs to start at zero, because every word a
  * call reads it has first written. Calls whose work overlaps on the GPU (two
  * streams, two handles on one device) race on the array and give undefined
@@ -219,6 +244,19 @@ lmoe_status lmoe_layer_forward(lmoe_handle* h, const uint16_t* x, int T, const u
  * T, LMOE_ERR_ALIGNMENT and LMOE_ERR_CUDA as lmoe_layer_forward does. */
 lmoe_status lmoe_layer_forward_noalloc(lmoe_handle* h, const uint16_t* x, int T, const uint16_t* residual,
                                        uint16_t* y, lmoe_stream stream);
+
+/* The routing a decode-path pass used, read back from its workspace: after
+ * lmoe_layer_forward with 1 <= T <= 16 tokens on the decode path (either
+ * decode kernel sequence) with workspace ws, copies that call's expert
+ * indices idx [T][k], weights w [T][k] and, if logits != NULL, router logits
+ * [T][E] (fp32, the values the selection was made on) from ws into the
+ * caller's device buffers, on `stream`. It exists so that the selection made
+ * inside the single-kernel pass can be compared index for index with a
+ * reference; it has no counterpart on the pages. Valid only until the next
+ * call that uses ws. LMOE_ERR_INVALID_ARG for T outside [0, 16] or null
+ * pointers. */
+lmoe_status lmoe_decode_routing(lmoe_handle* h, const void* ws, int T, int32_t* idx, float* w, float* logits,
+                                lmoe_stream stream);
 
 /* The whole layer from and to HOST memory: copies x (and residual) from
  * host to the workspace, runs lmoe_layer_forward, copies y back and waits

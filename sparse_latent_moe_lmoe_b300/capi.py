@@ -22,7 +22,7 @@ EXPORTS = ("lmoe_status_string", "lmoe_version", "lmoe_create", "lmoe_destroy", 
            "lmoe_permute", "lmoe_expert_forward", "lmoe_combine", "lmoe_layer_forward", "lmoe_layer_forward_noalloc",
            "lmoe_layer_forward_host", "lmoe_stack_forward", "lmoe_stack_workspace_size",
            "lmoe_host_staging_size", "lmoe_check", "lmoe_set_timeout", "lmoe_set_stage_events", "lmoe_stage_name",
-           "lmoe_launch_count")
+           "lmoe_launch_count", "lmoe_decode_routing")
 
 
 class LmoeError(RuntimeError):
@@ -82,6 +82,7 @@ def _load():
         "lmoe_set_stage_events": ([P, P, I], S),
         "lmoe_stage_name": ([P, I, I, ctypes.POINTER(I)], ctypes.c_char_p),
         "lmoe_launch_count": ([P, I], I),
+        "lmoe_decode_routing": ([P, P, I, P, P, P, P], S),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -182,6 +183,10 @@ def lmoe_check(h, stream) -> None:
 def lmoe_check_status(h, stream) -> int:
     """lmoe_check's raw status (no exception)."""
     return _lib.lmoe_check(h, stream)
+
+
+def lmoe_decode_routing(h, ws, T, idx, w, logits, stream) -> None:
+    _ok(_lib.lmoe_decode_routing(h, ws, int(T), idx, w, logits, stream), "lmoe_decode_routing")
 
 
 def lmoe_set_timeout(h, cycles: int) -> None:

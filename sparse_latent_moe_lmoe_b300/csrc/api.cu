@@ -1,6 +1,7 @@
 // The C ABI of the latent MoE layer (declared in include/lmoe.h): host-side
 // validation, the handle, the workspace layout and the dispatch to the
 // decode-path and prefill-path kernels.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -310,10 +311,42 @@ PrefillArgs prefill_args(const lmoe_handle* h) {
   return P;
 }
 
-// Scratch of lmoe_layer_forward_noalloc, looked up once per device.
+// Scratch of lmoe_layer_forward_noalloc, looked up once per device and
+// primary context: the address is cached together with the context it
+// belongs to, so a context made anew (after cudaDeviceReset) is looked up
+// again instead of being handed a stale address.
 constexpr int kNoAllocMaxDevices = 64;
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+unsigned long long g_noalloc_ctx[kNoAllocMaxDevices] = {};
+
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+// Identifier of the current context (0 if the driver cannot say).
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_cur = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static bool looked = false;
+  if (!looked) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+    cudaGetLastError();
+    looked = true;
+  }
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_cur || get_cur(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (!get_id || get_id(ctx, &id) != CUDA_SUCCESS) return (unsigned long long)(uintptr_t)ctx;
+  return id + 1;  // never 0
+}
 
 }  // namespace
 
@@ -326,11 +359,19 @@ namespace {
 // Device address of the scratch array on `device`, which must be current.
 lmoe_status noalloc_scratch(int device, void** out) {
   if (device < 0 || device >= kNoAllocMaxDevices) return LMOE_ERR_UNSUPPORTED;
+  // the runtime makes the primary context on first use; this call only looks
+  // it up (cudaFree(0) would be the usual way to force it, but this entry
+  // point calls no allocation routine at all)
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[device]) {
+  if (!g_noalloc_ptr[device] || g_noalloc_ctx[device] != ctx || ctx == 0) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, lmoe_noalloc_scratch) != cudaSuccess || !p) return LMOE_ERR_CUDA;
+    if (cudaGetSymbolAddress(&p, lmoe_noalloc_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return LMOE_ERR_CUDA;
+    }
     g_noalloc_ptr[device] = p;
+    g_noalloc_ctx[device] = current_context_id();
   }
   *out = g_noalloc_ptr[device];
   return LMOE_OK;
@@ -585,6 +626,27 @@ lmoe_status lmoe_layer_forward_noalloc(lmoe_handle* h, const uint16_t* x, int T,
   s = noalloc_scratch(h->device, &ws);
   if (s != LMOE_OK) return s;
   return decode_layer(h, x, T, residual, y, ws, (cudaStream_t)stream);
+}
+
+lmoe_status lmoe_decode_routing(lmoe_handle* h, const void* ws, int T, int32_t* idx, float* w, float* logits,
+                                lmoe_stream stream) {
+  if (check_handle(h) != LMOE_OK || T < 0 || T > kMaxDecodeT) return LMOE_ERR_INVALID_ARG;
+  if (T == 0) return LMOE_OK;
+  if (!ws || !idx || !w) return LMOE_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return LMOE_ERR_ALIGNMENT;
+  lmoe_status s = pending_error();
+  if (s != LMOE_OK) return s;
+  DeviceGuard guard(h->device);
+  cudaStream_t st = (cudaStream_t)stream;
+  const lmoe_config& c = h->cfg;
+  const DecodeWs m = decode_ws(c, 0);
+  const char* b = reinterpret_cast<const char*>(ws);
+  if (cudaMemcpyAsync(idx, b + m.idx, (size_t)T * c.k * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(w, b + m.w, (size_t)T * c.k * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  if (logits && cudaMemcpyAsync(logits, b + m.logits, (size_t)T * c.E * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  return LMOE_OK;
 }
 
 size_t lmoe_stack_workspace_size(const lmoe_handle* h, int T) {

@@ -1,14 +1,14 @@
-// A shared-memory weight ring for the decode path: one producer warp streams
-// the CTA's weight chunks (row segments of packed int4 plus their bf16
-// scales, or fp32 rows) into fixed slots with 16-byte asynchronous copies,
-// far ahead of the warps that consume them; each slot is handed over with an
-// mbarrier pair (full: one arrival per producer lane once its copies have
-// landed; empty: one arrival by the consuming warp).
+// A shared-memory weight ring for the decode path: one producer thread
+// streams the CTA's weight chunks into fixed slots with TMA tensor copies
+// (cp.async.bulk.tensor, completing on the slot's "full" mbarrier with a
+// transaction count), far ahead of the warps that consume them; a consuming
+// warp hands the slot back through its "empty" mbarrier.
 //
-// Slot layout for an int4 chunk of R rows x Kseg elements: weight rows at a
-// padded stride RS = Kseg/2 + 64 bytes (a stride of 64 mod 128 bytes makes the
-// 16-byte fragment loads of rows gid and gid+1 fall in different banks), then
-// the scales, [R][Kseg/32] bf16.
+// An int4 chunk in a slot is a TMA box in 128-byte swizzle: row r of the
+// chunk is LPR 128-byte lines (line i = r*LPR + k/256 for element k), and
+// 16-byte unit j of line i sits at unit j ^ (i & 7), so the 16-byte loads of
+// the 8 rows a warp reads at once fall in different banks. The chunk's bf16
+// scales, [rows][K/32], follow it in the slot as a second, unswizzled box.
 #pragma once
 #include "common.cuh"
 

@@ -128,6 +128,17 @@ class LatentMoE:
                                 _stream(stream))
         return y
 
+    def last_decode_routing(self, T: int, stream=None):
+        """(idx, w, logits) that the last decode-path forward of T <= 16 tokens
+        on this layer's workspace selected (lmoe_decode_routing)."""
+        sh = self.shape
+        idx = torch.empty((T, sh.k), dtype=torch.int32, device=self.device)
+        w = torch.empty((T, sh.k), dtype=torch.float32, device=self.device)
+        logits = torch.empty((T, sh.E), dtype=torch.float32, device=self.device)
+        capi.lmoe_decode_routing(self.h, _ptr(self.workspace(T)), T, _ptr(idx), _ptr(w), _ptr(logits),
+                                 _stream(stream))
+        return idx, w, logits
+
     def forward_noalloc(self, x: torch.Tensor, residual=None, out=None, stream=None) -> torch.Tensor:
         """The layer for T <= 16 tokens with the library's fixed per-device
         scratch instead of a workspace (lmoe_layer_forward_noalloc): the C call

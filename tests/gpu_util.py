@@ -75,6 +75,28 @@ def output_errors(y_gpu_bits: np.ndarray, y_ref: np.ndarray):
     return mean_rel, max_abs, mean_rel_unrounded
 
 
+# Element-wise bound on fp32 rows of the expert FFN (Y[(g, t)] against the
+# oracle's group row): every element within ROW_RTOL of its own row's largest
+# magnitude. The GPU keeps H, V and Z in fp16 (relative rounding <= 2^-11 per
+# element); the error each row reaches is a few times 2^-11 of the row's
+# scale, so a wrong or misplaced row -- whose error is of the size of the row
+# itself -- cannot pass, whatever its magnitude.
+ROW_RTOL = 1e-2
+
+
+def check_rows(Y_gpu: np.ndarray, Y_ref: np.ndarray, what=""):
+    """Per-row max-abs check of fp32 rows; returns the largest relative
+    error seen (max over rows of max|dY| / max|Y_ref row|)."""
+    Y_gpu = np.asarray(Y_gpu, np.float64)
+    scale = np.abs(Y_ref).max(axis=1)
+    err = np.abs(Y_gpu - Y_ref).max(axis=1)
+    rel = err / np.maximum(scale, 1e-30)
+    worst = int(np.argmax(rel)) if rel.size else 0
+    assert np.all(err <= ROW_RTOL * scale + 1e-12), (
+        f"{what}: row {worst} max-abs error {err[worst]:.3e} > {ROW_RTOL} x row scale {scale[worst]:.3e}")
+    return float(rel.max()) if rel.size else 0.0
+
+
 def check_outputs(y_gpu_bits, y_ref, what=""):
     mr, ma, mru = output_errors(y_gpu_bits, y_ref)
     assert mr <= MEAN_REL, f"{what}: mean relative error {mr:.3e} > {MEAN_REL}"

@@ -34,6 +34,7 @@ def test_host_side_validation_without_gpu():
     assert lib.lmoe_layer_forward(None, None, 8, None, None, None, None) == 1
     assert lib.lmoe_layer_forward_noalloc(None, None, 8, None, None, None) == 1
     assert lib.lmoe_set_timeout(None, 5) == 1
+    assert lib.lmoe_decode_routing(None, None, 8, None, None, None, None) == 1
     assert lib.lmoe_check(None, None) == 1
     assert lib.lmoe_destroy(None) == 0
     h = ctypes.c_void_p()

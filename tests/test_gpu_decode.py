@@ -8,7 +8,7 @@ import torch
 
 import lmoe_synth as S
 import oracle as O
-from gpu_util import (bf16_bits, bf16_tensor, check_outputs, check_routing)
+from gpu_util import (W_RTOL, ambiguous_rows, bf16_bits, bf16_tensor, check_outputs, check_routing, check_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -126,6 +126,8 @@ def test_expert_forward_and_combine(name, T, cuda_device):
             ref_rows[r] = O.group_row(Ly, g, x[t], idx[t], w[t].astype(np.float64))
     err = np.abs(Yn[:rows] - ref_rows).sum() / np.abs(ref_rows).sum()
     assert err < 1e-3, err
+    worst = check_rows(Yn[:rows], ref_rows, f"{name} Y rows")
+    print(f"{name}: Y rows mean rel {err:.2e}, worst row max-abs / row scale {worst:.2e}")
     y = m.combine(Y, idx_t, perm, T)
     torch.cuda.synchronize()
     y_ref = O.combine(Yn[:max(rows, 1)], idx, ref_perm["assign_row"], sh.E, sh.G)
@@ -231,3 +233,35 @@ def test_fused_decode_ragged_T(T, cuda_device):
     keep = ~ambiguous_rows(lg_ref, sh.k, 1e-5 * np.abs(lg_ref).max(axis=1))
     mr, ma, _ = check_outputs(got[keep], y_ref[keep], f"fused T={T}")
     print(f"fused T={T}: mean rel {mr:.2e} max abs {ma:.2e}")
+
+
+def check_routing_exact(idx_g, w_g, lg_g, lg_ref, k):
+    """The routing a pass used against the oracle: logits within the logit bar
+    of the oracle's, and the selection equal to the oracle's top-k run on the
+    GPU's own fp32 logits -- indices bit for bit (ties included, since both
+    sides order the same fp32 values), weights within the weight bar."""
+    tol = 1e-5 * np.abs(lg_ref).max(axis=1)
+    err = np.abs(lg_g.astype(np.float64) - lg_ref).max(axis=1)
+    assert np.all(err <= tol), f"logit error {err.max():.3e}"
+    idx_own, w_own = O.topk(lg_g.astype(np.float64), k)
+    assert np.array_equal(idx_g, idx_own), np.nonzero((idx_g != idx_own).any(1))[0][:8]
+    assert np.allclose(w_g, w_own, rtol=W_RTOL, atol=1e-7), np.abs(w_g - w_own).max()
+
+
+@pytest.mark.parametrize("T", [1, 3, 8, 9, 16])
+@pytest.mark.parametrize("multi", [False, True])
+def test_decode_pass_routing_index_for_index(T, multi, cuda_device):
+    """The routing computed inside a decode pass (the single persistent
+    kernel's routing warps, or route_kernel in the multi-kernel sequence),
+    read back from the workspace after lmoe_layer_forward."""
+    from sparse_latent_moe_lmoe_b300 import LatentMoE, capi
+    sh, _, W, _x, Ly, _y, _i, _w, _l = workload("decode_t8")
+    x = S.make_x(T, sh.d, 60 + T)
+    lg_ref = O.router_logits(Ly, x)
+    m = LatentMoE(sh, W, device=0, flags=capi.FLAG_MULTI_KERNEL_DECODE if multi else 0)
+    assert (capi.lmoe_stage_name(m.h, T, 0)[0] == "decode_fused") == (not multi)
+    m.forward(bf16_tensor(x, cuda_device))
+    idx, w, lg = m.last_decode_routing(T)
+    torch.cuda.synchronize()
+    m.check()
+    check_routing_exact(idx.cpu().numpy(), w.cpu().numpy(), lg.cpu().numpy(), lg_ref, sh.k)

@@ -9,7 +9,7 @@ import torch
 
 import lmoe_synth as S
 import oracle as O
-from gpu_util import ambiguous_rows, bf16_bits, bf16_tensor, check_outputs, check_routing
+from gpu_util import ambiguous_rows, bf16_bits, bf16_tensor, check_outputs, check_routing, check_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -74,6 +74,8 @@ def test_small_expert_forward_prefill(cuda_device):
             ref[r] = O.group_row(Ly, g, x[t], idx[t], w[t].astype(np.float64))
     err = np.abs(Yn[:rows] - ref).sum() / np.abs(ref).sum()
     assert err < 1e-3, err
+    worst = check_rows(Yn[:rows], ref, "small prefill Y rows")
+    print(f"small prefill Y rows: mean rel {err:.2e}, worst row max-abs / row scale {worst:.2e}")
 
 
 _big = {}

@@ -92,3 +92,39 @@ def test_stack_rejects_mismatched_shapes(cuda_device):
     st = capi.library().lmoe_stack_forward(carr, 2, ctypes.c_void_p(x.data_ptr()), 4, ctypes.c_void_p(x.data_ptr()),
                                            ctypes.c_void_p(ws.data_ptr()), None)
     assert st == 1
+
+
+def test_stack_edge0_48_layers_t1(cuda_device):
+    """The full 48-layer Edge0 stack at one token, every layer checked against
+    the oracle teacher-forced. Layers are built, run and checked one at a time
+    (only their device copies are kept), then the whole stack in one
+    lmoe_stack_forward call must equal that chain bit for bit."""
+    from sparse_latent_moe_lmoe_b300 import LatentMoE, LatentMoEStack
+    shape, n, T = S.EDGE0, 48, 1
+    x = S.make_x(T, shape.d, 9)
+    cur_bits = x
+    layers, flips = [], 0
+    for l in range(n):
+        W = S.make_stack_layer(shape, l)
+        m = LatentMoE(shape, W, device=0)
+        layers.append(m)
+        y = m.forward(bf16_tensor(cur_bits, cuda_device))
+        m.check()
+        y_bits = bf16_bits(y)
+        y_ref, idx_ref, w_ref, lg_ref = O.layer_forward(O.Layer(shape, W), cur_bits)
+        del W
+        keep = ~ambiguous_rows(lg_ref, shape.k, 1e-5 * np.abs(lg_ref).max(axis=1))
+        flips += int((~keep).sum())
+        if keep.any():
+            check_outputs(y_bits[keep], y_ref[keep], f"48-layer stack, layer {l}")
+        nxt = O.residual(cur_bits, O.bf16_value(y_bits))
+        # the GPU's own residual rule gives the same bits (checked through the stack below)
+        cur_bits = nxt
+    stack = LatentMoEStack(layers)
+    y_stack = bf16_bits(stack.forward(bf16_tensor(x, cuda_device)))
+    for m in layers:
+        m.check()
+    assert np.array_equal(y_stack, cur_bits), "48-layer stack differs from the chain of layer calls"
+    print(f"48-layer stack at T=1: every layer within the bars, {flips} near-tie layers excluded")
+    for m in layers:
+        m.close()

@@ -30,8 +30,14 @@ def _close(a_bits, b_bits):
     assert np.abs(a - b).max() <= MAX_ABS
 
 
-@pytest.mark.parametrize("workload,with_residual", [("decode_t8", False), ("decode_t8", True), ("tiny_t64", False)])
+@pytest.mark.parametrize("workload,with_residual", [("decode_t8", False), ("decode_t8", True), ("tiny_t64", False),
+                                                    ("lora_t16", False)])
 def test_noalloc_matches_workspace_entry_point(cuda_device, workload, with_residual):
+    """Both entry points run the same decode kernels on the same inputs, and
+    those kernels are deterministic: the outputs must agree bit for bit (the
+    tolerance check is kept as a second, weaker statement). lora_t16 takes the
+    multi-kernel sequence, whose LoRA projections use their own regions of the
+    scratch. The second call must not change the device's free memory."""
     from sparse_latent_moe_lmoe_b300 import LatentMoE, capi
     sh, T, W, x = S.make_workload(workload)
     T = min(T, capi.NOALLOC_MAX_T)
@@ -41,15 +47,21 @@ def test_noalloc_matches_workspace_entry_point(cuda_device, workload, with_resid
     res = bf16_tensor(S.make_x(T, sh.d, 77), cuda_device) if with_residual else None
     y_ref = bf16_bits(m.forward(xt, residual=res))
     m.check()
+    ys = [torch.empty((T, sh.d), dtype=torch.bfloat16, device=cuda_device) for _ in range(2)]
     outs = []
-    for _ in range(2):
-        y = torch.empty((T, sh.d), dtype=torch.bfloat16, device=cuda_device)
-        capi.lmoe_layer_forward_noalloc(m.h, _p(xt), T, _p(res), _p(y), _stream())
+    for i in range(2):
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
+        capi.lmoe_layer_forward_noalloc(m.h, _p(xt), T, _p(res), _p(ys[i]), _stream())
         m.check()
-        outs.append(bf16_bits(y))
+        free1 = torch.cuda.mem_get_info()[0]
+        if i == 1:
+            assert free1 == free0, f"free device memory changed by {free0 - free1} bytes"
+        outs.append(bf16_bits(ys[i]))
     for o in outs:
+        assert np.array_equal(o, y_ref), "no-alloc result differs from the workspace entry point"
         _close(o, y_ref)
-    _close(outs[1], outs[0])
+    assert np.array_equal(outs[1], outs[0])
     m.close()
 
 
