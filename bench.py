@@ -40,6 +40,8 @@ def parse():
     ap.add_argument("--copies", type=int, default=0, help="device weight copies rotated across steps (0: auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="decode_t8 only: skip the 16K-prefill sub-record")
+    ap.add_argument("--sweep", action="store_true",
+                    help="decode / speculative-verify sweep: one JSON line per batch T = 1..16 of the Edge0 layer")
     return ap.parse_args()
 
 
@@ -149,12 +151,26 @@ def stage_bytes(sh, T, idx):
     b["wout"] = len(groups) * sh.d * sh.L * wq + 2 * T * sh.d
     b["decode_fused"] = sum(b.values())
     if sh.lora_rank:
+        # the LoRA matrices of the routed groups; in the single-kernel pass the
+        # branch runs in its own kernels (lora_in: A_in, B_in; lora_q: A_out;
+        # lora_out: B_out), in the multi-kernel sequence beside W_in / W_out
         r = sh.lora_rank
-        b["lora_p"] = len(groups) * sh.d * r * 2
-        b["win"] += len(groups) * r * sh.L * 2
+        b["lora_in"] = len(groups) * (sh.d * r + r * sh.L) * 2 + 2 * T * sh.d
         b["lora_q"] = len(groups) * sh.L * r * 2
-        b["wout"] += len(groups) * r * sh.d * 2
+        b["lora_out"] = len(groups) * r * sh.d * 2 + 2 * T * sh.d
+        b["lora_p"] = len(groups) * sh.d * r * 2
+        b["win_lora"] = len(groups) * r * sh.L * 2
+        b["wout_lora"] = len(groups) * r * sh.d * 2
     return b
+
+
+def step_bytes(sb):
+    """Algorithmic bytes of one pass from stage_bytes: the layer's own stages
+    plus, with LoRA, the branch's matrices counted once."""
+    base = sum(sb[n] for n in ("route", "win", "gateup", "down", "wout"))
+    if "lora_in" in sb:
+        base += sb["lora_p"] + sb["win_lora"] + sb["lora_q"] + sb["wout_lora"]
+    return base
 
 
 def stage_flops(sh, T, idx):
@@ -173,6 +189,7 @@ def stage_flops(sh, T, idx):
     f["permute"] = 0.0
     f["zreduce"] = 0.0
     f["dequant"] = 0.0
+    f["tsort"] = 0.0
     return f, rows
 
 
@@ -417,7 +434,7 @@ def measure_layer(args, workload, local, dev, dist, world, steps, warmup, copies
                              "group_token_rows": rows}}
     else:
         achieved = sb.get(dom, 0.0) / (per[dom] * 1e-3) / 1e9
-        total_bytes = sum(v for n, v in sb.items() if n != "decode_fused")
+        total_bytes = step_bytes(sb)
         roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
                     "frac": achieved / hbm, "traffic": read_traffic(dom, workload), "peak_source": peak_src,
                     "bytes_per_launch": sb.get(dom, 0.0), "timing": stage_timing,
@@ -521,7 +538,7 @@ def run_stack(args):
         idx, _, _ = m.route(cur)
         idx_np = idx.cpu().numpy()
         sb = stage_bytes(sh, T, idx_np)
-        total_bytes += sum(v for n, v in sb.items() if n != "decode_fused")
+        total_bytes += step_bytes(sb)
         int4_bytes += sum(v for n, v in sb.items() if n in ("win", "gateup", "down", "wout")) - 4 * T * sh.d
         sf, _ = stage_flops(sh, T, idx_np)
         total_flops += sum(sf.values())
@@ -615,11 +632,70 @@ def run_stack(args):
         dist.destroy_process_group()
 
 
+def run_sweep(args):
+    """Tokens/s and HBM roofline fraction of the decode path at T = 1..16
+    (speculative decoding verifies several candidate tokens per weight read):
+    one JSON line per T, device time of K graph replays over 8 rotating weight
+    copies, the same input recipe as decode_t8 (x drawn for each T)."""
+    import numpy as np
+    import torch
+
+    import lmoe_synth as S
+    from sparse_latent_moe_lmoe_b300 import LatentMoE, capi
+    from sparse_latent_moe_lmoe_b300.layer import to_device
+
+    rank, local, world = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sh, _, W, _ = S.make_workload("decode_t8")
+    base = {n: to_device(W.get(n), dev) for n in capi.WEIGHT_FIELDS}
+    copies = [base] + [{n: (None if t is None else t.clone()) for n, t in base.items()} for _ in range(7)]
+    layers = [LatentMoE(sh, c, device=local) for c in copies]
+    hbm = measured_peaks()[0]
+    stream = torch.cuda.current_stream()
+    cap = torch.cuda.Stream()
+    for T in range(1, 17):
+        x = S.make_x(T, sh.d, 100 + T)
+        xt = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+        y = torch.empty_like(xt)
+        for m in layers:
+            m.forward(xt, out=y)
+        idx, _, _ = layers[0].route(xt)
+        sb = stage_bytes(sh, T, idx.cpu().numpy())
+        total = step_bytes(sb)
+        torch.cuda.synchronize()
+        graphs = []
+        for m in layers:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                m.forward(xt, out=y)
+            graphs.append(g)
+        for i in range(max(args.warmup, 3)):
+            graphs[i % 8].replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            graphs[i % 8].replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        line = {"mode": "sweep", "workload": f"Edge0 layer, decode T={T}", "T": T, "tokens_per_s": T / (ms * 1e-3),
+                "us_per_step": 1000 * ms, "bytes_per_step": total, "achieved_gbs": total / (ms * 1e-3) / 1e9,
+                "hbm_frac": total / (ms * 1e-3) / 1e9 / hbm, "distinct_experts": int(len(np.unique(idx.cpu().numpy()))),
+                "kernel": capi.lmoe_stage_name(layers[0].h, T, 0)[0], "steps": args.steps}
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        del graphs
+
+
 def main():
     args = parse()
     import lmoe_synth as S
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
     elif args.workload in S.STACK_WORKLOADS:
         run_stack(args)
     else:

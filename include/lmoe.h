@@ -274,8 +274,15 @@ size_t lmoe_host_staging_size(const lmoe_handle* h, int T);
  * l = 0 .. n_layers-1, y = x_{n_layers}. layers[l] are handles of the same
  * shape (d, E, G, k, L, f, lora_rank) on the same device, each with its own
  * weights; x and y are [T][d] bf16 device pointers (y may alias x). Each
- * layer runs exactly as lmoe_layer_forward without a residual; the residual
- * step is a separate kernel that rounds the sum once. ws must hold
+ * layer computes exactly what lmoe_layer_forward computes. When every layer
+ * takes the single-kernel decode pass (T <= 16), each layer is one launch:
+ * the kernel rounds its output to bf16 and adds the residual in its final
+ * combine, runs as a programmatic dependent of the previous layer's launch
+ * (its weight stream starts while that layer finishes; x is read after it
+ * completes), and prefetches the next layer's router rows and W_in tiles
+ * into L2 during its own tail. Otherwise each layer runs as
+ * lmoe_layer_forward without a residual, followed by a kernel that adds the
+ * residual and rounds once. The two give the same bits. ws must hold
  * lmoe_stack_workspace_size(layers[0], T) bytes. Returns LMOE_ERR_INVALID_ARG
  * for n_layers < 1, a null handle or mismatched shapes or devices, and the
  * errors of lmoe_layer_forward. */

@@ -30,6 +30,10 @@ struct lmoe_handle {
   bool maps_ok;
   unsigned* d_ctr;                   // its arrival counters (two copies)
   unsigned long long* d_launches;    // its launch counter
+  cudaStream_t aux;                  // second stream of the prefill path (fork / join by events)
+  cudaEvent_t ev_fork, ev_join;
+  uint8_t* d_dsl_q;                  // its slice-major copy of Down: [E][f/32][L][16 B] packed int4
+  uint16_t* d_dsl_s;                 // and the matching scales [E][f/32][L]
   std::vector<cudaEvent_t> events;
 };
 
@@ -101,10 +105,11 @@ TicketMap ticket_map(const lmoe_config& c) {
 
 // ----------------------------------------------------------- workspace map
 struct DecodeWs {
-  size_t logits, idx, w, eo, sa, inv, go, gto, gt, ar, Hp, V, Z, Yp, Pin, Qout, Lp, H, Zp, Hf, Vf, Zf, perm_scratch, end;
+  size_t logits, idx, w, eo, sa, inv, go, gto, gt, ar, Hp, V, Z, Yp, Pin, Qout, Hf, Zf, Zpart, diag, perm_scratch, end;
 };
 
-DecodeWs decode_ws(const lmoe_config& c, int T) {
+// grid: CTAs of the single-kernel decode pass (sizes its Z partials)
+DecodeWs decode_ws(const lmoe_config& c, int T, int grid) {
   DecodeWs m;
   const int n = kMaxDecodeT;
   size_t o = 0;
@@ -131,12 +136,10 @@ DecodeWs decode_ws(const lmoe_config& c, int T) {
   m.Yp = take((size_t)c.G * n * c.d * 4);
   m.Pin = take((size_t)c.G * n * (c.lora_rank > 0 ? c.lora_rank : 1) * 4);
   m.Qout = take((size_t)c.G * n * (c.lora_rank > 0 ? c.lora_rank : 1) * 4);
-  m.Lp = take((size_t)(c.d / 128 + 1) * n * c.E * 4);
-  m.H = take((size_t)c.G * n * c.L * 4);
-  m.Zp = take((size_t)256 * n * c.L * 4);  // [routed-expert slot <= 256][16][L]
   m.Hf = take((size_t)c.G * c.L * 32);     // fp16 fragments, two token tiles: L/128 x 256 x 16 B
-  m.Vf = take((size_t)256 * c.f * 32);
   m.Zf = take((size_t)c.G * c.L * 32);
+  m.Zpart = take(fused_zpart_bytes(c.G, c.L, grid > 0 ? grid : 1));
+  m.diag = take(fused_diag_bytes(grid > 0 ? grid : 1));
   m.perm_scratch = take(permute_scratch_bytes(T > n ? T : n, c.E, c.G));
   m.end = o;
   return m;
@@ -165,7 +168,7 @@ DecodeArgs base_args(const lmoe_handle* h, void* ws) {
   A.gate_q = h->w.gate_q; A.gate_s = h->w.gate_s; A.up_q = h->w.up_q; A.up_s = h->w.up_s;
   A.down_q = h->w.down_q; A.down_s = h->w.down_s;
   A.A_in = h->w.A_in; A.B_in = h->w.B_in; A.A_out = h->w.A_out; A.B_out = h->w.B_out;
-  const DecodeWs m = decode_ws(c, 0);
+  const DecodeWs m = decode_ws(c, 0, h->num_sms);
   char* b = reinterpret_cast<char*>(ws);
   A.idx = reinterpret_cast<int32_t*>(b + m.idx);
   A.w = reinterpret_cast<float*>(b + m.w);
@@ -188,7 +191,7 @@ DecodeArgs base_args(const lmoe_handle* h, void* ws) {
 }
 
 float* ws_logits(const lmoe_handle* h, void* ws) {
-  return reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + decode_ws(h->cfg, 0).logits);
+  return reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + decode_ws(h->cfg, 0, h->num_sms).logits);
 }
 
 // Records an event; inside a stream capture the record becomes an external
@@ -232,7 +235,7 @@ struct DeviceGuard {
 
 bool use_fused(const lmoe_handle* h, const DecodeArgs& A) {
   return !(h->cfg.flags & LMOE_FLAG_MULTI_KERNEL_DECODE) && h->fused_grid > 0 && h->maps_ok &&
-         fused_decode_supported(A);
+         fused_decode_supported(A, h->fused_grid);
 }
 
 bool use_fused(const lmoe_handle* h, const DecodeArgs& A);
@@ -242,15 +245,14 @@ FusedArgs fused_args(const lmoe_handle* h, const DecodeArgs& A, void* ws) {
   memset(&F, 0, sizeof(F));
   F.A = A;
   F.maps = h->maps;
-  const DecodeWs m = decode_ws(h->cfg, 0);
+  const DecodeWs m = decode_ws(h->cfg, 0, h->num_sms);
   char* b = reinterpret_cast<char*>(ws);
-  F.Lp = reinterpret_cast<float*>(b + m.Lp);
   F.logits = reinterpret_cast<float*>(b + m.logits);
-  F.H = reinterpret_cast<float*>(b + m.H);
-  F.Zp = reinterpret_cast<float*>(b + m.Zp);
   F.Hf = reinterpret_cast<uint4*>(b + m.Hf);
-  F.Vf = reinterpret_cast<uint4*>(b + m.Vf);
   F.Zf = reinterpret_cast<uint4*>(b + m.Zf);
+  F.Zpart = reinterpret_cast<float*>(b + m.Zpart);
+  F.Yp = reinterpret_cast<float*>(b + m.Yp);
+  F.diag = reinterpret_cast<unsigned long long*>(b + m.diag);
   F.ctr = h->d_ctr;
   F.launches = h->d_launches;
   F.timeout = h->timeout;
@@ -271,10 +273,32 @@ lmoe_status decode_layer(lmoe_handle* h, const uint16_t* x, int T, const uint16_
     A.y = y + (size_t)t0 * c.d;
     if (use_fused(h, A)) {
       FusedArgs F = fused_args(h, A, ws);
+      cudaError_t e;
+      if (A.r > 0) {  // the LoRA branch: lora_in before, lora_q and lora_out after
+        // scratch of the multi-kernel sequence, unused by the single kernel:
+        // Ppart in Hp, P in Pin, Hl in V, Z in fp32 in Z, Q in Qout
+        F.hl = A.V;
+        F.zlin = A.Z;
+        F.no_combine = 1;
+        hook.before(st);
+        e = launch_lora_in(A, A.Hp, A.Pin, A.V, h->d_tickets + 1 + (c.d + 63) / 64, st);
+        hook.after(st);
+        if (e != cudaSuccess) return LMOE_ERR_CUDA;
+      }
       hook.before(st);
-      cudaError_t e = launch_decode_fused(F, h->fused_grid, st);
+      e = launch_decode_fused(F, h->fused_grid, st);
       hook.after(st);
       if (e != cudaSuccess) return LMOE_ERR_CUDA;
+      if (A.r > 0) {
+        hook.before(st);
+        e = launch_lora_q(A, A.Z, A.Qout, st);
+        hook.after(st);
+        if (e != cudaSuccess) return LMOE_ERR_CUDA;
+        hook.before(st);
+        e = launch_lora_out(A, F.Yp, A.Qout, st);
+        hook.after(st);
+        if (e != cudaSuccess) return LMOE_ERR_CUDA;
+      }
       continue;
     }
     hook.before(st);
@@ -308,6 +332,9 @@ PrefillArgs prefill_args(const lmoe_handle* h) {
   P.err = h->d_err;
   P.num_sms = h->num_sms;
   P.timeout = h->timeout;
+  P.aux = h->aux;
+  P.ev_fork = h->ev_fork;
+  P.ev_join = h->ev_join;
   return P;
 }
 
@@ -435,6 +462,7 @@ lmoe_status lmoe_create(lmoe_handle** out, const lmoe_config* cfg, const lmoe_we
     return LMOE_ERR_NO_MEMORY;
   }
   if (decode_set_attributes() != cudaSuccess || permute_set_attributes() != cudaSuccess ||
+      lora_set_attributes() != cudaSuccess ||
       fused_set_attributes() != cudaSuccess || prefill_set_attributes() != cudaSuccess) {
     lmoe_destroy(h);
     return LMOE_ERR_CUDA;
@@ -452,7 +480,28 @@ lmoe_status lmoe_create(lmoe_handle** out, const lmoe_config* cfg, const lmoe_we
     cudaMemset(h->d_launches, 0, sizeof(unsigned long long));
     DecodeArgs probe = base_args(h, nullptr);
     probe.T = 1;
-    h->maps_ok = fused_decode_supported(probe) && fused_make_maps(probe, &h->maps);
+    h->maps_ok = false;
+    if (h->fused_grid > 0 && fused_decode_supported(probe, h->fused_grid)) {
+      const size_t nq = (size_t)cfg->E * cfg->L * cfg->f / 2, nb = fused_down_copy_bytes(cfg->E, cfg->L, cfg->f);
+      if (cudaMalloc(&h->d_dsl_q, nq) != cudaSuccess || cudaMalloc(&h->d_dsl_s, nb - nq) != cudaSuccess) {
+        cudaGetLastError();
+        lmoe_destroy(h);
+        return LMOE_ERR_NO_MEMORY;
+      }
+      if (launch_repack_down(h->w.down_q, h->w.down_s, cfg->E, cfg->L, cfg->f, h->d_dsl_q, h->d_dsl_s, 0) !=
+          cudaSuccess) {
+        lmoe_destroy(h);
+        return LMOE_ERR_CUDA;
+      }
+      h->maps_ok = fused_make_maps(probe, h->d_dsl_q, h->d_dsl_s, &h->maps);
+    }
+  }
+  if (cudaStreamCreateWithFlags(&h->aux, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    lmoe_destroy(h);
+    return LMOE_ERR_CUDA;
   }
   if (launch_split_router(h->w.W_r, cfg->E, cfg->d, h->d_wr_split, 0) != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess) {
@@ -472,13 +521,18 @@ lmoe_status lmoe_destroy(lmoe_handle* h) {
   if (h->d_wr_split) cudaFree(h->d_wr_split);
   if (h->d_ctr) cudaFree(h->d_ctr);
   if (h->d_launches) cudaFree(h->d_launches);
+  if (h->d_dsl_q) cudaFree(h->d_dsl_q);
+  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+  if (h->ev_join) cudaEventDestroy(h->ev_join);
+  if (h->aux) cudaStreamDestroy(h->aux);
+  if (h->d_dsl_s) cudaFree(h->d_dsl_s);
   delete h;
   return pending_error();
 }
 
 size_t lmoe_workspace_size(const lmoe_handle* h, int T) {
   if (!h || T < 0) return 0;
-  size_t a = decode_ws(h->cfg, T).end;
+  size_t a = decode_ws(h->cfg, T, h->num_sms).end;
   size_t b = prefill_workspace_bytes(prefill_args(h), T);
   return a > b ? a : b;
 }
@@ -538,7 +592,7 @@ lmoe_status lmoe_permute(lmoe_handle* h, const int32_t* idx, int T, const lmoe_p
   lmoe_status s = pending_error();
   if (s != LMOE_OK) return s;
   DeviceGuard guard(h->device);
-  const DecodeWs m = decode_ws(h->cfg, T);
+  const DecodeWs m = decode_ws(h->cfg, T, h->num_sms);
   void* scratch = reinterpret_cast<char*>(ws) + m.perm_scratch;
   return cuda_status(launch_permute(idx, T, h->cfg.E, h->cfg.G, h->cfg.k, to_ptrs(out), scratch, h->d_err,
                                     (cudaStream_t)stream));
@@ -559,7 +613,7 @@ lmoe_status lmoe_expert_forward(lmoe_handle* h, const uint16_t* x, int T, const 
     PrefillArgs P = prefill_args(h);
     return cuda_status(launch_prefill_experts(P, x, T, idx, w, to_ptrs(perm), Y, nullptr, nullptr, ws, st));
   }
-  const DecodeWs m = decode_ws(c, T);
+  const DecodeWs m = decode_ws(c, T, h->num_sms);
   for (int t0 = 0; t0 < T; t0 += kMaxDecodeT) {
     DecodeArgs A = base_args(h, ws);
     A.T = T - t0 < kMaxDecodeT ? T - t0 : kMaxDecodeT;
@@ -618,7 +672,7 @@ lmoe_status lmoe_layer_forward_noalloc(lmoe_handle* h, const uint16_t* x, int T,
   if (T == 0) return LMOE_OK;
   if (!x || !y || x == y) return LMOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(y) || (residual && !aligned16(residual))) return LMOE_ERR_ALIGNMENT;
-  if (decode_ws(h->cfg, T).end > (size_t)LMOE_NOALLOC_SCRATCH_BYTES) return LMOE_ERR_UNSUPPORTED;
+  if (decode_ws(h->cfg, T, h->num_sms).end > (size_t)LMOE_NOALLOC_SCRATCH_BYTES) return LMOE_ERR_UNSUPPORTED;
   lmoe_status s = pending_error();
   if (s != LMOE_OK) return s;
   DeviceGuard guard(h->device);
@@ -639,7 +693,7 @@ lmoe_status lmoe_decode_routing(lmoe_handle* h, const void* ws, int T, int32_t* 
   DeviceGuard guard(h->device);
   cudaStream_t st = (cudaStream_t)stream;
   const lmoe_config& c = h->cfg;
-  const DecodeWs m = decode_ws(c, 0);
+  const DecodeWs m = decode_ws(c, 0, h->num_sms);
   const char* b = reinterpret_cast<const char*>(ws);
   if (cudaMemcpyAsync(idx, b + m.idx, (size_t)T * c.k * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess ||
       cudaMemcpyAsync(w, b + m.w, (size_t)T * c.k * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
@@ -684,6 +738,47 @@ lmoe_status lmoe_stack_forward(lmoe_handle* const* layers, int n_layers, const u
   cudaStream_t st = (cudaStream_t)stream;
   const size_t n = (size_t)T * c0.d;
   const uint16_t* xin = x;
+  // Decode-sized batches on the single-kernel path: one launch per layer (the
+  // residual rule is applied in the kernel's final combine), each layer a
+  // programmatic dependent of the one before it (its weight stream starts
+  // while the previous layer finishes), and each prefetching the next layer's
+  // router rows and W_in tiles into L2 during its own tail.
+  bool fused_all = T <= kMaxDecodeT && c0.lora_rank == 0;
+  for (int l = 0; fused_all && l < n_layers; ++l) {
+    DecodeArgs A = base_args(layers[l], ws);
+    A.T = T;
+    fused_all = !use_prefill(layers[l], T) && use_fused(layers[l], A);
+  }
+  if (fused_all) {
+    lmoe_status s = pending_error();
+    if (s != LMOE_OK) return s;
+    for (int l = 0; l < n_layers; ++l) {
+      lmoe_handle* h = layers[l];
+      uint16_t* xout = l == n_layers - 1 ? y : (l % 2 == 0 ? xbuf : ybuf);
+      DecodeArgs A = base_args(h, ws);
+      A.T = T;
+      A.x = xin;
+      A.residual = xin;
+      A.y = xout;
+      FusedArgs F = fused_args(h, A, ws);
+      F.round_first = 1;
+      F.pdl = l > 0 && layers[l - 1] != h;  // distinct handles: distinct counters
+      if (l + 1 < n_layers && layers[l + 1] != h) {
+        F.has_next = 1;
+        F.next_wr = layers[l + 1]->maps.wr;
+        F.next_win_q = layers[l + 1]->maps.win_q;
+        F.next_win_s = layers[l + 1]->maps.win_s;
+      }
+      EventHook hook;
+      hook.ev = h->events.empty() ? nullptr : &h->events;
+      hook.before(st);
+      const cudaError_t e = launch_decode_fused(F, h->fused_grid, st, F.pdl);
+      hook.after(st);
+      if (e != cudaSuccess) return LMOE_ERR_CUDA;
+      xin = xout;
+    }
+    return LMOE_OK;
+  }
   for (int l = 0; l < n_layers; ++l) {
     lmoe_status s = lmoe_layer_forward(layers[l], xin, T, nullptr, ybuf, ws, stream);
     if (s != LMOE_OK) return s;
@@ -756,9 +851,11 @@ const char* lmoe_stage_name(const lmoe_handle* h, int T, int i, int* count) {
   DecodeArgs probe = base_args(h, nullptr);
   probe.T = T < kMaxDecodeT ? T : kMaxDecodeT;
   if (T >= 1 && use_fused(h, probe)) {
-    const int passes = (T + kMaxDecodeT - 1) / kMaxDecodeT;
-    if (count) *count = passes;
-    return (i >= 0 && i < passes) ? "decode_fused" : "";
+    static const char* fl[] = {"lora_in", "decode_fused", "lora_q", "lora_out"};
+    const int passes = (T + kMaxDecodeT - 1) / kMaxDecodeT, per = lora ? 4 : 1;
+    if (count) *count = per * passes;
+    if (i < 0 || i >= per * passes) return "";
+    return lora ? fl[i % per] : "decode_fused";
   }
   const int per = lora ? 7 : 5;
   const int passes = (T + kMaxDecodeT - 1) / kMaxDecodeT;

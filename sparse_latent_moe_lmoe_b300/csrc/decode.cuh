@@ -64,12 +64,13 @@ struct DecodeArgs {
 // TMA descriptors of the weights for the single-kernel decode pass (made
 // once per handle). Packed int4 matrices are viewed as [rows][K/256][128 B]
 // (128-byte swizzle), their scales as [rows][K/32] bf16, W_r as
-// [E][d/256][256] fp32.
+// [E][d/256][256] fp32, and the slice-major copy of Down as 128-byte lines
+// ([E][f/32][L][16 B]) with scales [E][f/32][L].
 struct DecodeMaps {
   CUtensorMap wr;
   CUtensorMap win_q, win_s;
   CUtensorMap gate_q, gate_s, up_q, up_s;
-  CUtensorMap down_q, down_s;
+  CUtensorMap dsl_q, dsl_s;
   CUtensorMap wout_q, wout_s;
 };
 
@@ -77,24 +78,48 @@ struct DecodeMaps {
 struct FusedArgs {
   DecodeArgs A;
   DecodeMaps maps;
-  float* Lp;                     // [d/1024][16][E] router partial sums
   float* logits;                 // [16][E]
-  float* H;                      // [G][16][L] shared down-projection outputs
-  float* Zp;                     // [256][16][L] per-expert down-projection partials
   uint4* Hf;                     // [G][L/128][128 NT] H as fp16 fragments (NT = token tiles of the launch)
-  uint4* Vf;                     // [256][f/128][128 NT] weighted SwiGLU outputs as fragments
+  float* Zpart;                  // [grid + G][16][L] partial sums of Z, one per (CTA, group) it worked on
   uint4* Zf;                     // [G][L/128][128 NT] Z as fragments
+  float* Yp;                     // [G][16][d] per-group outputs of W_out
   unsigned* ctr;                 // arrival counters, two copies (fused_counter_words)
   unsigned long long* launches;  // launch counter (selects the counter copy)
   long long timeout;             // spin budget (clock64 cycles)
+  // layer stacks: y = bf16(residual + bf16(layer(x))) instead of one rounding
+  int round_first;
+  // layer stacks: launched as a programmatic dependent of the previous layer
+  // (the weight stream starts at once; x is read after griddepcontrol.wait)
+  int pdl;
+  // layer stacks: the next layer's router rows and W_in tiles of this CTA are
+  // prefetched into L2 once this layer's own weights are requested
+  int has_next;
+  CUtensorMap next_wr, next_win_q, next_win_s;
+  // the Recover-LoRA branch (lora.cu): Hl [G][16][L] is added to H; Z is also
+  // written in fp32 to Zlin [G][16][L]; the per-group outputs are left in Yp
+  // for lora_out to combine (no combine here)
+  const float* hl;
+  float* zlin;
+  int no_combine;
+  // diagnosis: [0] where the first timed-out wait of a launch gave up, then
+  // per CTA 16 %globaltimer stamps of its phases (a region of the workspace)
+  unsigned long long* diag;
 };
 size_t fused_counter_words(int d, int E, int G, int L);
+size_t fused_zpart_bytes(int G, int L, int grid);
+size_t fused_diag_bytes(int grid);
+// bytes of the slice-major copy of Down (packed int4 and scales)
+size_t fused_down_copy_bytes(int E, int L, int f);
+cudaError_t launch_repack_down(const uint8_t* q, const uint16_t* s, int E, int L, int f, uint8_t* qo, uint16_t* so,
+                               cudaStream_t st);
 // Encodes the tensor maps; false if the driver refuses one of them.
-bool fused_make_maps(const DecodeArgs& A, DecodeMaps* maps);
-bool fused_decode_supported(const DecodeArgs& A);
+bool fused_make_maps(const DecodeArgs& A, const uint8_t* dsl_q, const uint16_t* dsl_s, DecodeMaps* maps);
+bool fused_decode_supported(const DecodeArgs& A, int grid);
 cudaError_t fused_set_attributes();
 int fused_grid(int num_sms);
-cudaError_t launch_decode_fused(const FusedArgs& F, int grid, cudaStream_t st);
+// pdl != 0: a plain launch with programmatic stream serialization (layer
+// stacks, after another layer's pass); else a cooperative launch
+cudaError_t launch_decode_fused(const FusedArgs& F, int grid, cudaStream_t st, int pdl = 0);
 
 // Records timing events around each launch when attached.
 struct StageHook {
@@ -109,6 +134,12 @@ cudaError_t launch_route(const DecodeArgs& A, int do_perm, float* logits_out, cu
 cudaError_t launch_lora_proj(const DecodeArgs& A, int which, cudaStream_t st);
 cudaError_t launch_experts(const DecodeArgs& A, int mode, cudaStream_t st, StageHook* hook);
 // out = bf16(x + y), n a multiple of 8 (the residual step of a layer stack)
+// The Recover-LoRA branch around the single-kernel decode pass (lora.cu).
+cudaError_t lora_set_attributes();
+bool lora_fused_supported(const DecodeArgs& A);
+cudaError_t launch_lora_in(const DecodeArgs& A, float* Ppart, float* P, float* Hl, unsigned* tickets, cudaStream_t st);
+cudaError_t launch_lora_q(const DecodeArgs& A, const float* Zlin, float* Q, cudaStream_t st);
+cudaError_t launch_lora_out(const DecodeArgs& A, const float* Yp, const float* Q, cudaStream_t st);
 cudaError_t launch_residual_add(const uint16_t* x, const uint16_t* y, size_t n, uint16_t* out, cudaStream_t st);
 cudaError_t launch_combine(const float* Y, const int32_t* idx, const int32_t* assign_row, int T, int d, int k,
                            int epg, const uint16_t* residual, uint16_t* y, cudaStream_t st);

@@ -1,40 +1,46 @@
-// The decode-path layer (<= 16 tokens, no LoRA branch) as one persistent
-// cooperative kernel built around a shared-memory weight ring.
+// The decode-path layer (<= 16 tokens) as one persistent cooperative kernel
+// built around a shared-memory weight ring (with the Recover-LoRA branch, the
+// small kernels of lora.cu run before and after it).
 //
-// Per CTA (one per SM, 16 warps): warp 15 is the producer. Its lane 0 walks
-// the CTA's list of weight chunks for the whole layer and loads each into the
-// next ring slot with TMA tensor copies (one box of up to 8 KB of packed int4
-// in 128-byte swizzle plus one box of bf16 scales, or 8 KB of fp32 router
-// rows), as far ahead as the ring allows (weights with an evict-first L2
-// policy; W_out also prefetched into L2 during the expert phases). Warps
-// 0..14 consume the chunks with tensor-core MMAs (int4 dequantised in
-// registers, fp16 operands, fp32 accumulation) against activation fragments
-// staged in shared memory.
+// Per CTA (one per SM): 16 consumer warps and one producer warp. The
+// producer's lane 0 walks the CTA's list of weight chunks for the whole layer
+// and loads each into the next ring slot (18 KB) with TMA tensor copies, as
+// far ahead as the ring allows; once the routing is known it also asks L2 to
+// prefetch every expert and W_out chunk the CTA will need, so that HBM keeps
+// streaming while the dependent phases run. The consumers contract the chunks
+// on the tensor cores (int4 dequantised in registers, fp16 operands, fp32
+// accumulation) against activation fragments in shared memory.
 //
-// Work, in ring order (KS = d/1024 reduction segments):
-//   A1  router logits: (segment, expert pair) items, partial sums reduced in
-//       segment order by the last arriver of each pair
-//   A2  H[g] = W_in[g] x for every group: (segment, group, 16-row tile)
-//       items, reduced in segment order by the last arriver of each tile
-//   --  every CTA computes the routing itself (top-k, softmax, tables) on
-//       the warps without a router item, while the others finish A2
-//   B   V[e] = silu(Gate_e h) * Up_e h for each routed expert: (expert,
-//       16-row tile) items, gate and up chunks back to back
-//   C   Z[g] = sum_{e in g} Down_e (w V_e): (expert, 32-row block) items with
-//       per-expert partials, summed in ascending expert order by the last
-//       arriver of each (group, block)
-//   D   Y[g] = W_out[g] Z[g]: (group, 16-row tile) items; the last group to
-//       finish a tile sums the groups in ascending order (+ residual) into y
-// Dependencies between CTAs are arrival counters (per group for H and Z, per
-// expert for V, one for the logits) instead of grid barriers: a CTA waits
-// only for the data it stages next, and the producer keeps streaming the next
-// phase's weights meanwhile. The counters come in two copies used by
-// alternate launches; each launch clears the copy the next one uses, so a
-// launch that ran out of its wait budget leaves the next one correct.
+// Every unit of work is split into the same 16 warp tasks, so no warp idles
+// within a phase; partial sums meet in shared memory, and after one barrier
+// of the consumer warps every thread reduces one output element (a serial
+// reducer warp would set the pace of the whole phase):
+//   A1  router logits: whole expert rows (K = d) per CTA, each warp a K
+//       slice; reduced in warp order -> logits
+//   A2  H[g] = W_in[g] x: whole 16-row tiles (K = d) per CTA, each warp a K
+//       slice; reduced in warp order -> H as fp16 fragments
+//   R   every CTA routes all tokens (top-k, softmax, tables)
+//   B   expert units (expert e, 32-wide slice of f): gate and up rows of the
+//       slice (the 16 warp tasks are (matrix, 16-row tile, K quarter)), then
+//       v = w silu(gate h) up h for the slice, then the slice's columns of
+//       Down_e (each warp 1/16 of the rows of the latent output); the Down
+//       results of a CTA's consecutive units of one group stay in registers
+//       and are written once per group as a partial of Z[g]
+//   C   Z[g] = the sum of its partials, in CTA order, by (group, 16-row) items
+//   D   Y[g] = W_out[g] Z[g] by (group, 32-row) items; after its last item
+//       a CTA takes one ticket per item, and the CTA that completes a row
+//       block sums the groups in ascending order (+ residual) into y
+// Between CTAs only five hand-offs remain: logits, H per group, Z partials
+// per group, Z per group, and the final tickets per row block of y. Each is
+// data, fence, counter atomic; counter seen by an acquire load, data. The
+// counters come in two copies used by alternate launches; each launch clears
+// the copy the next one uses.
 //
-// Every wait is bounded by the handle's cycle budget; running out sets the
-// timeout bit of the device error word and the kernel carries on to the end
-// (the output is then invalid and lmoe_check reports LMOE_ERR_TIMEOUT).
+// Every wait is bounded by the handle's cycle budget; the first wait of a CTA
+// that runs out sets the timeout bit of the device error word and turns every
+// later wait of that CTA into a no-op, so the kernel runs to its end (the
+// output is then invalid and lmoe_check reports LMOE_ERR_TIMEOUT); the
+// producer stops issuing copies and waits for the ones in flight.
 #include "common.cuh"
 #include "decode.cuh"
 #include "ring.cuh"
@@ -49,49 +55,63 @@ namespace lmoe {
 
 namespace {
 
-constexpr int NWARP = 16, NTHR = NWARP * 32, NCW = NWARP - 1, PROD = NWARP - 1, NCT = NCW * 32;
-constexpr int SLOT_BYTES = 10240;  // 8 KB of weights + 1 KB of scales, 1024-byte aligned
-constexpr int KEYS = 3;            // activation sets staged at once
-constexpr int KSEG = 1024;         // reduction segment of the router and W_in
-constexpr int DR = 32;             // rows of a down chunk
-constexpr int MAX_ACT = 256;       // routed experts per pass (16 tokens x k <= 16)
+constexpr int NCW = 16, NCT = NCW * 32, PROD = NCW, NTHR = NCT + 32;
+constexpr int SLOT = 18432;      // 16 KB of packed int4 (or fp32 router rows) + 2 KB of scales
+constexpr int FS = 32;           // f-slice of an expert unit
+constexpr int MAX_RX = 4;        // router experts per CTA
+constexpr int MAX_TILES = 4;     // W_in 16-row tiles per CTA
+constexpr int MAX_MPW = 4;       // Down 16-row tiles per warp (L <= 1024)
+constexpr int LMAX = 1024;
 
 template <int NT>
 __host__ __device__ constexpr int nslot() {
-  return NT == 1 ? 16 : 12;
+  return NT == 1 ? 8 : 4;
 }
 template <int NT>
-__host__ __device__ constexpr int key_bytes() {
-  return 16384 * NT;
+__host__ __device__ constexpr int xbytes() {
+  return 65536 * NT;
 }
 template <int NT>
 __host__ __device__ constexpr int dyn_smem() {
-  return 1024 + nslot<NT>() * SLOT_BYTES + KEYS * key_bytes<NT>();
+  return 1024 + nslot<NT>() * SLOT + xbytes<NT>();
 }
+// byte offsets inside the activation region after phase A
+template <int NT>
+__host__ __device__ constexpr int off_pbuf() {
+  return LMAX * NT * 16;  // after the H / Z fragments
+}
+template <int NT>
+__host__ __device__ constexpr int off_vbuf() {
+  return off_pbuf<NT>() + 2 * NCW * NT * 512;
+}
+template <int NT>
+__host__ __device__ constexpr int off_zred() {
+  return off_vbuf<NT>() + 2 * NT * 512;
+}
+static_assert(off_zred<1>() + 16384 <= xbytes<1>(), "activation region (one token tile)");
+static_assert(off_zred<2>() + 16384 <= xbytes<2>(), "activation region (two token tiles)");
 
 struct Tables {
-  int32_t idx[16 * 16];
+  uint64_t full[8], empty[8], tbar;
+  alignas(16) int32_t idx[16 * 16];
   float w[16 * 16];
   unsigned emask[16];        // bit e: expert e is routed by some token (E <= 512)
-  int16_t elist[MAX_ACT];    // routed experts, ascending
+  int16_t elist[512];        // routed experts, ascending
   int16_t glist[64];         // routed groups, ascending
   int16_t gslot0[65];        // first expert slot of each routed group
+  int16_t gplo[64], gpn[64], gpbase[64];  // Z partials of each routed group: first CTA, count, first slot
   int n_act, n_actg, par;
-  volatile int tables_ready;
+  int u_lo, u_hi, z_lo, z_hi, o_lo, o_hi;
+  volatile int abort;        // a wait of this CTA ran out: later waits return at once
   volatile int x_issued;     // the consumers' loads of x are in flight: weight copies may start
-  int key[KEYS];              // activation sets of the B, C and D phases
-  int keyA[KEYS];             // segments of x staged for the A phase
-  uint2 tkscr[NCW][32];       // top-k candidates, per routing warp
-  uint64_t full[16], empty[16];
-  volatile int seq[16];
+  int tk_z[4];
+  int16_t fin[64];           // per W_out item of this CTA: its row block when this CTA combines it, else -1
+  union {
+    float rred[NCW][MAX_RX][16];  // router partial logits per warp
+    uint2 tkscr[NCW][32];         // top-k candidates, per routing warp
+  } u;
 };
 
-// Orders this thread's earlier memory accesses before its later ones at GPU
-// scope. Every hand-off between CTAs here is a release/acquire pair (data,
-// fence, counter atomic; counter seen, fence or acquire load, data), for
-// which an acquire-release fence suffices: the sequentially consistent
-// fence (__threadfence) also joins one total order of all such fences on
-// the GPU, which thousands of hand-offs a pass would wait on.
 LMOE_DEV void fence_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 LMOE_DEV unsigned ld_acquire(const unsigned* p) {
@@ -100,134 +120,232 @@ LMOE_DEV unsigned ld_acquire(const unsigned* p) {
   return v;
 }
 
-// Whole warp, no divergence: lane i waits until *p_i >= target (p_i null:
-// nothing to wait for), polling with acquire loads.
-LMOE_COLD void wait_counts(const unsigned* p, unsigned target, long long budget, unsigned* err) {
-  const long long t0 = clock64();
-  #pragma unroll 1
-  while (!__all_sync(0xffffffffu, p == nullptr || ld_acquire(p) >= target)) {
-    if (__any_sync(0xffffffffu, clock64() - t0 > budget)) {
-      if ((threadIdx.x & 31) == 0) set_error(err, ERRBIT_TIMEOUT);
-      return;
-    }
-    __nanosleep(32);
-  }
-}
-
-// The routing warps (the last n consumer warps).
-LMOE_DEV void route_sync(int n) {
-  __syncwarp();
-  asm volatile("barrier.sync 3, %0;" ::"r"(n * 32) : "memory");
-}
-
-// Every warp, once, at the end of the kernel.
-LMOE_DEV void end_sync() { asm volatile("barrier.sync 2, %0;" ::"n"(NTHR) : "memory"); }
-
-// Consumer warps only (the producer never joins). Callers often reach it from
-// divergent code (a few lanes waiting on a counter), so the warp reconverges
-// first and the barrier is the non-aligned form, which counts every thread.
+// Consumer warps only (the producer never joins).
 LMOE_DEV void cons_sync() {
   __syncwarp();
   asm volatile("barrier.sync 1, %0;" ::"n"(NCT) : "memory");
 }
+// Every warp, once, at the end of the kernel.
+LMOE_DEV void end_sync() { asm volatile("barrier.sync 2, %0;" ::"n"(NTHR) : "memory"); }
 
-// The last of n arrivals on a ticket returns true; called by one lane after a
-// fence_gpu that publishes the caller's partial results.
-LMOE_DEV bool ticket_last(unsigned* t, unsigned n) { return atomicAdd(t, 1u) == n - 1; }
+// Where a wait gave up, for diagnosis: the first timeout of a launch is
+// recorded as bit 63 | site << 32 | CTA << 8 | warp in diag[0] (sites: the
+// wait_site enum below).
+enum WaitSite : unsigned {
+  WS_ROUTER_SLOT = 1, WS_WIN_SLOT, WS_LOGITS, WS_H, WS_GU_SLOT, WS_V, WS_DOWN_SLOT, WS_ZPART, WS_Z, WS_PFREE,
+  WS_WOUT_SLOT, WS_EMPTY, WS_TABLES, WS_DRAIN
+};
 
-LMOE_DEV float route_weight(const Tables& tb, int t, int e, int k) {
-  #pragma unroll 1
-  for (int j = 0; j < k; ++j)
-    if (tb.idx[t * 16 + j] == e) return tb.w[t * 16 + j];
-  return 0.f;
+LMOE_DEV void timeout_hit(Tables& tb, unsigned* err, unsigned site, unsigned long long* diag) {
+  set_error(err, ERRBIT_TIMEOUT);
+  tb.abort = 1;
+  if (diag)
+    atomicCAS(diag, 0ull,
+              (1ull << 63) | ((unsigned long long)site << 32) | ((unsigned long long)blockIdx.x << 8) | (threadIdx.x >> 5));
+}
+
+// %globaltimer (ns), for the per-CTA phase record
+LMOE_DEV unsigned long long gtime() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// One thread: until *p >= target (acquire loads), bounded.
+LMOE_COLD void wait_ge(Tables& tb, const unsigned* p, unsigned target, long long budget, unsigned* err, unsigned site,
+                       unsigned long long* diag) {
+  if (tb.abort) return;
+  const long long t0 = clock64();
+#pragma unroll 1
+  while (ld_acquire(p) < target) {
+    if (clock64() - t0 > budget) {
+      timeout_hit(tb, err, site, diag);
+      return;
+    }
+    __nanosleep(40);
+  }
+}
+
+// Whole warp: until *p >= target, every lane polling with acquire loads.
+LMOE_COLD void warp_wait_ge(Tables& tb, const unsigned* p, unsigned target, long long budget, unsigned* err,
+                            unsigned site, unsigned long long* diag) {
+  if (tb.abort) return;
+  const long long t0 = clock64();
+#pragma unroll 1
+  while (!__all_sync(0xffffffffu, ld_acquire(p) >= target)) {
+    if (__any_sync(0xffffffffu, clock64() - t0 > budget)) {
+      if ((threadIdx.x & 31) == 0) timeout_hit(tb, err, site, diag);
+      __syncwarp();
+      return;
+    }
+    __nanosleep(40);
+  }
+}
+
+// try_wait with a suspend-time hint: a waiting warp sleeps in hardware until
+// the phase completes or about `ns` nanoseconds pass, instead of spinning on
+// issue slots the working warps need
+LMOE_DEV bool mbar_sleep_wait(uint64_t* m, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(m)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+// mbarrier phase wait, bounded; true once the phase completed, false when it
+// gave up (a timeout of the CTA: every later wait returns false at once).
+LMOE_DEV bool mwait(Tables& tb, uint64_t* m, uint32_t parity, long long budget, unsigned* err, unsigned site,
+                    unsigned long long* diag) {
+  if (mbar_test(m, parity)) return true;
+  if (tb.abort) return false;
+  const long long t0 = clock64();
+#pragma unroll 1
+  while (!mbar_sleep_wait(m, parity, 4000u)) {
+    if (tb.abort) return false;
+    if (clock64() - t0 > budget) {
+      timeout_hit(tb, err, site, diag);
+      return false;
+    }
+  }
+  return true;
+}
+
+// This warp is done with ring chunk j (acquire's `landed`). Every warp hands
+// back every chunk, and only after the chunk's copy completed: an arrival
+// made earlier could count toward the slot's previous use (a warp that does
+// not read a chunk can run ahead) and complete that phase too early, and
+// after a timeout, when waits give up, a slot whose copy is still in flight
+// must never be re-armed and overwritten.
+template <int NS>
+LMOE_DEV void release_read(Tables& tb, int j, bool landed) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0 && landed) mbar_arrive(&tb.empty[j % NS]);
+}
+
+template <int NS>
+LMOE_DEV const unsigned char* acquire(Tables& tb, unsigned char* ring, int j, long long budget, unsigned* err,
+                                      unsigned site, unsigned long long* diag, bool& landed) {
+  landed = mwait(tb, &tb.full[j % NS], (uint32_t)(j / NS) & 1u, budget, err, site, diag);
+  landed = __all_sync(0xffffffffu, landed);
+  return ring + (j % NS) * SLOT;
 }
 
 // Counter layout (one copy; two copies alternate between launches). Every
-// counter sits on a 128-byte line of its own (CSTR words apart): the
-// completion counters are polled by whole CTAs, and the tickets take up to
-// a few hundred atomics each within microseconds, which one L2 line would
-// serialise.
+// counter sits on a 128-byte line of its own (CSTR words apart).
 constexpr int CSTR = 32;
 struct CtrMap {
-  int tk_router, done_router, tk_win, done_in, done_gu, tk_down, done_down, tk_wout, n;
+  int done_router, done_in, done_part, done_z, tk_wout, n;
 };
-__host__ __device__ inline CtrMap ctr_map(int d, int E, int G, int L) {
+__host__ __device__ inline CtrMap ctr_map(int d, int G) {
   CtrMap m;
   int o = 0;
-  m.tk_router = o; o += E / 2 * CSTR;
   m.done_router = o; o += CSTR;
-  m.tk_win = o; o += G * (L / 16) * CSTR;
   m.done_in = o; o += G * CSTR;
-  m.done_gu = o; o += MAX_ACT * CSTR;
-  m.tk_down = o; o += G * (L / DR) * CSTR;
-  m.done_down = o; o += G * CSTR;
-  m.tk_wout = o; o += d / 16 * CSTR;
-  m.n = (o + 31) & ~31;
+  m.done_part = o; o += G * CSTR;
+  m.done_z = o; o += G * CSTR;
+  m.tk_wout = o; o += d / 32 * CSTR;
+  m.n = o;
   return m;
 }
 
-// index range of CTA c of nC over n items
+// index range of CTA c of nC over n items (n nC < 2^32)
 LMOE_DEV void split(int n, int c, int nC, int& lo, int& hi) {
-  lo = (int)((long long)c * n / nC);
-  hi = (int)((long long)(c + 1) * n / nC);
+  lo = (int)((unsigned)c * (unsigned)n / (unsigned)nC);
+  hi = (int)((unsigned)(c + 1) * (unsigned)n / (unsigned)nC);
+}
+// the CTA whose range holds item u (of n split over nC)
+LMOE_DEV int owner(int u, int n, int nC) { return (int)(((unsigned)(u + 1) * (unsigned)nC - 1u) / (unsigned)n); }
+// how many of the CTAs a .. b-1 have a non-empty range of the n items: all of
+// them when n >= nC, else one per item boundary crossed
+LMOE_DEV int busy_ctas(int a, int b, int n, int nC) {
+  const int d = (int)((unsigned)b * (unsigned)n / (unsigned)nC - (unsigned)a * (unsigned)n / (unsigned)nC);
+  return d < b - a ? d : b - a;
 }
 
-// ------------------------------------------------------------ staging
-// Fragment layout of an activation set over K elements: frag_index(chunk c of
-// 128, token tile nt, m pair mp, lane) -> 8 consecutive elements of token
-// 8*nt + lane/4 starting at 128 c + 32 (lane % 4) + 8 mp, as fp16 pairs
-// (e0,e4) (e1,e5) (e2,e6) (e3,e7).
+// Index of the fragment entry holding elements k0 .. k0+7 (k0 a multiple of
+// 8) of token n: frag_index(chunk of 128, token tile, m pair, lane), see
+// common.cuh.
 template <int NT>
-LMOE_COLD void stage_x(Tables& tb, uint4* keyset, const uint16_t* x, int T, int d, int ctid) {
-  constexpr int N = (KSEG / 128) * NT * 128, PER = (N + NCT - 1) / NCT;
-  // every load first, then let the producer start the weight copies: x's
-  // loads must not queue behind them
-  uint4 v[KEYS][PER];
+LMOE_DEV int entry_index(int k0, int n) {
+  return frag_index(k0 >> 7, n >> 3, (k0 & 31) >> 3, (n & 7) * 4 + ((k0 & 127) >> 5), NT);
+}
+
+// the routing weight of expert e for token t (0 when t does not pick e; the
+// rows of tokens >= T and the entries past k hold no expert)
+LMOE_DEV float route_weight(const Tables& tb, int t, int e) {
+  const int4* ix = reinterpret_cast<const int4*>(tb.idx + t * 16);
+  int j = -1;
 #pragma unroll
-  for (int s = 0; s < KEYS; ++s) {
-    const int ks = tb.keyA[s];
+  for (int q = 0; q < 4; ++q) {
+    const int4 v = ix[q];
+    j = v.x == e ? 4 * q : j;
+    j = v.y == e ? 4 * q + 1 : j;
+    j = v.z == e ? 4 * q + 2 : j;
+    j = v.w == e ? 4 * q + 3 : j;
+  }
+  return j >= 0 ? tb.w[t * 16 + j] : 0.f;
+}
+
+// x (bf16 [T][d]) into shared memory as it is, 8 NT rows of d, rows >= T zero
+template <int NT>
+LMOE_COLD void stage_x(Tables& tb, uint4* xs, const uint16_t* x, int T, int d, int ctid) {
+  const int n = NT * d, nx = T * (d / 8);  // 16-byte units: all rows, rows of tokens
+  const uint4* x4 = reinterpret_cast<const uint4*>(x);
+#pragma unroll 1
+  for (int i0 = ctid; i0 < n; i0 += 8 * NCT) {
+    uint4 v[8];
 #pragma unroll
-    for (int r = 0; r < PER; ++r) {
-      const int si = ctid + r * NCT;
+    for (int r = 0; r < 8; ++r) {
+      const int si = i0 + r * NCT;
+      v[r] = si < nx ? __ldg(x4 + si) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (i0 == ctid && ctid == 0) tb.x_issued = 1;
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      if (i0 + r * NCT < n) xs[i0 + r * NCT] = v[r];
+  }
+}
+
+// The staged x, in place, into fp16 fragments over all of d (each fragment
+// entry is one 16-byte unit of x, converted and reordered).
+template <int NT>
+LMOE_COLD void x_to_frags(uint4* xs, int d, int ctid) {
+  const int n = NT * d;  // entries, <= 8 NT per thread (d <= 4096)
+  uint4 v[8 * NT];
+#pragma unroll
+  for (int r = 0; r < 8 * NT; ++r) {
+    const int si = ctid + r * NCT;
+    if (si < n) {
       const int ln = si & 31, mp = (si >> 5) & 3, rest = si >> 7;
       const int nt = rest % NT, cc = rest / NT;
-      const int tok = nt * 8 + (ln >> 2), tg = ln & 3;
-      const int k0 = ks * KSEG + cc * 128 + tg * 32 + mp * 8;
-      v[s][r] = (ks >= 0 && si < N && tok < T) ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * d + k0))
-                                               : make_uint4(0u, 0u, 0u, 0u);
+      const int tok = nt * 8 + (ln >> 2), k0 = cc * 128 + (ln & 3) * 32 + mp * 8;
+      v[r] = xs[tok * (d / 8) + (k0 >> 3)];
     }
   }
   cons_sync();
-  if (ctid == 0) tb.x_issued = 1;
 #pragma unroll
-  for (int s = 0; s < KEYS; ++s) {
-    uint4* fr = keyset + s * (key_bytes<NT>() / 16);
-#pragma unroll
-    for (int r = 0; r < PER; ++r) {
-      const int si = ctid + r * NCT;
-      if (tb.keyA[s] < 0 || si >= N) continue;
-      const uint32_t u[4] = {v[s][r].x, v[s][r].y, v[s][r].z, v[s][r].w};
+  for (int r = 0; r < 8 * NT; ++r) {
+    const int si = ctid + r * NCT;
+    if (si < n) {
+      const uint32_t u[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
       float e[8];
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         e[2 * h] = __uint_as_float(u[h] << 16);
         e[2 * h + 1] = __uint_as_float(u[h] & 0xffff0000u);
       }
-      fr[si] = pack_frag8(e);
+      xs[si] = pack_frag8(e);
     }
   }
-}
-
-// Index of the fragment entry holding elements k0 .. k0+7 (k0 a multiple of
-// 8) of token n, in the layout above.
-template <int NT>
-LMOE_DEV int entry_index(int k0, int n) {
-  return frag_index(k0 >> 7, n >> 3, (k0 & 31) >> 3, (n & 7) * 4 + ((k0 & 127) >> 5), NT);
+  cons_sync();
 }
 
 // n fragment entries from global memory into shared memory (consumer threads)
 LMOE_COLD void copy_frags(uint4* dst, const uint4* src, int n, int ctid) {
-  #pragma unroll 1
+#pragma unroll 1
   for (int i = ctid; i < n; i += 4 * NCT) {
     uint4 v[4];
 #pragma unroll
@@ -238,61 +356,6 @@ LMOE_COLD void copy_frags(uint4* dst, const uint4* src, int n, int ctid) {
   }
 }
 
-// Distinct keys of items [lo, hi) (nondecreasing) into the key table; returns
-// false (and flags bad data) if more than KEYS are needed. Consumer thread 0.
-template <class KeyF>
-LMOE_COLD void collect_keys(int* keys, int lo, int hi, KeyF key, unsigned* err) {
-  int n = 0, last = -1;
-  #pragma unroll 1
-  for (int i = lo; i < hi; ++i) {
-    const int kk = key(i);
-    if (kk != last) {
-      if (n == KEYS) {
-        set_error(err, ERRBIT_BAD_DATA);
-        break;
-      }
-      keys[n++] = kk;
-      last = kk;
-    }
-  }
-  #pragma unroll 1
-  for (int s = n; s < KEYS; ++s) keys[s] = -1;
-}
-
-LMOE_DEV int key_slot(const int* keys, int kk) {
-  #pragma unroll 1
-  for (int s = 0; s < KEYS; ++s)
-    if (keys[s] == kk) return s;
-  return 0;
-}
-
-// ------------------------------------------------------------ ring access
-template <int NS>
-LMOE_DEV const unsigned char* cons_wait(Tables& tb, unsigned char* ring, int j, long long budget, unsigned* err) {
-  const int s = j % NS, u = j / NS;
-  const long long t0 = clock64();
-  #pragma unroll 1
-  while (tb.seq[s] != j) {
-    if (clock64() - t0 > budget) {
-      set_error(err, ERRBIT_TIMEOUT);
-      break;
-    }
-    __nanosleep(20);
-  }
-  mbar_wait(&tb.full[s], u & 1, budget, err);
-  return ring + s * SLOT_BYTES;
-}
-
-template <int NS>
-LMOE_DEV void cons_release(Tables& tb, int j) {
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(&tb.empty[j % NS]);
-}
-
-
-}  // namespace
-
-// ==================================================================== kernel
 // Routed-expert and routed-group tables from the routed-expert bit mask (one
 // warp): elist = routed experts ascending, glist = their groups, gslot0[gi] =
 // first slot of group gi in elist (gslot0[n_actg] = n_act).
@@ -338,6 +401,55 @@ LMOE_COLD void build_tables(Tables& tb, int epg) {
   __syncwarp();
 }
 
+// The work split that follows from the routing (one warp): this CTA's expert
+// units, Z items and W_out items, and for every routed group the CTAs whose
+// units write its Z partials (contiguous: units are ordered by expert, hence
+// by group) and where its partials start.
+LMOE_COLD void plan(Tables& tb, int c, int nC, int NSF, int L, int d) {
+  const int lane = threadIdx.x & 31;
+  const int n_act = tb.n_act, n_actg = tb.n_actg, NU = n_act * NSF;
+  int run = 0;
+#pragma unroll 1
+  for (int g0 = 0; g0 < n_actg; g0 += 32) {
+    const int gi = g0 + lane;
+    int P = 0, lo = 0;
+    if (gi < n_actg) {  // the CTAs that own units of the group (some CTAs own none when NU < nC)
+      const int fu = tb.gslot0[gi] * NSF, lu = tb.gslot0[gi + 1] * NSF - 1;
+      lo = owner(fu, NU, nC);
+      P = busy_ctas(lo, owner(lu, NU, nC) + 1, NU, nC);
+    }
+    int pre = P;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, pre, o);
+      if (lane >= o) pre += y;
+    }
+    if (gi < n_actg) {
+      tb.gplo[gi] = (int16_t)lo;
+      tb.gpn[gi] = (int16_t)P;
+      tb.gpbase[gi] = (int16_t)(run + pre - P);
+    }
+    run += __shfl_sync(0xffffffffu, pre, 31);
+  }
+  if (lane == 0) {
+    split(NU, c, nC, tb.u_lo, tb.u_hi);
+    split(n_actg * (L / 16), c, nC, tb.z_lo, tb.z_hi);
+    split(n_actg * (d / 32), c, nC, tb.o_lo, tb.o_hi);
+  }
+  __syncwarp();
+}
+
+// the group slot (index in glist) of expert slot es
+LMOE_DEV int group_slot(const Tables& tb, int es) {
+  int gi = 0;
+#pragma unroll 1
+  while (gi + 1 < tb.n_actg && tb.gslot0[gi + 1] <= es) ++gi;
+  return gi;
+}
+
+}  // namespace
+
+// ==================================================================== kernel
 template <int NT>
 __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_constant__ FusedArgs F) {
   constexpr int NS = nslot<NT>();
@@ -346,206 +458,193 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
   __shared__ Tables tb;
   unsigned char* dsm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~(uintptr_t)1023);
   unsigned char* ring = dsm;
-  uint4* keyset = reinterpret_cast<uint4*>(dsm + NS * SLOT_BYTES);
-  auto kfr = [&](int s) { return keyset + s * (key_bytes<NT>() / 16); };
+  unsigned char* xr = dsm + NS * SLOT;                      // activation region
+  uint4* xf = reinterpret_cast<uint4*>(xr);                  // x / H / Z fragments
+  float4* pbuf = reinterpret_cast<float4*>(xr + off_pbuf<NT>());  // [2][NCW][NT][32] partial tiles
+  uint4* vbuf = reinterpret_cast<uint4*>(xr + off_vbuf<NT>());    // [2][NT][32] slice fragments
+  float4* zred = reinterpret_cast<float4*>(xr + off_zred<NT>());  // [4 items][4 quarters][32][2]
 
   const DecodeArgs& A = F.A;
   const int T = A.T, d = A.d, E = A.E, G = A.G, k = A.k, L = A.L, f = A.f, epg = A.epg;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
   const int nC = gridDim.x, c = blockIdx.x;
-  const int KS = d / KSEG, NPAIR = E / 2, NRT_IN = L / 16, NRB = L / DR, NRT_OUT = d / 16;
+  const int NSF = f / FS, CL = L / 128, PW = d < 2048 ? d : 2048, NPW = d / PW, MPW = L / 256;
   const long long budget = F.timeout;
   unsigned* err = A.err;
-  const CtrMap cm = ctr_map(d, E, G, L);
+  const CtrMap cm = ctr_map(d, G);
+  unsigned long long* diag = F.diag;  // [0] first timeout; [1 + 32 c + e] phase times of CTA c
+  unsigned long long* trace = diag ? diag + 1 + (size_t)c * 32 : nullptr;
 
   // ---------------------------------------------------------------- set-up
   if (threadIdx.x == 0) {
     const unsigned long long old = atomicAdd(F.launches, 1ull);
     tb.par = (int)((old / (unsigned long long)nC) & 1ull);
-    tb.tables_ready = 0;
+    tb.abort = 0;
     tb.x_issued = 0;
-    #pragma unroll 1
+#pragma unroll 1
     for (int s = 0; s < NS; ++s) {
       mbar_init(&tb.full[s], 1);
-      mbar_init(&tb.empty[s], 1);
-      tb.seq[s] = -1;
+      mbar_init(&tb.empty[s], NCW);
     }
+    mbar_init(&tb.tbar, 1);
+    tb.tk_z[0] = tb.tk_z[1] = tb.tk_z[2] = tb.tk_z[3] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  if (threadIdx.x < 256) {
+    tb.idx[threadIdx.x] = -1;
+    tb.w[threadIdx.x] = 0.f;
+  }
+  if (threadIdx.x < 16) tb.emask[threadIdx.x] = 0u;
   __syncthreads();
+  if (trace && threadIdx.x == 0) trace[0] = gtime();
   unsigned* ctr = F.ctr + (size_t)tb.par * cm.n;
   {  // clear the copy of the counters the next launch uses
     unsigned* nxt = F.ctr + (size_t)(tb.par ^ 1) * cm.n;
-    #pragma unroll 1
+#pragma unroll 1
     for (int i = c * NTHR + threadIdx.x; i < cm.n; i += nC * NTHR) nxt[i] = 0u;
   }
-  int a1lo, a1hi, a2lo, a2hi;
-  split(KS * NPAIR, c, nC, a1lo, a1hi);
-  split(KS * G * NRT_IN, c, nC, a2lo, a2hi);
-  const int nA1 = a1hi - a1lo, nA2 = a2hi - a2lo;
+  int e_lo, e_hi, t_lo, t_hi;
+  split(E, c, nC, e_lo, e_hi);
+  split(G * (L / 16), c, nC, t_lo, t_hi);
+  const int ne = e_hi - e_lo, ntl = t_hi - t_lo;
+  const int jA2 = ne, jB = jA2 + ntl * NPW;
 
   if (warp == PROD) {
     // ================================================== producer
-    // Lane 0 issues every chunk. Its loop is kept short (no divisions, no
-    // calls): it shares an SM sub-partition with three consumer warps, and
-    // its issue rate bounds how fast weights reach the ring.
-    int j = 0, slot = 0, use = 0;
-    bool ok = true;
-    auto claim = [&](uint32_t bytes) -> unsigned char* {  // next chunk's slot, armed for `bytes`
-      if (use > 0) {
-        const long long t0 = clock64();
-        while (!mbar_test(&tb.full[slot], (use - 1) & 1) || !mbar_test(&tb.empty[slot], (use - 1) & 1)) {
-          if (clock64() - t0 > budget) {
-            set_error(err, ERRBIT_TIMEOUT);
-            ok = false;
-            return nullptr;
-          }
-        }
-      }
-      tb.seq[slot] = j;
-      mbar_expect_tx(&tb.full[slot], bytes);
-      return ring + slot * SLOT_BYTES;
-    };
-    auto advance = [&]() {
-      ++j;
-      if (++slot == NS) {
-        slot = 0;
-        ++use;
-      }
-    };
     if (lane == 0) {
       const uint64_t pol = l2_evict_first();  // weights are read once per pass
-      {  // x first: its loads are small and every CTA waits on them
+      int j = 0;
+      auto claim = [&](uint32_t bytes) -> unsigned char* {  // chunk j's slot, armed for `bytes`
+        const int s = j % NS, u = j / NS;
+        if (u > 0) mwait(tb, &tb.empty[s], (uint32_t)(u - 1) & 1u, budget, err, WS_EMPTY, diag);
+        if (tb.abort) return nullptr;
+        mbar_expect_tx(&tb.full[s], bytes);
+        return ring + s * SLOT;
+      };
+      bool ok = true;
+      {  // x first: its loads are small and every CTA waits on them, so they
+         // must not queue behind this CTA's weight copies
         const long long t0 = clock64();
 #pragma unroll 1
-        while (tb.x_issued == 0) {
-          if (clock64() - t0 > budget) {
-            set_error(err, ERRBIT_TIMEOUT);
-            ok = false;
-            break;
-          }
-          __nanosleep(32);
-        }
+        while (!tb.x_issued && !tb.abort && clock64() - t0 < budget) __nanosleep(32);
       }
-      {  // router: (segment, expert pair)
-        int ks = a1lo / NPAIR, pr = a1lo % NPAIR;
+      // A1: router rows
 #pragma unroll 1
-        for (int i = a1lo; ok && i < a1hi; ++i) {
-          unsigned char* dst = claim(2 * KSEG * 4);
-          if (!dst) break;
-          tma_load_3d_hint(dst, &F.maps.wr, 0, ks * (KSEG / 256), 2 * pr, &tb.full[slot], pol);
-          advance();
-          if (++pr == NPAIR) { pr = 0; ++ks; }
-        }
+      for (int i = 0; ok && i < ne; ++i) {
+        unsigned char* dst = claim(4u * d);
+        if (!(ok = dst != nullptr)) break;
+        tma_load_3d_hint(dst, &F.maps.wr, 0, 0, e_lo + i, &tb.full[j % NS], pol);
+        if (trace && i == 0) trace[26] = gtime();
+        ++j;
       }
-      {  // W_in: (segment, group, 16-row tile)
-        const int per_ks = G * NRT_IN;
-        int ks = a2lo / per_ks, row = a2lo % per_ks;  // row tile index g * NRT_IN + rt
+      // every W_in piece of this CTA into L2, behind the router rows: most of
+      // them wait for a ring slot until the router rows are consumed
 #pragma unroll 1
-        for (int i = a2lo; ok && i < a2hi; ++i) {
-          unsigned char* dst = claim(16 * KSEG / 2 + 16 * KSEG / 16);
-          if (!dst) break;
-          tma_load_3d_hint(dst, &F.maps.win_q, 0, ks * (KSEG / 256), row * 16, &tb.full[slot], pol);
-          tma_load_2d_hint(dst + 16 * KSEG / 2, &F.maps.win_s, ks * (KSEG / 32), row * 16, &tb.full[slot], pol);
-          advance();
-          if (++row == per_ks) { row = 0; ++ks; }
+      for (int i = 0; i < ntl; ++i)
+#pragma unroll 1
+        for (int p = 0; p < NPW; ++p) {
+          tma_prefetch_3d(&F.maps.win_q, 0, p * (PW / 256), (t_lo + i) * 16);
+          tma_prefetch_2d(&F.maps.win_s, p * (PW / 32), (t_lo + i) * 16);
         }
-      }
-      if (ok) {  // the routing tables (built by the consumers)
-        const long long t0 = clock64();
+      // A2: W_in tiles in pieces of PW columns
 #pragma unroll 1
-        while (tb.tables_ready == 0) {
-          if (clock64() - t0 > budget) {
-            set_error(err, ERRBIT_TIMEOUT);
-            ok = false;
-            break;
-          }
-          __nanosleep(64);
+      for (int i = 0; ok && i < ntl; ++i)
+#pragma unroll 1
+        for (int p = 0; ok && p < NPW; ++p) {
+          unsigned char* dst = claim(9u * PW);
+          if (!(ok = dst != nullptr)) break;
+          const int row0 = (t_lo + i) * 16;
+          tma_load_3d_hint(dst, &F.maps.win_q, 0, p * (PW / 256), row0, &tb.full[j % NS], pol);
+          tma_load_2d_hint(dst + 8 * PW, &F.maps.win_s, p * (PW / 32), row0, &tb.full[j % NS], pol);
+          ++j;
         }
-        __threadfence_block();
+      // the routing tables, from the consumers
+      if (ok) {
+        mwait(tb, &tb.tbar, 0u, budget, err, WS_TABLES, diag);
+        ok = !tb.abort;
+        if (trace) trace[13] = gtime();
       }
-      const int n_act = tb.n_act, n_actg = tb.n_actg, FT = f / 16;
-      int lo = 0, hi = 0;
-      if (ok) split(n_act * FT, c, nC, lo, hi);
-      {  // gate/up: (expert slot, 16-row tile), gate then up
-        int es = lo / FT, rt = lo % FT;
-        int e = es < n_act ? tb.elist[es] : 0;
+      const int u_lo = tb.u_lo, nu = ok ? tb.u_hi - tb.u_lo : 0;
+      const int o_lo = tb.o_lo, no = ok ? tb.o_hi - tb.o_lo : 0;
+      // Every chunk this CTA streams from here on, into L2; asked for once the
+      // ring holds the first units, so that their own copies do not queue
+      // behind the whole layer's prefetches.
+      const int npre = NS / 3;
+      auto prefetch_rest = [&]() {
 #pragma unroll 1
-        for (int i = lo; ok && i < hi; ++i) {
-          const int row = e * f + rt * 16;
-          unsigned char* dst = claim(16 * L / 2 + 16 * L / 16);
-          if (!dst) break;
-          tma_load_3d_hint(dst, &F.maps.gate_q, 0, 0, row, &tb.full[slot], pol);
-          tma_load_2d_hint(dst + 16 * L / 2, &F.maps.gate_s, 0, row, &tb.full[slot], pol);
-          advance();
-          dst = claim(16 * L / 2 + 16 * L / 16);
-          if (!dst) break;
-          tma_load_3d_hint(dst, &F.maps.up_q, 0, 0, row, &tb.full[slot], pol);
-          tma_load_2d_hint(dst + 16 * L / 2, &F.maps.up_s, 0, row, &tb.full[slot], pol);
-          advance();
-          if (++rt == FT) {
-            rt = 0;
-            if (++es < n_act) e = tb.elist[es];
-          }
+        for (int q = npre; q < nu; ++q) {
+          const int u = u_lo + q, e = tb.elist[u / NSF], s = u % NSF, row = e * f + s * FS;
+          tma_prefetch_3d(&F.maps.gate_q, 0, 0, row);
+          tma_prefetch_2d(&F.maps.gate_s, 0, row);
+          tma_prefetch_3d(&F.maps.up_q, 0, 0, row);
+          tma_prefetch_2d(&F.maps.up_s, 0, row);
+          tma_prefetch_2d(&F.maps.dsl_q, 0, (e * NSF + s) * (L / 8));
+          tma_prefetch_2d(&F.maps.dsl_s, 0, (e * NSF + s) * (L / 256));
         }
-      }
-      if (ok) {  // this CTA's W_out chunks into L2 now, while the experts are computed:
-                 // fetched in a burst at the end they would slow the Z reductions
-        int plo, phi;
-        split(n_actg * NRT_OUT, c, nC, plo, phi);
-        int gi = plo / NRT_OUT, rt = plo % NRT_OUT;
 #pragma unroll 1
-        for (int i = plo; i < phi; ++i) {
-          const int row = tb.glist[gi] * d + rt * 16;
+        for (int q = 0; q < no; ++q) {
+          const int it = o_lo + q, row = tb.glist[it / (d / 32)] * d + (it % (d / 32)) * 32;
           tma_prefetch_3d(&F.maps.wout_q, 0, 0, row);
           tma_prefetch_2d(&F.maps.wout_s, 0, row);
-          if (++rt == NRT_OUT) { rt = 0; ++gi; }
         }
-      }
-      if (ok) split(n_act * NRB, c, nC, lo, hi);
-      {  // down: (expert slot, 32-row block)
-        int es = lo / NRB, rb = lo % NRB;
-        int e = es < n_act ? tb.elist[es] : 0;
+        if (F.has_next) {  // the next layer's first phase, behind this layer's requests
 #pragma unroll 1
-        for (int i = lo; ok && i < hi; ++i) {
-          const int row = e * L + rb * DR;
-          unsigned char* dst = claim(DR * f / 2 + DR * f / 16);
-          if (!dst) break;
-          tma_load_3d_hint(dst, &F.maps.down_q, 0, 0, row, &tb.full[slot], pol);
-          tma_load_2d_hint(dst + DR * f / 2, &F.maps.down_s, 0, row, &tb.full[slot], pol);
-          advance();
-          if (++rb == NRB) {
-            rb = 0;
-            if (++es < n_act) e = tb.elist[es];
-          }
-        }
-      }
-      if (ok) split(n_actg * NRT_OUT, c, nC, lo, hi);
-      {  // W_out: (group slot, 16-row tile)
-        int gi = lo / NRT_OUT, rt = lo % NRT_OUT;
-        int g = gi < n_actg ? tb.glist[gi] : 0;
+          for (int i = 0; i < ne; ++i) tma_prefetch_3d(&F.next_wr, 0, 0, e_lo + i);
 #pragma unroll 1
-        for (int i = lo; ok && i < hi; ++i) {
-          const int row = g * d + rt * 16;
-          unsigned char* dst = claim(16 * L / 2 + 16 * L / 16);
-          if (!dst) break;
-          tma_load_3d_hint(dst, &F.maps.wout_q, 0, 0, row, &tb.full[slot], pol);
-          tma_load_2d_hint(dst + 16 * L / 2, &F.maps.wout_s, 0, row, &tb.full[slot], pol);
-          advance();
-          if (++rt == NRT_OUT) {
-            rt = 0;
-            if (++gi < n_actg) g = tb.glist[gi];
-          }
+          for (int i = 0; i < ntl; ++i)
+#pragma unroll 1
+            for (int p = 0; p < NPW; ++p) {
+              tma_prefetch_3d(&F.next_win_q, 0, p * (PW / 256), (t_lo + i) * 16);
+              tma_prefetch_2d(&F.next_win_s, p * (PW / 32), (t_lo + i) * 16);
+            }
         }
+      };
+      bool pf = !ok;
+      // B: per unit the gate slice, the up slice, the Down slice
+#pragma unroll 1
+      for (int q = 0; ok && q < nu; ++q) {
+        if (q == npre) {
+          prefetch_rest();
+          pf = true;
+        }
+        const int u = u_lo + q, e = tb.elist[u / NSF], s = u % NSF, row = e * f + s * FS;
+        unsigned char* dst = claim(18u * L);
+        if (!(ok = dst != nullptr)) break;
+        tma_load_3d_hint(dst, &F.maps.gate_q, 0, 0, row, &tb.full[j % NS], pol);
+        if (trace && q == 0) trace[20] = gtime();
+        tma_load_2d_hint(dst + 16 * L, &F.maps.gate_s, 0, row, &tb.full[j % NS], pol);
+        ++j;
+        dst = claim(18u * L);
+        if (!(ok = dst != nullptr)) break;
+        tma_load_3d_hint(dst, &F.maps.up_q, 0, 0, row, &tb.full[j % NS], pol);
+        tma_load_2d_hint(dst + 16 * L, &F.maps.up_s, 0, row, &tb.full[j % NS], pol);
+        ++j;
+        dst = claim(18u * L);
+        if (!(ok = dst != nullptr)) break;
+        tma_load_2d_hint(dst, &F.maps.dsl_q, 0, (e * NSF + s) * (L / 8), &tb.full[j % NS], pol);
+        tma_load_2d_hint(dst + 16 * L, &F.maps.dsl_s, 0, (e * NSF + s) * (L / 256), &tb.full[j % NS], pol);
+        ++j;
+      }
+      if (ok && !pf) prefetch_rest();
+      // D: W_out, 32 rows of one group per chunk
+#pragma unroll 1
+      for (int q = 0; ok && q < no; ++q) {
+        const int it = o_lo + q, row = tb.glist[it / (d / 32)] * d + (it % (d / 32)) * 32;
+        unsigned char* dst = claim(18u * L);
+        if (!(ok = dst != nullptr)) break;
+        tma_load_3d_hint(dst, &F.maps.wout_q, 0, 0, row, &tb.full[j % NS], pol);
+        if (trace && q == 0) trace[24] = gtime();
+        tma_load_2d_hint(dst + 16 * L, &F.maps.wout_s, 0, row, &tb.full[j % NS], pol);
+        ++j;
       }
       // Wait for the copies still in flight before the CTA may exit. They do
       // not depend on other CTAs, so this drain gets a budget of its own.
+      if (trace) trace[10] = gtime();
       const long long drain = budget > (1ll << 28) ? budget : (1ll << 28);
 #pragma unroll 1
       for (int jj = (j > NS ? j - NS : 0); jj < j; ++jj) mbar_wait(&tb.full[jj % NS], (jj / NS) & 1, drain, err);
     }
-    // The whole producer warp stays resident until every consumer is done: a
-    // warp that exits changes what the consumers' named barrier counts.
+    // The whole producer warp stays resident until every consumer is done.
     __syncwarp();
     end_sync();
     return;
@@ -553,453 +652,472 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
 
   // ================================================================ consumers
   const int ctid = threadIdx.x;  // 0 .. NCT-1
-  int jbase = 0;
-
-  // ------------------------------------------------- segments of x (A1, A2)
-  if (ctid == 0) {
-    const int k1lo = a1lo / NPAIR, k1hi = (a1hi - 1) / NPAIR, k2lo = a2lo / (G * NRT_IN),
-              k2hi = (a2hi - 1) / (G * NRT_IN);
-    int n = 0;
-    #pragma unroll 1
-    for (int ks = 0; ks < KS; ++ks) {
-      const bool need = (nA1 > 0 && ks >= k1lo && ks <= k1hi) || (nA2 > 0 && ks >= k2lo && ks <= k2hi);
-      if (!need) continue;
-      if (n == KEYS) {
-        set_error(err, ERRBIT_BAD_DATA);
-        break;
-      }
-      tb.keyA[n++] = ks;
-    }
-    #pragma unroll 1
-    for (int s = n; s < KEYS; ++s) tb.keyA[s] = -1;
-  }
-  cons_sync();
-  stage_x<NT>(tb, keyset, A.x, T, d, ctid);
-  cons_sync();
 
   // ------------------------------------------------------------ A1 router
-  #pragma unroll 1
-  for (int li = warp; li < nA1; li += NCW) {
-    const int i = a1lo + li, ks = i / NPAIR, pr = i % NPAIR, e0 = 2 * pr;
-    const float* wr = reinterpret_cast<const float*>(cons_wait<NS>(tb, ring, jbase + li, budget, err));
-    const uint4* fr = kfr(key_slot(tb.keyA, ks));
-    // lane covers elements u*256 + 8*lane .. +7 (u < 4) of both experts; for
-    // each half of u the 32 weights stay in registers while the tokens stream
-    // past, 16 independent sums per lane
+  if (F.pdl) asm volatile("griddepcontrol.wait;" ::: "memory");  // x is the previous layer's output
+  stage_x<NT>(tb, xf, A.x, T, d, ctid);
+  cons_sync();
+  if (trace && ctid == 0) trace[1] = gtime();
+  {
+    const int OPW = d / 128;  // 8-element octets of K per warp
 #pragma unroll 1
-    for (int nt = 0; nt < NT; ++nt) {
-      float v[16];  // v[2 t + r]: token 8 nt + t, expert e0 + r
+    for (int i = 0; i < ne; ++i) {
+      bool landed;
+      const float* wr = reinterpret_cast<const float*>(acquire<NS>(tb, ring, i, budget, err, WS_ROUTER_SLOT, diag, landed));
+      if (trace && ctid == 0 && i == 0) trace[18] = gtime();
+      float v[16];
 #pragma unroll
       for (int q = 0; q < 16; ++q) v[q] = 0.f;
 #pragma unroll 1
-      for (int uh = 0; uh < 2; ++uh) {
-        float4 w0[2][2], w1[2][2];
+      for (int o = warp * OPW + lane; o < (warp + 1) * OPW; o += 32) {
+        const int k0 = o * 8;
+        const float4 a = *reinterpret_cast<const float4*>(wr + k0), b = *reinterpret_cast<const float4*>(wr + k0 + 4);
 #pragma unroll
-        for (int u2 = 0; u2 < 2; ++u2) {
-          const int kk = (2 * uh + u2) * 256 + lane * 8;
-          w0[u2][0] = *reinterpret_cast<const float4*>(wr + kk);
-          w0[u2][1] = *reinterpret_cast<const float4*>(wr + kk + 4);
-          w1[u2][0] = *reinterpret_cast<const float4*>(wr + KSEG + kk);
-          w1[u2][1] = *reinterpret_cast<const float4*>(wr + KSEG + kk + 4);
-        }
-        if (uh == 1 && nt == NT - 1) cons_release<NS>(tb, jbase + li);
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          float s0 = v[2 * t], s1 = v[2 * t + 1];
-#pragma unroll
-          for (int u2 = 0; u2 < 2; ++u2) {
-            const int kk = (2 * uh + u2) * 256 + lane * 8;
-            const int cc = kk >> 7, tg = (kk & 127) >> 5, mp = (kk & 31) >> 3;
-            const uint4 xv = fr[((cc * NT + nt) * 4 + mp) * 32 + t * 4 + tg];
-            const float2 p0 = __half22float2(*reinterpret_cast<const __half2*>(&xv.x));  // e0, e4
-            const float2 p1 = __half22float2(*reinterpret_cast<const __half2*>(&xv.y));  // e1, e5
-            const float2 p2 = __half22float2(*reinterpret_cast<const __half2*>(&xv.z));  // e2, e6
-            const float2 p3 = __half22float2(*reinterpret_cast<const __half2*>(&xv.w));  // e3, e7
-            const float4 a0 = w0[u2][0], a1 = w0[u2][1], b0 = w1[u2][0], b1 = w1[u2][1];
-            s0 = fmaf(a0.x, p0.x, s0); s0 = fmaf(a0.y, p1.x, s0); s0 = fmaf(a0.z, p2.x, s0); s0 = fmaf(a0.w, p3.x, s0);
-            s0 = fmaf(a1.x, p0.y, s0); s0 = fmaf(a1.y, p1.y, s0); s0 = fmaf(a1.z, p2.y, s0); s0 = fmaf(a1.w, p3.y, s0);
-            s1 = fmaf(b0.x, p0.x, s1); s1 = fmaf(b0.y, p1.x, s1); s1 = fmaf(b0.z, p2.x, s1); s1 = fmaf(b0.w, p3.x, s1);
-            s1 = fmaf(b1.x, p0.y, s1); s1 = fmaf(b1.y, p1.y, s1); s1 = fmaf(b1.z, p2.y, s1); s1 = fmaf(b1.w, p3.y, s1);
-          }
-          v[2 * t] = s0;
-          v[2 * t + 1] = s1;
+        for (int n = 0; n < 8 * NT; ++n) {  // x as staged (bf16: exact in fp32)
+          if (n >= T) break;
+          const uint4 xv = xf[n * (d / 8) + o];
+          float s = v[n];
+          s = fmaf(a.x, __uint_as_float(xv.x << 16), s); s = fmaf(a.y, __uint_as_float(xv.x & 0xffff0000u), s);
+          s = fmaf(a.z, __uint_as_float(xv.y << 16), s); s = fmaf(a.w, __uint_as_float(xv.y & 0xffff0000u), s);
+          s = fmaf(b.x, __uint_as_float(xv.z << 16), s); s = fmaf(b.y, __uint_as_float(xv.z & 0xffff0000u), s);
+          s = fmaf(b.z, __uint_as_float(xv.w << 16), s); s = fmaf(b.w, __uint_as_float(xv.w & 0xffff0000u), s);
+          v[n] = s;
         }
       }
+      release_read<NS>(tb, i, landed);
       // butterfly reduce-scatter over the warp: lanes 2q, 2q + 1 end with the
       // sum of v[q] over all lanes
 #pragma unroll
       for (int h = 8; h >= 1; h >>= 1) {
         const bool hi = lane & (2 * h);
 #pragma unroll
-        for (int j = 0; j < h; ++j) {
-          const float keep = hi ? v[j + h] : v[j], send = hi ? v[j] : v[j + h];
-          v[j] = keep + __shfl_xor_sync(0xffffffffu, send, 2 * h);
+        for (int q = 0; q < h; ++q) {
+          const float keep = hi ? v[q + h] : v[q], send = hi ? v[q] : v[q + h];
+          v[q] = keep + __shfl_xor_sync(0xffffffffu, send, 2 * h);
         }
       }
       v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
-      const int t = nt * 8 + (lane >> 2), r = (lane >> 1) & 1;
-      if ((lane & 1) == 0 && t < T) F.Lp[((size_t)ks * 16 + t) * E + e0 + r] = v[0];
+      if ((lane & 1) == 0) tb.u.rred[warp][i][lane >> 1] = v[0];
     }
-    fence_gpu();
-    __syncwarp();
-    bool last = false;
-    if (lane == 0) last = ticket_last(ctr + cm.tk_router + pr * CSTR, (unsigned)KS);
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (last) {
-      fence_gpu();
-      const int t = lane >> 1, r = lane & 1;
+    cons_sync();
+    if (ctid < ne * 16) {  // warps summed in order
+      const int i = ctid >> 4, t = ctid & 15;
       if (t < T) {
-        float part[8];
+        float s = 0.f;
 #pragma unroll
-        for (int s2 = 0; s2 < 8; ++s2) part[s2] = s2 < KS ? __ldcg(F.Lp + ((size_t)s2 * 16 + t) * E + e0 + r) : 0.f;
-        float v = 0.f;
-#pragma unroll
-        for (int s2 = 0; s2 < 8; ++s2) v += part[s2];
-        if (A.b_r) v += A.b_r[e0 + r];
-        F.logits[(size_t)t * E + e0 + r] = v;
+        for (int w = 0; w < NCW; ++w) s += tb.u.rred[w][i][t];
+        if (A.b_r) s += A.b_r[e_lo + i];
+        F.logits[(size_t)t * E + e_lo + i] = s;
       }
+    }
+    cons_sync();
+    if (ctid == 0) {
       fence_gpu();
-      __syncwarp();
-      if (lane == 0) atomicAdd(ctr + cm.done_router, 1u);
+      atomicAdd(ctr + cm.done_router, 1u);
+      if (trace) trace[2] = gtime();
     }
   }
-  jbase += nA1;
 
   // ------------------------------------------------------------ A2 W_in
-  #pragma unroll 1
-  for (int li = warp; li < nA2; li += NCW) {
-    const int i = a2lo + li, ks = i / (G * NRT_IN), rem = i % (G * NRT_IN), g = rem / NRT_IN, rt = rem % NRT_IN;
-    const unsigned char* sl = cons_wait<NS>(tb, ring, jbase + li, budget, err);
-    float acc[NT][4] = {};
-    mma_ring_rows_swz<NT>(sl, KSEG / 256, 0, reinterpret_cast<const uint16_t*>(sl + 16 * KSEG / 2), KSEG / 32,
-                          KSEG / 128, kfr(key_slot(tb.keyA, ks)), acc);
-    cons_release<NS>(tb, jbase + li);
-    float* Hp = A.Hp + ((size_t)ks * G + g) * 16 * L;
+  x_to_frags<NT>(xf, d, ctid);
+  if (trace && ctid == 0) trace[17] = gtime();
+  {
+    float acc[MAX_TILES][NT][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+    for (int i = 0; i < MAX_TILES; ++i)
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const int row = rt * 16 + gid + ((h & 2) ? 8 : 0), t = nt * 8 + 2 * tig + (h & 1);
-        if (t < T) Hp[(size_t)t * L + row] = acc[nt][h];
-      }
-    fence_gpu();
-    __syncwarp();
-    bool last = false;
-    if (lane == 0) last = ticket_last(ctr + cm.tk_win + (g * NRT_IN + rt) * CSTR, (unsigned)KS);
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (last) {  // sum the segment partials in order, straight into fp16 fragments
-      fence_gpu();
-      const int run = lane & 1, n = lane >> 1, k0 = rt * 16 + run * 8;
-      float e[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      if (n < T) {
-        float4 p[8][2];
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float* src = A.Hp + (((size_t)q * G + g) * 16 + n) * L + k0;
-          p[q][0] = q < KS ? __ldcg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
-          p[q][1] = q < KS ? __ldcg(reinterpret_cast<const float4*>(src + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        for (int h = 0; h < 4; ++h) acc[i][nt][h] = 0.f;
+    int c0, c1;
+    split(d / 128, warp, NCW, c0, c1);  // this warp's chunks of K (one piece)
+    const int pw = c0 / (PW / 128);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          e[0] += p[q][0].x; e[1] += p[q][0].y; e[2] += p[q][0].z; e[3] += p[q][0].w;
-          e[4] += p[q][1].x; e[5] += p[q][1].y; e[6] += p[q][1].z; e[7] += p[q][1].w;
+    for (int i = 0; i < MAX_TILES; ++i) {
+      if (i >= ntl) break;
+#pragma unroll 1
+      for (int p = 0; p < NPW; ++p) {
+        const int j = jA2 + i * NPW + p;
+        if (p == pw && c1 > c0) {
+          bool landed;
+          const unsigned char* sl = acquire<NS>(tb, ring, j, budget, err, WS_WIN_SLOT, diag, landed);
+          if (trace && ctid == 0 && i == 0) trace[19] = gtime();
+          mma_slot<NT>(sl, PW / 256, 0, reinterpret_cast<const uint16_t*>(sl + 8 * PW), PW / 32, c0 - p * (PW / 128),
+                       c1 - c0, xf + (size_t)c0 * FR, acc[i]);
+          release_read<NS>(tb, j, landed);
+        } else {  // not read by this warp: handed back once it landed (see release)
+          bool landed;
+          acquire<NS>(tb, ring, j, budget, err, WS_WIN_SLOT, diag, landed);
+          release_read<NS>(tb, j, landed);
         }
       }
-      if (n < 8 * NT) F.Hf[(size_t)g * (L / 128) * FR + entry_index<NT>(k0, n)] = pack_frag8(e);
+    }
+    cons_sync();  // every warp is done with x: its region takes the partials
+#pragma unroll
+    for (int i = 0; i < MAX_TILES; ++i) {
+      if (i >= ntl) break;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        pbuf[((i * NCW + warp) * NT + nt) * 32 + lane] = make_float4(acc[i][nt][0], acc[i][nt][1], acc[i][nt][2], acc[i][nt][3]);
+    }
+    cons_sync();
+    // H rows: thread (tile, token n, row r), warps summed in order; eight
+    // consecutive rows of a token gathered into one fragment entry
+#pragma unroll 1
+    for (int idx = ctid; idx < MAX_TILES * FR; idx += NCT) {  // FR = 16 rows x 8 NT tokens per tile
+      const int i = idx / FR, rem = idx % FR, n = rem >> 4, r = rem & 15;
+      if (i >= ntl) break;  // warp-uniform: a warp's 32 threads share i
+      const int ll = (r & 7) * 4 + ((n & 7) >> 1), h = 2 * (r >> 3) + (n & 1), nt = n >> 3;
+      const float* pf = reinterpret_cast<const float*>(pbuf);
+      const int tg = t_lo + i, g = tg / (L / 16), rt = tg % (L / 16);
+      float s = 0.f;
+#pragma unroll
+      for (int w = 0; w < NCW; ++w) s += pf[(((i * NCW + w) * NT + nt) * 32 + ll) * 4 + h];
+      if (F.hl && n < T) s += __ldcg(F.hl + ((size_t)g * 16 + n) * L + rt * 16 + r);  // the LoRA branch
+      float e[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) e[q] = __shfl_sync(0xffffffffu, s, (lane & ~7) + q);
+      if ((r & 7) == 0) {
+        F.Hf[(size_t)g * CL * FR + entry_index<NT>(rt * 16 + (r & 8), n)] = pack_frag8(e);
+      }
+    }
+    cons_sync();
+    if (ctid == 0) {
       fence_gpu();
-      __syncwarp();
-      if (lane == 0) atomicAdd(ctr + cm.done_in + g * CSTR, 1u);
+#pragma unroll 1
+      for (int i = 0; i < ntl; ++i) atomicAdd(ctr + cm.done_in + ((t_lo + i) / (L / 16)) * CSTR, 1u);
+      if (trace) trace[3] = gtime();
     }
   }
-  jbase += nA2;
 
   // ------------------------------------------------------------ routing
-  // Every CTA routes all tokens itself: top-k of each token (a warp per
-  // token), then the tables. The warps without a router item finish the A
-  // phase first; they route while the others finish their W_in items.
-  const int rw0 = nA1 < NCW - 1 ? nA1 : NCW - 1, nrw = NCW - rw0;
-  if (warp >= rw0) {
-    const int rt = (warp - rw0) * 32 + lane;
-    if (rt < 16) tb.emask[rt] = 0u;
-    if (warp == rw0) wait_counts(lane == 0 ? ctr + cm.done_router : nullptr, (unsigned)NPAIR, budget, err);
-    route_sync(nrw);
-#pragma unroll 1
-    for (int tw = warp - rw0; tw < T; tw += nrw) {
-      const float2 sw = topk_warp_thr(F.logits + (size_t)tw * E, E, k, tb.tkscr[warp]);
-      if (lane < k) {
-        const int e = __float_as_int(sw.x);
-        tb.idx[tw * 16 + lane] = e;
-        tb.w[tw * 16 + lane] = sw.y;
-        atomicOr(&tb.emask[e >> 5], 1u << (e & 31));
-        if (c == 0) {
-          A.idx[tw * k + lane] = e;
-          A.w[tw * k + lane] = sw.y;
-        }
+  // Every CTA routes all tokens itself: a warp per token selects the top-k
+  // (topk.cuh), then one warp builds the tables and the work split.
+  if (ctid == 0) wait_ge(tb, ctr + cm.done_router, (unsigned)nC, budget, err, WS_LOGITS, diag);
+  cons_sync();
+  if (trace && ctid == 0) trace[15] = gtime();
+  if (warp < T) {
+    const float2 sw = topk_warp_thr(F.logits + (size_t)warp * E, E, k, tb.u.tkscr[warp]);
+    if (lane < k) {
+      const int e = __float_as_int(sw.x);
+      tb.idx[warp * 16 + lane] = e;
+      tb.w[warp * 16 + lane] = sw.y;
+      atomicOr(&tb.emask[e >> 5], 1u << (e & 31));
+      if (c == 0) {
+        A.idx[warp * k + lane] = e;
+        A.w[warp * k + lane] = sw.y;
       }
-    }
-    route_sync(nrw);
-    if (warp == rw0) {
-      build_tables(tb, epg);
-      if (lane == 0) {
-        __threadfence_block();
-        tb.tables_ready = 1;  // the producer may issue the expert weights
-      }
-      // the B phase's groups and the completion of their H, while the other
-      // warps finish the A phase
-      int lo, hi;
-      split(tb.n_act * (f / 16), c, nC, lo, hi);
-      if (lane == 0) collect_keys(tb.key, lo, hi, [&](int i) { return tb.elist[i / (f / 16)] / epg; }, err);
-      __syncwarp();
-      wait_counts(lane < KEYS && tb.key[lane] >= 0 ? ctr + cm.done_in + tb.key[lane] * CSTR : nullptr, (unsigned)NRT_IN,
-                  budget, err);
     }
   }
   cons_sync();
-  const int n_act = tb.n_act, n_actg = tb.n_actg;
+  if (trace && ctid == 0) trace[11] = gtime();
+  if (warp == 0) {
+    build_tables(tb, epg);
+    if (trace && lane == 0) trace[16] = gtime();
+    plan(tb, c, nC, NSF, L, d);
+    if (lane == 0) mbar_arrive(&tb.tbar);  // the producer may stream the expert weights
+  }
+  cons_sync();
+  if (trace && ctid == 0) trace[4] = gtime();
+  const int n_actg = tb.n_actg;
 
-  // ------------------------------------------------------------ B gate/up
+  // ------------------------------------------------------------ B expert units
+  // Per unit q: the 16 gate / up tasks -> partials; one CTA barrier; then
+  // every thread forms one element of the unit's slice v = w silu(gate h) up h
+  // (the gate and up partials summed in K-quarter order), and the warps
+  // contract the previous unit's slice with its Down columns. The partials and
+  // slices are double-buffered, so the barrier of unit q + 1 also separates
+  // the slice writes of unit q from their reads.
   {
-    int lo, hi;
-    split(n_act * (f / 16), c, nC, lo, hi);  // keys collected, H completion awaited by the routing
-    #pragma unroll 1
-    for (int s = 0; s < KEYS; ++s)
-      if (tb.key[s] >= 0) copy_frags(kfr(s), F.Hf + (size_t)tb.key[s] * (L / 128) * FR, (L / 128) * FR, ctid);
-    cons_sync();
-    #pragma unroll 1
-    for (int li = warp; li < hi - lo; li += NCW) {
-      const int i = lo + li, es = i / (f / 16), rt = i % (f / 16), e = tb.elist[es];
-      const uint4* fr = kfr(key_slot(tb.key, e / epg));
-      float ag[NT][4] = {}, au[NT][4] = {};
-      const unsigned char* sg = cons_wait<NS>(tb, ring, jbase + 2 * li, budget, err);
-      const unsigned char* su = cons_wait<NS>(tb, ring, jbase + 2 * li + 1, budget, err);
-      mma_ring_rows_swz2<NT>(sg, reinterpret_cast<const uint16_t*>(sg + 16 * L / 2), su,
-                             reinterpret_cast<const uint16_t*>(su + 16 * L / 2), L / 256, L / 32, L / 128, fr, ag, au);
-      cons_release<NS>(tb, jbase + 2 * li);
-      cons_release<NS>(tb, jbase + 2 * li + 1);
-      // v = w(t, e) * silu(gate) * up, as the down projection's fragments;
-      // lane t < T looks up w(t, e), the other lanes take it by shuffle
-      const float wl = lane < T ? route_weight(tb, lane, e, k) : 0.f;
+    const int u_lo = tb.u_lo, nu = tb.u_hi - tb.u_lo;
+    const int mat = warp >> 3, mt = (warp >> 2) & 1, cw = warp & 3;
+    int gc0, gc1;
+    split(CL, cw, 4, gc0, gc1);  // this warp's K chunks of its gate / up tile
+    float zacc[MAX_MPW][NT][4];
+#pragma unroll
+    for (int m = 0; m < MAX_MPW; ++m)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const int t = nt * 8 + 2 * tig + h2;
-          const float wt = __shfl_sync(0xffffffffu, wl, t);
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const float a = ag[nt][hh * 2 + h2];
-            ag[nt][hh * 2 + h2] = wt != 0.f ? wt * a * __frcp_rn(1.f + __expf(-a)) * au[nt][hh * 2 + h2] : 0.f;
-          }
-        }
-      float ev[8];
-      acc_to_entry<NT>(ag, ev);
-      const int run = lane & 1, n = lane >> 1;
-      if (n < 8 * NT) F.Vf[(size_t)es * (f / 128) * FR + entry_index<NT>(rt * 16 + run * 8, n)] = pack_frag8(ev);
-      fence_gpu();
-      __syncwarp();
-      if (lane == 0) atomicAdd(ctr + cm.done_gu + es * CSTR, 1u);
-    }
-    jbase += 2 * (hi - lo);
-  }
-
-  // ------------------------------------------------------------ C down
-  {
-    int lo, hi;
-    split(n_act * NRB, c, nC, lo, hi);
-    cons_sync();
-    if (ctid == 0) collect_keys(tb.key, lo, hi, [&](int i) { return i / NRB; }, err);
-    cons_sync();
-    if (warp == 0)
-      wait_counts(lane < KEYS && tb.key[lane] >= 0 ? ctr + cm.done_gu + tb.key[lane] * CSTR : nullptr, (unsigned)(f / 16), budget,
-                  err);
-    cons_sync();
-    #pragma unroll 1
-    for (int s = 0; s < KEYS; ++s)
-      if (tb.key[s] >= 0) copy_frags(kfr(s), F.Vf + (size_t)tb.key[s] * (f / 128) * FR, (f / 128) * FR, ctid);
-    cons_sync();
-    // A warp's items are contracted back to back, then their partials are
-    // published with one fence: the second item does not wait on the first
-    // one's ticket and reduction
-    auto c_compute = [&](int li) {
-      const int i = lo + li, es = i / NRB, rb = i % NRB;
-      const uint4* fr = kfr(key_slot(tb.key, es));
-      const unsigned char* sl = cons_wait<NS>(tb, ring, jbase + li, budget, err);
-      float* Zp = F.Zp + (size_t)es * 16 * L;
+        for (int h = 0; h < 4; ++h) zacc[m][nt][h] = 0.f;
+    int hg = -1;
 #pragma unroll 1
-      for (int mt = 0; mt < DR / 16; ++mt) {
-        float acc[NT][4] = {};
-        mma_ring_rows_swz<NT>(sl, f / 256, mt * 16, reinterpret_cast<const uint16_t*>(sl + DR * f / 2), f / 32, f / 128,
-                              fr, acc);
+    for (int q = 0; q <= nu; ++q) {
+      const int par = q & 1;
+      if (q < nu) {  // ---- gate / up of unit q
+        const int u = u_lo + q, e = tb.elist[u / NSF], g = e / epg;
+        if (g != hg) {  // this group's H into shared memory
+          cons_sync();
+          if (ctid == 0) wait_ge(tb, ctr + cm.done_in + g * CSTR, (unsigned)(L / 16), budget, err, WS_H, diag);
+          cons_sync();
+          copy_frags(xf, F.Hf + (size_t)g * CL * FR, CL * FR, ctid);
+          cons_sync();
+          if (trace && ctid == 0 && hg < 0) trace[5] = gtime();
+          hg = g;
+        }
+        const int jg = jB + 3 * q;
+        {  // the other matrix's chunk is not read by this warp: handed back once it landed
+          bool landed;
+          acquire<NS>(tb, ring, jg + 1 - mat, budget, err, WS_GU_SLOT, diag, landed);
+          release_read<NS>(tb, jg + 1 - mat, landed);
+        }
+        float a[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const int row = rb * DR + mt * 16 + gid + ((h & 2) ? 8 : 0), t = nt * 8 + 2 * tig + (h & 1);
-            if (t < T) Zp[(size_t)t * L + row] = acc[nt][h];
+          for (int h = 0; h < 4; ++h) a[nt][h] = 0.f;
+        {
+          bool landed;
+          const unsigned char* sl = acquire<NS>(tb, ring, jg + mat, budget, err, WS_GU_SLOT, diag, landed);
+          if (trace && ctid == 0 && q == 0) trace[21] = gtime();
+          mma_slot<NT>(sl, L / 256, 16 * mt, reinterpret_cast<const uint16_t*>(sl + 16 * L), L / 32, gc0, gc1 - gc0,
+                       xf + (size_t)gc0 * FR, a);
+          release_read<NS>(tb, jg + mat, landed);
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          pbuf[((par * NCW + warp) * NT + nt) * 32 + lane] = make_float4(a[nt][0], a[nt][1], a[nt][2], a[nt][3]);
+      }
+      cons_sync();
+      if (trace && ctid == 0 && q == 0) trace[12] = gtime();
+      if (q < nu && ctid < 256 * NT) {  // ---- unit q's slice, one element per thread
+        const int e = tb.elist[(u_lo + q) / NSF];
+        const int h = ctid & 3, ln = (ctid >> 2) & 31, r2 = ctid >> 7, nt = r2 % NT, m2 = r2 / NT;
+        const float* pf = reinterpret_cast<const float*>(pbuf);
+        float gs = 0.f, us = 0.f;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          gs += pf[((((par * NCW + m2 * 4 + q4) * NT + nt) * 32 + ln) << 2) + h];
+          us += pf[((((par * NCW + 8 + m2 * 4 + q4) * NT + nt) * 32 + ln) << 2) + h];
+        }
+        const int r = 16 * m2 + (ln >> 2) + 8 * (h >> 1), n = nt * 8 + 2 * (ln & 3) + (h & 1);
+        const float wv = route_weight(tb, n, e);
+        const float v = wv != 0.f ? wv * gs * __frcp_rn(1.f + __expf(-gs)) * us : 0.f;
+        const int el = r & 7, ent = (n >> 3) * 32 + (n & 7) * 4 + (r >> 3);
+        reinterpret_cast<__half*>(vbuf + par * NT * 32)[ent * 8 + (el < 4 ? 2 * el : 2 * (el - 4) + 1)] =
+            __float2half_rn(v);
+      }
+      if (q >= 1) {  // ---- Down of unit q - 1 (its slice was formed before this unit's barrier)
+        const int qq = q - 1, pq = qq & 1, u = u_lo + qq, es = u / NSF;
+        const int jd = jB + 3 * qq + 2;
+        bool landed;
+        const unsigned char* sl = acquire<NS>(tb, ring, jd, budget, err, WS_DOWN_SLOT, diag, landed);
+        const uint32_t* wsl = reinterpret_cast<const uint32_t*>(sl);
+        const uint16_t* sc = reinterpret_cast<const uint16_t*>(sl + 16 * L);
+#pragma unroll
+        for (int m = 0; m < MAX_MPW; ++m)
+          if (m < MPW) mma_slice32<NT>(wsl, sc, warp * MPW + m, vbuf + pq * NT * 32, zacc[m]);
+        release_read<NS>(tb, jd, landed);
+        if (trace && ctid == 0 && qq == 0) trace[14] = gtime();
+        // the last unit of its group in this CTA: write the group's partial of Z
+        const int g = tb.elist[es] / epg;
+        const bool flush = qq + 1 == nu || tb.elist[(u + 1) / NSF] / epg != g;
+        if (flush) {
+          const int gi = group_slot(tb, es);
+          const int slot = tb.gpbase[gi] + busy_ctas(tb.gplo[gi], c, tb.n_act * NSF, nC);
+          float* zp = F.Zpart + (size_t)slot * 16 * L;
+#pragma unroll
+          for (int m = 0; m < MAX_MPW; ++m) {
+            if (m >= MPW) break;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                const int row = 16 * (warp * MPW + m) + gid + 8 * (h >> 1), n = nt * 8 + 2 * tig + (h & 1);
+                if (n < T) zp[(size_t)n * L + row] = zacc[m][nt][h];
+                zacc[m][nt][h] = 0.f;
+              }
           }
-      }
-      cons_release<NS>(tb, jbase + li);
-    };
-    // block (group, row block) of item li: its ticket and its group's expert slots
-    auto c_block = [&](int li, int& g, int& rb, int& s0, int& s1) {
-      const int i = lo + li, es = i / NRB;
-      rb = i % NRB;
-      g = tb.elist[es] / epg;
-      int gi = 0;
-      #pragma unroll 1
-      while (gi < n_actg && tb.glist[gi] != g) ++gi;
-      s0 = tb.gslot0[gi];
-      s1 = tb.gslot0[gi + 1];
-    };
-    // Z rows of a block: the group's experts in ascending order, into fragments
-    auto c_reduce = [&](int g, int rb, int s0, int s1) {
-        // fragment entries per lane: DR/8 runs x 8 NT tokens over 32 lanes;
-        // the experts' partials are loaded QB at a time, all loads first
-        constexpr int PE = DR / 8 * 8 * NT / 32, QB = NT == 1 ? 12 : 4;
-        float ev[PE][8];
-#pragma unroll
-        for (int u = 0; u < PE; ++u)
-#pragma unroll
-          for (int h = 0; h < 8; ++h) ev[u][h] = 0.f;
-#pragma unroll 1
-        for (int sl2 = s0; sl2 < s1; sl2 += QB) {
-          float4 p[QB][PE][2];
-#pragma unroll
-          for (int q = 0; q < QB; ++q)
-#pragma unroll
-            for (int u = 0; u < PE; ++u) {
-              const int en = lane + 32 * u, run = en % (DR / 8), n = en / (DR / 8);
-              const float* src = F.Zp + ((size_t)(sl2 + q) * 16 + n) * L + rb * DR + run * 8;
-              const bool v = n < T && sl2 + q < s1;
-              p[q][u][0] = v ? __ldcg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
-              p[q][u][1] = v ? __ldcg(reinterpret_cast<const float4*>(src + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-          for (int q = 0; q < QB; ++q)
-#pragma unroll
-            for (int u = 0; u < PE; ++u) {
-              ev[u][0] += p[q][u][0].x; ev[u][1] += p[q][u][0].y; ev[u][2] += p[q][u][0].z; ev[u][3] += p[q][u][0].w;
-              ev[u][4] += p[q][u][1].x; ev[u][5] += p[q][u][1].y; ev[u][6] += p[q][u][1].z; ev[u][7] += p[q][u][1].w;
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < PE; ++u) {
-          const int en = lane + 32 * u, run = en % (DR / 8), n = en / (DR / 8);
-          if (n < 8 * NT)
-            F.Zf[(size_t)g * (L / 128) * FR + entry_index<NT>(rb * DR + run * 8, n)] = pack_frag8(ev[u]);
-        }
-    };
-    #pragma unroll 1
-    for (int li = warp; li < hi - lo; li += 2 * NCW) {
-      const bool two = li + NCW < hi - lo;
-      #pragma unroll 1
-      for (int q = 0; q < (two ? 2 : 1); ++q) c_compute(li + q * NCW);  // one copy of the code
-      fence_gpu();
-      __syncwarp();
-      // both tickets in flight at once; a block's last arriver reduces it
-      int g0, rb0, a0, b0, g1 = 0, rb1 = 0, a1 = 0, b1 = 0;
-      c_block(li, g0, rb0, a0, b0);
-      if (two) c_block(li + NCW, g1, rb1, a1, b1);
-      bool l0 = false, l1 = false;
-      if (lane == 0) {
-        const unsigned o0 = atomicAdd(ctr + cm.tk_down + (g0 * NRB + rb0) * CSTR, 1u);
-        const unsigned o1 = two ? atomicAdd(ctr + cm.tk_down + (g1 * NRB + rb1) * CSTR, 1u) : 0u;
-        l0 = o0 == (unsigned)(b0 - a0 - 1);
-        l1 = two && o1 == (unsigned)(b1 - a1 - 1);
-      }
-      l0 = __shfl_sync(0xffffffffu, l0, 0);
-      l1 = __shfl_sync(0xffffffffu, l1, 0);
-      if (l0 || l1) {
-        fence_gpu();
-        #pragma unroll 1
-        for (int q = 0; q < 2; ++q)
-          if (q ? l1 : l0) c_reduce(q ? g1 : g0, q ? rb1 : rb0, q ? a1 : a0, q ? b1 : b0);
-        fence_gpu();
-        __syncwarp();
-        if (lane == 0) {
-          if (l0) atomicAdd(ctr + cm.done_down + g0 * CSTR, 1u);
-          if (l1) atomicAdd(ctr + cm.done_down + g1 * CSTR, 1u);
+          fence_gpu();
+          __syncwarp();
+          if (lane == 0) atomicAdd(ctr + cm.done_part + g * CSTR, 1u);
         }
       }
     }
-    jbase += hi - lo;
+  }
+
+  if (trace && ctid == 0) trace[6] = gtime();
+  // ------------------------------------------------------------ C Z reduce
+  {
+    const int z_lo = tb.z_lo, nz = tb.z_hi - tb.z_lo;
+    const int wg = warp >> 2, qt = warp & 3, run = lane & 1, n = lane >> 1;
+#pragma unroll 1
+    for (int r0 = 0; r0 < nz; r0 += 4) {
+      const int zq = r0 + wg;
+      if (zq < nz) {
+        const int it = z_lo + zq, gi = it / (L / 16), rb = it % (L / 16), g = tb.glist[gi];
+        const int P = tb.gpn[gi], base = tb.gpbase[gi];
+        warp_wait_ge(tb, ctr + cm.done_part + g * CSTR, (unsigned)(NCW * P), budget, err, WS_ZPART, diag);
+        int p0, p1;
+        split(P, qt, 4, p0, p1);
+        float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
+        if (n < T) {
+#pragma unroll 1
+          for (int p = p0; p < p1; p += 4) {
+            float4 v[4][2];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const float* src = F.Zpart + ((size_t)(base + p + q4) * 16 + n) * L + rb * 16 + run * 8;
+              const bool ok = p + q4 < p1;
+              v[q4][0] = ok ? __ldcg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+              v[q4][1] = ok ? __ldcg(reinterpret_cast<const float4*>(src + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              s0.x += v[q4][0].x; s0.y += v[q4][0].y; s0.z += v[q4][0].z; s0.w += v[q4][0].w;
+              s1.x += v[q4][1].x; s1.y += v[q4][1].y; s1.z += v[q4][1].z; s1.w += v[q4][1].w;
+            }
+          }
+        }
+        zred[((wg * 4 + qt) * 32 + lane) * 2] = s0;
+        zred[((wg * 4 + qt) * 32 + lane) * 2 + 1] = s1;
+        __threadfence_block();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(&tb.tk_z[wg], 1) == 3;
+        if (__shfl_sync(0xffffffffu, last, 0)) {  // quarters summed in order
+          __threadfence_block();
+          float e[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const float4 a = zred[((wg * 4 + q4) * 32 + lane) * 2], b = zred[((wg * 4 + q4) * 32 + lane) * 2 + 1];
+            e[0] += a.x; e[1] += a.y; e[2] += a.z; e[3] += a.w; e[4] += b.x; e[5] += b.y; e[6] += b.z; e[7] += b.w;
+          }
+          if (lane == 0) tb.tk_z[wg] = 0;
+          if (n < 8 * NT) F.Zf[(size_t)g * CL * FR + entry_index<NT>(rb * 16 + run * 8, n)] = pack_frag8(e);
+          if (F.zlin && n < T) {  // Z in fp32 for the LoRA branch
+            float* zl = F.zlin + ((size_t)g * 16 + n) * L + rb * 16 + run * 8;
+            *reinterpret_cast<float4*>(zl) = make_float4(e[0], e[1], e[2], e[3]);
+            *reinterpret_cast<float4*>(zl + 4) = make_float4(e[4], e[5], e[6], e[7]);
+          }
+          fence_gpu();
+          __syncwarp();
+          if (lane == 0) atomicAdd(ctr + cm.done_z + g * CSTR, 1u);
+        }
+      }
+      cons_sync();
+    }
   }
 
   // ------------------------------------------------------------ D W_out
+  // Per item (group g, 32 rows of Y[g]): the 16 warp tasks -> partials; one
+  // CTA barrier; every thread sums one element over the 8 K-eighths in order
+  // and writes it to Y[g]. After the CTA's last item, one ticket per item
+  // (behind a release fence); the CTA that brings a row block's count to the
+  // number of routed groups sums the groups in ascending order (+ residual)
+  // into y.
+  if (trace && ctid == 0) trace[7] = gtime();
+  if (ctid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   {
-    int lo, hi;
-    split(n_actg * NRT_OUT, c, nC, lo, hi);
-    cons_sync();
-    if (ctid == 0) collect_keys(tb.key, lo, hi, [&](int i) { return i / NRT_OUT; }, err);
-    cons_sync();
-    if (warp == 0)
-      wait_counts(lane < KEYS && tb.key[lane] >= 0 ? ctr + cm.done_down + tb.glist[tb.key[lane]] * CSTR : nullptr, (unsigned)NRB,
-                  budget, err);
-    cons_sync();
-    #pragma unroll 1
-    for (int s = 0; s < KEYS; ++s)
-      if (tb.key[s] >= 0)
-        copy_frags(kfr(s), F.Zf + (size_t)tb.glist[tb.key[s]] * (L / 128) * FR, (L / 128) * FR, ctid);
-    cons_sync();
-    #pragma unroll 1
-    for (int li = warp; li < hi - lo; li += NCW) {
-      const int i = lo + li, gi = i / NRT_OUT, rt = i % NRT_OUT, g = tb.glist[gi];
-      const unsigned char* sl = cons_wait<NS>(tb, ring, jbase + li, budget, err);
-      float acc[NT][4] = {};
-      mma_ring_rows_swz<NT>(sl, L / 256, 0, reinterpret_cast<const uint16_t*>(sl + 16 * L / 2), L / 32, L / 128,
-                            kfr(key_slot(tb.key, gi)), acc);
-      cons_release<NS>(tb, jbase + li);
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const int row = rt * 16 + gid + ((h & 2) ? 8 : 0), t = nt * 8 + 2 * tig + (h & 1);
-          if (t < T) A.Yp[((size_t)g * 16 + t) * d + row] = acc[nt][h];
+    const int o_lo = tb.o_lo, no = tb.o_hi - tb.o_lo, jD = jB + 3 * (tb.u_hi - tb.u_lo);
+    const int wm = warp >> 3;
+    int oc0, oc1;
+    split(CL, warp & 7, 8, oc0, oc1);
+    int zg = -1;
+#pragma unroll 1
+    for (int q = 0; q <= no; ++q) {
+      const int par = q & 1;
+      if (q < no) {
+        const int it = o_lo + q, g = tb.glist[it / (d / 32)];
+        if (g != zg) {  // this group's Z into shared memory
+          cons_sync();
+          if (ctid == 0) wait_ge(tb, ctr + cm.done_z + g * CSTR, (unsigned)(L / 16), budget, err, WS_Z, diag);
+          cons_sync();
+          copy_frags(xf, F.Zf + (size_t)g * CL * FR, CL * FR, ctid);
+          cons_sync();
+          if (trace && ctid == 0 && zg < 0) trace[8] = gtime();
+          zg = g;
         }
-      fence_gpu();
-      __syncwarp();
-      bool last = false;
-      if (lane == 0) last = ticket_last(ctr + cm.tk_wout + rt * CSTR, (unsigned)n_actg);
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {  // combine in ascending group order: lane -> 4 rows x 1 token, one float4 per group
+        float a[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int h = 0; h < 4; ++h) a[nt][h] = 0.f;
+        bool landed;
+        const unsigned char* sl = acquire<NS>(tb, ring, jD + q, budget, err, WS_WOUT_SLOT, diag, landed);
+        if (trace && ctid == 0 && q == 0) trace[25] = gtime();
+        mma_slot<NT>(sl, L / 256, 16 * wm, reinterpret_cast<const uint16_t*>(sl + 16 * L), L / 32, oc0, oc1 - oc0,
+                     xf + (size_t)oc0 * FR, a);
+        release_read<NS>(tb, jD + q, landed);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          pbuf[((par * NCW + warp) * NT + nt) * 32 + lane] = make_float4(a[nt][0], a[nt][1], a[nt][2], a[nt][3]);
+      }
+      if (q > 0 && ctid < 256 * NT) {  // ---- item q - 1's rows of Y[g], one element per thread
+        const int qq = q - 1, pq = qq & 1, it = o_lo + qq, g = tb.glist[it / (d / 32)], ot = it % (d / 32);
+        const int h = ctid & 3, ln = (ctid >> 2) & 31, r2 = ctid >> 7, nt = r2 % NT, m2 = r2 / NT;
+        const float* pf = reinterpret_cast<const float*>(pbuf);
+        float s = 0.f;
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) s += pf[((((pq * NCW + m2 * 8 + q8) * NT + nt) * 32 + ln) << 2) + h];
+        const int row = ot * 32 + 16 * m2 + (ln >> 2) + 8 * (h >> 1), n = nt * 8 + 2 * (ln & 3) + (h & 1);
+        if (n < T) F.Yp[((size_t)g * 16 + n) * d + row] = s;
+      }
+      cons_sync();
+    }
+    if (!F.no_combine) {  // (with the LoRA branch, lora_out combines the groups)
+      // the tickets: each behind a release fence, cumulative over the barrier above
+      if (ctid < no) {
+        const int ot = (o_lo + ctid) % (d / 32);
         fence_gpu();
+        const unsigned old = atomicAdd(ctr + cm.tk_wout + ot * CSTR, 1u);
+        tb.fin[ctid] = old == (unsigned)(n_actg - 1) ? (int16_t)ot : (int16_t)-1;
+        if (old == (unsigned)(n_actg - 1)) fence_gpu();
+      }
+      cons_sync();
+      // every group of a finished row block is in: combine in ascending group order
 #pragma unroll 1
-        for (int q = lane; q < 4 * T; q += 32) {
-          const int rq = q & 3, t = q >> 2, row = rt * 16 + rq * 4;
-          float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int qd = ctid; qd < no * 8 * T; qd += NCT) {
+        const int ot = tb.fin[qd / (8 * T)];
+        if (ot < 0) continue;
+        const int rem = qd % (8 * T), n = rem >> 3, row = ot * 32 + (rem & 7) * 4;
+        float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
-          for (int g0 = 0; g0 < n_actg; g0 += 8) {
-            float4 p4[8];
+        for (int g0 = 0; g0 < n_actg; g0 += 8) {
+          float4 p4[8];
 #pragma unroll
-            for (int gg = 0; gg < 8; ++gg)
-              p4[gg] = g0 + gg < n_actg
-                           ? __ldcg(reinterpret_cast<const float4*>(A.Yp + ((size_t)tb.glist[g0 + gg] * 16 + t) * d + row))
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int gg = 0; gg < 8; ++gg)
+            p4[gg] = g0 + gg < n_actg
+                         ? __ldcg(reinterpret_cast<const float4*>(F.Yp + ((size_t)tb.glist[g0 + gg] * 16 + n) * d + row))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int gg = 0; gg < 8; ++gg) {
-              acc4.x += p4[gg].x; acc4.y += p4[gg].y; acc4.z += p4[gg].z; acc4.w += p4[gg].w;
-            }
+          for (int gg = 0; gg < 8; ++gg) {
+            acc4.x += p4[gg].x; acc4.y += p4[gg].y; acc4.z += p4[gg].z; acc4.w += p4[gg].w;
           }
-          if (A.residual) {
-            const uint2 rb = *reinterpret_cast<const uint2*>(A.residual + (size_t)t * d + row);
-            acc4.x += __uint_as_float(rb.x << 16);
-            acc4.y += __uint_as_float(rb.x & 0xffff0000u);
-            acc4.z += __uint_as_float(rb.y << 16);
-            acc4.w += __uint_as_float(rb.y & 0xffff0000u);
-          }
-          uint2 o;
-          o.x = (uint32_t)f32_to_bf16_rne(acc4.x) | ((uint32_t)f32_to_bf16_rne(acc4.y) << 16);
-          o.y = (uint32_t)f32_to_bf16_rne(acc4.z) | ((uint32_t)f32_to_bf16_rne(acc4.w) << 16);
-          *reinterpret_cast<uint2*>(A.y + (size_t)t * d + row) = o;
         }
+        if (F.round_first) {  // the layer's output is rounded before the residual is added
+          acc4.x = bf16_to_f32(f32_to_bf16_rne(acc4.x));
+          acc4.y = bf16_to_f32(f32_to_bf16_rne(acc4.y));
+          acc4.z = bf16_to_f32(f32_to_bf16_rne(acc4.z));
+          acc4.w = bf16_to_f32(f32_to_bf16_rne(acc4.w));
+        }
+        if (A.residual) {
+          const uint2 rb = *reinterpret_cast<const uint2*>(A.residual + (size_t)n * d + row);
+          acc4.x += __uint_as_float(rb.x << 16);
+          acc4.y += __uint_as_float(rb.x & 0xffff0000u);
+          acc4.z += __uint_as_float(rb.y << 16);
+          acc4.w += __uint_as_float(rb.y & 0xffff0000u);
+        }
+        uint2 o;
+        o.x = (uint32_t)f32_to_bf16_rne(acc4.x) | ((uint32_t)f32_to_bf16_rne(acc4.y) << 16);
+        o.y = (uint32_t)f32_to_bf16_rne(acc4.z) | ((uint32_t)f32_to_bf16_rne(acc4.w) << 16);
+        *reinterpret_cast<uint2*>(A.y + (size_t)n * d + row) = o;
       }
     }
   }
+  if (trace && ctid == 0) trace[9] = gtime();
   end_sync();
 }
 
 // ===================================================================== host
-size_t fused_counter_words(int d, int E, int G, int L) { return 2 * (size_t)ctr_map(d, E, G, L).n; }
+size_t fused_counter_words(int d, int E, int G, int L) {
+  (void)E;
+  (void)L;
+  return 2 * (size_t)ctr_map(d, G).n;
+}
+
+size_t fused_zpart_bytes(int G, int L, int grid) { return (size_t)(grid + G) * 16 * L * 4; }
+size_t fused_diag_bytes(int grid) { return (size_t)(1 + 32 * grid) * 8; }
 
 namespace {
 // packed int4 [rows][K/2] as [rows][K/256][128 B], box {128, lines, box_rows}
@@ -1019,40 +1137,71 @@ bool map_s(CUtensorMap* m, const uint16_t* s, long long rows, int K, int box_col
 }
 }  // namespace
 
-bool fused_make_maps(const DecodeArgs& A, DecodeMaps* mp) {
-  if (!tmap_encode_fn() || !A.W_r) return false;
+bool fused_make_maps(const DecodeArgs& A, const uint8_t* dsl_q, const uint16_t* dsl_s, DecodeMaps* mp) {
+  if (!tmap_encode_fn() || !A.W_r || !dsl_q || !dsl_s) return false;
   const int d = A.d, E = A.E, G = A.G, L = A.L, f = A.f;
-  if (d % KSEG != 0 || L % 256 != 0 || f % 256 != 0) return false;
+  const int PW = d < 2048 ? d : 2048;
   bool ok = true;
-  {
+  {  // W_r as [E][d/256][256] fp32, one whole row per box
     const cuuint64_t dims[3] = {256, (cuuint64_t)(d / 256), (cuuint64_t)E};
     const cuuint64_t strides[2] = {1024, (cuuint64_t)d * 4};
-    const cuuint32_t box[3] = {256, KSEG / 256, 2};
+    const cuuint32_t box[3] = {256, (cuuint32_t)(d / 256), 1};
     ok = ok && tmap_encode(&mp->wr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, A.W_r, dims, strides, box,
                            CU_TENSOR_MAP_SWIZZLE_NONE);
   }
-  ok = ok && map_q(&mp->win_q, A.W_in_q, (long long)G * L, d, KSEG / 256, 16);
-  ok = ok && map_s(&mp->win_s, A.W_in_s, (long long)G * L, d, KSEG / 32, 16);
-  ok = ok && map_q(&mp->gate_q, A.gate_q, (long long)E * f, L, L / 256, 16);
-  ok = ok && map_s(&mp->gate_s, A.gate_s, (long long)E * f, L, L / 32, 16);
-  ok = ok && map_q(&mp->up_q, A.up_q, (long long)E * f, L, L / 256, 16);
-  ok = ok && map_s(&mp->up_s, A.up_s, (long long)E * f, L, L / 32, 16);
-  ok = ok && map_q(&mp->down_q, A.down_q, (long long)E * L, f, f / 256, DR);
-  ok = ok && map_s(&mp->down_s, A.down_s, (long long)E * L, f, f / 32, DR);
-  ok = ok && map_q(&mp->wout_q, A.W_out_q, (long long)G * d, L, L / 256, 16);
-  ok = ok && map_s(&mp->wout_s, A.W_out_s, (long long)G * d, L, L / 32, 16);
+  ok = ok && map_q(&mp->win_q, A.W_in_q, (long long)G * L, d, PW / 256, 16);
+  ok = ok && map_s(&mp->win_s, A.W_in_s, (long long)G * L, d, PW / 32, 16);
+  ok = ok && map_q(&mp->gate_q, A.gate_q, (long long)E * f, L, L / 256, FS);
+  ok = ok && map_s(&mp->gate_s, A.gate_s, (long long)E * f, L, L / 32, FS);
+  ok = ok && map_q(&mp->up_q, A.up_q, (long long)E * f, L, L / 256, FS);
+  ok = ok && map_s(&mp->up_s, A.up_s, (long long)E * f, L, L / 32, FS);
+  {  // the slice-major copy of Down: [E][f/32][L][16 B] as 128-byte lines
+    const cuuint64_t dims[2] = {128, (cuuint64_t)E * (f / FS) * L / 8};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {128, (cuuint32_t)(L / 8)};
+    ok = ok && tmap_encode(&mp->dsl_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dsl_q, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_NONE);
+    const cuuint64_t sd[2] = {256, (cuuint64_t)E * (f / FS) * L / 256};
+    const cuuint64_t ss[1] = {512};
+    const cuuint32_t sb[2] = {256, (cuuint32_t)(L / 256)};
+    ok = ok && tmap_encode(&mp->dsl_s, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, dsl_s, sd, ss, sb, CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+  ok = ok && map_q(&mp->wout_q, A.W_out_q, (long long)G * A.d, L, L / 256, 32);
+  ok = ok && map_s(&mp->wout_s, A.W_out_s, (long long)G * A.d, L, L / 32, 32);
   return ok;
 }
 
-bool fused_decode_supported(const DecodeArgs& A) {
-  if (A.r != 0 || A.T < 1 || A.T > 16) return false;
-  if (A.E > 512 || A.E % 2 != 0 || A.G > 64 || A.k > 16) return false;
-  if (A.d % KSEG != 0 || A.d / KSEG > 8) return false;
-  if (A.L != 256 && A.L != 512 && A.L != 1024) return false;  // gate/up/W_out chunks: 16 rows x L in one slot
-  if (A.f != 256 && A.f != 512) return false;                  // down chunks: 32 rows x f in one slot
-  if (A.f % 16 != 0 || (long long)A.T * A.k > MAX_ACT) return false;
+bool fused_decode_supported(const DecodeArgs& A, int grid) {
+  if ((A.r != 0 && !lora_fused_supported(A)) || A.T < 1 || A.T > 16 || grid < 1) return false;
+  if (A.E > 512 || A.G > 64 || A.k > 16 || A.E > MAX_RX * grid) return false;
+  if (A.d > 4096 || !(A.d == 1024 || A.d % 2048 == 0)) return false;  // router rows and W_in pieces
+  if (A.L != 256 && A.L != 512 && A.L != 1024) return false;
+  if (A.f % FS != 0 || A.f < FS || (long long)A.T * A.k > 256) return false;
+  if ((long long)A.G * (A.L / 16) > (long long)MAX_TILES * grid) return false;
   return true;
 }
+
+// Down [E][L][f/2] -> [E][f/32][L][16 B]; its scales [E][L][f/32] -> [E][f/32][L]
+__global__ void repack_down_kernel(const uint4* __restrict__ q, const uint16_t* __restrict__ s, int E, int L, int f,
+                                   uint4* __restrict__ qo, uint16_t* __restrict__ so) {
+  const int nsf = f / FS;
+  const size_t n = (size_t)E * nsf * L;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t e = i / ((size_t)nsf * L), rem = i % ((size_t)nsf * L);
+    const int sl = (int)(rem / L), l = (int)(rem % L);
+    qo[i] = q[(e * L + l) * nsf + sl];
+    so[i] = s[(e * L + l) * nsf + sl];
+  }
+}
+
+cudaError_t launch_repack_down(const uint8_t* q, const uint16_t* s, int E, int L, int f, uint8_t* qo, uint16_t* so,
+                               cudaStream_t st) {
+  repack_down_kernel<<<592, 256, 0, st>>>(reinterpret_cast<const uint4*>(q), s, E, L, f, reinterpret_cast<uint4*>(qo),
+                                          so);
+  return cudaGetLastError();
+}
+
+size_t fused_down_copy_bytes(int E, int L, int f) { return (size_t)E * L * f / 2 + (size_t)E * L * (f / FS) * 2; }
 
 cudaError_t fused_set_attributes() {
   cudaFuncSetAttribute(decode_fused_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<1>());
@@ -1073,14 +1222,21 @@ int fused_grid(int num_sms) {
   return num_sms;  // one CTA per SM
 }
 
-cudaError_t launch_decode_fused(const FusedArgs& F, int grid, cudaStream_t st) {
+cudaError_t launch_decode_fused(const FusedArgs& F, int grid, cudaStream_t st, int pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(NTHR);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  if (pdl) {
+    // one CTA per SM: the CTAs become resident as the previous layer's exit,
+    // and every wait across CTAs is bounded
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (F.A.T <= 8) {

@@ -10,16 +10,20 @@
 //            in 128-token x 256-expert tiles, then the top-k and softmax
 //            renormalisation by one warp per token over its E logits
 //   permute  the deterministic multi-CTA permutation (permute.cu)
-//   win      H[g][t] = Win[g] x_t for every (g, t) (dense; rows of tokens
-//            with no expert in g are dropped), stored once per assignment
-//            in the expert-sorted order
+//   tsort    (layer calls, G <= 8) tokens in a stable order of the set of
+//            groups they route into, the union of those sets per 128-token
+//            tile, and x in fp16 in that order: a token tile then reads only
+//            the groups its tokens use, in W_in and in W_out
+//   win      H[g][t] = Win[g] x_t for every token tile whose tokens use g
+//            (rows of tokens of the tile with no expert in g are dropped),
+//            stored once per assignment in the expert-sorted order
 //   gateup   V[a] = silu(Gate_e h) * Up_e h   grouped by expert (128 gate
 //            rows + the matching 128 up rows per tile, SwiGLU in the epilogue)
 //   down     U[a] = w_a * Down_e V[a]     grouped by expert
 //   zreduce  Z[(g,t)] = sum_{j: g(e_j) = g} U[(t,j)]  in ascending j
-//   wout     y_t = sum_g Wout[g] Z[(g,t)] (+ residual): one GEMM over K =
-//            G*L per token tile (absent (g,t) rows read as zero), so the
-//            weighted combine happens in the accumulator
+//   wout     y_t = sum_g Wout[g] Z[(g,t)] (+ residual): one GEMM per token
+//            tile over K = the tile's groups x L (absent (g,t) rows read as
+//            zero), so the weighted combine happens in the accumulator
 // Intermediates H, V, U, Z are fp16 (fp32 accumulation everywhere).
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -125,6 +129,7 @@ struct ProbRoute : ProbBase {
     tl.n0 = (t % ntn()) * 256;
     tl.rows = min(128, T - tl.m0);
     tl.nkb = 3 * (d / 64);
+    tl.gm = 0;
     return tl;
   }
   // K block kb: bf16 term kb % 3 of W_r against x's K block kb / 3 (rows
@@ -191,24 +196,39 @@ struct ProbWin : ProbBase {
   // assignment's position in the expert-sorted order, so the expert GEMM
   // reads its A operand by plain TMA boxes.
   static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 3, B_MODE = 2, STAGES = 4;
-  CUtensorMap am;   // x in fp16 as [T][d], box {64, 128}
+  CUtensorMap am;   // x in fp16 as [T][d] (in tsort order when sorted), box {64, 128}
   CUtensorMap bm;   // Win in fp16 as [G][L][d], box {64, 256, 1}
   int T, d, L, G, k, epg;
   const int32_t* idx;  // [T*k] routed experts
   const int32_t* inv;  // [T*k] assignment -> position in the expert-sorted order
   __half* H;           // [T*k][L] by sorted position
+  // sorted: A row p is token tsort[p]; group g visits only the token tiles
+  // gtl[g][0 .. gtc[g]) (the tiles whose union of groups holds g)
+  const int32_t* tsort;
+  const int* gtc;
+  const int* gtl;
   LMOE_DEV int ntn() const { return L / 256; }
   LMOE_DEV int ntm() const { return (T + 127) / 128; }
-  LMOE_DEV void init(int*) const {}
-  LMOE_DEV int num_tiles(const int*) const { return G * ntm() * ntn(); }
-  LMOE_DEV Tile tile(const int*, int t) const {
+  LMOE_DEV void init(int* sc) const {
+    if (tsort) tile_prefix(sc, G, [&](int g) { return gtc[g] * ntn(); });
+  }
+  LMOE_DEV int num_tiles(const int* sc) const { return tsort ? sc[G] : G * ntm() * ntn(); }
+  LMOE_DEV Tile tile(const int* sc, int t) const {
     Tile tl;
-    tl.prob = t / (ntm() * ntn());
-    const int loc = t % (ntm() * ntn());
-    tl.m0 = (loc / ntn()) * 128;
+    int loc;
+    if (tsort) {
+      tl.prob = find_prob(sc, G, t);
+      loc = t - sc[tl.prob];
+      tl.m0 = gtl[tl.prob * ntm() + loc / ntn()] * 128;
+    } else {
+      tl.prob = t / (ntm() * ntn());
+      loc = t % (ntm() * ntn());
+      tl.m0 = (loc / ntn()) * 128;
+    }
     tl.n0 = (loc % ntn()) * 256;
     tl.rows = min(128, T - tl.m0);
     tl.nkb = d / 64;
+    tl.gm = 0;
     return tl;
   }
   LMOE_DEV void load_a(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
@@ -224,7 +244,7 @@ struct ProbWin : ProbBase {
     mma_k4(d_tmem, da, db, tc::idesc(128, 256, 0), kb);
   }
   LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase) const {
-    const int t = tl.m0 + row;
+    const int t = row < tl.rows ? (tsort ? tsort[tl.m0 + row] : tl.m0 + row) : 0;
     unsigned dest = 0;  // bit j: assignment j of token t is an expert of group tl.prob
     if (row < tl.rows)
       for (int j = 0; j < k; ++j)
@@ -259,6 +279,7 @@ struct ProbGateUp : ProbBase {
     tl.n0 = (loc % ntn()) * 128;
     tl.rows = min(128, eo[e + 1] - eo[e] - tl.m0);
     tl.nkb = L / 64;
+    tl.gm = 0;
     return tl;
   }
   // A rows: the expert's assignments (rows past the expert's end belong to
@@ -312,6 +333,7 @@ struct ProbDown : ProbBase {
     tl.n0 = (loc % ntn()) * 256;
     tl.rows = min(128, eo[e + 1] - eo[e] - tl.m0);
     tl.nkb = f / 64;
+    tl.gm = 0;
     return tl;
   }
   // A: the expert's rows of V (rows past its range belong to the next expert
@@ -358,8 +380,19 @@ struct ProbWout : ProbBase {
   const uint16_t* residual;
   uint16_t* y;  // [T][d] bf16 (mode 0)
   float* Y;     // [rows][d] (mode 1)
+  // mode 0, sorted: A row p is token tsort[p], and token tile j reads only
+  // the K blocks of the groups in tunion[j]
+  const int32_t* tsort;
+  const uint32_t* tunion;
   LMOE_DEV int ntn() const { return d / 256; }
   LMOE_DEV int kpg() const { return L / 64; }
+  // the group of K block kb of a mode-0 tile: the (kb / kpg)-th group of its set
+  LMOE_DEV int kgroup(const Tile& tl, int kb) const {
+    unsigned m = tl.gm;
+#pragma unroll 1
+    for (int i = kb / kpg(); i > 0; --i) m &= m - 1u;
+    return __ffs(m) - 1;
+  }
   LMOE_DEV void init(int* sc) const {
     if (mode == 1) tile_prefix(sc, G, [&](int g) { return ((gto[g + 1] - gto[g] + 127) / 128) * ntn(); });
   }
@@ -371,7 +404,8 @@ struct ProbWout : ProbBase {
       tl.m0 = (t / ntn()) * 128;
       tl.n0 = (t % ntn()) * 256;
       tl.rows = min(128, T - tl.m0);
-      tl.nkb = G * kpg();
+      tl.gm = tsort ? tunion[t / ntn()] : (G >= 32 ? 0xffffffffu : (1u << G) - 1u);
+      tl.nkb = __popc(tl.gm) * kpg();
     } else {
       const int g = find_prob(sc, G, t), loc = t - sc[g];
       tl.prob = g;
@@ -379,18 +413,19 @@ struct ProbWout : ProbBase {
       tl.n0 = (loc % ntn()) * 256;
       tl.rows = min(128, gto[g + 1] - gto[g] - tl.m0);
       tl.nkb = kpg();
+      tl.gm = 0;
     }
     return tl;
   }
   LMOE_DEV void load_a(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
     if (mode == 0)
-      tma_load_2d(dst, &am, kb * 64, tl.m0, bar);
+      tma_load_2d(dst, &am, kgroup(tl, kb) * L + (kb % kpg()) * 64, tl.m0, bar);
     else  // rows past the group's range belong to the next group or read as zero; not stored
       tma_load_2d(dst, &am, kb * 64, gto[tl.prob] + tl.m0, bar);
   }
   LMOE_DEV const void* a_row(const int*, const Tile&, int, int) const { return nullptr; }
   LMOE_DEV void load_b(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
-    const int g = mode == 0 ? kb / kpg() : tl.prob;
+    const int g = mode == 0 ? kgroup(tl, kb) : tl.prob;
     tma_load_3d(dst, &bm, (mode == 0 ? kb % kpg() : kb) * 64, tl.n0, g, bar);
   }
   LMOE_DEV bool b_row(const int*, const Tile&, int, int, const uint8_t*&, const uint16_t*&) const { return false; }
@@ -405,7 +440,7 @@ struct ProbWout : ProbBase {
       tc::tmem_ld16(tbase + (uint32_t)c0, v);
       if (!valid) continue;
       if (mode == 0) {
-        const size_t o = (size_t)(tl.m0 + row) * d + tl.n0 + c0;
+        const size_t o = (size_t)(tsort ? tsort[tl.m0 + row] : tl.m0 + row) * d + tl.n0 + c0;
         uint32_t h[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -494,12 +529,123 @@ __global__ void zreduce_kernel(const __half* __restrict__ U, const int32_t* __re
 // expert in g. One warp per (t, g) (k <= 32).
 __global__ void zreduce_tok_kernel(const __half* __restrict__ U, const int32_t* __restrict__ idx,
                                    const int32_t* __restrict__ inv, int T, int G, int k, int epg, int L,
-                                   __half* __restrict__ Ztok) {
+                                   const int32_t* __restrict__ tpos, __half* __restrict__ Ztok) {
   const int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (item >= T * G) return;
   const int t = item / G, g = item % G;
   const unsigned mask = __ballot_sync(0xffffffffu, lane < k && idx[(size_t)t * k + lane] / epg == g);
-  sum_rows_f16(U, inv + (size_t)t * k, mask, L, Ztok + ((size_t)t * G + g) * L);
+  const int row = tpos ? tpos[t] : t;  // the token's row in the sorted order (or its own)
+  sum_rows_f16(U, inv + (size_t)t * k, mask, L, Ztok + ((size_t)row * G + g) * L);
+}
+
+// ------------------------------------------------------------- token order
+// Tokens in a stable order of the set of groups they route into (G <= 8: an
+// 8-bit mask), so that a 128-token tile of the order holds few distinct sets.
+// Three passes (no result depends on the order of atomics): masks and
+// per-block histograms; offsets; ranks within a block by warp match and
+// per-warp counts. Then the union of the sets per tile and, per group, the
+// tiles whose union holds it.
+constexpr int TS_TB = 1024;
+
+__global__ void __launch_bounds__(TS_TB) tsort_count_kernel(const int32_t* __restrict__ idx, int T, int k, int epg,
+                                                            uint8_t* __restrict__ mask, int* __restrict__ bh) {
+  __shared__ int h[256];
+  if (threadIdx.x < 256) h[threadIdx.x] = 0;
+  __syncthreads();
+  const int t = blockIdx.x * TS_TB + threadIdx.x;
+  if (t < T) {
+    unsigned m = 0;
+    for (int j = 0; j < k; ++j) m |= 1u << (idx[(size_t)t * k + j] / epg);
+    mask[t] = (uint8_t)m;
+    atomicAdd(&h[m & 255u], 1);
+  }
+  __syncthreads();
+  if (threadIdx.x < 256) bh[blockIdx.x * 256 + threadIdx.x] = h[threadIdx.x];
+}
+
+// one block of 256 threads: bh[b][m] -> first position of block b's tokens of set m
+__global__ void __launch_bounds__(256) tsort_scan_kernel(int* __restrict__ bh, int nb) {
+  __shared__ int tot[256];
+  const int m = threadIdx.x;
+  int s = 0;
+  for (int b = 0; b < nb; ++b) s += bh[b * 256 + m];
+  tot[m] = s;
+  __syncthreads();
+  if (m == 0) {
+    int run = 0;
+    for (int i = 0; i < 256; ++i) {
+      const int c = tot[i];
+      tot[i] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  int run = tot[m];
+  for (int b = 0; b < nb; ++b) {
+    const int c = bh[b * 256 + m];
+    bh[b * 256 + m] = run;
+    run += c;
+  }
+}
+
+__global__ void __launch_bounds__(TS_TB) tsort_scatter_kernel(const uint8_t* __restrict__ mask, int T,
+                                                              const int* __restrict__ bh, int32_t* __restrict__ tsort,
+                                                              int32_t* __restrict__ tpos) {
+  __shared__ int wc[TS_TB / 32][256];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < (TS_TB / 32) * 256; i += TS_TB) (&wc[0][0])[i] = 0;
+  __syncthreads();
+  const int t = blockIdx.x * TS_TB + threadIdx.x;
+  const unsigned m = t < T ? mask[t] : 256u;  // 256: no token
+  const unsigned peers = __match_any_sync(0xffffffffu, m);
+  const int rank = __popc(peers & ((1u << lane) - 1u));
+  if (m < 256u && rank == 0) wc[warp][m] = __popc(peers);
+  __syncthreads();
+  if (m < 256u) {
+    int pre = 0;
+    for (int w = 0; w < warp; ++w) pre += wc[w][m];
+    const int pos = bh[blockIdx.x * 256 + m] + pre + rank;
+    tsort[pos] = t;
+    tpos[t] = pos;
+  }
+}
+
+// one block: tunion[j] = OR of the sets of tile j's tokens; per group g, the
+// tiles whose union holds g, ascending: gtl[g][0 .. gtc[g])
+__global__ void __launch_bounds__(1024) tsort_tiles_kernel(const uint8_t* __restrict__ mask,
+                                                           const int32_t* __restrict__ tsort, int T, int G,
+                                                           uint32_t* __restrict__ tunion, int* __restrict__ gtc,
+                                                           int* __restrict__ gtl) {
+  const int nt = (T + 127) / 128, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int j = warp; j < nt; j += 32) {
+    unsigned u = 0;
+    for (int p = j * 128 + lane; p < min(T, j * 128 + 128); p += 32) u |= mask[tsort[p]];
+    for (int o = 16; o > 0; o >>= 1) u |= __shfl_xor_sync(0xffffffffu, u, o);
+    if (lane == 0) tunion[j] = u;
+  }
+  __syncthreads();
+  if (threadIdx.x < G) {
+    const int g = threadIdx.x;
+    int c = 0;
+    for (int j = 0; j < nt; ++j)
+      if ((tunion[j] >> g) & 1u) gtl[g * nt + c++] = j;
+    gtc[g] = c;
+  }
+}
+
+// x (bf16) to fp16 rows in the token order: x16[p] = x[tsort[p]]
+__global__ void __launch_bounds__(256) x_sorted_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ tsort,
+                                                       int T, int d8, uint4* __restrict__ x16) {
+  const size_t n = (size_t)T * d8, stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += stride) {
+    const size_t p = i / d8, c = i % d8;
+    const uint4 v = __ldcs(x + (size_t)tsort[p] * d8 + c);
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    uint32_t h[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) h[j] = pack_half2(__uint_as_float(u[j] << 16), __uint_as_float(u[j] & 0xffff0000u));
+    x16[i] = make_uint4(h[0], h[1], h[2], h[3]);
+  }
 }
 
 // W = hi + mid + lo with each term the bf16 rounding of what remains; the
@@ -578,7 +724,7 @@ size_t al(size_t v) { return (v + kAl - 1) & ~(kAl - 1); }
 
 struct PWs {
   size_t logits, idx, w, eo, sa, inv, go, gto, gt, ar, perm_scratch, H, V, U, Z, tokrow, x16, win16, wout16, gate16, up16,
-      down16, ztok, end;
+      down16, ztok, tmask, tsort, tpos, tbh, tunion, gtc, gtl, end;
 };
 
 PWs pws(const PrefillArgs& P, int T) {
@@ -613,6 +759,14 @@ PWs pws(const PrefillArgs& P, int T) {
   m.up16 = take((size_t)P.E * P.f * P.L * 2);
   m.down16 = take((size_t)P.E * P.L * P.f * 2);
   m.ztok = take((size_t)T * P.G * P.L * 2);
+  const size_t nt = (size_t)(T + 127) / 128, nb = (size_t)(T + TS_TB - 1) / TS_TB;
+  m.tmask = take((size_t)T);
+  m.tsort = take((size_t)T * 4);
+  m.tpos = take((size_t)T * 4);
+  m.tbh = take(nb * 256 * 4);
+  m.tunion = take(nt * 4);
+  m.gtc = take((size_t)P.G * 4);
+  m.gtl = take((size_t)P.G * nt * 4);
   m.end = o;
   return m;
 }
@@ -667,11 +821,23 @@ ProbBase base(const PrefillArgs& P) {
   return b;
 }
 
+// the token order of a layer call (all null: tokens in their own order)
+struct TokOrder {
+  const int32_t* tsort;
+  const int32_t* tpos;
+  const uint32_t* tunion;
+  const int* gtc;
+  const int* gtl;
+};
+
 // expert part of the layer after routing and permutation: win, gateup, down,
 // zreduce, then wout (mode 0 -> y, mode 1 -> Yrows)
+cudaError_t dequant(const PrefillArgs& P, const uint16_t* x, int T, char* b, const PWs& m, cudaStream_t st,
+                    EvHook* hook, bool with_x);
+
 cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_t* idx, const float* w,
                     const PermPtrs& pm, char* b, const PWs& m, int mode, float* Yrows, const uint16_t* residual,
-                    uint16_t* y, cudaStream_t st, EvHook* hook) {
+                    uint16_t* y, cudaStream_t st, EvHook* hook, bool dequant_here, const TokOrder& to) {
   const int grid = P.num_sms;
   __half* H = reinterpret_cast<__half*>(b + m.H);
   __half* V = reinterpret_cast<__half*>(b + m.V);
@@ -686,27 +852,7 @@ cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_
   __half* down16 = reinterpret_cast<__half*>(b + m.down16);
   __half* ztok = reinterpret_cast<__half*>(b + m.ztok);
   cudaError_t e;
-  {  // the shared matrices and x in fp16, once per call
-    if (hook) hook->before(st);
-    DqJob J;
-    const size_t wwords = (size_t)P.G * P.L * P.d / 8, ewords = (size_t)P.E * P.f * P.L / 8;
-    const void* q[5] = {P.W_in_q, P.W_out_q, P.gate_q, P.up_q, P.down_q};
-    const uint16_t* sc[5] = {P.W_in_s, P.W_out_s, P.gate_s, P.up_s, P.down_s};
-    __half* out[5] = {win16, wout16, gate16, up16, down16};
-    for (int i = 0; i < 5; ++i) {
-      J.seg[i].q = static_cast<const uint32_t*>(q[i]);
-      J.seg[i].s = sc[i];
-      J.seg[i].out = reinterpret_cast<uint4*>(out[i]);
-      J.seg[i].n = i < 2 ? wwords : ewords;
-    }
-    J.nseg = 5;
-    J.x = reinterpret_cast<const uint4*>(x);
-    J.x16 = reinterpret_cast<uint4*>(x16);
-    J.nx = (size_t)T * P.d / 8;
-    dequant_all_kernel<<<8 * grid, 256, 0, st>>>(J);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if (hook) hook->after(st);
-  }
+  if (dequant_here && (e = dequant(P, x, T, b, m, st, hook, to.tsort == nullptr)) != cudaSuccess) return e;
   {
     ProbWin p;
     static_cast<ProbBase&>(p) = base(P);
@@ -721,6 +867,7 @@ cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_
         return cudaErrorInvalidValue;
     }
     p.T = T; p.d = P.d; p.L = P.L; p.G = P.G; p.k = P.k; p.epg = P.epg; p.idx = idx; p.inv = pm.inv; p.H = H;
+    p.tsort = to.tsort; p.gtc = to.gtc; p.gtl = to.gtl;
     if (hook) hook->before(st);
     if ((e = run_gemm(p, grid, st)) != cudaSuccess) return e;
     if (hook) hook->after(st);
@@ -765,7 +912,7 @@ cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_
   {
     if (hook) hook->before(st);
     if (mode == 0) {
-      zreduce_tok_kernel<<<(T * P.G + 7) / 8, 256, 0, st>>>(U, idx, pm.inv, T, P.G, P.k, P.epg, P.L, ztok);
+      zreduce_tok_kernel<<<(T * P.G + 7) / 8, 256, 0, st>>>(U, idx, pm.inv, T, P.G, P.k, P.epg, P.L, to.tpos, ztok);
     } else {
       cudaMemsetAsync(tokrow, 0xff, (size_t)T * P.G * 4, st);
       const int rows_cap = T * (P.G < P.k ? P.G : P.k);
@@ -796,9 +943,46 @@ cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_
         return cudaErrorInvalidValue;
     }
     p.gto = pm.group_tok_offsets; p.T = T; p.d = P.d; p.L = P.L; p.G = P.G; p.mode = mode;
+    p.tsort = mode == 0 ? to.tsort : nullptr;
+    p.tunion = to.tunion;
     p.residual = residual; p.y = y; p.Y = Yrows;
     if (hook) hook->before(st);
     if ((e = run_gemm(p, grid, st)) != cudaSuccess) return e;
+    if (hook) hook->after(st);
+  }
+  return cudaSuccess;
+}
+
+// every int4 matrix and x in fp16 (x16 in the workspace); once per call
+cudaError_t dequant(const PrefillArgs& P, const uint16_t* x, int T, char* b, const PWs& m, cudaStream_t st,
+                    EvHook* hook, bool with_x) {
+  const int grid = P.num_sms;
+  __half* x16 = reinterpret_cast<__half*>(b + m.x16);
+  __half* win16 = reinterpret_cast<__half*>(b + m.win16);
+  __half* wout16 = reinterpret_cast<__half*>(b + m.wout16);
+  __half* gate16 = reinterpret_cast<__half*>(b + m.gate16);
+  __half* up16 = reinterpret_cast<__half*>(b + m.up16);
+  __half* down16 = reinterpret_cast<__half*>(b + m.down16);
+  cudaError_t e;
+  {
+    if (hook) hook->before(st);
+    DqJob J;
+    const size_t wwords = (size_t)P.G * P.L * P.d / 8, ewords = (size_t)P.E * P.f * P.L / 8;
+    const void* q[5] = {P.W_in_q, P.W_out_q, P.gate_q, P.up_q, P.down_q};
+    const uint16_t* sc[5] = {P.W_in_s, P.W_out_s, P.gate_s, P.up_s, P.down_s};
+    __half* out[5] = {win16, wout16, gate16, up16, down16};
+    for (int i = 0; i < 5; ++i) {
+      J.seg[i].q = static_cast<const uint32_t*>(q[i]);
+      J.seg[i].s = sc[i];
+      J.seg[i].out = reinterpret_cast<uint4*>(out[i]);
+      J.seg[i].n = i < 2 ? wwords : ewords;
+    }
+    J.nseg = 5;
+    J.x = reinterpret_cast<const uint4*>(x);
+    J.x16 = reinterpret_cast<uint4*>(x16);
+    J.nx = with_x ? (size_t)T * P.d / 8 : 0;
+    dequant_all_kernel<<<8 * grid, 256, 0, st>>>(J);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (hook) hook->after(st);
   }
   return cudaSuccess;
@@ -840,7 +1024,7 @@ cudaError_t prefill_set_attributes() {
 bool prefill_supported(const PrefillArgs& P) {
   if (P.r != 0) return false;  // the LoRA branch runs on the decode path
   if (P.d % 256 != 0 || P.L % 256 != 0 || P.f % 128 != 0) return false;
-  if (P.E > 512 || P.k > 16 || P.G > 64) return false;  // top-k: E <= 512 logits per warp
+  if (P.E > 512 || P.k > 16 || P.G > 32) return false;  // top-k: E <= 512 logits per warp; group masks: 32 bits
   return P.num_sms > 0;
 }
 
@@ -860,7 +1044,7 @@ cudaError_t launch_prefill_experts(const PrefillArgs& P, const uint16_t* x, int 
                                    cudaStream_t st) {
   char* b = reinterpret_cast<char*>(ws);
   const PWs m = pws(P, T);
-  return experts(P, x, T, idx, w, perm, b, m, 1, Yrows, nullptr, nullptr, st, nullptr);
+  return experts(P, x, T, idx, w, perm, b, m, 1, Yrows, nullptr, nullptr, st, nullptr, true, TokOrder{});
 }
 
 cudaError_t launch_prefill_layer(const PrefillArgs& P, const uint16_t* x, int T, const uint16_t* residual,
@@ -874,25 +1058,68 @@ cudaError_t launch_prefill_layer(const PrefillArgs& P, const uint16_t* x, int T,
   hook.ev = events;
   EvHook* hk = events ? &hook : nullptr;
   cudaError_t e;
+  // The dequantisation needs neither the routing nor the permutation: it runs
+  // on the handle's second stream, forked from and joined back into `st` by
+  // events (so the whole call stays in `st`'s order and can be captured).
+  const bool fork = P.aux != nullptr && P.ev_fork != nullptr && P.ev_join != nullptr;
+  const bool sorted = P.G <= 8;  // group sets fit the 8-bit keys of the token order
+  if (fork) {
+    if ((e = cudaEventRecord(P.ev_fork, st)) != cudaSuccess || (e = cudaStreamWaitEvent(P.aux, P.ev_fork, 0)) != cudaSuccess)
+      return e;
+    if (hk) hk->i = 2;  // stage order: route, permute, dequant, tsort, win, ...
+    if ((e = dequant(P, x, T, b, m, P.aux, hk, !sorted)) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(P.ev_join, P.aux)) != cudaSuccess) return e;
+    if (hk) hk->i = 0;
+  }
   if (hk) hk->before(st);
   if ((e = route(P, x, T, idx, w, reinterpret_cast<float*>(b + m.logits), st)) != cudaSuccess) return e;
   if (hk) hk->after(st);
   if (hk) hk->before(st);
   if ((e = launch_permute(idx, T, P.E, P.G, P.k, pm, b + m.perm_scratch, P.err, st)) != cudaSuccess) return e;
   if (hk) hk->after(st);
-  return experts(P, x, T, idx, w, pm, b, m, 0, nullptr, residual, y, st, hk);
+  TokOrder to{};
+  if (sorted) {
+    if (hk) hk->i = 3;
+    if (hk) hk->before(st);
+    uint8_t* tmask = reinterpret_cast<uint8_t*>(b + m.tmask);
+    int32_t* tsort = reinterpret_cast<int32_t*>(b + m.tsort);
+    int32_t* tpos = reinterpret_cast<int32_t*>(b + m.tpos);
+    int* tbh = reinterpret_cast<int*>(b + m.tbh);
+    uint32_t* tunion = reinterpret_cast<uint32_t*>(b + m.tunion);
+    int* gtc = reinterpret_cast<int*>(b + m.gtc);
+    int* gtl = reinterpret_cast<int*>(b + m.gtl);
+    const int nb = (T + TS_TB - 1) / TS_TB;
+    tsort_count_kernel<<<nb, TS_TB, 0, st>>>(idx, T, P.k, P.epg, tmask, tbh);
+    tsort_scan_kernel<<<1, 256, 0, st>>>(tbh, nb);
+    tsort_scatter_kernel<<<nb, TS_TB, 0, st>>>(tmask, T, tbh, tsort, tpos);
+    tsort_tiles_kernel<<<1, 1024, 0, st>>>(tmask, tsort, T, P.G, tunion, gtc, gtl);
+    x_sorted_kernel<<<4 * P.num_sms, 256, 0, st>>>(reinterpret_cast<const uint4*>(x), tsort, T, P.d / 8,
+                                                   reinterpret_cast<uint4*>(b + m.x16));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (hk) hk->after(st);
+    to = TokOrder{tsort, tpos, tunion, gtc, gtl};
+  }
+  if (fork) {
+    if ((e = cudaStreamWaitEvent(st, P.ev_join, 0)) != cudaSuccess) return e;
+    if (hk) hk->i = 4;
+  }
+  return experts(P, x, T, idx, w, pm, b, m, 0, nullptr, residual, y, st, hk, !fork, to);
 }
 
-int prefill_launch_count(const PrefillArgs&, int T) {
-  // route: GEMM + top-k; permute: count, scan, scatter; dequant; win; gateup;
-  // down; zreduce; wout
-  return T > 0 ? 11 : 0;
+int prefill_launch_count(const PrefillArgs& P, int T) {
+  // route: GEMM + top-k; permute: count, scan, scatter; dequant; tsort:
+  // count, scan, scatter, tiles, x in order (G <= 8); win; gateup; down;
+  // zreduce; wout
+  return T > 0 ? (P.G <= 8 ? 16 : 11) : 0;
 }
 
-const char* prefill_stage_name(const PrefillArgs&, int, int i, int* count) {
-  static const char* names[] = {"route", "permute", "dequant", "win", "gateup", "down", "zreduce", "wout"};
-  if (count) *count = 8;
-  return (i >= 0 && i < 8) ? names[i] : "";
+const char* prefill_stage_name(const PrefillArgs& P, int, int i, int* count) {
+  static const char* names[] = {"route", "permute", "dequant", "tsort", "win", "gateup", "down", "zreduce", "wout"};
+  static const char* names_u[] = {"route", "permute", "dequant", "win", "gateup", "down", "zreduce", "wout"};
+  const bool sorted = P.G <= 8;
+  const int n = sorted ? 9 : 8;
+  if (count) *count = n;
+  return (i >= 0 && i < n) ? (sorted ? names[i] : names_u[i]) : "";
 }
 
 }  // namespace lmoe

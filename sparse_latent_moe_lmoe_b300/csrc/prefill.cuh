@@ -31,6 +31,9 @@ struct PrefillArgs {
   unsigned* err;
   int num_sms;
   long long timeout;
+  // the handle's second stream and its fork / join events (null: everything on the caller's stream)
+  cudaStream_t aux;
+  cudaEvent_t ev_fork, ev_join;
 };
 
 // W_r fp32 [E][d] -> three bf16 matrices whose sum is W_r (to fp32 rounding).

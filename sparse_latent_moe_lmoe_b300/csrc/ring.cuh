@@ -79,15 +79,16 @@ LMOE_DEV bool mbar_test(uint64_t* m, uint32_t parity) {
   return ok != 0;
 }
 
-// acc[nt] += W[16 rows][128*nc elements] * fragments (see frag_index; chunk c
-// of the slot uses fragment chunk c), with W in a ring slot as a TMA box with
-// 128-byte swizzle: row r of the chunk is LPR 128-byte lines (line i = r*LPR
-// + k/256 for element k), and 16-byte unit j of line i sits at unit
-// j ^ (i & 7). `w` is the (1024-byte aligned) slot base, row0 the first row
-// of the tile, `s` the chunk's scales [rows][SS].
+// acc[nt] += W[16 rows][chunks c0 .. c0+nc of 128 elements] * fragments,
+// with W in a ring slot as a TMA box in 128-byte swizzle: row r of the box is
+// LPR 128-byte lines (line i = r*LPR + k/256 for element k of the box), and
+// 16-byte unit j of line i sits at unit j ^ (i & 7). `w` is the (1024-byte
+// aligned) slot base, row0 the first row of the tile, `s` the box's scales
+// [rows][SS]. Chunk c0 + c of the box meets fragment chunk c of `frag` (see
+// frag_index; the caller offsets `frag` to the box's chunk c0).
 template <int NT>
-LMOE_DEV void mma_ring_rows_swz(const unsigned char* w, int LPR, int row0, const uint16_t* s, int SS, int nc,
-                                const uint4* frag, float acc[NT][4]) {
+LMOE_DEV void mma_slot(const unsigned char* w, int LPR, int row0, const uint16_t* s, int SS, int c0, int nc,
+                       const uint4* frag, float acc[NT][4]) {
   const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
   const int r0 = row0 + gid, r8 = r0 + 8;
   const uint16_t* s0 = s + r0 * SS + tig;
@@ -99,15 +100,16 @@ LMOE_DEV void mma_ring_rows_swz(const unsigned char* w, int LPR, int row0, const
     for (int h = 0; h < 4; ++h) acc2[nt][h] = 0.f;
   // the next chunk's weights and scales are loaded while this one is contracted
   auto ld = [&](int c, uint4& a, uint4& b, uint16_t& sa, uint16_t& sb) {
-    const int i0 = r0 * LPR + (c >> 1), i8 = r8 * LPR + (c >> 1), j = ((c & 1) << 2) | tig;
+    const int cc = c0 + c;
+    const int i0 = r0 * LPR + (cc >> 1), i8 = r8 * LPR + (cc >> 1), j = ((cc & 1) << 2) | tig;
     a = *reinterpret_cast<const uint4*>(w + i0 * 128 + ((j ^ (i0 & 7)) << 4));
     b = *reinterpret_cast<const uint4*>(w + i8 * 128 + ((j ^ (i8 & 7)) << 4));
-    sa = s0[c * 4];
-    sb = s8[c * 4];
+    sa = s0[cc * 4];
+    sb = s8[cc * 4];
   };
-  uint4 a, b;
-  uint16_t sa, sb;
-  ld(0, a, b, sa, sb);
+  uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
+  uint16_t sa = 0, sb = 0;
+  if (nc > 0) ld(0, a, b, sa, sb);
 #pragma unroll 1
   for (int c = 0; c < nc; ++c) {
     const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
@@ -138,82 +140,24 @@ LMOE_DEV void mma_ring_rows_swz(const unsigned char* w, int LPR, int row0, const
     for (int h = 0; h < 4; ++h) acc[nt][h] += acc2[nt][h];
 }
 
-// Two matrices (same shape, same activations) in one pass: the fragment
-// loads are shared and the two accumulator chains interleave.
+// acc[nt] += W[16 rows m*16 ..][32 elements] * v, for a matrix slice of 32
+// reduction elements per row held as [rows][16 bytes] (row r's 32 packed int4
+// at byte 16 r) with one bf16 scale per row, `sc`. Lane (gid, tig) reads word
+// tig of rows gid and gid+8 -- elements 8 tig .. 8 tig + 7 -- so the matching
+// activation entry vfr[nt*32 + lane] holds elements 8 tig .. 8 tig + 7 of
+// token 8 nt + gid, packed as (e0,e4) (e1,e5) (e2,e6) (e3,e7).
 template <int NT>
-LMOE_DEV void mma_ring_rows_swz2(const unsigned char* w1, const uint16_t* s1, const unsigned char* w2,
-                                 const uint16_t* s2, int LPR, int SS, int nc, const uint4* frag, float acc1[NT][4],
-                                 float acc2[NT][4]) {
+LMOE_DEV void mma_slice32(const uint32_t* wsl, const uint16_t* sc, int m, const uint4* vfr, float acc[NT][4]) {
   const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
-  const int r0 = gid, r8 = gid + 8;
-  const uint16_t* s10 = s1 + r0 * SS + tig;
-  const uint16_t* s18 = s1 + r8 * SS + tig;
-  const uint16_t* s20 = s2 + r0 * SS + tig;
-  const uint16_t* s28 = s2 + r8 * SS + tig;
-  auto ld = [&](int c, uint4& a, uint4& b, uint4& a2, uint4& b2, uint16_t (&sc)[4]) {
-    const int i0 = r0 * LPR + (c >> 1), i8 = r8 * LPR + (c >> 1), j = ((c & 1) << 2) | tig;
-    const int o0 = i0 * 128 + ((j ^ (i0 & 7)) << 4), o8 = i8 * 128 + ((j ^ (i8 & 7)) << 4);
-    a = *reinterpret_cast<const uint4*>(w1 + o0);
-    b = *reinterpret_cast<const uint4*>(w1 + o8);
-    a2 = *reinterpret_cast<const uint4*>(w2 + o0);
-    b2 = *reinterpret_cast<const uint4*>(w2 + o8);
-    sc[0] = s10[c * 4];
-    sc[1] = s18[c * 4];
-    sc[2] = s20[c * 4];
-    sc[3] = s28[c * 4];
-  };
-  uint4 a, b, a2, b2;
-  uint16_t sc[4];
-  ld(0, a, b, a2, b2, sc);
-#pragma unroll 1
-  for (int c = 0; c < nc; ++c) {
-    const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
-    const uint32_t va[4] = {a2.x, a2.y, a2.z, a2.w}, vb[4] = {b2.x, b2.y, b2.z, b2.w};
-    const __half2 h0 = scale_h2(sc[0]), h8 = scale_h2(sc[1]), g0 = scale_h2(sc[2]), g8 = scale_h2(sc[3]);
-    if (c + 1 < nc) ld(c + 1, a, b, a2, b2, sc);
-    uint4 fv[4][NT];
+  const int r0 = 16 * m + gid, r8 = r0 + 8;
+  uint32_t A[4], B8[4];
+  dequant_word(wsl[r0 * 4 + tig], scale_h2(sc[r0]), A);
+  dequant_word(wsl[r8 * 4 + tig], scale_h2(sc[r8]), B8);
 #pragma unroll
-    for (int mp = 0; mp < 4; ++mp)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) fv[mp][nt] = frag[frag_index(c, nt, mp, lane, NT)];
-#pragma unroll
-    for (int mp = 0; mp < 4; ++mp) {
-      uint32_t A[4], B8[4], C[4], D8[4];
-      dequant_word(wa[mp], h0, A);
-      dequant_word(wb[mp], h8, B8);
-      dequant_word(va[mp], g0, C);
-      dequant_word(vb[mp], g8, D8);
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const uint4 f = fv[mp][nt];
-        mma16816(acc1[nt], A[0], B8[0], A[1], B8[1], f.x, f.y);
-        mma16816(acc2[nt], C[0], D8[0], C[1], D8[1], f.x, f.y);
-        mma16816(acc1[nt], A[2], B8[2], A[3], B8[3], f.z, f.w);
-        mma16816(acc2[nt], C[2], D8[2], C[3], D8[3], f.z, f.w);
-      }
-    }
-  }
-}
-
-// Transpose a warp's m16n8 accumulators (rows r0..r0+15 of an activation
-// that is the reduction dimension of the next contraction, tokens 8*nt + ..)
-// into this lane's fragment entry: lane = 2*n + run holds rows r0 + 8*run ..
-// + 7 of token n (n < 8*NT). Returns the 8 values in e[].
-template <int NT>
-LMOE_DEV void acc_to_entry(const float acc[NT][4], float e[8]) {
-  const int lane = threadIdx.x & 31, run = lane & 1, n = lane >> 1;
-  const int want = run * 2 + (n & 1), src_t = (n & 7) >> 1, want_nt = n >> 3;
-#pragma unroll
-  for (int g = 0; g < 8; ++g) {
-    float v = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const float x = __shfl_sync(0xffffffffu, acc[nt][h], g * 4 + src_t);
-        if (nt == want_nt && h == want) v = x;
-      }
-    e[g] = v;
+  for (int nt = 0; nt < NT; ++nt) {
+    const uint4 f = vfr[nt * 32 + lane];
+    mma16816(acc[nt], A[0], B8[0], A[1], B8[1], f.x, f.y);
+    mma16816(acc[nt], A[2], B8[2], A[3], B8[3], f.z, f.w);
   }
 }
 

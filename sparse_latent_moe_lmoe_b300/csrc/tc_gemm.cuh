@@ -97,6 +97,7 @@ struct Tile {
   int n0;      // first output column
   int rows;    // valid rows in this M tile (<= 128)
   int nkb;     // K blocks
+  unsigned gm; // problem-specific (the groups a token tile reads, for W_out)
 };
 
 struct Shared {
