@@ -26,14 +26,13 @@ struct lmoe_handle {
   uint16_t* d_wr_split;  // [3][E][d] bf16 split of W_r (hi, mid, lo) for the tensor-core router
   long long timeout;
   int fused_grid;  // CTAs of the single-kernel decode pass (0: unavailable)
-  DecodeMaps maps;                   // TMA descriptors of the weights (single-kernel decode)
-  bool maps_ok;
+  DecodePack pk;                     // where the single-kernel decode pass streams its weights from
+  bool pack_ok;                      // the decode pack exists (the single-kernel pass is possible)
   unsigned* d_ctr;                   // its arrival counters (two copies)
   unsigned long long* d_launches;    // its launch counter
   cudaStream_t aux;                  // second stream of the prefill path (fork / join by events)
   cudaEvent_t ev_fork, ev_join;
-  uint8_t* d_dsl_q;                  // its slice-major copy of Down: [E][f/32][L][16 B] packed int4
-  uint16_t* d_dsl_s;                 // and the matching scales [E][f/32][L]
+  uint8_t* d_pack;                   // the decode pass's chunk-major copy of the weights (decode_pack_bytes)
   std::vector<cudaEvent_t> events;
 };
 
@@ -234,7 +233,7 @@ struct DeviceGuard {
 };
 
 bool use_fused(const lmoe_handle* h, const DecodeArgs& A) {
-  return !(h->cfg.flags & LMOE_FLAG_MULTI_KERNEL_DECODE) && h->fused_grid > 0 && h->maps_ok &&
+  return !(h->cfg.flags & LMOE_FLAG_MULTI_KERNEL_DECODE) && h->fused_grid > 0 && h->pack_ok &&
          fused_decode_supported(A, h->fused_grid);
 }
 
@@ -244,7 +243,7 @@ FusedArgs fused_args(const lmoe_handle* h, const DecodeArgs& A, void* ws) {
   FusedArgs F;
   memset(&F, 0, sizeof(F));
   F.A = A;
-  F.maps = h->maps;
+  F.pk = h->pk;
   const DecodeWs m = decode_ws(h->cfg, 0, h->num_sms);
   char* b = reinterpret_cast<char*>(ws);
   F.logits = reinterpret_cast<float*>(b + m.logits);
@@ -480,20 +479,18 @@ lmoe_status lmoe_create(lmoe_handle** out, const lmoe_config* cfg, const lmoe_we
     cudaMemset(h->d_launches, 0, sizeof(unsigned long long));
     DecodeArgs probe = base_args(h, nullptr);
     probe.T = 1;
-    h->maps_ok = false;
+    h->pack_ok = false;
     if (h->fused_grid > 0 && fused_decode_supported(probe, h->fused_grid)) {
-      const size_t nq = (size_t)cfg->E * cfg->L * cfg->f / 2, nb = fused_down_copy_bytes(cfg->E, cfg->L, cfg->f);
-      if (cudaMalloc(&h->d_dsl_q, nq) != cudaSuccess || cudaMalloc(&h->d_dsl_s, nb - nq) != cudaSuccess) {
+      if (cudaMalloc(&h->d_pack, decode_pack_bytes(cfg->d, cfg->E, cfg->G, cfg->L, cfg->f)) != cudaSuccess) {
         cudaGetLastError();
         lmoe_destroy(h);
         return LMOE_ERR_NO_MEMORY;
       }
-      if (launch_repack_down(h->w.down_q, h->w.down_s, cfg->E, cfg->L, cfg->f, h->d_dsl_q, h->d_dsl_s, 0) !=
-          cudaSuccess) {
+      if (launch_decode_pack(probe, h->d_pack, &h->pk, 0) != cudaSuccess) {
         lmoe_destroy(h);
         return LMOE_ERR_CUDA;
       }
-      h->maps_ok = fused_make_maps(probe, h->d_dsl_q, h->d_dsl_s, &h->maps);
+      h->pack_ok = true;
     }
   }
   if (cudaStreamCreateWithFlags(&h->aux, cudaStreamNonBlocking) != cudaSuccess ||
@@ -521,11 +518,10 @@ lmoe_status lmoe_destroy(lmoe_handle* h) {
   if (h->d_wr_split) cudaFree(h->d_wr_split);
   if (h->d_ctr) cudaFree(h->d_ctr);
   if (h->d_launches) cudaFree(h->d_launches);
-  if (h->d_dsl_q) cudaFree(h->d_dsl_q);
+  if (h->d_pack) cudaFree(h->d_pack);
   if (h->ev_fork) cudaEventDestroy(h->ev_fork);
   if (h->ev_join) cudaEventDestroy(h->ev_join);
   if (h->aux) cudaStreamDestroy(h->aux);
-  if (h->d_dsl_s) cudaFree(h->d_dsl_s);
   delete h;
   return pending_error();
 }
@@ -765,9 +761,8 @@ lmoe_status lmoe_stack_forward(lmoe_handle* const* layers, int n_layers, const u
       F.pdl = l > 0 && layers[l - 1] != h;  // distinct handles: distinct counters
       if (l + 1 < n_layers && layers[l + 1] != h) {
         F.has_next = 1;
-        F.next_wr = layers[l + 1]->maps.wr;
-        F.next_win_q = layers[l + 1]->maps.win_q;
-        F.next_win_s = layers[l + 1]->maps.win_s;
+        F.next_wr = layers[l + 1]->pk.wr;
+        F.next_win = layers[l + 1]->pk.win;
       }
       EventHook hook;
       hook.ev = h->events.empty() ? nullptr : &h->events;

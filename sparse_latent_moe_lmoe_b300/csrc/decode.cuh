@@ -61,23 +61,30 @@ struct DecodeArgs {
   float* Yrows;
 };
 
-// TMA descriptors of the weights for the single-kernel decode pass (made
-// once per handle). Packed int4 matrices are viewed as [rows][K/256][128 B]
-// (128-byte swizzle), their scales as [rows][K/32] bf16, W_r as
-// [E][d/256][256] fp32, and the slice-major copy of Down as 128-byte lines
-// ([E][f/32][L][16 B]) with scales [E][f/32][L].
-struct DecodeMaps {
-  CUtensorMap wr;
-  CUtensorMap win_q, win_s;
-  CUtensorMap gate_q, gate_s, up_q, up_s;
-  CUtensorMap dsl_q, dsl_s;
-  CUtensorMap wout_q, wout_s;
+// The single-kernel decode pass streams its weights from a copy made when the
+// handle is created, laid out chunk by chunk in the order and form the
+// consumers read them: every chunk is one contiguous run of packed int4 (its
+// 128-byte lines already in the 128-byte swizzle of the shared-memory slot)
+// followed by the chunk's bf16 scales, so one bulk copy moves it.
+//   win   [G L/16 tiles of 16 rows][d/PW pieces][9 PW bytes], PW = min(d, 2048)
+//   unit  [E][f/32 slices][gate rows, up rows, Down columns][18 L bytes]
+//   wout  [G][d/32 blocks of 32 rows][18 L bytes]
+// The router rows are read from W_r itself (fp32 rows, contiguous).
+struct DecodePack {
+  const float* wr;
+  const uint8_t* win;
+  const uint8_t* unit;
+  const uint8_t* wout;
 };
+size_t decode_pack_bytes(int d, int E, int G, int L, int f);
+// fills `pk` (win/unit/wout carved from `buf`, decode_pack_bytes long) from
+// the layer's weights; wr is taken from A.W_r
+cudaError_t launch_decode_pack(const DecodeArgs& A, uint8_t* buf, DecodePack* pk, cudaStream_t st);
 
 // The single-kernel decode pass (decode_fused.cu).
 struct FusedArgs {
   DecodeArgs A;
-  DecodeMaps maps;
+  DecodePack pk;
   float* logits;                 // [16][E]
   uint4* Hf;                     // [G][L/128][128 NT] H as fp16 fragments (NT = token tiles of the launch)
   float* Zpart;                  // [grid + G][16][L] partial sums of Z, one per (CTA, group) it worked on
@@ -91,10 +98,11 @@ struct FusedArgs {
   // layer stacks: launched as a programmatic dependent of the previous layer
   // (the weight stream starts at once; x is read after griddepcontrol.wait)
   int pdl;
-  // layer stacks: the next layer's router rows and W_in tiles of this CTA are
-  // prefetched into L2 once this layer's own weights are requested
+  // layer stacks: the next layer's router rows and W_in chunks of this CTA
+  // are prefetched into L2 once this layer's own weights are requested
   int has_next;
-  CUtensorMap next_wr, next_win_q, next_win_s;
+  const float* next_wr;
+  const uint8_t* next_win;
   // the Recover-LoRA branch (lora.cu): Hl [G][16][L] is added to H; Z is also
   // written in fp32 to Zlin [G][16][L]; the per-group outputs are left in Yp
   // for lora_out to combine (no combine here)
@@ -102,18 +110,12 @@ struct FusedArgs {
   float* zlin;
   int no_combine;
   // diagnosis: [0] where the first timed-out wait of a launch gave up, then
-  // per CTA 16 %globaltimer stamps of its phases (a region of the workspace)
+  // per CTA 32 %globaltimer stamps of its phases (a region of the workspace)
   unsigned long long* diag;
 };
 size_t fused_counter_words(int d, int E, int G, int L);
 size_t fused_zpart_bytes(int G, int L, int grid);
 size_t fused_diag_bytes(int grid);
-// bytes of the slice-major copy of Down (packed int4 and scales)
-size_t fused_down_copy_bytes(int E, int L, int f);
-cudaError_t launch_repack_down(const uint8_t* q, const uint16_t* s, int E, int L, int f, uint8_t* qo, uint16_t* so,
-                               cudaStream_t st);
-// Encodes the tensor maps; false if the driver refuses one of them.
-bool fused_make_maps(const DecodeArgs& A, const uint8_t* dsl_q, const uint16_t* dsl_s, DecodeMaps* maps);
 bool fused_decode_supported(const DecodeArgs& A, int grid);
 cudaError_t fused_set_attributes();
 int fused_grid(int num_sms);

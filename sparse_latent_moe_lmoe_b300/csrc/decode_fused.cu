@@ -44,7 +44,6 @@
 #include "common.cuh"
 #include "decode.cuh"
 #include "ring.cuh"
-#include "tmap.cuh"
 #include "topk.cuh"
 
 namespace lmoe {
@@ -56,6 +55,7 @@ namespace lmoe {
 namespace {
 
 constexpr int NCW = 16, NCT = NCW * 32, PROD = NCW, NTHR = NCT + 32;
+constexpr int RW = 8;             // routing warps while the others compute W_in
 constexpr int SLOT = 18432;      // 16 KB of packed int4 (or fp32 router rows) + 2 KB of scales
 constexpr int FS = 32;           // f-slice of an expert unit
 constexpr int MAX_RX = 4;        // router experts per CTA
@@ -127,6 +127,12 @@ LMOE_DEV void cons_sync() {
 }
 // Every warp, once, at the end of the kernel.
 LMOE_DEV void end_sync() { asm volatile("barrier.sync 2, %0;" ::"n"(NTHR) : "memory"); }
+// The W_in warps and the routing warps, each among themselves.
+constexpr int BAR_WIN = 3, BAR_ROUTE = 4;
+LMOE_DEV void group_sync(int id, int n) {
+  __syncwarp();
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 
 // Where a wait gave up, for diagnosis: the first timeout of a launch is
 // recorded as bit 63 | site << 32 | CTA << 8 | warp in diag[0] (sites: the
@@ -197,9 +203,10 @@ LMOE_DEV bool mbar_sleep_wait(uint64_t* m, uint32_t parity, uint32_t ns) {
 
 // mbarrier phase wait, bounded; true once the phase completed, false when it
 // gave up (a timeout of the CTA: every later wait returns false at once).
-LMOE_DEV bool mwait(Tables& tb, uint64_t* m, uint32_t parity, long long budget, unsigned* err, unsigned site,
-                    unsigned long long* diag) {
-  if (mbar_test(m, parity)) return true;
+// The slow path is out of line: it is reached only when the phase is not
+// complete at the first test.
+LMOE_COLD bool mwait_slow(Tables& tb, uint64_t* m, uint32_t parity, long long budget, unsigned* err, unsigned site,
+                          unsigned long long* diag) {
   if (tb.abort) return false;
   const long long t0 = clock64();
 #pragma unroll 1
@@ -211,6 +218,10 @@ LMOE_DEV bool mwait(Tables& tb, uint64_t* m, uint32_t parity, long long budget, 
     }
   }
   return true;
+}
+LMOE_DEV bool mwait(Tables& tb, uint64_t* m, uint32_t parity, long long budget, unsigned* err, unsigned site,
+                    unsigned long long* diag) {
+  return mbar_test(m, parity) || mwait_slow(tb, m, parity, budget, err, site, diag);
 }
 
 // This warp is done with ring chunk j (acquire's `landed`). Every warp hands
@@ -289,58 +300,55 @@ LMOE_DEV float route_weight(const Tables& tb, int t, int e) {
   return j >= 0 ? tb.w[t * 16 + j] : 0.f;
 }
 
-// x (bf16 [T][d]) into shared memory as it is, 8 NT rows of d, rows >= T zero
+// x (bf16 [T][d]) into shared memory chunk-major: [d/128][8 NT tokens][16
+// units of 8 elements], tokens >= T zero
 template <int NT>
 LMOE_COLD void stage_x(Tables& tb, uint4* xs, const uint16_t* x, int T, int d, int ctid) {
-  const int n = NT * d, nx = T * (d / 8);  // 16-byte units: all rows, rows of tokens
+  const int n = NT * d, du = d / 8;  // 16-byte units: all rows, one row
   const uint4* x4 = reinterpret_cast<const uint4*>(x);
 #pragma unroll 1
-  for (int i0 = ctid; i0 < n; i0 += 8 * NCT) {
+  for (int i0 = ctid; i0 < n; i0 += 8 * NCT) {  // i: unit of the row-major [8 NT][d]
     uint4 v[8];
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
-      const int si = i0 + r * NCT;
-      v[r] = si < nx ? __ldg(x4 + si) : make_uint4(0u, 0u, 0u, 0u);
+      const int i = i0 + r * NCT;
+      v[r] = i < T * du ? __ldg(x4 + i) : make_uint4(0u, 0u, 0u, 0u);
     }
     if (i0 == ctid && ctid == 0) tb.x_issued = 1;
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
-      if (i0 + r * NCT < n) xs[i0 + r * NCT] = v[r];
+    for (int r = 0; r < 8; ++r) {
+      const int i = i0 + r * NCT, tok = i / du, u = i % du;
+      if (i < n) xs[((u >> 4) * 8 * NT + tok) * 16 + (u & 15)] = v[r];
+    }
   }
 }
 
-// The staged x, in place, into fp16 fragments over all of d (each fragment
-// entry is one 16-byte unit of x, converted and reordered).
+// Chunk cc (128 elements of every token) of the staged x -> its fp16
+// fragment entries, in place (one warp: the chunk's units and its entries
+// occupy the same 128 NT slots).
 template <int NT>
-LMOE_COLD void x_to_frags(uint4* xs, int d, int ctid) {
-  const int n = NT * d;  // entries, <= 8 NT per thread (d <= 4096)
-  uint4 v[8 * NT];
+LMOE_DEV void chunk_to_frags(uint4* xs, int cc) {
+  const int lane = threadIdx.x & 31;
+  uint4* blk = xs + (size_t)cc * 128 * NT;
+  uint4 v[4 * NT];
 #pragma unroll
-  for (int r = 0; r < 8 * NT; ++r) {
-    const int si = ctid + r * NCT;
-    if (si < n) {
-      const int ln = si & 31, mp = (si >> 5) & 3, rest = si >> 7;
-      const int nt = rest % NT, cc = rest / NT;
-      const int tok = nt * 8 + (ln >> 2), k0 = cc * 128 + (ln & 3) * 32 + mp * 8;
-      v[r] = xs[tok * (d / 8) + (k0 >> 3)];
-    }
+  for (int r = 0; r < 4 * NT; ++r) {  // entry r*32 + lane: token tile r/4, m pair r%4
+    const int tok = (r >> 2) * 8 + (lane >> 2), u = (lane & 3) * 4 + (r & 3);
+    v[r] = blk[tok * 16 + u];
   }
-  cons_sync();
+  __syncwarp();
 #pragma unroll
-  for (int r = 0; r < 8 * NT; ++r) {
-    const int si = ctid + r * NCT;
-    if (si < n) {
-      const uint32_t u[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
-      float e[8];
+  for (int r = 0; r < 4 * NT; ++r) {
+    const uint32_t w4[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+    float e[8];
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        e[2 * h] = __uint_as_float(u[h] << 16);
-        e[2 * h + 1] = __uint_as_float(u[h] & 0xffff0000u);
-      }
-      xs[si] = pack_frag8(e);
+    for (int h = 0; h < 4; ++h) {
+      e[2 * h] = __uint_as_float(w4[h] << 16);
+      e[2 * h + 1] = __uint_as_float(w4[h] & 0xffff0000u);
     }
+    blk[r * 32 + lane] = pack_frag8(e);
   }
-  cons_sync();
+  __syncwarp();
 }
 
 // n fragment entries from global memory into shared memory (consumer threads)
@@ -439,6 +447,24 @@ LMOE_COLD void plan(Tables& tb, int c, int nC, int NSF, int L, int d) {
   __syncwarp();
 }
 
+// One out-of-line copy of the ring-slot contraction (ring.cuh), shared by the
+// W_in, gate / up and W_out phases: the accumulators come back by value.
+template <int NT>
+struct Acc {
+  float v[NT][4];
+};
+template <int NT>
+__device__ __noinline__ Acc<NT> slot_mma(const unsigned char* w, int LPR, int row0, const uint16_t* s, int SS, int c0,
+                                         int nc, const uint4* frag) {
+  Acc<NT> r;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int h = 0; h < 4; ++h) r.v[nt][h] = 0.f;
+  mma_slot<NT>(w, LPR, row0, s, SS, c0, nc, frag, r.v);
+  return r;
+}
+
 // the group slot (index in glist) of expert slot es
 LMOE_DEV int group_slot(const Tables& tb, int es) {
   int gi = 0;
@@ -513,129 +539,83 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
     // ================================================== producer
     if (lane == 0) {
       const uint64_t pol = l2_evict_first();  // weights are read once per pass
-      int j = 0;
-      auto claim = [&](uint32_t bytes) -> unsigned char* {  // chunk j's slot, armed for `bytes`
-        const int s = j % NS, u = j / NS;
-        if (u > 0) mwait(tb, &tb.empty[s], (uint32_t)(u - 1) & 1u, budget, err, WS_EMPTY, diag);
-        if (tb.abort) return nullptr;
-        mbar_expect_tx(&tb.full[s], bytes);
-        return ring + s * SLOT;
-      };
-      bool ok = true;
+      const uint32_t CH = 18u * L, WCH = 9u * PW;  // bytes of a unit / W_out chunk, of a W_in chunk
       {  // x first: its loads are small and every CTA waits on them, so they
          // must not queue behind this CTA's weight copies
         const long long t0 = clock64();
 #pragma unroll 1
         while (!tb.x_issued && !tb.abort && clock64() - t0 < budget) __nanosleep(32);
       }
-      // A1: router rows
-#pragma unroll 1
-      for (int i = 0; ok && i < ne; ++i) {
-        unsigned char* dst = claim(4u * d);
-        if (!(ok = dst != nullptr)) break;
-        tma_load_3d_hint(dst, &F.maps.wr, 0, 0, e_lo + i, &tb.full[j % NS], pol);
-        if (trace && i == 0) trace[26] = gtime();
-        ++j;
-      }
-      // every W_in piece of this CTA into L2, behind the router rows: most of
-      // them wait for a ring slot until the router rows are consumed
-#pragma unroll 1
-      for (int i = 0; i < ntl; ++i)
-#pragma unroll 1
-        for (int p = 0; p < NPW; ++p) {
-          tma_prefetch_3d(&F.maps.win_q, 0, p * (PW / 256), (t_lo + i) * 16);
-          tma_prefetch_2d(&F.maps.win_s, p * (PW / 32), (t_lo + i) * 16);
-        }
-      // A2: W_in tiles in pieces of PW columns
-#pragma unroll 1
-      for (int i = 0; ok && i < ntl; ++i)
-#pragma unroll 1
-        for (int p = 0; ok && p < NPW; ++p) {
-          unsigned char* dst = claim(9u * PW);
-          if (!(ok = dst != nullptr)) break;
-          const int row0 = (t_lo + i) * 16;
-          tma_load_3d_hint(dst, &F.maps.win_q, 0, p * (PW / 256), row0, &tb.full[j % NS], pol);
-          tma_load_2d_hint(dst + 8 * PW, &F.maps.win_s, p * (PW / 32), row0, &tb.full[j % NS], pol);
-          ++j;
-        }
-      // the routing tables, from the consumers
-      if (ok) {
-        mwait(tb, &tb.tbar, 0u, budget, err, WS_TABLES, diag);
-        ok = !tb.abort;
-        if (trace) trace[13] = gtime();
-      }
-      const int u_lo = tb.u_lo, nu = ok ? tb.u_hi - tb.u_lo : 0;
-      const int o_lo = tb.o_lo, no = ok ? tb.o_hi - tb.o_lo : 0;
-      // Every chunk this CTA streams from here on, into L2; asked for once the
-      // ring holds the first units, so that their own copies do not queue
-      // behind the whole layer's prefetches.
+      // The CTA's chunks in ring order: router rows, W_in pieces, then (once
+      // the routing tables exist) gate / up / Down of each unit, then W_out.
+      // Prefetches into L2: the W_in pieces behind the router rows; the later
+      // units once the ring holds the first ones (so that their own copies do
+      // not queue behind the prefetches); W_out and the next layer's first
+      // chunks only once every unit is issued (they are needed last, and HBM
+      // time spent on them earlier is taken from the expert phase).
       const int npre = NS / 3;
-      auto prefetch_rest = [&]() {
+      int u_lo = 0, nu = 0, o_lo = 0, no = 0, jD = jB, jEnd = jB, j = 0;
 #pragma unroll 1
-        for (int q = npre; q < nu; ++q) {
-          const int u = u_lo + q, e = tb.elist[u / NSF], s = u % NSF, row = e * f + s * FS;
-          tma_prefetch_3d(&F.maps.gate_q, 0, 0, row);
-          tma_prefetch_2d(&F.maps.gate_s, 0, row);
-          tma_prefetch_3d(&F.maps.up_q, 0, 0, row);
-          tma_prefetch_2d(&F.maps.up_s, 0, row);
-          tma_prefetch_2d(&F.maps.dsl_q, 0, (e * NSF + s) * (L / 8));
-          tma_prefetch_2d(&F.maps.dsl_s, 0, (e * NSF + s) * (L / 256));
+      for (;; ++j) {
+        if (j == ne) {
+#pragma unroll 1
+          for (int i = 0; i < ntl * NPW; ++i) bulk_prefetch_l2(F.pk.win + ((size_t)t_lo * NPW + i) * WCH, WCH);
         }
-#pragma unroll 1
-        for (int q = 0; q < no; ++q) {
-          const int it = o_lo + q, row = tb.glist[it / (d / 32)] * d + (it % (d / 32)) * 32;
-          tma_prefetch_3d(&F.maps.wout_q, 0, 0, row);
-          tma_prefetch_2d(&F.maps.wout_s, 0, row);
+        if (j == jB) {  // the routing tables, from the consumers
+          mwait(tb, &tb.tbar, 0u, budget, err, WS_TABLES, diag);
+          if (tb.abort) break;
+          if (trace) trace[13] = gtime();
+          u_lo = tb.u_lo;
+          nu = tb.u_hi - tb.u_lo;
+          o_lo = tb.o_lo;
+          no = tb.o_hi - tb.o_lo;
+          jD = jB + 3 * nu;
+          jEnd = jD + no;
         }
-        if (F.has_next) {  // the next layer's first phase, behind this layer's requests
+        if (j == jB + 3 * npre && npre < nu) {
 #pragma unroll 1
-          for (int i = 0; i < ne; ++i) tma_prefetch_3d(&F.next_wr, 0, 0, e_lo + i);
-#pragma unroll 1
-          for (int i = 0; i < ntl; ++i)
-#pragma unroll 1
-            for (int p = 0; p < NPW; ++p) {
-              tma_prefetch_3d(&F.next_win_q, 0, p * (PW / 256), (t_lo + i) * 16);
-              tma_prefetch_2d(&F.next_win_s, p * (PW / 32), (t_lo + i) * 16);
-            }
+          for (int q = npre; q < nu; ++q) {
+            const int u = u_lo + q;
+            bulk_prefetch_l2(F.pk.unit + ((size_t)tb.elist[u / NSF] * NSF + u % NSF) * 3 * CH, 3 * CH);
+          }
         }
-      };
-      bool pf = !ok;
-      // B: per unit the gate slice, the up slice, the Down slice
+        if (j == jD && j >= jB) {
 #pragma unroll 1
-      for (int q = 0; ok && q < nu; ++q) {
-        if (q == npre) {
-          prefetch_rest();
-          pf = true;
+          for (int q = 0; q < no; ++q) {
+            const int it = o_lo + q;
+            bulk_prefetch_l2(F.pk.wout + ((size_t)tb.glist[it / (d / 32)] * (d / 32) + it % (d / 32)) * CH, CH);
+          }
+          if (F.has_next) {  // the next layer's first phase, behind this layer's requests
+#pragma unroll 1
+            for (int i = 0; i < ne; ++i)
+              bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(F.next_wr + (size_t)(e_lo + i) * d), 4u * d);
+#pragma unroll 1
+            for (int i = 0; i < ntl * NPW; ++i) bulk_prefetch_l2(F.next_win + ((size_t)t_lo * NPW + i) * WCH, WCH);
+          }
         }
-        const int u = u_lo + q, e = tb.elist[u / NSF], s = u % NSF, row = e * f + s * FS;
-        unsigned char* dst = claim(18u * L);
-        if (!(ok = dst != nullptr)) break;
-        tma_load_3d_hint(dst, &F.maps.gate_q, 0, 0, row, &tb.full[j % NS], pol);
-        if (trace && q == 0) trace[20] = gtime();
-        tma_load_2d_hint(dst + 16 * L, &F.maps.gate_s, 0, row, &tb.full[j % NS], pol);
-        ++j;
-        dst = claim(18u * L);
-        if (!(ok = dst != nullptr)) break;
-        tma_load_3d_hint(dst, &F.maps.up_q, 0, 0, row, &tb.full[j % NS], pol);
-        tma_load_2d_hint(dst + 16 * L, &F.maps.up_s, 0, row, &tb.full[j % NS], pol);
-        ++j;
-        dst = claim(18u * L);
-        if (!(ok = dst != nullptr)) break;
-        tma_load_2d_hint(dst, &F.maps.dsl_q, 0, (e * NSF + s) * (L / 8), &tb.full[j % NS], pol);
-        tma_load_2d_hint(dst + 16 * L, &F.maps.dsl_s, 0, (e * NSF + s) * (L / 256), &tb.full[j % NS], pol);
-        ++j;
-      }
-      if (ok && !pf) prefetch_rest();
-      // D: W_out, 32 rows of one group per chunk
-#pragma unroll 1
-      for (int q = 0; ok && q < no; ++q) {
-        const int it = o_lo + q, row = tb.glist[it / (d / 32)] * d + (it % (d / 32)) * 32;
-        unsigned char* dst = claim(18u * L);
-        if (!(ok = dst != nullptr)) break;
-        tma_load_3d_hint(dst, &F.maps.wout_q, 0, 0, row, &tb.full[j % NS], pol);
-        if (trace && q == 0) trace[24] = gtime();
-        tma_load_2d_hint(dst + 16 * L, &F.maps.wout_s, 0, row, &tb.full[j % NS], pol);
-        ++j;
+        if (j >= jB && j >= jEnd) break;
+        const uint8_t* src;
+        uint32_t bytes = CH;
+        if (j < ne) {
+          src = reinterpret_cast<const uint8_t*>(F.pk.wr + (size_t)(e_lo + j) * d);
+          bytes = 4u * d;
+        } else if (j < jB) {
+          src = F.pk.win + ((size_t)t_lo * NPW + (j - ne)) * WCH;
+          bytes = WCH;
+        } else if (j < jD) {
+          const int u = u_lo + (j - jB) / 3;
+          src = F.pk.unit + (((size_t)tb.elist[u / NSF] * NSF + u % NSF) * 3 + (j - jB) % 3) * CH;
+        } else {
+          const int it = o_lo + (j - jD);
+          src = F.pk.wout + ((size_t)tb.glist[it / (d / 32)] * (d / 32) + it % (d / 32)) * CH;
+        }
+        // chunk j's slot, once every consumer warp handed back its previous use
+        const int s = j % NS;
+        if (j >= NS) mwait(tb, &tb.empty[s], (uint32_t)(j / NS - 1) & 1u, budget, err, WS_EMPTY, diag);
+        if (tb.abort) break;
+        mbar_expect_tx(&tb.full[s], bytes);
+        bulk_load(ring + s * SLOT, src, bytes, &tb.full[s], pol);
+        if (trace && (j == 0 || j == jB || j == jD)) trace[j == 0 ? 26 : j == jD ? 24 : 20] = gtime();
       }
       // Wait for the copies still in flight before the CTA may exit. They do
       // not depend on other CTAs, so this drain gets a budget of its own.
@@ -675,7 +655,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
 #pragma unroll
         for (int n = 0; n < 8 * NT; ++n) {  // x as staged (bf16: exact in fp32)
           if (n >= T) break;
-          const uint4 xv = xf[n * (d / 8) + o];
+          const uint4 xv = xf[((o >> 4) * 8 * NT + n) * 16 + (o & 15)];
           float s = v[n];
           s = fmaf(a.x, __uint_as_float(xv.x << 16), s); s = fmaf(a.y, __uint_as_float(xv.x & 0xffff0000u), s);
           s = fmaf(a.z, __uint_as_float(xv.y << 16), s); s = fmaf(a.w, __uint_as_float(xv.y & 0xffff0000u), s);
@@ -718,53 +698,48 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
     }
   }
 
-  // ------------------------------------------------------------ A2 W_in
-  x_to_frags<NT>(xf, d, ctid);
-  if (trace && ctid == 0) trace[17] = gtime();
-  {
-    float acc[MAX_TILES][NT][4];
-#pragma unroll
-    for (int i = 0; i < MAX_TILES; ++i)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int h = 0; h < 4; ++h) acc[i][nt][h] = 0.f;
-    int c0, c1;
-    split(d / 128, warp, NCW, c0, c1);  // this warp's chunks of K (one piece)
-    const int pw = c0 / (PW / 128);
-#pragma unroll
-    for (int i = 0; i < MAX_TILES; ++i) {
-      if (i >= ntl) break;
+  // ------------------------------------------------------------ A2 W_in || routing
+  // Warps RW .. 15 compute H = W_in x while warps 0 .. RW-1 route: the routing
+  // needs every CTA's logits, W_in needs nothing but its chunks, so the two
+  // dependent fronts overlap instead of following each other.
+  if (warp >= RW) {
+    const int wt = ctid - RW * 32, wi = warp - RW;  // 0 .. 255, 0 .. 7
+    // task of warp wi: 16-row tile wi / 2 of this CTA, and either piece wi % 2
+    // of its K (two pieces) or half wi % 2 of its one piece
+    const int ti = wi >> 1, sub = wi & 1, CPP = PW / 128;
+    const int tp = NPW == 2 ? sub : 0, k0c = NPW == 2 ? 0 : sub * (CPP / 2), nkc = NPW == 2 ? CPP : CPP / 2;
+    {  // x chunks -> fragments, d/1024 chunks per warp
+      const int per = d / 128 / (NCW - RW);
 #pragma unroll 1
-      for (int p = 0; p < NPW; ++p) {
-        const int j = jA2 + i * NPW + p;
-        if (p == pw && c1 > c0) {
-          bool landed;
-          const unsigned char* sl = acquire<NS>(tb, ring, j, budget, err, WS_WIN_SLOT, diag, landed);
-          if (trace && ctid == 0 && i == 0) trace[19] = gtime();
-          mma_slot<NT>(sl, PW / 256, 0, reinterpret_cast<const uint16_t*>(sl + 8 * PW), PW / 32, c0 - p * (PW / 128),
-                       c1 - c0, xf + (size_t)c0 * FR, acc[i]);
-          release_read<NS>(tb, j, landed);
-        } else {  // not read by this warp: handed back once it landed (see release)
-          bool landed;
-          acquire<NS>(tb, ring, j, budget, err, WS_WIN_SLOT, diag, landed);
-          release_read<NS>(tb, j, landed);
-        }
+      for (int cc = wi * per; cc < (wi + 1) * per; ++cc) chunk_to_frags<NT>(xf, cc);
+    }
+    group_sync(BAR_WIN, NCT - RW * 32);
+    if (trace && wt == 0) trace[17] = gtime();
+    Acc<NT> acc;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int h = 0; h < 4; ++h) acc.v[nt][h] = 0.f;
+#pragma unroll 1
+    for (int jj = 0; jj < ntl * NPW; ++jj) {
+      bool landed;
+      const unsigned char* sl = acquire<NS>(tb, ring, jA2 + jj, budget, err, WS_WIN_SLOT, diag, landed);
+      if (jj == ti * NPW + tp) {
+        if (trace && wt == 0) trace[19] = gtime();
+        acc = slot_mma<NT>(sl, PW / 256, 0, reinterpret_cast<const uint16_t*>(sl + 8 * PW), PW / 32, k0c, nkc,
+                           xf + (size_t)(tp * CPP + k0c) * FR);
       }
+      release_read<NS>(tb, jA2 + jj, landed);  // a chunk this warp does not read is handed back once it landed
     }
-    cons_sync();  // every warp is done with x: its region takes the partials
+    group_sync(BAR_WIN, NCT - RW * 32);  // every W_in warp is done with x: its region takes the partials
 #pragma unroll
-    for (int i = 0; i < MAX_TILES; ++i) {
-      if (i >= ntl) break;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-        pbuf[((i * NCW + warp) * NT + nt) * 32 + lane] = make_float4(acc[i][nt][0], acc[i][nt][1], acc[i][nt][2], acc[i][nt][3]);
-    }
-    cons_sync();
-    // H rows: thread (tile, token n, row r), warps summed in order; eight
-    // consecutive rows of a token gathered into one fragment entry
+    for (int nt = 0; nt < NT; ++nt)
+      pbuf[(wi * NT + nt) * 32 + lane] = make_float4(acc.v[nt][0], acc.v[nt][1], acc.v[nt][2], acc.v[nt][3]);
+    group_sync(BAR_WIN, NCT - RW * 32);
+    // H rows: thread (tile, token n, row r), the tile's two partials summed in
+    // order; eight consecutive rows of a token gathered into one fragment entry
 #pragma unroll 1
-    for (int idx = ctid; idx < MAX_TILES * FR; idx += NCT) {  // FR = 16 rows x 8 NT tokens per tile
+    for (int idx = wt; idx < MAX_TILES * FR; idx += NCT - RW * 32) {  // FR = 16 rows x 8 NT tokens per tile
       const int i = idx / FR, rem = idx % FR, n = rem >> 4, r = rem & 15;
       if (i >= ntl) break;  // warp-uniform: a warp's 32 threads share i
       const int ll = (r & 7) * 4 + ((n & 7) >> 1), h = 2 * (r >> 3) + (n & 1), nt = n >> 3;
@@ -772,7 +747,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
       const int tg = t_lo + i, g = tg / (L / 16), rt = tg % (L / 16);
       float s = 0.f;
 #pragma unroll
-      for (int w = 0; w < NCW; ++w) s += pf[(((i * NCW + w) * NT + nt) * 32 + ll) * 4 + h];
+      for (int w = 0; w < 2; ++w) s += pf[((((2 * i + w) * NT + nt) * 32 + ll) << 2) + h];
       if (F.hl && n < T) s += __ldcg(F.hl + ((size_t)g * 16 + n) * L + rt * 16 + r);  // the LoRA branch
       float e[8];
 #pragma unroll
@@ -781,41 +756,49 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
         F.Hf[(size_t)g * CL * FR + entry_index<NT>(rt * 16 + (r & 8), n)] = pack_frag8(e);
       }
     }
-    cons_sync();
-    if (ctid == 0) {
+    group_sync(BAR_WIN, NCT - RW * 32);
+    if (wt == 0) {
       fence_gpu();
 #pragma unroll 1
       for (int i = 0; i < ntl; ++i) atomicAdd(ctr + cm.done_in + ((t_lo + i) / (L / 16)) * CSTR, 1u);
       if (trace) trace[3] = gtime();
     }
-  }
-
-  // ------------------------------------------------------------ routing
-  // Every CTA routes all tokens itself: a warp per token selects the top-k
-  // (topk.cuh), then one warp builds the tables and the work split.
-  if (ctid == 0) wait_ge(tb, ctr + cm.done_router, (unsigned)nC, budget, err, WS_LOGITS, diag);
-  cons_sync();
-  if (trace && ctid == 0) trace[15] = gtime();
-  if (warp < T) {
-    const float2 sw = topk_warp_thr(F.logits + (size_t)warp * E, E, k, tb.u.tkscr[warp]);
-    if (lane < k) {
-      const int e = __float_as_int(sw.x);
-      tb.idx[warp * 16 + lane] = e;
-      tb.w[warp * 16 + lane] = sw.y;
-      atomicOr(&tb.emask[e >> 5], 1u << (e & 31));
-      if (c == 0) {
-        A.idx[warp * k + lane] = e;
-        A.w[warp * k + lane] = sw.y;
+  } else {
+    // Every CTA routes all tokens itself: a warp per token selects the top-k
+    // (topk.cuh), then one warp builds the tables and the work split.
+    if (ctid == 0) wait_ge(tb, ctr + cm.done_router, (unsigned)nC, budget, err, WS_LOGITS, diag);
+    group_sync(BAR_ROUTE, RW * 32);
+    if (trace && ctid == 0) trace[15] = gtime();
+#pragma unroll 1
+    for (int t = warp; t < T; t += RW) {
+      const float2 sw = topk_warp_thr(F.logits + (size_t)t * E, E, k, tb.u.tkscr[warp]);
+      if (lane < k) {
+        const int e = __float_as_int(sw.x);
+        tb.idx[t * 16 + lane] = e;
+        tb.w[t * 16 + lane] = sw.y;
+        atomicOr(&tb.emask[e >> 5], 1u << (e & 31));
+        if (c == 0) {
+          A.idx[t * k + lane] = e;
+          A.w[t * k + lane] = sw.y;
+        }
       }
+      __syncwarp();
     }
-  }
-  cons_sync();
-  if (trace && ctid == 0) trace[11] = gtime();
-  if (warp == 0) {
-    build_tables(tb, epg);
-    if (trace && lane == 0) trace[16] = gtime();
-    plan(tb, c, nC, NSF, L, d);
-    if (lane == 0) mbar_arrive(&tb.tbar);  // the producer may stream the expert weights
+    group_sync(BAR_ROUTE, RW * 32);
+    if (trace && ctid == 0) trace[11] = gtime();
+    if (warp == 0) {
+      build_tables(tb, epg);
+      if (trace && lane == 0) trace[16] = gtime();
+      plan(tb, c, nC, NSF, L, d);
+      if (lane == 0) mbar_arrive(&tb.tbar);  // the producer may stream the expert weights
+    }
+    // the W_in chunks, handed back once they landed (this warp reads none)
+#pragma unroll 1
+    for (int j = jA2; j < jB; ++j) {
+      bool landed;
+      acquire<NS>(tb, ring, j, budget, err, WS_WIN_SLOT, diag, landed);
+      release_read<NS>(tb, j, landed);
+    }
   }
   cons_sync();
   if (trace && ctid == 0) trace[4] = gtime();
@@ -871,7 +854,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
           const unsigned char* sl = acquire<NS>(tb, ring, jg + mat, budget, err, WS_GU_SLOT, diag, landed);
           if (trace && ctid == 0 && q == 0) trace[21] = gtime();
           mma_slot<NT>(sl, L / 256, 16 * mt, reinterpret_cast<const uint16_t*>(sl + 16 * L), L / 32, gc0, gc1 - gc0,
-                       xf + (size_t)gc0 * FR, a);
+                       xf + (size_t)gc0 * FR, a);  // inline: the Down accumulators stay live across it
           release_read<NS>(tb, jg + mat, landed);
         }
 #pragma unroll
@@ -1036,8 +1019,12 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
         bool landed;
         const unsigned char* sl = acquire<NS>(tb, ring, jD + q, budget, err, WS_WOUT_SLOT, diag, landed);
         if (trace && ctid == 0 && q == 0) trace[25] = gtime();
-        mma_slot<NT>(sl, L / 256, 16 * wm, reinterpret_cast<const uint16_t*>(sl + 16 * L), L / 32, oc0, oc1 - oc0,
-                     xf + (size_t)oc0 * FR, a);
+        const Acc<NT> t = slot_mma<NT>(sl, L / 256, 16 * wm, reinterpret_cast<const uint16_t*>(sl + 16 * L), L / 32, oc0,
+                                       oc1 - oc0, xf + (size_t)oc0 * FR);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int h = 0; h < 4; ++h) a[nt][h] = t.v[nt][h];
         release_read<NS>(tb, jD + q, landed);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -1119,60 +1106,103 @@ size_t fused_counter_words(int d, int E, int G, int L) {
 size_t fused_zpart_bytes(int G, int L, int grid) { return (size_t)(grid + G) * 16 * L * 4; }
 size_t fused_diag_bytes(int grid) { return (size_t)(1 + 32 * grid) * 8; }
 
+// ------------------------------------------------------------ streaming pack
 namespace {
-// packed int4 [rows][K/2] as [rows][K/256][128 B], box {128, lines, box_rows}
-bool map_q(CUtensorMap* m, const uint8_t* q, long long rows, int K, int lines, int box_rows) {
-  const cuuint64_t dims[3] = {128, (cuuint64_t)(K / 256), (cuuint64_t)rows};
-  const cuuint64_t strides[2] = {128, (cuuint64_t)(K / 2)};
-  const cuuint32_t box[3] = {128, (cuuint32_t)lines, (cuuint32_t)box_rows};
-  return tmap_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, q, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+// One chunk per CTA: `rows` rows of `wb` bytes of packed int4 (wb a multiple
+// of 128) from q (row stride qs bytes), rows band*rows .. and bytes piece*wb ..
+// of each row, written as 128-byte lines in the 128-byte swizzle (16-byte unit
+// u of line i at unit u ^ (i & 7)); then the same rows' `wsc` bf16 scales
+// from s (row stride ss), columns piece*wsc ... Chunk c (band c / npc, piece
+// c % npc) goes to out + c * cstride + coff.
+struct PackSpec {
+  const uint8_t* q;
+  size_t qs;
+  const uint16_t* s;
+  size_t ss;
+  int rows, wb, wsc, npc;
+  uint8_t* out;
+  size_t cstride, coff;
+};
+
+__global__ void __launch_bounds__(256) pack_swz_kernel(PackSpec P) {
+  const int c = blockIdx.x, band = c / P.npc, piece = c % P.npc;
+  const size_t row0 = (size_t)band * P.rows;
+  uint8_t* dst = P.out + (size_t)c * P.cstride + P.coff;
+  const int lpr = P.wb / 128, nu = P.rows * lpr * 8;
+  for (int i = threadIdx.x; i < nu; i += blockDim.x) {
+    const int line = i >> 3, u = i & 7, r = line / lpr, li = line % lpr;
+    const uint4 v = *reinterpret_cast<const uint4*>(P.q + (row0 + r) * P.qs + (size_t)piece * P.wb + li * 128 + u * 16);
+    *reinterpret_cast<uint4*>(dst + line * 128 + ((u ^ (line & 7)) << 4)) = v;
+  }
+  uint16_t* sd = reinterpret_cast<uint16_t*>(dst + (size_t)P.rows * P.wb);
+  for (int i = threadIdx.x; i < P.rows * P.wsc; i += blockDim.x) {
+    const int r = i / P.wsc, cc = i % P.wsc;
+    sd[i] = P.s[(row0 + r) * P.ss + (size_t)piece * P.wsc + cc];
+  }
 }
 
-// bf16 scales [rows][K/32], box {box_cols, box_rows}
-bool map_s(CUtensorMap* m, const uint16_t* s, long long rows, int K, int box_cols, int box_rows) {
-  const cuuint64_t dims[2] = {(cuuint64_t)(K / 32), (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)(K / 32 * 2)};
-  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
-  return tmap_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, s, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+// The Down columns of unit c = (e, slice): for every latent row l, the 16
+// bytes of Down_e[l] holding the slice's 32 int4 ([L][16 B], unswizzled),
+// then the rows' scales of that slice ([L] bf16).
+__global__ void __launch_bounds__(256) pack_down_kernel(const uint8_t* q, const uint16_t* s, int L, int f,
+                                                        uint8_t* unit) {
+  const int nsf = f / FS, c = blockIdx.x, e = c / nsf, sl = c % nsf;
+  uint8_t* dst = unit + ((size_t)c * 3 + 2) * 18 * L;
+  for (int l = threadIdx.x; l < L; l += blockDim.x) {
+    const size_t row = (size_t)e * L + l;
+    *reinterpret_cast<uint4*>(dst + (size_t)l * 16) = *reinterpret_cast<const uint4*>(q + row * (f / 2) + sl * 16);
+    reinterpret_cast<uint16_t*>(dst + (size_t)16 * L)[l] = s[row * nsf + sl];
+  }
+}
+
+size_t al256(size_t v) { return (v + 255) & ~(size_t)255; }
+struct PackLayout {
+  size_t win, unit, wout, end;
+};
+PackLayout pack_layout(int d, int E, int G, int L, int f) {
+  const int PW = d < 2048 ? d : 2048;
+  PackLayout p;
+  p.win = 0;
+  p.unit = al256(p.win + (size_t)G * (L / 16) * (d / PW) * 9 * PW);
+  p.wout = al256(p.unit + (size_t)E * (f / FS) * 3 * 18 * L);
+  p.end = al256(p.wout + (size_t)G * (d / 32) * 18 * L);
+  return p;
 }
 }  // namespace
 
-bool fused_make_maps(const DecodeArgs& A, const uint8_t* dsl_q, const uint16_t* dsl_s, DecodeMaps* mp) {
-  if (!tmap_encode_fn() || !A.W_r || !dsl_q || !dsl_s) return false;
-  const int d = A.d, E = A.E, G = A.G, L = A.L, f = A.f;
-  const int PW = d < 2048 ? d : 2048;
-  bool ok = true;
-  {  // W_r as [E][d/256][256] fp32, one whole row per box
-    const cuuint64_t dims[3] = {256, (cuuint64_t)(d / 256), (cuuint64_t)E};
-    const cuuint64_t strides[2] = {1024, (cuuint64_t)d * 4};
-    const cuuint32_t box[3] = {256, (cuuint32_t)(d / 256), 1};
-    ok = ok && tmap_encode(&mp->wr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, A.W_r, dims, strides, box,
-                           CU_TENSOR_MAP_SWIZZLE_NONE);
-  }
-  ok = ok && map_q(&mp->win_q, A.W_in_q, (long long)G * L, d, PW / 256, 16);
-  ok = ok && map_s(&mp->win_s, A.W_in_s, (long long)G * L, d, PW / 32, 16);
-  ok = ok && map_q(&mp->gate_q, A.gate_q, (long long)E * f, L, L / 256, FS);
-  ok = ok && map_s(&mp->gate_s, A.gate_s, (long long)E * f, L, L / 32, FS);
-  ok = ok && map_q(&mp->up_q, A.up_q, (long long)E * f, L, L / 256, FS);
-  ok = ok && map_s(&mp->up_s, A.up_s, (long long)E * f, L, L / 32, FS);
-  {  // the slice-major copy of Down: [E][f/32][L][16 B] as 128-byte lines
-    const cuuint64_t dims[2] = {128, (cuuint64_t)E * (f / FS) * L / 8};
-    const cuuint64_t strides[1] = {128};
-    const cuuint32_t box[2] = {128, (cuuint32_t)(L / 8)};
-    ok = ok && tmap_encode(&mp->dsl_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dsl_q, dims, strides, box,
-                           CU_TENSOR_MAP_SWIZZLE_NONE);
-    const cuuint64_t sd[2] = {256, (cuuint64_t)E * (f / FS) * L / 256};
-    const cuuint64_t ss[1] = {512};
-    const cuuint32_t sb[2] = {256, (cuuint32_t)(L / 256)};
-    ok = ok && tmap_encode(&mp->dsl_s, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, dsl_s, sd, ss, sb, CU_TENSOR_MAP_SWIZZLE_NONE);
-  }
-  ok = ok && map_q(&mp->wout_q, A.W_out_q, (long long)G * A.d, L, L / 256, 32);
-  ok = ok && map_s(&mp->wout_s, A.W_out_s, (long long)G * A.d, L, L / 32, 32);
-  return ok;
+size_t decode_pack_bytes(int d, int E, int G, int L, int f) { return pack_layout(d, E, G, L, f).end; }
+
+cudaError_t launch_decode_pack(const DecodeArgs& A, uint8_t* buf, DecodePack* pk, cudaStream_t st) {
+  const int d = A.d, E = A.E, G = A.G, L = A.L, f = A.f, PW = d < 2048 ? d : 2048, nsf = f / FS;
+  const PackLayout lay = pack_layout(d, E, G, L, f);
+  pk->wr = A.W_r;
+  pk->win = buf + lay.win;
+  pk->unit = buf + lay.unit;
+  pk->wout = buf + lay.wout;
+  // W_in: 16-row tiles in pieces of PW columns
+  PackSpec w{A.W_in_q, (size_t)d / 2, A.W_in_s, (size_t)d / 32, 16, PW / 2, PW / 32, d / PW, buf + lay.win,
+             (size_t)9 * PW, 0};
+  pack_swz_kernel<<<G * (L / 16) * (d / PW), 256, 0, st>>>(w);
+  // gate and up: 32 rows (one f-slice of one expert) each, at parts 0 and 1 of the unit
+  PackSpec g{A.gate_q, (size_t)L / 2, A.gate_s, (size_t)L / 32, FS, L / 2, L / 32, 1, buf + lay.unit,
+             (size_t)3 * 18 * L, 0};
+  pack_swz_kernel<<<E * nsf, 256, 0, st>>>(g);
+  PackSpec u = g;
+  u.q = A.up_q;
+  u.s = A.up_s;
+  u.coff = (size_t)18 * L;
+  pack_swz_kernel<<<E * nsf, 256, 0, st>>>(u);
+  pack_down_kernel<<<E * nsf, 256, 0, st>>>(A.down_q, A.down_s, L, f, buf + lay.unit);
+  // W_out: 32-row blocks
+  PackSpec o{A.W_out_q, (size_t)L / 2, A.W_out_s, (size_t)L / 32, 32, L / 2, L / 32, 1, buf + lay.wout,
+             (size_t)18 * L, 0};
+  pack_swz_kernel<<<G * (d / 32), 256, 0, st>>>(o);
+  return cudaGetLastError();
 }
 
 bool fused_decode_supported(const DecodeArgs& A, int grid) {
   if ((A.r != 0 && !lora_fused_supported(A)) || A.T < 1 || A.T > 16 || grid < 1) return false;
+  if (!A.W_r || (reinterpret_cast<uintptr_t>(A.W_r) & 15) != 0) return false;  // router rows by bulk copy
   if (A.E > 512 || A.G > 64 || A.k > 16 || A.E > MAX_RX * grid) return false;
   if (A.d > 4096 || !(A.d == 1024 || A.d % 2048 == 0)) return false;  // router rows and W_in pieces
   if (A.L != 256 && A.L != 512 && A.L != 1024) return false;
@@ -1180,28 +1210,6 @@ bool fused_decode_supported(const DecodeArgs& A, int grid) {
   if ((long long)A.G * (A.L / 16) > (long long)MAX_TILES * grid) return false;
   return true;
 }
-
-// Down [E][L][f/2] -> [E][f/32][L][16 B]; its scales [E][L][f/32] -> [E][f/32][L]
-__global__ void repack_down_kernel(const uint4* __restrict__ q, const uint16_t* __restrict__ s, int E, int L, int f,
-                                   uint4* __restrict__ qo, uint16_t* __restrict__ so) {
-  const int nsf = f / FS;
-  const size_t n = (size_t)E * nsf * L;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-    const size_t e = i / ((size_t)nsf * L), rem = i % ((size_t)nsf * L);
-    const int sl = (int)(rem / L), l = (int)(rem % L);
-    qo[i] = q[(e * L + l) * nsf + sl];
-    so[i] = s[(e * L + l) * nsf + sl];
-  }
-}
-
-cudaError_t launch_repack_down(const uint8_t* q, const uint16_t* s, int E, int L, int f, uint8_t* qo, uint16_t* so,
-                               cudaStream_t st) {
-  repack_down_kernel<<<592, 256, 0, st>>>(reinterpret_cast<const uint4*>(q), s, E, L, f, reinterpret_cast<uint4*>(qo),
-                                          so);
-  return cudaGetLastError();
-}
-
-size_t fused_down_copy_bytes(int E, int L, int f) { return (size_t)E * L * f / 2 + (size_t)E * L * (f / FS) * 2; }
 
 cudaError_t fused_set_attributes() {
   cudaFuncSetAttribute(decode_fused_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<1>());

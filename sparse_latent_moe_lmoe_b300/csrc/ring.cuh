@@ -70,6 +70,20 @@ LMOE_DEV void tma_prefetch_3d(const void* tmap, int c0, int c1, int c2) {
                : "memory");
 }
 
+// Bulk (untiled) copy of `bytes` from global into shared memory, completing
+// on mbarrier m; both addresses 16-byte aligned, bytes a multiple of 16.
+LMOE_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* m, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(m)), "l"(pol)
+      : "memory");
+}
+// Prefetch of `bytes` of global memory into L2 (same alignment rules).
+LMOE_DEV void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 LMOE_DEV bool mbar_test(uint64_t* m, uint32_t parity) {
   uint32_t ok;
   asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
