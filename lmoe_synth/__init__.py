@@ -59,6 +59,9 @@ def _L():
         lib.synth_int4_matrix.argtypes = [u64, u64, i64, ctypes.c_int, d, p, p]
         lib.synth_int4_matrix.restype = ctypes.c_int
         lib.synth_int4_source.argtypes = [u64, u64, i64, ctypes.c_int, d, p]
+        lib.synth_nvfp4_matrix.argtypes = [u64, u64, i64, ctypes.c_int, d, i64, p, p, p]
+        lib.synth_e4m3_rne.argtypes = [ctypes.c_float]
+        lib.synth_e4m3_rne.restype = ctypes.c_uint8
         lib.synth_zipf_bias.argtypes = [u64, ctypes.c_int, d, p]
         lib.synth_routing.argtypes = [u64, ctypes.c_int, ctypes.c_int, ctypes.c_int, d, p, p]
         lib.synth_set_threads.argtypes = [ctypes.c_int]
@@ -98,6 +101,23 @@ def int4_matrix(seed: int, stream: int, rows: int, K: int, sigma: float):
     return q, s
 
 
+def nvfp4_matrix(seed: int, stream: int, rows: int, K: int, sigma: float, rows_per_tensor: int):
+    """The same draws as int4_matrix in NVFP4: (E2M1 codes u8 [rows][K/2],
+    E4M3 block scales u8 [rows][K/16], fp32 tensor scales [rows/rows_per_tensor])."""
+    q = np.empty((rows, K // 2), np.uint8)
+    s = np.empty((rows, K // 16), np.uint8)
+    gs = np.empty(rows // rows_per_tensor, np.float32)
+    rc = _L().synth_nvfp4_matrix(seed, stream, rows, K, sigma, rows_per_tensor, _ptr(q), _ptr(s), _ptr(gs))
+    if rc != 0:
+        raise ValueError("K must be a multiple of 16 and rows a multiple of rows_per_tensor")
+    return q, s, gs
+
+
+def e4m3_rne(x: float) -> int:
+    """The quantiser's fp32 -> E4M3 rounding (x >= 0, saturating at 448)."""
+    return int(_L().synth_e4m3_rne(float(x)))
+
+
 def int4_source(seed: int, stream: int, rows: int, K: int, sigma: float) -> np.ndarray:
     """The fp32 draws that int4_matrix quantises."""
     out = np.empty((rows, K), np.float32)
@@ -132,6 +152,7 @@ class LayerShape:
     f: int
     lora_rank: int = 0
     has_bias: bool = False
+    wfmt: str = "int4"  # or "nvfp4"
 
     @property
     def epg(self) -> int:
@@ -149,6 +170,10 @@ WORKLOADS = {
     "decode_t8": (EDGE0, 8, 0, 1, None, None),
     "prefill_t16384_zipf": (replace(EDGE0, has_bias=True), 16384, 0, 1, 2, None),
     "lora_t16": (replace(EDGE0, lora_rank=64), 16, 0, 1, None, 3),
+    # the same layers with NVFP4 weights (the same fp32 draws, quantised to NVIDIA's FP4 format)
+    "tiny_t64_nvfp4": (replace(TINY, wfmt="nvfp4"), 64, 0, 0, None, None),
+    "decode_t8_nvfp4": (replace(EDGE0, wfmt="nvfp4"), 8, 0, 1, None, None),
+    "prefill_t16384_zipf_nvfp4": (replace(EDGE0, has_bias=True, wfmt="nvfp4"), 16384, 0, 1, 2, None),
 }
 
 W_SIGMA = 0.02       # int4 weights and router before quantisation
@@ -162,16 +187,16 @@ def make_layer(shape: LayerShape, seed: int, bias_seed: int | None = None, lora_
     W = {}
     W["W_r"] = normal_f32(seed, S_WR, (E, d), W_SIGMA)
     W["b_r"] = zipf_bias(bias_seed, E, zipf_s) if shape.has_bias else None
-    q, s = int4_matrix(seed, S_WIN, G * L, d, W_SIGMA)
-    W["W_in_q"], W["W_in_s"] = q.reshape(G, L, d // 2), s.reshape(G, L, d // 32)
-    q, s = int4_matrix(seed, S_WOUT, G * d, L, W_SIGMA)
-    W["W_out_q"], W["W_out_s"] = q.reshape(G, d, L // 2), s.reshape(G, d, L // 32)
-    q, s = int4_matrix(seed, S_GATE, E * f, L, W_SIGMA)
-    W["gate_q"], W["gate_s"] = q.reshape(E, f, L // 2), s.reshape(E, f, L // 32)
-    q, s = int4_matrix(seed, S_UP, E * f, L, W_SIGMA)
-    W["up_q"], W["up_s"] = q.reshape(E, f, L // 2), s.reshape(E, f, L // 32)
-    q, s = int4_matrix(seed, S_DOWN, E * L, f, W_SIGMA)
-    W["down_q"], W["down_s"] = q.reshape(E, L, f // 2), s.reshape(E, L, f // 32)
+    # (name, stream, tensors, rows per tensor, K)
+    mats = [("W_in", S_WIN, G, L, d), ("W_out", S_WOUT, G, d, L), ("gate", S_GATE, E, f, L), ("up", S_UP, E, f, L),
+            ("down", S_DOWN, E, L, f)]
+    for name, stream, nt, rows, K in mats:
+        if shape.wfmt == "nvfp4":
+            q, s, gs = nvfp4_matrix(seed, stream, nt * rows, K, W_SIGMA, rows)
+            W[name + "_q"], W[name + "_s"], W[name + "_gs"] = q.reshape(nt, rows, K // 2), s.reshape(nt, rows, K // 16), gs
+        else:
+            q, s = int4_matrix(seed, stream, nt * rows, K, W_SIGMA)
+            W[name + "_q"], W[name + "_s"], W[name + "_gs"] = q.reshape(nt, rows, K // 2), s.reshape(nt, rows, K // 32), None
     if r > 0:
         ls = seed if lora_seed is None else lora_seed
         W["A_in"] = normal_bf16(ls, S_AIN, (G, d, r), LORA_A_SIGMA)

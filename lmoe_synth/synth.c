@@ -179,6 +179,103 @@ int synth_int4_matrix(uint64_t seed, uint64_t stream, int64_t rows, int K, doubl
   return 0;
 }
 
+/* ---------------------------------------------------------------------------
+ * NVFP4 weights (NVIDIA's FP4 format): the same fp32 draws as
+ * synth_int4_matrix, quantised per tensor of rows_per_tensor rows:
+ *   gs = amax(tensor) / (6 * 448)                        (fp32; 0 if amax == 0)
+ *   per block of 16 consecutive elements along K:
+ *     sb = e4m3_rne(amax(block) / 6 / gs), saturated at 448 (0 if gs == 0)
+ *     code_i = e2m1_rne(w_i / (e4m3(sb) * gs)), saturated at 6 (0 if sb == 0)
+ * E2M1 codes are packed two per byte like the int4 format (element 2j in the
+ * low nibble; bit 3 = sign); block scales [rows][K/16] bytes; gs [tensors].
+ * Ties go to the even code (mantissa bit 0) in both roundings.
+ */
+static const float E2M1_MAG[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
+
+static int e2m1_rne(float v) {
+  const float a = fabsf(v);
+  int best = 7;
+  if (a < 6.f) {
+    float bd = INFINITY;
+    for (int c = 0; c < 8; c++) {
+      const float dd = fabsf(a - E2M1_MAG[c]);
+      if (dd < bd || (dd == bd && (c & 1) == 0)) {
+        bd = dd;
+        best = c;
+      }
+    }
+  }
+  return (v < 0.f ? 8 : 0) | best;
+}
+
+static float e4m3_val(uint8_t b) {
+  const int e = (b >> 3) & 15, m = b & 7;
+  return e == 0 ? ldexpf((float)m / 8.f, -6) : ldexpf(1.f + (float)m / 8.f, e - 7);
+}
+
+/* x >= 0 -> the nearest E4M3 byte (ties to even mantissa), saturated at 448 */
+uint8_t synth_e4m3_rne(float x) {
+  if (!(x > 0.f)) return 0;
+  if (x >= 448.f) return 0x7E;
+  if (x < ldexpf(1.f, -6)) {
+    const int m = (int)nearbyintf(x / ldexpf(1.f, -9)); /* 0 .. 8; 8 is the smallest normal */
+    return (uint8_t)m;
+  }
+  int ex;
+  const float fr = frexpf(x, &ex); /* x = fr * 2^ex, fr in [0.5, 1) */
+  int e = ex - 1;
+  int m = (int)nearbyintf((fr * 2.f - 1.f) * 8.f);
+  if (m == 8) {
+    m = 0;
+    e += 1;
+  }
+  if (e + 7 > 15 || (e + 7 == 15 && m == 7)) return 0x7E;
+  return (uint8_t)(((e + 7) << 3) | m);
+}
+
+typedef struct { uint64_t key; double sigma; int K; int64_t rpt; uint8_t* q; uint8_t* s; float* gs; } nvctx;
+
+static void nvfp4_tensors(void* c, int64_t lo, int64_t hi) {
+  nvctx* x = (nvctx*)c;
+  const int K = x->K;
+  float w[16];
+  for (int64_t t = lo; t < hi; t++) {
+    float amax = 0.f;
+    for (int64_t r = t * x->rpt; r < (t + 1) * x->rpt; r++)
+      for (int c2 = 0; c2 < K; c2++) {
+        const float a = fabsf((float)(x->sigma * normal_at(x->key, (uint64_t)r * (uint64_t)K + (uint64_t)c2)));
+        if (a > amax) amax = a;
+      }
+    const float gs = amax / (6.f * 448.f);
+    x->gs[t] = gs;
+    for (int64_t r = t * x->rpt; r < (t + 1) * x->rpt; r++)
+      for (int b = 0; b < K / 16; b++) {
+        float ab = 0.f;
+        for (int i = 0; i < 16; i++) {
+          w[i] = (float)(x->sigma * normal_at(x->key, (uint64_t)r * (uint64_t)K + (uint64_t)(b * 16 + i)));
+          if (fabsf(w[i]) > ab) ab = fabsf(w[i]);
+        }
+        const uint8_t sb = gs > 0.f ? synth_e4m3_rne(ab / 6.f / gs) : 0;
+        x->s[r * (K / 16) + b] = sb;
+        const float denom = e4m3_val(sb) * gs;
+        uint8_t* qb = x->q + r * (K / 2) + b * 8;
+        for (int i = 0; i < 16; i += 2) {
+          const int c0 = denom > 0.f ? e2m1_rne(w[i] / denom) : 0;
+          const int c1 = denom > 0.f ? e2m1_rne(w[i + 1] / denom) : 0;
+          qb[i / 2] = (uint8_t)(c0 | (c1 << 4));
+        }
+      }
+  }
+}
+
+int synth_nvfp4_matrix(uint64_t seed, uint64_t stream, int64_t rows, int K, double sigma, int64_t rows_per_tensor,
+                       uint8_t* q, uint8_t* scales, float* gs) {
+  if (K % 16 != 0 || rows < 0 || rows_per_tensor <= 0 || rows % rows_per_tensor != 0) return -1;
+  nvctx c = {stream_key(seed, stream), sigma, K, rows_per_tensor, q, scales, gs};
+  parallel_for(rows / rows_per_tensor, 1, nvfp4_tensors, &c);
+  return 0;
+}
+
 /* the same fp32 draws synth_int4_matrix quantises (for tests of the quantiser) */
 void synth_int4_source(uint64_t seed, uint64_t stream, int64_t rows, int K, double sigma, float* out) {
   uint64_t key = stream_key(seed, stream);

@@ -29,10 +29,14 @@ def build(force: bool = False) -> str:
     return _SO
 
 
+_GS = ("W_in_gs", "W_out_gs", "gate_gs", "up_gs", "down_gs")
+
+
 class _Layer(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("d", "E", "G", "k", "L", "f", "r")] + [
         (n, ctypes.c_void_p) for n in ("W_r", "b_r", "W_in_q", "W_in_s", "W_out_q", "W_out_s", "gate_q", "gate_s",
-                                       "up_q", "up_s", "down_q", "down_s", "A_in", "B_in", "A_out", "B_out")]
+                                       "up_q", "up_s", "down_q", "down_s", "A_in", "B_in", "A_out", "B_out")] + [
+        ("wfmt", ctypes.c_int)] + [(n, ctypes.c_void_p) for n in _GS]
 
 
 def _p(a):
@@ -54,6 +58,11 @@ def _lib_():
         lib.oracle_int4_at.argtypes = [P, I]
         lib.oracle_int4_at.restype = I
         lib.oracle_dequant_rows.argtypes = [P, P, I, I64, I, P]
+        lib.oracle_e2m1_value.argtypes = [I]
+        lib.oracle_e2m1_value.restype = ctypes.c_double
+        lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_value.restype = ctypes.c_double
+        lib.oracle_nvfp4_dequant_rows.argtypes = [P, P, ctypes.c_double, I, I64, I, P]
         lib.oracle_router_logits.argtypes = [P, I, P, P]
         lib.oracle_topk.argtypes = [I, I, I, P, P, P]
         lib.oracle_permute.argtypes = [I, I, I, I, P, P, P, P, P, P, P, P]
@@ -85,6 +94,11 @@ class Layer:
                                                  "A_out", "B_out")])
         if shape.lora_rank == 0:
             self.s.A_in = self.s.B_in = self.s.A_out = self.s.B_out = None
+        self.s.wfmt = 1 if getattr(shape, "wfmt", "int4") == "nvfp4" else 0
+        for n in _GS:
+            setattr(self.s, n, _p(k.get(n)))
+        if self.s.wfmt == 1 and any(k.get(n) is None for n in _GS):
+            raise ValueError("NVFP4 weights need every per-tensor scale array")
 
     @property
     def ref(self):
@@ -118,6 +132,27 @@ def dequant(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     rows, K = q.shape[0], q.shape[1] * 2
     out = np.empty((rows, K), np.float64)
     _lib_().oracle_dequant_rows(_p(q), _p(s), K, 0, rows, _p(out))
+    return out
+
+
+def e2m1_value(code: int) -> float:
+    """Value of an FP4 E2M1 code (0..15)."""
+    return _lib_().oracle_e2m1_value(int(code))
+
+
+def e4m3_value(b: int) -> float:
+    """Value of an FP8 E4M3 byte (finite-only format; NaN for S.1111.111)."""
+    return _lib_().oracle_e4m3_value(int(b))
+
+
+def nvfp4_dequant(q: np.ndarray, s: np.ndarray, gs: float) -> np.ndarray:
+    """All rows of one NVFP4 tensor: codes q [rows][K/2], E4M3 block scales
+    s [rows][K/16] (bytes), fp32 tensor scale gs."""
+    q = np.ascontiguousarray(q.reshape(-1, q.shape[-1]))
+    s = np.ascontiguousarray(s.reshape(-1, s.shape[-1]), dtype=np.uint8)
+    rows, K = q.shape[0], q.shape[1] * 2
+    out = np.empty((rows, K), np.float64)
+    _lib_().oracle_nvfp4_dequant_rows(_p(q), _p(s), float(gs), K, 0, rows, _p(out))
     return out
 
 

@@ -57,6 +57,17 @@ typedef struct {
   const uint16_t* B_in;    /* [G][r][L] */
   const uint16_t* A_out;   /* [G][L][r] */
   const uint16_t* B_out;   /* [G][r][d] */
+  /* Weight format: 0 = int4 as above; 1 = NVFP4: every *_q holds E2M1 codes
+   * (same nibble order), every *_s points at E4M3 block scales, one byte per
+   * 16 elements along K ([rows][K/16]), and each weight tensor (one group's
+   * W_in or W_out, one expert's gate, up or Down) has an fp32 scale in the
+   * matching *_gs array ([G] or [E]). */
+  int wfmt;
+  const float* W_in_gs;
+  const float* W_out_gs;
+  const float* gate_gs;
+  const float* up_gs;
+  const float* down_gs;
 } oracle_layer;
 
 /* ------------------------------------------------------------------ formats */
@@ -113,11 +124,53 @@ void oracle_dequant_rows(const uint8_t* q, const uint16_t* s, int K, int64_t row
   }
 }
 
-/* y[o] = sum_c What[row0+o][c] * v[c] for o < nrows, What = int4 * scale */
-static void int4_matvec(const uint8_t* q, const uint16_t* s, int K, int64_t row0, int nrows, const double* v,
-                        double* y, double* rowbuf) {
+/* NVFP4 ("Edge0-145B: Run a 145B Open-Source Model on Your Laptop", section
+ * "What You Need to Run It": a checkpoint in NVIDIA's FP4 format). The
+ * elements are FP4 E2M1 -- sign, 2 exponent bits (bias 1), 1 mantissa bit,
+ * exponent 0 subnormal, no infinities or NaN -- so a code is
+ * (-1)^s * (e == 0 ? m/2 : (1 + m/2) * 2^(e-1)). */
+double oracle_e2m1_value(int code) {
+  const int sgn = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+  const double mag = e == 0 ? 0.5 * m : (1.0 + 0.5 * m) * ldexp(1.0, e - 1);
+  return sgn ? -mag : mag;
+}
+
+/* The block scales are FP8 E4M3 (finite-only): sign, 4 exponent bits (bias
+ * 7), 3 mantissa bits, exponent 0 subnormal; exponent 15 with mantissa 7 is
+ * NaN and there are no infinities. */
+double oracle_e4m3_value(uint8_t b) {
+  const int sgn = b >> 7, e = (b >> 3) & 15, m = b & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double mag = e == 0 ? (m / 8.0) * ldexp(1.0, -6) : (1.0 + m / 8.0) * ldexp(1.0, e - 7);
+  return sgn ? -mag : mag;
+}
+
+/* NVFP4 rows: out[i][c] = e2m1(q(row0+i, c)) * e4m3(s(row0+i, c/16)) * gs, the
+ * codes packed two per byte like the int4 format (element 2j in the low
+ * nibble), gs the fp32 scale of the tensor the rows belong to. */
+void oracle_nvfp4_dequant_rows(const uint8_t* q, const uint8_t* s, double gs, int K, int64_t row0, int nrows,
+                               double* out) {
+  for (int i = 0; i < nrows; i++) {
+    const uint8_t* qr = q + (row0 + i) * (int64_t)(K / 2);
+    const uint8_t* sr = s + (row0 + i) * (int64_t)(K / 16);
+    for (int c = 0; c < K; c++) {
+      const int code = (c & 1) ? (qr[c >> 1] >> 4) : (qr[c >> 1] & 15);
+      out[(int64_t)i * K + c] = oracle_e2m1_value(code) * oracle_e4m3_value(sr[c / 16]) * gs;
+    }
+  }
+}
+
+/* y[o] = sum_c What[row0+o][c] * v[c] for o < nrows, What the dequantised
+ * weights of the layer's format; rows row0 .. row0+nrows-1 lie in tensor
+ * row0 / rows_per_tensor (whose NVFP4 scale is gs[that tensor]). */
+static void w_matvec(const oracle_layer* Ly, const uint8_t* q, const uint16_t* s, const float* gs,
+                     int rows_per_tensor, int K, int64_t row0, int nrows, const double* v, double* y,
+                     double* rowbuf) {
   for (int o = 0; o < nrows; o++) {
-    oracle_dequant_rows(q, s, K, row0 + o, 1, rowbuf);
+    if (Ly->wfmt == 1)
+      oracle_nvfp4_dequant_rows(q, (const uint8_t*)s, gs[(row0 + o) / rows_per_tensor], K, row0 + o, 1, rowbuf);
+    else
+      oracle_dequant_rows(q, s, K, row0 + o, 1, rowbuf);
     double acc = 0.0;
     for (int c = 0; c < K; c++) acc += rowbuf[c] * v[c];
     y[o] = acc;
@@ -241,7 +294,7 @@ static double bf(uint16_t b) { return oracle_bf16_value(b); }
 void oracle_shared_in(const oracle_layer* Ly, int g, const double* x, double* h) {
   const int d = Ly->d, L = Ly->L, r = Ly->r;
   double* row = (double*)malloc(sizeof(double) * (size_t)d);
-  int4_matvec(Ly->W_in_q, Ly->W_in_s, d, (int64_t)g * L, L, x, h, row);
+  w_matvec(Ly, Ly->W_in_q, Ly->W_in_s, Ly->W_in_gs, L, d, (int64_t)g * L, L, x, h, row);
   if (r > 0) {
     /* Recover-LoRA: a bf16 low-rank branch in parallel with the int4 base */
     double* p = (double*)calloc((size_t)r, sizeof(double));
@@ -263,7 +316,7 @@ void oracle_shared_in(const oracle_layer* Ly, int g, const double* x, double* h)
 void oracle_shared_out(const oracle_layer* Ly, int g, const double* u, double* o) {
   const int d = Ly->d, L = Ly->L, r = Ly->r;
   double* row = (double*)malloc(sizeof(double) * (size_t)L);
-  int4_matvec(Ly->W_out_q, Ly->W_out_s, L, (int64_t)g * d, d, u, o, row);
+  w_matvec(Ly, Ly->W_out_q, Ly->W_out_s, Ly->W_out_gs, d, L, (int64_t)g * d, d, u, o, row);
   if (r > 0) {
     double* p = (double*)calloc((size_t)r, sizeof(double));
     const uint16_t* A = Ly->A_out + (int64_t)g * L * r;
@@ -289,10 +342,10 @@ void oracle_expert_latent(const oracle_layer* Ly, int e, const double* h, double
   double* a = (double*)malloc(sizeof(double) * (size_t)f);
   double* b = (double*)malloc(sizeof(double) * (size_t)f);
   double* row = (double*)malloc(sizeof(double) * (size_t)(L > f ? L : f));
-  int4_matvec(Ly->gate_q, Ly->gate_s, L, (int64_t)e * f, f, h, a, row);
-  int4_matvec(Ly->up_q, Ly->up_s, L, (int64_t)e * f, f, h, b, row);
+  w_matvec(Ly, Ly->gate_q, Ly->gate_s, Ly->gate_gs, f, L, (int64_t)e * f, f, h, a, row);
+  w_matvec(Ly, Ly->up_q, Ly->up_s, Ly->up_gs, f, L, (int64_t)e * f, f, h, b, row);
   for (int i = 0; i < f; i++) a[i] = a[i] / (1.0 + exp(-a[i])) * b[i];
-  int4_matvec(Ly->down_q, Ly->down_s, f, (int64_t)e * L, L, a, u, row);
+  w_matvec(Ly, Ly->down_q, Ly->down_s, Ly->down_gs, L, f, (int64_t)e * L, L, a, u, row);
   free(a);
   free(b);
   free(row);

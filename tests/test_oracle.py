@@ -463,3 +463,144 @@ def test_combine_closed_form():
     assert np.array_equal(y, np.stack([Y[0] + Y[1], Y[0] + Y[2], Y[2]]))
     res = np.full((3, 4), ONE, np.uint16)
     assert np.array_equal(O.combine(Y, idx, ar, 4, 2, residual=res), y + 1.0)
+
+
+# ------------------------------------------------------------------ NVFP4
+# NVFP4 ("Edge0-145B: Run a 145B Open-Source Model on Your Laptop", "What You
+# Need to Run It": the checkpoint in NVIDIA's FP4 format): E2M1 elements, one
+# E4M3 scale per 16 elements along K, one fp32 scale per weight tensor.
+
+def minifloat(code: int, ebits: int, mbits: int, bias: int, nan_code=None) -> float:
+    """Generic sign / exponent / mantissa decoder (exponent 0 subnormal), used
+    only by the tests: checked against the library's E4M3 first, then applied
+    to E2M1."""
+    if nan_code is not None and (code & ((1 << (ebits + mbits)) - 1)) == nan_code:
+        return float("nan")
+    sgn = (code >> (ebits + mbits)) & 1
+    e = (code >> mbits) & ((1 << ebits) - 1)
+    m = code & ((1 << mbits) - 1)
+    mag = (m / 2 ** mbits) * 2.0 ** (1 - bias) if e == 0 else (1 + m / 2 ** mbits) * 2.0 ** (e - bias)
+    return -mag if sgn else mag
+
+
+def e4m3_library(b) -> np.ndarray:
+    import torch
+    return torch.tensor(np.asarray(b, np.uint8)).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+
+
+def test_e4m3_decode_matches_library_all_codes():
+    lib = e4m3_library(np.arange(256))
+    ours = np.array([O.e4m3_value(b) for b in range(256)])
+    gen = np.array([minifloat(b, 4, 3, 7, nan_code=0x7F) for b in range(256)])
+    assert np.array_equal(np.isnan(lib), np.isnan(ours)) and np.isnan(lib).sum() == 2
+    fin = ~np.isnan(lib)
+    assert np.array_equal(ours[fin], lib[fin])
+    assert np.array_equal(gen[fin], lib[fin]) and np.array_equal(np.isnan(gen), np.isnan(lib))
+    assert O.e4m3_value(0x7E) == 448.0 and O.e4m3_value(0x01) == 2.0 ** -9
+
+
+def test_e2m1_decode_all_codes():
+    """The generic decoder (pinned to the library on E4M3 above) at E2M1's
+    parameters, and the format's invariants: 8 magnitudes strictly increasing
+    from 0 to 6, the sign bit negating."""
+    ours = [O.e2m1_value(c) for c in range(16)]
+    assert ours == [minifloat(c, 2, 1, 1) for c in range(16)]
+    mags = ours[:8]
+    assert mags[0] == 0.0 and mags[-1] == 6.0 and all(a < b for a, b in zip(mags, mags[1:]))
+    assert all(ours[c + 8] == -ours[c] for c in range(8))
+
+
+def test_generator_e4m3_rounding_matches_library():
+    import torch
+    rng = np.random.default_rng(5)
+    xs = np.concatenate([rng.uniform(0, 448, 4000), 2.0 ** rng.uniform(-12, 8.8, 4000),
+                         [e4m3_library([b])[0] for b in range(1, 0x7F)]]).astype(np.float32)
+    xs = xs[xs < 448]
+    # exact midpoints between neighbouring E4M3 values (ties go to the even mantissa)
+    vals = e4m3_library(np.arange(0, 0x7F))
+    mids = ((vals[1:] + vals[:-1]) / 2).astype(np.float32)
+    xs = np.concatenate([xs, mids[mids < 448]])
+    lib = torch.tensor(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    ours = np.array([S.e4m3_rne(v) for v in xs], np.uint8)
+    assert np.array_equal(ours, lib)
+    assert S.e4m3_rne(448.0) == 0x7E and S.e4m3_rne(1e6) == 0x7E and S.e4m3_rne(0.0) == 0
+
+
+def unpack_codes(b: np.ndarray) -> np.ndarray:
+    b = np.asarray(b, np.int64)
+    return np.stack([b & 15, b >> 4], axis=-1).reshape(*b.shape[:-1], b.shape[-1] * 2)
+
+
+def test_nvfp4_quantiser_is_nearest_level_and_dequant_exact():
+    """The generator's NVFP4 matrices against brute force: the tensor scale is
+    amax / (6 * 448), each block scale the library's E4M3 rounding of
+    amax_block / 6 / gs, each code a nearest level; the oracle's dequantiser
+    equals an independent unpack x decoder x library E4M3 x gs."""
+    rows, K, rpt = 24, 64, 8
+    q, s, gs = S.nvfp4_matrix(3, 11, rows, K, 0.02, rpt)
+    w = S.int4_source(3, 11, rows, K, 0.02)  # the same draws
+    table = np.array([minifloat(c, 2, 1, 1) for c in range(16)])
+    codes = unpack_codes(q)
+    for t in range(rows // rpt):
+        wt = w[t * rpt:(t + 1) * rpt]
+        assert gs[t] == np.float32(np.abs(wt).max()) / np.float32(6 * 448)
+        blk = wt.reshape(rpt, K // 16, 16)
+        amax = np.abs(blk).max(axis=-1).astype(np.float32)
+        import torch
+        sb = torch.tensor(amax / np.float32(6) / gs[t]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(s[t * rpt:(t + 1) * rpt], sb)
+        scale = e4m3_library(sb).astype(np.float32) * gs[t]
+        v = blk / scale[..., None]
+        got = table[codes[t * rpt:(t + 1) * rpt].reshape(rpt, K // 16, 16)]
+        err = np.abs(got - v)
+        best = np.abs(table[None, None, None, :8] - np.abs(v)[..., None]).min(axis=-1)
+        assert np.all(err <= best + 1e-6 * np.abs(v))
+        dq = O.nvfp4_dequant(q[t * rpt:(t + 1) * rpt], s[t * rpt:(t + 1) * rpt], gs[t])
+        ref = table[codes[t * rpt:(t + 1) * rpt]] * np.repeat(e4m3_library(s[t * rpt:(t + 1) * rpt]), 16, axis=-1) \
+            * np.float64(gs[t])
+        assert np.array_equal(dq, ref)
+
+
+def nv_dense(q, s, gs):
+    table = np.array([minifloat(c, 2, 1, 1) for c in range(16)])
+    return table[unpack_codes(q)] * np.repeat(e4m3_library(s), 16, axis=-1) * np.float64(gs)
+
+
+def test_full_layer_nvfp4_against_numpy_chain_tiny():
+    """The NVFP4 layer end to end on the tiny workload, experts from the
+    independently decoded matrices."""
+    sh, T, W, x = S.make_workload("tiny_t64_nvfp4")
+    y, idx, w, lg = O.layer_forward(O.Layer(sh, W), x)
+    xf = bf16_f(x)
+    epg = sh.E // sh.G
+    for t in range(T):
+        order = np.lexsort((np.arange(sh.E), -lg[t].astype(np.float32)))[:sh.k]
+        assert list(order) == list(idx[t])
+        sel = lg[t][order]
+        wr = np.exp(sel - sel[0]) / np.exp(sel - sel[0]).sum()
+        ref = np.zeros(sh.d)
+        for e, wj in zip(order, wr):
+            g = e // epg
+            h = nv_dense(W["W_in_q"][g], W["W_in_s"][g], W["W_in_gs"][g]) @ xf[t]
+            Gt = nv_dense(W["gate_q"][e], W["gate_s"][e], W["gate_gs"][e])
+            Up = nv_dense(W["up_q"][e], W["up_s"][e], W["up_gs"][e])
+            Dn = nv_dense(W["down_q"][e], W["down_s"][e], W["down_gs"][e])
+            Wo = nv_dense(W["W_out_q"][g], W["W_out_s"][g], W["W_out_gs"][g])
+            ref += wj * (Wo @ (Dn @ (silu(Gt @ h) * (Up @ h))))
+        assert np.allclose(y[t], ref, rtol=1e-10, atol=1e-16)
+
+
+def test_nvfp4_differs_from_int4_only_by_quantisation():
+    """Same draws, two formats: both dequantised matrices stay within their
+    own half-step of the source weights (a wrong scale or nibble order would
+    not)."""
+    q4, s4 = S.int4_matrix(0, 7, 16, 128, 0.02)
+    qn, sn, gs = S.nvfp4_matrix(0, 7, 16, 128, 0.02, 16)
+    w = S.int4_source(0, 7, 16, 128, 0.02).astype(np.float64)
+    d4 = O.dequant(q4, s4)
+    dn = O.nvfp4_dequant(qn, sn, gs[0])
+    half4 = np.repeat(bf16_f(s4), 32, axis=-1) / 2
+    assert np.all(np.abs(d4 - w) <= half4 * (1 + 1e-6))
+    # NVFP4 level spacing is at most 2 (between 4 and 6) in units of the block scale
+    stepn = np.repeat(e4m3_library(sn), 16, axis=-1) * gs[0]
+    assert np.all(np.abs(dn - w) <= stepn * (1 + 1e-6) + 1e-12)
