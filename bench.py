@@ -485,7 +485,9 @@ def run_ours(args):
     main = measure_layer(args, args.workload, local, dev, dist, world, args.steps, args.warmup, args.copies)
     line = {"metric": METRIC, "value": main.pop("value"), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": main.pop("ms_per_step"), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "int4 weights, fp16 tensor-core operands, fp32 accumulate",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": ("nvfp4" if args.workload.endswith("_nvfp4") else "int4")
+            + " weights, fp16 tensor-core operands, fp32 accumulate",
             "data": "synthetic"}
     line.update(main)
     # the metric's second half: the 16K-token prefill, in the same run

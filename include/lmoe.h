@@ -68,6 +68,14 @@ typedef enum {
  * sequence of per-step kernels instead of the single persistent kernel. */
 enum { LMOE_FLAG_MULTI_KERNEL_DECODE = 1u };
 
+/* config.weight_format: the five shared / expert weight families are int4
+ * (symmetric per 32 elements, bf16 scales) or NVFP4 (NVIDIA's FP4 format, the
+ * format of the NVFP4 checkpoint in "Edge0-145B: Run a 145B Open-Source Model
+ * on Your Laptop", "What You Need to Run It"): FP4 E2M1 codes packed like the
+ * int4 nibbles, an FP8 E4M3 scale per 16 elements along K, and an fp32 scale
+ * per weight tensor. The router is fp32 in both. */
+enum { LMOE_WEIGHTS_INT4 = 0, LMOE_WEIGHTS_NVFP4 = 1 };
+
 /* Execution path for lmoe_layer_forward / lmoe_expert_forward. */
 enum { LMOE_PATH_AUTO = 0, LMOE_PATH_DECODE = 1, LMOE_PATH_PREFILL = 2 };
 
@@ -78,18 +86,26 @@ typedef struct {
   int k;            /* experts per token; 1 <= k <= min(16, E) */
   int L;            /* latent width; multiple of 32 (prefill path: of 64) */
   int f;            /* per-expert SwiGLU width; multiple of 32 (prefill path: of 64) */
-  int qgroup;       /* int4 group size along the reduction dimension; must be 32 */
+  int qgroup;       /* scale group along the reduction dimension: 32 (int4) or 16 (NVFP4) */
   int lora_rank;    /* 0 = no LoRA branch; else a multiple of 16, <= 128 */
   int has_bias;     /* nonzero: router bias b_r is used */
   unsigned flags;   /* LMOE_FLAG_* bits */
   long long timeout_cycles; /* bound on any device-side wait (clock64 cycles); 0 = 2^31 */
   int decode_max_T; /* token count up to which AUTO takes the decode path; 0 = 16; <= 16 */
   int force_path;   /* LMOE_PATH_* */
+  int weight_format; /* LMOE_WEIGHTS_*; NVFP4 layers run the single-kernel decode pass and the prefill
+                        path (LMOE_ERR_UNSUPPORTED where only the multi-kernel decode path would fit) */
 } lmoe_config;
 
 /* Device pointers to the layer's weights (borrowed for the handle's life).
  * Shapes as in the layer description; packed int4 rows are [rows][K/2] bytes
- * and their scales [rows][K/32] bf16. */
+ * and their scales [rows][K/32] bf16. With LMOE_WEIGHTS_NVFP4 the *_q rows
+ * hold E2M1 codes ([rows][K/2] bytes, element 2j in the low nibble, bit 3 the
+ * sign), each *_s points at E4M3 bytes [rows][K/16] (the same byte count as
+ * the int4 scales; cast the pointer), and the *_gs arrays give each tensor's
+ * fp32 scale: W_in_gs / W_out_gs [G] (one per group's matrix), gate_gs /
+ * up_gs / down_gs [E] (one per expert's matrix). A weight is
+ * e2m1(q) * e4m3(s) * gs. The *_gs pointers are NULL for int4. */
 typedef struct {
   const float* W_r;           /* [E][d] fp32 */
   const float* b_r;           /* [E] fp32, or NULL when has_bias == 0 */
@@ -107,6 +123,11 @@ typedef struct {
   const uint16_t* B_in;       /* [G][r][L] */
   const uint16_t* A_out;      /* [G][L][r] */
   const uint16_t* B_out;      /* [G][r][d] */
+  const float* W_in_gs;       /* NVFP4 only: [G] */
+  const float* W_out_gs;      /* [G] */
+  const float* gate_gs;       /* [E] */
+  const float* up_gs;         /* [E] */
+  const float* down_gs;       /* [E] */
 } lmoe_weights;
 
 /* The token permutation (device arrays, caller-allocated, capacities in

@@ -170,6 +170,9 @@ WORKLOADS = {
     "decode_t8": (EDGE0, 8, 0, 1, None, None),
     "prefill_t16384_zipf": (replace(EDGE0, has_bias=True), 16384, 0, 1, 2, None),
     "lora_t16": (replace(EDGE0, lora_rank=64), 16, 0, 1, None, 3),
+    # a small layer within the single-kernel decode pass's shapes (d 1024, L 256), for quick path tests
+    "small_t16_nvfp4": (LayerShape(d=1024, E=64, G=4, k=10, L=256, f=256, wfmt="nvfp4"), 16, 0, 1, None, None),
+    "small_t256_nvfp4": (LayerShape(d=1024, E=64, G=4, k=10, L=256, f=256, wfmt="nvfp4"), 256, 0, 1, None, None),
     # the same layers with NVFP4 weights (the same fp32 draws, quantised to NVIDIA's FP4 format)
     "tiny_t64_nvfp4": (replace(TINY, wfmt="nvfp4"), 64, 0, 0, None, None),
     "decode_t8_nvfp4": (replace(EDGE0, wfmt="nvfp4"), 8, 0, 1, None, None),

@@ -35,11 +35,13 @@ class LmoeConfig(ctypes.Structure):
     _fields_ = [("d", ctypes.c_int), ("E", ctypes.c_int), ("G", ctypes.c_int), ("k", ctypes.c_int),
                 ("L", ctypes.c_int), ("f", ctypes.c_int), ("qgroup", ctypes.c_int), ("lora_rank", ctypes.c_int),
                 ("has_bias", ctypes.c_int), ("flags", ctypes.c_uint), ("timeout_cycles", ctypes.c_longlong),
-                ("decode_max_T", ctypes.c_int), ("force_path", ctypes.c_int)]
+                ("decode_max_T", ctypes.c_int), ("force_path", ctypes.c_int), ("weight_format", ctypes.c_int)]
 
+
+WEIGHTS_INT4, WEIGHTS_NVFP4 = 0, 1
 
 WEIGHT_FIELDS = ("W_r", "b_r", "W_in_q", "W_in_s", "W_out_q", "W_out_s", "gate_q", "gate_s", "up_q", "up_s", "down_q",
-                 "down_s", "A_in", "B_in", "A_out", "B_out")
+                 "down_s", "A_in", "B_in", "A_out", "B_out", "W_in_gs", "W_out_gs", "gate_gs", "up_gs", "down_gs")
 
 
 class LmoeWeights(ctypes.Structure):

@@ -49,7 +49,8 @@ lmoe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? LMOE_OK : LMO
 lmoe_status validate_config(const lmoe_config* c) {
   if (!c) return LMOE_ERR_INVALID_ARG;
   if (c->d <= 0 || c->E <= 0 || c->G <= 0 || c->k <= 0 || c->L <= 0 || c->f <= 0) return LMOE_ERR_INVALID_ARG;
-  if (c->qgroup != 32) return LMOE_ERR_UNSUPPORTED;
+  if (c->weight_format != LMOE_WEIGHTS_INT4 && c->weight_format != LMOE_WEIGHTS_NVFP4) return LMOE_ERR_INVALID_ARG;
+  if (c->qgroup != (c->weight_format == LMOE_WEIGHTS_NVFP4 ? 16 : 32)) return LMOE_ERR_UNSUPPORTED;
   if (c->E % c->G != 0) return LMOE_ERR_INVALID_ARG;
   if (c->k > c->E) return LMOE_ERR_INVALID_ARG;
   if (c->k > 16 || c->E > 1024 || c->G > 64) return LMOE_ERR_UNSUPPORTED;
@@ -72,6 +73,13 @@ lmoe_status validate_weights(const lmoe_config* c, const lmoe_weights* w) {
     if (!aligned16(p)) return LMOE_ERR_ALIGNMENT;
   }
   if (c->has_bias && !w->b_r) return LMOE_ERR_INVALID_ARG;
+  if (c->weight_format == LMOE_WEIGHTS_NVFP4) {
+    const void* gs[] = {w->W_in_gs, w->W_out_gs, w->gate_gs, w->up_gs, w->down_gs};
+    for (const void* p : gs) {
+      if (!p) return LMOE_ERR_INVALID_ARG;
+      if (((uintptr_t)p & 3u) != 0) return LMOE_ERR_ALIGNMENT;
+    }
+  }
   if (c->lora_rank > 0) {
     const void* lr[] = {w->A_in, w->B_in, w->A_out, w->B_out};
     for (const void* p : lr) {
@@ -167,6 +175,9 @@ DecodeArgs base_args(const lmoe_handle* h, void* ws) {
   A.gate_q = h->w.gate_q; A.gate_s = h->w.gate_s; A.up_q = h->w.up_q; A.up_s = h->w.up_s;
   A.down_q = h->w.down_q; A.down_s = h->w.down_s;
   A.A_in = h->w.A_in; A.B_in = h->w.B_in; A.A_out = h->w.A_out; A.B_out = h->w.B_out;
+  A.wfmt = c.weight_format;
+  A.W_in_gs = h->w.W_in_gs; A.W_out_gs = h->w.W_out_gs;
+  A.gate_gs = h->w.gate_gs; A.up_gs = h->w.up_gs; A.down_gs = h->w.down_gs;
   const DecodeWs m = decode_ws(c, 0, h->num_sms);
   char* b = reinterpret_cast<char*>(ws);
   A.idx = reinterpret_cast<int32_t*>(b + m.idx);
@@ -300,6 +311,7 @@ lmoe_status decode_layer(lmoe_handle* h, const uint16_t* x, int T, const uint16_
       }
       continue;
     }
+    if (A.wfmt != LMOE_WEIGHTS_INT4) return LMOE_ERR_UNSUPPORTED;  // the per-step kernels read int4 only
     hook.before(st);
     cudaError_t e = launch_route(A, 1, ws_logits(h, ws), st);
     hook.after(st);
@@ -328,6 +340,9 @@ PrefillArgs prefill_args(const lmoe_handle* h) {
   P.gate_q = h->w.gate_q; P.gate_s = h->w.gate_s; P.up_q = h->w.up_q; P.up_s = h->w.up_s;
   P.down_q = h->w.down_q; P.down_s = h->w.down_s;
   P.A_in = h->w.A_in; P.B_in = h->w.B_in; P.A_out = h->w.A_out; P.B_out = h->w.B_out;
+  P.wfmt = c.weight_format;
+  P.W_in_gs = h->w.W_in_gs; P.W_out_gs = h->w.W_out_gs;
+  P.gate_gs = h->w.gate_gs; P.up_gs = h->w.up_gs; P.down_gs = h->w.down_gs;
   P.err = h->d_err;
   P.num_sms = h->num_sms;
   P.timeout = h->timeout;
@@ -421,7 +436,7 @@ const char* lmoe_status_string(lmoe_status s) {
   return "unknown status";
 }
 
-int lmoe_version(void) { return 100; }
+int lmoe_version(void) { return 101; }
 
 lmoe_status lmoe_create(lmoe_handle** out, const lmoe_config* cfg, const lmoe_weights* w, int device) {
   if (!out) return LMOE_ERR_INVALID_ARG;
@@ -605,10 +620,12 @@ lmoe_status lmoe_expert_forward(lmoe_handle* h, const uint16_t* x, int T, const 
   DeviceGuard guard(h->device);
   cudaStream_t st = (cudaStream_t)stream;
   const lmoe_config& c = h->cfg;
-  if (use_prefill(h, T)) {
+  if (use_prefill(h, T) || (c.weight_format != LMOE_WEIGHTS_INT4 && prefill_supported(prefill_args(h)))) {
+    // (NVFP4 weights: the per-step decode kernels read int4 only, so every T takes the grouped GEMMs)
     PrefillArgs P = prefill_args(h);
     return cuda_status(launch_prefill_experts(P, x, T, idx, w, to_ptrs(perm), Y, nullptr, nullptr, ws, st));
   }
+  if (c.weight_format != LMOE_WEIGHTS_INT4) return LMOE_ERR_UNSUPPORTED;
   const DecodeWs m = decode_ws(c, T, h->num_sms);
   for (int t0 = 0; t0 < T; t0 += kMaxDecodeT) {
     DecodeArgs A = base_args(h, ws);

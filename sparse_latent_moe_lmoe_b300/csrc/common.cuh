@@ -73,6 +73,25 @@ LMOE_DEV __half2 scale_h2(uint16_t sbits) {
   return __halves2half2(h, h);
 }
 
+// Four bytes of FP4 E2M1 code pairs -> four half2, one per byte (the byte's
+// low nibble in the low half); exact. Hardware conversions (sm_100 and later).
+LMOE_DEV void e2m1x8_to_h2x4(uint32_t v, uint32_t out[4]) {
+  asm("{ .reg .b8 a0, a1, a2, a3;\n"
+      "  mov.b32 {a0, a1, a2, a3}, %4;\n"
+      "  cvt.rn.f16x2.e2m1x2 %0, a0;\n"
+      "  cvt.rn.f16x2.e2m1x2 %1, a1;\n"
+      "  cvt.rn.f16x2.e2m1x2 %2, a2;\n"
+      "  cvt.rn.f16x2.e2m1x2 %3, a3; }"
+      : "=r"(out[0]), "=r"(out[1]), "=r"(out[2]), "=r"(out[3])
+      : "r"(v));
+}
+// Two FP8 E4M3 bytes -> half2 (the low byte in the low half); exact.
+LMOE_DEV uint32_t e4m3x2_to_h2(uint16_t w) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(w));
+  return h;
+}
+
 // D += A * B, m16n8k16, fp16 inputs, fp32 accumulators
 LMOE_DEV void mma16816(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
   asm volatile(

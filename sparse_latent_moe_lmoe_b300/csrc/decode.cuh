@@ -39,6 +39,14 @@ struct DecodeArgs {
   const uint16_t* B_in;
   const uint16_t* A_out;
   const uint16_t* B_out;
+  // weight format (LMOE_WEIGHTS_*) and, for NVFP4, the per-tensor fp32 scales
+  // (the *_s pointers then hold E4M3 bytes)
+  int wfmt;
+  const float* W_in_gs;
+  const float* W_out_gs;
+  const float* gate_gs;
+  const float* up_gs;
+  const float* down_gs;
   // this pass's tokens
   const uint16_t* x;         // [T][d]
   const uint16_t* residual;  // [T][d] or null
@@ -63,9 +71,10 @@ struct DecodeArgs {
 
 // The single-kernel decode pass streams its weights from a copy made when the
 // handle is created, laid out chunk by chunk in the order and form the
-// consumers read them: every chunk is one contiguous run of packed int4 (its
-// 128-byte lines already in the 128-byte swizzle of the shared-memory slot)
-// followed by the chunk's bf16 scales, so one bulk copy moves it.
+// consumers read them: every chunk is one contiguous run of packed 4-bit
+// codes (its 128-byte lines already in the 128-byte swizzle of the
+// shared-memory slot) followed by the chunk's scales, so one bulk copy moves
+// it. NVFP4 code words are stored with byte b holding elements b and b + 4.
 //   win   [G L/16 tiles of 16 rows][d/PW pieces][9 PW bytes], PW = min(d, 2048)
 //   unit  [E][f/32 slices][gate rows, up rows, Down columns][18 L bytes]
 //   wout  [G][d/32 blocks of 32 rows][18 L bytes]

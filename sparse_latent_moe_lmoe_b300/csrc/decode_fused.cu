@@ -453,7 +453,7 @@ template <int NT>
 struct Acc {
   float v[NT][4];
 };
-template <int NT>
+template <int NT, int WF>
 __device__ __noinline__ Acc<NT> slot_mma(const unsigned char* w, int LPR, int row0, const uint16_t* s, int SS, int c0,
                                          int nc, const uint4* frag) {
   Acc<NT> r;
@@ -461,7 +461,7 @@ __device__ __noinline__ Acc<NT> slot_mma(const unsigned char* w, int LPR, int ro
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int h = 0; h < 4; ++h) r.v[nt][h] = 0.f;
-  mma_slot<NT>(w, LPR, row0, s, SS, c0, nc, frag, r.v);
+  mma_slot<NT, WF>(w, LPR, row0, s, SS, c0, nc, frag, r.v);
   return r;
 }
 
@@ -476,7 +476,7 @@ LMOE_DEV int group_slot(const Tables& tb, int es) {
 }  // namespace
 
 // ==================================================================== kernel
-template <int NT>
+template <int NT, int WF>
 __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_constant__ FusedArgs F) {
   constexpr int NS = nslot<NT>();
   constexpr int FR = 128 * NT;  // fragment entries per 128 elements of an activation set
@@ -634,6 +634,9 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
   const int ctid = threadIdx.x;  // 0 .. NCT-1
 
   // ------------------------------------------------------------ A1 router
+  // the router bias of this thread's logit, loaded now: its latency hides
+  // behind the staging of x instead of the router phase's end
+  const float bias = (A.b_r && ctid < ne * 16) ? __ldg(A.b_r + e_lo + (ctid >> 4)) : 0.f;
   if (F.pdl) asm volatile("griddepcontrol.wait;" ::: "memory");  // x is the previous layer's output
   stage_x<NT>(tb, xf, A.x, T, d, ctid);
   cons_sync();
@@ -686,7 +689,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
         float s = 0.f;
 #pragma unroll
         for (int w = 0; w < NCW; ++w) s += tb.u.rred[w][i][t];
-        if (A.b_r) s += A.b_r[e_lo + i];
+        if (A.b_r) s += bias;
         F.logits[(size_t)t * E + e_lo + i] = s;
       }
     }
@@ -726,7 +729,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
       const unsigned char* sl = acquire<NS>(tb, ring, jA2 + jj, budget, err, WS_WIN_SLOT, diag, landed);
       if (jj == ti * NPW + tp) {
         if (trace && wt == 0) trace[19] = gtime();
-        acc = slot_mma<NT>(sl, PW / 256, 0, reinterpret_cast<const uint16_t*>(sl + 8 * PW), PW / 32, k0c, nkc,
+        acc = slot_mma<NT, WF>(sl, PW / 256, 0, reinterpret_cast<const uint16_t*>(sl + 8 * PW), PW / 32, k0c, nkc,
                            xf + (size_t)(tp * CPP + k0c) * FR);
       }
       release_read<NS>(tb, jA2 + jj, landed);  // a chunk this warp does not read is handed back once it landed
@@ -748,6 +751,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
       float s = 0.f;
 #pragma unroll
       for (int w = 0; w < 2; ++w) s += pf[((((2 * i + w) * NT + nt) * 32 + ll) << 2) + h];
+      if (WF == 1) s *= __ldg(A.W_in_gs + g);  // the tensor scale of W_in[g]
       if (F.hl && n < T) s += __ldcg(F.hl + ((size_t)g * 16 + n) * L + rt * 16 + r);  // the LoRA branch
       float e[8];
 #pragma unroll
@@ -853,7 +857,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
           bool landed;
           const unsigned char* sl = acquire<NS>(tb, ring, jg + mat, budget, err, WS_GU_SLOT, diag, landed);
           if (trace && ctid == 0 && q == 0) trace[21] = gtime();
-          mma_slot<NT>(sl, L / 256, 16 * mt, reinterpret_cast<const uint16_t*>(sl + 16 * L), L / 32, gc0, gc1 - gc0,
+          mma_slot<NT, WF>(sl, L / 256, 16 * mt, reinterpret_cast<const uint16_t*>(sl + 16 * L), L / 32, gc0, gc1 - gc0,
                        xf + (size_t)gc0 * FR, a);  // inline: the Down accumulators stay live across it
           release_read<NS>(tb, jg + mat, landed);
         }
@@ -873,6 +877,10 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
           gs += pf[((((par * NCW + m2 * 4 + q4) * NT + nt) * 32 + ln) << 2) + h];
           us += pf[((((par * NCW + 8 + m2 * 4 + q4) * NT + nt) * 32 + ln) << 2) + h];
         }
+        if (WF == 1) {  // the tensor scales of Gate_e and Up_e
+          gs *= __ldg(A.gate_gs + e);
+          us *= __ldg(A.up_gs + e);
+        }
         const int r = 16 * m2 + (ln >> 2) + 8 * (h >> 1), n = nt * 8 + 2 * (ln & 3) + (h & 1);
         const float wv = route_weight(tb, n, e);
         const float v = wv != 0.f ? wv * gs * __frcp_rn(1.f + __expf(-gs)) * us : 0.f;
@@ -887,9 +895,27 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
         const unsigned char* sl = acquire<NS>(tb, ring, jd, budget, err, WS_DOWN_SLOT, diag, landed);
         const uint32_t* wsl = reinterpret_cast<const uint32_t*>(sl);
         const uint16_t* sc = reinterpret_cast<const uint16_t*>(sl + 16 * L);
+        if (WF == 0) {
 #pragma unroll
-        for (int m = 0; m < MAX_MPW; ++m)
-          if (m < MPW) mma_slice32<NT>(wsl, sc, warp * MPW + m, vbuf + pq * NT * 32, zacc[m]);
+          for (int m = 0; m < MAX_MPW; ++m)
+            if (m < MPW) mma_slice32<NT, WF>(wsl, sc, warp * MPW + m, vbuf + pq * NT * 32, zacc[m]);
+        } else {  // each expert's Down has its own tensor scale: applied before the group's sum
+          const float sd = __ldg(A.down_gs + tb.elist[es]);
+#pragma unroll
+          for (int m = 0; m < MAX_MPW; ++m) {
+            if (m >= MPW) break;
+            float t[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int hh = 0; hh < 4; ++hh) t[nt][hh] = 0.f;
+            mma_slice32<NT, WF>(wsl, sc, warp * MPW + m, vbuf + pq * NT * 32, t);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int hh = 0; hh < 4; ++hh) zacc[m][nt][hh] = fmaf(sd, t[nt][hh], zacc[m][nt][hh]);
+          }
+        }
         release_read<NS>(tb, jd, landed);
         if (trace && ctid == 0 && qq == 0) trace[14] = gtime();
         // the last unit of its group in this CTA: write the group's partial of Z
@@ -1019,7 +1045,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
         bool landed;
         const unsigned char* sl = acquire<NS>(tb, ring, jD + q, budget, err, WS_WOUT_SLOT, diag, landed);
         if (trace && ctid == 0 && q == 0) trace[25] = gtime();
-        const Acc<NT> t = slot_mma<NT>(sl, L / 256, 16 * wm, reinterpret_cast<const uint16_t*>(sl + 16 * L), L / 32, oc0,
+        const Acc<NT> t = slot_mma<NT, WF>(sl, L / 256, 16 * wm, reinterpret_cast<const uint16_t*>(sl + 16 * L), L / 32, oc0,
                                        oc1 - oc0, xf + (size_t)oc0 * FR);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -1037,6 +1063,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
         float s = 0.f;
 #pragma unroll
         for (int q8 = 0; q8 < 8; ++q8) s += pf[((((pq * NCW + m2 * 8 + q8) * NT + nt) * 32 + ln) << 2) + h];
+        if (WF == 1) s *= __ldg(A.W_out_gs + g);  // the tensor scale of W_out[g]
         const int row = ot * 32 + 16 * m2 + (ln >> 2) + 8 * (h >> 1), n = nt * 8 + 2 * (ln & 3) + (h & 1);
         if (n < T) F.Yp[((size_t)g * 16 + n) * d + row] = s;
       }
@@ -1122,7 +1149,20 @@ struct PackSpec {
   int rows, wb, wsc, npc;
   uint8_t* out;
   size_t cstride, coff;
+  int fp4;  // NVFP4 codes: each 32-bit word re-ordered (fp4_word_order)
 };
+
+// An NVFP4 code word, natural order (element i in nibble i), re-ordered so
+// that byte b holds elements b and b + 4.
+__device__ __forceinline__ uint32_t fp4_word_order(uint32_t v) {
+  uint32_t o = 0;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) o |= (((v >> (4 * b)) & 15u) | (((v >> (4 * (b + 4))) & 15u) << 4)) << (8 * b);
+  return o;
+}
+__device__ __forceinline__ uint4 fp4_order4(uint4 v) {
+  return make_uint4(fp4_word_order(v.x), fp4_word_order(v.y), fp4_word_order(v.z), fp4_word_order(v.w));
+}
 
 __global__ void __launch_bounds__(256) pack_swz_kernel(PackSpec P) {
   const int c = blockIdx.x, band = c / P.npc, piece = c % P.npc;
@@ -1131,7 +1171,8 @@ __global__ void __launch_bounds__(256) pack_swz_kernel(PackSpec P) {
   const int lpr = P.wb / 128, nu = P.rows * lpr * 8;
   for (int i = threadIdx.x; i < nu; i += blockDim.x) {
     const int line = i >> 3, u = i & 7, r = line / lpr, li = line % lpr;
-    const uint4 v = *reinterpret_cast<const uint4*>(P.q + (row0 + r) * P.qs + (size_t)piece * P.wb + li * 128 + u * 16);
+    uint4 v = *reinterpret_cast<const uint4*>(P.q + (row0 + r) * P.qs + (size_t)piece * P.wb + li * 128 + u * 16);
+    if (P.fp4) v = fp4_order4(v);
     *reinterpret_cast<uint4*>(dst + line * 128 + ((u ^ (line & 7)) << 4)) = v;
   }
   uint16_t* sd = reinterpret_cast<uint16_t*>(dst + (size_t)P.rows * P.wb);
@@ -1145,12 +1186,13 @@ __global__ void __launch_bounds__(256) pack_swz_kernel(PackSpec P) {
 // bytes of Down_e[l] holding the slice's 32 int4 ([L][16 B], unswizzled),
 // then the rows' scales of that slice ([L] bf16).
 __global__ void __launch_bounds__(256) pack_down_kernel(const uint8_t* q, const uint16_t* s, int L, int f,
-                                                        uint8_t* unit) {
+                                                        uint8_t* unit, int fp4) {
   const int nsf = f / FS, c = blockIdx.x, e = c / nsf, sl = c % nsf;
   uint8_t* dst = unit + ((size_t)c * 3 + 2) * 18 * L;
   for (int l = threadIdx.x; l < L; l += blockDim.x) {
     const size_t row = (size_t)e * L + l;
-    *reinterpret_cast<uint4*>(dst + (size_t)l * 16) = *reinterpret_cast<const uint4*>(q + row * (f / 2) + sl * 16);
+    const uint4 v = *reinterpret_cast<const uint4*>(q + row * (f / 2) + sl * 16);
+    *reinterpret_cast<uint4*>(dst + (size_t)l * 16) = fp4 ? fp4_order4(v) : v;
     reinterpret_cast<uint16_t*>(dst + (size_t)16 * L)[l] = s[row * nsf + sl];
   }
 }
@@ -1180,22 +1222,23 @@ cudaError_t launch_decode_pack(const DecodeArgs& A, uint8_t* buf, DecodePack* pk
   pk->unit = buf + lay.unit;
   pk->wout = buf + lay.wout;
   // W_in: 16-row tiles in pieces of PW columns
+  const int fp4 = A.wfmt != 0;  // (the scales move as 16-bit words in both formats: one bf16 or two E4M3 per 32)
   PackSpec w{A.W_in_q, (size_t)d / 2, A.W_in_s, (size_t)d / 32, 16, PW / 2, PW / 32, d / PW, buf + lay.win,
-             (size_t)9 * PW, 0};
+             (size_t)9 * PW, 0, fp4};
   pack_swz_kernel<<<G * (L / 16) * (d / PW), 256, 0, st>>>(w);
   // gate and up: 32 rows (one f-slice of one expert) each, at parts 0 and 1 of the unit
   PackSpec g{A.gate_q, (size_t)L / 2, A.gate_s, (size_t)L / 32, FS, L / 2, L / 32, 1, buf + lay.unit,
-             (size_t)3 * 18 * L, 0};
+             (size_t)3 * 18 * L, 0, fp4};
   pack_swz_kernel<<<E * nsf, 256, 0, st>>>(g);
   PackSpec u = g;
   u.q = A.up_q;
   u.s = A.up_s;
   u.coff = (size_t)18 * L;
   pack_swz_kernel<<<E * nsf, 256, 0, st>>>(u);
-  pack_down_kernel<<<E * nsf, 256, 0, st>>>(A.down_q, A.down_s, L, f, buf + lay.unit);
+  pack_down_kernel<<<E * nsf, 256, 0, st>>>(A.down_q, A.down_s, L, f, buf + lay.unit, fp4);
   // W_out: 32-row blocks
   PackSpec o{A.W_out_q, (size_t)L / 2, A.W_out_s, (size_t)L / 32, 32, L / 2, L / 32, 1, buf + lay.wout,
-             (size_t)18 * L, 0};
+             (size_t)18 * L, 0, fp4};
   pack_swz_kernel<<<G * (d / 32), 256, 0, st>>>(o);
   return cudaGetLastError();
 }
@@ -1212,16 +1255,18 @@ bool fused_decode_supported(const DecodeArgs& A, int grid) {
 }
 
 cudaError_t fused_set_attributes() {
-  cudaFuncSetAttribute(decode_fused_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<1>());
-  cudaFuncSetAttribute(decode_fused_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<2>());
+  cudaFuncSetAttribute(decode_fused_kernel<1, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<1>());
+  cudaFuncSetAttribute(decode_fused_kernel<2, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<2>());
+  cudaFuncSetAttribute(decode_fused_kernel<1, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<1>());
+  cudaFuncSetAttribute(decode_fused_kernel<2, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<2>());
   return cudaGetLastError();
 }
 
 int fused_grid(int num_sms) {
   int per1 = 0, per2 = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per1, decode_fused_kernel<1>, NTHR, dyn_smem<1>()) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per1, decode_fused_kernel<1, 0>, NTHR, dyn_smem<1>()) !=
           cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per2, decode_fused_kernel<2>, NTHR, dyn_smem<2>()) !=
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per2, decode_fused_kernel<2, 0>, NTHR, dyn_smem<2>()) !=
           cudaSuccess ||
       per1 < 1 || per2 < 1) {
     cudaGetLastError();
@@ -1249,10 +1294,12 @@ cudaError_t launch_decode_fused(const FusedArgs& F, int grid, cudaStream_t st, i
   cfg.numAttrs = 1;
   if (F.A.T <= 8) {
     cfg.dynamicSmemBytes = dyn_smem<1>();
-    return cudaLaunchKernelEx(&cfg, decode_fused_kernel<1>, F);
+    return F.A.wfmt ? cudaLaunchKernelEx(&cfg, decode_fused_kernel<1, 1>, F)
+                    : cudaLaunchKernelEx(&cfg, decode_fused_kernel<1, 0>, F);
   }
   cfg.dynamicSmemBytes = dyn_smem<2>();
-  return cudaLaunchKernelEx(&cfg, decode_fused_kernel<2>, F);
+  return F.A.wfmt ? cudaLaunchKernelEx(&cfg, decode_fused_kernel<2, 1>, F)
+                  : cudaLaunchKernelEx(&cfg, decode_fused_kernel<2, 0>, F);
 }
 
 }  // namespace lmoe

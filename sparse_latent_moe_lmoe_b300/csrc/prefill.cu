@@ -680,6 +680,12 @@ struct DqSeg {
   const uint16_t* s;
   uint4* out;
   size_t n;  // 32-bit words
+  // NVFP4: E2M1 codes with one E4M3 byte per 2 words and a per-tensor scale
+  // (tensor = wpt consecutive words); the fp16 copy holds e2m1 * e4m3 * gs,
+  // rounded once
+  int fp4;
+  const float* gs;
+  size_t wpt;
 };
 struct DqJob {
   DqSeg seg[5];
@@ -699,7 +705,20 @@ __global__ void __launch_bounds__(256) dequant_all_kernel(const __grid_constant_
     for (; i < base + S.n; i += stride) {
       const size_t w = i - base;
       uint32_t o[4];
-      tc::dequant_word_natural(__ldcs(S.q + w), scale_h2(__ldg(S.s + (w >> 2))), o);
+      if (S.fp4) {
+        const uint8_t sb = __ldg(reinterpret_cast<const uint8_t*>(S.s) + (w >> 1));
+        const uint32_t sh = e4m3x2_to_h2(sb);
+        const float sc = __low2float(*reinterpret_cast<const __half2*>(&sh)) * __ldg(S.gs + w / S.wpt);
+        e2m1x8_to_h2x4(__ldcs(S.q + w), o);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&o[j]));
+          const __half2 h = __floats2half2_rn(f.x * sc, f.y * sc);
+          o[j] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+      } else {
+        tc::dequant_word_natural(__ldcs(S.q + w), scale_h2(__ldg(S.s + (w >> 2))), o);
+      }
       __stcs(S.out + w, make_uint4(o[0], o[1], o[2], o[3]));
     }
     base += S.n;
@@ -971,11 +990,15 @@ cudaError_t dequant(const PrefillArgs& P, const uint16_t* x, int T, char* b, con
     const void* q[5] = {P.W_in_q, P.W_out_q, P.gate_q, P.up_q, P.down_q};
     const uint16_t* sc[5] = {P.W_in_s, P.W_out_s, P.gate_s, P.up_s, P.down_s};
     __half* out[5] = {win16, wout16, gate16, up16, down16};
+    const float* gsp[5] = {P.W_in_gs, P.W_out_gs, P.gate_gs, P.up_gs, P.down_gs};
     for (int i = 0; i < 5; ++i) {
       J.seg[i].q = static_cast<const uint32_t*>(q[i]);
       J.seg[i].s = sc[i];
       J.seg[i].out = reinterpret_cast<uint4*>(out[i]);
       J.seg[i].n = i < 2 ? wwords : ewords;
+      J.seg[i].fp4 = P.wfmt != 0;
+      J.seg[i].gs = gsp[i];
+      J.seg[i].wpt = i < 2 ? wwords / P.G : ewords / P.E;  // one group's / one expert's matrix
     }
     J.nseg = 5;
     J.x = reinterpret_cast<const uint4*>(x);

@@ -28,6 +28,14 @@ struct PrefillArgs {
   const uint16_t* B_in;
   const uint16_t* A_out;
   const uint16_t* B_out;
+  // weight format (LMOE_WEIGHTS_*); NVFP4: E4M3 bytes behind the *_s pointers
+  // and the per-tensor fp32 scales
+  int wfmt;
+  const float* W_in_gs;
+  const float* W_out_gs;
+  const float* gate_gs;
+  const float* up_gs;
+  const float* down_gs;
   unsigned* err;
   int num_sms;
   long long timeout;

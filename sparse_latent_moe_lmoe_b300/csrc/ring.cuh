@@ -4,11 +4,12 @@
 // transaction count), far ahead of the warps that consume them; a consuming
 // warp hands the slot back through its "empty" mbarrier.
 //
-// An int4 chunk in a slot is a TMA box in 128-byte swizzle: row r of the
-// chunk is LPR 128-byte lines (line i = r*LPR + k/256 for element k), and
-// 16-byte unit j of line i sits at unit j ^ (i & 7), so the 16-byte loads of
-// the 8 rows a warp reads at once fall in different banks. The chunk's bf16
-// scales, [rows][K/32], follow it in the slot as a second, unswizzled box.
+// A chunk of packed 4-bit codes in a slot is in the 128-byte swizzle: row r
+// of the chunk is LPR 128-byte lines (line i = r*LPR + k/256 for element k),
+// and 16-byte unit j of line i sits at unit j ^ (i & 7), so the 16-byte loads
+// of the 8 rows a warp reads at once fall in different banks. The chunk's
+// scales ([rows][K/32] 16-bit words: one bf16 for int4, two E4M3 bytes for
+// NVFP4) follow it in the slot, unswizzled.
 #pragma once
 #include "common.cuh"
 
@@ -93,6 +94,44 @@ LMOE_DEV bool mbar_test(uint64_t* m, uint32_t parity) {
   return ok != 0;
 }
 
+// Weight formats of a chunk: 0 = int4 with one bf16 scale per 32 elements; 1
+// = NVFP4 (E2M1 codes with one E4M3 scale per 16 elements). A lane's 16-bit
+// scale word covers the same 32 elements in both: one bf16, or two E4M3
+// bytes (the low byte for the first 16).
+//
+// NVFP4 words are stored with byte b holding elements b (low nibble) and
+// b + 4 (high nibble), so one hardware conversion per byte yields the half2
+// (e_b, e_{b+4}) that the fragments pair (the order dequant_word produces).
+LMOE_DEV void dequant_fp4_word(uint32_t v, __half2 s2, uint32_t out[4]) {
+  e2m1x8_to_h2x4(v, out);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2 h = __hmul2(*reinterpret_cast<__half2*>(&out[i]), s2);  // code * scale: exact in fp16
+    out[i] = *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+// a lane's scale word -> the half2 scales of its first and second 16 elements
+template <int WF>
+LMOE_DEV void lane_scales(uint16_t w, __half2& first, __half2& second) {
+  if (WF == 0) {
+    first = second = scale_h2(w);
+  } else {
+    const uint32_t h = e4m3x2_to_h2(w);
+    const __half2 hh = *reinterpret_cast<const __half2*>(&h);
+    first = __low2half2(hh);
+    second = __high2half2(hh);
+  }
+}
+
+template <int WF>
+LMOE_DEV void dequant_any(uint32_t v, __half2 s2, uint32_t out[4]) {
+  if (WF == 0)
+    dequant_word(v, s2, out);
+  else
+    dequant_fp4_word(v, s2, out);
+}
+
 // acc[nt] += W[16 rows][chunks c0 .. c0+nc of 128 elements] * fragments,
 // with W in a ring slot as a TMA box in 128-byte swizzle: row r of the box is
 // LPR 128-byte lines (line i = r*LPR + k/256 for element k of the box), and
@@ -100,7 +139,7 @@ LMOE_DEV bool mbar_test(uint64_t* m, uint32_t parity) {
 // aligned) slot base, row0 the first row of the tile, `s` the box's scales
 // [rows][SS]. Chunk c0 + c of the box meets fragment chunk c of `frag` (see
 // frag_index; the caller offsets `frag` to the box's chunk c0).
-template <int NT>
+template <int NT, int WF>
 LMOE_DEV void mma_slot(const unsigned char* w, int LPR, int row0, const uint16_t* s, int SS, int c0, int nc,
                        const uint4* frag, float acc[NT][4]) {
   const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
@@ -128,7 +167,9 @@ LMOE_DEV void mma_slot(const unsigned char* w, int LPR, int row0, const uint16_t
   for (int c = 0; c < nc; ++c) {
     const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
     const uint32_t wb[4] = {b.x, b.y, b.z, b.w};
-    const __half2 h0 = scale_h2(sa), h8 = scale_h2(sb);
+    __half2 h0a, h0b, h8a, h8b;  // scales of rows r0 / r8, first and second 16 elements
+    lane_scales<WF>(sa, h0a, h0b);
+    lane_scales<WF>(sb, h8a, h8b);
     if (c + 1 < nc) ld(c + 1, a, b, sa, sb);
     uint4 fv[4][NT];
 #pragma unroll
@@ -138,8 +179,8 @@ LMOE_DEV void mma_slot(const unsigned char* w, int LPR, int row0, const uint16_t
 #pragma unroll
     for (int mp = 0; mp < 4; ++mp) {
       uint32_t A[4], B8[4];
-      dequant_word(wa[mp], h0, A);
-      dequant_word(wb[mp], h8, B8);
+      dequant_any<WF>(wa[mp], mp < 2 ? h0a : h0b, A);
+      dequant_any<WF>(wb[mp], mp < 2 ? h8a : h8b, B8);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const uint4 f = fv[mp][nt];
@@ -155,18 +196,21 @@ LMOE_DEV void mma_slot(const unsigned char* w, int LPR, int row0, const uint16_t
 }
 
 // acc[nt] += W[16 rows m*16 ..][32 elements] * v, for a matrix slice of 32
-// reduction elements per row held as [rows][16 bytes] (row r's 32 packed int4
-// at byte 16 r) with one bf16 scale per row, `sc`. Lane (gid, tig) reads word
+// reduction elements per row held as [rows][16 bytes] (row r's 32 packed
+// codes at byte 16 r) with one scale word per row, `sc`. Lane (gid, tig) reads word
 // tig of rows gid and gid+8 -- elements 8 tig .. 8 tig + 7 -- so the matching
 // activation entry vfr[nt*32 + lane] holds elements 8 tig .. 8 tig + 7 of
 // token 8 nt + gid, packed as (e0,e4) (e1,e5) (e2,e6) (e3,e7).
-template <int NT>
+template <int NT, int WF>
 LMOE_DEV void mma_slice32(const uint32_t* wsl, const uint16_t* sc, int m, const uint4* vfr, float acc[NT][4]) {
   const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
   const int r0 = 16 * m + gid, r8 = r0 + 8;
   uint32_t A[4], B8[4];
-  dequant_word(wsl[r0 * 4 + tig], scale_h2(sc[r0]), A);
-  dequant_word(wsl[r8 * 4 + tig], scale_h2(sc[r8]), B8);
+  __half2 s0a, s0b, s8a, s8b;  // word tig holds elements 8 tig .. 8 tig + 7: the first 16 for tig < 2
+  lane_scales<WF>(sc[r0], s0a, s0b);
+  lane_scales<WF>(sc[r8], s8a, s8b);
+  dequant_any<WF>(wsl[r0 * 4 + tig], tig < 2 ? s0a : s0b, A);
+  dequant_any<WF>(wsl[r8 * 4 + tig], tig < 2 ? s8a : s8b, B8);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const uint4 f = vfr[nt * 32 + lane];

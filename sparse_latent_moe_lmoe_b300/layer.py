@@ -39,7 +39,8 @@ def _stream(stream=None):
 class LatentMoE:
     """One latent MoE layer on one GPU.
 
-    shape: any object with d, E, G, k, L, f, lora_rank, has_bias attributes.
+    shape: any object with d, E, G, k, L, f, lora_rank, has_bias attributes
+    (and optionally wfmt: "int4" or "nvfp4").
     weights: dict with the keys of capi.WEIGHT_FIELDS (numpy arrays or torch
     tensors in the layouts of include/lmoe.h; bf16 as uint16 bits).
     """
@@ -49,8 +50,10 @@ class LatentMoE:
         self.shape = shape
         self.device = torch.device("cuda", device)
         self.dev_weights = {n: to_device(weights.get(n), self.device) for n in capi.WEIGHT_FIELDS}
-        self.cfg = LmoeConfig(shape.d, shape.E, shape.G, shape.k, shape.L, shape.f, 32, shape.lora_rank,
-                              1 if shape.has_bias else 0, flags, timeout_cycles, decode_max_T, force_path)
+        nvfp4 = getattr(shape, "wfmt", "int4") == "nvfp4"
+        self.cfg = LmoeConfig(shape.d, shape.E, shape.G, shape.k, shape.L, shape.f, 16 if nvfp4 else 32,
+                              shape.lora_rank, 1 if shape.has_bias else 0, flags, timeout_cycles, decode_max_T,
+                              force_path, capi.WEIGHTS_NVFP4 if nvfp4 else capi.WEIGHTS_INT4)
         self.wts = LmoeWeights(*[None if t is None else t.data_ptr() for t in
                                  (self.dev_weights[n] for n in capi.WEIGHT_FIELDS)])
         self.h = capi.lmoe_create(self.cfg, self.wts, device)

@@ -28,7 +28,7 @@ def test_library_exports_every_declared_function():
 def test_host_side_validation_without_gpu():
     from sparse_latent_moe_lmoe_b300 import capi
     lib = capi.library()
-    assert capi.lmoe_version() == 100
+    assert capi.lmoe_version() == 101
     assert lib.lmoe_workspace_size(None, 8) == 0
     assert lib.lmoe_route(None, None, 8, None, None, None, None, None) == 1
     assert lib.lmoe_layer_forward(None, None, 8, None, None, None, None) == 1
@@ -45,6 +45,12 @@ def test_host_side_validation_without_gpu():
     cfg.G = 3  # E % G != 0
     assert lib.lmoe_create(ctypes.byref(h), ctypes.byref(cfg), ctypes.byref(w), 0) == 1
     cfg.G = 2
+    assert lib.lmoe_create(ctypes.byref(h), ctypes.byref(cfg), ctypes.byref(w), 0) == 1  # null weights
+    cfg.weight_format = 2  # no such format
+    assert lib.lmoe_create(ctypes.byref(h), ctypes.byref(cfg), ctypes.byref(w), 0) == 1
+    cfg.weight_format = capi.WEIGHTS_NVFP4  # NVFP4 scales come per 16 elements
+    assert lib.lmoe_create(ctypes.byref(h), ctypes.byref(cfg), ctypes.byref(w), 0) == 2
+    cfg.qgroup = 16
     assert lib.lmoe_create(ctypes.byref(h), ctypes.byref(cfg), ctypes.byref(w), 0) == 1  # null weights
     assert h.value is None
     for s in range(8):
