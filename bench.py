@@ -249,8 +249,9 @@ def run_reference(args):
         return
     import lmoe_synth as S
     import oracle as O
-    if args.workload in S.STACK_WORKLOADS:  # one token through one layer per step; value over the whole stack
-        sh, nl, T, xseed = S.STACK_WORKLOADS[args.workload]
+    stacks = {**S.STACK_WORKLOADS, **{n: v[:4] for n, v in S.STAGED_STACK_WORKLOADS.items()}}
+    if args.workload in stacks:  # one token through one layer per step; value over the whole stack
+        sh, nl, T, xseed = stacks[args.workload]
         Ly = O.Layer(sh, S.make_stack_layer(sh, 0))
         x = S.make_x(1, sh.d, xseed)
         for _ in range(max(args.warmup, 0)):
@@ -634,6 +635,94 @@ def run_stack(args):
         dist.destroy_process_group()
 
 
+def run_staged_stack(args):
+    """A stack whose expert weights stay in page-locked host memory, with a
+    fixed number of GPU slots per layer: every step routes new tokens, each
+    layer stages its routed experts that hold no slot, and the next layer's
+    prerouter stages its predicted experts on a second stream meanwhile. One
+    CUDA graph per input (the slot tables live on the device and carry over
+    from step to step). value = T / step time; the line adds the staging
+    counters and the bytes moved over the host link per token."""
+    import numpy as np
+    import torch
+
+    import lmoe_synth as S
+    from sparse_latent_moe_lmoe_b300 import LatentMoE, LatentMoEStack, capi
+
+    rank, local, world = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = dist_init(world, True)
+    sh, nl, T, xseed, slots = S.STAGED_STACK_WORKLOADS[args.workload]
+    t0 = time.perf_counter()
+    layers = []
+    for l in range(nl):
+        W = S.make_stack_layer(sh, l)
+        layers.append(LatentMoE(sh, W, device=local, flags=capi.FLAG_STAGED_EXPERTS, expert_slots=slots,
+                                expert_weights_on_host=True))
+        del W
+    gen_s = time.perf_counter() - t0
+    stack = LatentMoEStack(layers)
+    stack.workspace(T)
+    n_in = max(args.steps, 1) + max(args.warmup, 3)
+    xs = [torch.from_numpy(S.make_x(T, sh.d, 5000 + i).view(np.int16)).to(dev).view(torch.bfloat16)
+          for i in range(n_in)]
+    y = torch.empty_like(xs[0])
+    stack.forward(xs[0], out=y)
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream()
+    graphs = []
+    for xi in xs:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            stack.forward(xi, out=y)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    nw = max(args.warmup, 3)
+    for g in graphs[:nw]:
+        g.replay()
+    torch.cuda.synchronize()
+    before = [m.stage_stats() for m in layers]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(dist)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for g in graphs[nw:nw + args.steps]:
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    ms = max_over_ranks(dist, e0.elapsed_time(e1), dev)
+    ck = clocks.stop()
+    after = [m.stage_stats() for m in layers]
+    d = {k: sum(a[k] - b[k] for a, b in zip(after, before)) for k in after[0]}
+    step_s = ms / args.steps / 1000.0
+    value = world * T / step_s
+    tok = T * args.steps
+    staging = {"slots_per_layer": slots, "experts_per_layer": sh.E, "routed_per_token": d["routed"] / tok,
+               "hit_rate": d["hits"] / max(d["routed"], 1), "on_demand_per_token": d["staged_on_demand"] / tok,
+               "prefetched_per_token": d["prefetched"] / tok, "host_bytes_per_token": d["bytes_copied"] / tok,
+               "host_link_gbs": d["bytes_copied"] / (ms / 1000.0) / 1e9,
+               "predictor": "the next layer's own router on the current layer's input (a stand-in for a trained head)"}
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": nw, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int4 weights, fp16 tensor-core operands, fp32 accumulate",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "layers": nl, "T": T, "d": sh.d, "E": sh.E, "G": sh.G, "k": sh.k,
+                       "L": sh.L, "f": sh.f, "parallelism": f"replicas x{world}",
+                       "inputs": "new tokens every step (one graph per input)",
+                       "weight_generation_s": round(gen_s, 1)},
+            "staging": staging, "roofline": None, "e2e": None,
+            "gpu_launches": nl * (capi.lmoe_launch_count(layers[0].h, T) + 1 + 3) * args.steps, "clocks": ck}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def run_sweep(args):
     """Tokens/s and HBM roofline fraction of the decode path at T = 1..16
     (speculative decoding verifies several candidate tokens per weight read):
@@ -700,6 +789,8 @@ def main():
         run_sweep(args)
     elif args.workload in S.STACK_WORKLOADS:
         run_stack(args)
+    elif args.workload in S.STAGED_STACK_WORKLOADS:
+        run_staged_stack(args)
     else:
         run_ours(args)
 

@@ -65,8 +65,26 @@ typedef enum {
 } lmoe_status;
 
 /* config.flags: LMOE_FLAG_MULTI_KERNEL_DECODE runs the decode path as its
- * sequence of per-step kernels instead of the single persistent kernel. */
-enum { LMOE_FLAG_MULTI_KERNEL_DECODE = 1u };
+ * sequence of per-step kernels instead of the single persistent kernel.
+ *
+ * LMOE_FLAG_STAGED_EXPERTS keeps the per-expert weights (gate, up, Down) in
+ * host memory and only `expert_slots` of them in GPU memory ("Edge0-145B:
+ * Frontier AI Capabilities on Your Own Computer", "Under the Hood of Edge0",
+ * "Loading": hot experts stay in GPU memory, an expert library sits in system
+ * memory and experts are brought in as needed; "Edge0-145B: Run a 145B
+ * Open-Source Model on Your Laptop", "The Three Pillars That Make It Fast":
+ * active experts load into a staged fixed-slot buffer, and a prerouter's
+ * prediction of the next layer's experts drives the prefetch). The caller's
+ * gate / up / Down pointers may then be page-locked host memory that the
+ * device can address (cudaHostAlloc, or cudaHostRegister with mapping).
+ * lmoe_create copies them once into the handle's own page-locked library, in
+ * the layout the decode pass streams. A decode-path pass (T <= 16, the
+ * single-kernel pass) first routes its tokens, then copies every routed
+ * expert that holds no slot into a slot (the slots are reused in clock order,
+ * never one whose expert this pass routes), then runs the pass on the slots;
+ * its output is bit for bit that of an unstaged handle. The prefill path and
+ * the per-step decode kernels read the caller's expert pointers directly. */
+enum { LMOE_FLAG_MULTI_KERNEL_DECODE = 1u, LMOE_FLAG_STAGED_EXPERTS = 2u };
 
 /* config.weight_format: the five shared / expert weight families are int4
  * (symmetric per 32 elements, bf16 scales) or NVFP4 (NVIDIA's FP4 format, the
@@ -95,6 +113,7 @@ typedef struct {
   int force_path;   /* LMOE_PATH_* */
   int weight_format; /* LMOE_WEIGHTS_*; NVFP4 layers run the single-kernel decode pass and the prefill
                         path (LMOE_ERR_UNSUPPORTED where only the multi-kernel decode path would fit) */
+  int expert_slots;  /* LMOE_FLAG_STAGED_EXPERTS: experts held in GPU memory, min(E, 16 k) <= expert_slots <= E */
 } lmoe_config;
 
 /* Device pointers to the layer's weights (borrowed for the handle's life).
@@ -303,12 +322,38 @@ size_t lmoe_host_staging_size(const lmoe_handle* h, int T);
  * completes), and prefetches the next layer's router rows and W_in tiles
  * into L2 during its own tail. Otherwise each layer runs as
  * lmoe_layer_forward without a residual, followed by a kernel that adds the
- * residual and rounds once. The two give the same bits. ws must hold
+ * residual and rounds once. The two give the same bits. When the layers
+ * are staged handles (LMOE_FLAG_STAGED_EXPERTS), layer l + 1's prerouter
+ * runs on the handle's second stream while layer l runs (given x_l), and
+ * layer l + 1 starts after it. ws must hold
  * lmoe_stack_workspace_size(layers[0], T) bytes. Returns LMOE_ERR_INVALID_ARG
  * for n_layers < 1, a null handle or mismatched shapes or devices, and the
  * errors of lmoe_layer_forward. */
 lmoe_status lmoe_stack_forward(lmoe_handle* const* layers, int n_layers, const uint16_t* x, int T, uint16_t* y,
                                void* ws, lmoe_stream stream);
+
+/* The prerouter of a staged handle h (LMOE_FLAG_STAGED_EXPERTS): selects
+ * the top-k experts of h's router for the T <= 16 tokens x (device bf16
+ * [T][d]) and copies those that hold no slot into h's slots, on `stream`,
+ * as the forward does for a routed expert. It is meant for the next layer
+ * of a stack, given the current layer's input one layer ahead; the
+ * prediction here is h's own router applied to that earlier input (the
+ * pages' prerouter is a trained head: a stated stand-in). It uses scratch
+ * inside the handle, not a workspace, so it may run on a second stream while
+ * another layer runs; it must not run concurrently with a forward or another
+ * prefetch of the same handle. Returns LMOE_ERR_INVALID_ARG for a handle
+ * without staging or T outside 1..16. */
+lmoe_status lmoe_prefetch_experts(lmoe_handle* h, const uint16_t* x, int T, lmoe_stream stream);
+
+/* Counters of a staged handle since its creation (host copy; waits for the
+ * device): decode passes, experts those passes routed (distinct per pass),
+ * routed experts already in a slot when their pass started (hits), experts
+ * the passes had to copy themselves, experts the prerouter copied, and the
+ * bytes copied from host memory. */
+typedef struct {
+  unsigned long long passes, routed, hits, staged_on_demand, prefetched, bytes_copied;
+} lmoe_stage_stats;
+lmoe_status lmoe_get_stage_stats(lmoe_handle* h, lmoe_stage_stats* out);
 
 /* Workspace bytes of lmoe_stack_forward: one layer's workspace plus two
  * [T][d] bf16 activation buffers. 0 on a bad handle or T < 0. */

@@ -239,6 +239,14 @@ STACK_WORKLOADS = {
     "stack48_prefill_t4096": (EDGE0, 48, 4096, 1),
 }
 
+# stacks whose expert weights stay in page-locked host memory with a fixed
+# number of GPU slots per layer (the staged expert cache):
+# name: (layer shape, layers, tokens per step, x seed, GPU slots per layer)
+STAGED_STACK_WORKLOADS = {
+    "stack8_t1_staged": (EDGE0, 8, 1, 1, 160),
+    "stack8_t8_staged": (EDGE0, 8, 8, 1, 160),
+}
+
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (b.astype(np.uint32) << 16).view(np.float32)

@@ -17,12 +17,13 @@ STATUS = {0: "LMOE_OK", 1: "LMOE_ERR_INVALID_ARG", 2: "LMOE_ERR_UNSUPPORTED", 3:
           4: "LMOE_ERR_CUDA", 5: "LMOE_ERR_TIMEOUT", 6: "LMOE_ERR_DEVICE_CHECK", 7: "LMOE_ERR_NO_MEMORY"}
 PATH_AUTO, PATH_DECODE, PATH_PREFILL = 0, 1, 2
 FLAG_MULTI_KERNEL_DECODE = 1
+FLAG_STAGED_EXPERTS = 2
 
 EXPORTS = ("lmoe_status_string", "lmoe_version", "lmoe_create", "lmoe_destroy", "lmoe_workspace_size", "lmoe_route",
            "lmoe_permute", "lmoe_expert_forward", "lmoe_combine", "lmoe_layer_forward", "lmoe_layer_forward_noalloc",
            "lmoe_layer_forward_host", "lmoe_stack_forward", "lmoe_stack_workspace_size",
            "lmoe_host_staging_size", "lmoe_check", "lmoe_set_timeout", "lmoe_set_stage_events", "lmoe_stage_name",
-           "lmoe_launch_count", "lmoe_decode_routing")
+           "lmoe_launch_count", "lmoe_decode_routing", "lmoe_prefetch_experts", "lmoe_get_stage_stats")
 
 
 class LmoeError(RuntimeError):
@@ -35,7 +36,8 @@ class LmoeConfig(ctypes.Structure):
     _fields_ = [("d", ctypes.c_int), ("E", ctypes.c_int), ("G", ctypes.c_int), ("k", ctypes.c_int),
                 ("L", ctypes.c_int), ("f", ctypes.c_int), ("qgroup", ctypes.c_int), ("lora_rank", ctypes.c_int),
                 ("has_bias", ctypes.c_int), ("flags", ctypes.c_uint), ("timeout_cycles", ctypes.c_longlong),
-                ("decode_max_T", ctypes.c_int), ("force_path", ctypes.c_int), ("weight_format", ctypes.c_int)]
+                ("decode_max_T", ctypes.c_int), ("force_path", ctypes.c_int), ("weight_format", ctypes.c_int),
+                ("expert_slots", ctypes.c_int)]
 
 
 WEIGHTS_INT4, WEIGHTS_NVFP4 = 0, 1
@@ -50,6 +52,11 @@ class LmoeWeights(ctypes.Structure):
 
 PERM_FIELDS = ("expert_offsets", "sorted_assign", "inv", "group_offsets", "group_tok_offsets", "group_tokens",
                "assign_row")
+
+
+class LmoeStageStats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_ulonglong) for n in ("passes", "routed", "hits", "staged_on_demand", "prefetched",
+                                                   "bytes_copied")]
 
 
 class LmoePerm(ctypes.Structure):
@@ -85,6 +92,8 @@ def _load():
         "lmoe_stage_name": ([P, I, I, ctypes.POINTER(I)], ctypes.c_char_p),
         "lmoe_launch_count": ([P, I], I),
         "lmoe_decode_routing": ([P, P, I, P, P, P, P], S),
+        "lmoe_prefetch_experts": ([P, P, I, P], S),
+        "lmoe_get_stage_stats": ([P, ctypes.POINTER(LmoeStageStats)], S),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -207,3 +216,13 @@ def lmoe_stage_name(h, T: int, i: int):
     cnt = ctypes.c_int(0)
     name = _lib.lmoe_stage_name(h, int(T), int(i), ctypes.byref(cnt))
     return name.decode(), cnt.value
+
+
+def lmoe_prefetch_experts(h, x, T, stream) -> None:
+    _ok(_lib.lmoe_prefetch_experts(h, x, T, stream), "lmoe_prefetch_experts")
+
+
+def lmoe_get_stage_stats(h) -> dict:
+    st = LmoeStageStats()
+    _ok(_lib.lmoe_get_stage_stats(h, ctypes.byref(st)), "lmoe_get_stage_stats")
+    return {n: int(getattr(st, n)) for n, _ in LmoeStageStats._fields_}

@@ -34,6 +34,24 @@ struct lmoe_handle {
   cudaEvent_t ev_fork, ev_join;
   uint8_t* d_pack;                   // the decode pass's chunk-major copy of the weights (decode_pack_bytes)
   std::vector<cudaEvent_t> events;
+  // staged experts (LMOE_FLAG_STAGED_EXPERTS): the library in page-locked
+  // host memory, the slots in GPU memory, their tables and the prerouter's
+  // scratch
+  bool staged;
+  size_t expert_bytes;
+  uint8_t* h_lib;                    // [E] experts in the decode pass's layout
+  const uint8_t* d_lib;              // its device address
+  uint8_t* d_slots;                  // [expert_slots] experts
+  int32_t* d_slot_of;                // [E]
+  int32_t* d_expert_in;              // [expert_slots]
+  StageState* d_stage;
+  int2* d_copies;                    // [256], the forward's plan
+  int2* d_pre_copies;                // [256], the prerouter's plan
+  float* d_pre_logits;               // [16][E]
+  int32_t* d_pre_idx;                // [16][k]
+  float* d_pre_w;                    // [16][k]
+  unsigned* d_pre_tickets;           // the prerouter's router tickets
+  cudaEvent_t ev_pf_in, ev_pf_done;  // stack: the prerouter's start and end on the second stream
 };
 
 namespace {
@@ -57,7 +75,10 @@ lmoe_status validate_config(const lmoe_config* c) {
   if (c->d % 128 != 0 || c->L % 32 != 0 || c->f % 32 != 0) return LMOE_ERR_UNSUPPORTED;
   if (c->L % 16 != 0 || c->f % 16 != 0) return LMOE_ERR_UNSUPPORTED;
   if (c->lora_rank < 0 || c->lora_rank > 128 || c->lora_rank % 16 != 0) return LMOE_ERR_UNSUPPORTED;
-  if (c->flags & ~(unsigned)LMOE_FLAG_MULTI_KERNEL_DECODE) return LMOE_ERR_UNSUPPORTED;
+  if (c->flags & ~(unsigned)(LMOE_FLAG_MULTI_KERNEL_DECODE | LMOE_FLAG_STAGED_EXPERTS)) return LMOE_ERR_UNSUPPORTED;
+  if ((c->flags & LMOE_FLAG_STAGED_EXPERTS) &&
+      (c->expert_slots < (16 * c->k < c->E ? 16 * c->k : c->E) || c->expert_slots > c->E))
+    return LMOE_ERR_INVALID_ARG;  // a pass's routed experts (at most min(E, 16 k)) must fit
   if (c->decode_max_T < 0 || c->decode_max_T > kMaxDecodeT) return LMOE_ERR_UNSUPPORTED;
   if (c->force_path < LMOE_PATH_AUTO || c->force_path > LMOE_PATH_PREFILL) return LMOE_ERR_INVALID_ARG;
   if (c->timeout_cycles < 0) return LMOE_ERR_INVALID_ARG;
@@ -270,6 +291,8 @@ FusedArgs fused_args(const lmoe_handle* h, const DecodeArgs& A, void* ws) {
 }
 
 // decode path for any T, in passes of <= 16 tokens
+StagePlan stage_plan(const lmoe_handle* h, const int32_t* idx, int n, int must, int2* copies);
+
 lmoe_status decode_layer(lmoe_handle* h, const uint16_t* x, int T, const uint16_t* residual, uint16_t* y, void* ws,
                          cudaStream_t st) {
   const lmoe_config& c = h->cfg;
@@ -284,6 +307,22 @@ lmoe_status decode_layer(lmoe_handle* h, const uint16_t* x, int T, const uint16_
     if (use_fused(h, A)) {
       FusedArgs F = fused_args(h, A, ws);
       cudaError_t e;
+      if (h->staged) {  // route, then bring every routed expert without a slot into one
+        hook.before(st);
+        e = launch_route(A, 0, ws_logits(h, ws), st);
+        hook.after(st);
+        if (e != cudaSuccess) return LMOE_ERR_CUDA;
+        const StagePlan P = stage_plan(h, A.idx, A.T * c.k, 1, h->d_copies);
+        hook.before(st);
+        e = launch_stage_plan(P, st);
+        hook.after(st);
+        if (e != cudaSuccess) return LMOE_ERR_CUDA;
+        hook.before(st);
+        e = launch_stage_copy(P, h->d_lib, h->d_slots, h->num_sms, st);
+        hook.after(st);
+        if (e != cudaSuccess) return LMOE_ERR_CUDA;
+        F.slot_of = h->d_slot_of;
+      }
       if (A.r > 0) {  // the LoRA branch: lora_in before, lora_q and lora_out after
         // scratch of the multi-kernel sequence, unused by the single kernel:
         // Ppart in Hp, P in Pin, Hl in V, Z in fp32 in Z, Q in Qout
@@ -325,6 +364,98 @@ lmoe_status decode_layer(lmoe_handle* h, const uint16_t* x, int T, const uint16_
     e = launch_experts(A, 0, st, &hook);
     if (e != cudaSuccess) return LMOE_ERR_CUDA;
   }
+  return LMOE_OK;
+}
+
+// The staged-expert state of a new handle: every expert's unit chunks are
+// built once in GPU memory (from the caller's pointers, which may address
+// host memory), moved into a page-locked host library, and the handle keeps
+// expert_slots slots in GPU memory with empty tables.
+lmoe_status create_stage(lmoe_handle* h, const DecodeArgs& probe) {
+  const lmoe_config& c = h->cfg;
+  h->staged = true;
+  h->expert_bytes = decode_expert_bytes(c.L, c.f);
+  const size_t lib_bytes = (size_t)c.E * h->expert_bytes;
+  uint8_t* tmp = nullptr;
+  if (cudaMalloc(&tmp, lib_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return LMOE_ERR_NO_MEMORY;
+  }
+  lmoe_status s = LMOE_OK;
+  if (launch_decode_pack(probe, h->d_pack, &h->pk, 0, tmp) != cudaSuccess) s = LMOE_ERR_CUDA;
+  if (s == LMOE_OK && cudaHostAlloc(&h->h_lib, lib_bytes, cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess) {
+    h->h_lib = nullptr;
+    s = LMOE_ERR_NO_MEMORY;
+  }
+  if (s == LMOE_OK && cudaMemcpy(h->h_lib, tmp, lib_bytes, cudaMemcpyDeviceToHost) != cudaSuccess) s = LMOE_ERR_CUDA;
+  cudaFree(tmp);
+  void* dl = nullptr;
+  if (s == LMOE_OK && cudaHostGetDevicePointer(&dl, h->h_lib, 0) != cudaSuccess) s = LMOE_ERR_CUDA;
+  if (s != LMOE_OK) {
+    cudaGetLastError();
+    return s;
+  }
+  h->d_lib = static_cast<const uint8_t*>(dl);
+  const int S = c.expert_slots;
+  if (cudaMalloc(&h->d_slots, (size_t)S * h->expert_bytes) != cudaSuccess ||
+      cudaMalloc(&h->d_slot_of, (size_t)c.E * 4) != cudaSuccess ||
+      cudaMalloc(&h->d_expert_in, (size_t)S * 4) != cudaSuccess ||
+      cudaMalloc(&h->d_stage, sizeof(StageState)) != cudaSuccess ||
+      cudaMalloc(&h->d_copies, 256 * sizeof(int2)) != cudaSuccess ||
+      cudaMalloc(&h->d_pre_copies, 256 * sizeof(int2)) != cudaSuccess ||
+      cudaMalloc(&h->d_pre_logits, (size_t)kMaxDecodeT * c.E * 4) != cudaSuccess ||
+      cudaMalloc(&h->d_pre_idx, (size_t)kMaxDecodeT * c.k * 4) != cudaSuccess ||
+      cudaMalloc(&h->d_pre_w, (size_t)kMaxDecodeT * c.k * 4) != cudaSuccess ||
+      cudaMalloc(&h->d_pre_tickets, 64) != cudaSuccess) {
+    cudaGetLastError();
+    return LMOE_ERR_NO_MEMORY;
+  }
+  cudaMemset(h->d_slot_of, 0xff, (size_t)c.E * 4);
+  cudaMemset(h->d_expert_in, 0xff, (size_t)S * 4);
+  cudaMemset(h->d_stage, 0, sizeof(StageState));
+  cudaMemset(h->d_pre_tickets, 0, 64);
+  if (cudaEventCreateWithFlags(&h->ev_pf_in, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->ev_pf_done, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    return LMOE_ERR_CUDA;
+  }
+  h->pk.unit = h->d_slots;
+  return LMOE_OK;
+}
+
+StagePlan stage_plan(const lmoe_handle* h, const int32_t* idx, int n, int must, int2* copies);
+lmoe_status prefetch_on(lmoe_handle* h, const uint16_t* x, int T, cudaStream_t st);
+
+StagePlan stage_plan(const lmoe_handle* h, const int32_t* idx, int n, int must, int2* copies) {
+  StagePlan P;
+  P.idx = idx;
+  P.n = n;
+  P.E = h->cfg.E;
+  P.S = h->cfg.expert_slots;
+  P.must = must;
+  P.slot_of = h->d_slot_of;
+  P.expert_in = h->d_expert_in;
+  P.st = h->d_stage;
+  P.copies = copies;
+  P.expert_bytes = h->expert_bytes;
+  P.err = h->d_err;
+  return P;
+}
+
+// The prerouter of a staged handle: h's router on x (the tokens' input one
+// layer early), top-k into the handle's own scratch, then the staging of
+// those experts (as a prefetch).
+lmoe_status prefetch_on(lmoe_handle* h, const uint16_t* x, int T, cudaStream_t st) {
+  DecodeArgs A = base_args(h, nullptr);
+  A.T = T;
+  A.x = x;
+  A.idx = h->d_pre_idx;
+  A.w = h->d_pre_w;
+  A.tickets = h->d_pre_tickets;
+  if (launch_route(A, 0, h->d_pre_logits, st) != cudaSuccess) return LMOE_ERR_CUDA;
+  const StagePlan P = stage_plan(h, h->d_pre_idx, T * h->cfg.k, 0, h->d_pre_copies);
+  if (launch_stage_plan(P, st) != cudaSuccess) return LMOE_ERR_CUDA;
+  if (launch_stage_copy(P, h->d_lib, h->d_slots, h->num_sms, st) != cudaSuccess) return LMOE_ERR_CUDA;
   return LMOE_OK;
 }
 
@@ -496,12 +627,21 @@ lmoe_status lmoe_create(lmoe_handle** out, const lmoe_config* cfg, const lmoe_we
     probe.T = 1;
     h->pack_ok = false;
     if (h->fused_grid > 0 && fused_decode_supported(probe, h->fused_grid)) {
-      if (cudaMalloc(&h->d_pack, decode_pack_bytes(cfg->d, cfg->E, cfg->G, cfg->L, cfg->f)) != cudaSuccess) {
+      const bool staged = (cfg->flags & LMOE_FLAG_STAGED_EXPERTS) != 0;
+      const size_t pb = staged ? decode_pack_bytes_shared(cfg->d, cfg->E, cfg->G, cfg->L, cfg->f)
+                               : decode_pack_bytes(cfg->d, cfg->E, cfg->G, cfg->L, cfg->f);
+      if (cudaMalloc(&h->d_pack, pb) != cudaSuccess) {
         cudaGetLastError();
         lmoe_destroy(h);
         return LMOE_ERR_NO_MEMORY;
       }
-      if (launch_decode_pack(probe, h->d_pack, &h->pk, 0) != cudaSuccess) {
+      if (staged) {
+        lmoe_status ss = create_stage(h, probe);
+        if (ss != LMOE_OK) {
+          lmoe_destroy(h);
+          return ss;
+        }
+      } else if (launch_decode_pack(probe, h->d_pack, &h->pk, 0) != cudaSuccess) {
         lmoe_destroy(h);
         return LMOE_ERR_CUDA;
       }
@@ -534,6 +674,13 @@ lmoe_status lmoe_destroy(lmoe_handle* h) {
   if (h->d_ctr) cudaFree(h->d_ctr);
   if (h->d_launches) cudaFree(h->d_launches);
   if (h->d_pack) cudaFree(h->d_pack);
+  if (h->h_lib) cudaFreeHost(h->h_lib);
+  void* stage_bufs[] = {h->d_slots, h->d_slot_of, h->d_expert_in, h->d_stage, h->d_copies, h->d_pre_copies,
+                        h->d_pre_logits, h->d_pre_idx, h->d_pre_w, h->d_pre_tickets};
+  for (void* p : stage_bufs)
+    if (p) cudaFree(p);
+  if (h->ev_pf_in) cudaEventDestroy(h->ev_pf_in);
+  if (h->ev_pf_done) cudaEventDestroy(h->ev_pf_done);
   if (h->ev_fork) cudaEventDestroy(h->ev_fork);
   if (h->ev_join) cudaEventDestroy(h->ev_join);
   if (h->aux) cudaStreamDestroy(h->aux);
@@ -757,6 +904,7 @@ lmoe_status lmoe_stack_forward(lmoe_handle* const* layers, int n_layers, const u
   // while the previous layer finishes), and each prefetching the next layer's
   // router rows and W_in tiles into L2 during its own tail.
   bool fused_all = T <= kMaxDecodeT && c0.lora_rank == 0;
+  for (int l = 0; fused_all && l < n_layers; ++l) fused_all = !layers[l]->staged;
   for (int l = 0; fused_all && l < n_layers; ++l) {
     DecodeArgs A = base_args(layers[l], ws);
     A.T = T;
@@ -792,9 +940,22 @@ lmoe_status lmoe_stack_forward(lmoe_handle* const* layers, int n_layers, const u
     return LMOE_OK;
   }
   for (int l = 0; l < n_layers; ++l) {
+    // staged experts: the next layer's prerouter on the second stream, given
+    // this layer's input, while this layer runs
+    lmoe_handle* nx = l + 1 < n_layers ? layers[l + 1] : nullptr;
+    const bool pf = nx && nx->staged && T <= kMaxDecodeT && !use_prefill(nx, T);
+    if (pf) {
+      if (cudaEventRecord(nx->ev_pf_in, st) != cudaSuccess || cudaStreamWaitEvent(nx->aux, nx->ev_pf_in, 0) != cudaSuccess)
+        return LMOE_ERR_CUDA;
+      lmoe_status ps = prefetch_on(nx, xin, T, nx->aux);
+      if (ps != LMOE_OK) return ps;
+      if (cudaEventRecord(nx->ev_pf_done, nx->aux) != cudaSuccess) return LMOE_ERR_CUDA;
+    }
     lmoe_status s = lmoe_layer_forward(layers[l], xin, T, nullptr, ybuf, ws, stream);
     if (s != LMOE_OK) return s;
     uint16_t* xout = l == n_layers - 1 ? y : xbuf;
+    // (the prerouter reads xin, which the residual add may overwrite)
+    if (pf && cudaStreamWaitEvent(st, nx->ev_pf_done, 0) != cudaSuccess) return LMOE_ERR_CUDA;
     if (launch_residual_add(xin, ybuf, n, xout, st) != cudaSuccess) return LMOE_ERR_CUDA;
     xin = xout;
   }
@@ -864,10 +1025,14 @@ const char* lmoe_stage_name(const lmoe_handle* h, int T, int i, int* count) {
   probe.T = T < kMaxDecodeT ? T : kMaxDecodeT;
   if (T >= 1 && use_fused(h, probe)) {
     static const char* fl[] = {"lora_in", "decode_fused", "lora_q", "lora_out"};
-    const int passes = (T + kMaxDecodeT - 1) / kMaxDecodeT, per = lora ? 4 : 1;
+    static const char* stg[] = {"route", "stage_plan", "stage_copy"};
+    const int ns = h->staged ? 3 : 0;
+    const int passes = (T + kMaxDecodeT - 1) / kMaxDecodeT, per = ns + (lora ? 4 : 1);
     if (count) *count = per * passes;
     if (i < 0 || i >= per * passes) return "";
-    return lora ? fl[i % per] : "decode_fused";
+    const int j = i % per;
+    if (j < ns) return stg[j];
+    return lora ? fl[j - ns] : "decode_fused";
   }
   const int per = lora ? 7 : 5;
   const int passes = (T + kMaxDecodeT - 1) / kMaxDecodeT;
@@ -882,6 +1047,30 @@ int lmoe_launch_count(const lmoe_handle* h, int T) {
   int n = 0;
   lmoe_stage_name(h, T, 0, &n);  // decode: one kernel per stage
   return n;
+}
+
+lmoe_status lmoe_prefetch_experts(lmoe_handle* h, const uint16_t* x, int T, lmoe_stream stream) {
+  if (check_handle(h) != LMOE_OK || !h->staged || T < 1 || T > kMaxDecodeT || !x) return LMOE_ERR_INVALID_ARG;
+  if (!aligned16(x)) return LMOE_ERR_ALIGNMENT;
+  lmoe_status s = pending_error();
+  if (s != LMOE_OK) return s;
+  DeviceGuard guard(h->device);
+  return prefetch_on(h, x, T, (cudaStream_t)stream);
+}
+
+lmoe_status lmoe_get_stage_stats(lmoe_handle* h, lmoe_stage_stats* out) {
+  if (check_handle(h) != LMOE_OK || !h->staged || !out) return LMOE_ERR_INVALID_ARG;
+  DeviceGuard guard(h->device);
+  StageState st;
+  if (cudaDeviceSynchronize() != cudaSuccess || cudaMemcpy(&st, h->d_stage, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  out->passes = st.passes;
+  out->routed = st.routed;
+  out->hits = st.hits;
+  out->staged_on_demand = st.on_demand;
+  out->prefetched = st.prefetched;
+  out->bytes_copied = st.bytes;
+  return LMOE_OK;
 }
 
 }  // extern "C"

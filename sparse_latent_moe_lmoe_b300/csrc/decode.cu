@@ -17,6 +17,7 @@
 //             last CTA to finish each row block (a ticket, no waiting)
 #include "common.cuh"
 #include "decode.cuh"
+#include "topk.cuh"
 
 namespace lmoe {
 
@@ -255,6 +256,7 @@ __global__ void __launch_bounds__(ROUTE_WARPS * 32) route_kernel(DecodeArgs A, i
   }
   // the last CTA to finish does top-k (+ permutation)
   __shared__ int s_last;
+  __shared__ uint2 s_scr[ROUTE_WARPS * 32];  // top-k candidates, per warp
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -267,8 +269,24 @@ __global__ void __launch_bounds__(ROUTE_WARPS * 32) route_kernel(DecodeArgs A, i
   __threadfence();
   int32_t* s_idx = reinterpret_cast<int32_t*>(smem_raw);        // [T*k] (reuses the x area)
   int* s_cnt = reinterpret_cast<int*>(smem_raw + 16 * 16 * 4);  // [E+1]
-  if (warp < T) warp_topk(logits_out + (size_t)warp * E, E, A.k, A.idx + warp * A.k, A.w + warp * A.k,
-                          s_idx + warp * A.k, A.err);
+  if (warp < T) {
+    if (E <= 512) {  // the threshold selector (topk.cuh): a few dependent steps per token instead of k rounds
+      const float* row = logits_out + (size_t)warp * E;
+      bool bad = false;
+      for (int e = lane; e < E; e += 32) bad |= __ldcg(row + e) != __ldcg(row + e);
+      if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(A.err, ERRBIT_BAD_DATA);
+      const float2 sw = topk_warp_thr(row, E, A.k, reinterpret_cast<uint2*>(s_scr) + warp * 32);
+      if (lane < A.k) {
+        const int e = __float_as_int(sw.x);
+        A.idx[warp * A.k + lane] = e;
+        A.w[warp * A.k + lane] = sw.y;
+        s_idx[warp * A.k + lane] = e;
+      }
+    } else {
+      warp_topk(logits_out + (size_t)warp * E, E, A.k, A.idx + warp * A.k, A.w + warp * A.k, s_idx + warp * A.k,
+                A.err);
+    }
+  }
   __syncthreads();
   if (do_perm) block_permute(s_idx, T, E, A.G, A.k, s_cnt, A.pm, A.err);
 }

@@ -88,7 +88,33 @@ struct DecodePack {
 size_t decode_pack_bytes(int d, int E, int G, int L, int f);
 // fills `pk` (win/unit/wout carved from `buf`, decode_pack_bytes long) from
 // the layer's weights; wr is taken from A.W_r
-cudaError_t launch_decode_pack(const DecodeArgs& A, uint8_t* buf, DecodePack* pk, cudaStream_t st);
+cudaError_t launch_decode_pack(const DecodeArgs& A, uint8_t* buf, DecodePack* pk, cudaStream_t st,
+                               uint8_t* unit_buf = nullptr);
+// bytes of one expert's unit chunks (its f/32 units of gate, up and Down)
+size_t decode_expert_bytes(int L, int f);
+// decode_pack_bytes without the unit region (staged handles keep it elsewhere)
+size_t decode_pack_bytes_shared(int d, int E, int G, int L, int f);
+
+// The staged expert cache (staging.cu): device state of a handle's slots.
+struct StageState {
+  unsigned clock;   // the slot the next sweep for victims starts at
+  unsigned n_copy;  // experts the last plan assigned to slots (read by the copy kernel)
+  unsigned long long passes, routed, hits, on_demand, prefetched, bytes;
+};
+struct StagePlan {
+  const int32_t* idx;  // the set to stage: n expert indices (repeats allowed)
+  int n, E, S;
+  int must;            // 1: a forward pass's routed set (counted as such); 0: a prefetch
+  int32_t* slot_of;    // [E] slot of each expert or -1
+  int32_t* expert_in;  // [S] expert in each slot or -1
+  StageState* st;
+  int2* copies;        // [256] (expert, slot) of the plan
+  size_t expert_bytes; // one expert in the decode pass's layout (a multiple of 16)
+  unsigned* err;
+};
+cudaError_t launch_stage_plan(const StagePlan& P, cudaStream_t st);
+// lib: the device address of the host library
+cudaError_t launch_stage_copy(const StagePlan& P, const uint8_t* lib, uint8_t* slots, int num_sms, cudaStream_t st);
 
 // The single-kernel decode pass (decode_fused.cu).
 struct FusedArgs {
@@ -118,6 +144,9 @@ struct FusedArgs {
   const float* hl;
   float* zlin;
   int no_combine;
+  // staged experts: the unit chunks of expert e are read from slot
+  // slot_of[e] of pk.unit (null: from expert e's own place)
+  const int32_t* slot_of;
   // diagnosis: [0] where the first timed-out wait of a launch gave up, then
   // per CTA 32 %globaltimer stamps of its phases (a region of the workspace)
   unsigned long long* diag;

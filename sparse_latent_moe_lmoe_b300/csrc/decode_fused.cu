@@ -97,6 +97,7 @@ struct Tables {
   float w[16 * 16];
   unsigned emask[16];        // bit e: expert e is routed by some token (E <= 512)
   int16_t elist[512];        // routed experts, ascending
+  int16_t eslot[512];        // staged experts: the slot of each routed expert
   int16_t glist[64];         // routed groups, ascending
   int16_t gslot0[65];        // first expert slot of each routed group
   int16_t gplo[64], gpn[64], gpbase[64];  // Z partials of each routed group: first CTA, count, first slot
@@ -575,8 +576,8 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
         if (j == jB + 3 * npre && npre < nu) {
 #pragma unroll 1
           for (int q = npre; q < nu; ++q) {
-            const int u = u_lo + q;
-            bulk_prefetch_l2(F.pk.unit + ((size_t)tb.elist[u / NSF] * NSF + u % NSF) * 3 * CH, 3 * CH);
+            const int u = u_lo + q, ue = F.slot_of ? tb.eslot[u / NSF] : tb.elist[u / NSF];
+            bulk_prefetch_l2(F.pk.unit + ((size_t)ue * NSF + u % NSF) * 3 * CH, 3 * CH);
           }
         }
         if (j == jD && j >= jB) {
@@ -603,8 +604,8 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
           src = F.pk.win + ((size_t)t_lo * NPW + (j - ne)) * WCH;
           bytes = WCH;
         } else if (j < jD) {
-          const int u = u_lo + (j - jB) / 3;
-          src = F.pk.unit + (((size_t)tb.elist[u / NSF] * NSF + u % NSF) * 3 + (j - jB) % 3) * CH;
+          const int u = u_lo + (j - jB) / 3, ue = F.slot_of ? tb.eslot[u / NSF] : tb.elist[u / NSF];
+          src = F.pk.unit + (((size_t)ue * NSF + u % NSF) * 3 + (j - jB) % 3) * CH;
         } else {
           const int it = o_lo + (j - jD);
           src = F.pk.wout + ((size_t)tb.glist[it / (d / 32)] * (d / 32) + it % (d / 32)) * CH;
@@ -792,6 +793,11 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
     if (trace && ctid == 0) trace[11] = gtime();
     if (warp == 0) {
       build_tables(tb, epg);
+      if (F.slot_of) {  // staged experts: where each routed expert's chunks are
+#pragma unroll 1
+        for (int i = lane; i < tb.n_act; i += 32) tb.eslot[i] = (int16_t)__ldcg(F.slot_of + tb.elist[i]);
+        __syncwarp();
+      }
       if (trace && lane == 0) trace[16] = gtime();
       plan(tb, c, nC, NSF, L, d);
       if (lane == 0) mbar_arrive(&tb.tbar);  // the producer may stream the expert weights
@@ -1201,25 +1207,29 @@ size_t al256(size_t v) { return (v + 255) & ~(size_t)255; }
 struct PackLayout {
   size_t win, unit, wout, end;
 };
-PackLayout pack_layout(int d, int E, int G, int L, int f) {
+PackLayout pack_layout(int d, int E, int G, int L, int f, bool with_unit = true) {
   const int PW = d < 2048 ? d : 2048;
   PackLayout p;
   p.win = 0;
   p.unit = al256(p.win + (size_t)G * (L / 16) * (d / PW) * 9 * PW);
-  p.wout = al256(p.unit + (size_t)E * (f / FS) * 3 * 18 * L);
+  p.wout = al256(p.unit + (with_unit ? (size_t)E * (f / FS) * 3 * 18 * L : 0));
   p.end = al256(p.wout + (size_t)G * (d / 32) * 18 * L);
   return p;
 }
 }  // namespace
 
 size_t decode_pack_bytes(int d, int E, int G, int L, int f) { return pack_layout(d, E, G, L, f).end; }
+size_t decode_pack_bytes_shared(int d, int E, int G, int L, int f) { return pack_layout(d, E, G, L, f, false).end; }
+size_t decode_expert_bytes(int L, int f) { return (size_t)(f / FS) * 3 * 18 * L; }
 
-cudaError_t launch_decode_pack(const DecodeArgs& A, uint8_t* buf, DecodePack* pk, cudaStream_t st) {
+cudaError_t launch_decode_pack(const DecodeArgs& A, uint8_t* buf, DecodePack* pk, cudaStream_t st,
+                               uint8_t* unit_buf) {
   const int d = A.d, E = A.E, G = A.G, L = A.L, f = A.f, PW = d < 2048 ? d : 2048, nsf = f / FS;
-  const PackLayout lay = pack_layout(d, E, G, L, f);
+  const PackLayout lay = pack_layout(d, E, G, L, f, unit_buf == nullptr);
+  uint8_t* units = unit_buf ? unit_buf : buf + lay.unit;
   pk->wr = A.W_r;
   pk->win = buf + lay.win;
-  pk->unit = buf + lay.unit;
+  pk->unit = units;
   pk->wout = buf + lay.wout;
   // W_in: 16-row tiles in pieces of PW columns
   const int fp4 = A.wfmt != 0;  // (the scales move as 16-bit words in both formats: one bf16 or two E4M3 per 32)
@@ -1227,7 +1237,7 @@ cudaError_t launch_decode_pack(const DecodeArgs& A, uint8_t* buf, DecodePack* pk
              (size_t)9 * PW, 0, fp4};
   pack_swz_kernel<<<G * (L / 16) * (d / PW), 256, 0, st>>>(w);
   // gate and up: 32 rows (one f-slice of one expert) each, at parts 0 and 1 of the unit
-  PackSpec g{A.gate_q, (size_t)L / 2, A.gate_s, (size_t)L / 32, FS, L / 2, L / 32, 1, buf + lay.unit,
+  PackSpec g{A.gate_q, (size_t)L / 2, A.gate_s, (size_t)L / 32, FS, L / 2, L / 32, 1, units,
              (size_t)3 * 18 * L, 0, fp4};
   pack_swz_kernel<<<E * nsf, 256, 0, st>>>(g);
   PackSpec u = g;
@@ -1235,7 +1245,7 @@ cudaError_t launch_decode_pack(const DecodeArgs& A, uint8_t* buf, DecodePack* pk
   u.s = A.up_s;
   u.coff = (size_t)18 * L;
   pack_swz_kernel<<<E * nsf, 256, 0, st>>>(u);
-  pack_down_kernel<<<E * nsf, 256, 0, st>>>(A.down_q, A.down_s, L, f, buf + lay.unit, fp4);
+  pack_down_kernel<<<E * nsf, 256, 0, st>>>(A.down_q, A.down_s, L, f, units, fp4);
   // W_out: 32-row blocks
   PackSpec o{A.W_out_q, (size_t)L / 2, A.W_out_s, (size_t)L / 32, 32, L / 2, L / 32, 1, buf + lay.wout,
              (size_t)18 * L, 0, fp4};

@@ -27,6 +27,15 @@ def to_device(a, device) -> torch.Tensor:
     return torch.from_numpy(a).to(device).contiguous()
 
 
+def to_pinned(a):
+    """A numpy array (or tensor) as page-locked host memory the device can address."""
+    if a is None:
+        return None
+    t = a if isinstance(a, torch.Tensor) else torch.from_numpy(
+        np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16 else np.ascontiguousarray(a))
+    return t.cpu().contiguous().pin_memory()
+
+
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
@@ -46,14 +55,18 @@ class LatentMoE:
     """
 
     def __init__(self, shape, weights: dict, device: int = 0, force_path: int = capi.PATH_AUTO,
-                 decode_max_T: int = 0, timeout_cycles: int = 0, flags: int = 0):
+                 decode_max_T: int = 0, timeout_cycles: int = 0, flags: int = 0, expert_slots: int = 0,
+                 expert_weights_on_host: bool = False):
         self.shape = shape
         self.device = torch.device("cuda", device)
-        self.dev_weights = {n: to_device(weights.get(n), self.device) for n in capi.WEIGHT_FIELDS}
+        # staged experts may keep gate / up / Down in page-locked host memory
+        host = ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s") if expert_weights_on_host else ()
+        self.dev_weights = {n: (to_pinned(weights.get(n)) if n in host else to_device(weights.get(n), self.device))
+                            for n in capi.WEIGHT_FIELDS}
         nvfp4 = getattr(shape, "wfmt", "int4") == "nvfp4"
         self.cfg = LmoeConfig(shape.d, shape.E, shape.G, shape.k, shape.L, shape.f, 16 if nvfp4 else 32,
                               shape.lora_rank, 1 if shape.has_bias else 0, flags, timeout_cycles, decode_max_T,
-                              force_path, capi.WEIGHTS_NVFP4 if nvfp4 else capi.WEIGHTS_INT4)
+                              force_path, capi.WEIGHTS_NVFP4 if nvfp4 else capi.WEIGHTS_INT4, expert_slots)
         self.wts = LmoeWeights(*[None if t is None else t.data_ptr() for t in
                                  (self.dev_weights[n] for n in capi.WEIGHT_FIELDS)])
         self.h = capi.lmoe_create(self.cfg, self.wts, device)
@@ -130,6 +143,14 @@ class LatentMoE:
         capi.lmoe_layer_forward(self.h, _ptr(x), T, _ptr(residual), _ptr(y), _ptr(self.workspace(T)),
                                 _stream(stream))
         return y
+
+    def prefetch_experts(self, x: torch.Tensor, stream=None):
+        """Staged experts: the prerouter stages this layer's predicted experts
+        for the tokens x (lmoe_prefetch_experts)."""
+        capi.lmoe_prefetch_experts(self.h, _ptr(x), x.shape[0], _stream(stream))
+
+    def stage_stats(self) -> dict:
+        return capi.lmoe_get_stage_stats(self.h)
 
     def last_decode_routing(self, T: int, stream=None):
         """(idx, w, logits) that the last decode-path forward of T <= 16 tokens
