@@ -151,14 +151,15 @@ def stage_bytes(sh, T, idx):
     b["wout"] = len(groups) * sh.d * sh.L * wq + 2 * T * sh.d
     b["decode_fused"] = sum(b.values())
     if sh.lora_rank:
-        # the LoRA matrices of the routed groups; in the single-kernel pass the
-        # branch runs in its own kernels (lora_in: A_in, B_in; lora_q: A_out;
-        # lora_out: B_out), in the multi-kernel sequence beside W_in / W_out
+        # the LoRA matrices of the routed groups; around the single-kernel pass
+        # the branch runs in its own kernels (lora_p: A_in, lora_hl: B_in,
+        # lora_q: A_out, lora_out: B_out), in the multi-kernel sequence
+        # lora_p / lora_q and the B matrices beside W_in / W_out
         r = sh.lora_rank
-        b["lora_in"] = len(groups) * (sh.d * r + r * sh.L) * 2 + 2 * T * sh.d
+        b["lora_p"] = len(groups) * sh.d * r * 2
+        b["lora_hl"] = len(groups) * r * sh.L * 2
         b["lora_q"] = len(groups) * sh.L * r * 2
         b["lora_out"] = len(groups) * r * sh.d * 2 + 2 * T * sh.d
-        b["lora_p"] = len(groups) * sh.d * r * 2
         b["win_lora"] = len(groups) * r * sh.L * 2
         b["wout_lora"] = len(groups) * r * sh.d * 2
     return b
@@ -168,8 +169,8 @@ def step_bytes(sb):
     """Algorithmic bytes of one pass from stage_bytes: the layer's own stages
     plus, with LoRA, the branch's matrices counted once."""
     base = sum(sb[n] for n in ("route", "win", "gateup", "down", "wout"))
-    if "lora_in" in sb:
-        base += sb["lora_p"] + sb["win_lora"] + sb["lora_q"] + sb["wout_lora"]
+    if "lora_hl" in sb:
+        base += sb["lora_p"] + sb["lora_hl"] + sb["lora_q"] + sb["wout_lora"]
     return base
 
 

@@ -127,13 +127,14 @@ struct TicketMap {
 };
 TicketMap ticket_map(const lmoe_config& c) {
   TicketMap t;
-  t.total = 1 + (size_t)(c.d + 63) / 64 + 64;
+  t.total = 1 + (size_t)(c.d + 63) / 64 + lora_ticket_words(c.d, c.G);
   return t;
 }
 
 // ----------------------------------------------------------- workspace map
 struct DecodeWs {
-  size_t logits, idx, w, eo, sa, inv, go, gto, gt, ar, Hp, V, Z, Yp, Pin, Qout, Hf, Zf, Zpart, diag, perm_scratch, end;
+  size_t logits, idx, w, eo, sa, inv, go, gto, gt, ar, Hp, V, Z, Yp, Pin, Qout, Hf, Zf, Zpart, diag, perm_scratch, Lpart,
+      end;
 };
 
 // grid: CTAs of the single-kernel decode pass (sizes its Z partials)
@@ -169,6 +170,9 @@ DecodeWs decode_ws(const lmoe_config& c, int T, int grid) {
   m.Zpart = take(fused_zpart_bytes(c.G, c.L, grid > 0 ? grid : 1));
   m.diag = take(fused_diag_bytes(grid > 0 ? grid : 1));
   m.perm_scratch = take(permute_scratch_bytes(T > n ? T : n, c.E, c.G));
+  // the LoRA branch's partial sums around the single-kernel pass
+  m.Lpart = take(c.lora_rank > 0 ? lora_ppart_bytes(c.d, c.G, c.lora_rank) + lora_qpart_bytes(c.L, c.G, c.lora_rank)
+                                 : 0);
   m.end = o;
   return m;
 }
@@ -293,6 +297,16 @@ FusedArgs fused_args(const lmoe_handle* h, const DecodeArgs& A, void* ws) {
 // decode path for any T, in passes of <= 16 tokens
 StagePlan stage_plan(const lmoe_handle* h, const int32_t* idx, int n, int must, int2* copies);
 
+// the LoRA branch's tickets (after the multi-kernel path's) and partial sums
+unsigned* lora_tickets(const lmoe_handle* h) { return h->d_tickets + 1 + (h->cfg.d + 63) / 64; }
+float* lora_ppart(const lmoe_handle* h, void* ws) {
+  return reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + decode_ws(h->cfg, 0, h->num_sms).Lpart);
+}
+float* lora_qpart(const lmoe_handle* h, void* ws) {
+  return reinterpret_cast<float*>(reinterpret_cast<char*>(lora_ppart(h, ws)) +
+                                  lora_ppart_bytes(h->cfg.d, h->cfg.G, h->cfg.lora_rank));
+}
+
 lmoe_status decode_layer(lmoe_handle* h, const uint16_t* x, int T, const uint16_t* residual, uint16_t* y, void* ws,
                          cudaStream_t st) {
   const lmoe_config& c = h->cfg;
@@ -325,13 +339,11 @@ lmoe_status decode_layer(lmoe_handle* h, const uint16_t* x, int T, const uint16_
       }
       if (A.r > 0) {  // the LoRA branch: lora_in before, lora_q and lora_out after
         // scratch of the multi-kernel sequence, unused by the single kernel:
-        // Ppart in Hp, P in Pin, Hl in V, Z in fp32 in Z, Q in Qout
+        // P in Pin, Hl in V, Z in fp32 in Z, Q in Qout; the partials in Lpart
         F.hl = A.V;
         F.zlin = A.Z;
         F.no_combine = 1;
-        hook.before(st);
-        e = launch_lora_in(A, A.Hp, A.Pin, A.V, h->d_tickets + 1 + (c.d + 63) / 64, st);
-        hook.after(st);
+        e = launch_lora_in(A, lora_ppart(h, ws), A.Pin, A.V, lora_tickets(h), st, &hook);
         if (e != cudaSuccess) return LMOE_ERR_CUDA;
       }
       hook.before(st);
@@ -340,11 +352,11 @@ lmoe_status decode_layer(lmoe_handle* h, const uint16_t* x, int T, const uint16_
       if (e != cudaSuccess) return LMOE_ERR_CUDA;
       if (A.r > 0) {
         hook.before(st);
-        e = launch_lora_q(A, A.Z, A.Qout, st);
+        e = launch_lora_q(A, A.Z, lora_qpart(h, ws), A.Qout, lora_tickets(h), st);
         hook.after(st);
         if (e != cudaSuccess) return LMOE_ERR_CUDA;
         hook.before(st);
-        e = launch_lora_out(A, F.Yp, A.Qout, st);
+        e = launch_lora_out(A, F.Yp, A.Qout, lora_tickets(h), st);
         hook.after(st);
         if (e != cudaSuccess) return LMOE_ERR_CUDA;
       }
@@ -1024,10 +1036,10 @@ const char* lmoe_stage_name(const lmoe_handle* h, int T, int i, int* count) {
   DecodeArgs probe = base_args(h, nullptr);
   probe.T = T < kMaxDecodeT ? T : kMaxDecodeT;
   if (T >= 1 && use_fused(h, probe)) {
-    static const char* fl[] = {"lora_in", "decode_fused", "lora_q", "lora_out"};
+    static const char* fl[] = {"lora_p", "lora_hl", "decode_fused", "lora_q", "lora_out"};
     static const char* stg[] = {"route", "stage_plan", "stage_copy"};
     const int ns = h->staged ? 3 : 0;
-    const int passes = (T + kMaxDecodeT - 1) / kMaxDecodeT, per = ns + (lora ? 4 : 1);
+    const int passes = (T + kMaxDecodeT - 1) / kMaxDecodeT, per = ns + (lora ? 5 : 1);
     if (count) *count = per * passes;
     if (i < 0 || i >= per * passes) return "";
     const int j = i % per;

@@ -177,9 +177,17 @@ cudaError_t launch_experts(const DecodeArgs& A, int mode, cudaStream_t st, Stage
 // The Recover-LoRA branch around the single-kernel decode pass (lora.cu).
 cudaError_t lora_set_attributes();
 bool lora_fused_supported(const DecodeArgs& A);
-cudaError_t launch_lora_in(const DecodeArgs& A, float* Ppart, float* P, float* Hl, unsigned* tickets, cudaStream_t st);
-cudaError_t launch_lora_q(const DecodeArgs& A, const float* Zlin, float* Q, cudaStream_t st);
-cudaError_t launch_lora_out(const DecodeArgs& A, const float* Yp, const float* Q, cudaStream_t st);
+// tickets: lora_ticket_words(d, G) words, zero between calls
+size_t lora_ticket_words(int d, int G);
+// scratch of the partial sums: Ppart [G][d/256][16][r], Qpart [G][L/256][16][r]
+inline size_t lora_ppart_bytes(int d, int G, int r) { return (size_t)G * (d / 256) * 16 * r * 4; }
+inline size_t lora_qpart_bytes(int L, int G, int r) { return (size_t)G * (L / 256) * 16 * r * 4; }
+// lora_p then lora_hl (two kernels; the hook brackets each)
+cudaError_t launch_lora_in(const DecodeArgs& A, float* Ppart, float* P, float* Hl, unsigned* tickets,
+                           cudaStream_t st, StageHook* hook);
+cudaError_t launch_lora_q(const DecodeArgs& A, const float* Zlin, float* Qpart, float* Q, unsigned* tickets,
+                          cudaStream_t st);
+cudaError_t launch_lora_out(const DecodeArgs& A, float* Yp, const float* Q, unsigned* tickets, cudaStream_t st);
 cudaError_t launch_residual_add(const uint16_t* x, const uint16_t* y, size_t n, uint16_t* out, cudaStream_t st);
 cudaError_t launch_combine(const float* Y, const int32_t* idx, const int32_t* assign_row, int T, int d, int k,
                            int epg, const uint16_t* residual, uint16_t* y, cudaStream_t st);

@@ -4,181 +4,289 @@
 // beside the frozen 4-bit base). Per group g, with rank r:
 //   h  += B_in[g]^T (A_in[g]^T x)      added to H before the expert SwiGLU
 //   o  += B_out[g]^T (A_out[g]^T z)    added to the group's W_out output
-// The expert work stays in the single kernel; three small kernels surround it:
-//   lora_in   P = A_in^T x in row blocks of A_in (partial sums per block); the
-//             last block of a group sums them in block order and writes
-//             Hl[g][t] = B_in^T P, which the single kernel adds to H
-//   lora_q    Q[g][t] = A_out[g]^T Z[g][t], Z as the single kernel wrote it
-//             (fp32), for every routed group
-//   lora_out  y_t = sum over routed groups in ascending order of
-//             (Y[g][t] + B_out[g]^T Q[g][t]) (+ residual), rounded once
+// The expert work stays in the single kernel; four small kernels surround it:
+//   lora_p    P = A_in^T x: CTA (g, block of 256 rows of A_in) -> a partial;
+//             the last CTA of a group sums the partials in block order
+//   lora_hl   Hl[g][t] = B_in^T P[g][t] for a block of 128 latent columns,
+//             which the single kernel adds to H
+//   lora_q    Q[g][t] = A_out[g]^T Z[g][t] from the single kernel's fp32 Z,
+//             like lora_p, for the routed groups
+//   lora_out  Y[g] += B_out[g]^T Q[g] for (block of 256 output rows, group);
+//             the last group of a row block writes y_t = sum over the routed
+//             groups in ascending order (+ residual), rounded once
+// Each streams its bf16 matrix in whole rows (a warp reads 128 contiguous
+// bytes per load, eight loads in flight per lane) and reduces in a fixed order.
 #include "common.cuh"
 #include "decode.cuh"
 
 namespace lmoe {
 
 namespace {
-constexpr int LI_ROWS = 256;  // rows of A_in per lora_in block
-constexpr int LQ_COLS = 8;    // columns of Q per lora_q block
-constexpr int LO_ROWS = 32;   // output rows per lora_out block
-}  // namespace
+constexpr int LP_ROWS = 256;   // rows of A_in / A_out per lora_p / lora_q CTA (8 warps x 32)
+constexpr int LH_COLS = 128;   // latent columns per lora_hl CTA
+constexpr int LO_ROWS = 256;   // output rows per lora_out CTA
+constexpr int MAXR = 128;
 
-// grid (G, d / LI_ROWS), 256 threads. Ppart [G][d/LI_ROWS][16][r], P [G][16][r],
-// Hl [G][16][L]; tickets[g] zero between calls.
-__global__ void __launch_bounds__(256) lora_in_kernel(DecodeArgs A, float* __restrict__ Ppart, float* __restrict__ P,
-                                                      float* __restrict__ Hl, unsigned* __restrict__ tickets) {
-  extern __shared__ __align__(16) unsigned char lsm[];
-  const int g = blockIdx.x, kb = blockIdx.y, nkb = gridDim.y, T = A.T, r = A.r, d = A.d, L = A.L;
-  const int tid = threadIdx.x;
-  float* xs = reinterpret_cast<float*>(lsm);           // [16][LI_ROWS]
-  float* as = xs + 16 * LI_ROWS;                         // [LI_ROWS][r]
-  const int k0 = kb * LI_ROWS;
-  for (int i = tid; i < 16 * LI_ROWS; i += 256) {
-    const int t = i / LI_ROWS, kk = i % LI_ROWS;
-    xs[i] = t < T ? bf16_to_f32(A.x[(size_t)t * d + k0 + kk]) : 0.f;
-  }
-  const uint16_t* Ain = A.A_in + ((size_t)g * d + k0) * r;
-  for (int i = tid; i < LI_ROWS * r; i += 256) as[i] = bf16_to_f32(Ain[i]);
-  __syncthreads();
-  // thread -> (token t, column j) pairs; sums over the block's rows in order
-  for (int o = tid; o < 16 * r; o += 256) {
-    const int t = o / r, j = o % r;
-    float s = 0.f;
-    if (t < T)
-      for (int kk = 0; kk < LI_ROWS; ++kk) s = fmaf(xs[t * LI_ROWS + kk], as[kk * r + j], s);
-    Ppart[(((size_t)g * nkb + kb) * 16 + t) * r + j] = s;
-  }
-  __threadfence();
-  __syncthreads();
-  __shared__ int last;
-  if (tid == 0) {
-    last = atomicAdd(&tickets[g], 1u) == (unsigned)(nkb - 1);
-    if (last) tickets[g] = 0;
-  }
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  // P = sum of the blocks in order, then Hl = B_in^T P
-  float* ps = xs;  // [16][r]
-  for (int o = tid; o < 16 * r; o += 256) {
-    const int t = o / r, j = o % r;
-    float s = 0.f;
-    for (int b = 0; b < nkb; ++b) s += __ldcg(Ppart + (((size_t)g * nkb + b) * 16 + t) * r + j);
-    ps[o] = s;
-    P[((size_t)g * 16 + t) * r + j] = s;
-  }
-  __syncthreads();
-  const uint16_t* Bin = A.B_in + (size_t)g * r * L;
-  for (int l = tid; l < L; l += 256) {
-    float acc[16];
-#pragma unroll
-    for (int t = 0; t < 16; ++t) acc[t] = 0.f;
-    for (int j = 0; j < r; ++j) {
-      const float b = bf16_to_f32(Bin[(size_t)j * L + l]);
-#pragma unroll
-      for (int t = 0; t < 16; ++t) acc[t] = fmaf(b, ps[t * r + j], acc[t]);
-    }
-#pragma unroll
-    for (int t = 0; t < 16; ++t)
-      if (t < T) Hl[((size_t)g * 16 + t) * L + l] = acc[t];
-  }
-}
-
-// bit g: some token routes into group g
+// bit g: some token routes into group g (every thread of the CTA; the CTA's
+// threads load the routing once between them)
 LMOE_DEV unsigned long long routed_groups(const DecodeArgs& A) {
-  unsigned long long m = 0;
-  for (int a = 0; a < A.T * A.k; ++a) m |= 1ull << (A.idx[a] / A.epg);
+  __shared__ unsigned long long m;
+  if (threadIdx.x == 0) m = 0ull;
+  __syncthreads();
+  for (int a = threadIdx.x; a < A.T * A.k; a += blockDim.x) atomicOr(&m, 1ull << (__ldg(A.idx + a) / A.epg));
+  __syncthreads();
   return m;
 }
 
-// grid (G, r / LQ_COLS), 256 threads. Zlin [G][16][L] (written for routed
-// groups), Q [G][16][r].
-__global__ void __launch_bounds__(256) lora_q_kernel(DecodeArgs A, const float* __restrict__ Zlin, float* __restrict__ Q) {
-  __shared__ float red[8][16][LQ_COLS];
-  const int g = blockIdx.x, j0 = blockIdx.y * LQ_COLS, T = A.T, r = A.r, L = A.L;
+LMOE_DEV float2 bf16x2(uint32_t u) { return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u)); }
+
+// Partial of act^T M over rows k0 .. k0 + LP_ROWS of M ([K][r] bf16) for 16
+// tokens, act (fp32 in shared memory, [16][LP_ROWS]) -> out [16][r] (fp32,
+// global), the 8 warps summed in order. Lane l of a warp takes columns 2l,
+// 2l + 1 (a 128-byte row per warp load when r = 64); a warp takes 32 rows.
+LMOE_DEV void rows_partial(const uint16_t* __restrict__ M, int r, const float* act, float (*red)[16][MAXR],
+                           float* __restrict__ out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool routed = (routed_groups(A) >> g) & 1ull;
-  // warp w sums rows l = w, w + 8, ...; lane = (token t, column pair)
-  float acc[LQ_COLS / 2] = {};
-  const int t = lane >> 1, jh = (lane & 1) * (LQ_COLS / 2);
-  if (routed && t < T) {
-    const uint16_t* Ao = A.A_out + (size_t)g * L * r;
-    for (int l = warp; l < L; l += 8) {
-      const float z = __ldcg(Zlin + ((size_t)g * 16 + t) * L + l);
+  float acc[16][2];
 #pragma unroll
-      for (int q = 0; q < LQ_COLS / 2; ++q) acc[q] = fmaf(z, bf16_to_f32(Ao[(size_t)l * r + j0 + jh + q]), acc[q]);
+  for (int t = 0; t < 16; ++t) acc[t][0] = acc[t][1] = 0.f;
+  for (int c2 = lane; 2 * c2 < r; c2 += 32) {  // column pairs of this lane (one pass when r <= 64)
+#pragma unroll
+    for (int t = 0; t < 16; ++t) acc[t][0] = acc[t][1] = 0.f;
+#pragma unroll 1
+    for (int i0 = 0; i0 < 32; i0 += 8) {
+      uint32_t w[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) w[u] = __ldg(reinterpret_cast<const uint32_t*>(M + (size_t)(warp * 32 + i0 + u) * r) + c2);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float2 m = bf16x2(w[u]);
+        const int i = warp * 32 + i0 + u;
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const float a = act[t * LP_ROWS + i];
+          acc[t][0] = fmaf(a, m.x, acc[t][0]);
+          acc[t][1] = fmaf(a, m.y, acc[t][1]);
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      red[warp][t][2 * c2] = acc[t][0];
+      red[warp][t][2 * c2 + 1] = acc[t][1];
     }
   }
-#pragma unroll
-  for (int q = 0; q < LQ_COLS / 2; ++q) red[warp][t][jh + q] = acc[q];
   __syncthreads();
-  if (threadIdx.x < 16 * LQ_COLS) {
-    const int tt = threadIdx.x / LQ_COLS, j = threadIdx.x % LQ_COLS;
+  for (int o = threadIdx.x; o < 16 * r; o += blockDim.x) {
+    const int t = o / r, c = o % r;
     float s = 0.f;
-    for (int w = 0; w < 8; ++w) s += red[w][tt][j];
-    if (tt < T) Q[((size_t)g * 16 + tt) * r + j0 + j] = s;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) s += red[w][t][c];
+    out[o] = s;
   }
 }
 
-// grid d / LO_ROWS, 256 threads: thread (token t, row) of the block.
-__global__ void __launch_bounds__(256) lora_out_kernel(DecodeArgs A, const float* __restrict__ Yp,
-                                                       const float* __restrict__ Q) {
-  __shared__ float qs[16][128];
-  const int T = A.T, r = A.r, d = A.d, G = A.G;
-  const int row0 = blockIdx.x * LO_ROWS;
-  const unsigned long long gm = routed_groups(A);
-  float acc[2] = {0.f, 0.f};
-  const int rl = threadIdx.x % LO_ROWS, t0 = threadIdx.x / LO_ROWS;  // tokens t0 and t0 + 8
-  for (int g = 0; g < G; ++g) {
-    if (!((gm >> g) & 1ull)) continue;
-    __syncthreads();
-    for (int i = threadIdx.x; i < 16 * r; i += 256) qs[i / r][i % r] = __ldcg(Q + (size_t)g * 16 * r + i);
-    __syncthreads();
-    const uint16_t* Bo = A.B_out + (size_t)g * r * d + row0 + rl;
+// The last of `n` CTAs to arrive on *ticket (which it resets); all threads learn it.
+LMOE_DEV bool last_arrival(unsigned* ticket, unsigned n) {
+  __shared__ int last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    last = atomicAdd(ticket, 1u) == n - 1;
+    if (last) *ticket = 0;
+  }
+  __syncthreads();
+  if (last) __threadfence();
+  return last;
+}
+}  // namespace
+
+// grid (G, d / LP_ROWS). Ppart [G][d/LP_ROWS][16][r], P [G][16][r].
+__global__ void __launch_bounds__(256) lora_p_kernel(DecodeArgs A, float* __restrict__ Ppart, float* __restrict__ P,
+                                                     unsigned* __restrict__ tickets) {
+  extern __shared__ __align__(16) unsigned char lsm[];
+  float* act = reinterpret_cast<float*>(lsm);                               // [16][LP_ROWS]
+  float (*red)[16][MAXR] = reinterpret_cast<float (*)[16][MAXR]>(act + 16 * LP_ROWS);  // [8][16][r]
+  const int g = blockIdx.x, kb = blockIdx.y, nkb = gridDim.y, T = A.T, r = A.r, d = A.d;
+  const int k0 = kb * LP_ROWS;
+  for (int i = threadIdx.x; i < 16 * LP_ROWS; i += blockDim.x) {
+    const int t = i / LP_ROWS, kk = i % LP_ROWS;
+    act[i] = t < T ? bf16_to_f32(A.x[(size_t)t * d + k0 + kk]) : 0.f;
+  }
+  __syncthreads();
+  rows_partial(A.A_in + ((size_t)g * d + k0) * r, r, act, red, Ppart + ((size_t)g * nkb + kb) * 16 * r);
+  if (!last_arrival(tickets + g, (unsigned)nkb)) return;
+  for (int o = threadIdx.x; o < 16 * r; o += blockDim.x) {
+    float s = 0.f;
+    for (int b = 0; b < nkb; ++b) s += __ldcg(Ppart + ((size_t)g * nkb + b) * 16 * r + o);
+    P[(size_t)g * 16 * r + o] = s;
+  }
+}
+
+// grid (G, L / LH_COLS). Hl [G][16][L] = P[g]^T-contracted with B_in[g] ([r][L]).
+// Thread (column pair cp of the block, quarter q of r); quarters summed in order.
+__global__ void __launch_bounds__(256) lora_hl_kernel(DecodeArgs A, const float* __restrict__ P, float* __restrict__ Hl) {
+  __shared__ float ps[16][MAXR];
+  __shared__ float red[4][16][LH_COLS];
+  const int g = blockIdx.x, l0 = blockIdx.y * LH_COLS, T = A.T, r = A.r, L = A.L;
+  for (int i = threadIdx.x; i < 16 * r; i += blockDim.x) ps[i / r][i % r] = __ldcg(P + (size_t)g * 16 * r + i);
+  __syncthreads();
+  const int cp = threadIdx.x & 63, q = threadIdx.x >> 6, rq = r / 4;
+  const uint16_t* B = A.B_in + (size_t)g * r * L + l0 + 2 * cp;
+  float acc[16][2];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int t = t0 + 8 * h;
-      if (t >= T) continue;
-      float s = __ldcg(Yp + ((size_t)g * 16 + t) * d + row0 + rl);
-      for (int j = 0; j < r; ++j) s = fmaf(bf16_to_f32(Bo[(size_t)j * d]), qs[t][j], s);
-      acc[h] += s;
+  for (int t = 0; t < 16; ++t) acc[t][0] = acc[t][1] = 0.f;
+#pragma unroll 1
+  for (int j0 = q * rq; j0 < (q + 1) * rq; j0 += 8) {
+    uint32_t w[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) w[u] = j0 + u < (q + 1) * rq ? __ldg(reinterpret_cast<const uint32_t*>(B + (size_t)(j0 + u) * L)) : 0u;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (j0 + u >= (q + 1) * rq) break;
+      const float2 b = bf16x2(w[u]);
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        acc[t][0] = fmaf(ps[t][j0 + u], b.x, acc[t][0]);
+        acc[t][1] = fmaf(ps[t][j0 + u], b.y, acc[t][1]);
+      }
     }
   }
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int t = t0 + 8 * h;
-    if (t >= T) continue;
-    float v = acc[h];
-    const size_t o = (size_t)t * d + row0 + rl;
-    if (A.residual) v += bf16_to_f32(A.residual[o]);
-    A.y[o] = f32_to_bf16_rne(v);
+  for (int t = 0; t < 16; ++t) {
+    red[q][t][2 * cp] = acc[t][0];
+    red[q][t][2 * cp + 1] = acc[t][1];
+  }
+  __syncthreads();
+  for (int o = threadIdx.x; o < 16 * LH_COLS; o += blockDim.x) {
+    const int t = o / LH_COLS, c = o % LH_COLS;
+    if (t < T) Hl[((size_t)g * 16 + t) * L + l0 + c] = red[0][t][c] + red[1][t][c] + red[2][t][c] + red[3][t][c];
   }
 }
 
-size_t lora_in_smem(int r) { return (size_t)(16 * LI_ROWS + LI_ROWS * r) * 4; }
+// grid (G, L / LP_ROWS). Zlin [G][16][L] (routed groups), Qpart [G][L/LP_ROWS][16][r], Q [G][16][r].
+__global__ void __launch_bounds__(256) lora_q_kernel(DecodeArgs A, const float* __restrict__ Zlin,
+                                                     float* __restrict__ Qpart, float* __restrict__ Q,
+                                                     unsigned* __restrict__ tickets) {
+  extern __shared__ __align__(16) unsigned char lsm[];
+  float* act = reinterpret_cast<float*>(lsm);
+  float (*red)[16][MAXR] = reinterpret_cast<float (*)[16][MAXR]>(act + 16 * LP_ROWS);
+  const int g = blockIdx.x, kb = blockIdx.y, nkb = gridDim.y, T = A.T, r = A.r, L = A.L;
+  if (!((routed_groups(A) >> g) & 1ull)) return;  // the whole group's CTAs leave together
+  const int k0 = kb * LP_ROWS;
+  for (int i = threadIdx.x; i < 16 * LP_ROWS; i += blockDim.x) {
+    const int t = i / LP_ROWS, kk = i % LP_ROWS;
+    act[i] = t < T ? __ldcg(Zlin + ((size_t)g * 16 + t) * L + k0 + kk) : 0.f;
+  }
+  __syncthreads();
+  rows_partial(A.A_out + ((size_t)g * L + k0) * r, r, act, red, Qpart + ((size_t)g * nkb + kb) * 16 * r);
+  if (!last_arrival(tickets + g, (unsigned)nkb)) return;
+  for (int o = threadIdx.x; o < 16 * r; o += blockDim.x) {
+    float s = 0.f;
+    for (int b = 0; b < nkb; ++b) s += __ldcg(Qpart + ((size_t)g * nkb + b) * 16 * r + o);
+    Q[(size_t)g * 16 * r + o] = s;
+  }
+}
+
+// grid (d / LO_ROWS, G). Y[g][t][i] += sum_c Q[g][t][c] B_out[g][c][i] for the
+// block's rows (routed groups); thread (row pair rp, half h of r), halves summed
+// in order. The last group CTA of a row block sums the routed groups in
+// ascending order, adds the residual and writes y.
+__global__ void __launch_bounds__(256) lora_out_kernel(DecodeArgs A, float* __restrict__ Yp,
+                                                       const float* __restrict__ Q, unsigned* __restrict__ tickets) {
+  __shared__ float qs[16][MAXR];
+  __shared__ float red[2][16][LO_ROWS];
+  const int rb = blockIdx.x, g = blockIdx.y, G = gridDim.y, T = A.T, r = A.r, d = A.d;
+  const int row0 = rb * LO_ROWS;
+  const unsigned long long gm = routed_groups(A);
+  if ((gm >> g) & 1ull) {
+    for (int i = threadIdx.x; i < 16 * r; i += blockDim.x) qs[i / r][i % r] = __ldcg(Q + (size_t)g * 16 * r + i);
+    __syncthreads();
+    const int rp = threadIdx.x & 127, h = threadIdx.x >> 7, rh = r / 2;
+    const uint16_t* B = A.B_out + (size_t)g * r * d + row0 + 2 * rp;
+    float acc[16][2];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) acc[t][0] = acc[t][1] = 0.f;
+#pragma unroll 1
+    for (int j0 = h * rh; j0 < (h + 1) * rh; j0 += 8) {
+      uint32_t w[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) w[u] = j0 + u < (h + 1) * rh ? __ldg(reinterpret_cast<const uint32_t*>(B + (size_t)(j0 + u) * d)) : 0u;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (j0 + u >= (h + 1) * rh) break;
+        const float2 b = bf16x2(w[u]);
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          acc[t][0] = fmaf(qs[t][j0 + u], b.x, acc[t][0]);
+          acc[t][1] = fmaf(qs[t][j0 + u], b.y, acc[t][1]);
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      red[h][t][2 * rp] = acc[t][0];
+      red[h][t][2 * rp + 1] = acc[t][1];
+    }
+    __syncthreads();
+    for (int o = threadIdx.x; o < 16 * LO_ROWS; o += blockDim.x) {
+      const int t = o / LO_ROWS, c = o % LO_ROWS;
+      if (t < T) {
+        float* yp = Yp + ((size_t)g * 16 + t) * d + row0 + c;
+        *yp = __ldcg(yp) + (red[0][t][c] + red[1][t][c]);
+      }
+    }
+  }
+  if (!last_arrival(tickets + rb, (unsigned)G)) return;
+  for (int o = threadIdx.x; o < T * LO_ROWS; o += blockDim.x) {
+    const int t = o / LO_ROWS, i = row0 + o % LO_ROWS;
+    float v = 0.f;
+    for (int gg = 0; gg < G; ++gg)
+      if ((gm >> gg) & 1ull) v += __ldcg(Yp + ((size_t)gg * 16 + t) * d + i);
+    const size_t oi = (size_t)t * d + i;
+    if (A.residual) v += bf16_to_f32(A.residual[oi]);
+    A.y[oi] = f32_to_bf16_rne(v);
+  }
+}
+
+size_t lora_rows_smem() { return (size_t)(16 * LP_ROWS + 8 * 16 * MAXR) * 4; }
 
 cudaError_t lora_set_attributes() {
-  cudaFuncSetAttribute(lora_in_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lora_in_smem(128));
+  cudaFuncSetAttribute(lora_p_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lora_rows_smem());
+  cudaFuncSetAttribute(lora_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lora_rows_smem());
   return cudaGetLastError();
 }
 
 bool lora_fused_supported(const DecodeArgs& A) {
-  return A.r > 0 && A.r <= 128 && A.r % LQ_COLS == 0 && A.d % LI_ROWS == 0 && A.d % LO_ROWS == 0 && A.G <= 64;
+  return A.r > 0 && A.r <= MAXR && A.r % 8 == 0 && A.d % LP_ROWS == 0 && A.d % LO_ROWS == 0 &&
+         A.L % LP_ROWS == 0 && A.L % LH_COLS == 0 && A.G <= 64;
 }
+
+// tickets: [0, G) lora_p, [G, 2G) lora_q, [2G, 2G + d/LO_ROWS) lora_out
+size_t lora_ticket_words(int d, int G) { return (size_t)2 * G + d / LO_ROWS + 1; }
 
 cudaError_t launch_lora_in(const DecodeArgs& A, float* Ppart, float* P, float* Hl, unsigned* tickets,
-                           cudaStream_t st) {
-  lora_in_kernel<<<dim3(A.G, A.d / LI_ROWS), 256, lora_in_smem(A.r), st>>>(A, Ppart, P, Hl, tickets);
+                           cudaStream_t st, StageHook* hook) {
+  if (hook) hook->before(st);
+  lora_p_kernel<<<dim3(A.G, A.d / LP_ROWS), 256, lora_rows_smem(), st>>>(A, Ppart, P, tickets);
+  cudaError_t e = cudaGetLastError();
+  if (hook) hook->after(st);
+  if (e != cudaSuccess) return e;
+  if (hook) hook->before(st);
+  lora_hl_kernel<<<dim3(A.G, A.L / LH_COLS), 256, 0, st>>>(A, P, Hl);
+  e = cudaGetLastError();
+  if (hook) hook->after(st);
+  return e;
+}
+
+cudaError_t launch_lora_q(const DecodeArgs& A, const float* Zlin, float* Qpart, float* Q, unsigned* tickets,
+                          cudaStream_t st) {
+  lora_q_kernel<<<dim3(A.G, A.L / LP_ROWS), 256, lora_rows_smem(), st>>>(A, Zlin, Qpart, Q, tickets + A.G);
   return cudaGetLastError();
 }
 
-cudaError_t launch_lora_q(const DecodeArgs& A, const float* Zlin, float* Q, cudaStream_t st) {
-  lora_q_kernel<<<dim3(A.G, A.r / LQ_COLS), 256, 0, st>>>(A, Zlin, Q);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_lora_out(const DecodeArgs& A, const float* Yp, const float* Q, cudaStream_t st) {
-  lora_out_kernel<<<A.d / LO_ROWS, 256, 0, st>>>(A, Yp, Q);
+cudaError_t launch_lora_out(const DecodeArgs& A, float* Yp, const float* Q, unsigned* tickets, cudaStream_t st) {
+  lora_out_kernel<<<dim3(A.d / LO_ROWS, A.G), 256, 0, st>>>(A, Yp, Q, tickets + 2 * A.G);
   return cudaGetLastError();
 }
 
