@@ -40,6 +40,8 @@ def parse():
     ap.add_argument("--copies", type=int, default=0, help="device weight copies rotated across steps (0: auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="decode_t8 only: skip the 16K-prefill sub-record")
+    ap.add_argument("--passes", type=int, default=0,
+                    help="for profilers: build one weight copy of --workload, run N plain forwards, no timing")
     ap.add_argument("--sweep", action="store_true",
                     help="decode / speculative-verify sweep: one JSON line per batch T = 1..16 of the Edge0 layer")
     return ap.parse_args()
@@ -724,6 +726,26 @@ def run_staged_stack(args):
         dist.destroy_process_group()
 
 
+def run_passes(args):
+    """N plain forwards of one weight copy of the workload (the call a bench
+    step makes, without graphs or timing): a short, self-contained program
+    for ncu captures."""
+    import numpy as np
+    import torch
+
+    import lmoe_synth as S
+    from sparse_latent_moe_lmoe_b300 import LatentMoE
+
+    sh, T, W, x = S.make_workload(args.workload)
+    m = LatentMoE(sh, W, device=0)
+    xt = torch.from_numpy(x.view(np.int16)).to(torch.device("cuda", 0)).view(torch.bfloat16)
+    for _ in range(args.passes):
+        m.forward(xt)
+    torch.cuda.synchronize()
+    m.check()
+    print(json.dumps({"passes": args.passes, "workload": args.workload, "ok": True}), flush=True)
+
+
 def run_sweep(args):
     """Tokens/s and HBM roofline fraction of the decode path at T = 1..16
     (speculative decoding verifies several candidate tokens per weight read):
@@ -786,6 +808,8 @@ def main():
     import lmoe_synth as S
     if args.impl == "reference":
         run_reference(args)
+    elif args.passes > 0:
+        run_passes(args)
     elif args.sweep:
         run_sweep(args)
     elif args.workload in S.STACK_WORKLOADS:
