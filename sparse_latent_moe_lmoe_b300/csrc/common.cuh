@@ -208,6 +208,11 @@ LMOE_DEV void mbar_init(uint64_t* m, uint32_t cnt) {
 LMOE_DEV void mbar_arrive(uint64_t* m) {
   asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(smem_u32(m)) : "memory");
 }
+// n arrivals at once
+LMOE_DEV void mbar_arrive_n(uint64_t* m, uint32_t n) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0], %1; }" ::"r"(smem_u32(m)), "r"(n)
+               : "memory");
+}
 // bounded wait for the phase with the given parity to complete
 LMOE_DEV void mbar_wait(uint64_t* m, uint32_t parity, long long budget, unsigned* err) {
   const long long t0 = clock64();

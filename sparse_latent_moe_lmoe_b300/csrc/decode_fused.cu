@@ -56,6 +56,7 @@ namespace {
 
 constexpr int NCW = 16, NCT = NCW * 32, PROD = NCW, NTHR = NCT + 32;
 constexpr int RW = 8;             // routing warps while the others compute W_in
+static_assert(NCW % (NCW - RW) == 0, "each W_in warp hands back W_in chunks for a whole number of warps");
 constexpr int SLOT = 18432;      // 16 KB of packed int4 (or fp32 router rows) + 2 KB of scales
 constexpr int FS = 32;           // f-slice of an expert unit
 constexpr int MAX_RX = 4;        // router experts per CTA
@@ -232,9 +233,14 @@ LMOE_DEV bool mwait(Tables& tb, uint64_t* m, uint32_t parity, long long budget, 
 // after a timeout, when waits give up, a slot whose copy is still in flight
 // must never be re-armed and overwritten.
 template <int NS>
-LMOE_DEV void release_read(Tables& tb, int j, bool landed) {
+LMOE_DEV void release_read(Tables& tb, int j, bool landed, uint32_t weight = 1) {
   __syncwarp();
-  if ((threadIdx.x & 31) == 0 && landed) mbar_arrive(&tb.empty[j % NS]);
+  if ((threadIdx.x & 31) == 0 && landed) {
+    if (weight == 1)
+      mbar_arrive(&tb.empty[j % NS]);
+    else
+      mbar_arrive_n(&tb.empty[j % NS], weight);
+  }
 }
 
 template <int NS>
@@ -733,7 +739,10 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
         acc = slot_mma<NT, WF>(sl, PW / 256, 0, reinterpret_cast<const uint16_t*>(sl + 8 * PW), PW / 32, k0c, nkc,
                            xf + (size_t)(tp * CPP + k0c) * FR);
       }
-      release_read<NS>(tb, jA2 + jj, landed);  // a chunk this warp does not read is handed back once it landed
+      // a chunk this warp does not read is handed back once it landed; each
+      // W_in warp arrives for itself and for one routing warp, which never
+      // touches the W_in chunks (so that the slots recycle while it routes)
+      release_read<NS>(tb, jA2 + jj, landed, NCW / (NCW - RW));
     }
     group_sync(BAR_WIN, NCT - RW * 32);  // every W_in warp is done with x: its region takes the partials
 #pragma unroll
@@ -802,13 +811,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
       plan(tb, c, nC, NSF, L, d);
       if (lane == 0) mbar_arrive(&tb.tbar);  // the producer may stream the expert weights
     }
-    // the W_in chunks, handed back once they landed (this warp reads none)
-#pragma unroll 1
-    for (int j = jA2; j < jB; ++j) {
-      bool landed;
-      acquire<NS>(tb, ring, j, budget, err, WS_WIN_SLOT, diag, landed);
-      release_read<NS>(tb, j, landed);
-    }
+    // (the W_in chunks are handed back by the W_in warps alone, see above)
   }
   cons_sync();
   if (trace && ctid == 0) trace[4] = gtime();
