@@ -179,9 +179,10 @@ cudaError_t lora_set_attributes();
 bool lora_fused_supported(const DecodeArgs& A);
 // tickets: lora_ticket_words(d, G) words, zero between calls
 size_t lora_ticket_words(int d, int G);
-// scratch of the partial sums: Ppart [G][d/256][16][r], Qpart [G][L/256][16][r]
-inline size_t lora_ppart_bytes(int d, int G, int r) { return (size_t)G * (d / 256) * 16 * r * 4; }
-inline size_t lora_qpart_bytes(int L, int G, int r) { return (size_t)G * (L / 256) * 16 * r * 4; }
+// scratch of the partial sums: Ppart [G][d/LORA_ROWS][16][r], Qpart [G][L/LORA_ROWS][16][r]
+constexpr int LORA_ROWS = 128;
+inline size_t lora_ppart_bytes(int d, int G, int r) { return (size_t)G * (d / LORA_ROWS) * 16 * r * 4; }
+inline size_t lora_qpart_bytes(int L, int G, int r) { return (size_t)G * (L / LORA_ROWS) * 16 * r * 4; }
 // lora_p then lora_hl (two kernels; the hook brackets each)
 cudaError_t launch_lora_in(const DecodeArgs& A, float* Ppart, float* P, float* Hl, unsigned* tickets,
                            cudaStream_t st, StageHook* hook);

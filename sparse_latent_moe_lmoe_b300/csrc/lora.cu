@@ -22,9 +22,9 @@
 namespace lmoe {
 
 namespace {
-constexpr int LP_ROWS = 256;   // rows of A_in / A_out per lora_p / lora_q CTA (8 warps x 32)
+constexpr int LP_ROWS = LORA_ROWS;  // rows of A_in / A_out per lora_p / lora_q CTA (8 warps x LP_ROWS / 8)
 constexpr int LH_COLS = 128;   // latent columns per lora_hl CTA
-constexpr int LO_ROWS = 256;   // output rows per lora_out CTA
+constexpr int LO_ROWS = 128;   // output rows per lora_out CTA
 constexpr int MAXR = 128;
 
 // bit g: some token routes into group g (every thread of the CTA; the CTA's
@@ -43,7 +43,8 @@ LMOE_DEV float2 bf16x2(uint32_t u) { return make_float2(__uint_as_float(u << 16)
 // Partial of act^T M over rows k0 .. k0 + LP_ROWS of M ([K][r] bf16) for 16
 // tokens, act (fp32 in shared memory, [16][LP_ROWS]) -> out [16][r] (fp32,
 // global), the 8 warps summed in order. Lane l of a warp takes columns 2l,
-// 2l + 1 (a 128-byte row per warp load when r = 64); a warp takes 32 rows.
+// 2l + 1 (a 128-byte row per warp load when r = 64); a warp takes LP_ROWS / 8
+// rows.
 LMOE_DEV void rows_partial(const uint16_t* __restrict__ M, int r, const float* act, float (*red)[16][MAXR],
                            float* __restrict__ out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -54,14 +55,15 @@ LMOE_DEV void rows_partial(const uint16_t* __restrict__ M, int r, const float* a
 #pragma unroll
     for (int t = 0; t < 16; ++t) acc[t][0] = acc[t][1] = 0.f;
 #pragma unroll 1
-    for (int i0 = 0; i0 < 32; i0 += 8) {
+    for (int i0 = 0; i0 < LP_ROWS / 8; i0 += 8) {
       uint32_t w[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) w[u] = __ldg(reinterpret_cast<const uint32_t*>(M + (size_t)(warp * 32 + i0 + u) * r) + c2);
+      for (int u = 0; u < 8; ++u)
+        w[u] = __ldg(reinterpret_cast<const uint32_t*>(M + (size_t)(warp * (LP_ROWS / 8) + i0 + u) * r) + c2);
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const float2 m = bf16x2(w[u]);
-        const int i = warp * 32 + i0 + u;
+        const int i = warp * (LP_ROWS / 8) + i0 + u;
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
           const float a = act[t * LP_ROWS + i];
@@ -99,6 +101,26 @@ LMOE_DEV bool last_arrival(unsigned* ticket, unsigned n) {
   if (last) __threadfence();
   return last;
 }
+// out[o] = sum over b < n of part[b][o] in b order, o < len (a multiple of 4):
+// four values per thread, eight partials' loads in flight
+LMOE_DEV void sum_partials(const float* part, int n, int len, float* out) {
+  for (int o = 4 * threadIdx.x; o < len; o += 4 * blockDim.x) {
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+    for (int b0 = 0; b0 < n; b0 += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        v[u] = b0 + u < n ? __ldcg(reinterpret_cast<const float4*>(part + (size_t)(b0 + u) * len + o))
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        s.x += v[u].x; s.y += v[u].y; s.z += v[u].z; s.w += v[u].w;
+      }
+    }
+    *reinterpret_cast<float4*>(out + o) = s;
+  }
+}
 }  // namespace
 
 // grid (G, d / LP_ROWS). Ppart [G][d/LP_ROWS][16][r], P [G][16][r].
@@ -109,18 +131,21 @@ __global__ void __launch_bounds__(256) lora_p_kernel(DecodeArgs A, float* __rest
   float (*red)[16][MAXR] = reinterpret_cast<float (*)[16][MAXR]>(act + 16 * LP_ROWS);  // [8][16][r]
   const int g = blockIdx.x, kb = blockIdx.y, nkb = gridDim.y, T = A.T, r = A.r, d = A.d;
   const int k0 = kb * LP_ROWS;
-  for (int i = threadIdx.x; i < 16 * LP_ROWS; i += blockDim.x) {
-    const int t = i / LP_ROWS, kk = i % LP_ROWS;
-    act[i] = t < T ? bf16_to_f32(A.x[(size_t)t * d + k0 + kk]) : 0.f;
+  for (int i = threadIdx.x; i < 2 * LP_ROWS; i += blockDim.x) {  // 8 elements of x per thread
+    const int t = i / (LP_ROWS / 8), kk = (i % (LP_ROWS / 8)) * 8;
+    const uint4 v = t < T ? __ldg(reinterpret_cast<const uint4*>(A.x + (size_t)t * d + k0 + kk)) : make_uint4(0, 0, 0, 0);
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 f = bf16x2(u[q]);
+      act[t * LP_ROWS + kk + 2 * q] = f.x;
+      act[t * LP_ROWS + kk + 2 * q + 1] = f.y;
+    }
   }
   __syncthreads();
   rows_partial(A.A_in + ((size_t)g * d + k0) * r, r, act, red, Ppart + ((size_t)g * nkb + kb) * 16 * r);
   if (!last_arrival(tickets + g, (unsigned)nkb)) return;
-  for (int o = threadIdx.x; o < 16 * r; o += blockDim.x) {
-    float s = 0.f;
-    for (int b = 0; b < nkb; ++b) s += __ldcg(Ppart + ((size_t)g * nkb + b) * 16 * r + o);
-    P[(size_t)g * 16 * r + o] = s;
-  }
+  sum_partials(Ppart + (size_t)g * nkb * 16 * r, nkb, 16 * r, P + (size_t)g * 16 * r);
 }
 
 // grid (G, L / LH_COLS). Hl [G][16][L] = P[g]^T-contracted with B_in[g] ([r][L]).
@@ -181,28 +206,24 @@ __global__ void __launch_bounds__(256) lora_q_kernel(DecodeArgs A, const float* 
   __syncthreads();
   rows_partial(A.A_out + ((size_t)g * L + k0) * r, r, act, red, Qpart + ((size_t)g * nkb + kb) * 16 * r);
   if (!last_arrival(tickets + g, (unsigned)nkb)) return;
-  for (int o = threadIdx.x; o < 16 * r; o += blockDim.x) {
-    float s = 0.f;
-    for (int b = 0; b < nkb; ++b) s += __ldcg(Qpart + ((size_t)g * nkb + b) * 16 * r + o);
-    Q[(size_t)g * 16 * r + o] = s;
-  }
+  sum_partials(Qpart + (size_t)g * nkb * 16 * r, nkb, 16 * r, Q + (size_t)g * 16 * r);
 }
 
 // grid (d / LO_ROWS, G). Y[g][t][i] += sum_c Q[g][t][c] B_out[g][c][i] for the
-// block's rows (routed groups); thread (row pair rp, half h of r), halves summed
-// in order. The last group CTA of a row block sums the routed groups in
+// block's rows (routed groups); thread (row pair rp, quarter h of r), quarters
+// summed in order. The last group CTA of a row block sums the routed groups in
 // ascending order, adds the residual and writes y.
 __global__ void __launch_bounds__(256) lora_out_kernel(DecodeArgs A, float* __restrict__ Yp,
                                                        const float* __restrict__ Q, unsigned* __restrict__ tickets) {
   __shared__ float qs[16][MAXR];
-  __shared__ float red[2][16][LO_ROWS];
+  __shared__ float red[4][16][LO_ROWS];
   const int rb = blockIdx.x, g = blockIdx.y, G = gridDim.y, T = A.T, r = A.r, d = A.d;
   const int row0 = rb * LO_ROWS;
   const unsigned long long gm = routed_groups(A);
   if ((gm >> g) & 1ull) {
     for (int i = threadIdx.x; i < 16 * r; i += blockDim.x) qs[i / r][i % r] = __ldcg(Q + (size_t)g * 16 * r + i);
     __syncthreads();
-    const int rp = threadIdx.x & 127, h = threadIdx.x >> 7, rh = r / 2;
+    const int rp = threadIdx.x & (LO_ROWS / 2 - 1), h = threadIdx.x / (LO_ROWS / 2), rh = r / 4;
     const uint16_t* B = A.B_out + (size_t)g * r * d + row0 + 2 * rp;
     float acc[16][2];
 #pragma unroll
@@ -233,7 +254,7 @@ __global__ void __launch_bounds__(256) lora_out_kernel(DecodeArgs A, float* __re
       const int t = o / LO_ROWS, c = o % LO_ROWS;
       if (t < T) {
         float* yp = Yp + ((size_t)g * 16 + t) * d + row0 + c;
-        *yp = __ldcg(yp) + (red[0][t][c] + red[1][t][c]);
+        *yp = __ldcg(yp) + (red[0][t][c] + red[1][t][c] + red[2][t][c] + red[3][t][c]);
       }
     }
   }
