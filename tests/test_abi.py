@@ -53,6 +53,19 @@ def test_host_side_validation_without_gpu():
     cfg.qgroup = 16
     assert lib.lmoe_create(ctypes.byref(h), ctypes.byref(cfg), ctypes.byref(w), 0) == 1  # null weights
     assert h.value is None
+    # staged experts: the slot count must hold a 16-token pass's experts and fit the layer
+    cfg.flags = capi.FLAG_STAGED_EXPERTS
+    cfg.expert_slots = 0
+    assert lib.lmoe_create(ctypes.byref(h), ctypes.byref(cfg), ctypes.byref(w), 0) == 1
+    cfg.expert_slots = cfg.E + 1
+    assert lib.lmoe_create(ctypes.byref(h), ctypes.byref(cfg), ctypes.byref(w), 0) == 1
+    cfg.flags = 8  # no such flag
+    cfg.expert_slots = 0
+    assert lib.lmoe_create(ctypes.byref(h), ctypes.byref(cfg), ctypes.byref(w), 0) == 2
+    assert h.value is None
+    assert lib.lmoe_prefetch_experts(None, None, 8, None) == 1
+    st = capi.LmoeStageStats()
+    assert lib.lmoe_get_stage_stats(None, ctypes.byref(st)) == 1
     for s in range(8):
         assert capi.lmoe_status_string(s)
     name, count = capi.lmoe_stage_name(None, 8, 0)
