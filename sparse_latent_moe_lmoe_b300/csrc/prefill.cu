@@ -110,65 +110,115 @@ LMOE_DEV void store_half16(__half* dst, const float v[16]) {
 }
 
 // ------------------------------------------------------------------ router
+// logits[t][e] (+ bias) = x_t . (W_hi + W_mid + W_lo)[e] for 128 tokens x 256
+// experts per output tile; the top-k runs afterwards (route_topk_kernel), one
+// warp per token.
+//
+// Every product is exact (bf16 x bf16) but the tensor core's fp32
+// accumulator loses up to an ulp of its running value at each accumulate
+// step, so the error grows with the number of steps and with the size of the
+// sum being accumulated. Each output tile is therefore computed as separate
+// accumulations ("segments", each a tile of this problem with its own
+// accumulator): KSEG_HI K blocks of x . W_hi per segment, then one segment
+// for every K block of x . W_mid and x . W_lo (terms ~2^-8 the size of the
+// logit, whose rounding stays far smaller). A CTA takes the segments of one
+// output tile back to back; its epilogue adds each segment's result to the
+// logits row in fp32, in a fixed order (the W_hi segments in K order, then
+// W_mid + W_lo, then the bias), so the running sum stays in the CTA's own
+// rows of the logits array (L2-resident) and the result is deterministic.
 struct ProbRoute : ProbBase {
-  // logits[t][e] (+ bias) for 128 tokens x 256 experts per tile; the top-k
-  // runs afterwards (route_topk_kernel), one warp per token.
   static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 3, B_MODE = 2, STAGES = 4;
+  static constexpr int KSEG_HI = 16;
   CUtensorMap am;         // x as [T][d] bf16, box {64, 128}
   CUtensorMap bm;         // the split W_r as [3][E][d] bf16, box {64, 256, 1}
   const float* bias;      // [E] or null
   int T, d, E;
   float* logits;          // [T][E]
   LMOE_DEV int ntn() const { return (E + 255) / 256; }
+  LMOE_DEV int nmn() const { return ((T + 127) / 128) * ntn(); }
+  LMOE_DEV int nhi() const { return (d / 64 + KSEG_HI - 1) / KSEG_HI; }
+  LMOE_DEV int nseg() const { return nhi() + 1; }
   LMOE_DEV void init(int*) const {}
-  LMOE_DEV int num_tiles(const int*) const { return ((T + 127) / 128) * ntn(); }
+  // CTA c takes output tiles c, c + grid, ...; each as nseg() consecutive
+  // tiles of this problem (tiles past the last output tile are empty)
+  LMOE_DEV int num_tiles(const int*) const {
+    const int g = (int)gridDim.x;
+    return nseg() * g * ((nmn() + g - 1) / g);
+  }
   LMOE_DEV Tile tile(const int*, int t) const {
+    const int g = (int)gridDim.x, i = t / g;
+    const int mn = (i / nseg()) * g + t % g;
     Tile tl;
-    tl.prob = 0;
-    tl.m0 = (t / ntn()) * 128;  // both expert halves of a token tile run side by side (x shared in L2)
-    tl.n0 = (t % ntn()) * 256;
-    tl.rows = min(128, T - tl.m0);
-    tl.nkb = 3 * (d / 64);
+    tl.prob = i % nseg();
     tl.gm = 0;
+    if (mn >= nmn()) {
+      tl.m0 = tl.n0 = tl.rows = tl.nkb = 0;
+      return tl;
+    }
+    tl.m0 = (mn / ntn()) * 128;  // both expert halves of a token tile run side by side (x shared in L2)
+    tl.n0 = (mn % ntn()) * 256;
+    tl.rows = min(128, T - tl.m0);
+    const int kx = d / 64;
+    tl.nkb = tl.prob < nhi() ? min(KSEG_HI, kx - tl.prob * KSEG_HI) : 2 * kx;
     return tl;
   }
-  // K block kb: bf16 term kb % 3 of W_r against x's K block kb / 3 (rows
-  // beyond T or E read as zero)
+  // K block kb of segment s: x block s*KSEG_HI + kb against W_hi, or (the
+  // last segment) x block kb/2 against W_mid (kb even) and W_lo (kb odd);
+  // rows beyond T or E read as zero
   LMOE_DEV void load_a(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
-    tma_load_2d(dst, &am, (kb / 3) * 64, tl.m0, bar);
+    const int xb = tl.prob < nhi() ? tl.prob * KSEG_HI + kb : kb >> 1;
+    tma_load_2d(dst, &am, xb * 64, tl.m0, bar);
   }
   LMOE_DEV void load_b(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
-    tma_load_3d(dst, &bm, (kb / 3) * 64, tl.n0, kb % 3, bar);
+    const bool hi = tl.prob < nhi();
+    tma_load_3d(dst, &bm, (hi ? tl.prob * KSEG_HI + kb : kb >> 1) * 64, tl.n0, hi ? 0 : 1 + (kb & 1), bar);
   }
   LMOE_DEV const void* a_row(const int*, const Tile&, int, int) const { return nullptr; }
   LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int, int) const { return nullptr; }
   LMOE_DEV bool b_row(const int*, const Tile&, int, int, const uint8_t*&, const uint16_t*&) const { return false; }
   LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
-    const uint32_t id = tc::idesc(128, 256, 1);
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      tc::mma_f16(d_tmem, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), id, (kb > 0 || k > 0) ? 1u : 0u);
+    mma_k4(d_tmem, da, db, tc::idesc(128, 256, 1), kb);
   }
-  // one thread per token row: 256 logits (+ bias) to global memory
+  // one thread per token row: the segment's 256 sums added to the row's
+  // running value (written by this same thread for the previous segment)
   LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase) const {
-    const bool valid = row < tl.rows;
+    const bool valid = row < tl.rows, first = tl.prob == 0, last = tl.prob == nseg() - 1;
     float* out = logits + (size_t)(tl.m0 + row) * E + tl.n0;
     const int ne = min(256, E - tl.n0);
-    for (int c0 = 0; c0 < 256; c0 += 16) {
-      float v[16];
-      tc::tmem_ld16(tbase + (uint32_t)c0, v);  // warp-collective: every lane loads
-      if (!valid || c0 >= ne) continue;
-      if (bias) {
+    for (int c0 = 0; c0 < 256; c0 += 64) {
+      float old[64];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] += c0 + i < ne ? bias[tl.n0 + c0 + i] : 0.f;
+      for (int i = 0; i < 64; i += 4) {
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (valid && !first) {
+          if (c0 + i + 4 <= ne) o = *reinterpret_cast<const float4*>(out + c0 + i);
+          else {
+            if (c0 + i < ne) o.x = out[c0 + i];
+            if (c0 + i + 1 < ne) o.y = out[c0 + i + 1];
+            if (c0 + i + 2 < ne) o.z = out[c0 + i + 2];
+          }
+        }
+        old[i] = o.x; old[i + 1] = o.y; old[i + 2] = o.z; old[i + 3] = o.w;
       }
-      if (c0 + 16 <= ne) {
 #pragma unroll
-        for (int i = 0; i < 16; i += 4) *reinterpret_cast<float4*>(out + c0 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-      } else {
+      for (int h = 0; h < 64; h += 16) {
+        float v[16];
+        tc::tmem_ld16(tbase + (uint32_t)(c0 + h), v);  // warp-collective: every lane loads
+        if (!valid) continue;
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (c0 + i < ne) out[c0 + i] = v[i];
+        for (int i = 0; i < 16; ++i) {
+          v[i] = old[h + i] + v[i];
+          if (last && bias) v[i] += c0 + h + i < ne ? bias[tl.n0 + c0 + h + i] : 0.f;
+        }
+        if (c0 + h + 16 <= ne) {
+#pragma unroll
+          for (int i = 0; i < 16; i += 4)
+            *reinterpret_cast<float4*>(out + c0 + h + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (c0 + h + i < ne) out[c0 + h + i] = v[i];
+        }
       }
     }
   }
@@ -207,6 +257,12 @@ struct ProbWin : ProbBase {
   const int32_t* tsort;
   const int* gtc;
   const int* gtl;
+  // Recover-LoRA (rp > 0, the rank padded to 64): K blocks d/64 .. (d+rp)/64
+  // read P = x . A_in (every group, [T][G*rp] fp16 in x16's row order) and
+  // B_in[g]^T in fp16 as [G][L][rp], so H = [x | P_g] . [Win[g] ; B_in[g]]
+  CUtensorMap pm;   // P, box {64, 128}
+  CUtensorMap lbm;  // B_in^T, box {64, 256, 1}
+  int rp;
   LMOE_DEV int ntn() const { return L / 256; }
   LMOE_DEV int ntm() const { return (T + 127) / 128; }
   LMOE_DEV void init(int* sc) const {
@@ -227,15 +283,19 @@ struct ProbWin : ProbBase {
     }
     tl.n0 = (loc % ntn()) * 256;
     tl.rows = min(128, T - tl.m0);
-    tl.nkb = d / 64;
+    tl.nkb = (d + rp) / 64;
     tl.gm = 0;
     return tl;
   }
   LMOE_DEV void load_a(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
-    tma_load_2d(dst, &am, kb * 64, tl.m0, bar);
+    const int kx = d / 64;
+    if (kb < kx) tma_load_2d(dst, &am, kb * 64, tl.m0, bar);
+    else tma_load_2d(dst, &pm, tl.prob * rp + (kb - kx) * 64, tl.m0, bar);
   }
   LMOE_DEV void load_b(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
-    tma_load_3d(dst, &bm, kb * 64, tl.n0, tl.prob, bar);
+    const int kx = d / 64;
+    if (kb < kx) tma_load_3d(dst, &bm, kb * 64, tl.n0, tl.prob, bar);
+    else tma_load_3d(dst, &lbm, (kb - kx) * 64, tl.n0, tl.prob, bar);
   }
   LMOE_DEV const void* a_row(const int*, const Tile&, int, int) const { return nullptr; }
   LMOE_DEV bool b_row(const int*, const Tile&, int, int, const uint8_t*&, const uint16_t*&) const { return false; }
@@ -384,13 +444,20 @@ struct ProbWout : ProbBase {
   // the K blocks of the groups in tunion[j]
   const int32_t* tsort;
   const uint32_t* tunion;
+  // Recover-LoRA (rp > 0): after a group's L/64 K blocks of Z come rp/64 K
+  // blocks of Q = Z . A_out[g] against B_out[g]^T, so the accumulator takes
+  // [Z | Q] . [Wout[g] ; B_out[g]] for each group
+  CUtensorMap qm;   // mode 0: Q as [T][G*rp] (A's row order); mode 1: [rows][rp]; box {64, 128}
+  CUtensorMap lbm;  // B_out^T in fp16 as [G][d][rp], box {64, 256, 1}
+  int rp;
   LMOE_DEV int ntn() const { return d / 256; }
   LMOE_DEV int kpg() const { return L / 64; }
-  // the group of K block kb of a mode-0 tile: the (kb / kpg)-th group of its set
+  LMOE_DEV int kpg2() const { return (L + rp) / 64; }  // K blocks per group, LoRA included
+  // the group of K block kb of a mode-0 tile: the (kb / kpg2)-th group of its set
   LMOE_DEV int kgroup(const Tile& tl, int kb) const {
     unsigned m = tl.gm;
 #pragma unroll 1
-    for (int i = kb / kpg(); i > 0; --i) m &= m - 1u;
+    for (int i = kb / kpg2(); i > 0; --i) m &= m - 1u;
     return __ffs(m) - 1;
   }
   LMOE_DEV void init(int* sc) const {
@@ -405,28 +472,35 @@ struct ProbWout : ProbBase {
       tl.n0 = (t % ntn()) * 256;
       tl.rows = min(128, T - tl.m0);
       tl.gm = tsort ? tunion[t / ntn()] : (G >= 32 ? 0xffffffffu : (1u << G) - 1u);
-      tl.nkb = __popc(tl.gm) * kpg();
+      tl.nkb = __popc(tl.gm) * kpg2();
     } else {
       const int g = find_prob(sc, G, t), loc = t - sc[g];
       tl.prob = g;
       tl.m0 = (loc / ntn()) * 128;
       tl.n0 = (loc % ntn()) * 256;
       tl.rows = min(128, gto[g + 1] - gto[g] - tl.m0);
-      tl.nkb = kpg();
+      tl.nkb = kpg2();
       tl.gm = 0;
     }
     return tl;
   }
   LMOE_DEV void load_a(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
-    if (mode == 0)
-      tma_load_2d(dst, &am, kgroup(tl, kb) * L + (kb % kpg()) * 64, tl.m0, bar);
-    else  // rows past the group's range belong to the next group or read as zero; not stored
-      tma_load_2d(dst, &am, kb * 64, gto[tl.prob] + tl.m0, bar);
+    const int w = kb % kpg2();  // K block within its group
+    if (mode == 0) {
+      const int g = kgroup(tl, kb);
+      if (w < kpg()) tma_load_2d(dst, &am, g * L + w * 64, tl.m0, bar);
+      else tma_load_2d(dst, &qm, g * rp + (w - kpg()) * 64, tl.m0, bar);
+    } else {  // rows past the group's range belong to the next group or read as zero; not stored
+      const int r0 = gto[tl.prob] + tl.m0;
+      if (w < kpg()) tma_load_2d(dst, &am, w * 64, r0, bar);
+      else tma_load_2d(dst, &qm, (w - kpg()) * 64, r0, bar);
+    }
   }
   LMOE_DEV const void* a_row(const int*, const Tile&, int, int) const { return nullptr; }
   LMOE_DEV void load_b(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
-    const int g = mode == 0 ? kgroup(tl, kb) : tl.prob;
-    tma_load_3d(dst, &bm, (mode == 0 ? kb % kpg() : kb) * 64, tl.n0, g, bar);
+    const int g = mode == 0 ? kgroup(tl, kb) : tl.prob, w = kb % kpg2();
+    if (w < kpg()) tma_load_3d(dst, &bm, w * 64, tl.n0, g, bar);
+    else tma_load_3d(dst, &lbm, (w - kpg()) * 64, tl.n0, g, bar);
   }
   LMOE_DEV bool b_row(const int*, const Tile&, int, int, const uint8_t*&, const uint16_t*&) const { return false; }
   LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int, int) const { return nullptr; }
@@ -459,6 +533,118 @@ struct ProbWout : ProbBase {
 #pragma unroll
         for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
       }
+    }
+  }
+};
+
+// ------------------------------------------------------------ Recover-LoRA
+// P = x . A_in for every group at once: [T][d] x [d][G*rp] -> fp16 [T][G*rp]
+// (rows in x16's order; the rank padded to rp with zero columns)
+struct ProbLoraP : ProbBase {
+  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 3, B_MODE = 2, STAGES = 4;
+  CUtensorMap am;  // x in fp16 as [T][d], box {64, 128}
+  CUtensorMap bm;  // A_in^T in fp16 as [G*rp][d] (rows past G*rp read as zero), box {64, 256}
+  int T, d, N;     // N = G*rp
+  __half* P;
+  LMOE_DEV int ntn() const { return (N + 255) / 256; }
+  LMOE_DEV void init(int*) const {}
+  LMOE_DEV int num_tiles(const int*) const { return ((T + 127) / 128) * ntn(); }
+  LMOE_DEV Tile tile(const int*, int t) const {
+    Tile tl;
+    tl.prob = 0;
+    tl.m0 = (t / ntn()) * 128;
+    tl.n0 = (t % ntn()) * 256;
+    tl.rows = min(128, T - tl.m0);
+    tl.nkb = d / 64;
+    tl.gm = 0;
+    return tl;
+  }
+  LMOE_DEV void load_a(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
+    tma_load_2d(dst, &am, kb * 64, tl.m0, bar);
+  }
+  LMOE_DEV void load_b(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
+    tma_load_2d(dst, &bm, kb * 64, tl.n0, bar);
+  }
+  LMOE_DEV const void* a_row(const int*, const Tile&, int, int) const { return nullptr; }
+  LMOE_DEV bool b_row(const int*, const Tile&, int, int, const uint8_t*&, const uint16_t*&) const { return false; }
+  LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int, int) const { return nullptr; }
+  LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
+    mma_k4(d_tmem, da, db, tc::idesc(128, 256, 0), kb);
+  }
+  LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase) const {
+    for (int c0 = 0; c0 < 256; c0 += 16) {
+      float v[16];
+      tc::tmem_ld16(tbase + (uint32_t)c0, v);
+      if (row < tl.rows && tl.n0 + c0 < N) store_half16(P + (size_t)(tl.m0 + row) * N + tl.n0 + c0, v);
+    }
+  }
+};
+
+// Q = Z . A_out[g] per group, 64 columns of the padded rank per tile:
+// mode 0: Z by token ([T][G*L], A's row order), Q as [T][G*rp]; with the
+//         group -> token-tile lists only the tiles whose groups hold g
+// mode 1: Z by group rows ([rows][L]), Q as [rows][rp]
+struct ProbLoraQ : ProbBase {
+  static constexpr int BN = 64, ACC_COLS = 64, A_MODE = 3, B_MODE = 2, STAGES = 4;
+  CUtensorMap am;  // Z, box {64, 128}
+  CUtensorMap bm;  // A_out^T in fp16 as [G][rp][L], box {64, 64, 1}
+  const int32_t* gto;
+  const int* gtc;  // mode 0: null = every (token tile, group)
+  const int* gtl;
+  int T, L, G, rp, mode;
+  __half* Q;
+  LMOE_DEV int rpk() const { return rp / 64; }
+  LMOE_DEV int ntm() const { return (T + 127) / 128; }
+  LMOE_DEV void init(int* sc) const {
+    if (mode == 1) tile_prefix(sc, G, [&](int g) { return ((gto[g + 1] - gto[g] + 127) / 128) * rpk(); });
+    else if (gtc) tile_prefix(sc, G, [&](int g) { return gtc[g] * rpk(); });
+  }
+  LMOE_DEV int num_tiles(const int* sc) const { return (mode == 1 || gtc) ? sc[G] : G * ntm() * rpk(); }
+  LMOE_DEV Tile tile(const int* sc, int t) const {
+    Tile tl;
+    int loc;
+    if (mode == 1 || gtc) {
+      tl.prob = find_prob(sc, G, t);
+      loc = t - sc[tl.prob];
+    } else {
+      tl.prob = t / (ntm() * rpk());
+      loc = t % (ntm() * rpk());
+    }
+    const int mi = loc / rpk();
+    tl.n0 = (loc % rpk()) * 64;
+    if (mode == 1) {
+      tl.m0 = mi * 128;
+      tl.rows = min(128, gto[tl.prob + 1] - gto[tl.prob] - tl.m0);
+    } else {
+      tl.m0 = (gtc ? gtl[tl.prob * ntm() + mi] : mi) * 128;
+      tl.rows = min(128, T - tl.m0);
+    }
+    tl.nkb = L / 64;
+    tl.gm = 0;
+    return tl;
+  }
+  LMOE_DEV void load_a(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
+    if (mode == 0) tma_load_2d(dst, &am, tl.prob * L + kb * 64, tl.m0, bar);
+    else tma_load_2d(dst, &am, kb * 64, gto[tl.prob] + tl.m0, bar);  // rows past the group: not stored
+  }
+  LMOE_DEV void load_b(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
+    tma_load_3d(dst, &bm, kb * 64, tl.n0, tl.prob, bar);
+  }
+  LMOE_DEV const void* a_row(const int*, const Tile&, int, int) const { return nullptr; }
+  LMOE_DEV bool b_row(const int*, const Tile&, int, int, const uint8_t*&, const uint16_t*&) const { return false; }
+  LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int, int) const { return nullptr; }
+  LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
+    mma_k4(d_tmem, da, db, tc::idesc(128, 64, 0), kb);
+  }
+  LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase) const {
+    const bool valid = row < tl.rows;
+    __half* out = mode == 0 ? Q + (size_t)(tl.m0 + row) * G * rp + tl.prob * rp + tl.n0
+                            : Q + (size_t)(gto[tl.prob] + tl.m0 + row) * rp + tl.n0;
+#pragma unroll
+    for (int c0 = 0; c0 < 64; c0 += 16) {
+      float v[16];
+      tc::tmem_ld16(tbase + (uint32_t)c0, v);
+      if (valid) store_half16(out + c0, v);
     }
   }
 };
@@ -734,6 +920,58 @@ __global__ void __launch_bounds__(256) dequant_all_kernel(const __grid_constant_
   }
 }
 
+// The Recover-LoRA matrices, bf16 [G][R][C], to transposed fp16 copies
+// [G][Cp][Rp] (out[g][c][q] = in[g][q][c]; zero for q >= R or c >= C, the
+// rank's padding), 32 x 32 tiles through shared memory. bf16 -> fp16 is
+// exact from 2^-14 up to 65504; below 2^-14 it rounds to the fp16 subnormal
+// grid (error <= 2^-25); a finite value that overflows sets BAD_DATA.
+struct LoraT16 {
+  const uint16_t* in;
+  __half* out;
+  int R, C, Rp, Cp;
+  LMOE_DEV int tiles() const { return ((Cp + 31) / 32) * ((Rp + 31) / 32); }
+};
+struct LoraT16Job {
+  LoraT16 m[4];
+  int G;
+  unsigned* err;
+};
+
+__global__ void __launch_bounds__(256) lora_t16_kernel(const __grid_constant__ LoraT16Job J) {
+  __shared__ float tile[32][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  int per[4], total = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) total += (per[i] = J.G * J.m[i].tiles());
+#pragma unroll 1
+  for (int b = blockIdx.x; b < total; b += gridDim.x) {
+    int i = 0, loc = b;
+    while (loc >= per[i]) loc -= per[i++];
+    const LoraT16 M = J.m[i];
+    const int ntq = (M.Rp + 31) / 32, per_g = M.tiles();
+    const int g = loc / per_g, c0 = ((loc % per_g) / ntq) * 32, q0 = ((loc % per_g) % ntq) * 32;
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int q = q0 + ty + 8 * j, c = c0 + tx;
+      float v = 0.f;
+      if (q < M.R && c < M.C) {
+        v = bf16_to_f32(M.in[((size_t)g * M.R + q) * M.C + c]);
+        bad |= fabsf(v) < INFINITY && fabsf(__half2float(__float2half_rn(v))) == INFINITY;
+      }
+      tile[ty + 8 * j][tx] = v;
+    }
+    if (bad) set_error(J.err, ERRBIT_BAD_DATA);
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = c0 + ty + 8 * j, q = q0 + tx;
+      if (c < M.Cp && q < M.Rp) M.out[((size_t)g * M.Cp + c) * M.Rp + q] = __float2half_rn(tile[tx][ty + 8 * j]);
+    }
+    __syncthreads();
+  }
+}
+
 // ------------------------------------------------------------------ host side
 
 namespace {
@@ -743,8 +981,11 @@ size_t al(size_t v) { return (v + kAl - 1) & ~(kAl - 1); }
 
 struct PWs {
   size_t logits, idx, w, eo, sa, inv, go, gto, gt, ar, perm_scratch, H, V, U, Z, tokrow, x16, win16, wout16, gate16, up16,
-      down16, ztok, tmask, tsort, tpos, tbh, tunion, gtc, gtl, end;
+      down16, ztok, tmask, tsort, tpos, tbh, tunion, gtc, gtl, ain16, bin16, aout16, bout16, lp, lq, end;
 };
+
+// the LoRA rank padded to whole K blocks of 64 (0: no branch)
+int lora_rp(const PrefillArgs& P) { return (P.r + 63) / 64 * 64; }
 
 PWs pws(const PrefillArgs& P, int T) {
   PWs m;
@@ -786,6 +1027,14 @@ PWs pws(const PrefillArgs& P, int T) {
   m.tunion = take(nt * 4);
   m.gtc = take((size_t)P.G * 4);
   m.gtl = take((size_t)P.G * nt * 4);
+  // Recover-LoRA: the transposed fp16 matrices, P = x . A_in and Q = Z . A_out
+  const size_t rp = (size_t)lora_rp(P);
+  m.ain16 = take((size_t)P.G * rp * P.d * 2);
+  m.bin16 = take((size_t)P.G * P.L * rp * 2);
+  m.aout16 = take((size_t)P.G * rp * P.L * 2);
+  m.bout16 = take((size_t)P.G * P.d * rp * 2);
+  m.lp = take((size_t)T * P.G * rp * 2);
+  m.lq = take((size_t)T * P.G * rp * 2);  // mode 1: rows (<= T*G) x rp
   m.end = o;
   return m;
 }
@@ -870,8 +1119,33 @@ cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_
   __half* up16 = reinterpret_cast<__half*>(b + m.up16);
   __half* down16 = reinterpret_cast<__half*>(b + m.down16);
   __half* ztok = reinterpret_cast<__half*>(b + m.ztok);
+  const int rp = lora_rp(P);
+  __half* lp = reinterpret_cast<__half*>(b + m.lp);
+  __half* lq = reinterpret_cast<__half*>(b + m.lq);
   cudaError_t e;
-  if (dequant_here && (e = dequant(P, x, T, b, m, st, hook, to.tsort == nullptr)) != cudaSuccess) return e;
+  if (dequant_here) {
+    const int at = hook ? hook->i : 0;
+    if (hook) hook->i = 2;  // the dequant stage's slot
+    if ((e = dequant(P, x, T, b, m, st, hook, to.tsort == nullptr)) != cudaSuccess) return e;
+    if (hook) hook->i = at;
+  }
+  if (rp > 0) {  // lora_p: P = x . A_in for every group
+    ProbLoraP p;
+    static_cast<ProbBase&>(p) = base(P);
+    {
+      const cuuint64_t ad[2] = {(cuuint64_t)P.d, (cuuint64_t)T}, as[1] = {(cuuint64_t)P.d * 2};
+      const cuuint32_t ab[2] = {64, 128};
+      const cuuint64_t bd[2] = {(cuuint64_t)P.d, (cuuint64_t)P.G * rp}, bs[1] = {(cuuint64_t)P.d * 2};
+      const cuuint32_t bb[2] = {64, 256};
+      if (!tmap_encode(&p.am, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x16, ad, as, ab, CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !tmap_encode(&p.bm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, b + m.ain16, bd, bs, bb, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    }
+    p.T = T; p.d = P.d; p.N = P.G * rp; p.P = lp;
+    if (hook) hook->before(st);
+    if ((e = run_gemm(p, grid, st)) != cudaSuccess) return e;
+    if (hook) hook->after(st);
+  }
   {
     ProbWin p;
     static_cast<ProbBase&>(p) = base(P);
@@ -883,6 +1157,17 @@ cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_
       const cuuint32_t bb[3] = {64, 256, 1};
       if (!tmap_encode(&p.am, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x16, ad, as, ab, CU_TENSOR_MAP_SWIZZLE_128B) ||
           !tmap_encode(&p.bm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, win16, bd, bs, bb, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    }
+    p.rp = rp;
+    if (rp > 0) {
+      const cuuint64_t pd[2] = {(cuuint64_t)P.G * rp, (cuuint64_t)T}, ps[1] = {(cuuint64_t)P.G * rp * 2};
+      const cuuint32_t pb[2] = {64, 128};
+      const cuuint64_t ld[3] = {(cuuint64_t)rp, (cuuint64_t)P.L, (cuuint64_t)P.G};
+      const cuuint64_t ls[2] = {(cuuint64_t)rp * 2, (cuuint64_t)P.L * rp * 2};
+      const cuuint32_t lb[3] = {64, 256, 1};
+      if (!tmap_encode(&p.pm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, lp, pd, ps, pb, CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !tmap_encode(&p.lbm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, b + m.bin16, ld, ls, lb, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     }
     p.T = T; p.d = P.d; p.L = P.L; p.G = P.G; p.k = P.k; p.epg = P.epg; p.idx = idx; p.inv = pm.inv; p.H = H;
@@ -941,6 +1226,30 @@ cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (hook) hook->after(st);
   }
+  const int rows_cap = T * (P.G < P.k ? P.G : P.k);
+  if (rp > 0) {  // lora_q: Q = Z . A_out[g]
+    ProbLoraQ p;
+    static_cast<ProbBase&>(p) = base(P);
+    {
+      const cuuint64_t ad0[2] = {(cuuint64_t)P.G * P.L, (cuuint64_t)T}, as0[1] = {(cuuint64_t)P.G * P.L * 2};
+      const cuuint64_t ad1[2] = {(cuuint64_t)P.L, (cuuint64_t)rows_cap}, as1[1] = {(cuuint64_t)P.L * 2};
+      const cuuint32_t ab[2] = {64, 128};
+      const cuuint64_t bd[3] = {(cuuint64_t)P.L, (cuuint64_t)rp, (cuuint64_t)P.G};
+      const cuuint64_t bs[2] = {(cuuint64_t)P.L * 2, (cuuint64_t)rp * P.L * 2};
+      const cuuint32_t bb[3] = {64, 64, 1};
+      if (!tmap_encode(&p.am, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, mode == 0 ? (const void*)ztok : (const void*)Z,
+                       mode == 0 ? ad0 : ad1, mode == 0 ? as0 : as1, ab, CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !tmap_encode(&p.bm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, b + m.aout16, bd, bs, bb, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    }
+    p.gto = pm.group_tok_offsets;
+    p.gtc = mode == 0 ? to.gtc : nullptr;
+    p.gtl = mode == 0 ? to.gtl : nullptr;
+    p.T = T; p.L = P.L; p.G = P.G; p.rp = rp; p.mode = mode; p.Q = lq;
+    if (hook) hook->before(st);
+    if ((e = run_gemm(p, grid, st)) != cudaSuccess) return e;
+    if (hook) hook->after(st);
+  }
   {
     ProbWout p;
     static_cast<ProbBase&>(p) = base(P);
@@ -953,12 +1262,24 @@ cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_
         return cudaErrorInvalidValue;
     }
     {
-      const int rows_cap = T * (P.G < P.k ? P.G : P.k);
       const cuuint64_t ad0[2] = {(cuuint64_t)P.G * P.L, (cuuint64_t)T}, as0[1] = {(cuuint64_t)P.G * P.L * 2};
       const cuuint64_t ad1[2] = {(cuuint64_t)P.L, (cuuint64_t)rows_cap}, as1[1] = {(cuuint64_t)P.L * 2};
       const cuuint32_t ab[2] = {64, 128};
       if (!tmap_encode(&p.am, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, mode == 0 ? (const void*)ztok : (const void*)Z,
                        mode == 0 ? ad0 : ad1, mode == 0 ? as0 : as1, ab, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    }
+    p.rp = rp;
+    if (rp > 0) {
+      const cuuint64_t qd0[2] = {(cuuint64_t)P.G * rp, (cuuint64_t)T}, qs0[1] = {(cuuint64_t)P.G * rp * 2};
+      const cuuint64_t qd1[2] = {(cuuint64_t)rp, (cuuint64_t)rows_cap}, qs1[1] = {(cuuint64_t)rp * 2};
+      const cuuint32_t qb[2] = {64, 128};
+      const cuuint64_t ld[3] = {(cuuint64_t)rp, (cuuint64_t)P.d, (cuuint64_t)P.G};
+      const cuuint64_t ls[2] = {(cuuint64_t)rp * 2, (cuuint64_t)P.d * rp * 2};
+      const cuuint32_t lb[3] = {64, 256, 1};
+      if (!tmap_encode(&p.qm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, lq, mode == 0 ? qd0 : qd1, mode == 0 ? qs0 : qs1, qb,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !tmap_encode(&p.lbm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, b + m.bout16, ld, ls, lb, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     }
     p.gto = pm.group_tok_offsets; p.T = T; p.d = P.d; p.L = P.L; p.G = P.G; p.mode = mode;
@@ -1006,6 +1327,18 @@ cudaError_t dequant(const PrefillArgs& P, const uint16_t* x, int T, char* b, con
     J.nx = with_x ? (size_t)T * P.d / 8 : 0;
     dequant_all_kernel<<<8 * grid, 256, 0, st>>>(J);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int rp = lora_rp(P);
+    if (rp > 0) {  // A_in^T [G*rp][d], B_in^T [G][L][rp], A_out^T [G][rp][L], B_out^T [G][d][rp]
+      LoraT16Job L;
+      L.m[0] = LoraT16{P.A_in, reinterpret_cast<__half*>(b + m.ain16), P.d, P.r, P.d, rp};
+      L.m[1] = LoraT16{P.B_in, reinterpret_cast<__half*>(b + m.bin16), P.r, P.L, rp, P.L};
+      L.m[2] = LoraT16{P.A_out, reinterpret_cast<__half*>(b + m.aout16), P.L, P.r, P.L, rp};
+      L.m[3] = LoraT16{P.B_out, reinterpret_cast<__half*>(b + m.bout16), P.r, P.d, rp, P.d};
+      L.G = P.G;
+      L.err = P.err;
+      lora_t16_kernel<<<4 * grid, 256, 0, st>>>(L);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     if (hook) hook->after(st);
   }
   return cudaSuccess;
@@ -1041,13 +1374,16 @@ cudaError_t prefill_set_attributes() {
   if ((e = set_attr<ProbWin>()) != cudaSuccess) return e;
   if ((e = set_attr<ProbGateUp>()) != cudaSuccess) return e;
   if ((e = set_attr<ProbDown>()) != cudaSuccess) return e;
+  if ((e = set_attr<ProbLoraP>()) != cudaSuccess) return e;
+  if ((e = set_attr<ProbLoraQ>()) != cudaSuccess) return e;
   return set_attr<ProbWout>();
 }
 
 bool prefill_supported(const PrefillArgs& P) {
-  if (P.r != 0) return false;  // the LoRA branch runs on the decode path
+  if (P.r < 0 || P.r > 128) return false;
   if (P.d % 256 != 0 || P.L % 256 != 0 || P.f % 128 != 0) return false;
   if (P.E > 512 || P.k > 16 || P.G > 32) return false;  // top-k: E <= 512 logits per warp; group masks: 32 bits
+  if (P.E % 4 != 0) return false;                         // logits rows by 16-byte words
   return P.num_sms > 0;
 }
 
@@ -1124,25 +1460,29 @@ cudaError_t launch_prefill_layer(const PrefillArgs& P, const uint16_t* x, int T,
   }
   if (fork) {
     if ((e = cudaStreamWaitEvent(st, P.ev_join, 0)) != cudaSuccess) return e;
-    if (hk) hk->i = 4;
+    if (hk) hk->i = sorted ? 4 : 3;  // the first stage after the dequantisation and the token order
   }
   return experts(P, x, T, idx, w, pm, b, m, 0, nullptr, residual, y, st, hk, !fork, to);
 }
 
 int prefill_launch_count(const PrefillArgs& P, int T) {
-  // route: GEMM + top-k; permute: count, scan, scatter; dequant; tsort:
-  // count, scan, scatter, tiles, x in order (G <= 8); win; gateup; down;
-  // zreduce; wout
-  return T > 0 ? (P.G <= 8 ? 16 : 11) : 0;
+  // route: GEMM + top-k; permute: count, scan, scatter; dequant (+ the LoRA
+  // matrices); tsort: count, scan, scatter, tiles, x in order (G <= 8);
+  // [lora_p]; win; gateup; down; zreduce; [lora_q]; wout
+  if (T <= 0) return 0;
+  return (P.G <= 8 ? 16 : 11) + (P.r > 0 ? 3 : 0);
 }
 
 const char* prefill_stage_name(const PrefillArgs& P, int, int i, int* count) {
   static const char* names[] = {"route", "permute", "dequant", "tsort", "win", "gateup", "down", "zreduce", "wout"};
-  static const char* names_u[] = {"route", "permute", "dequant", "win", "gateup", "down", "zreduce", "wout"};
-  const bool sorted = P.G <= 8;
-  const int n = sorted ? 9 : 8;
+  static const char* names_l[] = {"route", "permute", "dequant", "tsort", "lora_p", "win",
+                                  "gateup", "down", "zreduce", "lora_q", "wout"};
+  const bool sorted = P.G <= 8, lora = P.r > 0;
+  const char* const* list = lora ? names_l : names;
+  const int n = (sorted ? 9 : 8) + (lora ? 2 : 0);
   if (count) *count = n;
-  return (i >= 0 && i < n) ? (sorted ? names[i] : names_u[i]) : "";
+  if (i < 0 || i >= n) return "";
+  return list[sorted || i < 3 ? i : i + 1];  // without the token order, "tsort" is skipped
 }
 
 }  // namespace lmoe
