@@ -189,6 +189,14 @@ def stage_flops(sh, T, idx):
     f["gateup"] = 2.0 * 2 * sh.L * sh.f * T * sh.k
     f["down"] = 2.0 * sh.f * sh.L * T * sh.k
     f["wout"] = 2.0 * sh.L * sh.d * rows
+    if sh.lora_rank:
+        # Recover-LoRA: P = x . A_in for every (group, token) that uses the
+        # group, Q = Z . A_out, and the rank-r K blocks of W_in and W_out
+        r = sh.lora_rank
+        f["lora_p"] = 2.0 * sh.d * r * rows
+        f["lora_q"] = 2.0 * sh.L * r * rows
+        f["win"] += 2.0 * r * sh.L * rows
+        f["wout"] += 2.0 * r * sh.d * rows
     f["permute"] = 0.0
     f["zreduce"] = 0.0
     f["dequant"] = 0.0

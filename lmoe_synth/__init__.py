@@ -177,6 +177,8 @@ WORKLOADS = {
     "tiny_t64_nvfp4": (replace(TINY, wfmt="nvfp4"), 64, 0, 0, None, None),
     "decode_t8_nvfp4": (replace(EDGE0, wfmt="nvfp4"), 8, 0, 1, None, None),
     "prefill_t16384_zipf_nvfp4": (replace(EDGE0, has_bias=True, wfmt="nvfp4"), 16384, 0, 1, 2, None),
+    # the 16K prefill layer with its rank-64 Recover-LoRA branch
+    "prefill_t16384_zipf_lora": (replace(EDGE0, has_bias=True, lora_rank=64), 16384, 0, 1, 2, 3),
 }
 
 W_SIGMA = 0.02       # int4 weights and router before quantisation

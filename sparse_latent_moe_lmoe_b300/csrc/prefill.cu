@@ -122,10 +122,12 @@ LMOE_DEV void store_half16(__half* dst, const float v[16]) {
 // accumulator): KSEG_HI K blocks of x . W_hi per segment, then one segment
 // for every K block of x . W_mid and x . W_lo (terms ~2^-8 the size of the
 // logit, whose rounding stays far smaller). A CTA takes the segments of one
-// output tile back to back; its epilogue adds each segment's result to the
-// logits row in fp32, in a fixed order (the W_hi segments in K order, then
-// W_mid + W_lo, then the bias), so the running sum stays in the CTA's own
-// rows of the logits array (L2-resident) and the result is deterministic.
+// output tile back to back; its epilogue adds each segment's result to a
+// running fp32 sum in a fixed order (the W_hi segments in K order, then
+// W_mid + W_lo, then the bias), so the result is deterministic. The running
+// sum lives in the CTA's own 128 KB scratch tile (L2-resident), laid out
+// [column / 4][row][4] so that a warp's 32 rows are one contiguous 512-byte
+// run per access; the last segment writes the logits rows.
 struct ProbRoute : ProbBase {
   static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 3, B_MODE = 2, STAGES = 4;
   static constexpr int KSEG_HI = 16;
@@ -134,6 +136,7 @@ struct ProbRoute : ProbBase {
   const float* bias;      // [E] or null
   int T, d, E;
   float* logits;          // [T][E]
+  float* part;            // [grid][64][128][4] running sums, one tile per CTA
   LMOE_DEV int ntn() const { return (E + 255) / 256; }
   LMOE_DEV int nmn() const { return ((T + 127) / 128) * ntn(); }
   LMOE_DEV int nhi() const { return (d / 64 + KSEG_HI - 1) / KSEG_HI; }
@@ -180,35 +183,46 @@ struct ProbRoute : ProbBase {
     mma_k4(d_tmem, da, db, tc::idesc(128, 256, 1), kb);
   }
   // one thread per token row: the segment's 256 sums added to the row's
-  // running value (written by this same thread for the previous segment)
+  // running value (this thread's own from the previous segment), 32 columns
+  // at a time with the next 32 columns' loads already in flight
   LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase) const {
     const bool valid = row < tl.rows, first = tl.prob == 0, last = tl.prob == nseg() - 1;
+    float4* pp = reinterpret_cast<float4*>(part) + (size_t)blockIdx.x * (64 * 128) + row;  // + (c / 4) * 128
+    const bool ld = valid && !first;
+    float4 cur[8], nxt[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) cur[i] = ld ? __ldcg(pp + i * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
     float* out = logits + (size_t)(tl.m0 + row) * E + tl.n0;
     const int ne = min(256, E - tl.n0);
-    for (int c0 = 0; c0 < 256; c0 += 64) {
-      float old[64];
 #pragma unroll
-      for (int i = 0; i < 64; i += 4) {
-        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (valid && !first) {
-          if (c0 + i + 4 <= ne) o = *reinterpret_cast<const float4*>(out + c0 + i);
-          else {
-            if (c0 + i < ne) o.x = out[c0 + i];
-            if (c0 + i + 1 < ne) o.y = out[c0 + i + 1];
-            if (c0 + i + 2 < ne) o.z = out[c0 + i + 2];
-          }
-        }
-        old[i] = o.x; old[i + 1] = o.y; old[i + 2] = o.z; old[i + 3] = o.w;
+    for (int c0 = 0; c0 < 256; c0 += 32) {
+      if (c0 + 32 < 256) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          nxt[i] = ld ? __ldcg(pp + ((c0 + 32) / 4 + i) * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
-      for (int h = 0; h < 64; h += 16) {
+      for (int h = 0; h < 32; h += 16) {
         float v[16];
         tc::tmem_ld16(tbase + (uint32_t)(c0 + h), v);  // warp-collective: every lane loads
         if (!valid) continue;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          v[i] = old[h + i] + v[i];
-          if (last && bias) v[i] += c0 + h + i < ne ? bias[tl.n0 + c0 + h + i] : 0.f;
+        for (int i = 0; i < 4; ++i) {
+          const float4 o = cur[h / 4 + i];
+          v[4 * i] = o.x + v[4 * i];
+          v[4 * i + 1] = o.y + v[4 * i + 1];
+          v[4 * i + 2] = o.z + v[4 * i + 2];
+          v[4 * i + 3] = o.w + v[4 * i + 3];
+        }
+        if (!last) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            __stcg(pp + ((c0 + h) / 4 + i) * 128, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+          continue;
+        }
+        if (bias) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] += c0 + h + i < ne ? bias[tl.n0 + c0 + h + i] : 0.f;
         }
         if (c0 + h + 16 <= ne) {
 #pragma unroll
@@ -220,6 +234,8 @@ struct ProbRoute : ProbBase {
             if (c0 + h + i < ne) out[c0 + h + i] = v[i];
         }
       }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
     }
   }
 };
@@ -980,7 +996,7 @@ constexpr size_t kAl = 256;
 size_t al(size_t v) { return (v + kAl - 1) & ~(kAl - 1); }
 
 struct PWs {
-  size_t logits, idx, w, eo, sa, inv, go, gto, gt, ar, perm_scratch, H, V, U, Z, tokrow, x16, win16, wout16, gate16, up16,
+  size_t logits, rpart, idx, w, eo, sa, inv, go, gto, gt, ar, perm_scratch, H, V, U, Z, tokrow, x16, win16, wout16, gate16, up16,
       down16, ztok, tmask, tsort, tpos, tbh, tunion, gtc, gtl, ain16, bin16, aout16, bout16, lp, lq, end;
 };
 
@@ -997,6 +1013,7 @@ PWs pws(const PrefillArgs& P, int T) {
   };
   const size_t n = (size_t)T * P.k, gk = (size_t)T * (P.G < P.k ? P.G : P.k);
   m.logits = take((size_t)T * P.E * 4);
+  m.rpart = take((size_t)(P.num_sms > 0 ? P.num_sms : 1) * 128 * 256 * 4);  // the router's running sums
   m.idx = take(n * 4);
   m.w = take(n * 4);
   m.eo = take((size_t)(P.E + 1) * 4);
@@ -1345,7 +1362,7 @@ cudaError_t dequant(const PrefillArgs& P, const uint16_t* x, int T, char* b, con
 }
 
 cudaError_t route(const PrefillArgs& P, const uint16_t* x, int T, int32_t* idx, float* w, float* logits,
-                  cudaStream_t st) {
+                  float* part, cudaStream_t st) {
   ProbRoute p;
   static_cast<ProbBase&>(p) = base(P);
   {
@@ -1360,6 +1377,7 @@ cudaError_t route(const PrefillArgs& P, const uint16_t* x, int T, int32_t* idx, 
   }
   p.bias = P.b_r; p.T = T; p.d = P.d; p.E = P.E;
   p.logits = logits;
+  p.part = part;
   cudaError_t e = run_gemm(p, P.num_sms, st);
   if (e != cudaSuccess) return e;
   route_topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits, T, P.E, P.k, idx, w);
@@ -1395,7 +1413,7 @@ size_t prefill_workspace_bytes(const PrefillArgs& P, int T) {
 cudaError_t launch_prefill_route(const PrefillArgs& P, const uint16_t* x, int T, int32_t* idx, float* w,
                                  float* logits, void* ws, cudaStream_t st) {
   if (!logits) logits = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + pws(P, T).logits);
-  return route(P, x, T, idx, w, logits, st);
+  return route(P, x, T, idx, w, logits, reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + pws(P, T).rpart), st);
 }
 
 cudaError_t launch_prefill_experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_t* idx, const float* w,
@@ -1431,7 +1449,9 @@ cudaError_t launch_prefill_layer(const PrefillArgs& P, const uint16_t* x, int T,
     if (hk) hk->i = 0;
   }
   if (hk) hk->before(st);
-  if ((e = route(P, x, T, idx, w, reinterpret_cast<float*>(b + m.logits), st)) != cudaSuccess) return e;
+  if ((e = route(P, x, T, idx, w, reinterpret_cast<float*>(b + m.logits), reinterpret_cast<float*>(b + m.rpart), st)) !=
+      cudaSuccess)
+    return e;
   if (hk) hk->after(st);
   if (hk) hk->before(st);
   if ((e = launch_permute(idx, T, P.E, P.G, P.k, pm, b + m.perm_scratch, P.err, st)) != cudaSuccess) return e;
