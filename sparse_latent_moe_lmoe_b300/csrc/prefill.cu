@@ -91,6 +91,7 @@ LMOE_DEV int find_prob(const int* scratch, int n, int t) {
 }
 
 struct ProbBase {
+  static constexpr int EPI_SETS = 2;  // epilogue warp sets (TMA operands only)
   long long budget;
   unsigned* err;
 };
@@ -107,6 +108,13 @@ LMOE_DEV void store_half16(__half* dst, const float v[16]) {
   uint4* d4 = reinterpret_cast<uint4*>(dst);
   d4[0] = make_uint4(h[0], h[1], h[2], h[3]);
   d4[1] = make_uint4(h[4], h[5], h[6], h[7]);
+}
+
+// the epilogue's column range of an n-column tile: every column (half < 0)
+// or the first / second half (two epilogue warp sets)
+LMOE_DEV void epi_cols(int half, int n, int& lo, int& hi) {
+  lo = half < 0 ? 0 : half * (n / 2);
+  hi = half < 0 ? n : lo + n / 2;
 }
 
 // ------------------------------------------------------------------ router
@@ -154,6 +162,7 @@ struct ProbRoute : ProbBase {
     Tile tl;
     tl.prob = i % nseg();
     tl.gm = 0;
+    tl.arow = 0;
     if (mn >= nmn()) {
       tl.m0 = tl.n0 = tl.rows = tl.nkb = 0;
       return tl;
@@ -182,60 +191,59 @@ struct ProbRoute : ProbBase {
   LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
     mma_k4(d_tmem, da, db, tc::idesc(128, 256, 1), kb);
   }
-  // one thread per token row: the segment's 256 sums added to the row's
-  // running value (this thread's own from the previous segment), 32 columns
-  // at a time with the next 32 columns' loads already in flight
-  LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase) const {
+  // one thread per token row: the segment's sums (this warp set's columns)
+  // added to the row's running value (this thread's own from the previous
+  // segment), 16 columns at a time with the next 16 columns' loads in flight
+  LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase, int half) const {
     const bool valid = row < tl.rows, first = tl.prob == 0, last = tl.prob == nseg() - 1;
     float4* pp = reinterpret_cast<float4*>(part) + (size_t)blockIdx.x * (64 * 128) + row;  // + (c / 4) * 128
     const bool ld = valid && !first;
-    float4 cur[8], nxt[8];
+    int lo, hi;
+    epi_cols(half, 256, lo, hi);
+    float4 cur[4], nxt[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) cur[i] = ld ? __ldcg(pp + i * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < 4; ++i) cur[i] = ld ? __ldcg(pp + (lo / 4 + i) * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
     float* out = logits + (size_t)(tl.m0 + row) * E + tl.n0;
     const int ne = min(256, E - tl.n0);
+#pragma unroll 1
+    for (int c0 = lo; c0 < hi; c0 += 16) {
+      if (c0 + 16 < hi) {
 #pragma unroll
-    for (int c0 = 0; c0 < 256; c0 += 32) {
-      if (c0 + 32 < 256) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          nxt[i] = ld ? __ldcg(pp + ((c0 + 32) / 4 + i) * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < 4; ++i)
+          nxt[i] = ld ? __ldcg(pp + ((c0 + 16) / 4 + i) * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-#pragma unroll
-      for (int h = 0; h < 32; h += 16) {
-        float v[16];
-        tc::tmem_ld16(tbase + (uint32_t)(c0 + h), v);  // warp-collective: every lane loads
-        if (!valid) continue;
+      float v[16];
+      tc::tmem_ld16(tbase + (uint32_t)c0, v);  // warp-collective: every lane loads
+      if (valid) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float4 o = cur[h / 4 + i];
-          v[4 * i] = o.x + v[4 * i];
-          v[4 * i + 1] = o.y + v[4 * i + 1];
-          v[4 * i + 2] = o.z + v[4 * i + 2];
-          v[4 * i + 3] = o.w + v[4 * i + 3];
+          v[4 * i] = cur[i].x + v[4 * i];
+          v[4 * i + 1] = cur[i].y + v[4 * i + 1];
+          v[4 * i + 2] = cur[i].z + v[4 * i + 2];
+          v[4 * i + 3] = cur[i].w + v[4 * i + 3];
         }
         if (!last) {
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            __stcg(pp + ((c0 + h) / 4 + i) * 128, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
-          continue;
-        }
-        if (bias) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] += c0 + h + i < ne ? bias[tl.n0 + c0 + h + i] : 0.f;
-        }
-        if (c0 + h + 16 <= ne) {
-#pragma unroll
-          for (int i = 0; i < 16; i += 4)
-            *reinterpret_cast<float4*>(out + c0 + h + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+            __stcg(pp + (c0 / 4 + i) * 128, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
         } else {
+          if (bias) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (c0 + h + i < ne) out[c0 + h + i] = v[i];
+            for (int i = 0; i < 16; ++i) v[i] += c0 + i < ne ? bias[tl.n0 + c0 + i] : 0.f;
+          }
+          if (c0 + 16 <= ne) {
+#pragma unroll
+            for (int i = 0; i < 16; i += 4)
+              *reinterpret_cast<float4*>(out + c0 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (c0 + i < ne) out[c0 + i] = v[i];
+          }
         }
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
+      for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
     }
   }
 };
@@ -301,6 +309,7 @@ struct ProbWin : ProbBase {
     tl.rows = min(128, T - tl.m0);
     tl.nkb = (d + rp) / 64;
     tl.gm = 0;
+    tl.arow = tl.m0;
     return tl;
   }
   LMOE_DEV void load_a(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
@@ -319,13 +328,15 @@ struct ProbWin : ProbBase {
   LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
     mma_k4(d_tmem, da, db, tc::idesc(128, 256, 0), kb);
   }
-  LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase) const {
+  LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase, int half) const {
     const int t = row < tl.rows ? (tsort ? tsort[tl.m0 + row] : tl.m0 + row) : 0;
     unsigned dest = 0;  // bit j: assignment j of token t is an expert of group tl.prob
     if (row < tl.rows)
       for (int j = 0; j < k; ++j)
         if (idx[(size_t)t * k + j] / epg == tl.prob) dest |= 1u << j;
-    for (int c0 = 0; c0 < 256; c0 += 16) {
+    int lo, hi;
+    epi_cols(half, 256, lo, hi);
+    for (int c0 = lo; c0 < hi; c0 += 16) {
       float v[16];
       tc::tmem_ld16(tbase + (uint32_t)c0, v);  // warp-collective: every lane loads
       for (unsigned m = dest; m; m &= m - 1u)
@@ -356,12 +367,13 @@ struct ProbGateUp : ProbBase {
     tl.rows = min(128, eo[e + 1] - eo[e] - tl.m0);
     tl.nkb = L / 64;
     tl.gm = 0;
+    tl.arow = eo[e] + tl.m0;
     return tl;
   }
   // A rows: the expert's assignments (rows past the expert's end belong to
   // the next expert or lie beyond T*k and read as zero; the epilogue drops them)
   LMOE_DEV void load_a(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
-    tma_load_2d(dst, &am, kb * 64, eo[tl.prob] + tl.m0, bar);
+    tma_load_2d(dst, &am, kb * 64, tl.arow, bar);
   }
   LMOE_DEV const void* a_row(const int*, const Tile&, int, int) const { return nullptr; }
   // B rows 0..127: gate rows n0.. of expert e; 128..255: the matching up rows
@@ -374,14 +386,16 @@ struct ProbGateUp : ProbBase {
   LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
     mma_k4(d_tmem, da, db, tc::idesc(128, 256, 0), kb);
   }
-  LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase) const {
-    for (int c0 = 0; c0 < 128; c0 += 16) {
+  LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase, int half) const {
+    int lo, hi;
+    epi_cols(half, 128, lo, hi);
+    for (int c0 = lo; c0 < hi; c0 += 16) {
       float g[16], u[16];
       tc::tmem_ld16(tbase + (uint32_t)c0, g);
       tc::tmem_ld16(tbase + (uint32_t)(128 + c0), u);
 #pragma unroll
       for (int i = 0; i < 16; ++i) g[i] = silu(g[i]) * u[i];
-      if (row < tl.rows) store_half16(V + (size_t)(eo[tl.prob] + tl.m0 + row) * f + tl.n0 + c0, g);
+      if (row < tl.rows) store_half16(V + (size_t)(tl.arow + row) * f + tl.n0 + c0, g);
     }
   }
 };
@@ -410,12 +424,13 @@ struct ProbDown : ProbBase {
     tl.rows = min(128, eo[e + 1] - eo[e] - tl.m0);
     tl.nkb = f / 64;
     tl.gm = 0;
+    tl.arow = eo[e] + tl.m0;
     return tl;
   }
   // A: the expert's rows of V (rows past its range belong to the next expert
   // or read as zero; their outputs are not stored)
   LMOE_DEV void load_a(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
-    tma_load_2d(dst, &am, kb * 64, eo[tl.prob] + tl.m0, bar);
+    tma_load_2d(dst, &am, kb * 64, tl.arow, bar);
   }
   LMOE_DEV void load_b(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
     tma_load_2d(dst, &bm, kb * 64, tl.prob * L + tl.n0, bar);
@@ -426,11 +441,13 @@ struct ProbDown : ProbBase {
   LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
     mma_k4(d_tmem, da, db, tc::idesc(128, 256, 0), kb);
   }
-  LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase) const {
+  LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase, int half) const {
     const bool valid = row < tl.rows;
-    const int p = eo[tl.prob] + tl.m0 + row;
+    const int p = tl.arow + row;
     const float wt = valid ? wts[sa[p]] : 0.f;
-    for (int c0 = 0; c0 < 256; c0 += 16) {
+    int lo, hi;
+    epi_cols(half, 256, lo, hi);
+    for (int c0 = lo; c0 < hi; c0 += 16) {
       float v[16];
       tc::tmem_ld16(tbase + (uint32_t)c0, v);
       if (!valid) continue;
@@ -467,13 +484,25 @@ struct ProbWout : ProbBase {
   CUtensorMap lbm;  // B_out^T in fp16 as [G][d][rp], box {64, 256, 1}
   int rp;
   LMOE_DEV int ntn() const { return d / 256; }
+  // K blocks per group (LoRA included) and its multiply-high reciprocal:
+  // kb / kpg2 = umulhi(kb, kdiv) for every kb < 2^32 / kpg2 (kdiv = ceil(2^32 / kpg2),
+  // set on the host). The K-block split runs on the one TMA-issuing thread
+  // for every K block, where a hardware-less integer division would cost
+  // about as much as the block's MMAs.
+  int kpg2_;
+  unsigned kdiv;
   LMOE_DEV int kpg() const { return L / 64; }
-  LMOE_DEV int kpg2() const { return (L + rp) / 64; }  // K blocks per group, LoRA included
-  // the group of K block kb of a mode-0 tile: the (kb / kpg2)-th group of its set
-  LMOE_DEV int kgroup(const Tile& tl, int kb) const {
+  LMOE_DEV int kpg2() const { return kpg2_; }
+  // K block kb -> (its group's index within the tile's set, K block within the group)
+  LMOE_DEV void ksplit(int kb, int& i, int& w) const {
+    i = (int)__umulhi((unsigned)kb, kdiv);
+    w = kb - i * kpg2_;
+  }
+  // the group of a mode-0 tile's K-block group index i: the i-th set bit of its set
+  LMOE_DEV int kgroup(const Tile& tl, int i) const {
     unsigned m = tl.gm;
 #pragma unroll 1
-    for (int i = kb / kpg2(); i > 0; --i) m &= m - 1u;
+    for (; i > 0; --i) m &= m - 1u;
     return __ffs(m) - 1;
   }
   LMOE_DEV void init(int* sc) const {
@@ -489,6 +518,7 @@ struct ProbWout : ProbBase {
       tl.rows = min(128, T - tl.m0);
       tl.gm = tsort ? tunion[t / ntn()] : (G >= 32 ? 0xffffffffu : (1u << G) - 1u);
       tl.nkb = __popc(tl.gm) * kpg2();
+      tl.arow = tl.m0;
     } else {
       const int g = find_prob(sc, G, t), loc = t - sc[g];
       tl.prob = g;
@@ -497,24 +527,27 @@ struct ProbWout : ProbBase {
       tl.rows = min(128, gto[g + 1] - gto[g] - tl.m0);
       tl.nkb = kpg2();
       tl.gm = 0;
+      tl.arow = gto[g] + tl.m0;
     }
     return tl;
   }
   LMOE_DEV void load_a(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
-    const int w = kb % kpg2();  // K block within its group
+    int i, w;  // group index in the tile's set, K block within the group
+    ksplit(kb, i, w);
     if (mode == 0) {
-      const int g = kgroup(tl, kb);
-      if (w < kpg()) tma_load_2d(dst, &am, g * L + w * 64, tl.m0, bar);
-      else tma_load_2d(dst, &qm, g * rp + (w - kpg()) * 64, tl.m0, bar);
+      const int g = kgroup(tl, i);
+      if (w < kpg()) tma_load_2d(dst, &am, g * L + w * 64, tl.arow, bar);
+      else tma_load_2d(dst, &qm, g * rp + (w - kpg()) * 64, tl.arow, bar);
     } else {  // rows past the group's range belong to the next group or read as zero; not stored
-      const int r0 = gto[tl.prob] + tl.m0;
-      if (w < kpg()) tma_load_2d(dst, &am, w * 64, r0, bar);
-      else tma_load_2d(dst, &qm, (w - kpg()) * 64, r0, bar);
+      if (w < kpg()) tma_load_2d(dst, &am, w * 64, tl.arow, bar);
+      else tma_load_2d(dst, &qm, (w - kpg()) * 64, tl.arow, bar);
     }
   }
   LMOE_DEV const void* a_row(const int*, const Tile&, int, int) const { return nullptr; }
   LMOE_DEV void load_b(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
-    const int g = mode == 0 ? kgroup(tl, kb) : tl.prob, w = kb % kpg2();
+    int i, w;
+    ksplit(kb, i, w);
+    const int g = mode == 0 ? kgroup(tl, i) : tl.prob;
     if (w < kpg()) tma_load_3d(dst, &bm, w * 64, tl.n0, g, bar);
     else tma_load_3d(dst, &lbm, (w - kpg()) * 64, tl.n0, g, bar);
   }
@@ -523,9 +556,11 @@ struct ProbWout : ProbBase {
   LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
     mma_k4(d_tmem, da, db, tc::idesc(128, 256, 0), kb);
   }
-  LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase) const {
+  LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase, int half) const {
     const bool valid = row < tl.rows;
-    for (int c0 = 0; c0 < 256; c0 += 16) {
+    int lo, hi;
+    epi_cols(half, 256, lo, hi);
+    for (int c0 = lo; c0 < hi; c0 += 16) {
       float v[16];
       tc::tmem_ld16(tbase + (uint32_t)c0, v);
       if (!valid) continue;
@@ -545,7 +580,7 @@ struct ProbWout : ProbBase {
         d4[0] = make_uint4(h[0], h[1], h[2], h[3]);
         d4[1] = make_uint4(h[4], h[5], h[6], h[7]);
       } else {
-        float4* dst = reinterpret_cast<float4*>(Y + (size_t)(gto[tl.prob] + tl.m0 + row) * d + tl.n0 + c0);
+        float4* dst = reinterpret_cast<float4*>(Y + (size_t)(tl.arow + row) * d + tl.n0 + c0);
 #pragma unroll
         for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
       }
@@ -573,6 +608,7 @@ struct ProbLoraP : ProbBase {
     tl.rows = min(128, T - tl.m0);
     tl.nkb = d / 64;
     tl.gm = 0;
+    tl.arow = tl.m0;
     return tl;
   }
   LMOE_DEV void load_a(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
@@ -587,8 +623,10 @@ struct ProbLoraP : ProbBase {
   LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
     mma_k4(d_tmem, da, db, tc::idesc(128, 256, 0), kb);
   }
-  LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase) const {
-    for (int c0 = 0; c0 < 256; c0 += 16) {
+  LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase, int half) const {
+    int lo, hi;
+    epi_cols(half, 256, lo, hi);
+    for (int c0 = lo; c0 < hi; c0 += 16) {
       float v[16];
       tc::tmem_ld16(tbase + (uint32_t)c0, v);
       if (row < tl.rows && tl.n0 + c0 < N) store_half16(P + (size_t)(tl.m0 + row) * N + tl.n0 + c0, v);
@@ -631,17 +669,19 @@ struct ProbLoraQ : ProbBase {
     if (mode == 1) {
       tl.m0 = mi * 128;
       tl.rows = min(128, gto[tl.prob + 1] - gto[tl.prob] - tl.m0);
+      tl.arow = gto[tl.prob] + tl.m0;
     } else {
       tl.m0 = (gtc ? gtl[tl.prob * ntm() + mi] : mi) * 128;
       tl.rows = min(128, T - tl.m0);
+      tl.arow = tl.m0;
     }
     tl.nkb = L / 64;
     tl.gm = 0;
     return tl;
   }
   LMOE_DEV void load_a(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
-    if (mode == 0) tma_load_2d(dst, &am, tl.prob * L + kb * 64, tl.m0, bar);
-    else tma_load_2d(dst, &am, kb * 64, gto[tl.prob] + tl.m0, bar);  // rows past the group: not stored
+    if (mode == 0) tma_load_2d(dst, &am, tl.prob * L + kb * 64, tl.arow, bar);
+    else tma_load_2d(dst, &am, kb * 64, tl.arow, bar);  // rows past the group: not stored
   }
   LMOE_DEV void load_b(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
     tma_load_3d(dst, &bm, kb * 64, tl.n0, tl.prob, bar);
@@ -652,12 +692,13 @@ struct ProbLoraQ : ProbBase {
   LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
     mma_k4(d_tmem, da, db, tc::idesc(128, 64, 0), kb);
   }
-  LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase) const {
+  LMOE_DEV void epilogue(const int*, const Tile& tl, int row, uint32_t tbase, int half) const {
     const bool valid = row < tl.rows;
     __half* out = mode == 0 ? Q + (size_t)(tl.m0 + row) * G * rp + tl.prob * rp + tl.n0
-                            : Q + (size_t)(gto[tl.prob] + tl.m0 + row) * rp + tl.n0;
-#pragma unroll
-    for (int c0 = 0; c0 < 64; c0 += 16) {
+                            : Q + (size_t)(tl.arow + row) * rp + tl.n0;
+    int lo, hi;
+    epi_cols(half, 64, lo, hi);
+    for (int c0 = lo; c0 < hi; c0 += 16) {
       float v[16];
       tc::tmem_ld16(tbase + (uint32_t)c0, v);
       if (valid) store_half16(out + c0, v);
@@ -1299,6 +1340,8 @@ cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_
           !tmap_encode(&p.lbm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, b + m.bout16, ld, ls, lb, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     }
+    p.kpg2_ = (P.L + rp) / 64;
+    p.kdiv = (unsigned)(((1ull << 32) + (unsigned long long)p.kpg2_ - 1) / (unsigned long long)p.kpg2_);
     p.gto = pm.group_tok_offsets; p.T = T; p.d = P.d; p.L = P.L; p.G = P.G; p.mode = mode;
     p.tsort = mode == 0 ? to.tsort : nullptr;
     p.tunion = to.tunion;

@@ -8,7 +8,9 @@
 //                dequantised to fp16 in registers, or bf16 copied)
 //   warp 8       one thread issues tcgen05.mma (kind::f16) and commits
 //   warps 12..15 epilogue: tcgen05.ld from tensor memory, problem-specific
-//                output (warp w reads TMEM lanes 32*(w%4) .. +31)
+//                output (warp w reads TMEM lanes 32*(w%4) .. +31); when both
+//                operands come by TMA (one producer thread), warps 4..7 take
+//                the second half of each tile's columns beside them
 // Shared-memory stages are handed over with mbarriers (full: producer
 // arrivals; empty: tcgen05.commit); two accumulators in tensor memory let
 // the epilogue of one tile overlap the MMAs of the next. Every wait is
@@ -98,6 +100,7 @@ struct Tile {
   int rows;    // valid rows in this M tile (<= 128)
   int nkb;     // K blocks
   unsigned gm; // problem-specific (the groups a token tile reads, for W_out)
+  int arow;    // problem-specific (the first A row of the tile, looked up once per tile)
 };
 
 struct Shared {
@@ -127,6 +130,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dyn) + 1023) & ~(uintptr_t)1023);
   const long long budget = prob.budget;
   unsigned* err = prob.err;
+  // TMA operands leave warps 1..7 free: warps 4..7 become a second epilogue
+  // set where the problem asks for it
+  constexpr bool EPI2 = P::A_MODE == 3 && P::EPI_SETS == 2;
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -135,7 +141,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&sh.acc_full[a], 1);
-      mbar_init(&sh.acc_empty[a], 4);
+      mbar_init(&sh.acc_empty[a], EPI2 ? 8 : 4);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -150,6 +156,24 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
   const int ntiles = prob.num_tiles(sh.scratch);
+
+  // epilogue over this CTA's tiles; half: -1 every column, 0 / 1 the first / second half
+  auto epilogue_loop = [&](int half) {
+    const int q = warp & 3;
+    int tcount = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tcount) {
+      const Tile tl = prob.tile(sh.scratch, t);
+      const int acc = tcount % NACC, ause = tcount / NACC;
+      mbar_wait(&sh.acc_full[acc], ause & 1, budget, err);
+      __syncwarp();
+      tc_fence_after();
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
+      prob.epilogue(sh.scratch, tl, q * 32 + lane, tbase, half);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.acc_empty[acc]);
+    }
+  };
 
   constexpr bool ASYNC = P::A_MODE != 1 && P::B_MODE != 0;
   static_assert(P::A_MODE != 3 || P::B_MODE == 2, "A by TMA needs B by TMA");
@@ -169,6 +193,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
           prob.load_b(tl, kb, sa + A_BYTES, &sh.full[s]);
         }
       }
+    } else if (EPI2 && warp >= 4) {  // the second epilogue set (acc_empty counts 8 arrivals)
+      epilogue_loop(1);
     }
    } else if constexpr (ASYNC) {
     // ------------------------------------------------ producers, all copies asynchronous
@@ -378,20 +404,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
     __syncwarp();
   } else if (warp >= EPI_WARP0) {
     // --------------------------------------------------------------- epilogue
-    const int q = warp & 3;
-    int tcount = 0;
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tcount) {
-      const Tile tl = prob.tile(sh.scratch, t);
-      const int acc = tcount % NACC, ause = tcount / NACC;
-      mbar_wait(&sh.acc_full[acc], ause & 1, budget, err);
-      __syncwarp();
-      tc_fence_after();
-      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
-      prob.epilogue(sh.scratch, tl, q * 32 + lane, tbase);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.acc_empty[acc]);
-    }
+    epilogue_loop(EPI2 ? 0 : -1);
   }
   tc_fence_before();
   __syncthreads();

@@ -80,3 +80,15 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(capi, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         capi._load()
+
+
+def test_kblock_reciprocal_is_exact():
+    """The W_out GEMM splits K blocks into (group, block) with a multiply-high
+    reciprocal, kb / D = (kb * ceil(2^32 / D)) >> 32; exact for kb < 2^32 / D.
+    Checked here for every divisor the prefill path can meet (L + rp over 64,
+    4..66) and every K block a tile can have (<= 32 groups x D)."""
+    for D in range(4, 67):
+        m = ((1 << 32) + D - 1) // D
+        assert m < (1 << 32)
+        for kb in range(0, 32 * D + 64):
+            assert (kb * m) >> 32 == kb // D, (D, kb)
