@@ -313,13 +313,13 @@ struct ProbWin : ProbBase {
     return tl;
   }
   LMOE_DEV void load_a(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
-    const int kx = d / 64;
-    if (kb < kx) tma_load_2d(dst, &am, kb * 64, tl.m0, bar);
+    const int kx = d >> 6;
+    if (rp == 0 || kb < kx) tma_load_2d(dst, &am, kb * 64, tl.m0, bar);
     else tma_load_2d(dst, &pm, tl.prob * rp + (kb - kx) * 64, tl.m0, bar);
   }
   LMOE_DEV void load_b(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
-    const int kx = d / 64;
-    if (kb < kx) tma_load_3d(dst, &bm, kb * 64, tl.n0, tl.prob, bar);
+    const int kx = d >> 6;
+    if (rp == 0 || kb < kx) tma_load_3d(dst, &bm, kb * 64, tl.n0, tl.prob, bar);
     else tma_load_3d(dst, &lbm, (kb - kx) * 64, tl.n0, tl.prob, bar);
   }
   LMOE_DEV const void* a_row(const int*, const Tile&, int, int) const { return nullptr; }
@@ -489,17 +489,25 @@ struct ProbWout : ProbBase {
   // set on the host). The K-block split runs on the one TMA-issuing thread
   // for every K block, where a hardware-less integer division would cost
   // about as much as the block's MMAs.
-  int kpg2_;
+  int kpg_, kpg2_, kshift;  // L/64, (L+rp)/64, log2(kpg2_) or -1 when kpg2_ is not a power of two
   unsigned kdiv;
-  LMOE_DEV int kpg() const { return L / 64; }
+  LMOE_DEV int kpg() const { return kpg_; }
   LMOE_DEV int kpg2() const { return kpg2_; }
   // K block kb -> (its group's index within the tile's set, K block within the group)
   LMOE_DEV void ksplit(int kb, int& i, int& w) const {
-    i = (int)__umulhi((unsigned)kb, kdiv);
-    w = kb - i * kpg2_;
+    if (kshift >= 0) {
+      i = kb >> kshift;
+      w = kb & (kpg2_ - 1);
+    } else {
+      i = (int)__umulhi((unsigned)kb, kdiv);
+      w = kb - i * kpg2_;
+    }
   }
-  // the group of a mode-0 tile's K-block group index i: the i-th set bit of its set
+  // the group of a mode-0 tile's K-block group index i: the i-th set bit of
+  // its set, from the tile's packed list when G <= 16 and the set has at
+  // most 8 groups
   LMOE_DEV int kgroup(const Tile& tl, int i) const {
+    if (i < 8 && G <= 16) return (int)((tl.gl >> (4 * i)) & 15u);
     unsigned m = tl.gm;
 #pragma unroll 1
     for (; i > 0; --i) m &= m - 1u;
@@ -519,6 +527,9 @@ struct ProbWout : ProbBase {
       tl.gm = tsort ? tunion[t / ntn()] : (G >= 32 ? 0xffffffffu : (1u << G) - 1u);
       tl.nkb = __popc(tl.gm) * kpg2();
       tl.arow = tl.m0;
+      tl.gl = 0;
+      unsigned m = tl.gm;
+      for (int i = 0; i < 8 && m; ++i, m &= m - 1u) tl.gl |= (unsigned)(__ffs(m) - 1) << (4 * i);
     } else {
       const int g = find_prob(sc, G, t), loc = t - sc[g];
       tl.prob = g;
@@ -534,12 +545,13 @@ struct ProbWout : ProbBase {
   LMOE_DEV void load_a(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
     int i, w;  // group index in the tile's set, K block within the group
     ksplit(kb, i, w);
+    const bool z = rp == 0 || w < kpg();  // a K block of Z (else of Q)
     if (mode == 0) {
       const int g = kgroup(tl, i);
-      if (w < kpg()) tma_load_2d(dst, &am, g * L + w * 64, tl.arow, bar);
+      if (z) tma_load_2d(dst, &am, g * L + w * 64, tl.arow, bar);
       else tma_load_2d(dst, &qm, g * rp + (w - kpg()) * 64, tl.arow, bar);
     } else {  // rows past the group's range belong to the next group or read as zero; not stored
-      if (w < kpg()) tma_load_2d(dst, &am, w * 64, tl.arow, bar);
+      if (z) tma_load_2d(dst, &am, w * 64, tl.arow, bar);
       else tma_load_2d(dst, &qm, (w - kpg()) * 64, tl.arow, bar);
     }
   }
@@ -548,7 +560,7 @@ struct ProbWout : ProbBase {
     int i, w;
     ksplit(kb, i, w);
     const int g = mode == 0 ? kgroup(tl, i) : tl.prob;
-    if (w < kpg()) tma_load_3d(dst, &bm, w * 64, tl.n0, g, bar);
+    if (rp == 0 || w < kpg()) tma_load_3d(dst, &bm, w * 64, tl.n0, g, bar);
     else tma_load_3d(dst, &lbm, (w - kpg()) * 64, tl.n0, g, bar);
   }
   LMOE_DEV bool b_row(const int*, const Tile&, int, int, const uint8_t*&, const uint16_t*&) const { return false; }
@@ -1340,7 +1352,9 @@ cudaError_t experts(const PrefillArgs& P, const uint16_t* x, int T, const int32_
           !tmap_encode(&p.lbm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, b + m.bout16, ld, ls, lb, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     }
+    p.kpg_ = P.L / 64;
     p.kpg2_ = (P.L + rp) / 64;
+    p.kshift = (p.kpg2_ & (p.kpg2_ - 1)) == 0 ? __builtin_ctz((unsigned)p.kpg2_) : -1;
     p.kdiv = (unsigned)(((1ull << 32) + (unsigned long long)p.kpg2_ - 1) / (unsigned long long)p.kpg2_);
     p.gto = pm.group_tok_offsets; p.T = T; p.d = P.d; p.L = P.L; p.G = P.G; p.mode = mode;
     p.tsort = mode == 0 ? to.tsort : nullptr;

@@ -101,6 +101,7 @@ struct Tile {
   int nkb;     // K blocks
   unsigned gm; // problem-specific (the groups a token tile reads, for W_out)
   int arow;    // problem-specific (the first A row of the tile, looked up once per tile)
+  unsigned gl; // problem-specific (W_out: the tile's groups in order, 4 bits each, when G <= 16)
 };
 
 struct Shared {
