@@ -302,7 +302,13 @@ lmoe_status lmoe_decode_routing(lmoe_handle* h, const void* ws, int T, int32_t* 
  * host to the workspace, runs lmoe_layer_forward, copies y back and waits
  * for the stream. x_host, residual_host (nullable) and y_host are host
  * pointers ([T][d] bf16; page-locked memory gives asynchronous copies). The
- * workspace must hold lmoe_workspace_size(h, T) + lmoe_host_staging_size(h, T) bytes. */
+ * workspace must hold lmoe_workspace_size(h, T) + lmoe_host_staging_size(h, T) bytes.
+ * The handle keeps the last call's copies and layer as a CUDA graph and
+ * replays it while x_host, residual_host, y_host, ws, T and the stream stay
+ * the same (every call still copies its inputs in and its output out); a
+ * call with other buffers captures anew. Staged handles, handles with stage
+ * events set, and calls on a stream that is being captured issue the work
+ * directly. The handle is not safe to share between host threads. */
 lmoe_status lmoe_layer_forward_host(lmoe_handle* h, const uint16_t* x_host, int T, const uint16_t* residual_host,
                                     uint16_t* y_host, void* ws, lmoe_stream stream);
 

@@ -52,6 +52,18 @@ struct lmoe_handle {
   float* d_pre_w;                    // [16][k]
   unsigned* d_pre_tickets;           // the prerouter's router tickets
   cudaEvent_t ev_pf_in, ev_pf_done;  // stack: the prerouter's start and end on the second stream
+  // lmoe_layer_forward_host: the last call's copies and layer as a CUDA
+  // graph (captured on a stream of the handle's own, launched on the
+  // caller's), replayed while the buffers and T stay the same
+  struct HostGraph {
+    const void* x;
+    const void* r;
+    void* y;
+    void* ws;
+    int T;
+    cudaGraphExec_t exec;
+  } hg;
+  cudaStream_t cap;  // the capture stream (made on first use)
 };
 
 namespace {
@@ -680,6 +692,8 @@ lmoe_status lmoe_destroy(lmoe_handle* h) {
   if (!h) return LMOE_OK;
   DeviceGuard guard(h->device);
   cudaDeviceSynchronize();
+  if (h->hg.exec) cudaGraphExecDestroy(h->hg.exec);
+  if (h->cap) cudaStreamDestroy(h->cap);
   if (h->d_err) cudaFree(h->d_err);
   if (h->d_tickets) cudaFree(h->d_tickets);
   if (h->d_wr_split) cudaFree(h->d_wr_split);
@@ -974,6 +988,30 @@ lmoe_status lmoe_stack_forward(lmoe_handle* const* layers, int n_layers, const u
   return LMOE_OK;
 }
 
+namespace {
+void drop_host_graph(lmoe_handle* h) {
+  if (h->hg.exec) cudaGraphExecDestroy(h->hg.exec);
+  h->hg = lmoe_handle::HostGraph{};
+}
+
+// the host-buffer call's work on `st`: copies in, the layer, the copy out
+lmoe_status enqueue_host_call(lmoe_handle* h, const uint16_t* x_host, int T, const uint16_t* residual_host,
+                              uint16_t* y_host, void* ws, cudaStream_t st) {
+  const size_t bytes = (size_t)T * h->cfg.d * 2;
+  char* stage = reinterpret_cast<char*>(ws) + align_up(lmoe_workspace_size(h, T));
+  uint16_t* dx = reinterpret_cast<uint16_t*>(stage);
+  uint16_t* dr = reinterpret_cast<uint16_t*>(stage + align_up(bytes));
+  uint16_t* dy = reinterpret_cast<uint16_t*>(stage + 2 * align_up(bytes));
+  if (cudaMemcpyAsync(dx, x_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return LMOE_ERR_CUDA;
+  if (residual_host && cudaMemcpyAsync(dr, residual_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  const lmoe_status s = lmoe_layer_forward(h, dx, T, residual_host ? dr : nullptr, dy, ws, (lmoe_stream)st);
+  if (s != LMOE_OK) return s;
+  if (cudaMemcpyAsync(y_host, dy, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return LMOE_ERR_CUDA;
+  return LMOE_OK;
+}
+}  // namespace
+
 lmoe_status lmoe_layer_forward_host(lmoe_handle* h, const uint16_t* x_host, int T, const uint16_t* residual_host,
                                     uint16_t* y_host, void* ws, lmoe_stream stream) {
   if (check_handle(h) != LMOE_OK || T < 0) return LMOE_ERR_INVALID_ARG;
@@ -984,17 +1022,52 @@ lmoe_status lmoe_layer_forward_host(lmoe_handle* h, const uint16_t* x_host, int 
   if (s != LMOE_OK) return s;
   DeviceGuard guard(h->device);
   cudaStream_t st = (cudaStream_t)stream;
-  const size_t bytes = (size_t)T * h->cfg.d * 2;
-  char* stage = reinterpret_cast<char*>(ws) + align_up(lmoe_workspace_size(h, T));
-  uint16_t* dx = reinterpret_cast<uint16_t*>(stage);
-  uint16_t* dr = reinterpret_cast<uint16_t*>(stage + align_up(bytes));
-  uint16_t* dy = reinterpret_cast<uint16_t*>(stage + 2 * align_up(bytes));
-  if (cudaMemcpyAsync(dx, x_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return LMOE_ERR_CUDA;
-  if (residual_host && cudaMemcpyAsync(dr, residual_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+  // Repeated calls with the same buffers (a serving loop's staging buffers)
+  // replay one CUDA graph of the copies and the layer instead of issuing
+  // them one by one; every call still copies its inputs in and its output
+  // out. Not for staged handles (their prefetch runs on its own stream), with
+  // stage events set, or inside the caller's own stream capture.
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return LMOE_ERR_CUDA;
+  const bool graph = !h->staged && h->events.empty() && cs == cudaStreamCaptureStatusNone;
+  if (!graph) {
+    s = enqueue_host_call(h, x_host, T, residual_host, y_host, ws, st);
+    if (s != LMOE_OK) return s;
+    return cuda_status(cudaStreamSynchronize(st));
+  }
+  lmoe_handle::HostGraph& g = h->hg;
+  if (!(g.exec && g.x == x_host && g.r == residual_host && g.y == y_host && g.ws == ws && g.T == T)) {
+    drop_host_graph(h);
+    // capture on the handle's own stream (the caller's may be the legacy
+    // default stream, which cannot be captured); it starts after the
+    // caller's earlier work because the graph is launched on the caller's stream
+    bool ok = h->cap || cudaStreamCreateWithFlags(&h->cap, cudaStreamNonBlocking) == cudaSuccess;
+    ok = ok && cudaStreamBeginCapture(h->cap, cudaStreamCaptureModeThreadLocal) == cudaSuccess;
+    if (ok) {
+      s = enqueue_host_call(h, x_host, T, residual_host, y_host, ws, h->cap);
+      cudaGraph_t cg = nullptr;
+      const cudaError_t ec = cudaStreamEndCapture(h->cap, &cg);
+      ok = s == LMOE_OK && ec == cudaSuccess && cg && cudaGraphInstantiate(&g.exec, cg, 0) == cudaSuccess;
+      if (cg) cudaGraphDestroy(cg);
+      if (s != LMOE_OK) {
+        g.exec = nullptr;
+        cudaGetLastError();
+        return s;
+      }
+    }
+    if (!ok) {  // not capturable here: issue the work directly
+      g.exec = nullptr;
+      cudaGetLastError();
+      s = enqueue_host_call(h, x_host, T, residual_host, y_host, ws, st);
+      if (s != LMOE_OK) return s;
+      return cuda_status(cudaStreamSynchronize(st));
+    }
+    g.x = x_host; g.r = residual_host; g.y = y_host; g.ws = ws; g.T = T;
+  }
+  if (cudaGraphLaunch(g.exec, st) != cudaSuccess) {
+    drop_host_graph(h);
     return LMOE_ERR_CUDA;
-  s = lmoe_layer_forward(h, dx, T, residual_host ? dr : nullptr, dy, ws, stream);
-  if (s != LMOE_OK) return s;
-  if (cudaMemcpyAsync(y_host, dy, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return LMOE_ERR_CUDA;
+  }
   return cuda_status(cudaStreamSynchronize(st));
 }
 
@@ -1013,6 +1086,7 @@ lmoe_status lmoe_check(lmoe_handle* h, lmoe_stream stream) {
 lmoe_status lmoe_set_timeout(lmoe_handle* h, long long cycles) {
   if (check_handle(h) != LMOE_OK || cycles < 0) return LMOE_ERR_INVALID_ARG;
   h->timeout = cycles ? cycles : (h->cfg.timeout_cycles ? h->cfg.timeout_cycles : (1ll << 31));
+  drop_host_graph(h);  // the captured kernels carry the old budget
   return LMOE_OK;
 }
 
@@ -1021,6 +1095,7 @@ lmoe_status lmoe_set_stage_events(lmoe_handle* h, void* const* events, int n) {
   h->events.clear();
   if (events)
     for (int i = 0; i < 2 * n; ++i) h->events.push_back((cudaEvent_t)events[i]);
+  drop_host_graph(h);
   return LMOE_OK;
 }
 
