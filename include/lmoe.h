@@ -308,7 +308,12 @@ lmoe_status lmoe_decode_routing(lmoe_handle* h, const void* ws, int T, int32_t* 
  * the same (every call still copies its inputs in and its output out); a
  * call with other buffers captures anew. Staged handles, handles with stage
  * events set, and calls on a stream that is being captured issue the work
- * directly. The handle is not safe to share between host threads. */
+ * directly. A prefill-sized call (at least 8192 tokens on the prefill path)
+ * runs as a pipeline of 4096-token chunks: each chunk's copy in, its layer
+ * and its copy out overlap those of its neighbours on three streams, the
+ * weights are dequantised once, and the result is that of one
+ * lmoe_layer_forward on all T tokens (every step of the layer is per token).
+ * The handle is not safe to share between host threads. */
 lmoe_status lmoe_layer_forward_host(lmoe_handle* h, const uint16_t* x_host, int T, const uint16_t* residual_host,
                                     uint16_t* y_host, void* ws, lmoe_stream stream);
 

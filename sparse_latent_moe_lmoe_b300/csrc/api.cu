@@ -64,6 +64,10 @@ struct lmoe_handle {
     cudaGraphExec_t exec;
   } hg;
   cudaStream_t cap;  // the capture stream (made on first use)
+  // prefill-sized host calls: copy-in and copy-out streams and their events
+  // (made on first use)
+  cudaStream_t cin, cout;
+  std::vector<cudaEvent_t> hev;
 };
 
 namespace {
@@ -694,6 +698,9 @@ lmoe_status lmoe_destroy(lmoe_handle* h) {
   cudaDeviceSynchronize();
   if (h->hg.exec) cudaGraphExecDestroy(h->hg.exec);
   if (h->cap) cudaStreamDestroy(h->cap);
+  if (h->cin) cudaStreamDestroy(h->cin);
+  if (h->cout) cudaStreamDestroy(h->cout);
+  for (cudaEvent_t e : h->hev) cudaEventDestroy(e);
   if (h->d_err) cudaFree(h->d_err);
   if (h->d_tickets) cudaFree(h->d_tickets);
   if (h->d_wr_split) cudaFree(h->d_wr_split);
@@ -994,9 +1001,68 @@ void drop_host_graph(lmoe_handle* h) {
   h->hg = lmoe_handle::HostGraph{};
 }
 
+constexpr int kHostChunk = 4096;  // tokens per chunk of a prefill-sized host call
+
+// A prefill-sized host call as a pipeline of token chunks on three streams:
+// the copy-in stream moves chunk i's x (and residual) while `st` computes
+// chunk i - 1 and the copy-out stream returns chunk i - 2's y. The weights
+// are dequantised once, into a workspace laid out for one chunk; each
+// chunk's tokens go through the layer exactly as in one call (every step of
+// the layer is per token), and the chunks run one after another on `st`, so
+// they share that workspace.
+lmoe_status enqueue_host_chunked(lmoe_handle* h, const uint16_t* x_host, int T, const uint16_t* residual_host,
+                                 uint16_t* y_host, void* ws, cudaStream_t st) {
+  const int C = kHostChunk, n = (T + C - 1) / C;
+  const size_t row = (size_t)h->cfg.d * 2, bytes = (size_t)T * row;
+  char* stage = reinterpret_cast<char*>(ws) + align_up(lmoe_workspace_size(h, T));
+  char* dx = stage;
+  char* dr = stage + align_up(bytes);
+  char* dy = stage + 2 * align_up(bytes);
+  if (!h->cin && cudaStreamCreateWithFlags(&h->cin, cudaStreamNonBlocking) != cudaSuccess) return LMOE_ERR_CUDA;
+  if (!h->cout && cudaStreamCreateWithFlags(&h->cout, cudaStreamNonBlocking) != cudaSuccess) return LMOE_ERR_CUDA;
+  while ((int)h->hev.size() < 2 * n + 2) {
+    cudaEvent_t e;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return LMOE_ERR_CUDA;
+    h->hev.push_back(e);
+  }
+  cudaEvent_t* ev = h->hev.data();  // [0] start, [1] done, [2 + i] chunk i in, [2 + n + i] chunk i computed
+  const PrefillArgs P = prefill_args(h);
+  // the copies start after the caller's earlier work on st (which may still use the staging buffers)
+  if (cudaEventRecord(ev[0], st) != cudaSuccess || cudaStreamWaitEvent(h->cin, ev[0], 0) != cudaSuccess ||
+      cudaStreamWaitEvent(h->cout, ev[0], 0) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  for (int i = 0; i < n; ++i) {
+    const size_t o = (size_t)i * C * row, nb = (size_t)(T - i * C < C ? T - i * C : C) * row;
+    if (cudaMemcpyAsync(dx + o, reinterpret_cast<const char*>(x_host) + o, nb, cudaMemcpyHostToDevice, h->cin) !=
+            cudaSuccess ||
+        (residual_host && cudaMemcpyAsync(dr + o, reinterpret_cast<const char*>(residual_host) + o, nb,
+                                          cudaMemcpyHostToDevice, h->cin) != cudaSuccess) ||
+        cudaEventRecord(ev[2 + i], h->cin) != cudaSuccess)
+      return LMOE_ERR_CUDA;
+  }
+  if (launch_prefill_weights(P, C, ws, st) != cudaSuccess) return LMOE_ERR_CUDA;
+  for (int i = 0; i < n; ++i) {
+    const int Ti = T - i * C < C ? T - i * C : C;
+    const size_t o = (size_t)i * C * row, nb = (size_t)Ti * row;
+    if (cudaStreamWaitEvent(st, ev[2 + i], 0) != cudaSuccess) return LMOE_ERR_CUDA;
+    if (launch_prefill_layer_chunk(P, reinterpret_cast<const uint16_t*>(dx + o), Ti, C,
+                                   residual_host ? reinterpret_cast<const uint16_t*>(dr + o) : nullptr,
+                                   reinterpret_cast<uint16_t*>(dy + o), ws, st) != cudaSuccess)
+      return LMOE_ERR_CUDA;
+    if (cudaEventRecord(ev[2 + n + i], st) != cudaSuccess || cudaStreamWaitEvent(h->cout, ev[2 + n + i], 0) != cudaSuccess ||
+        cudaMemcpyAsync(reinterpret_cast<char*>(y_host) + o, dy + o, nb, cudaMemcpyDeviceToHost, h->cout) != cudaSuccess)
+      return LMOE_ERR_CUDA;
+  }
+  if (cudaEventRecord(ev[1], h->cout) != cudaSuccess || cudaStreamWaitEvent(st, ev[1], 0) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  return LMOE_OK;
+}
+
 // the host-buffer call's work on `st`: copies in, the layer, the copy out
 lmoe_status enqueue_host_call(lmoe_handle* h, const uint16_t* x_host, int T, const uint16_t* residual_host,
                               uint16_t* y_host, void* ws, cudaStream_t st) {
+  if (use_prefill(h, T) && T >= 2 * kHostChunk && h->events.empty())
+    return enqueue_host_chunked(h, x_host, T, residual_host, y_host, ws, st);
   const size_t bytes = (size_t)T * h->cfg.d * 2;
   char* stage = reinterpret_cast<char*>(ws) + align_up(lmoe_workspace_size(h, T));
   uint16_t* dx = reinterpret_cast<uint16_t*>(stage);

@@ -1481,10 +1481,13 @@ cudaError_t launch_prefill_experts(const PrefillArgs& P, const uint16_t* x, int 
   return experts(P, x, T, idx, w, perm, b, m, 1, Yrows, nullptr, nullptr, st, nullptr, true, TokOrder{});
 }
 
-cudaError_t launch_prefill_layer(const PrefillArgs& P, const uint16_t* x, int T, const uint16_t* residual,
-                                 uint16_t* y, void* ws, cudaStream_t st, const std::vector<cudaEvent_t>* events) {
-  char* b = reinterpret_cast<char*>(ws);
-  const PWs m = pws(P, T);
+namespace {
+// the layer on T tokens in a workspace laid out for at least T tokens (m);
+// weights_ready: the fp16 weights are already in the workspace (made by
+// launch_prefill_weights), so only x is converted
+cudaError_t prefill_layer_impl(const PrefillArgs& P, const uint16_t* x, int T, const uint16_t* residual, uint16_t* y,
+                               char* b, const PWs& m, cudaStream_t st, const std::vector<cudaEvent_t>* events,
+                               bool weights_ready) {
   int32_t* idx = reinterpret_cast<int32_t*>(b + m.idx);
   float* w = reinterpret_cast<float*>(b + m.w);
   const PermPtrs pm = perm_ptrs(b, m);
@@ -1495,7 +1498,7 @@ cudaError_t launch_prefill_layer(const PrefillArgs& P, const uint16_t* x, int T,
   // The dequantisation needs neither the routing nor the permutation: it runs
   // on the handle's second stream, forked from and joined back into `st` by
   // events (so the whole call stays in `st`'s order and can be captured).
-  const bool fork = P.aux != nullptr && P.ev_fork != nullptr && P.ev_join != nullptr;
+  const bool fork = !weights_ready && P.aux != nullptr && P.ev_fork != nullptr && P.ev_join != nullptr;
   const bool sorted = P.G <= 8;  // group sets fit the 8-bit keys of the token order
   if (fork) {
     if ((e = cudaEventRecord(P.ev_fork, st)) != cudaSuccess || (e = cudaStreamWaitEvent(P.aux, P.ev_fork, 0)) != cudaSuccess)
@@ -1535,11 +1538,36 @@ cudaError_t launch_prefill_layer(const PrefillArgs& P, const uint16_t* x, int T,
     if (hk) hk->after(st);
     to = TokOrder{tsort, tpos, tunion, gtc, gtl};
   }
+  if (weights_ready && !sorted) {  // x in fp16, token order unchanged
+    DqJob J;
+    J.nseg = 0;
+    J.x = reinterpret_cast<const uint4*>(x);
+    J.x16 = reinterpret_cast<uint4*>(b + m.x16);
+    J.nx = (size_t)T * P.d / 8;
+    dequant_all_kernel<<<8 * P.num_sms, 256, 0, st>>>(J);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   if (fork) {
     if ((e = cudaStreamWaitEvent(st, P.ev_join, 0)) != cudaSuccess) return e;
     if (hk) hk->i = sorted ? 4 : 3;  // the first stage after the dequantisation and the token order
   }
-  return experts(P, x, T, idx, w, pm, b, m, 0, nullptr, residual, y, st, hk, !fork, to);
+  return experts(P, x, T, idx, w, pm, b, m, 0, nullptr, residual, y, st, hk, !fork && !weights_ready, to);
+}
+}  // namespace
+
+cudaError_t launch_prefill_layer(const PrefillArgs& P, const uint16_t* x, int T, const uint16_t* residual,
+                                 uint16_t* y, void* ws, cudaStream_t st, const std::vector<cudaEvent_t>* events) {
+  return prefill_layer_impl(P, x, T, residual, y, reinterpret_cast<char*>(ws), pws(P, T), st, events, false);
+}
+
+cudaError_t launch_prefill_weights(const PrefillArgs& P, int layout_T, void* ws, cudaStream_t st) {
+  return dequant(P, nullptr, 0, reinterpret_cast<char*>(ws), pws(P, layout_T), st, nullptr, false);
+}
+
+cudaError_t launch_prefill_layer_chunk(const PrefillArgs& P, const uint16_t* x, int T, int layout_T,
+                                       const uint16_t* residual, uint16_t* y, void* ws, cudaStream_t st) {
+  if (T > layout_T) return cudaErrorInvalidValue;
+  return prefill_layer_impl(P, x, T, residual, y, reinterpret_cast<char*>(ws), pws(P, layout_T), st, nullptr, true);
 }
 
 int prefill_launch_count(const PrefillArgs& P, int T) {

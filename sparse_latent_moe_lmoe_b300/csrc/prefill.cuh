@@ -57,6 +57,12 @@ cudaError_t launch_prefill_experts(const PrefillArgs& P, const uint16_t* x, int 
                                    void* ws, cudaStream_t st);
 cudaError_t launch_prefill_layer(const PrefillArgs& P, const uint16_t* x, int T, const uint16_t* residual,
                                  uint16_t* y, void* ws, cudaStream_t st, const std::vector<cudaEvent_t>* events);
+// The layer in token chunks sharing one dequantisation: the fp16 weights into
+// a workspace laid out for layout_T tokens, then the layer on T <= layout_T
+// tokens in that workspace (any number of times, in stream order)
+cudaError_t launch_prefill_weights(const PrefillArgs& P, int layout_T, void* ws, cudaStream_t st);
+cudaError_t launch_prefill_layer_chunk(const PrefillArgs& P, const uint16_t* x, int T, int layout_T,
+                                       const uint16_t* residual, uint16_t* y, void* ws, cudaStream_t st);
 const char* prefill_stage_name(const PrefillArgs& P, int T, int i, int* count);
 // kernels launched by launch_prefill_layer
 int prefill_launch_count(const PrefillArgs& P, int T);

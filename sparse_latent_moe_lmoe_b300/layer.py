@@ -71,12 +71,16 @@ class LatentMoE:
                                  (self.dev_weights[n] for n in capi.WEIGHT_FIELDS)])
         self.h = capi.lmoe_create(self.cfg, self.wts, device)
         self._ws = None
+        self._ws_bytes = {}  # (T, host_staging) -> bytes (fixed per handle)
 
     # ----------------------------------------------------------- plumbing
     def workspace(self, T: int, host_staging: bool = False) -> torch.Tensor:
-        n = capi.lmoe_workspace_size(self.h, T)
-        if host_staging:
-            n = ((n + 255) // 256) * 256 + capi.lmoe_host_staging_size(self.h, T)
+        n = self._ws_bytes.get((T, host_staging))
+        if n is None:
+            n = capi.lmoe_workspace_size(self.h, T)
+            if host_staging:
+                n = ((n + 255) // 256) * 256 + capi.lmoe_host_staging_size(self.h, T)
+            self._ws_bytes[(T, host_staging)] = n
         if self._ws is None or self._ws.numel() < n:
             self._ws = torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
         return self._ws

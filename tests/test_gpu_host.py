@@ -69,3 +69,28 @@ def test_host_call_prefill_path(cuda_device):
     torch.cuda.synchronize()
     m.check()
     assert np.array_equal(host_bits(yh), y_dev)
+
+
+@pytest.mark.parametrize("name,T", [("small", 9000), ("prefill_t16384_zipf", 16384)])
+def test_host_call_chunked_prefill(name, T, cuda_device):
+    """Prefill-sized host calls run as a pipeline of 4096-token chunks (one
+    dequantisation, copies overlapping the compute of neighbouring chunks):
+    bit-identical to one device call on all T tokens (every step of the layer
+    is per token), with a ragged last chunk and a residual."""
+    from sparse_latent_moe_lmoe_b300 import LatentMoE, capi
+    if name == "small":
+        sh = S.LayerShape(d=256, E=64, G=4, k=4, L=256, f=128)
+        W = S.make_layer(sh, 91)
+        x = S.make_x(T, sh.d, 92)
+    else:
+        sh, T, W, x = S.make_workload(name)
+    res = S.make_x(T, sh.d, 93)
+    m = LatentMoE(sh, W, device=0)
+    xh, rh = pinned(x), pinned(res)
+    yh = torch.empty_like(xh).pin_memory()
+    for _ in range(2):  # captured, then replayed
+        m.forward_host(xh, yh, residual_host=rh)
+    y_dev = bf16_bits(m.forward(bf16_tensor(x, cuda_device), residual=bf16_tensor(res, cuda_device)))
+    torch.cuda.synchronize()
+    m.check()
+    assert np.array_equal(host_bits(yh), y_dev)
