@@ -353,26 +353,30 @@ lmoe_status decode_layer(lmoe_handle* h, const uint16_t* x, int T, const uint16_
         if (e != cudaSuccess) return LMOE_ERR_CUDA;
         F.slot_of = h->d_slot_of;
       }
+      // the LoRA kernels and the single kernel chained by programmatic
+      // dependent launch, unless stage events go between them
+      const bool pdl = A.r > 0 && h->events.empty();
       if (A.r > 0) {  // the LoRA branch: lora_in before, lora_q and lora_out after
         // scratch of the multi-kernel sequence, unused by the single kernel:
         // P in Pin, Hl in V, Z in fp32 in Z, Q in Qout; the partials in Lpart
         F.hl = A.V;
         F.zlin = A.Z;
         F.no_combine = 1;
-        e = launch_lora_in(A, lora_ppart(h, ws), A.Pin, A.V, lora_tickets(h), st, &hook);
+        F.pdl_hl = pdl ? 1 : 0;
+        e = launch_lora_in(A, lora_ppart(h, ws), A.Pin, A.V, lora_tickets(h), st, &hook, pdl);
         if (e != cudaSuccess) return LMOE_ERR_CUDA;
       }
       hook.before(st);
-      e = launch_decode_fused(F, h->fused_grid, st);
+      e = launch_decode_fused(F, h->fused_grid, st, pdl ? 1 : 0);
       hook.after(st);
       if (e != cudaSuccess) return LMOE_ERR_CUDA;
       if (A.r > 0) {
         hook.before(st);
-        e = launch_lora_q(A, A.Z, lora_qpart(h, ws), A.Qout, lora_tickets(h), st);
+        e = launch_lora_q(A, A.Z, lora_qpart(h, ws), A.Qout, lora_tickets(h), st, pdl);
         hook.after(st);
         if (e != cudaSuccess) return LMOE_ERR_CUDA;
         hook.before(st);
-        e = launch_lora_out(A, F.Yp, A.Qout, lora_tickets(h), st);
+        e = launch_lora_out(A, F.Yp, A.Qout, lora_tickets(h), st, pdl);
         hook.after(st);
         if (e != cudaSuccess) return LMOE_ERR_CUDA;
       }

@@ -133,6 +133,9 @@ struct FusedArgs {
   // layer stacks: launched as a programmatic dependent of the previous layer
   // (the weight stream starts at once; x is read after griddepcontrol.wait)
   int pdl;
+  // the LoRA branch: launched as a programmatic dependent of lora_hl; Hl is
+  // read after griddepcontrol.wait (x and the weights are ready at launch)
+  int pdl_hl;
   // layer stacks: the next layer's router rows and W_in chunks of this CTA
   // are prefetched into L2 once this layer's own weights are requested
   int has_next;
@@ -184,11 +187,14 @@ constexpr int LORA_ROWS = 128;
 inline size_t lora_ppart_bytes(int d, int G, int r) { return (size_t)G * (d / LORA_ROWS) * 16 * r * 4; }
 inline size_t lora_qpart_bytes(int L, int G, int r) { return (size_t)G * (L / LORA_ROWS) * 16 * r * 4; }
 // lora_p then lora_hl (two kernels; the hook brackets each)
+// pdl: lora_hl, lora_q and lora_out launch as programmatic dependents of
+// their stream predecessors (lora_p, the single kernel, lora_q)
 cudaError_t launch_lora_in(const DecodeArgs& A, float* Ppart, float* P, float* Hl, unsigned* tickets,
-                           cudaStream_t st, StageHook* hook);
+                           cudaStream_t st, StageHook* hook, bool pdl = false);
 cudaError_t launch_lora_q(const DecodeArgs& A, const float* Zlin, float* Qpart, float* Q, unsigned* tickets,
-                          cudaStream_t st);
-cudaError_t launch_lora_out(const DecodeArgs& A, float* Yp, const float* Q, unsigned* tickets, cudaStream_t st);
+                          cudaStream_t st, bool pdl = false);
+cudaError_t launch_lora_out(const DecodeArgs& A, float* Yp, const float* Q, unsigned* tickets, cudaStream_t st,
+                            bool pdl = false);
 cudaError_t launch_residual_add(const uint16_t* x, const uint16_t* y, size_t n, uint16_t* out, cudaStream_t st);
 cudaError_t launch_combine(const float* Y, const int32_t* idx, const int32_t* assign_row, int T, int d, int k,
                            int epg, const uint16_t* residual, uint16_t* y, cudaStream_t st);

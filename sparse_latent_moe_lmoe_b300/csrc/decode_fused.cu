@@ -751,6 +751,7 @@ __global__ void __launch_bounds__(NTHR, 1) decode_fused_kernel(const __grid_cons
     group_sync(BAR_WIN, NCT - RW * 32);
     // H rows: thread (tile, token n, row r), the tile's two partials summed in
     // order; eight consecutive rows of a token gathered into one fragment entry
+    if (F.hl && F.pdl_hl) asm volatile("griddepcontrol.wait;" ::: "memory");  // Hl (lora_hl)
 #pragma unroll 1
     for (int idx = wt; idx < MAX_TILES * FR; idx += NCT - RW * 32) {  // FR = 16 rows x 8 NT tokens per tile
       const int i = idx / FR, rem = idx % FR, n = rem >> 4, r = rem & 15;

@@ -16,6 +16,13 @@
 //             groups in ascending order (+ residual), rounded once
 // Each streams its bf16 matrix in whole rows (a warp reads 128 contiguous
 // bytes per load, eight loads in flight per lane) and reduces in a fixed order.
+// Chained by programmatic dependent launch (unless stage events are being
+// recorded between them): each kernel lets its successor launch as soon as
+// it starts, the successor waits (griddepcontrol.wait) before it reads what
+// the predecessor wrote, and the single kernel waits only where it adds Hl,
+// so that its router and W_in work overlap lora_p and lora_hl. A successor
+// launches only once every CTA of its predecessor has started, so each
+// predecessor runs to completion whatever its successors occupy.
 #include "common.cuh"
 #include "decode.cuh"
 
@@ -131,6 +138,7 @@ __global__ void __launch_bounds__(256) lora_p_kernel(DecodeArgs A, float* __rest
   float (*red)[16][MAXR] = reinterpret_cast<float (*)[16][MAXR]>(act + 16 * LP_ROWS);  // [8][16][r]
   const int g = blockIdx.x, kb = blockIdx.y, nkb = gridDim.y, T = A.T, r = A.r, d = A.d;
   const int k0 = kb * LP_ROWS;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (int i = threadIdx.x; i < 2 * LP_ROWS; i += blockDim.x) {  // 8 elements of x per thread
     const int t = i / (LP_ROWS / 8), kk = (i % (LP_ROWS / 8)) * 8;
     const uint4 v = t < T ? __ldg(reinterpret_cast<const uint4*>(A.x + (size_t)t * d + k0 + kk)) : make_uint4(0, 0, 0, 0);
@@ -154,6 +162,8 @@ __global__ void __launch_bounds__(256) lora_hl_kernel(DecodeArgs A, const float*
   __shared__ float ps[16][MAXR];
   __shared__ float red[4][16][LH_COLS];
   const int g = blockIdx.x, l0 = blockIdx.y * LH_COLS, T = A.T, r = A.r, L = A.L;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // P (lora_p)
   for (int i = threadIdx.x; i < 16 * r; i += blockDim.x) ps[i / r][i % r] = __ldcg(P + (size_t)g * 16 * r + i);
   __syncthreads();
   const int cp = threadIdx.x & 63, q = threadIdx.x >> 6, rq = r / 4;
@@ -197,6 +207,8 @@ __global__ void __launch_bounds__(256) lora_q_kernel(DecodeArgs A, const float* 
   float* act = reinterpret_cast<float*>(lsm);
   float (*red)[16][MAXR] = reinterpret_cast<float (*)[16][MAXR]>(act + 16 * LP_ROWS);
   const int g = blockIdx.x, kb = blockIdx.y, nkb = gridDim.y, T = A.T, r = A.r, L = A.L;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // Z and the routing (the single kernel)
   if (!((routed_groups(A) >> g) & 1ull)) return;  // the whole group's CTAs leave together
   const int k0 = kb * LP_ROWS;
   for (int i = threadIdx.x; i < 16 * LP_ROWS; i += blockDim.x) {
@@ -219,6 +231,7 @@ __global__ void __launch_bounds__(256) lora_out_kernel(DecodeArgs A, float* __re
   __shared__ float red[4][16][LO_ROWS];
   const int rb = blockIdx.x, g = blockIdx.y, G = gridDim.y, T = A.T, r = A.r, d = A.d;
   const int row0 = rb * LO_ROWS;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // Q (lora_q), Y and the routing (the single kernel)
   const unsigned long long gm = routed_groups(A);
   if ((gm >> g) & 1ull) {
     for (int i = threadIdx.x; i < 16 * r; i += blockDim.x) qs[i / r][i % r] = __ldcg(Q + (size_t)g * 16 * r + i);
@@ -286,29 +299,45 @@ bool lora_fused_supported(const DecodeArgs& A) {
 // tickets: [0, G) lora_p, [G, 2G) lora_q, [2G, 2G + d/LO_ROWS) lora_out
 size_t lora_ticket_words(int d, int G) { return (size_t)2 * G + d / LO_ROWS + 1; }
 
+namespace {
+// a launch that may start while its stream predecessor runs (pdl), or after it
+template <typename... Params, typename... Args>
+cudaError_t launch(void (*k)(Params...), dim3 grid, size_t smem, cudaStream_t st, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k, args...);
+}
+}  // namespace
+
 cudaError_t launch_lora_in(const DecodeArgs& A, float* Ppart, float* P, float* Hl, unsigned* tickets,
-                           cudaStream_t st, StageHook* hook) {
+                           cudaStream_t st, StageHook* hook, bool pdl) {
   if (hook) hook->before(st);
-  lora_p_kernel<<<dim3(A.G, A.d / LP_ROWS), 256, lora_rows_smem(), st>>>(A, Ppart, P, tickets);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch(lora_p_kernel, dim3(A.G, A.d / LP_ROWS), lora_rows_smem(), st, false, A, Ppart, P, tickets);
   if (hook) hook->after(st);
   if (e != cudaSuccess) return e;
   if (hook) hook->before(st);
-  lora_hl_kernel<<<dim3(A.G, A.L / LH_COLS), 256, 0, st>>>(A, P, Hl);
-  e = cudaGetLastError();
+  e = launch(lora_hl_kernel, dim3(A.G, A.L / LH_COLS), 0, st, pdl, A, (const float*)P, Hl);
   if (hook) hook->after(st);
   return e;
 }
 
 cudaError_t launch_lora_q(const DecodeArgs& A, const float* Zlin, float* Qpart, float* Q, unsigned* tickets,
-                          cudaStream_t st) {
-  lora_q_kernel<<<dim3(A.G, A.L / LP_ROWS), 256, lora_rows_smem(), st>>>(A, Zlin, Qpart, Q, tickets + A.G);
-  return cudaGetLastError();
+                          cudaStream_t st, bool pdl) {
+  return launch(lora_q_kernel, dim3(A.G, A.L / LP_ROWS), lora_rows_smem(), st, pdl, A, Zlin, Qpart, Q,
+                tickets + A.G);
 }
 
-cudaError_t launch_lora_out(const DecodeArgs& A, float* Yp, const float* Q, unsigned* tickets, cudaStream_t st) {
-  lora_out_kernel<<<dim3(A.d / LO_ROWS, A.G), 256, 0, st>>>(A, Yp, Q, tickets + 2 * A.G);
-  return cudaGetLastError();
+cudaError_t launch_lora_out(const DecodeArgs& A, float* Yp, const float* Q, unsigned* tickets, cudaStream_t st,
+                            bool pdl) {
+  return launch(lora_out_kernel, dim3(A.d / LO_ROWS, A.G), 0, st, pdl, A, Yp, Q, tickets + 2 * A.G);
 }
 
 }  // namespace lmoe
