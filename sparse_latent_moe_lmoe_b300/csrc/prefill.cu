@@ -722,10 +722,10 @@ struct ProbLoraQ : ProbBase {
 // One warp per (group, token) row: Z[row] = sum over the token's experts in
 // that group, in ascending j, of U[inv[t*k + j]]; tokrow[t][g] = row.
 // One warp: out[0 .. L) = sum over the set bits j of `mask`, ascending, of
-// the fp16 rows U + row[j] * L, in fp32, rounded to fp16. Each pass over j
-// loads four 256-element runs of the row at once.
-LMOE_DEV void sum_rows_f16(const __half* __restrict__ U, const int32_t* __restrict__ row, unsigned mask, int L,
-                           __half* __restrict__ out) {
+// the fp16 rows U + r_j * L, in fp32, rounded to fp16; lane j holds r_j (the
+// row indices come in one parallel load, not one dependent load per row).
+// Each pass over j loads four 256-element runs of the row at once.
+LMOE_DEV void sum_rows_f16(const __half* __restrict__ U, int my_row, unsigned mask, int L, __half* __restrict__ out) {
   const int lane = threadIdx.x & 31;
   for (int c0 = 0; c0 < L; c0 += 1024) {
     float acc[4][8];
@@ -733,9 +733,9 @@ LMOE_DEV void sum_rows_f16(const __half* __restrict__ U, const int32_t* __restri
     for (int q = 0; q < 4; ++q)
 #pragma unroll
       for (int h = 0; h < 8; ++h) acc[q][h] = 0.f;
-    unsigned m = mask;
+    unsigned m = mask;  // warp-uniform
     while (m) {
-      const int rj = row[__ffs(m) - 1];
+      const int rj = __shfl_sync(0xffffffffu, my_row, __ffs(m) - 1);
       m &= m - 1u;
       uint4 u[4];
 #pragma unroll
@@ -775,8 +775,9 @@ __global__ void zreduce_kernel(const __half* __restrict__ U, const int32_t* __re
   while (g + 1 < G && gto[g + 1] <= row) ++g;
   const int t = gtok[row];
   if (lane == 0) tokrow[(size_t)t * G + g] = row;
-  const unsigned mask = __ballot_sync(0xffffffffu, lane < k && idx[(size_t)t * k + lane] / epg == g);
-  sum_rows_f16(U, inv + (size_t)t * k, mask, L, Z + (size_t)row * L);
+  const bool mine = lane < k && idx[(size_t)t * k + lane] / epg == g;
+  const unsigned mask = __ballot_sync(0xffffffffu, mine);
+  sum_rows_f16(U, mine ? inv[(size_t)t * k + lane] : 0, mask, L, Z + (size_t)row * L);
 }
 
 // Mode-0 operand of W_out: Ztok[t][g][:] = sum over the token's experts in
@@ -788,9 +789,10 @@ __global__ void zreduce_tok_kernel(const __half* __restrict__ U, const int32_t* 
   const int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (item >= T * G) return;
   const int t = item / G, g = item % G;
-  const unsigned mask = __ballot_sync(0xffffffffu, lane < k && idx[(size_t)t * k + lane] / epg == g);
+  const bool mine = lane < k && idx[(size_t)t * k + lane] / epg == g;
+  const unsigned mask = __ballot_sync(0xffffffffu, mine);
   const int row = tpos ? tpos[t] : t;  // the token's row in the sorted order (or its own)
-  sum_rows_f16(U, inv + (size_t)t * k, mask, L, Ztok + ((size_t)row * G + g) * L);
+  sum_rows_f16(U, mine ? inv[(size_t)t * k + lane] : 0, mask, L, Ztok + ((size_t)row * G + g) * L);
 }
 
 // ------------------------------------------------------------- token order
@@ -871,20 +873,31 @@ __global__ void __launch_bounds__(1024) tsort_tiles_kernel(const uint8_t* __rest
                                                            const int32_t* __restrict__ tsort, int T, int G,
                                                            uint32_t* __restrict__ tunion, int* __restrict__ gtc,
                                                            int* __restrict__ gtl) {
+  constexpr int SU = 4096;  // unions kept in shared memory (T <= 524288 tokens; beyond, read back from tunion)
+  __shared__ uint32_t su[SU];
   const int nt = (T + 127) / 128, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int j = warp; j < nt; j += 32) {
     unsigned u = 0;
     for (int p = j * 128 + lane; p < min(T, j * 128 + 128); p += 32) u |= mask[tsort[p]];
     for (int o = 16; o > 0; o >>= 1) u |= __shfl_xor_sync(0xffffffffu, u, o);
-    if (lane == 0) tunion[j] = u;
+    if (lane == 0) {
+      tunion[j] = u;
+      if (j < SU) su[j] = u;
+    }
   }
   __syncthreads();
-  if (threadIdx.x < G) {
-    const int g = threadIdx.x;
+  // warp g: the tiles whose union holds group g, in order, 32 tiles per ballot
+  if (warp < G) {
+    const int g = warp;
     int c = 0;
-    for (int j = 0; j < nt; ++j)
-      if ((tunion[j] >> g) & 1u) gtl[g * nt + c++] = j;
-    gtc[g] = c;
+    for (int j0 = 0; j0 < nt; j0 += 32) {
+      const int j = j0 + lane;
+      const bool in = j < nt && (((j < SU ? su[j] : __ldcg(tunion + j)) >> g) & 1u);
+      const unsigned b = __ballot_sync(0xffffffffu, in);
+      if (in) gtl[g * nt + c + __popc(b & ((1u << lane) - 1u))] = j;
+      c += __popc(b);
+    }
+    if (lane == 0) gtc[g] = c;
   }
 }
 
