@@ -94,22 +94,32 @@ LMOE_DEV int block_exclusive_scan(int v, int* s_warp, int& excl) {
   return total;
 }
 
+// in-place exclusive scan of col[b * stride], b < n, by one thread; returns
+// the total. Loads go out 16 at a time (the column is n dependent steps).
+LMOE_DEV int column_exclusive_scan(int* col, size_t stride, int n) {
+  int run = 0;
+#pragma unroll 1
+  for (int b0 = 0; b0 < n; b0 += 16) {
+    int v[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) v[u] = b0 + u < n ? col[(size_t)(b0 + u) * stride] : 0;
+#pragma unroll
+    for (int u = 0; u < 16; ++u)
+      if (b0 + u < n) {
+        col[(size_t)(b0 + u) * stride] = run;
+        run += v[u];
+      }
+  }
+  return run;
+}
+
 __global__ void __launch_bounds__(PERM_THREADS) perm_scan_kernel(int nblk, int E, int G, int* cnt, int* gcnt,
                                                                  PermPtrs pm) {
   __shared__ int s_warp[33];
   const int epg = E / G;
   int tot = 0;
   const int e = threadIdx.x;
-  if (e < E) {
-    int run = 0;
-#pragma unroll 8
-    for (int b = 0; b < nblk; ++b) {
-      const int v = cnt[(size_t)b * E + e];
-      cnt[(size_t)b * E + e] = run;
-      run += v;
-    }
-    tot = run;
-  }
+  if (e < E) tot = column_exclusive_scan(cnt + e, (size_t)E, nblk);
   int excl;
   const int total = block_exclusive_scan(e < E ? tot : 0, s_warp, excl);
   if (e < E) pm.expert_offsets[e] = excl;
@@ -117,15 +127,7 @@ __global__ void __launch_bounds__(PERM_THREADS) perm_scan_kernel(int nblk, int E
   __syncthreads();
   if (e <= G) pm.group_offsets[e] = (e == G) ? total : pm.expert_offsets[e * epg];
   int gt = 0;
-  if (e < G) {
-    int run = 0;
-    for (int b = 0; b < nblk; ++b) {
-      const int v = gcnt[(size_t)b * G + e];
-      gcnt[(size_t)b * G + e] = run;
-      run += v;
-    }
-    gt = run;
-  }
+  if (e < G) gt = column_exclusive_scan(gcnt + e, (size_t)G, nblk);
   int gex;
   const int gtotal = block_exclusive_scan(e < G ? gt : 0, s_warp, gex);
   if (e < G) pm.group_tok_offsets[e] = gex;
