@@ -92,6 +92,9 @@ LMOE_DEV int find_prob(const int* scratch, int n, int t) {
 
 struct ProbBase {
   static constexpr int EPI_SETS = 2;  // epilogue warp sets (TMA operands only)
+  // the problem splits its copies into kprep (coordinates, before the stage
+  // wait) and kissue (the copies), instead of load_a / load_b
+  static constexpr bool KPREP = false;
   long long budget;
   unsigned* err;
 };
@@ -541,6 +544,32 @@ struct ProbWout : ProbBase {
       tl.arow = gto[g] + tl.m0;
     }
     return tl;
+  }
+  static constexpr bool KPREP = true;
+  struct KC {
+    const CUtensorMap* am;  // A: Z or Q
+    const CUtensorMap* bm;  // B: Wout or B_out
+    int ax, ay, bx, by, bz;
+  };
+  LMOE_DEV KC kprep(const Tile& tl, int kb) const {
+    int i, w;
+    ksplit(kb, i, w);
+    const int g = mode == 0 ? kgroup(tl, i) : tl.prob;
+    const bool z = rp == 0 || w < kpg();  // a K block of Z (else of Q)
+    KC c;
+    c.am = z ? &am : &qm;
+    c.bm = z ? &bm : &lbm;
+    const int wx = (z ? w : w - kpg()) * 64;
+    c.ax = mode == 0 ? g * (z ? L : rp) + wx : wx;
+    c.ay = tl.arow;
+    c.bx = wx;
+    c.by = tl.n0;
+    c.bz = g;
+    return c;
+  }
+  LMOE_DEV void kissue(const KC& c, void* da, void* db, uint64_t* bar) const {
+    tma_load_2d(da, c.am, c.ax, c.ay, bar);
+    tma_load_3d(db, c.bm, c.bx, c.by, c.bz, bar);
   }
   LMOE_DEV void load_a(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
     int i, w;  // group index in the tile's set, K block within the group

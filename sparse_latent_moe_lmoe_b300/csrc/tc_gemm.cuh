@@ -187,11 +187,20 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_kernel(const __grid_constant_
         const Tile tl = prob.tile(sh.scratch, t);
         for (int kb = 0; kb < tl.nkb; ++kb, ++kiter) {
           const int s = kiter % STAGES, use = kiter / STAGES;
-          if (use > 0) mbar_wait(&sh.empty[s], (use - 1) & 1, budget, err);
           unsigned char* sa = base + s * STAGE_BYTES;
-          mbar_expect_tx(&sh.full[s], (uint32_t)(A_BYTES + B_BYTES));
-          prob.load_a(tl, kb, sa, &sh.full[s]);
-          prob.load_b(tl, kb, sa + A_BYTES, &sh.full[s]);
+          if constexpr (P::KPREP) {
+            // the K block's copy coordinates are worked out before the wait
+            // for its stage, so that only the copies follow the wait
+            const auto kc = prob.kprep(tl, kb);
+            if (use > 0) mbar_wait(&sh.empty[s], (use - 1) & 1, budget, err);
+            mbar_expect_tx(&sh.full[s], (uint32_t)(A_BYTES + B_BYTES));
+            prob.kissue(kc, sa, sa + A_BYTES, &sh.full[s]);
+          } else {
+            if (use > 0) mbar_wait(&sh.empty[s], (use - 1) & 1, budget, err);
+            mbar_expect_tx(&sh.full[s], (uint32_t)(A_BYTES + B_BYTES));
+            prob.load_a(tl, kb, sa, &sh.full[s]);
+            prob.load_b(tl, kb, sa + A_BYTES, &sh.full[s]);
+          }
         }
       }
     } else if (EPI2 && warp >= 4) {  // the second epilogue set (acc_empty counts 8 arrivals)
