@@ -140,7 +140,7 @@ LMOE_DEV void epi_cols(int half, int n, int& lo, int& hi) {
 // [column / 4][row][4] so that a warp's 32 rows are one contiguous 512-byte
 // run per access; the last segment writes the logits rows.
 struct ProbRoute : ProbBase {
-  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 3, B_MODE = 2, STAGES = 4;
+  static constexpr int BN = 256, ACC_COLS = 256, STAGES = 4;
   static constexpr int KSEG_HI = 16;
   CUtensorMap am;         // x as [T][d] bf16, box {64, 128}
   CUtensorMap bm;         // the split W_r as [3][E][d] bf16, box {64, 256, 1}
@@ -188,9 +188,6 @@ struct ProbRoute : ProbBase {
     const bool hi = tl.prob < nhi();
     tma_load_3d(dst, &bm, (hi ? tl.prob * KSEG_HI + kb : kb >> 1) * 64, tl.n0, hi ? 0 : 1 + (kb & 1), bar);
   }
-  LMOE_DEV const void* a_row(const int*, const Tile&, int, int) const { return nullptr; }
-  LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int, int) const { return nullptr; }
-  LMOE_DEV bool b_row(const int*, const Tile&, int, int, const uint8_t*&, const uint16_t*&) const { return false; }
   LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
     mma_k4(d_tmem, da, db, tc::idesc(128, 256, 1), kb);
   }
@@ -272,7 +269,7 @@ struct ProbWin : ProbBase {
   // (g, t) once for each of the token's assignments in group g, at that
   // assignment's position in the expert-sorted order, so the expert GEMM
   // reads its A operand by plain TMA boxes.
-  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 3, B_MODE = 2, STAGES = 4;
+  static constexpr int BN = 256, ACC_COLS = 256, STAGES = 4;
   CUtensorMap am;   // x in fp16 as [T][d] (in tsort order when sorted), box {64, 128}
   CUtensorMap bm;   // Win in fp16 as [G][L][d], box {64, 256, 1}
   int T, d, L, G, k, epg;
@@ -325,9 +322,6 @@ struct ProbWin : ProbBase {
     if (rp == 0 || kb < kx) tma_load_3d(dst, &bm, kb * 64, tl.n0, tl.prob, bar);
     else tma_load_3d(dst, &lbm, (kb - kx) * 64, tl.n0, tl.prob, bar);
   }
-  LMOE_DEV const void* a_row(const int*, const Tile&, int, int) const { return nullptr; }
-  LMOE_DEV bool b_row(const int*, const Tile&, int, int, const uint8_t*&, const uint16_t*&) const { return false; }
-  LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int, int) const { return nullptr; }
   LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
     mma_k4(d_tmem, da, db, tc::idesc(128, 256, 0), kb);
   }
@@ -350,7 +344,7 @@ struct ProbWin : ProbBase {
 
 // ---------------------------------------------------------------- gate/up
 struct ProbGateUp : ProbBase {
-  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 3, B_MODE = 2, STAGES = 4;
+  static constexpr int BN = 256, ACC_COLS = 256, STAGES = 4;
   CUtensorMap gm, um;  // gate / up in fp16 as [E*f][L], box {64, 128}
   CUtensorMap am;      // H by sorted position as [T*k][L] fp16, box {64, 128}
   int L, f, E;
@@ -378,14 +372,11 @@ struct ProbGateUp : ProbBase {
   LMOE_DEV void load_a(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
     tma_load_2d(dst, &am, kb * 64, tl.arow, bar);
   }
-  LMOE_DEV const void* a_row(const int*, const Tile&, int, int) const { return nullptr; }
   // B rows 0..127: gate rows n0.. of expert e; 128..255: the matching up rows
   LMOE_DEV void load_b(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
     tma_load_2d(dst, &gm, kb * 64, tl.prob * f + tl.n0, bar);
     tma_load_2d(static_cast<char*>(dst) + 128 * 128, &um, kb * 64, tl.prob * f + tl.n0, bar);
   }
-  LMOE_DEV bool b_row(const int*, const Tile&, int, int, const uint8_t*&, const uint16_t*&) const { return false; }
-  LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int, int) const { return nullptr; }
   LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
     mma_k4(d_tmem, da, db, tc::idesc(128, 256, 0), kb);
   }
@@ -405,7 +396,7 @@ struct ProbGateUp : ProbBase {
 
 // ------------------------------------------------------------------- down
 struct ProbDown : ProbBase {
-  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 3, B_MODE = 2, STAGES = 4;
+  static constexpr int BN = 256, ACC_COLS = 256, STAGES = 4;
   CUtensorMap am;  // V as [T*k][f] fp16, box {64, 128}
   CUtensorMap bm;  // down in fp16 as [E*L][f], box {64, 256}
   int L, f, E;
@@ -438,9 +429,6 @@ struct ProbDown : ProbBase {
   LMOE_DEV void load_b(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
     tma_load_2d(dst, &bm, kb * 64, tl.prob * L + tl.n0, bar);
   }
-  LMOE_DEV const void* a_row(const int*, const Tile&, int, int) const { return nullptr; }
-  LMOE_DEV bool b_row(const int*, const Tile&, int, int, const uint8_t*&, const uint16_t*&) const { return false; }
-  LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int, int) const { return nullptr; }
   LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
     mma_k4(d_tmem, da, db, tc::idesc(128, 256, 0), kb);
   }
@@ -467,7 +455,7 @@ struct ProbDown : ProbBase {
 // mode 0: y_t = sum_g Wout[g] Z[(g,t)] (+ residual), tiles over tokens, K = G*L
 // mode 1: Y[(g,t)] = Wout[g] Z[(g,t)] (fp32 rows), tiles over group rows
 struct ProbWout : ProbBase {
-  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 3, B_MODE = 2, STAGES = 4;
+  static constexpr int BN = 256, ACC_COLS = 256, STAGES = 4;
   CUtensorMap bm;         // Wout in fp16 as [G][d][L], box {64, 256, 1}
   CUtensorMap am;         // mode 0: Z by token as [T][G*L] (zero rows for absent (t, g));
                           // mode 1: Z by group rows as [rows][L]; box {64, 128}
@@ -584,7 +572,6 @@ struct ProbWout : ProbBase {
       else tma_load_2d(dst, &qm, (w - kpg()) * 64, tl.arow, bar);
     }
   }
-  LMOE_DEV const void* a_row(const int*, const Tile&, int, int) const { return nullptr; }
   LMOE_DEV void load_b(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
     int i, w;
     ksplit(kb, i, w);
@@ -592,8 +579,6 @@ struct ProbWout : ProbBase {
     if (rp == 0 || w < kpg()) tma_load_3d(dst, &bm, w * 64, tl.n0, g, bar);
     else tma_load_3d(dst, &lbm, (w - kpg()) * 64, tl.n0, g, bar);
   }
-  LMOE_DEV bool b_row(const int*, const Tile&, int, int, const uint8_t*&, const uint16_t*&) const { return false; }
-  LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int, int) const { return nullptr; }
   LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
     mma_k4(d_tmem, da, db, tc::idesc(128, 256, 0), kb);
   }
@@ -633,7 +618,7 @@ struct ProbWout : ProbBase {
 // P = x . A_in for every group at once: [T][d] x [d][G*rp] -> fp16 [T][G*rp]
 // (rows in x16's order; the rank padded to rp with zero columns)
 struct ProbLoraP : ProbBase {
-  static constexpr int BN = 256, ACC_COLS = 256, A_MODE = 3, B_MODE = 2, STAGES = 4;
+  static constexpr int BN = 256, ACC_COLS = 256, STAGES = 4;
   CUtensorMap am;  // x in fp16 as [T][d], box {64, 128}
   CUtensorMap bm;  // A_in^T in fp16 as [G*rp][d] (rows past G*rp read as zero), box {64, 256}
   int T, d, N;     // N = G*rp
@@ -658,9 +643,6 @@ struct ProbLoraP : ProbBase {
   LMOE_DEV void load_b(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
     tma_load_2d(dst, &bm, kb * 64, tl.n0, bar);
   }
-  LMOE_DEV const void* a_row(const int*, const Tile&, int, int) const { return nullptr; }
-  LMOE_DEV bool b_row(const int*, const Tile&, int, int, const uint8_t*&, const uint16_t*&) const { return false; }
-  LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int, int) const { return nullptr; }
   LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
     mma_k4(d_tmem, da, db, tc::idesc(128, 256, 0), kb);
   }
@@ -680,7 +662,7 @@ struct ProbLoraP : ProbBase {
 //         group -> token-tile lists only the tiles whose groups hold g
 // mode 1: Z by group rows ([rows][L]), Q as [rows][rp]
 struct ProbLoraQ : ProbBase {
-  static constexpr int BN = 64, ACC_COLS = 64, A_MODE = 3, B_MODE = 2, STAGES = 4;
+  static constexpr int BN = 64, ACC_COLS = 64, STAGES = 4;
   CUtensorMap am;  // Z, box {64, 128}
   CUtensorMap bm;  // A_out^T in fp16 as [G][rp][L], box {64, 64, 1}
   const int32_t* gto;
@@ -727,9 +709,6 @@ struct ProbLoraQ : ProbBase {
   LMOE_DEV void load_b(const Tile& tl, int kb, void* dst, uint64_t* bar) const {
     tma_load_3d(dst, &bm, kb * 64, tl.n0, tl.prob, bar);
   }
-  LMOE_DEV const void* a_row(const int*, const Tile&, int, int) const { return nullptr; }
-  LMOE_DEV bool b_row(const int*, const Tile&, int, int, const uint8_t*&, const uint16_t*&) const { return false; }
-  LMOE_DEV const uint16_t* b_row_bf16(const int*, const Tile&, int, int) const { return nullptr; }
   LMOE_DEV void mma_stage(const Tile&, int kb, uint32_t d_tmem, uint64_t da, uint64_t db) const {
     mma_k4(d_tmem, da, db, tc::idesc(128, 64, 0), kb);
   }
