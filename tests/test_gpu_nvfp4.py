@@ -98,3 +98,35 @@ def test_nvfp4_per_step_decode_kernels_refuse(cuda_device):
                   flags=capi.FLAG_MULTI_KERNEL_DECODE)
     with pytest.raises(LmoeError):
         m.forward(bf16_tensor(x[:4], cuda_device))
+
+
+@pytest.mark.parametrize("T", [16, 256])
+def test_nvfp4_with_lora(T, cuda_device):
+    """NVFP4 weights together with a rank-64 Recover-LoRA branch (drawn large
+    enough to matter at this shape): the single-kernel pass with the branch's
+    kernels around it (T = 16) and the grouped GEMMs with the rank K blocks
+    (T = 256), against the oracle"""
+    from dataclasses import replace
+    from sparse_latent_moe_lmoe_b300 import capi
+    sh0, _, _, _ = S.make_workload("small_t16_nvfp4")
+    sh = replace(sh0, lora_rank=64)
+    W = S.make_layer(sh, 0)
+    W["A_in"] = S.normal_bf16(7, S.S_AIN, (sh.G, sh.d, 64), 0.05)
+    W["B_in"] = S.normal_bf16(7, S.S_BIN, (sh.G, 64, sh.L), 0.03)
+    W["A_out"] = S.normal_bf16(7, S.S_AOUT, (sh.G, sh.L, 64), 0.05)
+    W["B_out"] = S.normal_bf16(7, S.S_BOUT, (sh.G, 64, sh.d), 0.03)
+    x = S.make_x(T, sh.d, 8)
+    y_ref, idx_ref, w_ref, lg_ref = O.layer_forward(O.Layer(sh, W), x)
+    W0 = dict(W)
+    W0["B_in"] = np.zeros_like(W["B_in"])
+    W0["B_out"] = np.zeros_like(W["B_out"])
+    y0 = O.layer_forward(O.Layer(sh, W0), x)[0]
+    assert np.abs(y0 - y_ref).sum() / np.abs(y_ref).sum() > 30e-3  # the branch moves the output
+    m = layer(sh, W, cuda_device, capi.PATH_AUTO)
+    expect = "lora_p" if T > 16 else None
+    names = [capi.lmoe_stage_name(m.h, T, i)[0] for i in range(capi.lmoe_stage_name(m.h, T, 0)[1])]
+    assert (expect in names) if expect else ("decode_fused" in names)
+    got = bf16_bits(m.forward(bf16_tensor(x, cuda_device)))
+    torch.cuda.synchronize()
+    m.check()
+    compare(f"NVFP4 + LoRA, T={T}", sh, got, y_ref, lg_ref)
