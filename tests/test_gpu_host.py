@@ -94,3 +94,19 @@ def test_host_call_chunked_prefill(name, T, cuda_device):
     torch.cuda.synchronize()
     m.check()
     assert np.array_equal(host_bits(yh), y_dev)
+
+
+def test_host_call_lora_decode(cuda_device):
+    """The LoRA decode sequence (its kernels chained by programmatic dependent
+    launch) inside the host call's graph: bit-identical to the device call"""
+    from sparse_latent_moe_lmoe_b300 import LatentMoE
+    sh, T, W, x = S.make_workload("lora_t16")
+    m = LatentMoE(sh, W, device=0)
+    xh = pinned(x)
+    yh = torch.empty_like(xh).pin_memory()
+    for _ in range(3):
+        m.forward_host(xh, yh)
+    y_dev = bf16_bits(m.forward(bf16_tensor(x, cuda_device)))
+    torch.cuda.synchronize()
+    m.check()
+    assert np.array_equal(host_bits(yh), y_dev)
