@@ -309,7 +309,8 @@ lmoe_status lmoe_decode_routing(lmoe_handle* h, const void* ws, int T, int32_t* 
  * call with other buffers captures anew. Staged handles, handles with stage
  * events set, and calls on a stream that is being captured issue the work
  * directly. A prefill-sized call (at least 8192 tokens on the prefill path)
- * runs as a pipeline of 4096-token chunks: each chunk's copy in, its layer
+ * runs as a pipeline of token chunks (1024 tokens, then 4096 each): each
+ * chunk's copy in, its layer
  * and its copy out overlap those of its neighbours on three streams, the
  * weights are dequantised once, and the result is that of one
  * lmoe_layer_forward on all T tokens (every step of the layer is per token).

@@ -1006,17 +1006,23 @@ void drop_host_graph(lmoe_handle* h) {
 }
 
 constexpr int kHostChunk = 4096;  // tokens per chunk of a prefill-sized host call
+constexpr int kHostFirst = 1024;  // the first chunk: the compute starts after a short copy
 
 // A prefill-sized host call as a pipeline of token chunks on three streams:
 // the copy-in stream moves chunk i's x (and residual) while `st` computes
-// chunk i - 1 and the copy-out stream returns chunk i - 2's y. The weights
-// are dequantised once, into a workspace laid out for one chunk; each
-// chunk's tokens go through the layer exactly as in one call (every step of
-// the layer is per token), and the chunks run one after another on `st`, so
-// they share that workspace.
+// chunk i - 1 and the copy-out stream returns chunk i - 2's y. The first
+// chunk is short, so that the compute starts early; the rest are kHostChunk
+// tokens (the last, what remains). The weights are dequantised once, into a
+// workspace laid out for one full chunk; each chunk's tokens go through the
+// layer exactly as in one call (every step of the layer is per token), and
+// the chunks run one after another on `st`, so they share that workspace.
 lmoe_status enqueue_host_chunked(lmoe_handle* h, const uint16_t* x_host, int T, const uint16_t* residual_host,
                                  uint16_t* y_host, void* ws, cudaStream_t st) {
-  const int C = kHostChunk, n = (T + C - 1) / C;
+  const int C = kHostChunk;
+  // chunk i covers tokens [c0(i), c0(i) + cn(i))
+  const int n = 1 + (T - kHostFirst + C - 1) / C;
+  auto c0 = [&](int i) { return i == 0 ? 0 : kHostFirst + (i - 1) * C; };
+  auto cn = [&](int i) { return (i == 0 ? kHostFirst : (T - c0(i) < C ? T - c0(i) : C)); };
   const size_t row = (size_t)h->cfg.d * 2, bytes = (size_t)T * row;
   char* stage = reinterpret_cast<char*>(ws) + align_up(lmoe_workspace_size(h, T));
   char* dx = stage;
@@ -1036,7 +1042,7 @@ lmoe_status enqueue_host_chunked(lmoe_handle* h, const uint16_t* x_host, int T, 
       cudaStreamWaitEvent(h->cout, ev[0], 0) != cudaSuccess)
     return LMOE_ERR_CUDA;
   for (int i = 0; i < n; ++i) {
-    const size_t o = (size_t)i * C * row, nb = (size_t)(T - i * C < C ? T - i * C : C) * row;
+    const size_t o = (size_t)c0(i) * row, nb = (size_t)cn(i) * row;
     if (cudaMemcpyAsync(dx + o, reinterpret_cast<const char*>(x_host) + o, nb, cudaMemcpyHostToDevice, h->cin) !=
             cudaSuccess ||
         (residual_host && cudaMemcpyAsync(dr + o, reinterpret_cast<const char*>(residual_host) + o, nb,
@@ -1046,8 +1052,8 @@ lmoe_status enqueue_host_chunked(lmoe_handle* h, const uint16_t* x_host, int T, 
   }
   if (launch_prefill_weights(P, C, ws, st) != cudaSuccess) return LMOE_ERR_CUDA;
   for (int i = 0; i < n; ++i) {
-    const int Ti = T - i * C < C ? T - i * C : C;
-    const size_t o = (size_t)i * C * row, nb = (size_t)Ti * row;
+    const int Ti = cn(i);
+    const size_t o = (size_t)c0(i) * row, nb = (size_t)Ti * row;
     if (cudaStreamWaitEvent(st, ev[2 + i], 0) != cudaSuccess) return LMOE_ERR_CUDA;
     if (launch_prefill_layer_chunk(P, reinterpret_cast<const uint16_t*>(dx + o), Ti, C,
                                    residual_host ? reinterpret_cast<const uint16_t*>(dr + o) : nullptr,
