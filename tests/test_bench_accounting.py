@@ -44,3 +44,29 @@ def test_prefill_flops_count_distinct_group_token_pairs():
     assert f["route"] == 2.0 * T * SH.d * SH.E
     assert f["gateup"] == 2.0 * (2 * SH.f) * SH.L * T * SH.k
     assert f["down"] == 2.0 * SH.L * SH.f * T * SH.k
+
+
+def test_prefill_flops_with_lora_by_brute_force():
+    """With a rank-r branch: per distinct (group, token) pair, P = x . A_in
+    (d x r), Q = Z . A_out (L x r), and the rank K blocks of W_in (r x L) and
+    W_out (r x d); counted here pair by pair"""
+    from dataclasses import replace
+    sh = replace(SH, lora_rank=16)
+    rng = np.random.default_rng(7)
+    T = 33
+    idx = np.stack([rng.choice(sh.E, sh.k, replace=False) for _ in range(T)]).astype(np.int32)
+    f, rows = bench.stage_flops(sh, T, idx)
+    f0, _ = bench.stage_flops(SH, T, idx)
+    epg = sh.E // sh.G
+    pairs = {(int(e) // epg, t) for t in range(T) for e in idx[t]}
+    r = sh.lora_rank
+    lp = lq = win = wout = 0.0
+    for _ in pairs:
+        lp += 2.0 * sh.d * r
+        lq += 2.0 * sh.L * r
+        win += 2.0 * sh.d * sh.L + 2.0 * r * sh.L
+        wout += 2.0 * sh.L * sh.d + 2.0 * r * sh.d
+    assert f["lora_p"] == lp and f["lora_q"] == lq
+    assert f["win"] == win and f["wout"] == wout
+    for n in ("route", "gateup", "down"):
+        assert f[n] == f0[n]
